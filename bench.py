@@ -1,0 +1,319 @@
+"""Benchmark: prefill-only decisions on the 4B-class hybrid decoder (1 GB300).
+
+One step = one request of the workload: prefill a 1024-token state prefix, then decide 3
+questions (choice over 3 labels, score over 4 levels, noul) with 48-token suffixes branched
+from the prefix snapshot -> 3 decisions per step. Weights are seeded random-init of the
+4B-class shape (bf16, rank-32 LoRA merged at load); inputs are seeded synthetic token ids.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 4b] [--impl ours|reference]
+
+value  = decisions/s measured on the device (CUDA events on the library's stream) with the
+         request's ids already in device memory (stream-ordered API);
+e2e    = decisions/s through the blocking public API (host ids in, host results out,
+         host<->device copies inside the timed region), with its p50 latency;
+roofline = the tensor-core GEMM (the dominant kernel) against the measured bf16 peak;
+cpu_baseline = the oracle (numpy, fp32) on a bounded sample of the same workload.
+`--impl reference` times the oracle alone (the reference arm of this comparison).
+Under torchrun (N > 1) every rank runs an independent replica ("replicas only").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            out = {"source": "measured"}
+            for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                out[k] = float(v) if v is not None else FALLBACK[k]
+            return out
+        except Exception:
+            pass
+    return dict(FALLBACK, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi sampling during the timed region (clocks, throttle reasons)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def time_oracle(cfg, W, req, budget_s: float = 25.0):
+    """The oracle (as it stands) on a bounded sample: whole questions of the request, each
+    the plain unbranched forward over prefix + suffix, until ~budget_s of CPU time."""
+    from oracle import model as om
+    o = om.Oracle(W, np.float32)
+    t0 = time.perf_counter()
+    n = 0
+    for q in req.questions:
+        o.decide_unbranched(req.tokens, req.embeds, [q])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    rows = req.prefix_rows + int(np.mean([len(q.suffix) for q in req.questions]))
+    return {"value": n / dt, "unit": "decisions/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} question(s) of request 0, each a full unbranched forward over ~{rows} rows "
+                      f"(numpy fp32, {cores} host threads), {dt:.1f} s"}
+
+
+def run_reference(args, cfg):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    from prefill_only_decision_gb300 import synth
+    W = synth.make_weights(cfg)
+    req = synth.make_requests(cfg)[0]
+    vals = []
+    for _ in range(args.warmup + args.steps):
+        vals.append(time_oracle(cfg, W, req, budget_s=float(os.environ.get("S1_REF_BUDGET", "10")))["value"])
+    v = float(np.mean(vals[args.warmup:])) if args.steps else float(vals[-1])
+    cb = time_oracle(cfg, W, req, budget_s=1.0)
+    cb["value"] = v
+    line = {"impl": "reference", "metric": "decisions/s", "value": v, "unit": "decisions/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * len(req.questions) / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": cfg.name + " (oracle sample)", "prefix_rows": req.prefix_rows,
+                       "questions": len(req.questions), "suffix_len": len(req.questions[0].suffix)},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "decisions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="4b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from prefill_only_decision_gb300 import configs
+    cfg = configs.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+
+    import ctypes as C
+    import torch
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from prefill_only_decision_gb300 import binding, synth
+
+    W = synth.make_weights(cfg)
+    reqs = synth.make_requests(cfg)
+    req = reqs[0]
+    stream = torch.cuda.current_stream()
+    binding.use_torch_allocator()
+    model = binding.Model(W, stream=stream.cuda_stream)
+    n_q = len(req.questions)
+    P = req.prefix_rows
+
+    # ---- stream-ordered path, ids resident in device memory --------------------------------
+    st = model.state_create(P)
+    d_tok = torch.from_numpy(req.tokens).cuda()
+    d_emb = torch.from_numpy(req.embeds.view(np.int16)).cuda() if req.embeds is not None else None
+    dq = []
+    for q in req.questions:
+        dq.append((torch.from_numpy(q.suffix).cuda(), torch.from_numpy(q.option_ids).cuda(), q.type))
+    qarr = (binding.Question * n_q)()
+    for j, (s, o, t) in enumerate(dq):
+        qarr[j] = binding.Question(t, C.cast(C.c_void_p(s.data_ptr()), C.POINTER(C.c_int32)), s.numel(),
+                                   C.cast(C.c_void_p(o.data_ptr()), C.POINTER(C.c_int32)), o.numel())
+    n_opt = sum(len(q.option_ids) for q in req.questions)
+    d_probs = torch.zeros(n_opt, dtype=torch.float32, device="cuda")
+    d_stats = torch.zeros((n_q, 8), dtype=torch.float32, device="cuda")
+
+    def step():
+        model.prefill_async(st, d_tok.data_ptr(), len(req.tokens), d_emb.data_ptr() if d_emb is not None else 0,
+                            0 if d_emb is None else d_emb.shape[0])
+        model.decide_async(st, qarr, n_q, d_probs.data_ptr(), d_stats.data_ptr(), 0)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    model.sync()
+    # per-phase split (events between prefill and decide), outside the main timed loop
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev[0].record(stream)
+    model.prefill_async(st, d_tok.data_ptr(), len(req.tokens), d_emb.data_ptr() if d_emb is not None else 0,
+                        0 if d_emb is None else d_emb.shape[0])
+    ev[1].record(stream)
+    model.decide_async(st, qarr, n_q, d_probs.data_ptr(), d_stats.data_ptr(), 0)
+    ev[2].record(stream)
+    model.sync()
+    t_prefill, t_decide = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+
+    launches0 = model.counters()["launches"]
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+    ms_total = e0.elapsed_time(e1)
+    launches = (model.counters()["launches"] - launches0) // max(1, args.steps)
+    model.sync()
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / max(1, args.steps)
+    value = ws * n_q * args.steps / (ms_total / 1000.0)
+
+    # ---- roofline of the dominant kernel (tensor-core GEMM), profiled over the same steps ----
+    model.profile(True)
+    for _ in range(args.steps):
+        step()
+    prof = model.profile_read()
+    model.profile(False)
+    peaks = load_peaks()
+    g = prof["gemm"]
+    achieved = g["flops"] / (g["ms"] / 1000.0) / 1e12 if g["ms"] > 0 else 0.0
+    peak = peaks["bf16_tflops_sustained"]
+    total_prof_ms = sum(v["ms"] for v in prof.values())
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05, all projections)", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 sustained",
+                "share_of_step": g["ms"] / total_prof_ms if total_prof_ms else None,
+                "launches_per_step": g["count"] / max(1, args.steps),
+                "flops_per_step": g["flops"] / max(1, args.steps)}
+    phase_split = {k: round(v["ms"] / max(1, args.steps), 4) for k, v in prof.items()}
+
+    # ---- end to end through the blocking public API (host buffers) ---------------------------
+    model.sync()
+    c0 = model.counters()
+    lat = []
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        a = time.perf_counter()
+        s2 = model.prefill(req.tokens, req.embeds)
+        model.decide(s2, req.questions, want_hidden=False)
+        s2.close()
+        lat.append((time.perf_counter() - a) * 1000.0)
+    barrier()
+    e2e_s = time.perf_counter() - t0
+    c1 = model.counters()
+    e2e = {"value": ws * n_q * args.steps / e2e_s, "unit": "decisions/s",
+           "h2d_bytes_per_step": (c1["h2d_bytes"] - c0["h2d_bytes"]) // max(1, args.steps),
+           "d2h_bytes_per_step": (c1["d2h_bytes"] - c0["d2h_bytes"]) // max(1, args.steps),
+           "p50_ms": float(np.median(lat)), "p95_ms": float(np.percentile(lat, 95))}
+
+    line = {"metric": "decisions/s", "value": value, "unit": "decisions/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights and token ids)",
+            "p50_ms": e2e["p50_ms"],
+            "config": {"workload": f"{cfg.name}: 1 request, {P}-row state prefix + {n_q} x "
+                                   f"{len(req.questions[0].suffix)}-token questions",
+                       "model": "4B-class hybrid decoder (24 gated delta-rule + 8 GQA layers, d 2560, "
+                                "FFN 9216, LoRA r32 merged)" if cfg.name.startswith("4b") else cfg.name,
+                       "decisions_per_step": n_q, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2 (weights read every step)",
+                       "phase_ms": {"prefill": round(t_prefill, 4), "decide": round(t_decide, 4)},
+                       "class_ms_per_step": phase_split},
+            "roofline": roofline, "clocks": clk.summary(), "gpu_launches": int(launches), "e2e": e2e}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(cfg, W, req, budget_s=float(os.environ.get("S1_CPU_BUDGET", "25")))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    st.close()
+    model.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

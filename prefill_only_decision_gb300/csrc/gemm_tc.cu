@@ -1,0 +1,502 @@
+// Tensor-core GEMM for sm_103a: TMA -> shared memory -> tcgen05.mma -> TMEM -> epilogue.
+//
+//   Y = epi(X[M,K] . W[N,K]^T), bf16 operands (both K-major), fp32 accumulation in TMEM.
+//
+// Persistent, warp-specialised CTA of 6 warps, one CTA per SM:
+//   warp 0       TMA producer: 128 x 64 A tile and BN x 64 B tile per stage (128-byte swizzle)
+//   warp 1       TMEM allocator and MMA issuer (one thread): 4 x tcgen05.mma (K = 16) per stage
+//   warps 2..5   epilogue: tcgen05.ld of the 128 x BN accumulator (one row per thread),
+//                fused epilogue (fp32 / bf16 / residual add / SwiGLU / split-K partial)
+// The accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
+// overlaps the main loop of the next. Work units are (m tile, split, n tile) with the m tile
+// fastest, so CTAs running at the same time read the same weight tile (L2 reuse). When the
+// tile count cannot fill the SMs, K is split and a reduction kernel applies the epilogue in a
+// fixed order (deterministic).
+//
+// Every mbarrier wait is bounded (~1 s of %globaltimer); on expiry the kernel records an
+// error code in the caller's error word and every role leaves its loop, so no launch can
+// hang the GPU.
+#include <cuda.h>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "common.cuh"
+
+namespace s1 {
+
+namespace tc {
+
+constexpr int BM = 128, BK = 64;
+constexpr int NUM_THREADS = 192;
+constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded wait: 1 s
+constexpr int ERR_TIMEOUT_FULL = 0x101, ERR_TIMEOUT_EMPTY = 0x102, ERR_TIMEOUT_TFULL = 0x103,
+              ERR_TIMEOUT_TEMPTY = 0x104;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait. Returns false (and records `code`) if the phase does not complete in time or
+// another role of this CTA has already given up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* d_err, int code) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = now_ns();
+  uint32_t it = 0;
+  while (true) {
+    if (mbar_try(bar, parity)) return true;
+    if ((++it & 255) == 0) {
+      if (*abort_flag) return false;
+      if (now_ns() - t0 > WAIT_NS) {
+        *abort_flag = 1;
+        atomicExch(d_err, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)1 << 16;                      // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;            // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                      // descriptor version
+  d |= (uint64_t)2 << 61;                      // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A/B, fp32 D, both K-major, M = 128, N = bn.
+__host__ __device__ constexpr uint32_t idesc_bf16(int bn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+struct Params {
+  int M, N, K;
+  int m_tiles, n_tiles, splits, kb_per_split, kb_total;
+  int units;
+  int epi;          // epilogue; EPI_SPLITK_PARTIAL = write fp32 partials to ws
+  void* out;
+  int ldo;
+  float* ws;        // split-K partials [splits, m_tiles*BM, N]
+  int* d_err;
+};
+constexpr int EPI_PARTIAL = 100;
+
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, Params p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* bars = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 4); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapB)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const int mt = u % p.m_tiles;
+        const int rest = u / p.m_tiles;
+        const int sp = rest % p.splits;
+        const int nt = rest / p.splits;
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
+          mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(sA + stage * C::A_BYTES, &mapA, &full[stage], kb * BK, mt * BM);
+          tma_load_2d(sB + stage * C::B_BYTES, &mapB, &full[stage], kb * BK, nt * BN);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++it) {
+        const int rest = u / p.m_tiles;
+        const int sp = rest % p.splits;
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        const int buf = it & 1;
+        if (!mbar_wait(&tempty[buf], ((it >> 1) & 1) ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_TEMPTY)) { ok = false; break; }
+        fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * 256);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.d_err, ERR_TIMEOUT_FULL)) { ok = false; break; }
+          fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            mma_bf16(tmem_d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                     (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (ok) mma_commit(&tfull[buf]);
+      }
+    }
+  } else {
+    // epilogue warps 2..5: TMEM lane quadrant = warp % 4
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int it = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++it) {
+      const int mt = u % p.m_tiles;
+      const int rest = u / p.m_tiles;
+      const int sp = rest % p.splits;
+      const int nt = rest / p.splits;
+      const int buf = it & 1;
+      if (!mbar_wait(&tfull[buf], (it >> 1) & 1, abort_flag, p.d_err, ERR_TIMEOUT_TFULL)) break;
+      fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
+      const int m = mt * BM + row_in_tile;
+      const int n0 = nt * BN;
+      const bool row_ok = m < p.M;
+      if (p.epi == EPI_SWIGLU) {
+        // tile columns [32b, 32b+16) gate, [32b+16, 32b+32) up -> output columns n0/2 + 16b
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          float g[16], v[16];
+          tmem_ld16(tbase + c, g);
+          tmem_ld16(tbase + c + 16, v);
+          if (row_ok && n0 + c < p.N) {
+            bf16* o = reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + (n0 + c) / 2;
+            __align__(16) bf16 r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = f2bf(silu_f(g[i]) * v[i]);
+            reinterpret_cast<uint4*>(o)[0] = reinterpret_cast<uint4*>(r)[0];
+            reinterpret_cast<uint4*>(o)[1] = reinterpret_cast<uint4*>(r)[1];
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 16) {
+          float v[16];
+          tmem_ld16(tbase + c, v);
+          const int n = n0 + c;
+          if (!row_ok || n >= p.N) continue;
+          if (p.epi == EPI_F32) {
+            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          } else if (p.epi == EPI_RESADD) {
+            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float4 x = o[i];
+              x.x += v[4 * i]; x.y += v[4 * i + 1]; x.z += v[4 * i + 2]; x.w += v[4 * i + 3];
+              o[i] = x;
+            }
+          } else if (p.epi == EPI_BF16) {
+            __align__(16) bf16 r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = f2bf(v[i]);
+            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
+            o[0] = reinterpret_cast<uint4*>(r)[0];
+            o[1] = reinterpret_cast<uint4*>(r)[1];
+          } else {  // split-K partial
+            float4* o = reinterpret_cast<float4*>(p.ws + ((size_t)sp * p.m_tiles * BM + m) * p.N + n);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      }
+      fence_before();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512));
+  }
+}
+
+// Sum of the split-K partials in split order, then the epilogue.
+__global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int Mpad, int M, int N, int epi,
+                                     void* __restrict__ out, int ldo) {
+  const int cols = (epi == EPI_SWIGLU) ? N / 2 : N;
+  const size_t total = (size_t)M * (cols / 4);
+  for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < total; t += (size_t)gridDim.x * blockDim.x) {
+    const int m = (int)(t / (cols / 4));
+    const int c = (int)(t % (cols / 4)) * 4;
+    if (epi == EPI_SWIGLU) {
+      // output column c..c+3 -> gate column 32*(c/16) + c%16, up = gate + 16
+      const int gcol = 32 * (c / 16) + (c % 16);
+      float4 g = make_float4(0, 0, 0, 0), u = make_float4(0, 0, 0, 0);
+      for (int s = 0; s < splits; ++s) {
+        const float* rp = ws + ((size_t)s * Mpad + m) * N;
+        const float4 a = *reinterpret_cast<const float4*>(rp + gcol);
+        const float4 b = *reinterpret_cast<const float4*>(rp + gcol + 16);
+        g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
+        u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+      }
+      bf16* o = reinterpret_cast<bf16*>(out) + (size_t)m * ldo + c;
+      o[0] = f2bf(silu_f(g.x) * u.x); o[1] = f2bf(silu_f(g.y) * u.y);
+      o[2] = f2bf(silu_f(g.z) * u.z); o[3] = f2bf(silu_f(g.w) * u.w);
+    } else {
+      float4 a = make_float4(0, 0, 0, 0);
+      for (int s = 0; s < splits; ++s) {
+        const float4 b = *reinterpret_cast<const float4*>(ws + ((size_t)s * Mpad + m) * N + c);
+        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+      }
+      if (epi == EPI_F32) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)m * ldo + c) = a;
+      } else if (epi == EPI_RESADD) {
+        float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)m * ldo + c);
+        float4 x = *o;
+        x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+        *o = x;
+      } else {
+        bf16* o = reinterpret_cast<bf16*>(out) + (size_t)m * ldo + c;
+        o[0] = f2bf(a.x); o[1] = f2bf(a.y); o[2] = f2bf(a.z); o[3] = f2bf(a.w);
+      }
+    }
+  }
+}
+
+// ---- host side -------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix, box = [box_rows, 64 cols], 128-byte swizzle.
+// Cached by (pointer, rows, cols, box_rows).
+bool make_map(CUtensorMap* out, const void* ptr, int rows, int cols, int box_rows) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, int>, CUtensorMap> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_tuple(ptr, rows, cols, box_rows);
+  auto itc = cache.find(key);
+  if (itc != cache.end()) { *out = itc->second; return true; }
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = *out;
+  return true;
+}
+
+struct Plan {
+  int bn, m_tiles, n_tiles, splits, kb_per_split, kb_total, units, grid;
+};
+
+// Choose the N tile and K split: minimise waves x per-tile cost over the candidates.
+Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
+  Plan best{};
+  double best_cost = 1e30;
+  const int kb_total = K / BK;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int cands[4] = {256, 192, 144, 128};
+  for (int bn : cands) {
+    if (epi == EPI_SWIGLU && (bn % 32)) continue;
+    const int n_tiles = (N + bn - 1) / bn;
+    const int tiles = m_tiles * n_tiles;
+    for (int splits = 1; splits <= 16; ++splits) {
+      if (splits > 1 && (kb_total / splits) < 4) break;
+      const int kbp = (kb_total + splits - 1) / splits;
+      const int sp = (kb_total + kbp - 1) / kbp;
+      if (sp != splits) continue;
+      const int units = tiles * sp;
+      if (sp > 1 && (size_t)sp * m_tiles * BM * (size_t)N > ws_cap) break;
+      const int waves = (units + num_sms - 1) / num_sms;
+      // per-unit cost ~ k blocks x (bn + fixed overhead); split-K adds the partial traffic
+      double cost = (double)waves * kbp * (bn + 48.0);
+      if (sp > 1) cost *= 1.0 + 0.04 * sp;
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, units < num_sms ? units : num_sms};
+      }
+      if (units >= num_sms) break;
+    }
+  }
+  return best;
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t st) {
+  using C = Cfg<BN>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  gemm_kernel<BN><<<grid, NUM_THREADS, C::SMEM, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+bool gemm_tc_supported(int M, int N, int K, int epi) {
+  return M >= 0 && N > 0 && K > 0 && (K % tc::BK) == 0 && (N % 32) == 0 && epi >= 0 && epi <= 3 &&
+         tc::get_encode() != nullptr;
+}
+
+size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms) {
+  // K is split only while the tile count is below the SM count, so the partials of one
+  // launch never exceed about 2 x num_sms tiles of 128 x 256.
+  (void)M; (void)N; (void)K; (void)epi;
+  return (size_t)2 * (num_sms > 0 ? num_sms : 160) * tc::BM * 256;
+}
+
+cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
+                           float* splitk_ws, size_t ws_floats, const LaunchCtx& lc) {
+  if (M == 0) return cudaSuccess;
+  if (!gemm_tc_supported(M, N, K, epi)) return cudaErrorInvalidValue;
+  const tc::Plan pl = tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
+  CUtensorMap ma, mb;
+  if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, pl.bn)) return cudaErrorInvalidValue;
+  tc::Params p;
+  p.M = M; p.N = N; p.K = K;
+  p.m_tiles = pl.m_tiles; p.n_tiles = pl.n_tiles; p.splits = pl.splits;
+  p.kb_per_split = pl.kb_per_split; p.kb_total = pl.kb_total; p.units = pl.units;
+  p.epi = pl.splits > 1 ? tc::EPI_PARTIAL : epi;
+  p.out = out; p.ldo = ldo; p.ws = splitk_ws; p.d_err = lc.d_err;
+  cudaError_t e;
+  switch (pl.bn) {
+    case 256: e = tc::launch_bn<256>(ma, mb, p, pl.grid, lc.stream); break;
+    case 192: e = tc::launch_bn<192>(ma, mb, p, pl.grid, lc.stream); break;
+    case 144: e = tc::launch_bn<144>(ma, mb, p, pl.grid, lc.stream); break;
+    default: e = tc::launch_bn<128>(ma, mb, p, pl.grid, lc.stream); break;
+  }
+  if (lc.launches) *lc.launches += 1;
+  if (e != cudaSuccess || pl.splits == 1) return e;
+  const int cols = epi == EPI_SWIGLU ? N / 2 : N;
+  const size_t work = (size_t)M * cols / 4;
+  int blocks = (int)((work + 255) / 256);
+  if (blocks > 4 * lc.num_sms) blocks = 4 * lc.num_sms;
+  tc::splitk_reduce_kernel<<<blocks, 256, 0, lc.stream>>>(splitk_ws, pl.splits, pl.m_tiles * tc::BM, M, N, epi,
+                                                           out, ldo);
+  if (lc.launches) *lc.launches += 1;
+  return cudaGetLastError();
+}
+
+}  // namespace s1

@@ -1,0 +1,78 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace s1 {
+
+typedef __nv_bfloat16 bf16;
+
+// GEMM epilogues: Y = X[M,K] . W[N,K]^T accumulated in fp32, then
+enum Epilogue {
+  EPI_F32 = 0,      // out fp32 [M, ldo]: out = acc
+  EPI_BF16 = 1,     // out bf16 [M, ldo]: out = bf16(acc)
+  EPI_RESADD = 2,   // out fp32 [M, ldo]: out += acc   (residual stream)
+  EPI_SWIGLU = 3,   // W rows interleaved in blocks of 16 gate / 16 up rows;
+                    // out bf16 [M, ldo] with N/2 columns: silu(gate) * up
+};
+
+// Packed description of the sequences of one forward call.
+struct SeqDesc {
+  int row0;     // first packed row
+  int len;      // rows
+  int pos0;     // position of the first row
+  int ctx_in;   // context continued (-1: start from zero state / no cached keys)
+  int ctx_out;  // context whose snapshot this sequence writes (-1: none)
+};
+
+// A prefix snapshot as seen by kernels: all layers' tensors of one state.
+struct CtxDesc {
+  float* S;     // [n_gdn_layers, H, Dv, Dk] fp32
+  bf16* KV;     // [n_fa_layers, 2, cap, Hkv, hd] bf16
+  int P;        // cached rows
+  int cap;      // capacity rows
+};
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  int* d_err;        // device error word (bounded waits record here)
+  int num_sms;
+  long* launches;    // incremented per kernel launched (may be NULL)
+};
+
+// ---- kernels (launchers) ----
+cudaError_t launch_embed(const bf16* E, const int* row_src, const bf16* embeds, float* x, int R, int d,
+                         cudaStream_t st);
+cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int d, float eps,
+                           cudaStream_t st);
+cudaError_t launch_gemm_simt(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out,
+                             int ldo, cudaStream_t st);
+bool gemm_tc_supported(int M, int N, int K, int epi);
+cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out,
+                           int ldo, float* splitk_ws, size_t ws_floats, const LaunchCtx& lc);
+size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms);
+cudaError_t launch_gdn_prep(float* proj, int ld, float* alpha, float* beta, int R, int H, int Dk,
+                            int Dv, float eps, cudaStream_t st);
+cudaError_t launch_gdn_scan(const float* proj, int ld, const float* alpha, const float* beta,
+                            bf16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
+                            int layer_g, int H, int Dk, int Dv, cudaStream_t st);
+cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab, const int* row_seq,
+                              const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, bf16* q,
+                              bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,
+                              cudaStream_t st);
+cudaError_t launch_attention(const bf16* q, const bf16* knew, const bf16* vnew, bf16* out,
+                             const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx, int layer_f,
+                             int Hq, int Hkv, int hd, int max_len, cudaStream_t st);
+cudaError_t launch_readout(const float* x, const float* final_norm, const bf16* E, int d, float eps,
+                           const int* q_row, const int* q_type, const int* opt_off,
+                           const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,
+                           int max_opts, cudaStream_t st);
+cudaError_t launch_merge_lora(const void* W, int w_is_bf16, const void* A, const void* B,
+                              int ab_is_bf16, int rank, float scale, int out_f, int in_f,
+                              bf16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,
+                              int swiglu_F, float* tmpA, float* tmpB, cudaStream_t st);
+cudaError_t launch_to_f32(const void* src, int is_bf16, float* dst, size_t n, cudaStream_t st);
+cudaError_t launch_rope_table(float2* tab, int max_pos, int hd, double theta, cudaStream_t st);
+
+}  // namespace s1

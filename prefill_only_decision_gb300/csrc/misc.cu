@@ -1,0 +1,268 @@
+// Small kernels of the path: embedding gather, RMSNorm, RoPE + KV split,
+// decision readout, load-time LoRA merge and the rotary table.
+#include "common.cuh"
+
+namespace s1 {
+
+// ---- embedding rows: x[r] = E[id] (fp32), or a given embedding row ---------------------
+// row_src[r] >= 0: token id; row_src[r] < 0: row (-1 - row_src[r]) of `embeds`.
+__global__ void embed_kernel(const bf16* __restrict__ E, const int* __restrict__ row_src,
+                             const bf16* __restrict__ embeds, float* __restrict__ x, int d) {
+  const int r = blockIdx.x;
+  const int s = row_src[r];
+  const bf16* src = (s >= 0) ? E + (size_t)s * d : embeds + (size_t)(-1 - s) * d;
+  float* dst = x + (size_t)r * d;
+  for (int i = threadIdx.x * 2; i < d; i += blockDim.x * 2) {
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(src + i);
+    float2 f = __bfloat1622float2(v);
+    *reinterpret_cast<float2*>(dst + i) = f;
+  }
+}
+
+cudaError_t launch_embed(const bf16* E, const int* row_src, const bf16* embeds, float* x, int R, int d,
+                         cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  embed_kernel<<<R, 256, 0, st>>>(E, row_src, embeds, x, d);
+  return cudaGetLastError();
+}
+
+// ---- RMSNorm: out = bf16(x / sqrt(mean(x^2) + eps) * w) --------------------------------
+__global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                               bf16* __restrict__ out, int d, float eps) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)r * d);
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+    float4 v = xr[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  const float4* wr = reinterpret_cast<const float4*>(w);
+  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out + (size_t)r * d);
+  for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
+    float4 v = xr[i], g = wr[i];
+    o2[2 * i] = __floats2bfloat162_rn(v.x * inv * g.x, v.y * inv * g.y);
+    o2[2 * i + 1] = __floats2bfloat162_rn(v.z * inv * g.z, v.w * inv * g.w);
+  }
+}
+
+cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int d, float eps,
+                           cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  rmsnorm_kernel<<<R, 256, 0, st>>>(x, w, out, d, eps);
+  return cudaGetLastError();
+}
+
+// ---- RoPE (rotate-half over the whole head) + split of the fused q|k|v projection -------
+// proj row r: [q (Hq*hd) | k (Hkv*hd) | v (Hkv*hd)] fp32. Writes q, k_new, v_new (bf16) at
+// packed row r and, for sequences that own a snapshot, K/V into its cache at row = position.
+__global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const float2* __restrict__ tab,
+                                  const int* __restrict__ row_seq, const SeqDesc* __restrict__ seqs,
+                                  const CtxDesc* __restrict__ ctxs, int layer_f, bf16* __restrict__ q,
+                                  bf16* __restrict__ knew, bf16* __restrict__ vnew, int Hq, int Hkv,
+                                  int hd) {
+  const int r = blockIdx.x;
+  const SeqDesc sd = seqs[row_seq[r]];
+  const int pos = sd.pos0 + (r - sd.row0);
+  const int half = hd / 2;
+  const float* pr = proj + (size_t)r * ld;
+  const float2* tr = tab + (size_t)pos * half;
+  bf16* kc = nullptr;
+  bf16* vc = nullptr;
+  if (sd.ctx_out >= 0) {
+    const CtxDesc c = ctxs[sd.ctx_out];
+    const size_t plane = (size_t)c.cap * Hkv * hd;
+    kc = c.KV + (size_t)layer_f * 2 * plane + (size_t)pos * Hkv * hd;
+    vc = kc + plane;
+  }
+  const int nq = Hq * half, nk = Hkv * half;
+  for (int t = threadIdx.x; t < nq + nk; t += blockDim.x) {
+    const bool isq = t < nq;
+    const int tt = isq ? t : t - nq;
+    const int h = tt / half, i = tt % half;
+    const float* src = pr + (isq ? 0 : Hq * hd) + h * hd;
+    const float x1 = src[i], x2 = src[i + half];
+    const float2 cs = tr[i];
+    const bf16 y1 = f2bf(x1 * cs.x - x2 * cs.y);
+    const bf16 y2 = f2bf(x2 * cs.x + x1 * cs.y);
+    if (isq) {
+      q[(size_t)r * Hq * hd + h * hd + i] = y1;
+      q[(size_t)r * Hq * hd + h * hd + i + half] = y2;
+    } else {
+      knew[(size_t)r * Hkv * hd + h * hd + i] = y1;
+      knew[(size_t)r * Hkv * hd + h * hd + i + half] = y2;
+      if (kc) { kc[h * hd + i] = y1; kc[h * hd + i + half] = y2; }
+    }
+  }
+  const float* vs = pr + (Hq + Hkv) * hd;
+  for (int t = threadIdx.x; t < Hkv * hd; t += blockDim.x) {
+    const bf16 v = f2bf(vs[t]);
+    vnew[(size_t)r * Hkv * hd + t] = v;
+    if (vc) vc[t] = v;
+  }
+}
+
+cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab, const int* row_seq,
+                              const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, bf16* q,
+                              bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,
+                              cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  rope_split_kernel<<<R, 256, 0, st>>>(proj, ld, rope_tab, row_seq, d_seq, d_ctx, layer_f, q, knew,
+                                       vnew, Hq, Hkv, hd);
+  return cudaGetLastError();
+}
+
+// cos/sin table: tab[pos*half + i] = (cos, sin)(pos * theta^(-2i/hd)), evaluated in double.
+__global__ void rope_table_kernel(float2* tab, int max_pos, int hd, double theta) {
+  const int half = hd / 2;
+  const size_t n = (size_t)max_pos * half;
+  for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n; t += (size_t)gridDim.x * blockDim.x) {
+    const int pos = (int)(t / half), i = (int)(t % half);
+    const double inv = pow(theta, -2.0 * i / (double)hd);
+    double s, c;
+    sincos((double)pos * inv, &s, &c);
+    tab[t] = make_float2((float)c, (float)s);
+  }
+}
+
+cudaError_t launch_rope_table(float2* tab, int max_pos, int hd, double theta, cudaStream_t st) {
+  rope_table_kernel<<<1024, 256, 0, st>>>(tab, max_pos, hd, theta);
+  return cudaGetLastError();
+}
+
+// ---- decision readout -----------------------------------------------------------------
+// One block per question: final RMSNorm of its last row, tied-embedding logits over its
+// option ids (fp32), softmax, argmax, expected level, yes probability and confidences.
+__global__ void readout_kernel(const float* __restrict__ x, const float* __restrict__ fnorm,
+                               const bf16* __restrict__ E, int d, float eps,
+                               const int* __restrict__ q_row, const int* __restrict__ q_type,
+                               const int* __restrict__ opt_off, const int* __restrict__ opt_ids,
+                               float* __restrict__ probs, float* __restrict__ stats,
+                               float* __restrict__ hidden) {
+  extern __shared__ float sm[];
+  float* hn = sm;            // [d]
+  float* z = sm + d;         // [n]
+  __shared__ float red[32];
+  const int j = blockIdx.x;
+  const int row = q_row[j];
+  const int o0 = opt_off[j], n = opt_off[j + 1] - o0;
+  const float* h = x + (size_t)row * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const float v = h[i];
+    ss += v * v;
+    if (hidden) hidden[(size_t)j * d + i] = v;
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) hn[i] = h[i] * inv * fnorm[i];
+  __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int m = w; m < n; m += nw) {
+    const bf16* e = E + (size_t)opt_ids[o0 + m] * d;
+    float acc = 0.f;
+    for (int i = lane; i < d; i += 32) acc += hn[i] * bf2f(e[i]);
+    acc = warp_sum(acc);
+    if (lane == 0) z[m] = acc;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mx = -INFINITY;
+    int am = 0;
+    for (int m = 0; m < n; ++m) if (z[m] > mx) { mx = z[m]; am = m; }
+    float se = 0.f;
+    for (int m = 0; m < n; ++m) se += expf(z[m] - mx);
+    const float lse = logf(se);
+    float ent = 0.f, ex = 0.f, p2 = 0.f;
+    for (int m = 0; m < n; ++m) {
+      const float lp = z[m] - mx - lse;
+      const float p = expf(lp);
+      probs[o0 + m] = p;
+      if (p > 0.f) ent -= p * lp;
+      ex += (float)m * p;
+      if (m != am && p > p2) p2 = p;
+    }
+    const float pmax = expf(-lse);
+    const float econf = (n == 1) ? 1.f : 1.f - ent / logf((float)n);
+    float* s = stats + (size_t)j * 8;
+    s[0] = (float)am;
+    s[1] = ex;
+    s[2] = expf(z[0] - mx - lse);
+    s[3] = pmax;
+    s[4] = (q_type[j] == 2) ? pmax : econf;
+    s[5] = econf;
+    s[6] = pmax - p2;
+    s[7] = (float)n;
+  }
+}
+
+cudaError_t launch_readout(const float* x, const float* final_norm, const bf16* E, int d, float eps,
+                           const int* q_row, const int* q_type, const int* opt_off,
+                           const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,
+                           int max_opts, cudaStream_t st) {
+  if (n_q <= 0) return cudaSuccess;
+  const size_t smem = (size_t)(d + max_opts) * sizeof(float);
+  readout_kernel<<<n_q, 256, smem, st>>>(x, final_norm, E, d, eps, q_row, q_type, opt_off, opt_ids,
+                                         probs, stats, hidden);
+  return cudaGetLastError();
+}
+
+// ---- load-time: W' = W + scale * B A (fp32 accumulate, one bf16 rounding) ----------------
+// dst row mapping: plain (dst_row0 + o), or SwiGLU interleave: the gate (half 0) / up
+// (half 1) row o lands at 32*(o/16) + 16*half + o%16 of the packed [2F, in] matrix.
+__device__ __forceinline__ float ld_any(const void* p, int is_bf16, size_t i) {
+  return is_bf16 ? __bfloat162float(reinterpret_cast<const bf16*>(p)[i])
+                 : reinterpret_cast<const float*>(p)[i];
+}
+
+__global__ void merge_lora_kernel(const void* __restrict__ W, int w_bf16, const void* __restrict__ A,
+                                  const void* __restrict__ B, int ab_bf16, int rank, float scale,
+                                  int out_f, int in_f, bf16* __restrict__ dst, int dst_row0,
+                                  int interleave, int half) {
+  const int o = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= in_f) return;
+  float acc = ld_any(W, w_bf16, (size_t)o * in_f + i);
+  if (rank > 0) {
+    float t = 0.f;
+    for (int r = 0; r < rank; ++r)
+      t = fmaf(ld_any(B, ab_bf16, (size_t)o * rank + r), ld_any(A, ab_bf16, (size_t)r * in_f + i), t);
+    acc = fmaf(scale, t, acc);
+  }
+  const int drow = interleave ? (32 * (o / 16) + 16 * half + (o % 16)) : (dst_row0 + o);
+  dst[(size_t)drow * in_f + i] = __float2bfloat16_rn(acc);
+}
+
+cudaError_t launch_merge_lora(const void* W, int w_is_bf16, const void* A, const void* B,
+                              int ab_is_bf16, int rank, float scale, int out_f, int in_f,
+                              bf16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,
+                              int swiglu_F, float* tmpA, float* tmpB, cudaStream_t st) {
+  (void)swiglu_F; (void)tmpA; (void)tmpB;
+  if (interleave_swiglu && out_f > 65535) return cudaErrorNotSupported;
+  // grid.y is limited to 65535 rows per launch: split tall matrices (plain mapping only).
+  for (int o0 = 0; o0 < out_f; o0 += 65535) {
+    const int rows = (out_f - o0) < 65535 ? (out_f - o0) : 65535;
+    dim3 grid((in_f + 255) / 256, rows);
+    const void* Wc = (const char*)W + (size_t)o0 * in_f * (w_is_bf16 ? 2 : 4);
+    const void* Bc = B ? (const void*)((const char*)B + (size_t)o0 * rank * (ab_is_bf16 ? 2 : 4)) : nullptr;
+    merge_lora_kernel<<<grid, 256, 0, st>>>(Wc, w_is_bf16, A, Bc, ab_is_bf16, rank, scale, rows, in_f,
+                                            dst, dst_row0 + o0, interleave_swiglu, swiglu_half);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+__global__ void to_f32_kernel(const void* __restrict__ src, int is_bf16, float* __restrict__ dst, size_t n) {
+  for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < n; t += (size_t)gridDim.x * blockDim.x)
+    dst[t] = ld_any(src, is_bf16, t);
+}
+
+cudaError_t launch_to_f32(const void* src, int is_bf16, float* dst, size_t n, cudaStream_t st) {
+  to_f32_kernel<<<256, 256, 0, st>>>(src, is_bf16, dst, n);
+  return cudaGetLastError();
+}
+
+}  // namespace s1
