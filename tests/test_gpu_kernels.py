@@ -93,8 +93,8 @@ def test_gemm_swiglu(B, impl, M, F, K):
     gt, up = Xd @ Wg.T.astype(np.float64), Xd @ Wu.T.astype(np.float64)
     ref = om.silu(gt) * up
     out = torch.zeros((M, F), dtype=torch.bfloat16, device="cuda")
-    B.op_gemm(to_dev_bf16(X).data_ptr(), to_dev_bf16(swiglu_pack(Wg, Wu)).data_ptr(), M, 2 * F, K, 3,
-              out.data_ptr(), F, impl)
+    dX, dW = to_dev_bf16(X), to_dev_bf16(swiglu_pack(Wg, Wu))   # keep the device buffers alive
+    B.op_gemm(dX.data_ptr(), dW.data_ptr(), M, 2 * F, K, 3, out.data_ptr(), F, impl)
     got = from_dev_bf16(out)
     err = np.abs(got - ref)
     assert np.all(err <= np.abs(ref) * 2.0 ** -8 + 1e-4), err.max()
@@ -122,8 +122,8 @@ def test_rmsnorm(B):
     x = (g.standard_normal((37, 2560)) * 3).astype(np.float32)
     w = (1 + 0.1 * g.standard_normal(2560)).astype(np.float32)
     out = torch.zeros((37, 2560), dtype=torch.bfloat16, device="cuda")
-    B.op_rmsnorm(torch.from_numpy(x).cuda().data_ptr(), torch.from_numpy(w).cuda().data_ptr(), 37, 2560, 1e-6,
-                 out.data_ptr())
+    dx, dw = torch.from_numpy(x).cuda(), torch.from_numpy(w).cuda()
+    B.op_rmsnorm(dx.data_ptr(), dw.data_ptr(), 37, 2560, 1e-6, out.data_ptr())
     ref = om.rmsnorm(x.astype(np.float64), w.astype(np.float64), 1e-6)
     np.testing.assert_allclose(from_dev_bf16(out), ref, rtol=2.0 ** -8, atol=1e-6)
 
@@ -179,8 +179,9 @@ def test_attention(B, Hq, Hkv, hd, P, lens):
     row0 = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int32)
     kv = to_dev_bf16(np.stack([kc, vc])) if P else None
     out = torch.zeros((R, Hq * hd), dtype=torch.bfloat16, device="cuda")
-    B.op_attention(to_dev_bf16(q).data_ptr(), to_dev_bf16(kn).data_ptr(), to_dev_bf16(vn).data_ptr(),
-                   kv.data_ptr() if P else 0, P, row0, lens, Hq, Hkv, hd, out.data_ptr())
+    dq, dk, dv = to_dev_bf16(q), to_dev_bf16(kn), to_dev_bf16(vn)
+    B.op_attention(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), kv.data_ptr() if P else 0, P, row0, lens, Hq, Hkv,
+                   hd, out.data_ptr())
     got = from_dev_bf16(out).reshape(R, Hq, hd)
     for r0, n in zip(row0, lens):
         K = np.concatenate([kc, kn[r0:r0 + n]]).astype(np.float64)
