@@ -1,76 +1,265 @@
 // Causal GQA attention over packed sequences, with suffix-over-prefix continuation.
 //
-// A query at row i of sequence s (position pos0 + i) attends to every cached key of the
-// snapshot it continues (positions 0 .. P-1) and to its own sequence's keys 0 .. i; never
-// to another sequence ("execute isolated question/option suffixes", System1-Omni RFC #114,
-// section 4, "Branching" row). q head h reads kv head floor(h * Hkv / Hq).
-// softmax(q.k / sqrt(hd)) v with an online (running max / sum) softmax in fp32.
+// A query at row i of sequence s (position pos0 + i, pos0 = P of the snapshot it continues)
+// attends to every cached key of that snapshot (positions 0 .. P-1) and to its own sequence's
+// keys 0 .. i; never to another sequence ("execute isolated question/option suffixes",
+// System1-Omni RFC #114, section 4, "Branching" row). q head h reads kv head floor(h*Hkv/Hq).
+// out = softmax(q.k / sqrt(hd)) v, online (running max / sum) softmax in fp32.
+//
+// Keys are addressed as one virtual array per sequence: j < P -> snapshot row j, j >= P ->
+// the sequence's own row j - P. Key j has position j, query i has position P + i, so the
+// causal rule is j <= P + i.
+//
+// flash kernel: CTA = 64 queries x one q head (4 warps x 16 rows); K/V tiles of 64 keys staged
+// in shared memory by cp.async (double-buffered, 16-byte chunks XOR-swizzled by row);
+// S = Q K^T and O += P V on the tensor cores (mma.sync m16n8k16 bf16 -> fp32).
 #include "common.cuh"
 
 namespace s1 {
 
-// One warp per (row, q head); a lane holds hd/32 consecutive dims.
+namespace fa {
+
+constexpr int BQ = 64, BKV = 64, NWARP = 4;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;   // src-size 0 -> zero fill
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// byte offset of 16-byte chunk c of row r in a tile whose rows are HD bf16 wide
 template <int HD>
-__global__ void __launch_bounds__(128) attn_rowwarp_kernel(
-    const bf16* __restrict__ q, const bf16* __restrict__ knew, const bf16* __restrict__ vnew,
-    bf16* __restrict__ out, const SeqDesc* __restrict__ seqs, const CtxDesc* __restrict__ ctxs,
-    int layer_f, int Hq, int Hkv, float scale_log2) {
-  constexpr int E = HD / 32;
-  const int sq = blockIdx.y;
-  const SeqDesc sd = seqs[sq];
-  const int lane = threadIdx.x & 31;
-  const int item = blockIdx.x * 4 + (threadIdx.x >> 5);   // (row, head) within the sequence
-  if (item >= sd.len * Hq) return;
-  const int i = item / Hq, h = item % Hq;
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return (uint32_t)(r * (HD * 2) + ((c ^ (r & 7)) << 4));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, const bf16* __restrict__ knew,
+                                                    const bf16* __restrict__ vnew, bf16* __restrict__ out,
+                                                    const SeqDesc* __restrict__ seqs,
+                                                    const CtxDesc* __restrict__ ctxs, int layer_f, int Hq,
+                                                    int Hkv, float scale_log2) {
+  constexpr int CH = HD / 8;                 // 16-byte chunks per row
+  constexpr int TILE = BKV * HD * 2;         // bytes per K or V tile
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint8_t* sQ = sm;                          // BQ x HD
+  uint8_t* sK = sm + BQ * HD * 2;            // 2 stages
+  uint8_t* sV = sK + 2 * TILE;               // 2 stages
+
+  const SeqDesc sd = seqs[blockIdx.z];
+  const int q0 = blockIdx.x * BQ;
+  if (q0 >= sd.len) return;
+  const int h = blockIdx.y;
   const int g = (h * Hkv) / Hq;
-  const int row = sd.row0 + i;
-  float qv[E];
-  const bf16* qp = q + ((size_t)row * Hq + h) * HD + lane * E;
-#pragma unroll
-  for (int e = 0; e < E; ++e) qv[e] = bf2f(qp[e]) * scale_log2;
-  float m = -INFINITY, l = 0.f, acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  auto visit = [&](const bf16* kp, const bf16* vp) {
-    float sdot = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) sdot = fmaf(qv[e], bf2f(kp[e]), sdot);
-    sdot = warp_sum(sdot);
-    const float mn = fmaxf(m, sdot);
-    const float c = exp2f(m - mn), p = exp2f(sdot - mn);
-    l = l * c + p;
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(acc[e], c, p * bf2f(vp[e]));
-    m = mn;
-  };
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  int P = 0;
+  const bf16* Kc = nullptr;
+  const bf16* Vc = nullptr;
   if (sd.ctx_in >= 0) {
     const CtxDesc c = ctxs[sd.ctx_in];
+    P = c.P;
     const size_t plane = (size_t)c.cap * Hkv * HD;
-    const bf16* Kc = c.KV + (size_t)layer_f * 2 * plane + (size_t)g * HD + lane * E;
-    const bf16* Vc = Kc + plane;
-    for (int j = 0; j < c.P; ++j) visit(Kc + (size_t)j * Hkv * HD, Vc + (size_t)j * Hkv * HD);
+    Kc = c.KV + (size_t)layer_f * 2 * plane + (size_t)g * HD;
+    Vc = Kc + plane;
   }
-  const bf16* Kn = knew + ((size_t)sd.row0 * Hkv + g) * HD + lane * E;
-  const bf16* Vn = vnew + ((size_t)sd.row0 * Hkv + g) * HD + lane * E;
-  for (int j = 0; j <= i; ++j) visit(Kn + (size_t)j * Hkv * HD, Vn + (size_t)j * Hkv * HD);
-  const float inv = 1.f / l;
-  bf16* op = out + ((size_t)row * Hq + h) * HD + lane * E;
+  const bf16* Kn = knew + ((size_t)sd.row0 * Hkv + g) * HD;
+  const bf16* Vn = vnew + ((size_t)sd.row0 * Hkv + g) * HD;
+  const size_t kstride = (size_t)Hkv * HD;
+  const int n_keys = P + min(sd.len, q0 + BQ);     // keys any query of this tile can see
+  const int n_tiles = (n_keys + BKV - 1) / BKV;
+
+  // ---- stage Q (rows beyond len are zero)
+  for (int i = tid; i < BQ * CH; i += 128) {
+    const int r = i / CH, c = i % CH;
+    const bool ok = q0 + r < sd.len;
+    const bf16* src = q + ((size_t)(sd.row0 + (ok ? q0 + r : 0)) * Hq + h) * HD + c * 8;
+    cp_async16(smem_u32(sQ) + swz<HD>(r, c), src, ok);
+  }
+  auto load_kv = [&](int t, int stage) {
+    const int j0 = t * BKV;
+    for (int i = tid; i < BKV * CH; i += 128) {
+      const int r = i / CH, c = i % CH;
+      const int j = j0 + r;
+      const bool ok = j < n_keys;
+      const bf16* ks;
+      const bf16* vs;
+      if (j < P) { ks = Kc + (size_t)j * kstride; vs = Vc + (size_t)j * kstride; }
+      else { const int jj = ok ? j - P : 0; ks = Kn + (size_t)jj * kstride; vs = Vn + (size_t)jj * kstride; }
+      cp_async16(smem_u32(sK + stage * TILE) + swz<HD>(r, c), ks + c * 8, ok);
+      cp_async16(smem_u32(sV + stage * TILE) + swz<HD>(r, c), vs + c * 8, ok);
+    }
+  };
+  load_kv(0, 0);
+  cp_commit();
+
+  // Q fragments (A operand), rows 16*warp .. +15
+  cp_wait<0>();
+  __syncthreads();
+  uint32_t qa[HD / 16][4];
+  {
+    const int r = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
-  for (int e = 0; e < E; ++e) op[e] = f2bf(acc[e] * inv);
+    for (int kk = 0; kk < HD / 16; ++kk) {
+      const int c = 2 * kk + (lane >> 4);
+      ldsm_x4(smem_u32(sQ) + swz<HD>(r, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+    }
+  }
+  float o[HD / 8][4];
+#pragma unroll
+  for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int qi0 = q0 + warp * 16 + (lane >> 2);    // this thread's rows: qi0 and qi0 + 8
+  const int lim0 = P + qi0, lim1 = P + qi0 + 8;    // last visible key index
+
+  for (int t = 0; t < n_tiles; ++t) {
+    const int stage = t & 1;
+    if (t + 1 < n_tiles) load_kv(t + 1, stage ^ 1);
+    cp_commit();
+    cp_wait<1>();
+    __syncthreads();
+    const uint32_t kb = smem_u32(sK + stage * TILE), vb = smem_u32(sV + stage * TILE);
+    // S = Q K^T  (16 x 64 per warp)
+    float s[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {       // pairs of 8-key n-tiles
+        const int key = np * 16 + 8 * (lane >> 4) + (lane & 7);
+        const int c = 2 * kk + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + swz<HD>(key, c), b0, b1, b2, b3);
+        mma16816(s[2 * np], qa[kk], b0, b1);
+        mma16816(s[2 * np + 1], qa[kk], b2, b3);
+      }
+    }
+    // mask + online softmax (log2 domain)
+    const int j0 = t * BKV;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const int jb = j0 + n * 8 + 2 * (lane & 3);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int j = jb + e;
+        s[n][e] = (j <= lim0 && j < n_keys) ? s[n][e] * scale_log2 : -INFINITY;
+        s[n][2 + e] = (j <= lim1 && j < n_keys) ? s[n][2 + e] * scale_log2 : -INFINITY;
+        mx0 = fmaxf(mx0, s[n][e]);
+        mx1 = fmaxf(mx1, s[n][2 + e]);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float sc0 = (mn0 == -INFINITY) ? 1.f : exp2f(m0 - mn0);
+    const float sc1 = (mn1 == -INFINITY) ? 1.f : exp2f(m1 - mn1);
+    const float base0 = (mn0 == -INFINITY) ? 0.f : mn0, base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+    float rs0 = 0.f, rs1 = 0.f;
+    uint32_t pa[4][4];                       // P as A fragments, one per 16-key step
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const float p0 = exp2f(s[n][0] - base0), p1 = exp2f(s[n][1] - base0);
+      const float p2 = exp2f(s[n][2] - base1), p3 = exp2f(s[n][3] - base1);
+      rs0 += p0 + p1;
+      rs1 += p2 + p3;
+      pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16(p0, p1);
+      pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16(p2, p3);
+    }
+    rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
+    rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
+    rs1 += __shfl_xor_sync(0xffffffffu, rs1, 1);
+    rs1 += __shfl_xor_sync(0xffffffffu, rs1, 2);
+    l0 = l0 * sc0 + rs0;
+    l1 = l1 * sc1 + rs1;
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) { o[i][0] *= sc0; o[i][1] *= sc0; o[i][2] *= sc1; o[i][3] *= sc1; }
+    // O += P V
+#pragma unroll
+    for (int kk = 0; kk < BKV / 16; ++kk) {
+#pragma unroll
+      for (int np = 0; np < HD / 16; ++np) {
+        const int key = kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int c = 2 * np + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + swz<HD>(key, c), b0, b1, b2, b3);
+        mma16816(o[2 * np], pa[kk], b0, b1);
+        mma16816(o[2 * np + 1], pa[kk], b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+  // normalise and store rows qi0, qi0 + 8
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const int col = 2 * (lane & 3);
+  if (qi0 < sd.len) {
+    bf16* op = out + ((size_t)(sd.row0 + qi0) * Hq + h) * HD + col;
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i)
+      *reinterpret_cast<uint32_t*>(op + i * 8) = pack_bf16(o[i][0] * inv0, o[i][1] * inv0);
+  }
+  if (qi0 + 8 < sd.len) {
+    bf16* op = out + ((size_t)(sd.row0 + qi0 + 8) * Hq + h) * HD + col;
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i)
+      *reinterpret_cast<uint32_t*>(op + i * 8) = pack_bf16(o[i][2] * inv1, o[i][3] * inv1);
+  }
 }
+
+}  // namespace fa
 
 cudaError_t launch_attention(const bf16* q, const bf16* knew, const bf16* vnew, bf16* out,
                              const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx, int layer_f,
                              int Hq, int Hkv, int hd, int max_len, cudaStream_t st) {
   if (n_seq <= 0 || max_len <= 0) return cudaSuccess;
+  if (n_seq > 65535) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-  dim3 grid((max_len * Hq + 3) / 4, n_seq);
-  if (hd == 128)
-    attn_rowwarp_kernel<128><<<grid, 128, 0, st>>>(q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2);
-  else if (hd == 64)
-    attn_rowwarp_kernel<64><<<grid, 128, 0, st>>>(q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2);
-  else
+  dim3 grid((max_len + fa::BQ - 1) / fa::BQ, Hq, n_seq);
+  if (hd == 128) {
+    constexpr int smem = fa::BQ * 128 * 2 + 4 * fa::BKV * 128 * 2;
+    static bool set = false;
+    if (!set) {
+      cudaError_t e = cudaFuncSetAttribute(fa::flash_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      set = true;
+    }
+    fa::flash_kernel<128><<<grid, 128, smem, st>>>(q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2);
+  } else if (hd == 64) {
+    constexpr int smem = fa::BQ * 64 * 2 + 4 * fa::BKV * 64 * 2;
+    fa::flash_kernel<64><<<grid, 128, smem, st>>>(q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2);
+  } else {
     return cudaErrorNotSupported;
+  }
   return cudaGetLastError();
 }
 

@@ -1,0 +1,498 @@
+// Chunked gated delta rule (WY form) for prefill-length sequences.
+//
+// For a chunk of n <= 64 rows with state S0 at its start ([Dv, Dk] per head), with
+// g = cumsum(log alpha) inside the chunk, gamma = exp(g), Gamma_ts = exp(g_t - g_s):
+//   A  = strict_lower(diag(beta) (Gamma * K K^T))
+//   W  = (I + A)^-1 diag(beta gamma) K,    Ut = (I + A)^-1 diag(beta) V
+//   U  = Ut - W S0^T                                  (the delta-rule write vectors)
+//   O  = diag(gamma) Q S0^T + lower_incl(Gamma * Q K^T) U
+//   S_next = gamma_n S0 + U^T diag(exp(g_n - g)) K
+// (WY representation of the gated delta rule, Yang, Kautz & Hatamizadeh, "Gated Delta
+// Networks", 2024; it reaches the token recurrence's result up to rounding, which the pages
+// allow for chunk boundaries: System1-Omni RFC #114, section 5.)
+//
+// Three launches per layer:
+//   chunk_prep   (chunk, head)          : g, A, forward substitution for W and Ut   (parallel)
+//   chunk_state  (sequence, head, 16 v) : U = Ut - W S^T, S <- gamma S + U^T K'     (sequential
+//                                         over chunks; records each chunk's start state)
+//   chunk_out    (chunk, head)          : O = gamma Q S_c^T + P U                   (parallel)
+// The two small matrix products of the state pass and all of chunk_out run on the tensor
+// cores (mma.sync m16n8k8 TF32 -> fp32); the state itself stays fp32.
+#include "common.cuh"
+
+namespace s1 {
+namespace gc {
+
+constexpr int C = 64;      // chunk rows
+constexpr int BV = 16;     // value rows per state-pass CTA
+// D = dk = dv (64 or 128) is a template parameter of every kernel.
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint32_t tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// D += A(16x8, row) * B(8x8, col), tf32 inputs, fp32 accumulate
+__device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------------------
+// chunk_prep: one CTA per (chunk, head), 256 threads.
+// Writes g (within-chunk cumsum of log alpha) over loga, W and Ut (fp32 [R, H, 128]).
+template <int D>
+__global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict__ proj, int ld,
+                                                         float* __restrict__ loga,
+                                                         const float* __restrict__ beta,
+                                                         const ChunkDesc* __restrict__ chunks, int H, int Dv,
+                                                         float* __restrict__ Wbuf, float* __restrict__ Ubuf) {
+  constexpr int SK = D + 4;       // row stride (floats) of the K tile
+  extern __shared__ float sm[];
+  float* sK = sm;                 // [C][SK]  K rows
+  float* sX = sK + C * SK;        // [C][2*D] rhs -> solution: W (cols 0..127) | Ut (cols 128..255)
+  float* sA = sX + C * 2 * D;     // [C][C+1]
+  float* sg = sA + C * (C + 1);   // [C]
+  float* sb = sg + C;             // [C]
+  const ChunkDesc cd = chunks[blockIdx.x];
+  const int h = blockIdx.y, n = cd.len, tid = threadIdx.x;
+  const int HDk = H * D;
+  // load K (normalised), V, g, beta
+  for (int i = tid; i < C * (D / 4); i += 256) {
+    const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+    float4 kv = make_float4(0, 0, 0, 0), vv = make_float4(0, 0, 0, 0);
+    if (r < n) {
+      const float* pr = proj + (size_t)(cd.row0 + r) * ld;
+      kv = *reinterpret_cast<const float4*>(pr + HDk + h * D + c4);
+      vv = *reinterpret_cast<const float4*>(pr + 2 * HDk + h * Dv + c4);
+    }
+    *reinterpret_cast<float4*>(sK + r * SK + c4) = kv;
+    *reinterpret_cast<float4*>(sX + r * 2 * D + D + c4) = vv;
+  }
+  if (tid < 32) {
+    // inclusive cumsum of log alpha over the chunk (2 values per lane)
+    float a0 = (2 * tid < n) ? loga[(size_t)(cd.row0 + 2 * tid) * H + h] : 0.f;
+    float a1 = (2 * tid + 1 < n) ? loga[(size_t)(cd.row0 + 2 * tid + 1) * H + h] : 0.f;
+    float s = a0 + a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(0xffffffffu, s, o);
+      if (tid >= o) s += t;
+    }
+    const float excl = s - (a0 + a1);
+    sg[2 * tid] = excl + a0;
+    sg[2 * tid + 1] = excl + a0 + a1;
+  } else if (tid < 32 + C) {
+    const int r = tid - 32;
+    sb[r] = (r < n) ? beta[(size_t)(cd.row0 + r) * H + h] : 0.f;
+  }
+  __syncthreads();
+  // A = strict_lower(beta_t exp(g_t - g_s) k_t.k_s): each thread a 4x4 block of the 64x64
+  {
+    const int tr = (tid >> 4) * 4, tc = (tid & 15) * 4;
+    float acc[4][4] = {};
+    for (int j = 0; j < D; j += 4) {
+      float4 a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = *reinterpret_cast<const float4*>(sK + (tr + i) * SK + j);
+        b[i] = *reinterpret_cast<const float4*>(sK + (tc + i) * SK + j);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          acc[i][k] += a[i].x * b[k].x + a[i].y * b[k].y + a[i].z * b[k].z + a[i].w * b[k].w;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = tr + i, s = tc + k;
+        sA[t * (C + 1) + s] = (s < t && t < n) ? sb[t] * __expf(sg[t] - sg[s]) * acc[i][k] : 0.f;
+      }
+  }
+  // rhs: W rows = beta_t gamma_t k_t ; Ut rows = beta_t v_t
+  for (int i = tid; i < C * D; i += 256) {
+    const int r = i / D, c = i % D;
+    sX[r * 2 * D + c] = sb[r] * __expf(sg[r]) * sK[r * SK + c];
+    sX[r * 2 * D + D + c] *= sb[r];
+  }
+  __syncthreads();
+  // forward substitution, one column per thread: X_t -= sum_{s<t} A_ts X_s
+  {
+    const int c = tid;   // 0 .. 2D-1
+    for (int t = 1; t < n && c < 2 * D; ++t) {
+      float acc = sX[t * 2 * D + c];
+      const float* Ar = sA + t * (C + 1);
+      for (int s = 0; s < t; ++s) acc = fmaf(-Ar[s], sX[s * 2 * D + c], acc);
+      sX[t * 2 * D + c] = acc;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < n * (D / 4); i += 256) {
+    const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+    const size_t o = ((size_t)(cd.row0 + r) * H + h) * D + c4;
+    *reinterpret_cast<float4*>(Wbuf + o) = *reinterpret_cast<const float4*>(sX + r * 2 * D + c4);
+    *reinterpret_cast<float4*>(Ubuf + o) = *reinterpret_cast<const float4*>(sX + r * 2 * D + D + c4);
+  }
+  if (tid < n) loga[(size_t)(cd.row0 + tid) * H + h] = sg[tid];
+}
+
+// ---------------------------------------------------------------------------------------
+// chunk_state: one CTA per (sequence, head, block of 16 value rows), 128 threads (4 warps).
+// Per chunk: U = Ut - W S^T (64 x 16, K = 128); S <- gamma_n S + U^T K' (16 x 128, K = 64),
+// K'_t = exp(g_n - g_t) k_t. Records S at each chunk's start (for chunk_out) and writes U
+// over Ut. The state block stays in shared memory in fp32.
+template <int D>
+struct StateSmem {
+  static constexpr int SW = D + 4;      // W tile stride  ([t][j], A-operand pattern)
+  static constexpr int SKK = D + 8;     // K tile stride  ([t][j], B-operand k-major pattern)
+  static constexpr int SS = D + 4;      // state stride   ([i][j])
+  static constexpr int SU = BV + 8;     // U tile stride  ([t][i])
+  float W[2][C * SW];
+  float K[2][C * SKK];
+  float Ut[2][C * BV];
+  float g[2][C];
+  float S[BV * SS];
+  float U[C * SU];
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restrict__ proj, int ld,
+                                                          const float* __restrict__ gbuf,
+                                                          const SeqDesc* __restrict__ seqs,
+                                                          const ChunkDesc* __restrict__ chunks,
+                                                          const CtxDesc* __restrict__ ctxs, int layer_g, int H,
+                                                          const float* __restrict__ Wbuf, float* __restrict__ Ubuf,
+                                                          float* __restrict__ Schunk) {
+  extern __shared__ __align__(16) uint8_t smraw[];
+  using SM = StateSmem<D>;
+  constexpr int SW = SM::SW, SKK = SM::SKK, SS = SM::SS, SU = SM::SU;
+  constexpr int NTS = D / 32;            // 8-column n-tiles per warp in the state update
+  SM& s = *reinterpret_cast<SM*>(smraw);
+  const SeqDesc sd = seqs[blockIdx.x];
+  const int h = blockIdx.y, v0 = blockIdx.z * BV;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int HDk = H * D;
+  const size_t head_off = (size_t)(layer_g * H + h) * D * D;
+  // initial state block
+  const float* S0 = sd.ctx_in >= 0 ? ctxs[sd.ctx_in].S + head_off : nullptr;
+  for (int i = tid; i < BV * D; i += 128) {
+    const int r = i / D, c = i % D;
+    s.S[r * SS + c] = S0 ? S0[(size_t)(v0 + r) * D + c] : 0.f;
+  }
+  const int nch = (sd.len + C - 1) / C;
+  auto load = [&](int cl, int st) {
+    const ChunkDesc cd = chunks[sd.chunk0 + cl];
+    for (int i = tid; i < C * (D / 4); i += 128) {
+      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+      const bool ok = r < cd.len;
+      const int row = cd.row0 + (ok ? r : 0);
+      cp16(&s.W[st][r * SW + c4], Wbuf + ((size_t)row * H + h) * D + c4, ok);
+      cp16(&s.K[st][r * SKK + c4], proj + (size_t)row * ld + HDk + h * D + c4, ok);
+    }
+    for (int i = tid; i < C * (BV / 4); i += 128) {
+      const int r = i / (BV / 4), c4 = (i % (BV / 4)) * 4;
+      const bool ok = r < cd.len;
+      const int row = cd.row0 + (ok ? r : 0);
+      cp16(&s.Ut[st][r * BV + c4], Ubuf + ((size_t)row * H + h) * D + v0 + c4, ok);
+    }
+    if (tid < C) {
+      const bool ok = tid < cd.len;
+      s.g[st][tid] = ok ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
+    }
+  };
+  if (nch > 0) load(0, 0);
+  cp_commit();
+  for (int cl = 0; cl < nch; ++cl) {
+    const int st = cl & 1;
+    const ChunkDesc cd = chunks[sd.chunk0 + cl];
+    if (cl + 1 < nch) load(cl + 1, st ^ 1);
+    cp_commit();
+    cp_wait<1>();
+    __syncthreads();
+    // record the chunk-start state block
+    {
+      float* dst = Schunk + ((size_t)(sd.chunk0 + cl) * H + h) * D * D + (size_t)v0 * D;
+      for (int i = tid; i < BV * (D / 4); i += 128) {
+        const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+        *reinterpret_cast<float4*>(dst + (size_t)r * D + c4) = *reinterpret_cast<const float4*>(&s.S[r * SS + c4]);
+      }
+    }
+    // U = Ut - W S^T : warp w -> rows 16w..16w+15, both 8-column n-tiles
+    {
+      float acc[2][4] = {};
+      const float* Wt = s.W[st];
+      const int r0 = warp * 16;
+#pragma unroll 4
+      for (int k = 0; k < D; k += 8) {
+        const uint32_t a0 = tf32(Wt[(r0 + gq) * SW + k + tq]), a1 = tf32(Wt[(r0 + gq + 8) * SW + k + tq]);
+        const uint32_t a2 = tf32(Wt[(r0 + gq) * SW + k + tq + 4]), a3 = tf32(Wt[(r0 + gq + 8) * SW + k + tq + 4]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint32_t b0 = tf32(s.S[(nt * 8 + gq) * SS + k + tq]);
+          const uint32_t b1 = tf32(s.S[(nt * 8 + gq) * SS + k + tq + 4]);
+          mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int c = nt * 8 + 2 * tq;
+        const int ra = r0 + gq, rb = r0 + gq + 8;
+        s.U[ra * SU + c] = s.Ut[st][ra * BV + c] - acc[nt][0];
+        s.U[ra * SU + c + 1] = s.Ut[st][ra * BV + c + 1] - acc[nt][1];
+        s.U[rb * SU + c] = s.Ut[st][rb * BV + c] - acc[nt][2];
+        s.U[rb * SU + c + 1] = s.Ut[st][rb * BV + c + 1] - acc[nt][3];
+      }
+    }
+    __syncthreads();
+    // write U (this block's 16 value columns) over Ut
+    for (int i = tid; i < cd.len * (BV / 4); i += 128) {
+      const int r = i / (BV / 4), c4 = (i % (BV / 4)) * 4;
+      *reinterpret_cast<float4*>(Ubuf + ((size_t)(cd.row0 + r) * H + h) * D + v0 + c4) =
+          make_float4(s.U[r * SU + c4], s.U[r * SU + c4 + 1], s.U[r * SU + c4 + 2], s.U[r * SU + c4 + 3]);
+    }
+    // S <- gamma_n S + U^T K' : warp w -> value rows 0..15, key columns (D/4)w .. (NTS n-tiles)
+    {
+      const float gn = s.g[st][cd.len - 1];
+      const float gam = __expf(gn);
+      float acc[NTS][4];
+#pragma unroll
+      for (int nt = 0; nt < NTS; ++nt) {
+        const int c = warp * (D / 4) + nt * 8 + 2 * tq;
+        acc[nt][0] = gam * s.S[gq * SS + c];
+        acc[nt][1] = gam * s.S[gq * SS + c + 1];
+        acc[nt][2] = gam * s.S[(gq + 8) * SS + c];
+        acc[nt][3] = gam * s.S[(gq + 8) * SS + c + 1];
+      }
+      const float* Kt = s.K[st];
+#pragma unroll 2
+      for (int k = 0; k < C; k += 8) {
+        // A[i][t] = U[t][i]
+        const uint32_t a0 = tf32(s.U[(k + tq) * SU + gq]), a1 = tf32(s.U[(k + tq) * SU + gq + 8]);
+        const uint32_t a2 = tf32(s.U[(k + tq + 4) * SU + gq]), a3 = tf32(s.U[(k + tq + 4) * SU + gq + 8]);
+        const float e0 = __expf(gn - s.g[st][k + tq]), e1 = __expf(gn - s.g[st][k + tq + 4]);
+#pragma unroll
+        for (int nt = 0; nt < NTS; ++nt) {
+          const int c = warp * (D / 4) + nt * 8 + gq;
+          const uint32_t b0 = tf32(e0 * Kt[(k + tq) * SKK + c]);
+          const uint32_t b1 = tf32(e1 * Kt[(k + tq + 4) * SKK + c]);
+          mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      __syncthreads();   // every warp has read S and U
+#pragma unroll
+      for (int nt = 0; nt < NTS; ++nt) {
+        const int c = warp * (D / 4) + nt * 8 + 2 * tq;
+        s.S[gq * SS + c] = acc[nt][0];
+        s.S[gq * SS + c + 1] = acc[nt][1];
+        s.S[(gq + 8) * SS + c] = acc[nt][2];
+        s.S[(gq + 8) * SS + c + 1] = acc[nt][3];
+      }
+    }
+    __syncthreads();
+  }
+  if (sd.ctx_out >= 0) {
+    float* So = ctxs[sd.ctx_out].S + head_off;
+    for (int i = tid; i < BV * D; i += 128) {
+      const int r = i / D, c = i % D;
+      So[(size_t)(v0 + r) * D + c] = s.S[r * SS + c];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// chunk_out: one CTA per (chunk, head), 256 threads (8 warps).
+// O = diag(gamma) Q S_c^T + P U, P = lower_incl(Gamma * Q K^T); out bf16 [R, H*Dv].
+template <int D>
+struct OutSmem {
+  static constexpr int SQ = D + 4;   // Q, K tiles ([t][j], A / B(n-major) pattern)
+  static constexpr int SSC = D + 4;  // chunk-start state ([i][j])
+  static constexpr int SUo = D + 8;  // U tile ([s][i], B k-major pattern)
+  static constexpr int SP = C + 4;   // P ([t][s])
+  float Q[C * SQ];
+  float KU[C * SUo];        // K, then U
+  float S[D * SSC];
+  float P[C * SP];
+  float g[C];
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict__ proj, int ld,
+                                                        const float* __restrict__ gbuf,
+                                                        const ChunkDesc* __restrict__ chunks, int H,
+                                                        const float* __restrict__ Ubuf,
+                                                        const float* __restrict__ Schunk, bf16* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t smraw[];
+  using SM = OutSmem<D>;
+  constexpr int SQ = SM::SQ, SSC = SM::SSC, SUo = SM::SUo, SP = SM::SP;
+  constexpr int NTO = D / 16;            // 8-column n-tiles per warp of the output
+  SM& s = *reinterpret_cast<SM*>(smraw);
+  const int ci = blockIdx.x, h = blockIdx.y;
+  const ChunkDesc cd = chunks[ci];
+  const int n = cd.len;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int HDk = H * D;
+  for (int i = tid; i < C * (D / 4); i += 256) {
+    const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+    const bool ok = r < n;
+    const int row = cd.row0 + (ok ? r : 0);
+    cp16(&s.Q[r * SQ + c4], proj + (size_t)row * ld + h * D + c4, ok);
+    cp16(&s.KU[r * SQ + c4], proj + (size_t)row * ld + HDk + h * D + c4, ok);   // K with the Q stride
+  }
+  const float* Sc = Schunk + ((size_t)ci * H + h) * D * D;
+  for (int i = tid; i < D * (D / 4); i += 256) {
+    const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+    cp16(&s.S[r * SSC + c4], Sc + (size_t)r * D + c4, true);
+  }
+  if (tid < C) s.g[tid] = tid < n ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
+  cp_commit();
+  cp_wait<0>();
+  __syncthreads();
+  const int mt = warp & 3;          // 16-row m-tile
+  const int r0 = mt * 16;
+  // P = lower_incl(exp(g_t - g_s) q_t.k_s): warp -> rows r0.., key columns 32*(warp>>2) .. +31
+  {
+    float acc[4][4] = {};
+    const int c0 = (warp >> 2) * 32;
+#pragma unroll 4
+    for (int k = 0; k < D; k += 8) {
+      const uint32_t a0 = tf32(s.Q[(r0 + gq) * SQ + k + tq]), a1 = tf32(s.Q[(r0 + gq + 8) * SQ + k + tq]);
+      const uint32_t a2 = tf32(s.Q[(r0 + gq) * SQ + k + tq + 4]), a3 = tf32(s.Q[(r0 + gq + 8) * SQ + k + tq + 4]);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int key = c0 + nt * 8 + gq;
+        const uint32_t b0 = tf32(s.KU[key * SQ + k + tq]), b1 = tf32(s.KU[key * SQ + k + tq + 4]);
+        mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = r0 + gq + (e >> 1) * 8, sidx = c0 + nt * 8 + 2 * tq + (e & 1);
+        s.P[t * SP + sidx] = (sidx <= t && t < n) ? __expf(s.g[t] - s.g[sidx]) * acc[nt][e] : 0.f;
+      }
+    }
+  }
+  __syncthreads();
+  // U tile over K (k-major stride)
+  for (int i = tid; i < C * (D / 4); i += 256) {
+    const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+    const bool ok = r < n;
+    const int row = cd.row0 + (ok ? r : 0);
+    cp16(&s.KU[r * SUo + c4], Ubuf + ((size_t)row * H + h) * D + c4, ok);
+  }
+  cp_commit();
+  // O1 = Q S_c^T  (warp -> rows r0.., value columns (D/2)*(warp>>2) .. : NTO n-tiles)
+  float o[NTO][4] = {};
+  const int cbase = (warp >> 2) * (D / 2);
+#pragma unroll 2
+  for (int k = 0; k < D; k += 8) {
+    const uint32_t a0 = tf32(s.Q[(r0 + gq) * SQ + k + tq]), a1 = tf32(s.Q[(r0 + gq + 8) * SQ + k + tq]);
+    const uint32_t a2 = tf32(s.Q[(r0 + gq) * SQ + k + tq + 4]), a3 = tf32(s.Q[(r0 + gq + 8) * SQ + k + tq + 4]);
+#pragma unroll
+    for (int nt = 0; nt < NTO; ++nt) {
+      const int i = cbase + nt * 8 + gq;
+      const uint32_t b0 = tf32(s.S[i * SSC + k + tq]), b1 = tf32(s.S[i * SSC + k + tq + 4]);
+      mma_tf32(o[nt], a0, a1, a2, a3, b0, b1);
+    }
+  }
+  {
+    const float ga = __expf(s.g[r0 + gq]), gb = __expf(s.g[r0 + gq + 8]);
+#pragma unroll
+    for (int nt = 0; nt < NTO; ++nt) { o[nt][0] *= ga; o[nt][1] *= ga; o[nt][2] *= gb; o[nt][3] *= gb; }
+  }
+  cp_wait<0>();
+  __syncthreads();
+  // O += P U
+#pragma unroll 2
+  for (int k = 0; k < C; k += 8) {
+    const uint32_t a0 = tf32(s.P[(r0 + gq) * SP + k + tq]), a1 = tf32(s.P[(r0 + gq + 8) * SP + k + tq]);
+    const uint32_t a2 = tf32(s.P[(r0 + gq) * SP + k + tq + 4]), a3 = tf32(s.P[(r0 + gq + 8) * SP + k + tq + 4]);
+#pragma unroll
+    for (int nt = 0; nt < NTO; ++nt) {
+      const int i = cbase + nt * 8 + gq;
+      const uint32_t b0 = tf32(s.KU[(k + tq) * SUo + i]), b1 = tf32(s.KU[(k + tq + 4) * SUo + i]);
+      mma_tf32(o[nt], a0, a1, a2, a3, b0, b1);
+    }
+  }
+  const int HDv = H * D;
+#pragma unroll
+  for (int nt = 0; nt < NTO; ++nt) {
+    const int c = cbase + nt * 8 + 2 * tq;
+    const int ta = r0 + gq, tb = r0 + gq + 8;
+    if (ta < n)
+      *reinterpret_cast<__nv_bfloat162*>(out + (size_t)(cd.row0 + ta) * HDv + h * D + c) =
+          __floats2bfloat162_rn(o[nt][0], o[nt][1]);
+    if (tb < n)
+      *reinterpret_cast<__nv_bfloat162*>(out + (size_t)(cd.row0 + tb) * HDv + h * D + c) =
+          __floats2bfloat162_rn(o[nt][2], o[nt][3]);
+  }
+}
+
+}  // namespace gc
+
+bool gdn_chunked_supported(int H, int Dk, int Dv, int ld) {
+  return Dk == Dv && (Dk == 64 || Dk == 128) && H > 0 && (ld % 4) == 0;
+}
+
+template <int D>
+static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const float* beta, bf16* out,
+                                    const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
+                                    const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
+                                    float* Schunk, cudaStream_t st) {
+  static bool attr = false;
+  const size_t sp = (size_t)(gc::C * (D + 4) + gc::C * 2 * D + gc::C * (gc::C + 1) + 2 * gc::C) * 4;
+  const size_t ss = sizeof(gc::StateSmem<D>);
+  const size_t so = sizeof(gc::OutSmem<D>);
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gc::chunk_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gc::chunk_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gc::chunk_out_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  gc::chunk_prep_kernel<D><<<dim3(n_chunks, H), 256, sp, st>>>(proj, ld, loga, beta, d_chunks, H, D, Wbuf, Ubuf);
+  gc::chunk_state_kernel<D><<<dim3(n_seq, H, D / gc::BV), 128, ss, st>>>(proj, ld, loga, d_seq, d_chunks, d_ctx,
+                                                                         layer_g, H, Wbuf, Ubuf, Schunk);
+  gc::chunk_out_kernel<D><<<dim3(n_chunks, H), 256, so, st>>>(proj, ld, loga, d_chunks, H, Ubuf, Schunk, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gdn_chunked(float* proj, int ld, float* loga, const float* beta, bf16* out,
+                               const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
+                               const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
+                               float* Schunk, cudaStream_t st, long* launches) {
+  if (n_seq <= 0 || n_chunks <= 0) return cudaSuccess;
+  if (!gdn_chunked_supported(H, Dk, Dv, ld)) return cudaErrorNotSupported;
+  if (n_seq > 65535 || n_chunks > 2147483647 / 2) return cudaErrorInvalidValue;
+  cudaError_t e = (Dk == 128)
+                      ? launch_chunked_d<128>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
+                                              layer_g, H, Wbuf, Ubuf, Schunk, st)
+                      : launch_chunked_d<64>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
+                                             layer_g, H, Wbuf, Ubuf, Schunk, st);
+  if (launches) *launches += 3;
+  return e;
+}
+
+}  // namespace s1

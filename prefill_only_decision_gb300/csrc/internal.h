@@ -24,7 +24,16 @@ struct SeqDesc {
   int pos0;     // position of the first row
   int ctx_in;   // context continued (-1: start from zero state / no cached keys)
   int ctx_out;  // context whose snapshot this sequence writes (-1: none)
+  int chunk0;   // index of its first 64-row chunk in the chunk table
 };
+
+// 64-row chunks of the sequences (chunk boundaries restart at every sequence start).
+struct ChunkDesc {
+  int row0;
+  int len;      // 1 .. 64
+  int seq;
+};
+constexpr int GDN_CHUNK = 64;
 
 // A prefix snapshot as seen by kernels: all layers' tensors of one state.
 struct CtxDesc {
@@ -57,6 +66,11 @@ cudaError_t launch_gdn_prep(float* proj, int ld, float* alpha, float* beta, int 
 cudaError_t launch_gdn_scan(const float* proj, int ld, const float* alpha, const float* beta,
                             bf16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
                             int layer_g, int H, int Dk, int Dv, cudaStream_t st);
+bool gdn_chunked_supported(int H, int Dk, int Dv, int ld);
+cudaError_t launch_gdn_chunked(float* proj, int ld, float* loga, const float* beta, bf16* out,
+                               const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
+                               const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
+                               float* Schunk, cudaStream_t st, long* launches);
 cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab, const int* row_seq,
                               const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, bf16* q,
                               bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,

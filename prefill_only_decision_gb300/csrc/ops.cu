@@ -76,24 +76,39 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
   if (R < 0 || H <= 0 || n_seq <= 0 || !row0 || !len) return op_fail(S1_ERR_INVALID_ARG, "gdn: bad arguments");
   std::vector<SeqDesc> seqs(n_seq);
   std::vector<CtxDesc> ctxs(2 * n_seq);
+  std::vector<ChunkDesc> chunks;
   const size_t per = (size_t)H * dv * dk;
   for (int s = 0; s < n_seq; ++s) {
     if (row0[s] < 0 || len[s] < 0 || row0[s] + len[s] > R) return op_fail(S1_ERR_INVALID_ARG, "gdn: sequence outside rows");
-    seqs[s] = SeqDesc{row0[s], len[s], 0, S0 ? s : -1, S_out ? n_seq + s : -1};
+    seqs[s] = SeqDesc{row0[s], len[s], 0, S0 ? s : -1, S_out ? n_seq + s : -1, (int)chunks.size()};
+    for (int c = 0; c < len[s]; c += GDN_CHUNK)
+      chunks.push_back(ChunkDesc{row0[s] + c, len[s] - c < GDN_CHUNK ? len[s] - c : GDN_CHUNK, s});
     ctxs[s] = CtxDesc{const_cast<float*>(S0 ? S0 + s * per : nullptr), nullptr, 0, 0};
     ctxs[n_seq + s] = CtxDesc{S_out ? S_out + s * per : nullptr, nullptr, 0, 0};
   }
+  const int nch = (int)chunks.size();
   Tmp t;
   SeqDesc* dseq = (SeqDesc*)t.get(seqs.size() * sizeof(SeqDesc));
   CtxDesc* dctx = (CtxDesc*)t.get(ctxs.size() * sizeof(CtxDesc));
-  float* loga = (float*)t.get((size_t)R * H * 4);
-  float* beta = (float*)t.get((size_t)R * H * 4);
-  if (!dseq || !dctx || !loga || !beta) return op_fail(S1_ERR_OOM, "gdn: temporaries");
+  ChunkDesc* dch = (ChunkDesc*)t.get((nch + 1) * sizeof(ChunkDesc));
+  float* loga = (float*)t.get((size_t)R * H * 4 + 16);
+  float* beta = (float*)t.get((size_t)R * H * 4 + 16);
+  if (!dseq || !dctx || !dch || !loga || !beta) return op_fail(S1_ERR_OOM, "gdn: temporaries");
   OCK(cudaMemcpyAsync(dseq, seqs.data(), seqs.size() * sizeof(SeqDesc), cudaMemcpyHostToDevice, st));
   OCK(cudaMemcpyAsync(dctx, ctxs.data(), ctxs.size() * sizeof(CtxDesc), cudaMemcpyHostToDevice, st));
+  if (nch) OCK(cudaMemcpyAsync(dch, chunks.data(), nch * sizeof(ChunkDesc), cudaMemcpyHostToDevice, st));
   const int ld = 2 * H * dk + H * dv + 2 * H;
   OCK(launch_gdn_prep(proj, ld, loga, beta, R, H, dk, dv, l2_eps, st));
-  OCK(launch_gdn_scan(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dctx, 0, H, dk, dv, st));
+  if (gdn_chunked_supported(H, dk, dv, ld)) {
+    float* W = (float*)t.get((size_t)R * H * dk * 4 + 16);
+    float* U = (float*)t.get((size_t)R * H * dv * 4 + 16);
+    float* Sc = (float*)t.get((size_t)(nch + 1) * per * 4);
+    if (!W || !U || !Sc) return op_fail(S1_ERR_OOM, "gdn: temporaries");
+    OCK(launch_gdn_chunked(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
+                           st, nullptr));
+  } else {
+    OCK(launch_gdn_scan(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dctx, 0, H, dk, dv, st));
+  }
   OCK(cudaStreamSynchronize(st));
   return S1_OK;
 }
@@ -107,7 +122,7 @@ int s1_op_attention(const void* q, const void* k_new, const void* v_new, const v
   std::vector<SeqDesc> seqs(n_seq);
   int max_len = 0;
   for (int s = 0; s < n_seq; ++s) {
-    seqs[s] = SeqDesc{row0[s], len[s], P, P > 0 ? 0 : -1, -1};
+    seqs[s] = SeqDesc{row0[s], len[s], P, P > 0 ? 0 : -1, -1, 0};
     max_len = len[s] > max_len ? len[s] : max_len;
   }
   CtxDesc c{nullptr, (bf16*)kv_cache, P, P};

@@ -93,6 +93,8 @@ struct Scratch {
   bf16* vnew = nullptr;
   float* loga = nullptr;
   float* beta = nullptr;
+  float* gw = nullptr;       // chunked scan: W rows [R, H, dk]
+  float* gu = nullptr;       // chunked scan: Ut / U rows [R, H, dv]
   int* meta = nullptr;       // row_src | row_seq | seqs | ctxs | readout metadata
   size_t meta_bytes = 0;
   float* ws = nullptr;       // split-K workspace
@@ -117,6 +119,9 @@ struct s1_model {
   int max_pos = 0;
   int* d_err = nullptr;
   Scratch sc;
+  float* schunk = nullptr;     // chunk-start states of the chunked scan [chunks, H, dv, dk]
+  size_t schunk_chunks = 0;
+  bool gdn_token = false;      // S1_GDN=token: token-by-token scan (debugging)
   char* pinned = nullptr;      // host staging for metadata uploads
   size_t pinned_bytes = 0;
   cudaEvent_t meta_done = nullptr;
@@ -180,6 +185,7 @@ struct ProfScope {
 namespace {
 size_t meta_bytes_for(int rows, int max_seq, int max_ctx, int max_q, int max_opt) {
   return align_up((size_t)rows * 2 * sizeof(int), 256) + align_up((size_t)max_seq * sizeof(SeqDesc), 256) +
+         align_up((size_t)(rows + max_seq) * sizeof(ChunkDesc), 256) +
          align_up((size_t)max_ctx * sizeof(CtxDesc), 256) +
          align_up((size_t)(3 * max_q + 1 + max_opt) * sizeof(int), 256);
 }
@@ -215,6 +221,8 @@ int ensure_scratch(s1_model* m, int rows) {
   sc.vnew = (bf16*)take(R * (size_t)s.fa_kv_heads * s.fa_head_dim * 2 + 256);
   sc.loga = (float*)take(R * H * 4);
   sc.beta = (float*)take(R * H * 4);
+  sc.gw = (float*)take(R * H * (size_t)std::max(s.la_dk, 1) * 4);
+  sc.gu = (float*)take(R * H * (size_t)std::max(s.la_dv, 1) * 4);
   const int max_seq = want, max_ctx = want, max_q = want, max_opt = 64 * want;
   sc.meta_bytes = meta_bytes_for(want, max_seq, max_ctx, max_q, max_opt);
   sc.meta = (int*)take(sc.meta_bytes);
@@ -223,7 +231,8 @@ int ensure_scratch(s1_model* m, int rows) {
   sc.out_floats = (size_t)max_opt + (size_t)max_q * S1_STAT_COUNT + (size_t)max_q * s.d_model;
   sc.out = (float*)take(sc.out_floats * 4);
   for (void* p : {(void*)sc.x, (void*)sc.xn, (void*)sc.proj, (void*)sc.mix, (void*)sc.h, (void*)sc.q,
-                  (void*)sc.knew, (void*)sc.vnew, (void*)sc.loga, (void*)sc.beta, (void*)sc.meta,
+                  (void*)sc.knew, (void*)sc.vnew, (void*)sc.loga, (void*)sc.beta, (void*)sc.gw, (void*)sc.gu,
+                  (void*)sc.meta,
                   (void*)sc.ws, (void*)sc.out}) {
     if (!p) {
       free_scratch(sc);
@@ -250,6 +259,7 @@ struct Meta {
   std::vector<int> row_src, row_seq;
   std::vector<SeqDesc> seqs;
   std::vector<CtxDesc> ctxs;
+  std::vector<ChunkDesc> chunks;
   std::vector<int> q_row, q_type, opt_off, opt_ids;
   int max_len = 0, max_opts = 0;
   // device views
@@ -257,10 +267,23 @@ struct Meta {
   int* d_row_seq = nullptr;
   SeqDesc* d_seqs = nullptr;
   CtxDesc* d_ctxs = nullptr;
+  ChunkDesc* d_chunks = nullptr;
   int *d_q_row = nullptr, *d_q_type = nullptr, *d_opt_off = nullptr, *d_opt_ids = nullptr;
 };
 
+// Splits every sequence into 64-row chunks (chunk boundaries restart at each sequence).
+void build_chunks(Meta& mt) {
+  mt.chunks.clear();
+  for (size_t s = 0; s < mt.seqs.size(); ++s) {
+    SeqDesc& sd = mt.seqs[s];
+    sd.chunk0 = (int)mt.chunks.size();
+    for (int c = 0; c < sd.len; c += GDN_CHUNK)
+      mt.chunks.push_back(ChunkDesc{sd.row0 + c, std::min(GDN_CHUNK, sd.len - c), (int)s});
+  }
+}
+
 int upload_meta(s1_model* m, Meta& mt) {
+  build_chunks(mt);
   const int R = (int)mt.row_src.size();
   const size_t need = meta_bytes_for(R, (int)mt.seqs.size(), (int)mt.ctxs.size(), (int)mt.q_row.size(),
                                      (int)mt.opt_ids.size());
@@ -280,6 +303,7 @@ int upload_meta(s1_model* m, Meta& mt) {
   mt.d_row_seq = (int*)put(mt.row_seq.data(), R * sizeof(int));
   mt.d_seqs = (SeqDesc*)put(mt.seqs.data(), mt.seqs.size() * sizeof(SeqDesc));
   mt.d_ctxs = (CtxDesc*)put(mt.ctxs.data(), mt.ctxs.size() * sizeof(CtxDesc));
+  mt.d_chunks = (ChunkDesc*)put(mt.chunks.data(), mt.chunks.size() * sizeof(ChunkDesc));
   std::vector<int> rq;
   rq.insert(rq.end(), mt.q_row.begin(), mt.q_row.end());
   rq.insert(rq.end(), mt.q_type.begin(), mt.q_type.end());
@@ -344,9 +368,24 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
       {
         ProfScope ps(m, S1_PROF_GDN, 0, 0);
         CK(launch_gdn_prep(sc.proj, L.n_in, sc.loga, sc.beta, R, H, s.la_dk, s.la_dv, s.l2_eps, st));
-        CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_ctxs,
-                           L.ord, H, s.la_dk, s.la_dv, st));
-        m->launches += 2;
+        m->launches += 1;
+        const int nch = (int)mt.chunks.size();
+        if (!m->gdn_token && gdn_chunked_supported(H, s.la_dk, s.la_dv, L.n_in)) {
+          if ((size_t)nch > m->schunk_chunks) {
+            CK(cudaStreamSynchronize(st));
+            dfree(m->schunk);
+            const size_t cap = std::max<size_t>(nch, 2 * m->schunk_chunks);
+            m->schunk = (float*)dalloc(cap * H * (size_t)s.la_dv * s.la_dk * 4);
+            m->schunk_chunks = m->schunk ? cap : 0;
+            if (!m->schunk) return fail(S1_ERR_OOM, "chunk-state buffer (%zu chunks) allocation failed", cap);
+          }
+          CK(launch_gdn_chunked(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
+                                mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, st, &m->launches));
+        } else {
+          CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_ctxs,
+                             L.ord, H, s.la_dk, s.la_dv, st));
+          m->launches += 1;
+        }
       }
     } else {
       {
@@ -475,7 +514,7 @@ int build_decide_meta(s1_model* m, int n_req, const s1_state* const* states, con
     for (int j = 0; j < n_q[r]; ++j) {
       const s1_question& q = qs[r][j];
       const int sidx = (int)mt.seqs.size();
-      mt.seqs.push_back(SeqDesc{row, q.n_suffix, st->P, r, -1});
+      mt.seqs.push_back(SeqDesc{row, q.n_suffix, st->P, r, -1, 0});
       mt.max_len = std::max(mt.max_len, q.n_suffix);
       for (int i = 0; i < q.n_suffix; ++i) {
         mt.row_src.push_back(check_ids ? q.suffix[i] : 0);
@@ -513,7 +552,7 @@ int build_prefill_meta(s1_model* m, int n_req, const int32_t* n_tokens, const in
   for (int r = 0; r < n_req; ++r) {
     const int P = n_tokens[r] + n_embeds[r];
     mt.ctxs.push_back(CtxDesc{states[r]->S, states[r]->KV, 0, states[r]->cap});
-    mt.seqs.push_back(SeqDesc{row, P, 0, -1, r});
+    mt.seqs.push_back(SeqDesc{row, P, 0, -1, r, 0});
     mt.max_len = std::max(mt.max_len, P);
     for (int i = 0; i < P; ++i) mt.row_seq.push_back(r);
     for (int i = 0; i < n_embeds[r]; ++i) mt.row_src.push_back(-1 - (erow + i));
@@ -579,6 +618,8 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   m->n_mix = std::max(nG ? H * Dv : 0, nF ? Hq * hd : 0);
   const char* gi = getenv("S1_GEMM");
   m->force_simt = gi && strcmp(gi, "simt") == 0;
+  const char* gd = getenv("S1_GDN");
+  m->gdn_token = gd && strcmp(gd, "token") == 0;
   m->gemm_impl = m->force_simt ? 1 : 0;
   auto bail = [&](int rc) {
     s1_model_destroy(m);
@@ -740,6 +781,7 @@ void s1_model_destroy(s1_model* m) {
   dfree(m->arena);
   dfree(m->rope_tab);
   dfree(m->d_err);
+  dfree(m->schunk);
   if (m->pinned) cudaFreeHost(m->pinned);
   if (m->meta_done) cudaEventDestroy(m->meta_done);
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
