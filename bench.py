@@ -157,6 +157,66 @@ def run_reference(args, cfg):
     return 0
 
 
+def run_kernel(args):
+    """Time one kernel-level entry point (s1_ops.h) in isolation: `--kernel gemm --shape M,N,K[,epi]`,
+    `--kernel gdn --shape R,H,D[,nseq]` or `--kernel attn --shape P,len,nseq,Hq,Hkv,hd`."""
+    import torch
+    from prefill_only_decision_gb300 import binding as B
+    dims = [int(x) for x in args.shape.split(",")]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.kernel == "gemm":
+        M, N, K = dims[:3]
+        epi = dims[3] if len(dims) > 3 else 0
+        X = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
+        W = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.bfloat16)
+        out = torch.zeros((M, N // 2 if epi == 3 else N), device="cuda",
+                          dtype=torch.bfloat16 if epi in (1, 3) else torch.float32)
+        ldo = out.shape[1]
+        fn = lambda: B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), ldo, 0)
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+    elif args.kernel == "gdn":
+        R, H, D = dims[:3]
+        nseq = dims[3] if len(dims) > 3 else 1
+        ld = 3 * H * D + 2 * H
+        proj = torch.randn((R, ld), device="cuda", generator=g)
+        out = torch.zeros((R, H * D), device="cuda", dtype=torch.bfloat16)
+        lens = [R // nseq] * nseq
+        lens[-1] += R - sum(lens)
+        row0 = list(np.cumsum([0] + lens[:-1]))
+        fn = lambda: B.op_gdn(proj.data_ptr(), R, H, D, D, 1e-6, row0, lens, 0, 0, out.data_ptr())
+        work, unit = 6.0 * R * H * D * D, "GFLOP/s (recurrence count)"
+    else:
+        P, L, nseq, Hq, Hkv, hd = dims[:6]
+        R = L * nseq
+        q = torch.randn((R, Hq, hd), device="cuda", generator=g).to(torch.bfloat16)
+        kn = torch.randn((R, Hkv, hd), device="cuda", generator=g).to(torch.bfloat16)
+        vn = torch.randn((R, Hkv, hd), device="cuda", generator=g).to(torch.bfloat16)
+        kv = torch.randn((2, max(P, 1), Hkv, hd), device="cuda", generator=g).to(torch.bfloat16)
+        out = torch.zeros((R, Hq * hd), device="cuda", dtype=torch.bfloat16)
+        row0 = [i * L for i in range(nseq)]
+        fn = lambda: B.op_attention(q.data_ptr(), kn.data_ptr(), vn.data_ptr(), kv.data_ptr() if P else 0, P, row0,
+                                    [L] * nseq, Hq, Hkv, hd, out.data_ptr())
+        keys = sum(P + i + 1 for i in range(L)) * nseq
+        work, unit = 4.0 * hd * Hq * keys, "TFLOP/s"
+    for _ in range(max(1, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(1, args.steps)):
+        ev0.record()
+        fn()
+        ev1.record()
+        torch.cuda.synchronize()
+        ts.append(ev0.elapsed_time(ev1))
+    ms = float(np.median(ts))
+    scale = 1e12 if unit.startswith("TFLOP") else 1e9
+    print(json.dumps({"kernel": args.kernel, "shape": dims, "ms_median": ms, "ms_min": float(min(ts)),
+                      "achieved": work / (ms / 1e3) / scale, "unit": unit,
+                      "note": "op-level call (includes its small temporaries and one synchronisation)"}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -165,7 +225,11 @@ def main():
     ap.add_argument("--config", default="4b")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["gemm", "gdn", "attn"], help="time one kernel entry point alone")
+    ap.add_argument("--shape", default="1024,18432,2560,3")
     args = ap.parse_args()
+    if args.kernel:
+        return run_kernel(args)
     from prefill_only_decision_gb300 import configs
     cfg = configs.CONFIGS[args.config]
     if args.impl == "reference":
@@ -234,11 +298,16 @@ def main():
     launches0 = model.counters()["launches"]
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nvtx = os.environ.get("S1_NVTX") == "1"     # lets ncu --nvtx-include "timed/" select the timed steps
     with ClockSampler(local) as clk:
+        if nvtx:
+            torch.cuda.nvtx.range_push("timed")
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
+        if nvtx:
+            torch.cuda.nvtx.range_pop()
         barrier()
     ms_total = e0.elapsed_time(e1)
     launches = (model.counters()["launches"] - launches0) // max(1, args.steps)

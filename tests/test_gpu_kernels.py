@@ -163,7 +163,8 @@ def test_gdn_scan(B, H, D, lens, with_s0):
         o, S = ogdn.recurrent(q, k, v, al, be, s0)
         o = o.reshape(n, HD)
         assert np.abs(got[r0:r0 + n] - o).max() <= 2.0 ** -8 * np.abs(o).max() + 1e-4
-        np.testing.assert_allclose(gotS[s], S, atol=1e-4 * max(1.0, np.abs(S).max()))
+        # state products run on TF32 inputs (10-bit mantissa) with fp32 accumulation
+        np.testing.assert_allclose(gotS[s], S, atol=3e-3 * max(1.0, np.abs(S).max()))
 
 
 @pytest.mark.parametrize("Hq,Hkv,hd,P,lens", [(4, 2, 64, 0, [96]), (16, 4, 128, 0, [300, 17]),
