@@ -107,10 +107,8 @@ class ClockSampler:
 
 
 def dist_setup():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    from prefill_only_decision_gb300 import replicas
+    return replicas.world()
 
 
 def time_oracle(cfg, W, req, budget_s: float = 25.0):
@@ -312,11 +310,8 @@ def main():
     ms_total = e0.elapsed_time(e1)
     launches = (model.counters()["launches"] - launches0) // max(1, args.steps)
     model.sync()
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    from prefill_only_decision_gb300 import replicas
+    ms_total = replicas.max_over_ranks(ms_total, device="cuda")
     ms_step = ms_total / max(1, args.steps)
     value = ws * n_q * args.steps / (ms_total / 1000.0)
 

