@@ -41,6 +41,23 @@ enum { S1_EPI_F32 = 0, S1_EPI_BF16 = 1, S1_EPI_RESADD = 2, S1_EPI_SWIGLU = 3 };
 int s1_op_gemm(const void* X, const void* W, int32_t M, int32_t N, int32_t K, int32_t epi,
                void* out, int32_t ldo, int32_t impl, void* stream);
 
+/* s1_op_gemm without any device allocation. This entry point has no counterpart in the
+ * pages: it exists for callers that cannot call cudaMalloc when they run a projection —
+ * code whose device memory is owned and budgeted by another framework, real-time loops that
+ * must not allocate (an allocation can synchronise the device), or processes whose memory is
+ * fixed up front. Same arguments, plan and results as s1_op_gemm (blocking; stream may be
+ * NULL). Its split-K partials and its error word live in fixed device arrays inside the
+ * library: S1_NOALLOC_WS_FLOATS floats (16 MiB) plus 256 bytes, reserved on every GPU that
+ * loads the library until the process exits. The first call on a device looks up the arrays'
+ * device addresses (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call shares the arrays: calls that overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller. A shape whose
+ * split-K plan needs more than S1_NOALLOC_WS_FLOATS floats of partials is rejected with
+ * S1_ERR_BUDGET before any device work. */
+#define S1_NOALLOC_WS_FLOATS (4 * 1024 * 1024)
+int s1_op_gemm_noalloc(const void* X, const void* W, int32_t M, int32_t N, int32_t K, int32_t epi,
+                       void* out, int32_t ldo, void* stream);
+
 /* Gated delta rule over packed sequences, per head (Yang, Kautz & Hatamizadeh 2024):
  *   q, k <- L2-normalised (x / sqrt(sum x^2 + l2_eps)), alpha = exp(-softplus(a)),
  *   beta = sigmoid(b), S_t = alpha S_{t-1}(I - beta k k^T) + beta v k^T, o_t = S_t q_t.

@@ -460,6 +460,11 @@ bool gemm_tc_supported(int M, int N, int K, int epi) {
          tc::get_encode() != nullptr;
 }
 
+size_t gemm_tc_plan_ws_floats(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
+  const tc::Plan pl = tc::plan_for(M, N, K, epi, num_sms, ws_cap);
+  return pl.splits > 1 ? (size_t)pl.splits * pl.m_tiles * tc::BM * (size_t)N : 0;
+}
+
 size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms) {
   // K is split only while the tile count is below the SM count, so the partials of one
   // launch never exceed about 2 x num_sms tiles of 128 x 256.
@@ -500,3 +505,91 @@ cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, in
 }
 
 }  // namespace s1
+
+// =======================================================================================
+// GEMM entry point that allocates nothing.
+//
+// For callers that cannot allocate device memory at call time: code running where
+// cudaMalloc is not allowed or not wanted (inside a real-time serving loop that must not
+// synchronise the device, under an allocator that is owned by another framework, or in a
+// process whose memory budget is fixed up front). Its split-K partials and its error word live
+// in file-scope device arrays of a fixed size, reserved when the library is loaded; every
+// GPU that loads the library holds them until the process exits.
+#include "../../include/s1.h"
+#include "../../include/s1_ops.h"
+
+namespace s1 {
+int set_error(int code, const char* msg);
+}
+
+namespace {
+static __device__ __align__(256) float g_noalloc_ws[S1_NOALLOC_WS_FLOATS];
+static __device__ __align__(256) int g_noalloc_err[64];
+
+struct NoAllocDev {
+  bool ready = false;
+  float* ws = nullptr;   // device address of g_noalloc_ws on this device
+  int* err = nullptr;    // device address of g_noalloc_err on this device
+  int sms = 0;
+};
+std::mutex g_noalloc_mu;
+NoAllocDev g_noalloc_dev[64];
+
+// Set-up, once per device, with that device current: host code only has a stand-in for the
+// arrays' names, so their device addresses are looked up here.
+int noalloc_setup(int dev, NoAllocDev** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (dev < 0 || dev >= 64) return s1::set_error(S1_ERR_UNSUPPORTED, "gemm_noalloc: device index out of range");
+  NoAllocDev& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_ws);
+    if (e != cudaSuccess) return s1::set_error(S1_ERR_CUDA, "gemm_noalloc: cudaGetSymbolAddress(workspace) failed");
+    d.ws = (float*)p;
+    e = cudaGetSymbolAddress(&p, g_noalloc_err);
+    if (e != cudaSuccess) return s1::set_error(S1_ERR_CUDA, "gemm_noalloc: cudaGetSymbolAddress(error word) failed");
+    d.err = (int*)p;
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return s1::set_error(S1_ERR_CUDA, "gemm_noalloc: device query failed");
+    d.ready = true;
+  }
+  *out = &d;
+  return S1_OK;
+}
+}  // namespace
+
+extern "C" int s1_op_gemm_noalloc(const void* X, const void* W, int32_t M, int32_t N, int32_t K, int32_t epi,
+                                  void* out, int32_t ldo, void* stream) {
+  using namespace s1;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (M < 0 || N <= 0 || K <= 0 || K % 64 || N % 32 || epi < 0 || epi > 3 || !X || !W || !out)
+    return set_error(S1_ERR_INVALID_ARG, "gemm_noalloc: bad sizes, epilogue or NULL pointer");
+  if (!gemm_tc_supported(M, N, K, epi)) return set_error(S1_ERR_UNSUPPORTED, "gemm_noalloc: shape not supported");
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return set_error(S1_ERR_CUDA, "gemm_noalloc: no current device");
+  NoAllocDev* d = nullptr;
+  int rc = noalloc_setup(dev, &d);
+  if (rc) return rc;
+  // Same plan as s1_op_gemm (so the two give identical results); its split-K partials must
+  // fit the fixed array.
+  const size_t plan_cap = gemm_tc_workspace_floats(M, N, K, epi, d->sms);
+  const size_t need = gemm_tc_plan_ws_floats(M, N, K, epi, d->sms, plan_cap);
+  if (need > (size_t)S1_NOALLOC_WS_FLOATS) {
+    char msg[200];
+    snprintf(msg, sizeof(msg), "gemm_noalloc: this shape needs %zu floats of split-K scratch, more than the %d reserved",
+             need, (int)S1_NOALLOC_WS_FLOATS);
+    return set_error(S1_ERR_BUDGET, msg);
+  }
+  if (cudaMemsetAsync(d->err, 0, sizeof(int), st) != cudaSuccess)
+    return set_error(S1_ERR_CUDA, "gemm_noalloc: clearing the error word failed");
+  LaunchCtx lc{st, d->err, d->sms, nullptr};
+  // the plan writes only `need` floats of the array; plan_cap only selects the same plan
+  cudaError_t e = launch_gemm_tc((const bf16*)X, (const bf16*)W, M, N, K, epi, out, ldo, d->ws, plan_cap, lc);
+  if (e != cudaSuccess) return set_error(S1_ERR_CUDA, cudaGetErrorString(e));
+  int h = 0;
+  if (cudaMemcpyAsync(&h, d->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return set_error(S1_ERR_CUDA, "gemm_noalloc: synchronisation failed");
+  if (h) return set_error(S1_ERR_DEVICE_TIMEOUT, "gemm_noalloc: a bounded device wait gave up");
+  return S1_OK;
+}

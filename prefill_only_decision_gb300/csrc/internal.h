@@ -61,6 +61,7 @@ bool gemm_tc_supported(int M, int N, int K, int epi);
 cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out,
                            int ldo, float* splitk_ws, size_t ws_floats, const LaunchCtx& lc);
 size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms);
+size_t gemm_tc_plan_ws_floats(int M, int N, int K, int epi, int num_sms, size_t ws_cap);
 cudaError_t launch_gdn_prep(float* proj, int ld, float* alpha, float* beta, int R, int H, int Dk,
                             int Dv, float eps, cudaStream_t st);
 cudaError_t launch_gdn_scan(const float* proj, int ld, const float* alpha, const float* beta,
