@@ -224,6 +224,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", choices=["gemm", "gdn", "attn"], help="time one kernel entry point alone")
+    ap.add_argument("--path", default="fused", choices=["fused", "two-call"],
+                    help="fused: s1_prefill_decide (one sweep); two-call: s1_prefill_state + s1_decide")
     ap.add_argument("--shape", default="1024,18432,2560,3")
     args = ap.parse_args()
     if args.kernel:
@@ -267,10 +269,17 @@ def main():
     d_probs = torch.zeros(n_opt, dtype=torch.float32, device="cuda")
     d_stats = torch.zeros((n_q, 8), dtype=torch.float32, device="cuda")
 
-    def step():
+    def step_two_call():
         model.prefill_async(st, d_tok.data_ptr(), len(req.tokens), d_emb.data_ptr() if d_emb is not None else 0,
                             0 if d_emb is None else d_emb.shape[0])
         model.decide_async(st, qarr, n_q, d_probs.data_ptr(), d_stats.data_ptr(), 0)
+
+    def step_fused():
+        model.prefill_decide_async(st, d_tok.data_ptr(), len(req.tokens), qarr, n_q, d_probs.data_ptr(),
+                                   d_stats.data_ptr(), 0, d_emb.data_ptr() if d_emb is not None else 0,
+                                   0 if d_emb is None else d_emb.shape[0])
+
+    step = step_fused if args.path == "fused" else step_two_call
 
     def barrier():
         torch.cuda.synchronize()
@@ -282,16 +291,20 @@ def main():
     for _ in range(max(3, args.warmup)):
         step()
     model.sync()
-    # per-phase split (events between prefill and decide), outside the main timed loop
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    # the two-call path with an event between its phases, and one fused step (outside the timed loop)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(2):
+        step_two_call()
     ev[0].record(stream)
     model.prefill_async(st, d_tok.data_ptr(), len(req.tokens), d_emb.data_ptr() if d_emb is not None else 0,
                         0 if d_emb is None else d_emb.shape[0])
     ev[1].record(stream)
     model.decide_async(st, qarr, n_q, d_probs.data_ptr(), d_stats.data_ptr(), 0)
     ev[2].record(stream)
+    step_fused()
+    ev[3].record(stream)
     model.sync()
-    t_prefill, t_decide = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+    t_prefill, t_decide, t_fused = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3])
 
     launches0 = model.counters()["launches"]
     barrier()
@@ -342,9 +355,12 @@ def main():
     t0 = time.perf_counter()
     for _ in range(args.steps):
         a = time.perf_counter()
-        s2 = model.prefill(req.tokens, req.embeds)
-        model.decide(s2, req.questions, want_hidden=False)
-        s2.close()
+        if args.path == "fused":
+            model.prefill_decide(req, want_hidden=False)
+        else:
+            s2 = model.prefill(req.tokens, req.embeds)
+            model.decide(s2, req.questions, want_hidden=False)
+            s2.close()
         lat.append((time.perf_counter() - a) * 1000.0)
     barrier()
     e2e_s = time.perf_counter() - t0
@@ -364,7 +380,10 @@ def main():
                                 "FFN 9216, LoRA r32 merged)" if cfg.name.startswith("4b") else cfg.name,
                        "decisions_per_step": n_q, "parallelism": f"replicas x{ws}",
                        "l2": "inputs larger than L2 (weights read every step)",
-                       "phase_ms": {"prefill": round(t_prefill, 4), "decide": round(t_decide, 4)},
+                       "path": args.path + (" (s1_prefill_decide_async)" if args.path == "fused"
+                                            else " (s1_prefill_async + s1_decide_async)"),
+                       "one_step_ms": {"two_call_prefill": round(t_prefill, 4), "two_call_decide": round(t_decide, 4),
+                                       "fused": round(t_fused, 4)},
                        "class_ms_per_step": phase_split},
             "roofline": roofline, "clocks": clk.summary(), "gpu_launches": int(launches), "e2e": e2e}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

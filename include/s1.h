@@ -166,6 +166,25 @@ int s1_decide_batch(s1_model* m, int32_t n_req, const s1_state* const* states,
                     const s1_question* const* qs, const int32_t* n_q,
                     s1_result* const* out, float* const* last_hidden);
 
+/* ---- one sweep: prefix and questions together ---------------------------------------------
+ * Same results as s1_prefill_state followed by s1_decide, computed in one pass over the
+ * layers: each layer's projections run once over the prefix rows and all suffix rows (the
+ * weights are read once per request), the gated delta-rule state pass runs the prefix and
+ * then the suffixes from the just-written snapshot, and suffix queries read the prefix K/V
+ * the same layer has just cached (System1-Omni RFC #114, section 5: encode the prefix once,
+ * then the isolated suffixes, in bounded batches). state_out (may be NULL) receives the
+ * prefix snapshot for further s1_decide calls. Host pointers; blocking. */
+int s1_prefill_decide(s1_model* m, const int32_t* tokens, int32_t n_tokens, const void* embeds,
+                      int32_t n_embeds, const s1_question* qs, int32_t n_q, s1_result* out,
+                      float* last_hidden, s1_state** state_out);
+/* n_req requests (each a prefix with its questions) in one sweep; last_hidden and states_out
+ * may be NULL, or arrays of n_req entries (entries may be NULL for last_hidden). */
+int s1_prefill_decide_batch(s1_model* m, int32_t n_req, const int32_t* const* tokens,
+                            const int32_t* n_tokens, const void* const* embeds,
+                            const int32_t* n_embeds, const s1_question* const* qs,
+                            const int32_t* n_q, s1_result* const* out, float* const* last_hidden,
+                            s1_state** states_out);
+
 /* ---- stream-ordered variants (device pointers, no host synchronisation) ----------------
  * For callers whose inputs are already in device memory. Host-side metadata
  * (lengths, types, counts) is still passed in host structs; the id arrays they
@@ -179,6 +198,10 @@ int s1_prefill_async(s1_model* m, s1_state* st, const int32_t* d_tokens, int32_t
                      const void* d_embeds, int32_t n_embeds);
 int s1_decide_async(s1_model* m, const s1_state* st, const s1_question* qs_dev, int32_t n_q,
                     float* d_probs, float* d_stats, float* d_last_hidden);
+/* one sweep (as s1_prefill_decide) into a state from s1_state_create; outputs as s1_decide_async */
+int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, int32_t n_tokens,
+                            const void* d_embeds, int32_t n_embeds, const s1_question* qs_dev,
+                            int32_t n_q, float* d_probs, float* d_stats, float* d_last_hidden);
 int s1_sync(s1_model* m);   /* waits for the stream; reports device-side timeouts */
 
 const char* s1_last_error(void);

@@ -82,6 +82,10 @@ def lib():
         "s1_prefill_async": (C.c_int, [vp, vp, vp, i32, vp, i32]),
         "s1_decide_async": (C.c_int, [vp, vp, P(Question), i32, vp, vp, vp]),
         "s1_sync": (C.c_int, [vp]),
+        "s1_prefill_decide": (C.c_int, [vp, P(i32), i32, vp, i32, P(Question), i32, P(Result), P(f32), P(vp)]),
+        "s1_prefill_decide_batch": (C.c_int, [vp, i32, P(P(i32)), P(i32), P(vp), P(i32), P(P(Question)), P(i32),
+                                              P(P(Result)), P(P(f32)), P(vp)]),
+        "s1_prefill_decide_async": (C.c_int, [vp, vp, vp, i32, vp, i32, P(Question), i32, vp, vp, vp]),
         "s1_last_error": (C.c_char_p, []),
         "s1_version": (C.c_char_p, []),
         "s1_op_gemm": (C.c_int, [vp, vp, i32, i32, i32, i32, vp, i32, i32, vp]),
@@ -240,6 +244,68 @@ class Model:
                             "hidden": hids[r][j] if want_hidden else None})
             out.append(lst)
         return out
+
+    def _result_arrays(self, question_lists, want_hidden):
+        keep, qarrs, rarrs, probs, hids = [], [], [], [], []
+        for qs in question_lists:
+            qa, k = make_questions(qs)
+            keep += k
+            qarrs.append(qa)
+            ra = (Result * len(qs))()
+            pl = []
+            for j, q in enumerate(qs):
+                p = np.zeros(len(q.option_ids), dtype=np.float32)
+                pl.append(p)
+                ra[j].probs = p.ctypes.data_as(C.POINTER(C.c_float))
+            probs.append(pl)
+            rarrs.append(ra)
+            hids.append(np.zeros((len(qs), self.shape.d_model), dtype=np.float32) if want_hidden else None)
+        return keep, qarrs, rarrs, probs, hids
+
+    @staticmethod
+    def _unpack(question_lists, rarrs, probs, hids, want_hidden):
+        out = []
+        for r in range(len(question_lists)):
+            lst = []
+            for j in range(len(question_lists[r])):
+                x = rarrs[r][j]
+                lst.append({"probs": probs[r][j], "argmax": x.argmax, "expected_score": x.expected_score,
+                            "yes_prob": x.yes_prob, "answer_confidence": x.answer_confidence,
+                            "confidence": x.confidence, "entropy_confidence": x.entropy_confidence,
+                            "hidden": hids[r][j] if want_hidden else None})
+            out.append(lst)
+        return out
+
+    def prefill_decide(self, request, want_hidden: bool = True, keep_state: bool = False):
+        """One sweep over prefix + questions (s1_prefill_decide). Returns (results, state or None)."""
+        res, sts = self.prefill_decide_batch([request], want_hidden, keep_state)
+        return res[0], (sts[0] if sts else None)
+
+    def prefill_decide_batch(self, requests, want_hidden: bool = True, keep_state: bool = False):
+        n = len(requests)
+        toks = [_i32(r.tokens) for r in requests]
+        embs = [None if r.embeds is None else np.ascontiguousarray(r.embeds, dtype=np.uint16) for r in requests]
+        qls = [r.questions for r in requests]
+        keep, qarrs, rarrs, probs, hids = self._result_arrays(qls, want_hidden)
+        tp = (C.POINTER(C.c_int32) * n)(*[_iptr(t) for t in toks])
+        nt = (C.c_int32 * n)(*[len(t) for t in toks])
+        ep = (C.c_void_p * n)(*[None if e is None else e.ctypes.data for e in embs])
+        ne = (C.c_int32 * n)(*[0 if e is None else e.shape[0] for e in embs])
+        qp = (C.POINTER(Question) * n)(*[C.cast(q, C.POINTER(Question)) for q in qarrs])
+        nq = (C.c_int32 * n)(*[len(q) for q in qls])
+        rp = (C.POINTER(Result) * n)(*[C.cast(r, C.POINTER(Result)) for r in rarrs])
+        hp = (C.POINTER(C.c_float) * n)(*[h.ctypes.data_as(C.POINTER(C.c_float)) for h in hids]) if want_hidden else None
+        so = (C.c_void_p * n)() if keep_state else None
+        check(lib().s1_prefill_decide_batch(self.h, n, tp, nt, ep, ne, qp, nq, rp, hp, so))
+        states = [State(self, C.c_void_p(so[i])) for i in range(n)] if keep_state else None
+        return self._unpack(qls, rarrs, probs, hids, want_hidden), states
+
+    def prefill_decide_async(self, state: "State", d_tokens: int, n_tokens: int, qarr, n_q: int, d_probs: int,
+                             d_stats: int, d_hidden: int = 0, d_embeds: int = 0, n_embeds: int = 0):
+        check(lib().s1_prefill_decide_async(self.h, state.h, C.c_void_p(d_tokens), n_tokens,
+                                            C.c_void_p(d_embeds) if d_embeds else None, n_embeds, qarr, n_q,
+                                            C.c_void_p(d_probs), C.c_void_p(d_stats),
+                                            C.c_void_p(d_hidden) if d_hidden else None))
 
     # -- stream-ordered API (device pointers) -----------------------------------------------
     def state_create(self, capacity_rows: int) -> "State":

@@ -53,104 +53,173 @@ __device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uin
 }
 
 // ---------------------------------------------------------------------------------------
-// chunk_prep: one CTA per (chunk, head), 256 threads.
-// Writes g (within-chunk cumsum of log alpha) over loga, W and Ut (fp32 [R, H, 128]).
+// chunk_prep: one CTA per (chunk, head), 256 threads (8 warps).
+// Writes g (within-chunk cumsum of log alpha) over loga, W and Ut (fp32 [R, H, D]).
+// The unit-lower-triangular system (I + A) X = [diag(beta gamma) K | diag(beta) V] is solved
+// in 16-row blocks: the four 16 x 16 diagonal blocks are inverted by substitution (one lane
+// per column), then X_b = T_bb (RHS_b - sum_{c<b} A_bc X_c) with the block products on the
+// tensor cores (TF32 in, fp32 accumulate).
+template <int D>
+struct PrepSmem {
+  static constexpr int SKp = D + 4;        // K tile   ([s][j]: A / B(n-major) operand pattern)
+  static constexpr int SX = 2 * D + 8;     // X = [W | Ut] ([k][n]: B(k-major) operand pattern)
+  static constexpr int SA = C + 4;         // A        ([t][s]: A operand pattern)
+  static constexpr int ST = 20;            // diagonal-block inverses [16][ST]
+  float K[C * SKp];
+  float X[C * SX];
+  float A[C * SA];
+  float T[4][16 * ST];
+  float g[C];
+  float b[C];
+};
+
 template <int D>
 __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict__ proj, int ld,
                                                          float* __restrict__ loga,
                                                          const float* __restrict__ beta,
                                                          const ChunkDesc* __restrict__ chunks, int H, int Dv,
                                                          float* __restrict__ Wbuf, float* __restrict__ Ubuf) {
-  constexpr int SK = D + 4;       // row stride (floats) of the K tile
-  extern __shared__ float sm[];
-  float* sK = sm;                 // [C][SK]  K rows
-  float* sX = sK + C * SK;        // [C][2*D] rhs -> solution: W (cols 0..127) | Ut (cols 128..255)
-  float* sA = sX + C * 2 * D;     // [C][C+1]
-  float* sg = sA + C * (C + 1);   // [C]
-  float* sb = sg + C;             // [C]
+  using SM = PrepSmem<D>;
+  constexpr int SKp = SM::SKp, SX = SM::SX, SA = SM::SA, ST = SM::ST;
+  constexpr int NX = 2 * D;                 // columns of X
+  extern __shared__ __align__(16) uint8_t smraw[];
+  SM& s = *reinterpret_cast<SM*>(smraw);
   const ChunkDesc cd = chunks[blockIdx.x];
   const int h = blockIdx.y, n = cd.len, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   const int HDk = H * D;
-  // load K (normalised), V, g, beta
+  // ---- load K (normalised) and V (into the Ut half of X), g = cumsum(log alpha), beta
   for (int i = tid; i < C * (D / 4); i += 256) {
     const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-    float4 kv = make_float4(0, 0, 0, 0), vv = make_float4(0, 0, 0, 0);
-    if (r < n) {
-      const float* pr = proj + (size_t)(cd.row0 + r) * ld;
-      kv = *reinterpret_cast<const float4*>(pr + HDk + h * D + c4);
-      vv = *reinterpret_cast<const float4*>(pr + 2 * HDk + h * Dv + c4);
-    }
-    *reinterpret_cast<float4*>(sK + r * SK + c4) = kv;
-    *reinterpret_cast<float4*>(sX + r * 2 * D + D + c4) = vv;
+    const bool ok = r < n;
+    const float* pr = proj + (size_t)(cd.row0 + (ok ? r : 0)) * ld;
+    cp16(&s.K[r * SKp + c4], pr + HDk + h * D + c4, ok);
+    cp16(&s.X[r * SX + D + c4], pr + 2 * HDk + h * Dv + c4, ok);
   }
+  cp_commit();
   if (tid < 32) {
-    // inclusive cumsum of log alpha over the chunk (2 values per lane)
-    float a0 = (2 * tid < n) ? loga[(size_t)(cd.row0 + 2 * tid) * H + h] : 0.f;
-    float a1 = (2 * tid + 1 < n) ? loga[(size_t)(cd.row0 + 2 * tid + 1) * H + h] : 0.f;
-    float s = a0 + a1;
+    const float a0 = (2 * tid < n) ? loga[(size_t)(cd.row0 + 2 * tid) * H + h] : 0.f;
+    const float a1 = (2 * tid + 1 < n) ? loga[(size_t)(cd.row0 + 2 * tid + 1) * H + h] : 0.f;
+    float v = a0 + a1;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(0xffffffffu, s, o);
-      if (tid >= o) s += t;
+      const float t = __shfl_up_sync(0xffffffffu, v, o);
+      if (tid >= o) v += t;
     }
-    const float excl = s - (a0 + a1);
-    sg[2 * tid] = excl + a0;
-    sg[2 * tid + 1] = excl + a0 + a1;
+    const float excl = v - (a0 + a1);
+    s.g[2 * tid] = excl + a0;
+    s.g[2 * tid + 1] = excl + a0 + a1;
   } else if (tid < 32 + C) {
     const int r = tid - 32;
-    sb[r] = (r < n) ? beta[(size_t)(cd.row0 + r) * H + h] : 0.f;
+    s.b[r] = (r < n) ? beta[(size_t)(cd.row0 + r) * H + h] : 0.f;
   }
+  cp_wait<0>();
   __syncthreads();
-  // A = strict_lower(beta_t exp(g_t - g_s) k_t.k_s): each thread a 4x4 block of the 64x64
+  // ---- A = strict_lower(beta_t exp(g_t - g_s) k_t.k_s): warp -> m-tile (warp & 3), 4 n-tiles
   {
-    const int tr = (tid >> 4) * 4, tc = (tid & 15) * 4;
+    const int r0 = (warp & 3) * 16, c0 = (warp >> 2) * 32;
     float acc[4][4] = {};
-    for (int j = 0; j < D; j += 4) {
-      float4 a[4], b[4];
+#pragma unroll 4
+    for (int k = 0; k < D; k += 8) {
+      const uint32_t a0 = tf32(s.K[(r0 + gq) * SKp + k + tq]), a1 = tf32(s.K[(r0 + gq + 8) * SKp + k + tq]);
+      const uint32_t a2 = tf32(s.K[(r0 + gq) * SKp + k + tq + 4]), a3 = tf32(s.K[(r0 + gq + 8) * SKp + k + tq + 4]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = *reinterpret_cast<const float4*>(sK + (tr + i) * SK + j);
-        b[i] = *reinterpret_cast<const float4*>(sK + (tc + i) * SK + j);
+      for (int nt = 0; nt < 4; ++nt) {
+        const int key = c0 + nt * 8 + gq;
+        mma_tf32(acc[nt], a0, a1, a2, a3, tf32(s.K[key * SKp + k + tq]), tf32(s.K[key * SKp + k + tq + 4]));
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          acc[i][k] += a[i].x * b[k].x + a[i].y * b[k].y + a[i].z * b[k].z + a[i].w * b[k].w;
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int t = tr + i, s = tc + k;
-        sA[t * (C + 1) + s] = (s < t && t < n) ? sb[t] * __expf(sg[t] - sg[s]) * acc[i][k] : 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const int t = r0 + gq + (e >> 1) * 8, sc = c0 + nt * 8 + 2 * tq + (e & 1);
+        s.A[t * SA + sc] = (sc < t && t < n) ? s.b[t] * __expf(s.g[t] - s.g[sc]) * acc[nt][e] : 0.f;
       }
   }
-  // rhs: W rows = beta_t gamma_t k_t ; Ut rows = beta_t v_t
+  // ---- right-hand sides: W half = beta_t gamma_t k_t, Ut half = beta_t v_t
   for (int i = tid; i < C * D; i += 256) {
     const int r = i / D, c = i % D;
-    sX[r * 2 * D + c] = sb[r] * __expf(sg[r]) * sK[r * SK + c];
-    sX[r * 2 * D + D + c] *= sb[r];
+    s.X[r * SX + c] = s.b[r] * __expf(s.g[r]) * s.K[r * SKp + c];
+    s.X[r * SX + D + c] *= s.b[r];
   }
   __syncthreads();
-  // forward substitution, one column per thread: X_t -= sum_{s<t} A_ts X_s
-  {
-    const int c = tid;   // 0 .. 2D-1
-    for (int t = 1; t < n && c < 2 * D; ++t) {
-      float acc = sX[t * 2 * D + c];
-      const float* Ar = sA + t * (C + 1);
-      for (int s = 0; s < t; ++s) acc = fmaf(-Ar[s], sX[s * 2 * D + c], acc);
-      sX[t * 2 * D + c] = acc;
+  // ---- inverses of the diagonal blocks: warp b < 4, lane j < 16 owns column j of T_bb
+  if (warp < 4 && lane < 16) {
+    float* T = s.T[warp];
+    const float* Ab = s.A + (warp * 16) * SA + warp * 16;
+    const int j = lane;
+    for (int t = 0; t < 16; ++t) {
+      float v = (t == j) ? 1.f : 0.f;
+      for (int q = j; q < t; ++q) v = fmaf(-Ab[t * SA + q], T[q * ST + j], v);
+      T[t * ST + j] = v;
     }
   }
   __syncthreads();
+  // ---- block forward substitution over the 4 row blocks; warp -> 4 of the 2D/8 n-tiles
+  constexpr int NT = NX / 8 / 8;           // n-tiles per warp (D=128: 4, D=64: 2)
+  for (int bb = 0; bb < 4; ++bb) {
+    const int r0 = bb * 16;
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int c = (warp * NT + nt) * 8 + 2 * tq;
+      acc[nt][0] = s.X[(r0 + gq) * SX + c];
+      acc[nt][1] = s.X[(r0 + gq) * SX + c + 1];
+      acc[nt][2] = s.X[(r0 + gq + 8) * SX + c];
+      acc[nt][3] = s.X[(r0 + gq + 8) * SX + c + 1];
+    }
+    // R = RHS_b - A[b, 0:16b] X[0:16b]
+    for (int k = 0; k < r0; k += 8) {
+      const uint32_t a0 = tf32(-s.A[(r0 + gq) * SA + k + tq]), a1 = tf32(-s.A[(r0 + gq + 8) * SA + k + tq]);
+      const uint32_t a2 = tf32(-s.A[(r0 + gq) * SA + k + tq + 4]), a3 = tf32(-s.A[(r0 + gq + 8) * SA + k + tq + 4]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = (warp * NT + nt) * 8 + gq;
+        mma_tf32(acc[nt], a0, a1, a2, a3, tf32(s.X[(k + tq) * SX + c]), tf32(s.X[(k + tq + 4) * SX + c]));
+      }
+    }
+    __syncthreads();   // all warps read the solved rows before block b is overwritten
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int c = (warp * NT + nt) * 8 + 2 * tq;
+      s.X[(r0 + gq) * SX + c] = acc[nt][0];
+      s.X[(r0 + gq) * SX + c + 1] = acc[nt][1];
+      s.X[(r0 + gq + 8) * SX + c] = acc[nt][2];
+      s.X[(r0 + gq + 8) * SX + c + 1] = acc[nt][3];
+    }
+    __syncthreads();
+    // X_b = T_bb R_b
+    float xb[NT][4] = {};
+    const float* T = s.T[bb];
+#pragma unroll
+    for (int k = 0; k < 16; k += 8) {
+      const uint32_t a0 = tf32(T[gq * ST + k + tq]), a1 = tf32(T[(gq + 8) * ST + k + tq]);
+      const uint32_t a2 = tf32(T[gq * ST + k + tq + 4]), a3 = tf32(T[(gq + 8) * ST + k + tq + 4]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int c = (warp * NT + nt) * 8 + gq;
+        mma_tf32(xb[nt], a0, a1, a2, a3, tf32(s.X[(r0 + k + tq) * SX + c]), tf32(s.X[(r0 + k + tq + 4) * SX + c]));
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int c = (warp * NT + nt) * 8 + 2 * tq;
+      s.X[(r0 + gq) * SX + c] = xb[nt][0];
+      s.X[(r0 + gq) * SX + c + 1] = xb[nt][1];
+      s.X[(r0 + gq + 8) * SX + c] = xb[nt][2];
+      s.X[(r0 + gq + 8) * SX + c + 1] = xb[nt][3];
+    }
+    __syncthreads();
+  }
   for (int i = tid; i < n * (D / 4); i += 256) {
     const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
     const size_t o = ((size_t)(cd.row0 + r) * H + h) * D + c4;
-    *reinterpret_cast<float4*>(Wbuf + o) = *reinterpret_cast<const float4*>(sX + r * 2 * D + c4);
-    *reinterpret_cast<float4*>(Ubuf + o) = *reinterpret_cast<const float4*>(sX + r * 2 * D + D + c4);
+    *reinterpret_cast<float4*>(Wbuf + o) = *reinterpret_cast<const float4*>(&s.X[r * SX + c4]);
+    *reinterpret_cast<float4*>(Ubuf + o) = *reinterpret_cast<const float4*>(&s.X[r * SX + D + c4]);
   }
-  if (tid < n) loga[(size_t)(cd.row0 + tid) * H + h] = sg[tid];
+  if (tid < n) loga[(size_t)(cd.row0 + tid) * H + h] = s.g[tid];
 }
 
 // ---------------------------------------------------------------------------------------
@@ -458,9 +527,9 @@ template <int D>
 static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const float* beta, bf16* out,
                                     const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                     const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
-                                    float* Schunk, cudaStream_t st) {
+                                    float* Schunk, int n_first, cudaStream_t st) {
   static bool attr = false;
-  const size_t sp = (size_t)(gc::C * (D + 4) + gc::C * 2 * D + gc::C * (gc::C + 1) + 2 * gc::C) * 4;
+  const size_t sp = sizeof(gc::PrepSmem<D>);
   const size_t ss = sizeof(gc::StateSmem<D>);
   const size_t so = sizeof(gc::OutSmem<D>);
   if (!attr) {
@@ -473,8 +542,13 @@ static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const floa
     attr = true;
   }
   gc::chunk_prep_kernel<D><<<dim3(n_chunks, H), 256, sp, st>>>(proj, ld, loga, beta, d_chunks, H, D, Wbuf, Ubuf);
-  gc::chunk_state_kernel<D><<<dim3(n_seq, H, D / gc::BV), 128, ss, st>>>(proj, ld, loga, d_seq, d_chunks, d_ctx,
+  // sequences [0, n_first) run before the rest (the rest continue from their states)
+  const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
+  gc::chunk_state_kernel<D><<<dim3(split, H, D / gc::BV), 128, ss, st>>>(proj, ld, loga, d_seq, d_chunks, d_ctx,
                                                                          layer_g, H, Wbuf, Ubuf, Schunk);
+  if (split < n_seq)
+    gc::chunk_state_kernel<D><<<dim3(n_seq - split, H, D / gc::BV), 128, ss, st>>>(
+        proj, ld, loga, d_seq + split, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk);
   gc::chunk_out_kernel<D><<<dim3(n_chunks, H), 256, so, st>>>(proj, ld, loga, d_chunks, H, Ubuf, Schunk, out);
   return cudaGetLastError();
 }
@@ -482,16 +556,16 @@ static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const floa
 cudaError_t launch_gdn_chunked(float* proj, int ld, float* loga, const float* beta, bf16* out,
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
-                               float* Schunk, cudaStream_t st, long* launches) {
+                               float* Schunk, int n_first, cudaStream_t st, long* launches) {
   if (n_seq <= 0 || n_chunks <= 0) return cudaSuccess;
   if (!gdn_chunked_supported(H, Dk, Dv, ld)) return cudaErrorNotSupported;
   if (n_seq > 65535 || n_chunks > 2147483647 / 2) return cudaErrorInvalidValue;
   cudaError_t e = (Dk == 128)
                       ? launch_chunked_d<128>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
-                                              layer_g, H, Wbuf, Ubuf, Schunk, st)
+                                              layer_g, H, Wbuf, Ubuf, Schunk, n_first, st)
                       : launch_chunked_d<64>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
-                                             layer_g, H, Wbuf, Ubuf, Schunk, st);
-  if (launches) *launches += 3;
+                                             layer_g, H, Wbuf, Ubuf, Schunk, n_first, st);
+  if (launches) *launches += (n_first > 0 && n_first < n_seq) ? 4 : 3;
   return e;
 }
 

@@ -105,7 +105,7 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
     float* Sc = (float*)t.get((size_t)(nch + 1) * per * 4);
     if (!W || !U || !Sc) return op_fail(S1_ERR_OOM, "gdn: temporaries");
     OCK(launch_gdn_chunked(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
-                           st, nullptr));
+                           0, st, nullptr));
   } else {
     OCK(launch_gdn_scan(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dctx, 0, H, dk, dv, st));
   }

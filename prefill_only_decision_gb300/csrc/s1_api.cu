@@ -83,6 +83,7 @@ struct Layer {
 
 struct Scratch {
   int rows = 0;
+  int opt_cap = 0;           // option ids the metadata / output blocks hold
   float* x = nullptr;
   bf16* xn = nullptr;
   float* proj = nullptr;
@@ -195,8 +196,9 @@ void free_scratch(Scratch& sc) {
   sc = Scratch();
 }
 
-int ensure_scratch(s1_model* m, int rows) {
-  if (rows <= m->sc.rows) return S1_OK;
+int ensure_scratch(s1_model* m, int rows, int n_opts = 0) {
+  if (rows <= m->sc.rows && n_opts <= m->sc.opt_cap) return S1_OK;
+  rows = std::max(rows, m->sc.rows);
   int want = std::max(rows, 256);
   want = std::min(std::max(want, m->sc.rows * 2), m->sh.max_rows);
   want = std::max(want, rows);
@@ -223,7 +225,9 @@ int ensure_scratch(s1_model* m, int rows) {
   sc.beta = (float*)take(R * H * 4);
   sc.gw = (float*)take(R * H * (size_t)std::max(s.la_dk, 1) * 4);
   sc.gu = (float*)take(R * H * (size_t)std::max(s.la_dv, 1) * 4);
-  const int max_seq = want, max_ctx = want, max_q = want, max_opt = 64 * want;
+  const int max_seq = want, max_ctx = want, max_q = want;
+  const int max_opt = std::max(64 * want, std::max(n_opts, m->sc.opt_cap));
+  sc.opt_cap = max_opt;
   sc.meta_bytes = meta_bytes_for(want, max_seq, max_ctx, max_q, max_opt);
   sc.meta = (int*)take(sc.meta_bytes);
   sc.ws_floats = std::max<size_t>(gemm_tc_workspace_floats(want, std::max(m->n_proj, 2 * s.ffn), s.ffn, EPI_RESADD, m->num_sms), 1);
@@ -262,6 +266,7 @@ struct Meta {
   std::vector<ChunkDesc> chunks;
   std::vector<int> q_row, q_type, opt_off, opt_ids;
   int max_len = 0, max_opts = 0;
+  int n_first = 0;   // fused sweep: the first n_first sequences (prefixes) scan before the rest
   // device views
   int* d_row_src = nullptr;
   int* d_row_seq = nullptr;
@@ -380,11 +385,16 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
             if (!m->schunk) return fail(S1_ERR_OOM, "chunk-state buffer (%zu chunks) allocation failed", cap);
           }
           CK(launch_gdn_chunked(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
-                                mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, st, &m->launches));
+                                mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first, st,
+                                &m->launches));
         } else {
-          CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_ctxs,
+          const int split = (mt.n_first > 0 && mt.n_first < nseq) ? mt.n_first : nseq;
+          CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, split, mt.d_ctxs,
                              L.ord, H, s.la_dk, s.la_dv, st));
-          m->launches += 1;
+          if (split < nseq)
+            CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs + split, nseq - split,
+                               mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, st));
+          m->launches += split < nseq ? 2 : 1;
         }
       }
     } else {
@@ -501,8 +511,7 @@ int build_decide_meta(s1_model* m, int n_req, const s1_state* const* states, con
     }
   }
   if (NQ == 0) return fail(S1_ERR_INVALID_ARG, "no questions");
-  if (NO > 64 * m->sh.max_rows) return fail(S1_ERR_BUDGET, "too many option ids");
-  int rc = ensure_scratch(m, R);
+  int rc = ensure_scratch(m, R, NO);
   if (rc) return rc;
   mt.row_src.reserve(R);
   mt.row_seq.reserve(R);
@@ -933,33 +942,18 @@ static int decide_impl(s1_model* m, int n_req, const s1_state* const* states, co
   return run_forward(m, mt, nullptr, d_probs, d_stats, d_hidden);
 }
 
-int s1_decide_batch(s1_model* m, int32_t n_req, const s1_state* const* states, const s1_question* const* qs,
-                    const int32_t* n_q, s1_result* const* out, float* const* last_hidden) {
-  if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
-  if (n_req < 1 || !states || !qs || !n_q || !out) return fail(S1_ERR_INVALID_ARG, "bad batch arguments");
-  for (int r = 0; r < n_req; ++r)
-    if (n_q[r] > 0 && !out[r]) return fail(S1_ERR_INVALID_ARG, "request %d: NULL results", r);
-  Meta mt;
-  int NQ = 0, NO = 0;
-  // outputs land in the scratch output block, then one copy back
-  int R = 0;
-  int rc = build_decide_meta(m, n_req, states, qs, n_q, true, mt, &R, &NQ, &NO);
-  if (rc) return rc;
+// Copies the readout outputs (probs | stats | hidden in the scratch output block) back into
+// the caller's result structs. Blocking.
+static int fetch_results(s1_model* m, int n_req, const s1_question* const* qs, const int32_t* n_q, int NQ, int NO,
+                         bool want_hidden, s1_result* const* out, float* const* last_hidden) {
   float* probs = m->sc.out;
   float* stats = probs + align_up(NO, 64);
   float* hidden = stats + align_up((size_t)NQ * S1_STAT_COUNT, 64);
-  bool want_hidden = false;
-  if (last_hidden)
-    for (int r = 0; r < n_req; ++r) want_hidden |= (last_hidden[r] != nullptr);
-  rc = upload_meta(m, mt);
-  if (rc) return rc;
-  rc = run_forward(m, mt, nullptr, probs, stats, want_hidden ? hidden : nullptr);
-  if (rc) return rc;
   const size_t nfl = (size_t)(hidden - probs) + (want_hidden ? (size_t)NQ * m->sh.d_model : 0);
   std::vector<float> h(nfl);
   CK(cudaMemcpyAsync(h.data(), probs, nfl * 4, cudaMemcpyDeviceToHost, m->stream));
   m->d2h_bytes += (long long)(nfl * 4);
-  rc = s1_sync(m);
+  int rc = s1_sync(m);
   if (rc) return rc;
   const float* hp = h.data();
   const float* hs = hp + (stats - probs);
@@ -984,6 +978,34 @@ int s1_decide_batch(s1_model* m, int32_t n_req, const s1_state* const* states, c
   return S1_OK;
 }
 
+static void output_slots(s1_model* m, int NQ, int NO, float** probs, float** stats, float** hidden) {
+  *probs = m->sc.out;
+  *stats = *probs + align_up(NO, 64);
+  *hidden = *stats + align_up((size_t)NQ * S1_STAT_COUNT, 64);
+}
+
+int s1_decide_batch(s1_model* m, int32_t n_req, const s1_state* const* states, const s1_question* const* qs,
+                    const int32_t* n_q, s1_result* const* out, float* const* last_hidden) {
+  if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  if (n_req < 1 || !states || !qs || !n_q || !out) return fail(S1_ERR_INVALID_ARG, "bad batch arguments");
+  for (int r = 0; r < n_req; ++r)
+    if (n_q[r] > 0 && !out[r]) return fail(S1_ERR_INVALID_ARG, "request %d: NULL results", r);
+  Meta mt;
+  int NQ = 0, NO = 0, R = 0;
+  int rc = build_decide_meta(m, n_req, states, qs, n_q, true, mt, &R, &NQ, &NO);
+  if (rc) return rc;
+  float *probs, *stats, *hidden;
+  output_slots(m, NQ, NO, &probs, &stats, &hidden);
+  bool want_hidden = false;
+  if (last_hidden)
+    for (int r = 0; r < n_req; ++r) want_hidden |= (last_hidden[r] != nullptr);
+  rc = upload_meta(m, mt);
+  if (rc) return rc;
+  rc = run_forward(m, mt, nullptr, probs, stats, want_hidden ? hidden : nullptr);
+  if (rc) return rc;
+  return fetch_results(m, n_req, qs, n_q, NQ, NO, want_hidden, out, last_hidden);
+}
+
 int s1_decide(s1_model* m, const s1_state* st, const s1_question* qs, int32_t n_q, s1_result* out,
               float* last_hidden) {
   return s1_decide_batch(m, 1, &st, &qs, &n_q, &out, &last_hidden);
@@ -996,6 +1018,186 @@ int s1_decide_async(s1_model* m, const s1_state* st, const s1_question* qs_dev, 
   Meta mt;
   int NQ = 0, NO = 0;
   return decide_impl(m, 1, &st, &qs_dev, &n_q, true, d_probs, d_stats, d_last_hidden, mt, &NQ, &NO);
+}
+
+// -- fused sweep: prefixes and their questions in one pass over the layers ---------------
+// Rows: every prefix, then every question suffix. Each layer's projections run once over all
+// rows (the weights are streamed once per request instead of once per call); the gated
+// delta-rule state pass runs the prefixes first and then the suffixes, which continue from
+// the snapshot written moments before in the same layer; suffix queries read the prefix K/V
+// that the same layer's RoPE step has just cached.
+static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, const int32_t* n_tokens,
+                      const void* const* embeds, const int32_t* n_embeds, s1_state* const* states,
+                      const s1_question* const* qs, const int32_t* n_q, bool device_ptrs, float* d_probs,
+                      float* d_stats, float* d_hidden, int* NQ_out, int* NO_out) {
+  int Rp = 0, Rs = 0, NQ = 0, NO = 0, NE = 0;
+  for (int r = 0; r < n_req; ++r) {
+    const int P = n_tokens[r] + n_embeds[r];
+    if (n_tokens[r] < 0 || n_embeds[r] < 0 || P < 1) return fail(S1_ERR_INVALID_ARG, "request %d: empty prefix", r);
+    if (!valid_state(m, states[r])) return fail(S1_ERR_INVALID_HANDLE, "request %d: invalid state", r);
+    if (P > states[r]->cap) return fail(S1_ERR_BUDGET, "request %d: prefix %d rows > state capacity %d", r, P, states[r]->cap);
+    if (n_q[r] < 0 || (n_q[r] > 0 && !qs[r])) return fail(S1_ERR_INVALID_ARG, "request %d: bad question array", r);
+    if (n_tokens[r] > 0 && (!tokens || !tokens[r])) return fail(S1_ERR_INVALID_ARG, "request %d: NULL tokens", r);
+    if (n_embeds[r] > 0 && (!embeds || !embeds[r])) return fail(S1_ERR_INVALID_ARG, "request %d: NULL embeds", r);
+    if (!device_ptrs && n_tokens[r] > 0) {
+      int rc = validate_ids(tokens[r], n_tokens[r], m->sh.vocab, "token");
+      if (rc) return rc;
+    }
+    Rp += P;
+    NE += n_embeds[r];
+    for (int j = 0; j < n_q[r]; ++j) {
+      int rc = validate_question(m, qs[r][j], j, !device_ptrs);
+      if (rc) return rc;
+      if (P + qs[r][j].n_suffix > m->max_pos) return fail(S1_ERR_BUDGET, "position budget exceeded");
+      Rs += qs[r][j].n_suffix;
+      NO += qs[r][j].n_options;
+      NQ += 1;
+    }
+    if (Rp + Rs > m->sh.max_rows) return fail(S1_ERR_BUDGET, "%d rows exceed max_rows %d", Rp + Rs, m->sh.max_rows);
+  }
+  if (NQ == 0) return fail(S1_ERR_INVALID_ARG, "no questions");
+  int rc = ensure_scratch(m, Rp + Rs, NO);
+  if (rc) return rc;
+  Meta mt;
+  mt.n_first = n_req;
+  int row = 0, erow = 0;
+  for (int r = 0; r < n_req; ++r) {
+    const int P = n_tokens[r] + n_embeds[r];
+    mt.ctxs.push_back(CtxDesc{states[r]->S, states[r]->KV, P, states[r]->cap});
+    mt.seqs.push_back(SeqDesc{row, P, 0, -1, r, 0});
+    mt.max_len = std::max(mt.max_len, P);
+    for (int i = 0; i < P; ++i) mt.row_seq.push_back(r);
+    for (int i = 0; i < n_embeds[r]; ++i) mt.row_src.push_back(-1 - (erow + i));
+    for (int i = 0; i < n_tokens[r]; ++i) mt.row_src.push_back(device_ptrs ? 0 : tokens[r][i]);
+    erow += n_embeds[r];
+    row += P;
+  }
+  mt.opt_off.push_back(0);
+  for (int r = 0; r < n_req; ++r)
+    for (int j = 0; j < n_q[r]; ++j) {
+      const s1_question& q = qs[r][j];
+      const int sidx = (int)mt.seqs.size();
+      mt.seqs.push_back(SeqDesc{row, q.n_suffix, n_tokens[r] + n_embeds[r], r, -1, 0});
+      mt.max_len = std::max(mt.max_len, q.n_suffix);
+      for (int i = 0; i < q.n_suffix; ++i) {
+        mt.row_src.push_back(device_ptrs ? 0 : q.suffix[i]);
+        mt.row_seq.push_back(sidx);
+      }
+      mt.q_row.push_back(row + q.n_suffix - 1);
+      mt.q_type.push_back(q.type);
+      for (int o = 0; o < q.n_options; ++o) mt.opt_ids.push_back(device_ptrs ? 0 : q.option_ids[o]);
+      mt.opt_off.push_back(mt.opt_off.back() + q.n_options);
+      mt.max_opts = std::max(mt.max_opts, q.n_options);
+      row += q.n_suffix;
+    }
+  rc = upload_meta(m, mt);
+  if (rc) return rc;
+  if (device_ptrs) {
+    int rr = 0, opt = 0;
+    for (int r = 0; r < n_req; ++r) {
+      rr += n_embeds[r];
+      if (n_tokens[r] > 0)
+        CK(cudaMemcpyAsync(mt.d_row_src + rr, tokens[r], n_tokens[r] * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+      rr += n_tokens[r];
+    }
+    for (int r = 0; r < n_req; ++r)
+      for (int j = 0; j < n_q[r]; ++j) {
+        const s1_question& q = qs[r][j];
+        CK(cudaMemcpyAsync(mt.d_row_src + rr, q.suffix, q.n_suffix * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+        CK(cudaMemcpyAsync(mt.d_opt_ids + opt, q.option_ids, q.n_options * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+        rr += q.n_suffix;
+        opt += q.n_options;
+      }
+  }
+  if (NE > 0) {
+    const size_t rowb = (size_t)m->sh.d_model * 2;
+    size_t eoff = 0;
+    for (int r = 0; r < n_req; ++r) {
+      if (n_embeds[r] == 0) continue;
+      CK(cudaMemcpyAsync((char*)m->sc.xn + eoff, embeds[r], n_embeds[r] * rowb,
+                         device_ptrs ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, m->stream));
+      if (!device_ptrs) m->h2d_bytes += (long long)(n_embeds[r] * rowb);
+      eoff += n_embeds[r] * rowb;
+    }
+  }
+  rc = run_forward(m, mt, m->sc.xn, d_probs, d_stats, d_hidden);
+  if (rc) return rc;
+  for (int r = 0; r < n_req; ++r) states[r]->P = n_tokens[r] + n_embeds[r];
+  *NQ_out = NQ;
+  *NO_out = NO;
+  return S1_OK;
+}
+
+int s1_prefill_decide_batch(s1_model* m, int32_t n_req, const int32_t* const* tokens, const int32_t* n_tokens,
+                            const void* const* embeds, const int32_t* n_embeds, const s1_question* const* qs,
+                            const int32_t* n_q, s1_result* const* out, float* const* last_hidden,
+                            s1_state** states_out) {
+  if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  if (n_req < 1 || !n_tokens || !qs || !n_q || !out) return fail(S1_ERR_INVALID_ARG, "bad batch arguments");
+  for (int r = 0; r < n_req; ++r)
+    if (n_q[r] > 0 && !out[r]) return fail(S1_ERR_INVALID_ARG, "request %d: NULL results", r);
+  std::vector<int32_t> ne(n_req, 0);
+  if (n_embeds) ne.assign(n_embeds, n_embeds + n_req);
+  std::vector<s1_state*> sts(n_req, nullptr);
+  auto cleanup = [&](int rc) {
+    for (s1_state* x : sts) s1_state_destroy(x);
+    return rc;
+  };
+  for (int r = 0; r < n_req; ++r) {
+    const int P = n_tokens[r] + ne[r];
+    if (P < 1) return cleanup(fail(S1_ERR_INVALID_ARG, "request %d: empty prefix", r));
+    if (P > m->sh.max_rows) return cleanup(fail(S1_ERR_BUDGET, "request %d: prefix %d > max_rows", r, P));
+    int rc = new_state(m, P, &sts[r]);
+    if (rc) return cleanup(rc);
+  }
+  bool want_hidden = false;
+  if (last_hidden)
+    for (int r = 0; r < n_req; ++r) want_hidden |= (last_hidden[r] != nullptr);
+  int NQ = 0, NO = 0;
+  // output slots are sized after validation: count first
+  int nq_tot = 0, no_tot = 0;
+  for (int r = 0; r < n_req; ++r)
+    for (int j = 0; j < n_q[r]; ++j) { nq_tot++; no_tot += std::max(0, qs[r][j].n_options); }
+  int rc = S1_OK;
+  {
+    int rows = 0;
+    for (int r = 0; r < n_req; ++r) {
+      rows += n_tokens[r] + ne[r];
+      for (int j = 0; j < n_q[r]; ++j) rows += std::max(0, qs[r][j].n_suffix);
+    }
+    if (rows > m->sh.max_rows) return cleanup(fail(S1_ERR_BUDGET, "%d rows exceed max_rows %d", rows, m->sh.max_rows));
+    rc = ensure_scratch(m, std::max(rows, 1), no_tot);
+    if (rc) return cleanup(rc);
+  }
+  float *probs, *stats, *hidden;
+  output_slots(m, nq_tot, no_tot, &probs, &stats, &hidden);
+  rc = fused_impl(m, n_req, tokens, n_tokens, embeds, ne.data(), sts.data(), qs, n_q, false, probs, stats,
+                  want_hidden ? hidden : nullptr, &NQ, &NO);
+  if (!rc) rc = fetch_results(m, n_req, qs, n_q, NQ, NO, want_hidden, out, last_hidden);
+  if (rc) return cleanup(rc);
+  for (int r = 0; r < n_req; ++r) {
+    if (states_out) states_out[r] = sts[r];
+    else s1_state_destroy(sts[r]);
+  }
+  return S1_OK;
+}
+
+int s1_prefill_decide(s1_model* m, const int32_t* tokens, int32_t n_tokens, const void* embeds, int32_t n_embeds,
+                      const s1_question* qs, int32_t n_q, s1_result* out, float* last_hidden, s1_state** state_out) {
+  const void* e[1] = {embeds};
+  return s1_prefill_decide_batch(m, 1, &tokens, &n_tokens, e, &n_embeds, &qs, &n_q, &out, &last_hidden, state_out);
+}
+
+int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, int32_t n_tokens,
+                            const void* d_embeds, int32_t n_embeds, const s1_question* qs_dev, int32_t n_q,
+                            float* d_probs, float* d_stats, float* d_last_hidden) {
+  if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  if (!valid_state(m, st)) return fail(S1_ERR_INVALID_HANDLE, "invalid state");
+  if (!d_probs || !d_stats) return fail(S1_ERR_INVALID_ARG, "NULL output");
+  const void* e[1] = {d_embeds};
+  int NQ = 0, NO = 0;
+  return fused_impl(m, 1, &d_tokens, &n_tokens, e, &n_embeds, &st, &qs_dev, &n_q, true, d_probs, d_stats,
+                    d_last_hidden, &NQ, &NO);
 }
 
 // -- instrumentation ---------------------------------------------------------------------

@@ -269,3 +269,44 @@ def test_27b_sampled_requests(B):
     o = om.Oracle(W, np.float32)
     ref = o.decide(reqs[i], branched=True)
     compare(res[i], ref, reqs[i].questions, f"27b req {i} P={len(reqs[i].tokens)}")
+
+
+# -- one sweep over prefix + questions ---------------------------------------------------------
+def test_tiny_fused_vs_oracle_and_two_call(tiny, tiny_weights, tiny_requests):
+    r = tiny_requests[0]
+    ref = om.Oracle(tiny_weights, np.float32).decide(r, branched=False)
+    fused, st = tiny.prefill_decide(r, keep_state=True)
+    compare(fused, ref, r.questions, "tiny fused")
+    # the returned snapshot serves further decisions, and agrees with the two-call path
+    again = tiny.decide(st, r.questions)
+    two = tiny.decide(tiny.prefill(r.tokens), r.questions)
+    for a, b, c in zip(fused, again, two):
+        assert np.abs(a["probs"] - b["probs"]).max() < 2e-3
+        assert np.abs(b["probs"] - c["probs"]).max() < 2e-3   # prefix GEMMs ran at a different M
+
+
+def test_tiny_fused_edge_cases(tiny, tiny_weights):
+    o = om.Oracle(tiny_weights, np.float32)
+    g = np.random.default_rng(8)
+    qs = [synth.random_question(g, 4096, configs.CHOICE, 1, 1), synth.random_question(g, 4096, configs.NOUL, 65, 2),
+          synth.random_question(g, 4096, configs.SCORE, 130, 5)]
+    for P in (1, 64, 129):
+        toks = g.integers(16, 4096, size=P).astype(np.int32)
+        req = synth.Request(toks, None, qs)
+        gpu, _ = tiny.prefill_decide(req)
+        _, caches, PP = o.prefill(toks)
+        compare(gpu, o.decide_branched(caches, PP, qs), qs, f"fused edge P={P}")
+
+
+def test_small_fused_batch_vs_oracle(B):
+    cfg = configs.SMALL
+    W = synth.make_weights(cfg)
+    reqs = synth.make_requests(cfg)
+    m = B.Model(W)
+    try:
+        gpu, _ = m.prefill_decide_batch(reqs)
+    finally:
+        m.close()
+    o = om.Oracle(W, np.float32)
+    for i in (0, 9, 15):
+        compare(gpu[i], o.decide(reqs[i], branched=True), reqs[i].questions, f"small fused {i}")
