@@ -18,6 +18,8 @@
 //   chunk_out    (chunk, head)          : O = gamma Q S_c^T + P U                   (parallel)
 // The two small matrix products of the state pass and all of chunk_out run on the tensor
 // cores (mma.sync m16n8k8 TF32 -> fp32); the state itself stays fp32.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace s1 {
@@ -227,21 +229,23 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
 // Per chunk: U = Ut - W S^T (64 x 16, K = 128); S <- gamma_n S + U^T K' (16 x 128, K = 64),
 // K'_t = exp(g_n - g_t) k_t. Records S at each chunk's start (for chunk_out) and writes U
 // over Ut. The state block stays in shared memory in fp32.
-template <int D>
+template <int D, int NS>
 struct StateSmem {
   static constexpr int SW = D + 4;      // W tile stride  ([t][j], A-operand pattern)
   static constexpr int SKK = D + 8;     // K tile stride  ([t][j], B-operand k-major pattern)
   static constexpr int SS = D + 4;      // state stride   ([i][j])
   static constexpr int SU = BV + 8;     // U tile stride  ([t][i])
-  float W[2][C * SW];
-  float K[2][C * SKK];
-  float Ut[2][C * BV];
-  float g[2][C];
+  float W[NS][C * SW];                  // NS = 2: next chunk loads while this one computes
+  float K[NS][C * SKK];
+  float Ut[NS][C * BV];
+  float g[NS][C];
   float S[BV * SS];
   float U[C * SU];
 };
 
-template <int D>
+// NS = 1 serves launches whose sequences have a single chunk (no prefetch needed, half the
+// shared memory, two CTAs per SM).
+template <int D, int NS>
 __global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restrict__ proj, int ld,
                                                           const float* __restrict__ gbuf,
                                                           const SeqDesc* __restrict__ seqs,
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restric
                                                           const float* __restrict__ Wbuf, float* __restrict__ Ubuf,
                                                           float* __restrict__ Schunk) {
   extern __shared__ __align__(16) uint8_t smraw[];
-  using SM = StateSmem<D>;
+  using SM = StateSmem<D, NS>;
   constexpr int SW = SM::SW, SKK = SM::SKK, SS = SM::SS, SU = SM::SU;
   constexpr int NTS = D / 32;            // 8-column n-tiles per warp in the state update
   SM& s = *reinterpret_cast<SM*>(smraw);
@@ -290,11 +294,17 @@ __global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restric
   if (nch > 0) load(0, 0);
   cp_commit();
   for (int cl = 0; cl < nch; ++cl) {
-    const int st = cl & 1;
+    const int st = NS == 2 ? (cl & 1) : 0;
     const ChunkDesc cd = chunks[sd.chunk0 + cl];
-    if (cl + 1 < nch) load(cl + 1, st ^ 1);
-    cp_commit();
-    cp_wait<1>();
+    if (NS == 2) {
+      if (cl + 1 < nch) load(cl + 1, st ^ 1);
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      if (cl > 0) load(cl, 0);   // single stage: the previous chunk's tiles are no longer read
+      cp_commit();
+      cp_wait<0>();
+    }
     __syncthreads();
     // record the chunk-start state block
     {
@@ -338,7 +348,8 @@ __global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restric
           make_float4(s.U[r * SU + c4], s.U[r * SU + c4 + 1], s.U[r * SU + c4 + 2], s.U[r * SU + c4 + 3]);
     }
     // S <- gamma_n S + U^T K' : warp w -> value rows 0..15, key columns (D/4)w .. (NTS n-tiles)
-    {
+    // (not needed after the last chunk of a sequence whose final state nobody keeps)
+    if (cl + 1 < nch || sd.ctx_out >= 0) {
       const float gn = s.g[st][cd.len - 1];
       const float gam = __expf(gn);
       float acc[NTS][4];
@@ -524,18 +535,38 @@ bool gdn_chunked_supported(int H, int Dk, int Dv, int ld) {
 }
 
 template <int D>
+static cudaError_t launch_state(const float* proj, int ld, const float* g, const SeqDesc* d_seq, int n_seq,
+                                const ChunkDesc* d_chunks, const CtxDesc* d_ctx, int layer_g, int H,
+                                const float* Wbuf, float* Ubuf, float* Schunk, int max_chunks, cudaStream_t st) {
+  if (n_seq <= 0) return cudaSuccess;
+  const dim3 grid(n_seq, H, D / gc::BV);
+  if (max_chunks <= 1) {
+    gc::chunk_state_kernel<D, 1><<<grid, 128, sizeof(gc::StateSmem<D, 1>), st>>>(
+        proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk);
+  } else {
+    gc::chunk_state_kernel<D, 2><<<grid, 128, sizeof(gc::StateSmem<D, 2>), st>>>(
+        proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk);
+  }
+  return cudaGetLastError();
+}
+
+template <int D>
 static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const float* beta, bf16* out,
                                     const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                     const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
-                                    float* Schunk, int n_first, cudaStream_t st) {
+                                    float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
+                                    cudaStream_t st) {
   static bool attr = false;
   const size_t sp = sizeof(gc::PrepSmem<D>);
-  const size_t ss = sizeof(gc::StateSmem<D>);
   const size_t so = sizeof(gc::OutSmem<D>);
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(gc::chunk_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gc::chunk_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ss);
+      e = cudaFuncSetAttribute(gc::chunk_state_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sizeof(gc::StateSmem<D, 1>));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gc::chunk_state_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sizeof(gc::StateSmem<D, 2>));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gc::chunk_out_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so);
     if (e != cudaSuccess) return e;
@@ -544,11 +575,14 @@ static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const floa
   gc::chunk_prep_kernel<D><<<dim3(n_chunks, H), 256, sp, st>>>(proj, ld, loga, beta, d_chunks, H, D, Wbuf, Ubuf);
   // sequences [0, n_first) run before the rest (the rest continue from their states)
   const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
-  gc::chunk_state_kernel<D><<<dim3(split, H, D / gc::BV), 128, ss, st>>>(proj, ld, loga, d_seq, d_chunks, d_ctx,
-                                                                         layer_g, H, Wbuf, Ubuf, Schunk);
-  if (split < n_seq)
-    gc::chunk_state_kernel<D><<<dim3(n_seq - split, H, D / gc::BV), 128, ss, st>>>(
-        proj, ld, loga, d_seq + split, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk);
+  cudaError_t e = launch_state<D>(proj, ld, loga, d_seq, split, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk,
+                                  split < n_seq ? max_chunks_first : std::max(max_chunks_first, max_chunks_rest), st);
+  if (e != cudaSuccess) return e;
+  if (split < n_seq) {
+    e = launch_state<D>(proj, ld, loga, d_seq + split, n_seq - split, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf,
+                        Schunk, max_chunks_rest, st);
+    if (e != cudaSuccess) return e;
+  }
   gc::chunk_out_kernel<D><<<dim3(n_chunks, H), 256, so, st>>>(proj, ld, loga, d_chunks, H, Ubuf, Schunk, out);
   return cudaGetLastError();
 }
@@ -556,15 +590,18 @@ static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const floa
 cudaError_t launch_gdn_chunked(float* proj, int ld, float* loga, const float* beta, bf16* out,
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
-                               float* Schunk, int n_first, cudaStream_t st, long* launches) {
+                               float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
+                               cudaStream_t st, long* launches) {
   if (n_seq <= 0 || n_chunks <= 0) return cudaSuccess;
   if (!gdn_chunked_supported(H, Dk, Dv, ld)) return cudaErrorNotSupported;
   if (n_seq > 65535 || n_chunks > 2147483647 / 2) return cudaErrorInvalidValue;
   cudaError_t e = (Dk == 128)
                       ? launch_chunked_d<128>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
-                                              layer_g, H, Wbuf, Ubuf, Schunk, n_first, st)
+                                              layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
+                                              max_chunks_rest, st)
                       : launch_chunked_d<64>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
-                                             layer_g, H, Wbuf, Ubuf, Schunk, n_first, st);
+                                             layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
+                                             max_chunks_rest, st);
   if (launches) *launches += (n_first > 0 && n_first < n_seq) ? 4 : 3;
   return e;
 }

@@ -90,6 +90,25 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Multicast variant: the box lands at the same shared-memory offset in every CTA of `mask`
+// and completes bytes on each destination CTA's mbarrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
@@ -118,6 +137,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
+// Arrive (when this thread's earlier MMAs complete) on the mbarrier at `bar`'s offset in every
+// CTA of `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
@@ -145,7 +173,8 @@ struct Cfg {
 struct Params {
   int M, N, K;
   int m_tiles, n_tiles, splits, kb_per_split, kb_total;
-  int units;
+  int m_groups;     // groups of CM consecutive m tiles (one group per cluster unit)
+  int units;        // cluster units: m_groups x splits x n_tiles
   int epi;          // epilogue; EPI_SPLITK_PARTIAL = write fp32 partials to ws
   void* out;
   int ldo;
@@ -154,10 +183,18 @@ struct Params {
 };
 constexpr int EPI_PARTIAL = 100;
 
-template <int BN>
+// CM CTAs of a cluster (consecutive m tiles of the same n tile and K split) share each B
+// tile: CTA r loads rows [r*BN/CM, (r+1)*BN/CM) of it and multicasts them to the cluster, so
+// each weight byte leaves L2 once per cluster instead of once per CTA. A stage is refilled only
+// after every CTA of the cluster has released it (each MMA commit arrives on all CTAs' empty
+// barriers).
+template <int BN, int CM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, Params p) {
   using C = Cfg<BN>;
+  constexpr int SLICE = BN / CM;                    // B rows loaded by each CTA of the cluster
+  constexpr uint16_t MASK = (uint16_t)((1u << CM) - 1);
+  static_assert(SLICE % 8 == 0, "B slices must be whole 8-row swizzle atoms");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -171,8 +208,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int crank = CM > 1 ? (int)cluster_rank() : 0;
+  const int cid = blockIdx.x / CM, ncl = gridDim.x / CM;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CM); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 4); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -185,6 +224,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   __syncthreads();
+  if (CM > 1) cluster_sync_all();   // peers' barriers are initialised before anyone multicasts
   fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -193,20 +233,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-        const int mt = u % p.m_tiles;
-        const int rest = u / p.m_tiles;
+      for (int u = cid; u < p.units && ok; u += ncl) {
+        const int mg = u % p.m_groups;
+        const int rest = u / p.m_groups;
         const int sp = rest % p.splits;
         const int nt = rest / p.splits;
+        const int mt = mg * CM + crank;
         const int kb0 = sp * p.kb_per_split;
         const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
           mbar_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_2d(sA + stage * C::A_BYTES, &mapA, &full[stage], kb * BK, mt * BM);
-          tma_load_2d(sB + stage * C::B_BYTES, &mapB, &full[stage], kb * BK, nt * BN);
+          if (CM == 1)
+            tma_load_2d(sB + stage * C::B_BYTES, &mapB, &full[stage], kb * BK, nt * BN);
+          else
+            tma_load_2d_mc(sB + stage * C::B_BYTES + crank * SLICE * (BK * 2), &mapB, &full[stage], kb * BK,
+                           nt * BN + crank * SLICE, MASK);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
+      }
+      // drain: every CTA's release of the stages this CTA filled has arrived here, so no peer
+      // signals this CTA's barriers after it exits
+      for (int i = 0; i < C::STAGES && ok; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) break;
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
       }
     }
   } else if (warp == 1) {
@@ -216,8 +267,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       int it = 0;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++it) {
-        const int rest = u / p.m_tiles;
+      for (int u = cid; u < p.units && ok; u += ncl, ++it) {
+        const int rest = u / p.m_groups;
         const int sp = rest % p.splits;
         const int kb0 = sp * p.kb_per_split;
         const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
@@ -235,7 +286,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mma_bf16(tmem_d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                      (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&empty[stage]);
+          if (CM == 1) mma_commit(&empty[stage]);
+          else mma_commit_mc(&empty[stage], MASK);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
         if (ok) mma_commit(&tfull[buf]);
@@ -246,11 +298,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int q = warp & 3;
     const int row_in_tile = q * 32 + lane;
     int it = 0;
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++it) {
-      const int mt = u % p.m_tiles;
-      const int rest = u / p.m_tiles;
+    for (int u = cid; u < p.units; u += ncl, ++it) {
+      const int mg = u % p.m_groups;
+      const int rest = u / p.m_groups;
       const int sp = rest % p.splits;
       const int nt = rest / p.splits;
+      const int mt = mg * CM + crank;
       const int buf = it & 1;
       if (!mbar_wait(&tfull[buf], (it >> 1) & 1, abort_flag, p.d_err, ERR_TIMEOUT_TFULL)) break;
       fence_after();
@@ -312,6 +365,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   __syncthreads();
+  if (CM > 1) cluster_sync_all();   // no CTA leaves while a peer may still target its memory
   if (warp == 1) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512));
@@ -406,7 +460,15 @@ bool make_map(CUtensorMap* out, const void* ptr, int rows, int cols, int box_row
 
 struct Plan {
   int bn, m_tiles, n_tiles, splits, kb_per_split, kb_total, units, grid;
+  int cm;   // cluster size along M (B tiles multicast within the cluster)
 };
+
+// Cluster size along M: as many m tiles as share a B tile, up to 4 (2 when BN = 144).
+inline int cluster_m(int m_tiles, int bn) {
+  int cm = m_tiles >= 4 ? 4 : (m_tiles >= 2 ? 2 : 1);
+  if (bn == 144 && cm > 2) cm = 2;
+  return cm;
+}
 
 // Choose the N tile and K split: minimise waves x per-tile cost over the candidates.
 Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
@@ -432,7 +494,7 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
       if (sp > 1) cost *= 1.0 + 0.04 * sp;
       if (cost < best_cost * 0.999) {
         best_cost = cost;
-        best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, units < num_sms ? units : num_sms};
+        best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, units < num_sms ? units : num_sms, 1};
       }
       if (units >= num_sms) break;
     }
@@ -440,17 +502,46 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
   return best;
 }
 
-template <int BN>
-cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid, cudaStream_t st) {
+template <int BN, int CM>
+cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, Params p, int num_sms, cudaStream_t st) {
   using C = Cfg<BN>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  static int max_clusters = -1;   // co-resident clusters of this configuration
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters < 0) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    cfg.gridDim = dim3(CM * ((num_sms + CM - 1) / CM));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, CM>, &cfg);
+    if (e != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms / CM;
+    }
+    max_clusters = n;
   }
-  gemm_kernel<BN><<<grid, NUM_THREADS, C::SMEM, st>>>(ma, mb, p);
-  return cudaGetLastError();
+  p.m_groups = (p.m_tiles + CM - 1) / CM;
+  p.units = p.m_groups * p.splits * p.n_tiles;
+  const int ncl = p.units < max_clusters ? p.units : max_clusters;
+  cfg.gridDim = dim3(ncl * CM);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, CM>, ma, mb, p);
+}
+
+template <int BN>
+cudaError_t launch_cm(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int cm, int num_sms,
+                      cudaStream_t st) {
+  if (cm == 4) return launch_bn<BN, (BN == 144 ? 2 : 4)>(ma, mb, p, num_sms, st);
+  if (cm == 2) return launch_bn<BN, 2>(ma, mb, p, num_sms, st);
+  return launch_bn<BN, 1>(ma, mb, p, num_sms, st);
 }
 
 }  // namespace tc
@@ -477,20 +568,22 @@ cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, in
   if (M == 0) return cudaSuccess;
   if (!gemm_tc_supported(M, N, K, epi)) return cudaErrorInvalidValue;
   const tc::Plan pl = tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
+  const int cm = tc::cluster_m(pl.m_tiles, pl.bn);
   CUtensorMap ma, mb;
-  if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, pl.bn)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, pl.bn / cm)) return cudaErrorInvalidValue;
   tc::Params p;
   p.M = M; p.N = N; p.K = K;
   p.m_tiles = pl.m_tiles; p.n_tiles = pl.n_tiles; p.splits = pl.splits;
-  p.kb_per_split = pl.kb_per_split; p.kb_total = pl.kb_total; p.units = pl.units;
+  p.kb_per_split = pl.kb_per_split; p.kb_total = pl.kb_total;
+  p.m_groups = 0; p.units = 0;   // set by the launcher for its cluster size
   p.epi = pl.splits > 1 ? tc::EPI_PARTIAL : epi;
   p.out = out; p.ldo = ldo; p.ws = splitk_ws; p.d_err = lc.d_err;
   cudaError_t e;
   switch (pl.bn) {
-    case 256: e = tc::launch_bn<256>(ma, mb, p, pl.grid, lc.stream); break;
-    case 192: e = tc::launch_bn<192>(ma, mb, p, pl.grid, lc.stream); break;
-    case 144: e = tc::launch_bn<144>(ma, mb, p, pl.grid, lc.stream); break;
-    default: e = tc::launch_bn<128>(ma, mb, p, pl.grid, lc.stream); break;
+    case 256: e = tc::launch_cm<256>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
+    case 192: e = tc::launch_cm<192>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
+    case 144: e = tc::launch_cm<144>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
+    default: e = tc::launch_cm<128>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
   }
   if (lc.launches) *lc.launches += 1;
   if (e != cudaSuccess || pl.splits == 1) return e;

@@ -1,4 +1,5 @@
 // Kernel-level entry points (s1_ops.h): one step of the path on device pointers.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -104,8 +105,10 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
     float* U = (float*)t.get((size_t)R * H * dv * 4 + 16);
     float* Sc = (float*)t.get((size_t)(nch + 1) * per * 4);
     if (!W || !U || !Sc) return op_fail(S1_ERR_OOM, "gdn: temporaries");
+    int maxc = 0;
+    for (int q = 0; q < n_seq; ++q) maxc = std::max(maxc, (len[q] + GDN_CHUNK - 1) / GDN_CHUNK);
     OCK(launch_gdn_chunked(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
-                           0, st, nullptr));
+                           0, maxc, maxc, st, nullptr));
   } else {
     OCK(launch_gdn_scan(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dctx, 0, H, dk, dv, st));
   }

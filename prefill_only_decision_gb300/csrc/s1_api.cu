@@ -267,6 +267,7 @@ struct Meta {
   std::vector<int> q_row, q_type, opt_off, opt_ids;
   int max_len = 0, max_opts = 0;
   int n_first = 0;   // fused sweep: the first n_first sequences (prefixes) scan before the rest
+  int max_chunks_first = 0, max_chunks_rest = 0;   // longest sequence (in chunks) of each group
   // device views
   int* d_row_src = nullptr;
   int* d_row_seq = nullptr;
@@ -284,6 +285,9 @@ void build_chunks(Meta& mt) {
     sd.chunk0 = (int)mt.chunks.size();
     for (int c = 0; c < sd.len; c += GDN_CHUNK)
       mt.chunks.push_back(ChunkDesc{sd.row0 + c, std::min(GDN_CHUNK, sd.len - c), (int)s});
+    const int nc = (sd.len + GDN_CHUNK - 1) / GDN_CHUNK;
+    int& mx = ((int)s < mt.n_first) ? mt.max_chunks_first : mt.max_chunks_rest;
+    mx = std::max(mx, nc);
   }
 }
 
@@ -385,8 +389,8 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
             if (!m->schunk) return fail(S1_ERR_OOM, "chunk-state buffer (%zu chunks) allocation failed", cap);
           }
           CK(launch_gdn_chunked(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
-                                mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first, st,
-                                &m->launches));
+                                mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first,
+                                mt.max_chunks_first, mt.max_chunks_rest, st, &m->launches));
         } else {
           const int split = (mt.n_first > 0 && mt.n_first < nseq) ? mt.n_first : nseq;
           CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, split, mt.d_ctxs,
