@@ -164,15 +164,27 @@ def run_kernel(args):
     g = torch.Generator(device="cuda").manual_seed(0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.kernel == "gemm":
-        M, N, K = dims[:3]
-        epi = dims[3] if len(dims) > 3 else 0
-        X = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
-        W = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.bfloat16)
-        out = torch.zeros((M, N // 2 if epi == 3 else N), device="cuda",
-                          dtype=torch.bfloat16 if epi in (1, 3) else torch.float32)
-        ldo = out.shape[1]
-        fn = lambda: B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), ldo, 0)
-        work, unit = 2.0 * M * N * K, "TFLOP/s"
+        # several shapes may be given as "M,N,K,epi;M,N,K,epi"; --cm-sweep repeats each with
+        # cluster sizes 1, 2, 4 (S1_GEMM_CM) for a measurement pass under ncu
+        shapes = [[int(x) for x in sh.split(",")] for sh in args.shape.split(";")]
+        res = []
+        for sh in shapes:
+            M, N, K = sh[:3]
+            epi = sh[3] if len(sh) > 3 else 0
+            X = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
+            W = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.bfloat16)
+            out = torch.zeros((M, N // 2 if epi == 3 else N), device="cuda",
+                              dtype=torch.bfloat16 if epi in (1, 3) else torch.float32)
+            for cm in ((1, 2, 4) if args.cm_sweep else (None,)):
+                if cm is not None:
+                    os.environ["S1_GEMM_CM"] = str(cm)
+                for _ in range(max(1, args.steps)):
+                    B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), out.shape[1], 0)
+                res.append({"shape": sh, "cm": cm})
+            os.environ.pop("S1_GEMM_CM", None)
+        torch.cuda.synchronize()
+        print(json.dumps({"kernel": "gemm", "runs": res, "note": "time these launches with the ncu launch list"}))
+        return 0
     elif args.kernel == "gdn":
         R, H, D = dims[:3]
         nseq = dims[3] if len(dims) > 3 else 1
@@ -227,6 +239,7 @@ def main():
     ap.add_argument("--path", default="fused", choices=["fused", "two-call"],
                     help="fused: s1_prefill_decide (one sweep); two-call: s1_prefill_state + s1_decide")
     ap.add_argument("--shape", default="1024,18432,2560,3")
+    ap.add_argument("--cm-sweep", action="store_true", help="gemm kernel mode: repeat with cluster sizes 1, 2, 4")
     args = ap.parse_args()
     if args.kernel:
         return run_kernel(args)

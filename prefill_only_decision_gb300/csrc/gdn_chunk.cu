@@ -55,34 +55,35 @@ __device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uin
 }
 
 // ---------------------------------------------------------------------------------------
-// chunk_prep: one CTA per (chunk, head), 256 threads (8 warps).
+// chunk_prep: one CTA per (chunk, head), 256 threads (8 warps), two CTAs per SM.
 // Writes g (within-chunk cumsum of log alpha) over loga, W and Ut (fp32 [R, H, D]).
 // The unit-lower-triangular system (I + A) X = [diag(beta gamma) K | diag(beta) V] is solved
-// in 16-row blocks: the four 16 x 16 diagonal blocks are inverted by substitution (one lane
-// per column), then X_b = T_bb (RHS_b - sum_{c<b} A_bc X_c) with the block products on the
-// tensor cores (TF32 in, fp32 accumulate).
+// in 16-row blocks: each 16 x 16 diagonal block's inverse comes from the nilpotent series
+// (I + N)^-1 = (I - N)(I + N^2)(I + N^4)(I + N^8) (N strictly lower, N^16 = 0) in fp32, then
+// X_b = T_bb (RHS_b - sum_{c<b} A_bc X_c) with the block products on the tensor cores (TF32
+// in, fp32 accumulate).
 template <int D>
 struct PrepSmem {
-  static constexpr int SKp = D + 4;        // K tile   ([s][j]: A / B(n-major) operand pattern)
-  static constexpr int SX = 2 * D + 8;     // X = [W | Ut] ([k][n]: B(k-major) operand pattern)
+  static constexpr int SX = 2 * D + 8;     // X = [K -> W | V -> Ut] ([k][n]: B(k-major) operand pattern)
   static constexpr int SA = C + 4;         // A        ([t][s]: A operand pattern)
-  static constexpr int ST = 20;            // diagonal-block inverses [16][ST]
-  float K[C * SKp];
+  static constexpr int ST = 20;            // diagonal-block inverses [16][ST] (A operand pattern)
+  static constexpr int SM17 = 16 * 17;     // 16 x 16 scratch matrices, row stride 17
   float X[C * SX];
   float A[C * SA];
   float T[4][16 * ST];
+  float M[3][4 * SM17];                    // series scratch: N^(2^k) and products
   float g[C];
   float b[C];
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict__ proj, int ld,
-                                                         float* __restrict__ loga,
-                                                         const float* __restrict__ beta,
-                                                         const ChunkDesc* __restrict__ chunks, int H, int Dv,
-                                                         float* __restrict__ Wbuf, float* __restrict__ Ubuf) {
+__global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restrict__ proj, int ld,
+                                                            float* __restrict__ loga,
+                                                            const float* __restrict__ beta,
+                                                            const ChunkDesc* __restrict__ chunks, int H, int Dv,
+                                                            float* __restrict__ Wbuf, float* __restrict__ Ubuf) {
   using SM = PrepSmem<D>;
-  constexpr int SKp = SM::SKp, SX = SM::SX, SA = SM::SA, ST = SM::ST;
+  constexpr int SX = SM::SX, SA = SM::SA, ST = SM::ST, S17 = SM::SM17;
   constexpr int NX = 2 * D;                 // columns of X
   extern __shared__ __align__(16) uint8_t smraw[];
   SM& s = *reinterpret_cast<SM*>(smraw);
@@ -90,12 +91,12 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
   const int h = blockIdx.y, n = cd.len, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   const int HDk = H * D;
-  // ---- load K (normalised) and V (into the Ut half of X), g = cumsum(log alpha), beta
+  // ---- load K (normalised) and V into X, g = cumsum(log alpha), beta
   for (int i = tid; i < C * (D / 4); i += 256) {
     const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
     const bool ok = r < n;
     const float* pr = proj + (size_t)(cd.row0 + (ok ? r : 0)) * ld;
-    cp16(&s.K[r * SKp + c4], pr + HDk + h * D + c4, ok);
+    cp16(&s.X[r * SX + c4], pr + HDk + h * D + c4, ok);
     cp16(&s.X[r * SX + D + c4], pr + 2 * HDk + h * Dv + c4, ok);
   }
   cp_commit();
@@ -123,12 +124,12 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
     float acc[4][4] = {};
 #pragma unroll 4
     for (int k = 0; k < D; k += 8) {
-      const uint32_t a0 = tf32(s.K[(r0 + gq) * SKp + k + tq]), a1 = tf32(s.K[(r0 + gq + 8) * SKp + k + tq]);
-      const uint32_t a2 = tf32(s.K[(r0 + gq) * SKp + k + tq + 4]), a3 = tf32(s.K[(r0 + gq + 8) * SKp + k + tq + 4]);
+      const uint32_t a0 = tf32(s.X[(r0 + gq) * SX + k + tq]), a1 = tf32(s.X[(r0 + gq + 8) * SX + k + tq]);
+      const uint32_t a2 = tf32(s.X[(r0 + gq) * SX + k + tq + 4]), a3 = tf32(s.X[(r0 + gq + 8) * SX + k + tq + 4]);
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const int key = c0 + nt * 8 + gq;
-        mma_tf32(acc[nt], a0, a1, a2, a3, tf32(s.K[key * SKp + k + tq]), tf32(s.K[key * SKp + k + tq + 4]));
+        mma_tf32(acc[nt], a0, a1, a2, a3, tf32(s.X[key * SX + k + tq]), tf32(s.X[key * SX + k + tq + 4]));
       }
     }
 #pragma unroll
@@ -139,26 +140,63 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
         s.A[t * SA + sc] = (sc < t && t < n) ? s.b[t] * __expf(s.g[t] - s.g[sc]) * acc[nt][e] : 0.f;
       }
   }
-  // ---- right-hand sides: W half = beta_t gamma_t k_t, Ut half = beta_t v_t
+  __syncthreads();   // K rows are read by every warp above; they become the W right-hand side below
+  // ---- right-hand sides in place: W half = beta_t gamma_t k_t, Ut half = beta_t v_t
   for (int i = tid; i < C * D; i += 256) {
     const int r = i / D, c = i % D;
-    s.X[r * SX + c] = s.b[r] * __expf(s.g[r]) * s.K[r * SKp + c];
-    s.X[r * SX + D + c] *= s.b[r];
+    const float bt = s.b[r];
+    s.X[r * SX + c] *= bt * __expf(s.g[r]);
+    s.X[r * SX + D + c] *= bt;
   }
-  __syncthreads();
-  // ---- inverses of the diagonal blocks: warp b < 4, lane j < 16 owns column j of T_bb
-  if (warp < 4 && lane < 16) {
-    float* T = s.T[warp];
-    const float* Ab = s.A + (warp * 16) * SA + warp * 16;
-    const int j = lane;
-    for (int t = 0; t < 16; ++t) {
-      float v = (t == j) ? 1.f : 0.f;
-      for (int q = j; q < t; ++q) v = fmaf(-Ab[t * SA + q], T[q * ST + j], v);
-      T[t * ST + j] = v;
+  // ---- diagonal-block inverses by the nilpotent series; thread -> block bb, row i, cols j0..j0+3
+  {
+    const int bb = tid >> 6, e = tid & 63, i = e >> 2, j0 = (e & 3) * 4;
+    float* N = s.M[0] + bb * S17;
+    // N = A_bb
+#pragma unroll
+    for (int j = 0; j < 4; ++j) N[i * 17 + j0 + j] = s.A[(bb * 16 + i) * SA + bb * 16 + j0 + j];
+    __syncthreads();
+    auto mm = [&](const float* Y, const float* Z, float* o) {   // o[4] = (Y Z)[i][j0..j0+3]
+      o[0] = o[1] = o[2] = o[3] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float y = Y[i * 17 + k];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = fmaf(y, Z[k * 17 + j0 + j], o[j]);
+      }
+    };
+    float* Pa = s.M[1] + bb * S17;
+    float* Pb = s.M[2] + bb * S17;
+    float o[4], tt[4];
+    mm(N, N, o);                                   // P1 = N^2
+#pragma unroll
+    for (int j = 0; j < 4; ++j) Pa[i * 17 + j0 + j] = o[j];
+    __syncthreads();
+    mm(N, Pa, o);                                  // N P1
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {                  // T1 = (I - N)(I + P1) = I - N + P1 - N P1
+      const int c = j0 + j;
+      tt[j] = (i == c ? 1.f : 0.f) - N[i * 17 + c] + Pa[i * 17 + c] - o[j];
     }
+    mm(Pa, Pa, o);                                 // P2 = P1^2
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { N[i * 17 + j0 + j] = tt[j]; Pb[i * 17 + j0 + j] = o[j]; }   // N <- T1
+    __syncthreads();
+    mm(N, Pb, o);                                  // T1 P2
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tt[j] = N[i * 17 + j0 + j] + o[j];   // T2 = T1 (I + P2)
+    mm(Pb, Pb, o);                                 // P3 = P2^2
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { N[i * 17 + j0 + j] = tt[j]; Pa[i * 17 + j0 + j] = o[j]; }  // N <- T2
+    __syncthreads();
+    mm(N, Pa, o);                                  // T2 P3
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s.T[bb][i * ST + j0 + j] = N[i * 17 + j0 + j] + o[j];   // T3 = T2 (I + P3)
   }
   __syncthreads();
-  // ---- block forward substitution over the 4 row blocks; warp -> 4 of the 2D/8 n-tiles
+  // ---- block forward substitution over the 4 row blocks; each warp owns NT n-tiles of X
   constexpr int NT = NX / 8 / 8;           // n-tiles per warp (D=128: 4, D=64: 2)
   for (int bb = 0; bb < 4; ++bb) {
     const int r0 = bb * 16;
@@ -181,7 +219,7 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
         mma_tf32(acc[nt], a0, a1, a2, a3, tf32(s.X[(k + tq) * SX + c]), tf32(s.X[(k + tq + 4) * SX + c]));
       }
     }
-    __syncthreads();   // all warps read the solved rows before block b is overwritten
+    __syncwarp();
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int c = (warp * NT + nt) * 8 + 2 * tq;
@@ -190,7 +228,7 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
       s.X[(r0 + gq + 8) * SX + c] = acc[nt][2];
       s.X[(r0 + gq + 8) * SX + c + 1] = acc[nt][3];
     }
-    __syncthreads();
+    __syncwarp();
     // X_b = T_bb R_b
     float xb[NT][4] = {};
     const float* T = s.T[bb];
@@ -204,7 +242,7 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
         mma_tf32(xb[nt], a0, a1, a2, a3, tf32(s.X[(r0 + k + tq) * SX + c]), tf32(s.X[(r0 + k + tq + 4) * SX + c]));
       }
     }
-    __syncthreads();
+    __syncwarp();
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int c = (warp * NT + nt) * 8 + 2 * tq;
@@ -213,8 +251,9 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
       s.X[(r0 + gq + 8) * SX + c] = xb[nt][2];
       s.X[(r0 + gq + 8) * SX + c + 1] = xb[nt][3];
     }
-    __syncthreads();
+    __syncwarp();
   }
+  __syncthreads();
   for (int i = tid; i < n * (D / 4); i += 256) {
     const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
     const size_t o = ((size_t)(cd.row0 + r) * H + h) * D + c4;
@@ -225,7 +264,7 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(const float* __restrict
 }
 
 // ---------------------------------------------------------------------------------------
-// chunk_state: one CTA per (sequence, head, block of 16 value rows), 128 threads (4 warps).
+// chunk_state: one CTA per (sequence, head, block of 16 value rows), 256 threads (8 warps).
 // Per chunk: U = Ut - W S^T (64 x 16, K = 128); S <- gamma_n S + U^T K' (16 x 128, K = 64),
 // K'_t = exp(g_n - g_t) k_t. Records S at each chunk's start (for chunk_out) and writes U
 // over Ut. The state block stays in shared memory in fp32.
@@ -244,9 +283,10 @@ struct StateSmem {
 };
 
 // NS = 1 serves launches whose sequences have a single chunk (no prefetch needed, half the
-// shared memory, two CTAs per SM).
+// shared memory, two CTAs per SM). 8 warps; every matrix-product chain is split over two
+// accumulators so the tensor-core latency of the sequential pass is halved.
 template <int D, int NS>
-__global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restrict__ proj, int ld,
+__global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restrict__ proj, int ld,
                                                           const float* __restrict__ gbuf,
                                                           const SeqDesc* __restrict__ seqs,
                                                           const ChunkDesc* __restrict__ chunks,
@@ -256,7 +296,8 @@ __global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restric
   extern __shared__ __align__(16) uint8_t smraw[];
   using SM = StateSmem<D, NS>;
   constexpr int SW = SM::SW, SKK = SM::SKK, SS = SM::SS, SU = SM::SU;
-  constexpr int NTS = D / 32;            // 8-column n-tiles per warp in the state update
+  constexpr int NTS = D / 64;            // 8-column n-tiles per warp in the state update
+  constexpr int NTH = 256;
   SM& s = *reinterpret_cast<SM*>(smraw);
   const SeqDesc sd = seqs[blockIdx.x];
   const int h = blockIdx.y, v0 = blockIdx.z * BV;
@@ -264,23 +305,22 @@ __global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restric
   const int gq = lane >> 2, tq = lane & 3;
   const int HDk = H * D;
   const size_t head_off = (size_t)(layer_g * H + h) * D * D;
-  // initial state block
   const float* S0 = sd.ctx_in >= 0 ? ctxs[sd.ctx_in].S + head_off : nullptr;
-  for (int i = tid; i < BV * D; i += 128) {
+  for (int i = tid; i < BV * D; i += NTH) {
     const int r = i / D, c = i % D;
     s.S[r * SS + c] = S0 ? S0[(size_t)(v0 + r) * D + c] : 0.f;
   }
   const int nch = (sd.len + C - 1) / C;
   auto load = [&](int cl, int st) {
     const ChunkDesc cd = chunks[sd.chunk0 + cl];
-    for (int i = tid; i < C * (D / 4); i += 128) {
+    for (int i = tid; i < C * (D / 4); i += NTH) {
       const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
       const bool ok = r < cd.len;
       const int row = cd.row0 + (ok ? r : 0);
       cp16(&s.W[st][r * SW + c4], Wbuf + ((size_t)row * H + h) * D + c4, ok);
       cp16(&s.K[st][r * SKK + c4], proj + (size_t)row * ld + HDk + h * D + c4, ok);
     }
-    for (int i = tid; i < C * (BV / 4); i += 128) {
+    for (int i = tid; i < C * (BV / 4); i += NTH) {
       const int r = i / (BV / 4), c4 = (i % (BV / 4)) * 4;
       const bool ok = r < cd.len;
       const int row = cd.row0 + (ok ? r : 0);
@@ -309,88 +349,90 @@ __global__ void __launch_bounds__(128) chunk_state_kernel(const float* __restric
     // record the chunk-start state block
     {
       float* dst = Schunk + ((size_t)(sd.chunk0 + cl) * H + h) * D * D + (size_t)v0 * D;
-      for (int i = tid; i < BV * (D / 4); i += 128) {
+      for (int i = tid; i < BV * (D / 4); i += NTH) {
         const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
         *reinterpret_cast<float4*>(dst + (size_t)r * D + c4) = *reinterpret_cast<const float4*>(&s.S[r * SS + c4]);
       }
     }
-    // U = Ut - W S^T : warp w -> rows 16w..16w+15, both 8-column n-tiles
+    // U = Ut - W S^T : warp -> rows 16*(warp&3) .., value columns 8*(warp>>2) .. +7
     {
-      float acc[2][4] = {};
+      float a0c[4] = {0.f, 0.f, 0.f, 0.f}, a1c[4] = {0.f, 0.f, 0.f, 0.f};
       const float* Wt = s.W[st];
-      const int r0 = warp * 16;
+      const int r0 = (warp & 3) * 16, n0 = (warp >> 2) * 8;
 #pragma unroll 4
-      for (int k = 0; k < D; k += 8) {
-        const uint32_t a0 = tf32(Wt[(r0 + gq) * SW + k + tq]), a1 = tf32(Wt[(r0 + gq + 8) * SW + k + tq]);
-        const uint32_t a2 = tf32(Wt[(r0 + gq) * SW + k + tq + 4]), a3 = tf32(Wt[(r0 + gq + 8) * SW + k + tq + 4]);
+      for (int k = 0; k < D; k += 16) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const uint32_t b0 = tf32(s.S[(nt * 8 + gq) * SS + k + tq]);
-          const uint32_t b1 = tf32(s.S[(nt * 8 + gq) * SS + k + tq + 4]);
-          mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+        for (int half = 0; half < 2; ++half) {
+          const int kk = k + half * 8;
+          const uint32_t x0 = tf32(Wt[(r0 + gq) * SW + kk + tq]), x1 = tf32(Wt[(r0 + gq + 8) * SW + kk + tq]);
+          const uint32_t x2 = tf32(Wt[(r0 + gq) * SW + kk + tq + 4]), x3 = tf32(Wt[(r0 + gq + 8) * SW + kk + tq + 4]);
+          const uint32_t b0 = tf32(s.S[(n0 + gq) * SS + kk + tq]), b1 = tf32(s.S[(n0 + gq) * SS + kk + tq + 4]);
+          mma_tf32(half ? a1c : a0c, x0, x1, x2, x3, b0, b1);
         }
       }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int c = nt * 8 + 2 * tq;
-        const int ra = r0 + gq, rb = r0 + gq + 8;
-        s.U[ra * SU + c] = s.Ut[st][ra * BV + c] - acc[nt][0];
-        s.U[ra * SU + c + 1] = s.Ut[st][ra * BV + c + 1] - acc[nt][1];
-        s.U[rb * SU + c] = s.Ut[st][rb * BV + c] - acc[nt][2];
-        s.U[rb * SU + c + 1] = s.Ut[st][rb * BV + c + 1] - acc[nt][3];
-      }
+      const int c = n0 + 2 * tq;
+      const int ra = r0 + gq, rb = r0 + gq + 8;
+      s.U[ra * SU + c] = s.Ut[st][ra * BV + c] - (a0c[0] + a1c[0]);
+      s.U[ra * SU + c + 1] = s.Ut[st][ra * BV + c + 1] - (a0c[1] + a1c[1]);
+      s.U[rb * SU + c] = s.Ut[st][rb * BV + c] - (a0c[2] + a1c[2]);
+      s.U[rb * SU + c + 1] = s.Ut[st][rb * BV + c + 1] - (a0c[3] + a1c[3]);
     }
     __syncthreads();
     // write U (this block's 16 value columns) over Ut
-    for (int i = tid; i < cd.len * (BV / 4); i += 128) {
+    for (int i = tid; i < cd.len * (BV / 4); i += NTH) {
       const int r = i / (BV / 4), c4 = (i % (BV / 4)) * 4;
       *reinterpret_cast<float4*>(Ubuf + ((size_t)(cd.row0 + r) * H + h) * D + v0 + c4) =
           make_float4(s.U[r * SU + c4], s.U[r * SU + c4 + 1], s.U[r * SU + c4 + 2], s.U[r * SU + c4 + 3]);
     }
-    // S <- gamma_n S + U^T K' : warp w -> value rows 0..15, key columns (D/4)w .. (NTS n-tiles)
+    // S <- gamma_n S + U^T K' : warp -> value rows 0..15, key columns 8*NTS*warp .. (NTS n-tiles)
     // (not needed after the last chunk of a sequence whose final state nobody keeps)
     if (cl + 1 < nch || sd.ctx_out >= 0) {
       const float gn = s.g[st][cd.len - 1];
       const float gam = __expf(gn);
-      float acc[NTS][4];
+      float acc[NTS][4], acc2[NTS][4];
 #pragma unroll
       for (int nt = 0; nt < NTS; ++nt) {
-        const int c = warp * (D / 4) + nt * 8 + 2 * tq;
+        const int c = warp * (8 * NTS) + nt * 8 + 2 * tq;
         acc[nt][0] = gam * s.S[gq * SS + c];
         acc[nt][1] = gam * s.S[gq * SS + c + 1];
         acc[nt][2] = gam * s.S[(gq + 8) * SS + c];
         acc[nt][3] = gam * s.S[(gq + 8) * SS + c + 1];
+        acc2[nt][0] = acc2[nt][1] = acc2[nt][2] = acc2[nt][3] = 0.f;
       }
       const float* Kt = s.K[st];
 #pragma unroll 2
-      for (int k = 0; k < C; k += 8) {
-        // A[i][t] = U[t][i]
-        const uint32_t a0 = tf32(s.U[(k + tq) * SU + gq]), a1 = tf32(s.U[(k + tq) * SU + gq + 8]);
-        const uint32_t a2 = tf32(s.U[(k + tq + 4) * SU + gq]), a3 = tf32(s.U[(k + tq + 4) * SU + gq + 8]);
-        const float e0 = __expf(gn - s.g[st][k + tq]), e1 = __expf(gn - s.g[st][k + tq + 4]);
+      for (int k = 0; k < C; k += 16) {
 #pragma unroll
-        for (int nt = 0; nt < NTS; ++nt) {
-          const int c = warp * (D / 4) + nt * 8 + gq;
-          const uint32_t b0 = tf32(e0 * Kt[(k + tq) * SKK + c]);
-          const uint32_t b1 = tf32(e1 * Kt[(k + tq + 4) * SKK + c]);
-          mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+        for (int half = 0; half < 2; ++half) {
+          const int kk = k + half * 8;
+          // A[i][t] = U[t][i]
+          const uint32_t x0 = tf32(s.U[(kk + tq) * SU + gq]), x1 = tf32(s.U[(kk + tq) * SU + gq + 8]);
+          const uint32_t x2 = tf32(s.U[(kk + tq + 4) * SU + gq]), x3 = tf32(s.U[(kk + tq + 4) * SU + gq + 8]);
+          const float e0 = __expf(gn - s.g[st][kk + tq]), e1 = __expf(gn - s.g[st][kk + tq + 4]);
+#pragma unroll
+          for (int nt = 0; nt < NTS; ++nt) {
+            const int c = warp * (8 * NTS) + nt * 8 + gq;
+            const uint32_t b0 = tf32(e0 * Kt[(kk + tq) * SKK + c]);
+            const uint32_t b1 = tf32(e1 * Kt[(kk + tq + 4) * SKK + c]);
+            mma_tf32(half ? acc2[nt] : acc[nt], x0, x1, x2, x3, b0, b1);
+          }
         }
       }
       __syncthreads();   // every warp has read S and U
 #pragma unroll
       for (int nt = 0; nt < NTS; ++nt) {
-        const int c = warp * (D / 4) + nt * 8 + 2 * tq;
-        s.S[gq * SS + c] = acc[nt][0];
-        s.S[gq * SS + c + 1] = acc[nt][1];
-        s.S[(gq + 8) * SS + c] = acc[nt][2];
-        s.S[(gq + 8) * SS + c + 1] = acc[nt][3];
+        const int c = warp * (8 * NTS) + nt * 8 + 2 * tq;
+        s.S[gq * SS + c] = acc[nt][0] + acc2[nt][0];
+        s.S[gq * SS + c + 1] = acc[nt][1] + acc2[nt][1];
+        s.S[(gq + 8) * SS + c] = acc[nt][2] + acc2[nt][2];
+        s.S[(gq + 8) * SS + c + 1] = acc[nt][3] + acc2[nt][3];
       }
     }
     __syncthreads();
   }
   if (sd.ctx_out >= 0) {
     float* So = ctxs[sd.ctx_out].S + head_off;
-    for (int i = tid; i < BV * D; i += 128) {
+    for (int i = tid; i < BV * D; i += NTH) {
       const int r = i / D, c = i % D;
       So[(size_t)(v0 + r) * D + c] = s.S[r * SS + c];
     }
@@ -541,10 +583,10 @@ static cudaError_t launch_state(const float* proj, int ld, const float* g, const
   if (n_seq <= 0) return cudaSuccess;
   const dim3 grid(n_seq, H, D / gc::BV);
   if (max_chunks <= 1) {
-    gc::chunk_state_kernel<D, 1><<<grid, 128, sizeof(gc::StateSmem<D, 1>), st>>>(
+    gc::chunk_state_kernel<D, 1><<<grid, 256, sizeof(gc::StateSmem<D, 1>), st>>>(
         proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk);
   } else {
-    gc::chunk_state_kernel<D, 2><<<grid, 128, sizeof(gc::StateSmem<D, 2>), st>>>(
+    gc::chunk_state_kernel<D, 2><<<grid, 256, sizeof(gc::StateSmem<D, 2>), st>>>(
         proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk);
   }
   return cudaGetLastError();

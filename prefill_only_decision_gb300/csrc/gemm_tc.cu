@@ -18,6 +18,7 @@
 // hang the GPU.
 #include <cuda.h>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -470,46 +471,57 @@ inline int cluster_m(int m_tiles, int bn) {
   return cm;
 }
 
-// Choose the N tile and K split: minimise waves x per-tile cost over the candidates.
+inline int max_clusters_of(int bn, int cm, int num_sms);
+
+// Choose the N tile, the K split and the cluster size together: minimise
+// (waves of cluster units) x (k blocks per unit) x (per-k-block cost of the tile), where a
+// cluster unit is CM m tiles (padding tiles when CM does not divide the m-tile count cost
+// like real ones) and sharing the weight tile in a cluster lowers the per-block cost
+// (fewer bytes requested from L2 per stage).
 Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
   Plan best{};
   double best_cost = 1e30;
   const int kb_total = K / BK;
   const int m_tiles = (M + BM - 1) / BM;
   const int cands[4] = {256, 192, 144, 128};
+  const char* fe = getenv("S1_GEMM_CM");   // measurement override of the cluster size
+  const int force_cm = fe ? atoi(fe) : -1;
   for (int bn : cands) {
     if (epi == EPI_SWIGLU && (bn % 32)) continue;
     const int n_tiles = (N + bn - 1) / bn;
-    const int tiles = m_tiles * n_tiles;
-    for (int splits = 1; splits <= 16; ++splits) {
-      if (splits > 1 && (kb_total / splits) < 4) break;
-      const int kbp = (kb_total + splits - 1) / splits;
-      const int sp = (kb_total + kbp - 1) / kbp;
-      if (sp != splits) continue;
-      const int units = tiles * sp;
-      if (sp > 1 && (size_t)sp * m_tiles * BM * (size_t)N > ws_cap) break;
-      const int waves = (units + num_sms - 1) / num_sms;
-      // per-unit cost ~ k blocks x (bn + fixed overhead); split-K adds the partial traffic
-      double cost = (double)waves * kbp * (bn + 48.0);
-      if (sp > 1) cost *= 1.0 + 0.04 * sp;
-      if (cost < best_cost * 0.999) {
-        best_cost = cost;
-        best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, units < num_sms ? units : num_sms, 1};
+    for (int cm = 1; cm <= 4; cm *= 2) {
+      if (bn == 144 && cm == 4) continue;
+      if (cm > 1 && m_tiles < 2) continue;
+      if (force_cm > 0 && cm != force_cm) continue;
+      const int maxcl = max_clusters_of(bn, cm, num_sms);
+      const int groups = (m_tiles + cm - 1) / cm;
+      const double share = cm == 1 ? 1.0 : (cm == 2 ? 0.88 : 0.82);
+      for (int splits = 1; splits <= 16; ++splits) {
+        if (splits > 1 && (kb_total / splits) < 4) break;
+        const int kbp = (kb_total + splits - 1) / splits;
+        const int sp = (kb_total + kbp - 1) / kbp;
+        if (sp != splits) continue;
+        if (sp > 1 && (size_t)sp * m_tiles * BM * (size_t)N > ws_cap) break;
+        const int cunits = groups * n_tiles * sp;
+        const int waves = (cunits + maxcl - 1) / maxcl;
+        double cost = (double)waves * kbp * (bn + 48.0) * share;
+        if (sp > 1) cost *= 1.0 + 0.04 * sp;
+        if (cost < best_cost * 0.999) {
+          best_cost = cost;
+          best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, m_tiles * n_tiles * sp, 0, cm};
+        }
+        if (cunits >= maxcl) break;
       }
-      if (units >= num_sms) break;
     }
   }
   return best;
 }
 
 template <int BN, int CM>
-cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, Params p, int num_sms, cudaStream_t st) {
-  using C = Cfg<BN>;
-  static int max_clusters = -1;   // co-resident clusters of this configuration
+cudaLaunchConfig_t launch_config(cudaLaunchAttribute* attr, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = CM;
@@ -517,21 +529,54 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, Params p, in
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_clusters < 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
+  return cfg;
+}
+
+// Clusters of this configuration that fit on the GPU at once (queried once, then cached).
+template <int BN, int CM>
+int max_clusters(int num_sms) {
+  static int cached = -1;
+  if (cached < 0) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config<BN, CM>(attr, 0);
     cfg.gridDim = dim3(CM * ((num_sms + CM - 1) / CM));
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, CM>, &cfg);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, CM>, &cfg);
     if (e != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = num_sms / CM;
     }
-    max_clusters = n;
+    cached = n;
   }
+  return cached;
+}
+
+inline int max_clusters_of(int bn, int cm, int num_sms) {
+  switch (bn * 8 + cm) {
+    case 256 * 8 + 1: return max_clusters<256, 1>(num_sms);
+    case 256 * 8 + 2: return max_clusters<256, 2>(num_sms);
+    case 256 * 8 + 4: return max_clusters<256, 4>(num_sms);
+    case 192 * 8 + 1: return max_clusters<192, 1>(num_sms);
+    case 192 * 8 + 2: return max_clusters<192, 2>(num_sms);
+    case 192 * 8 + 4: return max_clusters<192, 4>(num_sms);
+    case 144 * 8 + 1: return max_clusters<144, 1>(num_sms);
+    case 144 * 8 + 2: return max_clusters<144, 2>(num_sms);
+    case 128 * 8 + 1: return max_clusters<128, 1>(num_sms);
+    case 128 * 8 + 2: return max_clusters<128, 2>(num_sms);
+    case 128 * 8 + 4: return max_clusters<128, 4>(num_sms);
+    default: return num_sms / cm;
+  }
+}
+
+template <int BN, int CM>
+cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, Params p, int num_sms, cudaStream_t st) {
+  const int mc = max_clusters<BN, CM>(num_sms);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config<BN, CM>(attr, st);
   p.m_groups = (p.m_tiles + CM - 1) / CM;
   p.units = p.m_groups * p.splits * p.n_tiles;
-  const int ncl = p.units < max_clusters ? p.units : max_clusters;
+  const int ncl = p.units < mc ? p.units : mc;
   cfg.gridDim = dim3(ncl * CM);
   return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, CM>, ma, mb, p);
 }
@@ -568,7 +613,7 @@ cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, in
   if (M == 0) return cudaSuccess;
   if (!gemm_tc_supported(M, N, K, epi)) return cudaErrorInvalidValue;
   const tc::Plan pl = tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
-  const int cm = tc::cluster_m(pl.m_tiles, pl.bn);
+  const int cm = pl.cm;
   CUtensorMap ma, mb;
   if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, pl.bn / cm)) return cudaErrorInvalidValue;
   tc::Params p;
