@@ -160,7 +160,7 @@ def run_kernel(args):
     `--kernel gdn --shape R,H,D[,nseq]` or `--kernel attn --shape P,len,nseq,Hq,Hkv,hd`."""
     import torch
     from prefill_only_decision_gb300 import binding as B
-    dims = [int(x) for x in args.shape.split(",")]
+    dims = [int(x) for x in args.shape.split(";")[0].split(",")]
     g = torch.Generator(device="cuda").manual_seed(0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.kernel == "gemm":

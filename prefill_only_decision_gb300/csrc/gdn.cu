@@ -26,7 +26,13 @@ __global__ void gdn_prep_kernel(float* __restrict__ proj, int ld, float* __restr
     for (int i = lane; i < Dk; i += 32) ss += x[i] * x[i];
     ss = warp_sum(ss);
     const float inv = 1.0f / sqrtf(ss + eps);
-    for (int i = lane; i < Dk; i += 32) x[i] *= inv;
+    // stored rounded to TF32 (10-bit mantissa): every later product of q and k runs on TF32
+    // tensor-core inputs, so the rounding happens once here instead of at each use
+    for (int i = lane; i < Dk; i += 32) {
+      uint32_t r;
+      asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x[i] * inv));
+      x[i] = __uint_as_float(r);
+    }
   }
   const float* ab = pr + 2 * H * Dk + H * Dv;
   for (int h = threadIdx.x; h < H; h += blockDim.x) {

@@ -45,6 +45,10 @@ __device__ __forceinline__ uint32_t tf32(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return r;
 }
+// Operands already rounded to TF32 when they were produced (q, k by gdn_prep; W, Ut, U and the
+// recorded chunk states by the kernels below) are passed to the tensor cores as they are.
+__device__ __forceinline__ uint32_t raw(float x) { return __float_as_uint(x); }
+__device__ __forceinline__ float rnd(float x) { return __uint_as_float(tf32(x)); }
 // D += A(16x8, row) * B(8x8, col), tf32 inputs, fp32 accumulate
 __device__ __forceinline__ void mma_tf32(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
@@ -124,12 +128,12 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
     float acc[4][4] = {};
 #pragma unroll 4
     for (int k = 0; k < D; k += 8) {
-      const uint32_t a0 = tf32(s.X[(r0 + gq) * SX + k + tq]), a1 = tf32(s.X[(r0 + gq + 8) * SX + k + tq]);
-      const uint32_t a2 = tf32(s.X[(r0 + gq) * SX + k + tq + 4]), a3 = tf32(s.X[(r0 + gq + 8) * SX + k + tq + 4]);
+      const uint32_t a0 = raw(s.X[(r0 + gq) * SX + k + tq]), a1 = raw(s.X[(r0 + gq + 8) * SX + k + tq]);
+      const uint32_t a2 = raw(s.X[(r0 + gq) * SX + k + tq + 4]), a3 = raw(s.X[(r0 + gq + 8) * SX + k + tq + 4]);
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const int key = c0 + nt * 8 + gq;
-        mma_tf32(acc[nt], a0, a1, a2, a3, tf32(s.X[key * SX + k + tq]), tf32(s.X[key * SX + k + tq + 4]));
+        mma_tf32(acc[nt], a0, a1, a2, a3, raw(s.X[key * SX + k + tq]), raw(s.X[key * SX + k + tq + 4]));
       }
     }
 #pragma unroll
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int t = r0 + gq + (e >> 1) * 8, sc = c0 + nt * 8 + 2 * tq + (e & 1);
-        s.A[t * SA + sc] = (sc < t && t < n) ? s.b[t] * __expf(s.g[t] - s.g[sc]) * acc[nt][e] : 0.f;
+        s.A[t * SA + sc] = (sc < t && t < n) ? rnd(s.b[t] * __expf(s.g[t] - s.g[sc]) * acc[nt][e]) : 0.f;
       }
   }
   __syncthreads();   // K rows are read by every warp above; they become the W right-hand side below
@@ -145,8 +149,8 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
   for (int i = tid; i < C * D; i += 256) {
     const int r = i / D, c = i % D;
     const float bt = s.b[r];
-    s.X[r * SX + c] *= bt * __expf(s.g[r]);
-    s.X[r * SX + D + c] *= bt;
+    s.X[r * SX + c] = rnd(s.X[r * SX + c] * (bt * __expf(s.g[r])));
+    s.X[r * SX + D + c] = rnd(s.X[r * SX + D + c] * bt);
   }
   // ---- diagonal-block inverses by the nilpotent series; thread -> block bb, row i, cols j0..j0+3
   {
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
     __syncthreads();
     mm(N, Pa, o);                                  // T2 P3
 #pragma unroll
-    for (int j = 0; j < 4; ++j) s.T[bb][i * ST + j0 + j] = N[i * 17 + j0 + j] + o[j];   // T3 = T2 (I + P3)
+    for (int j = 0; j < 4; ++j) s.T[bb][i * ST + j0 + j] = rnd(N[i * 17 + j0 + j] + o[j]);   // T3 = T2 (I + P3)
   }
   __syncthreads();
   // ---- block forward substitution over the 4 row blocks; each warp owns NT n-tiles of X
@@ -211,22 +215,22 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
     }
     // R = RHS_b - A[b, 0:16b] X[0:16b]
     for (int k = 0; k < r0; k += 8) {
-      const uint32_t a0 = tf32(-s.A[(r0 + gq) * SA + k + tq]), a1 = tf32(-s.A[(r0 + gq + 8) * SA + k + tq]);
-      const uint32_t a2 = tf32(-s.A[(r0 + gq) * SA + k + tq + 4]), a3 = tf32(-s.A[(r0 + gq + 8) * SA + k + tq + 4]);
+      const uint32_t a0 = raw(-s.A[(r0 + gq) * SA + k + tq]), a1 = raw(-s.A[(r0 + gq + 8) * SA + k + tq]);
+      const uint32_t a2 = raw(-s.A[(r0 + gq) * SA + k + tq + 4]), a3 = raw(-s.A[(r0 + gq + 8) * SA + k + tq + 4]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = (warp * NT + nt) * 8 + gq;
-        mma_tf32(acc[nt], a0, a1, a2, a3, tf32(s.X[(k + tq) * SX + c]), tf32(s.X[(k + tq + 4) * SX + c]));
+        mma_tf32(acc[nt], a0, a1, a2, a3, raw(s.X[(k + tq) * SX + c]), raw(s.X[(k + tq + 4) * SX + c]));
       }
     }
     __syncwarp();
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int c = (warp * NT + nt) * 8 + 2 * tq;
-      s.X[(r0 + gq) * SX + c] = acc[nt][0];
-      s.X[(r0 + gq) * SX + c + 1] = acc[nt][1];
-      s.X[(r0 + gq + 8) * SX + c] = acc[nt][2];
-      s.X[(r0 + gq + 8) * SX + c + 1] = acc[nt][3];
+      s.X[(r0 + gq) * SX + c] = rnd(acc[nt][0]);
+      s.X[(r0 + gq) * SX + c + 1] = rnd(acc[nt][1]);
+      s.X[(r0 + gq + 8) * SX + c] = rnd(acc[nt][2]);
+      s.X[(r0 + gq + 8) * SX + c + 1] = rnd(acc[nt][3]);
     }
     __syncwarp();
     // X_b = T_bb R_b
@@ -234,22 +238,22 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
     const float* T = s.T[bb];
 #pragma unroll
     for (int k = 0; k < 16; k += 8) {
-      const uint32_t a0 = tf32(T[gq * ST + k + tq]), a1 = tf32(T[(gq + 8) * ST + k + tq]);
-      const uint32_t a2 = tf32(T[gq * ST + k + tq + 4]), a3 = tf32(T[(gq + 8) * ST + k + tq + 4]);
+      const uint32_t a0 = raw(T[gq * ST + k + tq]), a1 = raw(T[(gq + 8) * ST + k + tq]);
+      const uint32_t a2 = raw(T[gq * ST + k + tq + 4]), a3 = raw(T[(gq + 8) * ST + k + tq + 4]);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int c = (warp * NT + nt) * 8 + gq;
-        mma_tf32(xb[nt], a0, a1, a2, a3, tf32(s.X[(r0 + k + tq) * SX + c]), tf32(s.X[(r0 + k + tq + 4) * SX + c]));
+        mma_tf32(xb[nt], a0, a1, a2, a3, raw(s.X[(r0 + k + tq) * SX + c]), raw(s.X[(r0 + k + tq + 4) * SX + c]));
       }
     }
     __syncwarp();
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int c = (warp * NT + nt) * 8 + 2 * tq;
-      s.X[(r0 + gq) * SX + c] = xb[nt][0];
-      s.X[(r0 + gq) * SX + c + 1] = xb[nt][1];
-      s.X[(r0 + gq + 8) * SX + c] = xb[nt][2];
-      s.X[(r0 + gq + 8) * SX + c + 1] = xb[nt][3];
+      s.X[(r0 + gq) * SX + c] = rnd(xb[nt][0]);
+      s.X[(r0 + gq) * SX + c + 1] = rnd(xb[nt][1]);
+      s.X[(r0 + gq + 8) * SX + c] = rnd(xb[nt][2]);
+      s.X[(r0 + gq + 8) * SX + c + 1] = rnd(xb[nt][3]);
     }
     __syncwarp();
   }
@@ -279,7 +283,8 @@ struct StateSmem {
   float Ut[NS][C * BV];
   float g[NS][C];
   float S[BV * SS];
-  float U[C * SU];
+  float U[C * SU];      // U (TF32-rounded), written back for chunk_out
+  float Us[C * SU];     // exp(g_n - g_t) U_t (TF32-rounded), A operand of the state update
 };
 
 // NS = 1 serves launches whose sequences have a single chunk (no prefetch needed, half the
@@ -351,7 +356,8 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
       float* dst = Schunk + ((size_t)(sd.chunk0 + cl) * H + h) * D * D + (size_t)v0 * D;
       for (int i = tid; i < BV * (D / 4); i += NTH) {
         const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-        *reinterpret_cast<float4*>(dst + (size_t)r * D + c4) = *reinterpret_cast<const float4*>(&s.S[r * SS + c4]);
+        const float4 v = *reinterpret_cast<const float4*>(&s.S[r * SS + c4]);
+        *reinterpret_cast<float4*>(dst + (size_t)r * D + c4) = make_float4(rnd(v.x), rnd(v.y), rnd(v.z), rnd(v.w));
       }
     }
     // U = Ut - W S^T : warp -> rows 16*(warp&3) .., value columns 8*(warp>>2) .. +7
@@ -364,18 +370,26 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int kk = k + half * 8;
-          const uint32_t x0 = tf32(Wt[(r0 + gq) * SW + kk + tq]), x1 = tf32(Wt[(r0 + gq + 8) * SW + kk + tq]);
-          const uint32_t x2 = tf32(Wt[(r0 + gq) * SW + kk + tq + 4]), x3 = tf32(Wt[(r0 + gq + 8) * SW + kk + tq + 4]);
+          const uint32_t x0 = raw(Wt[(r0 + gq) * SW + kk + tq]), x1 = raw(Wt[(r0 + gq + 8) * SW + kk + tq]);
+          const uint32_t x2 = raw(Wt[(r0 + gq) * SW + kk + tq + 4]), x3 = raw(Wt[(r0 + gq + 8) * SW + kk + tq + 4]);
           const uint32_t b0 = tf32(s.S[(n0 + gq) * SS + kk + tq]), b1 = tf32(s.S[(n0 + gq) * SS + kk + tq + 4]);
           mma_tf32(half ? a1c : a0c, x0, x1, x2, x3, b0, b1);
         }
       }
       const int c = n0 + 2 * tq;
       const int ra = r0 + gq, rb = r0 + gq + 8;
-      s.U[ra * SU + c] = s.Ut[st][ra * BV + c] - (a0c[0] + a1c[0]);
-      s.U[ra * SU + c + 1] = s.Ut[st][ra * BV + c + 1] - (a0c[1] + a1c[1]);
-      s.U[rb * SU + c] = s.Ut[st][rb * BV + c] - (a0c[2] + a1c[2]);
-      s.U[rb * SU + c + 1] = s.Ut[st][rb * BV + c + 1] - (a0c[3] + a1c[3]);
+      const float gn = s.g[st][cd.len - 1];
+      const float ea = __expf(gn - s.g[st][ra]), eb = __expf(gn - s.g[st][rb]);
+      const float u0 = s.Ut[st][ra * BV + c] - (a0c[0] + a1c[0]), u1 = s.Ut[st][ra * BV + c + 1] - (a0c[1] + a1c[1]);
+      const float u2 = s.Ut[st][rb * BV + c] - (a0c[2] + a1c[2]), u3 = s.Ut[st][rb * BV + c + 1] - (a0c[3] + a1c[3]);
+      s.U[ra * SU + c] = rnd(u0);
+      s.U[ra * SU + c + 1] = rnd(u1);
+      s.U[rb * SU + c] = rnd(u2);
+      s.U[rb * SU + c + 1] = rnd(u3);
+      s.Us[ra * SU + c] = rnd(ea * u0);
+      s.Us[ra * SU + c + 1] = rnd(ea * u1);
+      s.Us[rb * SU + c] = rnd(eb * u2);
+      s.Us[rb * SU + c + 1] = rnd(eb * u3);
     }
     __syncthreads();
     // write U (this block's 16 value columns) over Ut
@@ -405,16 +419,14 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int kk = k + half * 8;
-          // A[i][t] = U[t][i]
-          const uint32_t x0 = tf32(s.U[(kk + tq) * SU + gq]), x1 = tf32(s.U[(kk + tq) * SU + gq + 8]);
-          const uint32_t x2 = tf32(s.U[(kk + tq + 4) * SU + gq]), x3 = tf32(s.U[(kk + tq + 4) * SU + gq + 8]);
-          const float e0 = __expf(gn - s.g[st][kk + tq]), e1 = __expf(gn - s.g[st][kk + tq + 4]);
+          // A[i][t] = exp(g_n - g_t) U[t][i]
+          const uint32_t x0 = raw(s.Us[(kk + tq) * SU + gq]), x1 = raw(s.Us[(kk + tq) * SU + gq + 8]);
+          const uint32_t x2 = raw(s.Us[(kk + tq + 4) * SU + gq]), x3 = raw(s.Us[(kk + tq + 4) * SU + gq + 8]);
 #pragma unroll
           for (int nt = 0; nt < NTS; ++nt) {
             const int c = warp * (8 * NTS) + nt * 8 + gq;
-            const uint32_t b0 = tf32(e0 * Kt[(kk + tq) * SKK + c]);
-            const uint32_t b1 = tf32(e1 * Kt[(kk + tq + 4) * SKK + c]);
-            mma_tf32(half ? acc2[nt] : acc[nt], x0, x1, x2, x3, b0, b1);
+            mma_tf32(half ? acc2[nt] : acc[nt], x0, x1, x2, x3, raw(Kt[(kk + tq) * SKK + c]),
+                     raw(Kt[(kk + tq + 4) * SKK + c]));
           }
         }
       }
@@ -496,12 +508,12 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
     const int c0 = (warp >> 2) * 32;
 #pragma unroll 4
     for (int k = 0; k < D; k += 8) {
-      const uint32_t a0 = tf32(s.Q[(r0 + gq) * SQ + k + tq]), a1 = tf32(s.Q[(r0 + gq + 8) * SQ + k + tq]);
-      const uint32_t a2 = tf32(s.Q[(r0 + gq) * SQ + k + tq + 4]), a3 = tf32(s.Q[(r0 + gq + 8) * SQ + k + tq + 4]);
+      const uint32_t a0 = raw(s.Q[(r0 + gq) * SQ + k + tq]), a1 = raw(s.Q[(r0 + gq + 8) * SQ + k + tq]);
+      const uint32_t a2 = raw(s.Q[(r0 + gq) * SQ + k + tq + 4]), a3 = raw(s.Q[(r0 + gq + 8) * SQ + k + tq + 4]);
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const int key = c0 + nt * 8 + gq;
-        const uint32_t b0 = tf32(s.KU[key * SQ + k + tq]), b1 = tf32(s.KU[key * SQ + k + tq + 4]);
+        const uint32_t b0 = raw(s.KU[key * SQ + k + tq]), b1 = raw(s.KU[key * SQ + k + tq + 4]);
         mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
       }
     }
@@ -510,7 +522,7 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int t = r0 + gq + (e >> 1) * 8, sidx = c0 + nt * 8 + 2 * tq + (e & 1);
-        s.P[t * SP + sidx] = (sidx <= t && t < n) ? __expf(s.g[t] - s.g[sidx]) * acc[nt][e] : 0.f;
+        s.P[t * SP + sidx] = (sidx <= t && t < n) ? rnd(__expf(s.g[t] - s.g[sidx]) * acc[nt][e]) : 0.f;
       }
     }
   }
@@ -528,12 +540,12 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
   const int cbase = (warp >> 2) * (D / 2);
 #pragma unroll 2
   for (int k = 0; k < D; k += 8) {
-    const uint32_t a0 = tf32(s.Q[(r0 + gq) * SQ + k + tq]), a1 = tf32(s.Q[(r0 + gq + 8) * SQ + k + tq]);
-    const uint32_t a2 = tf32(s.Q[(r0 + gq) * SQ + k + tq + 4]), a3 = tf32(s.Q[(r0 + gq + 8) * SQ + k + tq + 4]);
+    const uint32_t a0 = raw(s.Q[(r0 + gq) * SQ + k + tq]), a1 = raw(s.Q[(r0 + gq + 8) * SQ + k + tq]);
+    const uint32_t a2 = raw(s.Q[(r0 + gq) * SQ + k + tq + 4]), a3 = raw(s.Q[(r0 + gq + 8) * SQ + k + tq + 4]);
 #pragma unroll
     for (int nt = 0; nt < NTO; ++nt) {
       const int i = cbase + nt * 8 + gq;
-      const uint32_t b0 = tf32(s.S[i * SSC + k + tq]), b1 = tf32(s.S[i * SSC + k + tq + 4]);
+      const uint32_t b0 = raw(s.S[i * SSC + k + tq]), b1 = raw(s.S[i * SSC + k + tq + 4]);
       mma_tf32(o[nt], a0, a1, a2, a3, b0, b1);
     }
   }
@@ -547,12 +559,12 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
   // O += P U
 #pragma unroll 2
   for (int k = 0; k < C; k += 8) {
-    const uint32_t a0 = tf32(s.P[(r0 + gq) * SP + k + tq]), a1 = tf32(s.P[(r0 + gq + 8) * SP + k + tq]);
-    const uint32_t a2 = tf32(s.P[(r0 + gq) * SP + k + tq + 4]), a3 = tf32(s.P[(r0 + gq + 8) * SP + k + tq + 4]);
+    const uint32_t a0 = raw(s.P[(r0 + gq) * SP + k + tq]), a1 = raw(s.P[(r0 + gq + 8) * SP + k + tq]);
+    const uint32_t a2 = raw(s.P[(r0 + gq) * SP + k + tq + 4]), a3 = raw(s.P[(r0 + gq + 8) * SP + k + tq + 4]);
 #pragma unroll
     for (int nt = 0; nt < NTO; ++nt) {
       const int i = cbase + nt * 8 + gq;
-      const uint32_t b0 = tf32(s.KU[(k + tq) * SUo + i]), b1 = tf32(s.KU[(k + tq + 4) * SUo + i]);
+      const uint32_t b0 = raw(s.KU[(k + tq) * SUo + i]), b1 = raw(s.KU[(k + tq + 4) * SUo + i]);
       mma_tf32(o[nt], a0, a1, a2, a3, b0, b1);
     }
   }

@@ -32,6 +32,7 @@ namespace tc {
 
 constexpr int BM = 128, BK = 64;
 constexpr int NUM_THREADS = 192;
+constexpr int PF = 8;   // weight tiles are prefetched into L2 this many k blocks ahead
 constexpr uint64_t WAIT_NS = 1000000000ull;   // bounded wait: 1 s
 constexpr int ERR_TIMEOUT_FULL = 0x101, ERR_TIMEOUT_EMPTY = 0x102, ERR_TIMEOUT_TFULL = 0x103,
               ERR_TIMEOUT_TEMPTY = 0x104;
@@ -100,6 +101,12 @@ __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map
       "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
       : "memory");
+}
+// Hint: bring a box of the tensor into L2 ahead of its TMA load (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -242,7 +249,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int mt = mg * CM + crank;
         const int kb0 = sp * p.kb_per_split;
         const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        // the weight slice this CTA loads is fetched from DRAM into L2 PF blocks ahead
+        const int brow = nt * BN + (CM > 1 ? crank * SLICE : 0);
+        for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, brow);
         for (int kb = kb0; kb < kb1; ++kb) {
+          if (kb + PF < kb1) tma_prefetch_l2(&mapB, (kb + PF) * BK, brow);
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
           mbar_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_2d(sA + stage * C::A_BYTES, &mapA, &full[stage], kb * BK, mt * BM);
