@@ -37,6 +37,41 @@ __device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
                : "memory");
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// One contiguous global -> shared copy completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)));
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void bar_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// Bounded wait for the phase with the given parity; returns false after ~1 s (error recorded).
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, int* d_err) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    if (it == 0) t0 = t;
+    else if (t - t0 > 1000000000ull) {
+      if (d_err) atomicExch(d_err, 0x201);
+      return false;
+    }
+  }
+}
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
@@ -285,6 +320,7 @@ struct StateSmem {
   float S[BV * SS];
   float U[C * SU];      // U (TF32-rounded), written back for chunk_out
   float Us[C * SU];     // exp(g_n - g_t) U_t (TF32-rounded), A operand of the state update
+  uint64_t bar[NS];     // completion of each stage's bulk copies
 };
 
 // NS = 1 serves launches whose sequences have a single chunk (no prefetch needed, half the
@@ -297,7 +333,7 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
                                                           const ChunkDesc* __restrict__ chunks,
                                                           const CtxDesc* __restrict__ ctxs, int layer_g, int H,
                                                           const float* __restrict__ Wbuf, float* __restrict__ Ubuf,
-                                                          float* __restrict__ Schunk) {
+                                                          float* __restrict__ Schunk, int* __restrict__ d_err) {
   extern __shared__ __align__(16) uint8_t smraw[];
   using SM = StateSmem<D, NS>;
   constexpr int SW = SM::SW, SKK = SM::SKK, SS = SM::SS, SU = SM::SU;
@@ -316,41 +352,46 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
     s.S[r * SS + c] = S0 ? S0[(size_t)(v0 + r) * D + c] : 0.f;
   }
   const int nch = (sd.len + C - 1) / C;
+  if (tid == 0)
+    for (int i = 0; i < NS; ++i) bar_init(&s.bar[i]);
+  __syncthreads();
+  // Stage a chunk: bulk copies of its W, K and Ut rows (one thread per row) completing on the
+  // stage's mbarrier; rows past the chunk's end are zero-filled; g by plain loads.
   auto load = [&](int cl, int st) {
     const ChunkDesc cd = chunks[sd.chunk0 + cl];
-    for (int i = tid; i < C * (D / 4); i += NTH) {
-      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-      const bool ok = r < cd.len;
-      const int row = cd.row0 + (ok ? r : 0);
-      cp16(&s.W[st][r * SW + c4], Wbuf + ((size_t)row * H + h) * D + c4, ok);
-      cp16(&s.K[st][r * SKK + c4], proj + (size_t)row * ld + HDk + h * D + c4, ok);
+    constexpr uint32_t RB = D * 4, UB = BV * 4;
+    if (tid == 0) bar_expect(&s.bar[st], (uint32_t)cd.len * (2 * RB + UB));
+    if (tid < cd.len) {
+      const int row = cd.row0 + tid;
+      bulk_g2s(&s.W[st][tid * SW], Wbuf + ((size_t)row * H + h) * D, RB, &s.bar[st]);
+      bulk_g2s(&s.K[st][tid * SKK], proj + (size_t)row * ld + HDk + h * D, RB, &s.bar[st]);
+      bulk_g2s(&s.Ut[st][tid * BV], Ubuf + ((size_t)row * H + h) * D + v0, UB, &s.bar[st]);
     }
-    for (int i = tid; i < C * (BV / 4); i += NTH) {
-      const int r = i / (BV / 4), c4 = (i % (BV / 4)) * 4;
-      const bool ok = r < cd.len;
-      const int row = cd.row0 + (ok ? r : 0);
-      cp16(&s.Ut[st][r * BV + c4], Ubuf + ((size_t)row * H + h) * D + v0 + c4, ok);
+    for (int i = cd.len * D + tid; i < C * D; i += NTH) {
+      const int r = i / D, c = i % D;
+      s.W[st][r * SW + c] = 0.f;
+      s.K[st][r * SKK + c] = 0.f;
     }
-    if (tid < C) {
-      const bool ok = tid < cd.len;
-      s.g[st][tid] = ok ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
-    }
+    for (int i = cd.len * BV + tid; i < C * BV; i += NTH) s.Ut[st][i] = 0.f;
+    if (tid < C) s.g[st][tid] = tid < cd.len ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
   };
   if (nch > 0) load(0, 0);
-  cp_commit();
-  for (int cl = 0; cl < nch; ++cl) {
+  bool ok = true;
+  for (int cl = 0; cl < nch && ok; ++cl) {
     const int st = NS == 2 ? (cl & 1) : 0;
+    const uint32_t parity = NS == 2 ? ((cl >> 1) & 1) : (cl & 1);
     const ChunkDesc cd = chunks[sd.chunk0 + cl];
     if (NS == 2) {
       if (cl + 1 < nch) load(cl + 1, st ^ 1);
-      cp_commit();
-      cp_wait<1>();
-    } else {
-      if (cl > 0) load(cl, 0);   // single stage: the previous chunk's tiles are no longer read
-      cp_commit();
-      cp_wait<0>();
+    } else if (cl > 0) {
+      load(cl, 0);   // single stage: the previous chunk's tiles are no longer read
     }
-    __syncthreads();
+    ok = bar_wait(&s.bar[st], parity, d_err);
+    if (!__syncthreads_and(ok)) {
+      // a copy never completed: wait (bounded) for the prefetch issued this iteration, then stop
+      if (NS == 2 && cl + 1 < nch) bar_wait(&s.bar[st ^ 1], ((cl + 1) >> 1) & 1, d_err);
+      break;
+    }
     // record the chunk-start state block
     {
       float* dst = Schunk + ((size_t)(sd.chunk0 + cl) * H + h) * D * D + (size_t)v0 * D;
@@ -442,7 +483,7 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
     }
     __syncthreads();
   }
-  if (sd.ctx_out >= 0) {
+  if (ok && sd.ctx_out >= 0) {
     float* So = ctxs[sd.ctx_out].S + head_off;
     for (int i = tid; i < BV * D; i += NTH) {
       const int r = i / D, c = i % D;
@@ -591,15 +632,16 @@ bool gdn_chunked_supported(int H, int Dk, int Dv, int ld) {
 template <int D>
 static cudaError_t launch_state(const float* proj, int ld, const float* g, const SeqDesc* d_seq, int n_seq,
                                 const ChunkDesc* d_chunks, const CtxDesc* d_ctx, int layer_g, int H,
-                                const float* Wbuf, float* Ubuf, float* Schunk, int max_chunks, cudaStream_t st) {
+                                const float* Wbuf, float* Ubuf, float* Schunk, int max_chunks, int* d_err,
+                                cudaStream_t st) {
   if (n_seq <= 0) return cudaSuccess;
   const dim3 grid(n_seq, H, D / gc::BV);
   if (max_chunks <= 1) {
     gc::chunk_state_kernel<D, 1><<<grid, 256, sizeof(gc::StateSmem<D, 1>), st>>>(
-        proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk);
+        proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk, d_err);
   } else {
     gc::chunk_state_kernel<D, 2><<<grid, 256, sizeof(gc::StateSmem<D, 2>), st>>>(
-        proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk);
+        proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk, d_err);
   }
   return cudaGetLastError();
 }
@@ -609,7 +651,7 @@ static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const floa
                                     const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                     const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
                                     float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                                    cudaStream_t st) {
+                                    int* d_err, cudaStream_t st) {
   static bool attr = false;
   const size_t sp = sizeof(gc::PrepSmem<D>);
   const size_t so = sizeof(gc::OutSmem<D>);
@@ -630,11 +672,12 @@ static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const floa
   // sequences [0, n_first) run before the rest (the rest continue from their states)
   const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
   cudaError_t e = launch_state<D>(proj, ld, loga, d_seq, split, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk,
-                                  split < n_seq ? max_chunks_first : std::max(max_chunks_first, max_chunks_rest), st);
+                                  split < n_seq ? max_chunks_first : std::max(max_chunks_first, max_chunks_rest),
+                                  d_err, st);
   if (e != cudaSuccess) return e;
   if (split < n_seq) {
     e = launch_state<D>(proj, ld, loga, d_seq + split, n_seq - split, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf,
-                        Schunk, max_chunks_rest, st);
+                        Schunk, max_chunks_rest, d_err, st);
     if (e != cudaSuccess) return e;
   }
   gc::chunk_out_kernel<D><<<dim3(n_chunks, H), 256, so, st>>>(proj, ld, loga, d_chunks, H, Ubuf, Schunk, out);
@@ -645,17 +688,17 @@ cudaError_t launch_gdn_chunked(float* proj, int ld, float* loga, const float* be
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                               cudaStream_t st, long* launches) {
+                               int* d_err, cudaStream_t st, long* launches) {
   if (n_seq <= 0 || n_chunks <= 0) return cudaSuccess;
   if (!gdn_chunked_supported(H, Dk, Dv, ld)) return cudaErrorNotSupported;
   if (n_seq > 65535 || n_chunks > 2147483647 / 2) return cudaErrorInvalidValue;
   cudaError_t e = (Dk == 128)
                       ? launch_chunked_d<128>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                               layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
-                                              max_chunks_rest, st)
+                                              max_chunks_rest, d_err, st)
                       : launch_chunked_d<64>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                              layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
-                                             max_chunks_rest, st);
+                                             max_chunks_rest, d_err, st);
   if (launches) *launches += (n_first > 0 && n_first < n_seq) ? 4 : 3;
   return e;
 }

@@ -250,10 +250,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int kb0 = sp * p.kb_per_split;
         const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
         // the weight slice this CTA loads is fetched from DRAM into L2 PF blocks ahead
+        // (only the first m group of each n tile prefetches; the others run alongside it)
         const int brow = nt * BN + (CM > 1 ? crank * SLICE : 0);
-        for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, brow);
+        const bool pf = mg == 0;
+        if (pf)
+          for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, brow);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (kb + PF < kb1) tma_prefetch_l2(&mapB, (kb + PF) * BK, brow);
+          if (pf && kb + PF < kb1) tma_prefetch_l2(&mapB, (kb + PF) * BK, brow);
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
           mbar_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_2d(sA + stage * C::A_BYTES, &mapA, &full[stage], kb * BK, mt * BM);
@@ -339,6 +342,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             reinterpret_cast<uint4*>(o)[1] = reinterpret_cast<uint4*>(r)[1];
           }
         }
+      } else if (p.epi == EPI_RESADD) {
+        // residual add: the 64 residual values of a column group are loaded together before the
+        // accumulator chunks are read, so one memory latency covers four 16-column chunks
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 64) {
+          const int nc = (BN - c0) < 64 ? (BN - c0) / 16 : 4;   // 16-column chunks in this group
+          float4 xr[16];
+          float* xrow = reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n0 + c0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              xr[j * 4 + i] = (j < nc && row_ok && n0 + c0 + 16 * j < p.N)
+                                  ? reinterpret_cast<const float4*>(xrow + 16 * j)[i]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j < nc) {
+              float v[16];
+              tmem_ld16(tbase + c0 + 16 * j, v);
+              if (row_ok && n0 + c0 + 16 * j < p.N) {
+                float4* o = reinterpret_cast<float4*>(xrow + 16 * j);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float4 x = xr[j * 4 + i];
+                  o[i] = make_float4(x.x + v[4 * i], x.y + v[4 * i + 1], x.z + v[4 * i + 2], x.w + v[4 * i + 3]);
+                }
+              }
+            }
+          }
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 16) {
@@ -350,14 +384,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
 #pragma unroll
             for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          } else if (p.epi == EPI_RESADD) {
-            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float4 x = o[i];
-              x.x += v[4 * i]; x.y += v[4 * i + 1]; x.z += v[4 * i + 2]; x.w += v[4 * i + 3];
-              o[i] = x;
-            }
           } else if (p.epi == EPI_BF16) {
             __align__(16) bf16 r[16];
 #pragma unroll

@@ -104,11 +104,17 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
     float* W = (float*)t.get((size_t)R * H * dk * 4 + 16);
     float* U = (float*)t.get((size_t)R * H * dv * 4 + 16);
     float* Sc = (float*)t.get((size_t)(nch + 1) * per * 4);
-    if (!W || !U || !Sc) return op_fail(S1_ERR_OOM, "gdn: temporaries");
+    int* err = (int*)t.get(256);
+    if (!W || !U || !Sc || !err) return op_fail(S1_ERR_OOM, "gdn: temporaries");
+    OCK(cudaMemsetAsync(err, 0, 256, st));
     int maxc = 0;
     for (int q = 0; q < n_seq; ++q) maxc = std::max(maxc, (len[q] + GDN_CHUNK - 1) / GDN_CHUNK);
     OCK(launch_gdn_chunked(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
-                           0, maxc, maxc, st, nullptr));
+                           0, maxc, maxc, err, st, nullptr));
+    int herr = 0;
+    OCK(cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
+    OCK(cudaStreamSynchronize(st));
+    if (herr) return op_fail(S1_ERR_DEVICE_TIMEOUT, "gdn: a bounded device wait gave up");
   } else {
     OCK(launch_gdn_scan(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dctx, 0, H, dk, dv, st));
   }

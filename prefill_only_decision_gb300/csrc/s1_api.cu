@@ -390,7 +390,7 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
           }
           CK(launch_gdn_chunked(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
                                 mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first,
-                                mt.max_chunks_first, mt.max_chunks_rest, st, &m->launches));
+                                mt.max_chunks_first, mt.max_chunks_rest, m->d_err, st, &m->launches));
         } else {
           const int split = (mt.n_first > 0 && mt.n_first < nseq) ? mt.n_first : nseq;
           CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, split, mt.d_ctxs,
