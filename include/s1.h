@@ -204,6 +204,18 @@ int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, 
                             int32_t n_q, float* d_probs, float* d_stats, float* d_last_hidden);
 int s1_sync(s1_model* m);   /* waits for the stream; reports device-side timeouts */
 
+/* ---- prefix split (host only) ------------------------------------------------------------
+ * For callers that hold one whole token stream per question: the length P of the prefix the
+ * streams share, to be prefilled once (System1-Omni RFC #114, implementer's plan comment: the
+ * questions' longest common token prefix, cut at least one token before the end of every
+ * stream, runs once; the native split may sit at multiples of 64). P is the longest common
+ * prefix of the n streams, capped at (shortest length - min_suffix), then rounded down to a
+ * multiple of `align` when align > 1 (align = 64 matches the scan's chunk length). Writes P
+ * (>= 0) to *prefix_len. Errors: INVALID_ARG (n < 1, a NULL stream, min_suffix < 1, a stream
+ * shorter than min_suffix). No device work. */
+int s1_split_prefix(const int32_t* const* streams, const int32_t* lens, int32_t n, int32_t min_suffix,
+                    int32_t align, int32_t* prefix_len);
+
 const char* s1_last_error(void);
 const char* s1_version(void);
 

@@ -96,6 +96,7 @@ def lib():
         "s1_profile_read": (C.c_int, [vp, P(C.c_double), P(C.c_double), P(C.c_double), P(C.c_long)]),
         "s1_set_gemm_impl": (C.c_int, [vp, C.c_int]),
         "s1_counters": (C.c_int, [vp, P(C.c_longlong), P(C.c_longlong), P(C.c_longlong)]),
+        "s1_split_prefix": (C.c_int, [P(P(i32)), P(i32), i32, i32, i32, P(i32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -365,6 +366,16 @@ class State:
             self.close()
         except Exception:
             pass
+
+
+def split_prefix(streams, min_suffix: int = 1, align: int = 0) -> int:
+    """Length of the shared prefix of whole per-question token streams (s1_split_prefix)."""
+    arrs = [_i32(s) for s in streams]
+    sp = (C.POINTER(C.c_int32) * len(arrs))(*[_iptr(a) for a in arrs])
+    ln = (C.c_int32 * len(arrs))(*[len(a) for a in arrs])
+    out = C.c_int32()
+    check(lib().s1_split_prefix(sp, ln, len(arrs), min_suffix, align, C.byref(out)))
+    return out.value
 
 
 _ALLOC_T = C.CFUNCTYPE(C.c_void_p, C.c_size_t, C.c_void_p)

@@ -5,6 +5,7 @@
 // packed rows on one stream. A state (prefix snapshot) owns the per-layer gated
 // delta-rule states (fp32) and full-attention K/V (bf16, post-RoPE).
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -585,6 +586,28 @@ int build_prefill_meta(s1_model* m, int n_req, const int32_t* n_tokens, const in
 extern "C" {
 
 const char* s1_last_error(void) { return g_err.c_str(); }
+
+int s1_split_prefix(const int32_t* const* streams, const int32_t* lens, int32_t n, int32_t min_suffix,
+                    int32_t align, int32_t* prefix_len) {
+  if (n < 1 || !streams || !lens || !prefix_len) return fail(S1_ERR_INVALID_ARG, "split: bad arguments");
+  if (min_suffix < 1) return fail(S1_ERR_INVALID_ARG, "split: min_suffix must be >= 1");
+  int32_t cap = INT32_MAX;
+  for (int i = 0; i < n; ++i) {
+    if (!streams[i] || lens[i] < min_suffix) return fail(S1_ERR_INVALID_ARG, "split: stream %d shorter than min_suffix", i);
+    cap = std::min(cap, lens[i] - min_suffix);
+  }
+  int32_t P = 0;
+  while (P < cap) {
+    const int32_t t = streams[0][P];
+    bool same = true;
+    for (int i = 1; i < n && same; ++i) same = streams[i][P] == t;
+    if (!same) break;
+    ++P;
+  }
+  if (align > 1) P -= P % align;
+  *prefix_len = P;
+  return S1_OK;
+}
 const char* s1_version(void) { return "s1 0.1 (sm_103a)"; }
 
 int s1_set_allocator(void* (*alloc)(size_t, void*), void (*free_fn)(void*, void*), void* ctx) {
