@@ -105,7 +105,12 @@ typedef struct {
  * (ties -> lowest index). expected_score: sum_i i*p_i. yes_prob: p[0].
  * answer_confidence: max_i p_i. confidence: 1 - H(p)/ln(n) for choice/score,
  * answer_confidence for noul. entropy_confidence: 1 - H(p)/ln(n) for every type
- * (1 when n == 1). */
+ * (1 when n == 1). lm_logprobs: NULL, or caller-allocated [n_options] that receives each
+ * option token's log-probability under the full vocabulary at the readout row,
+ * z_o - log sum_v exp(z_v) over all vocab rows of the tied embedding (System1-Omni RFC #114,
+ * section 4 "Readout" and the LM-feature paragraph after its table); renormalising these over
+ * the options gives back probs. Requesting it for any question of a call streams the whole
+ * embedding once more (blocking calls only). */
 typedef struct {
   float* probs;
   int32_t argmax;
@@ -114,6 +119,7 @@ typedef struct {
   float answer_confidence;
   float confidence;
   float entropy_confidence;
+  float* lm_logprobs;
 } s1_result;
 
 /* Per-question statistics written by the stream-ordered decide (device floats). */

@@ -214,6 +214,24 @@ class Oracle:
         z = Eopt @ hn
         return decision(z, qtype)
 
+    def option_lm_logprobs(self, h_last, option_ids):
+        """Log-probability of each option token under the full vocabulary at the readout row.
+
+        log p(o) = z_o - log sum_v exp(z_v), z = E RMSNorm(h_last), E the tied embedding
+        (System1-Omni RFC #114, section 4 "Readout" row and the paragraph after the table: token
+        log-probabilities normalised over the full vocabulary; a further normalisation across the
+        candidates of a question gives back the option softmax). Returns (logprobs, lse).
+        """
+        hn = rmsnorm(h_last[None, :], upcast(self.W.final_norm, self.dt), self.s.rms_eps)[0]
+        V = self.W.embed.shape[0]
+        z = np.empty(V, dtype=np.float64)
+        step = 16384
+        for v0 in range(0, V, step):          # the full vocabulary, a block of rows at a time
+            z[v0:v0 + step] = upcast(self.W.embed[v0:v0 + step], self.dt) @ hn
+        m = z.max()
+        lse = float(m + np.log(np.sum(np.exp(z - m))))
+        return z[np.asarray(option_ids, dtype=np.int64)] - lse, lse
+
     def prefill(self, tokens, embeds=None):
         x0 = self.embed_rows(tokens, embeds)
         P = x0.shape[0]

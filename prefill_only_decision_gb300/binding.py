@@ -51,7 +51,7 @@ class Question(C.Structure):
 class Result(C.Structure):
     _fields_ = [("probs", C.POINTER(C.c_float)), ("argmax", C.c_int32), ("expected_score", C.c_float),
                 ("yes_prob", C.c_float), ("answer_confidence", C.c_float), ("confidence", C.c_float),
-                ("entropy_confidence", C.c_float)]
+                ("entropy_confidence", C.c_float), ("lm_logprobs", C.POINTER(C.c_float))]
 
 
 _lib = None
@@ -207,26 +207,13 @@ class Model:
         check(lib().s1_prefill_state_batch(self.h, n, tp, nt, ep, ne, out))
         return [State(self, C.c_void_p(out[i])) for i in range(n)]
 
-    def decide(self, state: "State", questions, want_hidden: bool = True):
-        res = self.decide_batch([state], [questions], want_hidden)
+    def decide(self, state: "State", questions, want_hidden: bool = True, want_lm: bool = False):
+        res = self.decide_batch([state], [questions], want_hidden, want_lm)
         return res[0]
 
-    def decide_batch(self, states, question_lists, want_hidden: bool = True):
+    def decide_batch(self, states, question_lists, want_hidden: bool = True, want_lm: bool = False):
         n = len(states)
-        keep, qarrs, rarrs, probs, hids = [], [], [], [], []
-        for qs in question_lists:
-            qa, k = make_questions(qs)
-            keep += k
-            qarrs.append(qa)
-            ra = (Result * len(qs))()
-            pl = []
-            for j, q in enumerate(qs):
-                p = np.zeros(len(q.option_ids), dtype=np.float32)
-                pl.append(p)
-                ra[j].probs = p.ctypes.data_as(C.POINTER(C.c_float))
-            probs.append(pl)
-            rarrs.append(ra)
-            hids.append(np.zeros((len(qs), self.shape.d_model), dtype=np.float32) if want_hidden else None)
+        keep, qarrs, rarrs, probs, hids = self._result_arrays(question_lists, want_hidden, want_lm)
         sp = (C.c_void_p * n)(*[s.h.value for s in states])
         qp = (C.POINTER(Question) * n)(*[C.cast(q, C.POINTER(Question)) for q in qarrs])
         nq = (C.c_int32 * n)(*[len(qs) for qs in question_lists])
@@ -234,19 +221,9 @@ class Model:
         hp = (C.POINTER(C.c_float) * n)(*[h.ctypes.data_as(C.POINTER(C.c_float)) if h is not None else None
                                            for h in hids]) if want_hidden else None
         check(lib().s1_decide_batch(self.h, n, sp, qp, nq, rp, hp))
-        out = []
-        for r in range(n):
-            lst = []
-            for j in range(len(question_lists[r])):
-                x = rarrs[r][j]
-                lst.append({"probs": probs[r][j], "argmax": x.argmax, "expected_score": x.expected_score,
-                            "yes_prob": x.yes_prob, "answer_confidence": x.answer_confidence,
-                            "confidence": x.confidence, "entropy_confidence": x.entropy_confidence,
-                            "hidden": hids[r][j] if want_hidden else None})
-            out.append(lst)
-        return out
+        return self._unpack(question_lists, rarrs, probs, hids, want_hidden)
 
-    def _result_arrays(self, question_lists, want_hidden):
+    def _result_arrays(self, question_lists, want_hidden, want_lm=False):
         keep, qarrs, rarrs, probs, hids = [], [], [], [], []
         for qs in question_lists:
             qa, k = make_questions(qs)
@@ -258,6 +235,10 @@ class Model:
                 p = np.zeros(len(q.option_ids), dtype=np.float32)
                 pl.append(p)
                 ra[j].probs = p.ctypes.data_as(C.POINTER(C.c_float))
+                if want_lm:
+                    lmv = np.zeros(len(q.option_ids), dtype=np.float32)
+                    keep.append(lmv)
+                    ra[j].lm_logprobs = lmv.ctypes.data_as(C.POINTER(C.c_float))
             probs.append(pl)
             rarrs.append(ra)
             hids.append(np.zeros((len(qs), self.shape.d_model), dtype=np.float32) if want_hidden else None)
@@ -270,24 +251,27 @@ class Model:
             lst = []
             for j in range(len(question_lists[r])):
                 x = rarrs[r][j]
+                n = len(question_lists[r][j].option_ids)
+                lm = np.ctypeslib.as_array(x.lm_logprobs, shape=(n,)).copy() if x.lm_logprobs else None
                 lst.append({"probs": probs[r][j], "argmax": x.argmax, "expected_score": x.expected_score,
                             "yes_prob": x.yes_prob, "answer_confidence": x.answer_confidence,
                             "confidence": x.confidence, "entropy_confidence": x.entropy_confidence,
-                            "hidden": hids[r][j] if want_hidden else None})
+                            "hidden": hids[r][j] if want_hidden else None, "lm_logprobs": lm})
             out.append(lst)
         return out
 
-    def prefill_decide(self, request, want_hidden: bool = True, keep_state: bool = False):
+    def prefill_decide(self, request, want_hidden: bool = True, keep_state: bool = False, want_lm: bool = False):
         """One sweep over prefix + questions (s1_prefill_decide). Returns (results, state or None)."""
-        res, sts = self.prefill_decide_batch([request], want_hidden, keep_state)
+        res, sts = self.prefill_decide_batch([request], want_hidden, keep_state, want_lm)
         return res[0], (sts[0] if sts else None)
 
-    def prefill_decide_batch(self, requests, want_hidden: bool = True, keep_state: bool = False):
+    def prefill_decide_batch(self, requests, want_hidden: bool = True, keep_state: bool = False,
+                             want_lm: bool = False):
         n = len(requests)
         toks = [_i32(r.tokens) for r in requests]
         embs = [None if r.embeds is None else np.ascontiguousarray(r.embeds, dtype=np.uint16) for r in requests]
         qls = [r.questions for r in requests]
-        keep, qarrs, rarrs, probs, hids = self._result_arrays(qls, want_hidden)
+        keep, qarrs, rarrs, probs, hids = self._result_arrays(qls, want_hidden, want_lm)
         tp = (C.POINTER(C.c_int32) * n)(*[_iptr(t) for t in toks])
         nt = (C.c_int32 * n)(*[len(t) for t in toks])
         ep = (C.c_void_p * n)(*[None if e is None else e.ctypes.data for e in embs])

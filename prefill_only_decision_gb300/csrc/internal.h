@@ -83,7 +83,10 @@ cudaError_t launch_attention(const bf16* q, const bf16* knew, const bf16* vnew, 
 cudaError_t launch_readout(const float* x, const float* final_norm, const bf16* E, int d, float eps,
                            const int* q_row, const int* q_type, const int* opt_off,
                            const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,
-                           int max_opts, cudaStream_t st);
+                           int max_opts, float* hn_out, float* z_out, cudaStream_t st);
+size_t vocab_lm_scratch_floats(int n_q, int n_opts, int d, int num_sms);
+cudaError_t launch_vocab_lm(const bf16* E, int V, int d, const float* hn, const float* z, const int* opt_off, int n_q,
+                            float* lm, float* scratch, int num_sms, cudaStream_t st, long* launches);
 cudaError_t launch_merge_lora(const void* W, int w_is_bf16, const void* A, const void* B,
                               int ab_is_bf16, int rank, float scale, int out_f, int in_f,
                               bf16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,

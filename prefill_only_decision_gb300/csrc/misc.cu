@@ -140,7 +140,8 @@ __global__ void readout_kernel(const float* __restrict__ x, const float* __restr
                                const int* __restrict__ q_row, const int* __restrict__ q_type,
                                const int* __restrict__ opt_off, const int* __restrict__ opt_ids,
                                float* __restrict__ probs, float* __restrict__ stats,
-                               float* __restrict__ hidden) {
+                               float* __restrict__ hidden, float* __restrict__ hn_out,
+                               float* __restrict__ z_out) {
   extern __shared__ float sm[];
   float* hn = sm;            // [d]
   float* z = sm + d;         // [n]
@@ -157,7 +158,10 @@ __global__ void readout_kernel(const float* __restrict__ x, const float* __restr
   }
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)d + eps);
-  for (int i = threadIdx.x; i < d; i += blockDim.x) hn[i] = h[i] * inv * fnorm[i];
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    hn[i] = h[i] * inv * fnorm[i];
+    if (hn_out) hn_out[(size_t)j * d + i] = hn[i];
+  }
   __syncthreads();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int m = w; m < n; m += nw) {
@@ -165,7 +169,10 @@ __global__ void readout_kernel(const float* __restrict__ x, const float* __restr
     float acc = 0.f;
     for (int i = lane; i < d; i += 32) acc += hn[i] * bf2f(e[i]);
     acc = warp_sum(acc);
-    if (lane == 0) z[m] = acc;
+    if (lane == 0) {
+      z[m] = acc;
+      if (z_out) z_out[o0 + m] = acc;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -201,11 +208,11 @@ __global__ void readout_kernel(const float* __restrict__ x, const float* __restr
 cudaError_t launch_readout(const float* x, const float* final_norm, const bf16* E, int d, float eps,
                            const int* q_row, const int* q_type, const int* opt_off,
                            const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,
-                           int max_opts, cudaStream_t st) {
+                           int max_opts, float* hn_out, float* z_out, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   const size_t smem = (size_t)(d + max_opts) * sizeof(float);
   readout_kernel<<<n_q, 256, smem, st>>>(x, final_norm, E, d, eps, q_row, q_type, opt_off, opt_ids,
-                                         probs, stats, hidden);
+                                         probs, stats, hidden, hn_out, z_out);
   return cudaGetLastError();
 }
 

@@ -121,6 +121,8 @@ struct s1_model {
   int max_pos = 0;
   int* d_err = nullptr;
   Scratch sc;
+  float* lm_buf = nullptr;     // full-vocabulary option log-probabilities: lm | z | h_hat | partials
+  size_t lm_floats = 0;
   float* schunk = nullptr;     // chunk-start states of the chunked scan [chunks, H, dv, dk]
   size_t schunk_chunks = 0;
   bool gdn_token = false;      // S1_GDN=token: token-by-token scan (debugging)
@@ -353,7 +355,7 @@ int gemm(s1_model* m, const bf16* X, const bf16* W, int M, int N, int K, int epi
 // One forward pass over the packed rows described by `mt` (metadata already uploaded):
 // input rows, every decoder layer, and (if questions are present) the readout.
 int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float* stats,
-                float* hidden) {
+                float* hidden, bool want_lm = false) {
   const s1_shape& s = m->sh;
   const int R = (int)mt.row_src.size();
   const int nseq = (int)mt.seqs.size();
@@ -384,6 +386,7 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
           if ((size_t)nch > m->schunk_chunks) {
             CK(cudaStreamSynchronize(st));
             dfree(m->schunk);
+  dfree(m->lm_buf);
             const size_t cap = std::max<size_t>(nch, 2 * m->schunk_chunks);
             m->schunk = (float*)dalloc(cap * H * (size_t)s.la_dv * s.la_dk * 4);
             m->schunk_chunks = m->schunk ? cap : 0;
@@ -431,9 +434,26 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
   const int nq = (int)mt.q_row.size();
   if (nq > 0) {
     ProfScope ps(m, S1_PROF_OTHER, 0, 0);
+    float *hn = nullptr, *z = nullptr;
+    const int no = (int)mt.opt_ids.size();
+    if (want_lm) {
+      const size_t need = (size_t)no + vocab_lm_scratch_floats(nq, no, d, m->num_sms);
+      if (need > m->lm_floats) {
+        CK(cudaStreamSynchronize(st));
+        dfree(m->lm_buf);
+        m->lm_buf = (float*)dalloc(need * 4);
+        m->lm_floats = m->lm_buf ? need : 0;
+        if (!m->lm_buf) return fail(S1_ERR_OOM, "log-probability scratch allocation failed");
+      }
+      z = m->lm_buf + no;
+      hn = z + no;
+    }
     CK(launch_readout(sc.x, m->final_norm, m->embed, d, s.rms_eps, mt.d_q_row, mt.d_q_type,
-                      mt.d_opt_off, mt.d_opt_ids, nq, probs, stats, hidden, mt.max_opts, st));
+                      mt.d_opt_off, mt.d_opt_ids, nq, probs, stats, hidden, mt.max_opts, hn, z, st));
     m->launches += 1;
+    if (want_lm)
+      CK(launch_vocab_lm(m->embed, s.vocab, d, hn, z, mt.d_opt_off, nq, m->lm_buf, hn + (size_t)nq * d,
+                         m->num_sms, st, &m->launches));
   }
   return S1_OK;
 }
@@ -818,6 +838,7 @@ void s1_model_destroy(s1_model* m) {
   dfree(m->rope_tab);
   dfree(m->d_err);
   dfree(m->schunk);
+  dfree(m->lm_buf);
   if (m->pinned) cudaFreeHost(m->pinned);
   if (m->meta_done) cudaEventDestroy(m->meta_done);
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
@@ -971,8 +992,22 @@ static int decide_impl(s1_model* m, int n_req, const s1_state* const* states, co
 
 // Copies the readout outputs (probs | stats | hidden in the scratch output block) back into
 // the caller's result structs. Blocking.
+static bool wants_lm(int n_req, const int32_t* n_q, s1_result* const* out) {
+  for (int r = 0; r < n_req; ++r)
+    for (int j = 0; j < n_q[r]; ++j)
+      if (out[r] && out[r][j].lm_logprobs) return true;
+  return false;
+}
+
 static int fetch_results(s1_model* m, int n_req, const s1_question* const* qs, const int32_t* n_q, int NQ, int NO,
                          bool want_hidden, s1_result* const* out, float* const* last_hidden) {
+  std::vector<float> lmh;
+  const bool want_lm = wants_lm(n_req, n_q, out);
+  if (want_lm) {
+    lmh.resize(NO);
+    CK(cudaMemcpyAsync(lmh.data(), m->lm_buf, (size_t)NO * 4, cudaMemcpyDeviceToHost, m->stream));
+    m->d2h_bytes += (long long)NO * 4;
+  }
   float* probs = m->sc.out;
   float* stats = probs + align_up(NO, 64);
   float* hidden = stats + align_up((size_t)NQ * S1_STAT_COUNT, 64);
@@ -1000,6 +1035,7 @@ static int fetch_results(s1_model* m, int n_req, const s1_question* const* qs, c
       res.entropy_confidence = sv[S1_STAT_ENTROPY_CONF];
       if (want_hidden && last_hidden[r])
         memcpy(last_hidden[r] + (size_t)j * m->sh.d_model, hh + (size_t)qi * m->sh.d_model, m->sh.d_model * 4);
+      if (want_lm && res.lm_logprobs) memcpy(res.lm_logprobs, lmh.data() + oi, n * 4);
       oi += n;
     }
   return S1_OK;
@@ -1028,7 +1064,7 @@ int s1_decide_batch(s1_model* m, int32_t n_req, const s1_state* const* states, c
     for (int r = 0; r < n_req; ++r) want_hidden |= (last_hidden[r] != nullptr);
   rc = upload_meta(m, mt);
   if (rc) return rc;
-  rc = run_forward(m, mt, nullptr, probs, stats, want_hidden ? hidden : nullptr);
+  rc = run_forward(m, mt, nullptr, probs, stats, want_hidden ? hidden : nullptr, wants_lm(n_req, n_q, out));
   if (rc) return rc;
   return fetch_results(m, n_req, qs, n_q, NQ, NO, want_hidden, out, last_hidden);
 }
@@ -1056,7 +1092,7 @@ int s1_decide_async(s1_model* m, const s1_state* st, const s1_question* qs_dev, 
 static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, const int32_t* n_tokens,
                       const void* const* embeds, const int32_t* n_embeds, s1_state* const* states,
                       const s1_question* const* qs, const int32_t* n_q, bool device_ptrs, float* d_probs,
-                      float* d_stats, float* d_hidden, int* NQ_out, int* NO_out) {
+                      float* d_stats, float* d_hidden, int* NQ_out, int* NO_out, bool want_lm = false) {
   int Rp = 0, Rs = 0, NQ = 0, NO = 0, NE = 0;
   for (int r = 0; r < n_req; ++r) {
     const int P = n_tokens[r] + n_embeds[r];
@@ -1147,7 +1183,7 @@ static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, cons
       eoff += n_embeds[r] * rowb;
     }
   }
-  rc = run_forward(m, mt, m->sc.xn, d_probs, d_stats, d_hidden);
+  rc = run_forward(m, mt, m->sc.xn, d_probs, d_stats, d_hidden, want_lm);
   if (rc) return rc;
   for (int r = 0; r < n_req; ++r) states[r]->P = n_tokens[r] + n_embeds[r];
   *NQ_out = NQ;
@@ -1199,7 +1235,7 @@ int s1_prefill_decide_batch(s1_model* m, int32_t n_req, const int32_t* const* to
   float *probs, *stats, *hidden;
   output_slots(m, nq_tot, no_tot, &probs, &stats, &hidden);
   rc = fused_impl(m, n_req, tokens, n_tokens, embeds, ne.data(), sts.data(), qs, n_q, false, probs, stats,
-                  want_hidden ? hidden : nullptr, &NQ, &NO);
+                  want_hidden ? hidden : nullptr, &NQ, &NO, wants_lm(n_req, n_q, out));
   if (!rc) rc = fetch_results(m, n_req, qs, n_q, NQ, NO, want_hidden, out, last_hidden);
   if (rc) return cleanup(rc);
   for (int r = 0; r < n_req; ++r) {

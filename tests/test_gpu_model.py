@@ -310,3 +310,21 @@ def test_small_fused_batch_vs_oracle(B):
     o = om.Oracle(W, np.float32)
     for i in (0, 9, 15):
         compare(gpu[i], o.decide(reqs[i], branched=True), reqs[i].questions, f"small fused {i}")
+
+
+# -- full-vocabulary option log-probabilities --------------------------------------------------
+def test_tiny_lm_logprobs_vs_oracle(tiny, tiny_weights, tiny_requests):
+    r = tiny_requests[0]
+    st = tiny.prefill(r.tokens)
+    gpu = tiny.decide(st, r.questions, want_lm=True)
+    fused, _ = tiny.prefill_decide(r, want_lm=True)
+    o = om.Oracle(tiny_weights, np.float32)
+    ref = o.decide(r, branched=True)
+    from scipy.special import logsumexp
+    for g, f, rr, q in zip(gpu, fused, ref, r.questions):
+        lp_ref, _ = o.option_lm_logprobs(rr["hidden"], q.option_ids)
+        assert np.abs(g["lm_logprobs"] - lp_ref).max() < 5e-2
+        assert np.abs(f["lm_logprobs"] - lp_ref).max() < 5e-2
+        # renormalised over the options they give back the option probabilities
+        np.testing.assert_allclose(np.exp(g["lm_logprobs"] - logsumexp(g["lm_logprobs"])), g["probs"], atol=1e-4)
+        assert np.all(g["lm_logprobs"] < 0)

@@ -212,3 +212,22 @@ def test_readout_invariants():
     assert abs(om.decision(np.zeros(7), 0)["confidence"]) < 1e-12
     # ties -> lowest index
     assert om.decision(np.array([1.0, 3.0, 3.0]), 0)["argmax"] == 1
+
+
+# -- full-vocabulary option log-probabilities ------------------------------------------------
+def test_lm_logprobs_vs_library_and_candidate_renormalisation(tiny_weights):
+    from scipy.special import logsumexp
+    o = om.Oracle(tiny_weights, np.float64)
+    g = np.random.default_rng(13)
+    h = g.standard_normal(256) * 3
+    opts = np.array([17, 400, 4095, 1000], dtype=np.int32)
+    lp, lse = o.option_lm_logprobs(h, opts)
+    E = om.upcast(tiny_weights.embed, np.float64)
+    hn = om.rmsnorm(h[None], np.ones(256), 1e-6)[0]
+    z = E @ hn
+    assert abs(lse - logsumexp(z)) < 1e-10
+    np.testing.assert_allclose(lp, z[opts] - logsumexp(z), atol=1e-10)
+    assert np.all(lp < 0) and np.exp(lp).sum() < 1
+    # renormalising over the candidates gives back the option softmax of the readout
+    r = o.readout(h, 0, opts)
+    np.testing.assert_allclose(np.exp(lp - logsumexp(lp)), r["probs"], atol=1e-12)
