@@ -38,40 +38,6 @@ __device__ __forceinline__ void cp16(void* dst, const void* src, bool valid) {
 }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
-// One contiguous global -> shared copy completing `bytes` on the mbarrier.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void bar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)));
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void bar_expect(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-// Bounded wait for the phase with the given parity; returns false after ~1 s (error recorded).
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, int* d_err) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    if (it == 0) t0 = t;
-    else if (t - t0 > 1000000000ull) {
-      if (d_err) atomicExch(d_err, 0x201);
-      return false;
-    }
-  }
-}
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
@@ -320,7 +286,6 @@ struct StateSmem {
   float S[BV * SS];
   float U[C * SU];      // U (TF32-rounded), written back for chunk_out
   float Us[C * SU];     // exp(g_n - g_t) U_t (TF32-rounded), A operand of the state update
-  uint64_t bar[NS];     // completion of each stage's bulk copies
 };
 
 // NS = 1 serves launches whose sequences have a single chunk (no prefetch needed, half the
@@ -352,46 +317,39 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
     s.S[r * SS + c] = S0 ? S0[(size_t)(v0 + r) * D + c] : 0.f;
   }
   const int nch = (sd.len + C - 1) / C;
-  if (tid == 0)
-    for (int i = 0; i < NS; ++i) bar_init(&s.bar[i]);
-  __syncthreads();
-  // Stage a chunk: bulk copies of its W, K and Ut rows (one thread per row) completing on the
-  // stage's mbarrier; rows past the chunk's end are zero-filled; g by plain loads.
   auto load = [&](int cl, int st) {
     const ChunkDesc cd = chunks[sd.chunk0 + cl];
-    constexpr uint32_t RB = D * 4, UB = BV * 4;
-    if (tid == 0) bar_expect(&s.bar[st], (uint32_t)cd.len * (2 * RB + UB));
-    if (tid < cd.len) {
-      const int row = cd.row0 + tid;
-      bulk_g2s(&s.W[st][tid * SW], Wbuf + ((size_t)row * H + h) * D, RB, &s.bar[st]);
-      bulk_g2s(&s.K[st][tid * SKK], proj + (size_t)row * ld + HDk + h * D, RB, &s.bar[st]);
-      bulk_g2s(&s.Ut[st][tid * BV], Ubuf + ((size_t)row * H + h) * D + v0, UB, &s.bar[st]);
+    for (int i = tid; i < C * (D / 4); i += NTH) {
+      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+      const bool okr = r < cd.len;
+      const int row = cd.row0 + (okr ? r : 0);
+      cp16(&s.W[st][r * SW + c4], Wbuf + ((size_t)row * H + h) * D + c4, okr);
+      cp16(&s.K[st][r * SKK + c4], proj + (size_t)row * ld + HDk + h * D + c4, okr);
     }
-    for (int i = cd.len * D + tid; i < C * D; i += NTH) {
-      const int r = i / D, c = i % D;
-      s.W[st][r * SW + c] = 0.f;
-      s.K[st][r * SKK + c] = 0.f;
+    for (int i = tid; i < C * (BV / 4); i += NTH) {
+      const int r = i / (BV / 4), c4 = (i % (BV / 4)) * 4;
+      const bool okr = r < cd.len;
+      const int row = cd.row0 + (okr ? r : 0);
+      cp16(&s.Ut[st][r * BV + c4], Ubuf + ((size_t)row * H + h) * D + v0 + c4, okr);
     }
-    for (int i = cd.len * BV + tid; i < C * BV; i += NTH) s.Ut[st][i] = 0.f;
     if (tid < C) s.g[st][tid] = tid < cd.len ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
   };
   if (nch > 0) load(0, 0);
-  bool ok = true;
-  for (int cl = 0; cl < nch && ok; ++cl) {
+  cp_commit();
+  const bool ok = true;
+  for (int cl = 0; cl < nch; ++cl) {
     const int st = NS == 2 ? (cl & 1) : 0;
-    const uint32_t parity = NS == 2 ? ((cl >> 1) & 1) : (cl & 1);
     const ChunkDesc cd = chunks[sd.chunk0 + cl];
     if (NS == 2) {
       if (cl + 1 < nch) load(cl + 1, st ^ 1);
-    } else if (cl > 0) {
-      load(cl, 0);   // single stage: the previous chunk's tiles are no longer read
+      cp_commit();
+      cp_wait<1>();
+    } else {
+      if (cl > 0) load(cl, 0);   // single stage: the previous chunk's tiles are no longer read
+      cp_commit();
+      cp_wait<0>();
     }
-    ok = bar_wait(&s.bar[st], parity, d_err);
-    if (!__syncthreads_and(ok)) {
-      // a copy never completed: wait (bounded) for the prefetch issued this iteration, then stop
-      if (NS == 2 && cl + 1 < nch) bar_wait(&s.bar[st ^ 1], ((cl + 1) >> 1) & 1, d_err);
-      break;
-    }
+    __syncthreads();
     // record the chunk-start state block
     {
       float* dst = Schunk + ((size_t)(sd.chunk0 + cl) * H + h) * D * D + (size_t)v0 * D;

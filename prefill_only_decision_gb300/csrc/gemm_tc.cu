@@ -510,6 +510,12 @@ inline int cluster_m(int m_tiles, int bn) {
 
 inline int max_clusters_of(int bn, int cm, int num_sms);
 
+// The plan of a fixed tile width and cluster size without a K split.
+inline Plan plan_with(int M, int N, int K, int bn, int cm) {
+  const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + bn - 1) / bn, kb = K / BK;
+  return Plan{bn, m_tiles, n_tiles, 1, kb, kb, m_tiles * n_tiles, 0, cm};
+}
+
 // Choose the N tile, the K split and the cluster size together: minimise
 // (waves of cluster units) x (k blocks per unit) x (per-k-block cost of the tile), where a
 // cluster unit is CM m tiles (padding tiles when CM does not divide the m-tile count cost
@@ -645,11 +651,8 @@ size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms) {
   return (size_t)2 * (num_sms > 0 ? num_sms : 160) * tc::BM * 256;
 }
 
-cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
-                           float* splitk_ws, size_t ws_floats, const LaunchCtx& lc) {
-  if (M == 0) return cudaSuccess;
-  if (!gemm_tc_supported(M, N, K, epi)) return cudaErrorInvalidValue;
-  const tc::Plan pl = tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
+static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, int epi,
+                               void* out, int ldo, float* splitk_ws, const LaunchCtx& lc) {
   const int cm = pl.cm;
   CUtensorMap ma, mb;
   if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, pl.bn / cm)) return cudaErrorInvalidValue;
@@ -677,6 +680,88 @@ cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, in
                                                            out, ldo);
   if (lc.launches) *lc.launches += 1;
   return cudaGetLastError();
+}
+
+namespace tc {
+// Measured choice of (BN, CM) per GEMM shape for plans without a K split. Every such plan
+// accumulates each output over K in the same order, so the choice never changes results.
+std::mutex g_tune_mu;
+std::map<std::tuple<int, int, int, int, int>, std::pair<int, int>> g_tuned;
+
+bool tune_enabled() {
+  const char* e = getenv("S1_GEMM_TUNE");
+  return !(e && e[0] == '0');
+}
+
+// Times every (BN, CM) candidate twice on the caller's stream (tuning output `scratch`,
+// RESADD shapes tuned with a plain fp32 store of the same size) and keeps the fastest.
+cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
+                 const LaunchCtx& lc) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, M, N, K, epi);
+  {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    auto it = g_tuned.find(key);
+    if (it != g_tuned.end()) {
+      pl = plan_with(M, N, K, it->second.first, it->second.second);
+      return cudaSuccess;
+    }
+  }
+  const bool resadd = epi == EPI_RESADD;
+  void* tout = resadd ? lc.tune_out : out;
+  const int tldo = resadd ? N : ldo;
+  const int tepi = resadd ? EPI_F32 : epi;
+  if (!tout || (resadd && (size_t)M * N > lc.tune_floats)) return cudaSuccess;   // keep the heuristic plan
+  LaunchCtx l2 = lc;
+  l2.launches = nullptr;
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess) return cudaGetLastError();
+  if (cudaEventCreate(&e1) != cudaSuccess) { cudaEventDestroy(e0); return cudaGetLastError(); }
+  float best = 1e30f;
+  int bbn = pl.bn, bcm = pl.cm;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int bns[4] = {256, 192, 144, 128};
+  cudaError_t err = cudaSuccess;
+  for (int bn : bns) {
+    if (epi == EPI_SWIGLU && (bn % 32)) continue;
+    for (int cm = 1; cm <= 4 && err == cudaSuccess; cm *= 2) {
+      if ((bn == 144 && cm == 4) || (cm > 1 && m_tiles < 2)) continue;
+      const Plan cand = plan_with(M, N, K, bn, cm);
+      float t = 1e30f;
+      for (int rep = 0; rep < 3 && err == cudaSuccess; ++rep) {
+        cudaEventRecord(e0, lc.stream);
+        err = launch_plan(cand, X, W, M, N, K, tepi, tout, tldo, nullptr, l2);
+        cudaEventRecord(e1, lc.stream);
+        if (err == cudaSuccess) err = cudaEventSynchronize(e1);
+        float ms = 0.f;
+        if (err == cudaSuccess && rep > 0 && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) t = std::min(t, ms);
+      }
+      if (t < best) { best = t; bbn = bn; bcm = cm; }
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (err != cudaSuccess) return err;
+  {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    g_tuned[key] = std::make_pair(bbn, bcm);
+  }
+  pl = plan_with(M, N, K, bbn, bcm);
+  return cudaSuccess;
+}
+}  // namespace tc
+
+cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
+                           float* splitk_ws, size_t ws_floats, const LaunchCtx& lc) {
+  if (M == 0) return cudaSuccess;
+  if (!gemm_tc_supported(M, N, K, epi)) return cudaErrorInvalidValue;
+  tc::Plan pl = tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
+  if (pl.splits == 1 && lc.tune && tc::tune_enabled() && !getenv("S1_GEMM_CM")) {
+    cudaError_t e = tc::tune(pl, X, W, M, N, K, epi, out, ldo, lc);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_plan(pl, X, W, M, N, K, epi, out, ldo, splitk_ws, lc);
 }
 
 }  // namespace s1

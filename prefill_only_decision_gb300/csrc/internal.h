@@ -48,6 +48,9 @@ struct LaunchCtx {
   int* d_err;        // device error word (bounded waits record here)
   int num_sms;
   long* launches;    // incremented per kernel launched (may be NULL)
+  bool tune = false;          // GEMM: measure the tile / cluster choice on first use of a shape
+  void* tune_out = nullptr;   // GEMM tuning: scratch output for residual-add shapes (fp32)
+  size_t tune_floats = 0;
 };
 
 // ---- kernels (launchers) ----

@@ -344,6 +344,11 @@ int gemm(s1_model* m, const bf16* X, const bf16* W, int M, int N, int K, int epi
   ProfScope ps(m, S1_PROF_GEMM, 2.0 * M * N * K, (double)N * K * 2 + (double)M * K * 2);
   if (m->gemm_impl == 0 && !m->force_simt && gemm_tc_supported(M, N, K, epi)) {
     LaunchCtx lc{m->stream, m->d_err, m->num_sms, &m->launches};
+    // the projection buffer is free whenever a residual-add GEMM runs (its contents were
+    // consumed by the layer's mixer), so it serves as the tuning output of those shapes
+    lc.tune = !m->prof;
+    lc.tune_out = m->sc.proj;
+    lc.tune_floats = (size_t)m->sc.rows * m->n_proj;
     CK(launch_gemm_tc(X, W, M, N, K, epi, out, ldo, m->sc.ws, m->sc.ws_floats, lc));
   } else {
     CK(launch_gemm_simt(X, W, M, N, K, epi, out, ldo, m->stream));

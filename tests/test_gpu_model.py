@@ -54,6 +54,7 @@ def compare(gpu, ref, qs, tag=""):
         assert abs(g["confidence"] - r["confidence"]) <= 5e-2
         worst["p"] = max(worst["p"], p_err)
         worst["e"] = max(worst["e"], e_err)
+    print(f"[parity {tag}] max |dp| {worst['p']:.2e}  max |dE| {worst['e']:.2e}  max hidden rel L2 {worst['h']:.2e}")
     return worst
 
 
