@@ -46,6 +46,17 @@ _FA_IDX = {"q": 1, "k": 2, "v": 3, "o": 4, "gate": 6, "up": 7, "down": 8}
 _TARGETS = ("q", "k", "v", "o", "gate", "up", "down")
 
 
+def round_bf16(x):
+    """Round to the nearest bf16 value (ties to even) and return it as float32.
+
+    bf16 keeps the top 16 bits of an IEEE float32; rounding adds half of the dropped range
+    (0x7FFF, plus one when the kept part is odd) before truncating.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16 << 16
+    return u.astype(np.uint32).view(np.float32)
+
+
 def upcast(w, dt):
     """Weights as stored (float32, or bf16 bit patterns in uint16) -> dt."""
     if w is None:
@@ -113,10 +124,21 @@ class LayerCache:
 
 
 class Oracle:
-    def __init__(self, weights, dtype=np.float32):
+    """precision="fp32": every step in dt, LoRA unmerged (the author's-reference semantics).
+    precision="bf16": the pages' BF16 backbone policy (System1-Omni issue #10, the fast path's
+    "bfloat16 ... float32 head"; RFC #114 section 2 "Start with BF16 CUDA inference" and section 3
+    on merging the adapter): the LoRA delta is merged into each weight at load in fp32 and the
+    merged weight rounded once to bf16, and every matrix-product input (normed rows, mixer
+    output, SwiGLU output) is rounded to bf16; accumulation, the recurrent state, attention
+    softmax, residual stream and the readout stay fp32."""
+
+    def __init__(self, weights, dtype=np.float32, precision="fp32"):
         self.W = weights
         self.s = weights.shape
         self.dt = np.dtype(dtype)
+        if precision not in ("fp32", "bf16"):
+            raise ValueError(precision)
+        self.bf16 = precision == "bf16"
         self.full = list(self.s.layer_is_full)
         r = self.s.lora_rank
         self.lora_scale = (self.s.lora_alpha / r) if r > 0 else 0.0
@@ -133,8 +155,16 @@ class Oracle:
             j = _TARGETS.index(target_or_idx)
         else:
             idx, j = target_or_idx, None
+        has_lora = j is not None and self.s.lora_rank > 0 and self.W.lora_a[l][j] is not None
+        if self.bf16:
+            Wm = self._w(l, idx)
+            if has_lora:
+                A = upcast(self.W.lora_a[l][j], self.dt)
+                B = upcast(self.W.lora_b[l][j], self.dt)
+                Wm = Wm + self.dt.type(self.lora_scale) * (B @ A)
+            return round_bf16(x).astype(self.dt) @ round_bf16(Wm).astype(self.dt).T
         y = x @ self._w(l, idx).T
-        if j is not None and self.s.lora_rank > 0 and self.W.lora_a[l][j] is not None:
+        if has_lora:
             A = upcast(self.W.lora_a[l][j], self.dt)
             B = upcast(self.W.lora_b[l][j], self.dt)
             y = y + self.dt.type(self.lora_scale) * ((x @ A.T) @ B.T)
@@ -154,8 +184,9 @@ class Oracle:
         q = self.linear(xn, l, "q").reshape(T, H, Dk)
         k = self.linear(xn, l, "k").reshape(T, H, Dk)
         v = self.linear(xn, l, "v").reshape(T, H, Dv)
-        a = xn @ self._w(l, 4).T
-        b = xn @ self._w(l, 5).T
+        xa = round_bf16(xn).astype(self.dt) if self.bf16 else xn
+        a = xa @ self._w(l, 4).T
+        b = xa @ self._w(l, 5).T
         q = gdn.l2norm(q, s.l2_eps)
         k = gdn.l2norm(k, s.l2_eps)
         alpha, beta = gdn.gates(a, b)
@@ -171,6 +202,8 @@ class Oracle:
         q = rope(self.linear(xn, l, "q").reshape(T, Hq, hd), pos, s.rope_theta)
         k = rope(self.linear(xn, l, "k").reshape(T, Hkv, hd), pos, s.rope_theta)
         v = self.linear(xn, l, "v").reshape(T, Hkv, hd)
+        if self.bf16:   # attention operands and the cached K/V are stored in bf16 by the policy
+            q, k, v = (round_bf16(t).astype(self.dt) for t in (q, k, v))
         if cache is not None:
             K = np.concatenate([cache.K, k]); V = np.concatenate([cache.V, v])
             kp = np.concatenate([cache.pos, pos])
@@ -181,6 +214,7 @@ class Oracle:
         return y, LayerCache(K=K, V=V, pos=kp)
 
     def mlp(self, l, xn):
+        # (in bf16 mode, `linear` rounds the SwiGLU output like every other product input)
         return self.linear(silu(self.linear(xn, l, "gate")) * self.linear(xn, l, "up"), l, "down")
 
     # -- forward ------------------------------------------------------------

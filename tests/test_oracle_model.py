@@ -231,3 +231,34 @@ def test_lm_logprobs_vs_library_and_candidate_renormalisation(tiny_weights):
     # renormalising over the candidates gives back the option softmax of the readout
     r = o.readout(h, 0, opts)
     np.testing.assert_allclose(np.exp(lp - logsumexp(lp)), r["probs"], atol=1e-12)
+
+
+# -- the bf16 backbone policy mode ------------------------------------------------------------
+def test_round_bf16_vs_torch():
+    g = np.random.default_rng(21)
+    x = np.concatenate([g.standard_normal(10000) * 10.0 ** g.integers(-6, 6, 10000),
+                        np.array([1.0, 1.00390625, 1.01171875, -2.5, 0.0, 65504.0])]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(om.round_bf16(x), ref)
+
+
+def test_bf16_policy_rounds_only_product_inputs(tiny_weights):
+    """Exact bf16 inputs and weights: the bf16 mode equals the fp32 mode exactly; otherwise the
+    product equals the fp32 product of the rounded operands."""
+    o32 = om.Oracle(tiny_weights, np.float32)
+    o16 = om.Oracle(tiny_weights, np.float32, precision="bf16")
+    g = np.random.default_rng(22)
+    xb = om.round_bf16(g.standard_normal((6, 256)))
+    W = om.round_bf16(tiny_weights.layers[0][1])
+    np.testing.assert_array_equal(o16.linear(xb, 0, 1), xb @ W.T)
+    x = g.standard_normal((6, 256)).astype(np.float32)
+    np.testing.assert_array_equal(o16.linear(x, 0, 1), om.round_bf16(x) @ W.T)
+    assert np.abs(o16.linear(x, 0, 1) - o32.linear(x, 0, 1)).max() > 0
+
+
+def test_bf16_policy_merges_lora_then_rounds():
+    W = _small_lora_weights()
+    o16 = om.Oracle(W, np.float64, precision="bf16")
+    x = om.round_bf16(np.random.default_rng(23).standard_normal((3, 32)))
+    Wm = W.layers[0][1].astype(np.float64) + 2.0 * W.lora_b[0][0].astype(np.float64) @ W.lora_a[0][0].astype(np.float64)
+    np.testing.assert_allclose(o16.linear(x, 0, "q"), x @ om.round_bf16(Wm).astype(np.float64).T, rtol=1e-12)
