@@ -108,6 +108,10 @@ __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, i
                "r"(x), "r"(y)
                : "memory");
 }
+// Hint: bring `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2_bytes(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -320,6 +324,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int nt = rest / p.splits;
       const int mt = mg * CM + crank;
       const int buf = it & 1;
+      if (p.epi == EPI_RESADD) {
+        // the residual rows this thread will add to are fetched into L2 while the tile's main
+        // loop runs (otherwise the epilogue waits on DRAM after the last MMA)
+        const int mm = mt * BM + row_in_tile, nn = nt * BN;
+        if (mm < p.M && nn < p.N) {
+          const int cols = min(BN, p.N - nn);
+          prefetch_l2_bytes(reinterpret_cast<const float*>(p.out) + (size_t)mm * p.ldo + nn, (uint32_t)cols * 4);
+        }
+      }
       if (!mbar_wait(&tfull[buf], (it >> 1) & 1, abort_flag, p.d_err, ERR_TIMEOUT_TFULL)) break;
       fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);

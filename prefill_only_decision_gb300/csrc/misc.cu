@@ -27,6 +27,38 @@ cudaError_t launch_embed(const bf16* E, const int* row_src, const bf16* embeds, 
 }
 
 // ---- RMSNorm: out = bf16(x / sqrt(mean(x^2) + eps) * w) --------------------------------
+// One warp per row, the row held in registers (one read of x), 8 rows per block.
+template <int NV>   // float4 per lane: d = 128 * NV
+__global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                                           bf16* __restrict__ out, int R, int d, float eps) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= R) return;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)r * d);
+  float4 v[NV];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    v[i] = xr[lane + 32 * i];
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  }
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  const float4* wr = reinterpret_cast<const float4*>(w);
+  uint2* o = reinterpret_cast<uint2*>(out + (size_t)r * d);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const float4 g = wr[lane + 32 * i];
+    __nv_bfloat162 a = __floats2bfloat162_rn(v[i].x * inv * g.x, v[i].y * inv * g.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[i].z * inv * g.z, v[i].w * inv * g.w);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+    o[lane + 32 * i] = u;
+  }
+}
+
+// General width (d % 4 == 0): one block per row, two passes.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                bf16* __restrict__ out, int d, float eps) {
   __shared__ float red[32];
@@ -51,7 +83,14 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
 cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int d, float eps,
                            cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
-  rmsnorm_kernel<<<R, 256, 0, st>>>(x, w, out, d, eps);
+  const int blocks = (R + 7) / 8;
+  switch (d) {
+    case 256: rmsnorm_warp_kernel<2><<<blocks, 256, 0, st>>>(x, w, out, R, d, eps); break;
+    case 1024: rmsnorm_warp_kernel<8><<<blocks, 256, 0, st>>>(x, w, out, R, d, eps); break;
+    case 2560: rmsnorm_warp_kernel<20><<<blocks, 256, 0, st>>>(x, w, out, R, d, eps); break;
+    case 5120: rmsnorm_warp_kernel<40><<<blocks, 256, 0, st>>>(x, w, out, R, d, eps); break;
+    default: rmsnorm_kernel<<<R, 256, 0, st>>>(x, w, out, d, eps); break;
+  }
   return cudaGetLastError();
 }
 
