@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
                                                     const SeqDesc* __restrict__ seqs,
                                                     const CtxDesc* __restrict__ ctxs, int layer_f, int Hq,
                                                     int Hkv, float scale_log2) {
+  allow_dependents();
   constexpr int CH = HD / 8;                 // 16-byte chunks per row
   constexpr int TILE = BKV * HD * 2;         // bytes per K or V tile
   extern __shared__ __align__(128) uint8_t sm[];

@@ -35,4 +35,12 @@ __device__ __forceinline__ bf16 f2bf(float x) { return __float2bfloat16_rn(x); }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.f + __expf(-g)); }
 
+// Programmatic dependent launch: lets the next kernel in the stream (launched with the
+// programmatic-serialisation attribute) start its independent prologue now; it still waits
+// for this grid's completion before it touches data this grid produces.
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Waits until the preceding grid in the stream has completed and its writes are visible (a
+// no-op for kernels launched without the attribute).
+__device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace s1

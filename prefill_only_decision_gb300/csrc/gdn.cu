@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(128) gdn_scan_token_kernel(
     const float* __restrict__ proj, int ld, const float* __restrict__ loga,
     const float* __restrict__ beta, bf16* __restrict__ out, const SeqDesc* __restrict__ seqs,
     const CtxDesc* __restrict__ ctxs, int layer_g, int H, int Dv) {
+  allow_dependents();
   constexpr int E = DK / 32;
   const int sq = blockIdx.x, h = blockIdx.y;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;

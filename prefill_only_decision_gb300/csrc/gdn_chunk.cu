@@ -472,6 +472,7 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
                                                         const ChunkDesc* __restrict__ chunks, int H,
                                                         const float* __restrict__ Ubuf,
                                                         const float* __restrict__ Schunk, bf16* __restrict__ out) {
+  allow_dependents();
   extern __shared__ __align__(16) uint8_t smraw[];
   using SM = OutSmem<D>;
   constexpr int SQ = SM::SQ, SSC = SM::SSC, SUo = SM::SUo, SP = SM::SP;

@@ -161,6 +161,21 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
+// Issue one 32-lane x 16-column TMEM load; the values are valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Keeps the compiler from moving uses of a TMEM-loaded value above tmem_wait_ld().
+__device__ __forceinline__ void reg_fence(float& x) { asm volatile("" : "+f"(x)); }
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
   asm volatile(
@@ -239,6 +254,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (CM > 1) cluster_sync_all();   // peers' barriers are initialised before anyone multicasts
   fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  allow_dependents();
+  // The weights do not depend on earlier kernels: the first weight tiles go to L2 while the
+  // kernel producing this GEMM's activations may still be running.
+  if (warp == 0 && lane == 0 && cid < p.units) {
+    const int u = cid;
+    const int mg = u % p.m_groups, rest = u / p.m_groups, sp = rest % p.splits, nt = rest / p.splits;
+    if (mg == 0) {
+      const int kb0 = sp * p.kb_per_split, kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+      for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, nt * BN + (CM > 1 ? crank * SLICE : 0));
+    }
+  }
+  wait_prerequisites();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -339,75 +366,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int m = mt * BM + row_in_tile;
       const int n0 = nt * BN;
       const bool row_ok = m < p.M;
-      if (p.epi == EPI_SWIGLU) {
-        // tile columns [32b, 32b+16) gate, [32b+16, 32b+32) up -> output columns n0/2 + 16b
+      // Epilogue in 64-column groups: up to four TMEM loads in flight per wait.
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          float g[16], v[16];
-          tmem_ld16(tbase + c, g);
-          tmem_ld16(tbase + c + 16, v);
-          if (row_ok && n0 + c < p.N) {
-            bf16* o = reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + (n0 + c) / 2;
-            __align__(16) bf16 r[16];
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        const int nc = (BN - c0) < 64 ? (BN - c0) / 16 : 4;   // 16-column chunks in this group
+        float v[4][16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = f2bf(silu_f(g[i]) * v[i]);
-            reinterpret_cast<uint4*>(o)[0] = reinterpret_cast<uint4*>(r)[0];
-            reinterpret_cast<uint4*>(o)[1] = reinterpret_cast<uint4*>(r)[1];
+        for (int j = 0; j < 4; ++j)
+          if (j < nc) tmem_ld16_async(tbase + c0 + 16 * j, v[j]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) reg_fence(v[j][i]);
+        if (!row_ok) continue;
+        if (p.epi == EPI_SWIGLU) {
+          // chunk pairs (gate, up): tile columns [32b, 32b+16) gate, [32b+16, 32b+32) up
+#pragma unroll
+          for (int j = 0; j + 1 < 4; j += 2) {
+            if (j + 1 < nc && n0 + c0 + 16 * j < p.N) {
+              bf16* o = reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + (n0 + c0 + 16 * j) / 2;
+              __align__(16) bf16 r[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) r[i] = f2bf(silu_f(v[j][i]) * v[j + 1][i]);
+              reinterpret_cast<uint4*>(o)[0] = reinterpret_cast<uint4*>(r)[0];
+              reinterpret_cast<uint4*>(o)[1] = reinterpret_cast<uint4*>(r)[1];
+            }
           }
-        }
-      } else if (p.epi == EPI_RESADD) {
-        // residual add: the 64 residual values of a column group are loaded together before the
-        // accumulator chunks are read, so one memory latency covers four 16-column chunks
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 64) {
-          const int nc = (BN - c0) < 64 ? (BN - c0) / 16 : 4;   // 16-column chunks in this group
-          float4 xr[16];
+        } else if (p.epi == EPI_RESADD) {
           float* xrow = reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n0 + c0;
+          float4 xr[16];
 #pragma unroll
           for (int j = 0; j < 4; ++j)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              xr[j * 4 + i] = (j < nc && row_ok && n0 + c0 + 16 * j < p.N)
-                                  ? reinterpret_cast<const float4*>(xrow + 16 * j)[i]
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+              xr[j * 4 + i] = (j < nc && n0 + c0 + 16 * j < p.N) ? reinterpret_cast<const float4*>(xrow + 16 * j)[i]
+                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            if (j < nc) {
-              float v[16];
-              tmem_ld16(tbase + c0 + 16 * j, v);
-              if (row_ok && n0 + c0 + 16 * j < p.N) {
-                float4* o = reinterpret_cast<float4*>(xrow + 16 * j);
+            if (j < nc && n0 + c0 + 16 * j < p.N) {
+              float4* o = reinterpret_cast<float4*>(xrow + 16 * j);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const float4 x = xr[j * 4 + i];
-                  o[i] = make_float4(x.x + v[4 * i], x.y + v[4 * i + 1], x.z + v[4 * i + 2], x.w + v[4 * i + 3]);
-                }
+              for (int i = 0; i < 4; ++i) {
+                const float4 x = xr[j * 4 + i];
+                o[i] = make_float4(x.x + v[j][4 * i], x.y + v[j][4 * i + 1], x.z + v[j][4 * i + 2], x.w + v[j][4 * i + 3]);
               }
             }
           }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 16) {
-          float v[16];
-          tmem_ld16(tbase + c, v);
-          const int n = n0 + c;
-          if (!row_ok || n >= p.N) continue;
-          if (p.epi == EPI_F32) {
-            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
+        } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          } else if (p.epi == EPI_BF16) {
-            __align__(16) bf16 r[16];
+          for (int j = 0; j < 4; ++j) {
+            const int n = n0 + c0 + 16 * j;
+            if (j >= nc || n >= p.N) continue;
+            if (p.epi == EPI_F32) {
+              float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) r[i] = f2bf(v[i]);
-            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
-            o[0] = reinterpret_cast<uint4*>(r)[0];
-            o[1] = reinterpret_cast<uint4*>(r)[1];
-          } else {  // split-K partial
-            float4* o = reinterpret_cast<float4*>(p.ws + ((size_t)sp * p.m_tiles * BM + m) * p.N + n);
+              for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
+            } else if (p.epi == EPI_BF16) {
+              __align__(16) bf16 r[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              for (int i = 0; i < 16; ++i) r[i] = f2bf(v[j][i]);
+              uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
+              o[0] = reinterpret_cast<uint4*>(r)[0];
+              o[1] = reinterpret_cast<uint4*>(r)[1];
+            } else {  // split-K partial
+              float4* o = reinterpret_cast<float4*>(p.ws + ((size_t)sp * p.m_tiles * BM + m) * p.N + n);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
+            }
           }
         }
       }
@@ -574,7 +600,7 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
 }
 
 template <int BN, int CM>
-cudaLaunchConfig_t launch_config(cudaLaunchAttribute* attr, cudaStream_t st) {
+cudaLaunchConfig_t launch_config(cudaLaunchAttribute* attr, cudaStream_t st, bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
@@ -583,8 +609,10 @@ cudaLaunchConfig_t launch_config(cudaLaunchAttribute* attr, cudaStream_t st) {
   attr[0].val.clusterDim.x = CM;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cfg;
 }
 
@@ -594,7 +622,7 @@ int max_clusters(int num_sms) {
   static int cached = -1;
   if (cached < 0) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<BN, CM>(attr, 0);
     cfg.gridDim = dim3(CM * ((num_sms + CM - 1) / CM));
     int n = 0;
@@ -628,8 +656,9 @@ inline int max_clusters_of(int bn, int cm, int num_sms) {
 template <int BN, int CM>
 cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, Params p, int num_sms, cudaStream_t st) {
   const int mc = max_clusters<BN, CM>(num_sms);
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config<BN, CM>(attr, st);
+  cudaLaunchAttribute attr[2];
+  static const bool pdl = !(getenv("S1_PDL") && getenv("S1_PDL")[0] == '0');
+  cudaLaunchConfig_t cfg = launch_config<BN, CM>(attr, st, pdl);
   p.m_groups = (p.m_tiles + CM - 1) / CM;
   p.units = p.m_groups * p.splits * p.n_tiles;
   const int ncl = p.units < mc ? p.units : mc;

@@ -8,6 +8,7 @@ namespace s1 {
 // row_src[r] >= 0: token id; row_src[r] < 0: row (-1 - row_src[r]) of `embeds`.
 __global__ void embed_kernel(const bf16* __restrict__ E, const int* __restrict__ row_src,
                              const bf16* __restrict__ embeds, float* __restrict__ x, int d) {
+  allow_dependents();
   const int r = blockIdx.x;
   const int s = row_src[r];
   const bf16* src = (s >= 0) ? E + (size_t)s * d : embeds + (size_t)(-1 - s) * d;
@@ -31,6 +32,7 @@ cudaError_t launch_embed(const bf16* E, const int* row_src, const bf16* embeds, 
 template <int NV>   // float4 per lane: d = 128 * NV
 __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                            bf16* __restrict__ out, int R, int d, float eps) {
+  allow_dependents();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= R) return;
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restri
 // General width (d % 4 == 0): one block per row, two passes.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                bf16* __restrict__ out, int d, float eps) {
+  allow_dependents();
   __shared__ float red[32];
   const int r = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)r * d);
