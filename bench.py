@@ -178,12 +178,24 @@ def run_kernel(args):
             for cm in ((1, 2, 4) if args.cm_sweep else (None,)):
                 if cm is not None:
                     os.environ["S1_GEMM_CM"] = str(cm)
+                call = lambda: B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), out.shape[1], 0)
+                for _ in range(max(1, args.warmup)):
+                    call()
+                torch.cuda.synchronize()
+                ts = []
                 for _ in range(max(1, args.steps)):
-                    B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), out.shape[1], 0)
-                res.append({"shape": sh, "cm": cm})
+                    ev0.record()
+                    call()
+                    ev1.record()
+                    torch.cuda.synchronize()
+                    ts.append(ev0.elapsed_time(ev1))
+                ms = float(np.median(ts))
+                res.append({"shape": sh, "cm": cm, "us_median": round(1e3 * ms, 2),
+                            "tflops": round(2.0 * M * N * K / (ms / 1e3) / 1e12, 1)})
             os.environ.pop("S1_GEMM_CM", None)
         torch.cuda.synchronize()
-        print(json.dumps({"kernel": "gemm", "runs": res, "note": "time these launches with the ncu launch list"}))
+        print(json.dumps({"kernel": "gemm", "runs": res,
+                          "note": "CUDA events around each op call (one launch; inputs L2-resident after the first call)"}))
         return 0
     elif args.kernel == "gdn":
         R, H, D = dims[:3]

@@ -36,7 +36,10 @@ enum { S1_EPI_F32 = 0, S1_EPI_BF16 = 1, S1_EPI_RESADD = 2, S1_EPI_SWIGLU = 3 };
  *   S1_EPI_RESADD: out fp32 [M, ldo] += acc        (residual stream)
  *   S1_EPI_SWIGLU: W rows interleaved in blocks of 16 gate rows then 16 up rows;
  *                  out bf16 [M, ldo], N/2 columns: silu(gate) * up
- * impl: 0 = tcgen05 tensor-core kernel (the product path), 1 = SIMT reference.
+ * impl: 0 = tcgen05 tensor-core kernel (the product path: single-CTA or CTA-pair tiles, the
+ *       planner's choice), 1 = SIMT reference, 2 = tensor-core kernel restricted to CTA-pair
+ *       tiles (256 x N per pair, tcgen05.mma.cta_group::2), 3 = restricted to single-CTA tiles.
+ *       Any other value: S1_ERR_INVALID_ARG.
  * Requires K % 64 == 0 and N % 32 == 0 (SWIGLU: N % 32 == 0); X, W 16-byte aligned. */
 int s1_op_gemm(const void* X, const void* W, int32_t M, int32_t N, int32_t K, int32_t epi,
                void* out, int32_t ldo, int32_t impl, void* stream);

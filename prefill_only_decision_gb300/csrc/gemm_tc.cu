@@ -23,6 +23,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <vector>
 
 #include "common.cuh"
 
@@ -188,12 +189,96 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+
+// ---- CTA-pair (cta_group::2) forms ----------------------------------------------------------
+// Address of the same shared-memory variable in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// TMA load into this CTA's shared memory that completes its bytes on an mbarrier of either CTA
+// of the pair (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// D[256 x N] (+)= A[256 x 16] . B[N x 16]^T over the CTA pair: A rows 0..127 and B rows
+// 0..N/2-1 from the issuing CTA's shared memory, the rest from the peer's at the same offsets;
+// D rows 0..127 land in the issuing CTA's TMEM, rows 128..255 in the peer's.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+// Arrive (when the pair's earlier MMAs issued by this thread complete) on `bar` in both CTAs.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a barrier that the peer CTA also arrives on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  int* d_err, int code) {
+  const uint64_t t0 = now_ns();
+  uint32_t it = 0;
+  while (true) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    if ((++it & 255) == 0) {
+      if (*abort_flag) return false;
+      if (now_ns() - t0 > WAIT_NS) {
+        *abort_flag = 1;
+        atomicExch(d_err, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Instruction descriptor for the pair: M = 256.
+__host__ __device__ constexpr uint32_t idesc_bf16_pair(int bn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
 template <int BN>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+
+// TMEM columns the pair kernel allocates (in both CTAs of the pair, collectively).
+constexpr int PAIR_TMEM_COLS = 512;
+
+// Per-CTA stage of the pair kernel: 128 A rows and half of the BN B rows.
+template <int BN>
+struct Cfg2 {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (208 * 1024) / STAGE_BYTES > 8 ? 8 : (208 * 1024) / STAGE_BYTES;
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
@@ -209,6 +294,83 @@ struct Params {
   int* d_err;
 };
 constexpr int EPI_PARTIAL = 100;
+
+// Epilogue of one accumulator row: this thread's output row m (stored only if row_ok) over the
+// BN columns from n0, read from TMEM at tbase (lane = this thread's row, column = tile column).
+// 64-column groups: up to four TMEM loads in flight per wait.
+template <int BN>
+__device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, int m, int n0, int sp, bool row_ok) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 64) {
+    const int nc = (BN - c0) < 64 ? (BN - c0) / 16 : 4;   // 16-column chunks in this group
+    float v[4][16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < nc) tmem_ld16_async(tbase + c0 + 16 * j, v[j]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < 16; ++i) reg_fence(v[j][i]);
+    if (!row_ok) continue;
+    if (p.epi == EPI_SWIGLU) {
+      // chunk pairs (gate, up): tile columns [32b, 32b+16) gate, [32b+16, 32b+32) up
+#pragma unroll
+      for (int j = 0; j + 1 < 4; j += 2) {
+        if (j + 1 < nc && n0 + c0 + 16 * j < p.N) {
+          bf16* o = reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + (n0 + c0 + 16 * j) / 2;
+          __align__(16) bf16 r[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = f2bf(silu_f(v[j][i]) * v[j + 1][i]);
+          reinterpret_cast<uint4*>(o)[0] = reinterpret_cast<uint4*>(r)[0];
+          reinterpret_cast<uint4*>(o)[1] = reinterpret_cast<uint4*>(r)[1];
+        }
+      }
+    } else if (p.epi == EPI_RESADD) {
+      float* xrow = reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n0 + c0;
+      float4 xr[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          xr[j * 4 + i] = (j < nc && n0 + c0 + 16 * j < p.N) ? reinterpret_cast<const float4*>(xrow + 16 * j)[i]
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j < nc && n0 + c0 + 16 * j < p.N) {
+          float4* o = reinterpret_cast<float4*>(xrow + 16 * j);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 x = xr[j * 4 + i];
+            o[i] = make_float4(x.x + v[j][4 * i], x.y + v[j][4 * i + 1], x.z + v[j][4 * i + 2], x.w + v[j][4 * i + 3]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int n = n0 + c0 + 16 * j;
+        if (j >= nc || n >= p.N) continue;
+        if (p.epi == EPI_F32) {
+          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
+        } else if (p.epi == EPI_BF16) {
+          __align__(16) bf16 r[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) r[i] = f2bf(v[j][i]);
+          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
+          o[0] = reinterpret_cast<uint4*>(r)[0];
+          o[1] = reinterpret_cast<uint4*>(r)[1];
+        } else {  // split-K partial
+          float4* o = reinterpret_cast<float4*>(p.ws + ((size_t)sp * p.m_tiles * BM + m) * p.N + n);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
+        }
+      }
+    }
+  }
+}
 
 // CM CTAs of a cluster (consecutive m tiles of the same n tile and K split) share each B
 // tile: CTA r loads rows [r*BN/CM, (r+1)*BN/CM) of it and multicasts them to the cluster, so
@@ -366,77 +528,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int m = mt * BM + row_in_tile;
       const int n0 = nt * BN;
       const bool row_ok = m < p.M;
-      // Epilogue in 64-column groups: up to four TMEM loads in flight per wait.
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 64) {
-        const int nc = (BN - c0) < 64 ? (BN - c0) / 16 : 4;   // 16-column chunks in this group
-        float v[4][16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (j < nc) tmem_ld16_async(tbase + c0 + 16 * j, v[j]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int i = 0; i < 16; ++i) reg_fence(v[j][i]);
-        if (!row_ok) continue;
-        if (p.epi == EPI_SWIGLU) {
-          // chunk pairs (gate, up): tile columns [32b, 32b+16) gate, [32b+16, 32b+32) up
-#pragma unroll
-          for (int j = 0; j + 1 < 4; j += 2) {
-            if (j + 1 < nc && n0 + c0 + 16 * j < p.N) {
-              bf16* o = reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + (n0 + c0 + 16 * j) / 2;
-              __align__(16) bf16 r[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) r[i] = f2bf(silu_f(v[j][i]) * v[j + 1][i]);
-              reinterpret_cast<uint4*>(o)[0] = reinterpret_cast<uint4*>(r)[0];
-              reinterpret_cast<uint4*>(o)[1] = reinterpret_cast<uint4*>(r)[1];
-            }
-          }
-        } else if (p.epi == EPI_RESADD) {
-          float* xrow = reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n0 + c0;
-          float4 xr[16];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              xr[j * 4 + i] = (j < nc && n0 + c0 + 16 * j < p.N) ? reinterpret_cast<const float4*>(xrow + 16 * j)[i]
-                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j < nc && n0 + c0 + 16 * j < p.N) {
-              float4* o = reinterpret_cast<float4*>(xrow + 16 * j);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float4 x = xr[j * 4 + i];
-                o[i] = make_float4(x.x + v[j][4 * i], x.y + v[j][4 * i + 1], x.z + v[j][4 * i + 2], x.w + v[j][4 * i + 3]);
-              }
-            }
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int n = n0 + c0 + 16 * j;
-            if (j >= nc || n >= p.N) continue;
-            if (p.epi == EPI_F32) {
-              float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
-            } else if (p.epi == EPI_BF16) {
-              __align__(16) bf16 r[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) r[i] = f2bf(v[j][i]);
-              uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
-              o[0] = reinterpret_cast<uint4*>(r)[0];
-              o[1] = reinterpret_cast<uint4*>(r)[1];
-            } else {  // split-K partial
-              float4* o = reinterpret_cast<float4*>(p.ws + ((size_t)sp * p.m_tiles * BM + m) * p.N + n);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
-            }
-          }
-        }
-      }
+      epilogue_row<BN>(p, tbase, m, n0, sp, row_ok);
       fence_before();
       if (lane == 0) mbar_arrive(&tempty[buf]);
     }
@@ -446,6 +538,166 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 1) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512));
+  }
+}
+
+
+// CTA-pair variant: a cluster of two CTAs computes a 256 x BN tile with tcgen05.mma.cta_group::2.
+// Each CTA stages its own 128 A rows and one half of the B tile, so a stage costs each SM
+// 16 KB + BN x 64 B of shared memory and of L2-to-SM traffic for 128 x BN x 64 of MMA work (the
+// single-CTA kernel moves 16 KB + BN x 128 B for the same work): deeper pipelines and less
+// traffic per FLOP. The even CTA of the pair issues the MMAs and owns the barriers that gate
+// them: both CTAs' TMA loads complete on its `full` barriers, and both CTAs' epilogue warps
+// release a TMEM buffer on its `tempty` barriers. Its MMA commits arrive on both CTAs' `empty`
+// and `tfull` barriers. Work units are (m pair tile, split, n tile), m fastest.
+template <int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, Params p) {
+  using C = Cfg2<BN>;
+  static_assert((BN / 2) % 8 == 0 && BN % 16 == 0 && BN <= 256, "pair tile width");
+  constexpr int BUFCOLS = BN <= 128 ? 128 : 256;          // TMEM columns per accumulator buffer
+  constexpr int NBUF = PAIR_TMEM_COLS / BUFCOLS;            // accumulator buffers (1, 2 or 4)
+  static_assert(NBUF >= 1 && NBUF <= 4, "TMEM buffers");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* bars = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + NBUF;
+  uint32_t* tmem_slot = (uint32_t*)(tempty + NBUF);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank();           // 0 = MMA issuer, 1 = peer
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < NBUF; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 8); }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mapB)) : "memory");
+  }
+  if (warp == 1) {   // one warp of each CTA: the pair allocates the same columns in both TMEMs
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(PAIR_TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers are initialised before any cross-CTA signal
+  fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  allow_dependents();
+  if (warp == 0 && lane == 0 && cid < p.units) {
+    const int u = cid;
+    const int mg = u % p.m_groups, rest = u / p.m_groups, sp = rest % p.splits, nt = rest / p.splits;
+    if (mg == 0) {
+      const int kb0 = sp * p.kb_per_split, kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+      for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb)
+        tma_prefetch_l2(&mapB, kb * BK, nt * BN + (int)crank * (BN / 2));
+    }
+  }
+  wait_prerequisites();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t full0 = mapa_shared(smem_u32(full), 0);   // issuer's full barriers
+      for (int u = cid; u < p.units && ok; u += ncl) {
+        const int mg = u % p.m_groups;
+        const int rest = u / p.m_groups;
+        const int sp = rest % p.splits;
+        const int nt = rest / p.splits;
+        const int arow = mg * (2 * BM) + (int)crank * BM;
+        const int brow = nt * BN + (int)crank * (BN / 2);
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        const bool pf = mg == 0;
+        if (pf)
+          for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, brow);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (pf && kb + PF < kb1) tma_prefetch_l2(&mapB, (kb + PF) * BK, brow);
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
+          if (crank == 0) mbar_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          const uint32_t fb = full0 + (uint32_t)(stage * 8);
+          tma_load_2d_pair(sA + stage * C::A_BYTES, &mapA, fb, kb * BK, arow);
+          tma_load_2d_pair(sB + stage * C::B_BYTES, &mapB, fb, kb * BK, brow);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // drain: the issuer's releases of this CTA's stages have all arrived
+      for (int i = 0; i < C::STAGES && ok; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) break;
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && crank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_pair(BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int u = cid; u < p.units && ok; u += ncl, ++it) {
+        const int rest = u / p.m_groups;
+        const int sp = rest % p.splits;
+        const int kb0 = sp * p.kb_per_split;
+        const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+        const int buf = it % NBUF, use = it / NBUF;
+        if (!mbar_wait_cluster(&tempty[buf], (use & 1) ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_TEMPTY)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint32_t tmem_d = tmem_base + (uint32_t)(buf * BUFCOLS);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.d_err, ERR_TIMEOUT_FULL)) { ok = false; break; }
+          fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16_pair(tmem_d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                          (kb > kb0 || kk > 0) ? 1u : 0u);
+          mma_commit_pair(&empty[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (ok) mma_commit_pair(&tfull[buf]);
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
+    int it = 0;
+    for (int u = cid; u < p.units; u += ncl, ++it) {
+      const int mg = u % p.m_groups;
+      const int rest = u / p.m_groups;
+      const int sp = rest % p.splits;
+      const int nt = rest / p.splits;
+      const int buf = it % NBUF, use = it / NBUF;
+      const int m = mg * (2 * BM) + (int)crank * BM + row_in_tile;
+      const int n0 = nt * BN;
+      if (p.epi == EPI_RESADD && m < p.M && n0 < p.N)
+        prefetch_l2_bytes(reinterpret_cast<const float*>(p.out) + (size_t)m * p.ldo + n0, (uint32_t)min(BN, p.N - n0) * 4);
+      if (!mbar_wait(&tfull[buf], use & 1, abort_flag, p.d_err, ERR_TIMEOUT_TFULL)) break;
+      fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BUFCOLS);
+      epilogue_row<BN>(p, tbase, m, n0, sp, m < p.M);
+      fence_before();
+      if (lane == 0) mbar_arrive_remote(tempty0 + (uint32_t)(buf * 8));
+    }
+  }
+  __syncthreads();
+  cluster_sync_all();   // neither CTA leaves while the other may still signal or read it
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(PAIR_TMEM_COLS));
   }
 }
 
@@ -537,7 +789,8 @@ bool make_map(CUtensorMap* out, const void* ptr, int rows, int cols, int box_row
 
 struct Plan {
   int bn, m_tiles, n_tiles, splits, kb_per_split, kb_total, units, grid;
-  int cm;   // cluster size along M (B tiles multicast within the cluster)
+  int cm;     // cluster size along M (B tiles multicast within the cluster)
+  int pair;   // 1: CTA-pair kernel (256-row tiles, cta_group::2); bn is the pair's tile width
 };
 
 // Cluster size along M: as many m tiles as share a B tile, up to 4 (2 when BN = 144).
@@ -552,7 +805,30 @@ inline int max_clusters_of(int bn, int cm, int num_sms);
 // The plan of a fixed tile width and cluster size without a K split.
 inline Plan plan_with(int M, int N, int K, int bn, int cm) {
   const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + bn - 1) / bn, kb = K / BK;
-  return Plan{bn, m_tiles, n_tiles, 1, kb, kb, m_tiles * n_tiles, 0, cm};
+  return Plan{bn, m_tiles, n_tiles, 1, kb, kb, m_tiles * n_tiles, 0, cm, 0};
+}
+
+// The CTA-pair plan of tile width bn (no K split): m_tiles counts 128-row halves, units pairs.
+inline Plan plan_pair(int M, int N, int K, int bn) {
+  const int m_pairs = (M + 2 * BM - 1) / (2 * BM), n_tiles = (N + bn - 1) / bn, kb = K / BK;
+  return Plan{bn, 2 * m_pairs, n_tiles, 1, kb, kb, m_pairs * n_tiles, 0, 1, 1};
+}
+
+inline int max_pairs_of(int bn, int num_sms);
+
+// Heuristic choice among the pair plans: fewest waves of pairs x tile width.
+inline Plan plan_pair_for(int M, int N, int K, int num_sms) {
+  const int cands[3] = {256, 192, 128};
+  Plan best{};
+  double best_cost = 1e30;
+  for (int bn : cands) {
+    const Plan pl = plan_pair(M, N, K, bn);
+    const int maxp = max_pairs_of(bn, num_sms);
+    const int waves = (pl.units + maxp - 1) / maxp;
+    const double cost = (double)waves * (bn + 32.0);
+    if (cost < best_cost * 0.999) { best_cost = cost; best = pl; }
+  }
+  return best;
 }
 
 // Choose the N tile, the K split and the cluster size together: minimise
@@ -590,7 +866,7 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
         if (sp > 1) cost *= 1.0 + 0.04 * sp;
         if (cost < best_cost * 0.999) {
           best_cost = cost;
-          best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, m_tiles * n_tiles * sp, 0, cm};
+          best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, m_tiles * n_tiles * sp, 0, cm, 0};
         }
         if (cunits >= maxcl) break;
       }
@@ -653,6 +929,64 @@ inline int max_clusters_of(int bn, int cm, int num_sms) {
   }
 }
 
+template <int BN>
+cudaLaunchConfig_t launch_config_pair(cudaLaunchAttribute* attr, cudaStream_t st, bool pdl = false) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Cfg2<BN>::SMEM;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cfg;
+}
+
+// CTA pairs of this tile width that fit on the GPU at once (queried once, then cached).
+template <int BN>
+int max_pairs(int num_sms) {
+  static int cached = -1;
+  if (cached < 0) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<BN>::SMEM);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config_pair<BN>(attr, 0);
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    int n = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<BN>, &cfg);
+    if (e != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = num_sms / 2;
+    }
+    cached = n;
+  }
+  return cached;
+}
+
+inline int max_pairs_of(int bn, int num_sms) {
+  switch (bn) {
+    case 256: return max_pairs<256>(num_sms);
+    case 192: return max_pairs<192>(num_sms);
+    default: return max_pairs<128>(num_sms);
+  }
+}
+
+template <int BN>
+cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, Params p, int num_sms, cudaStream_t st) {
+  const int mp = max_pairs<BN>(num_sms);
+  cudaLaunchAttribute attr[2];
+  static const bool pdl = !(getenv("S1_PDL") && getenv("S1_PDL")[0] == '0');
+  cudaLaunchConfig_t cfg = launch_config_pair<BN>(attr, st, pdl);
+  p.m_groups = p.m_tiles / 2;
+  p.units = p.m_groups * p.splits * p.n_tiles;
+  const int ncl = p.units < mp ? p.units : mp;
+  cfg.gridDim = dim3(2 * ncl);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN>, ma, mb, p);
+}
+
 template <int BN, int CM>
 cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, Params p, int num_sms, cudaStream_t st) {
   const int mc = max_clusters<BN, CM>(num_sms);
@@ -697,7 +1031,8 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
                                void* out, int ldo, float* splitk_ws, const LaunchCtx& lc) {
   const int cm = pl.cm;
   CUtensorMap ma, mb;
-  if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, pl.bn / cm)) return cudaErrorInvalidValue;
+  const int brows = pl.pair ? pl.bn / 2 : pl.bn / cm;
+  if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, brows)) return cudaErrorInvalidValue;
   tc::Params p;
   p.M = M; p.N = N; p.K = K;
   p.m_tiles = pl.m_tiles; p.n_tiles = pl.n_tiles; p.splits = pl.splits;
@@ -706,7 +1041,13 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
   p.epi = pl.splits > 1 ? tc::EPI_PARTIAL : epi;
   p.out = out; p.ldo = ldo; p.ws = splitk_ws; p.d_err = lc.d_err;
   cudaError_t e;
-  switch (pl.bn) {
+  if (pl.pair) {
+    switch (pl.bn) {
+      case 256: e = tc::launch_pair<256>(ma, mb, p, lc.num_sms, lc.stream); break;
+      case 192: e = tc::launch_pair<192>(ma, mb, p, lc.num_sms, lc.stream); break;
+      default: e = tc::launch_pair<128>(ma, mb, p, lc.num_sms, lc.stream); break;
+    }
+  } else switch (pl.bn) {
     case 256: e = tc::launch_cm<256>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
     case 192: e = tc::launch_cm<192>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
     case 144: e = tc::launch_cm<144>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
@@ -725,28 +1066,44 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
 }
 
 namespace tc {
-// Measured choice of (BN, CM) per GEMM shape for plans without a K split. Every such plan
+// Measured choice of (BN, CM, pair) per GEMM shape for plans without a K split. Every such plan
 // accumulates each output over K in the same order, so the choice never changes results.
+struct Tuned { int bn, cm, pair; };
 std::mutex g_tune_mu;
-std::map<std::tuple<int, int, int, int, int>, std::pair<int, int>> g_tuned;
+std::map<std::tuple<int, int, int, int, int, int>, Tuned> g_tuned;
 
 bool tune_enabled() {
   const char* e = getenv("S1_GEMM_TUNE");
   return !(e && e[0] == '0');
 }
 
-// Times every (BN, CM) candidate twice on the caller's stream (tuning output `scratch`,
-// RESADD shapes tuned with a plain fp32 store of the same size) and keeps the fastest.
+// Which kernel families a launch may use: the caller's variant, narrowed by the S1_GEMM_PAIR
+// measurement override ("0": single-CTA only, "1": CTA pairs only).
+int variant_of(const LaunchCtx& lc) {
+  if (lc.variant != GEMM_ANY) return lc.variant;
+  const char* e = getenv("S1_GEMM_PAIR");
+  if (e && e[0] == '0') return GEMM_SINGLE;
+  if (e && e[0] == '1') return GEMM_PAIR;
+  return GEMM_ANY;
+}
+
+inline Plan plan_of(int M, int N, int K, const Tuned& t) {
+  return t.pair ? plan_pair(M, N, K, t.bn) : plan_with(M, N, K, t.bn, t.cm);
+}
+
+// Times every candidate (single-CTA BN x CM, and CTA-pair BN) three times on the caller's stream
+// (tuning output `scratch`, RESADD shapes tuned with a plain fp32 store of the same size) and
+// keeps the fastest of the last two runs.
 cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
-                 const LaunchCtx& lc) {
+                 const LaunchCtx& lc, int variant) {
   int dev = 0;
   cudaGetDevice(&dev);
-  const auto key = std::make_tuple(dev, M, N, K, epi);
+  const auto key = std::make_tuple(dev, M, N, K, epi, variant);
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
     auto it = g_tuned.find(key);
     if (it != g_tuned.end()) {
-      pl = plan_with(M, N, K, it->second.first, it->second.second);
+      pl = plan_of(M, N, K, it->second);
       return cudaSuccess;
     }
   }
@@ -761,35 +1118,48 @@ cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, in
   if (cudaEventCreate(&e0) != cudaSuccess) return cudaGetLastError();
   if (cudaEventCreate(&e1) != cudaSuccess) { cudaEventDestroy(e0); return cudaGetLastError(); }
   float best = 1e30f;
-  int bbn = pl.bn, bcm = pl.cm;
+  Tuned bt{pl.bn, pl.cm, pl.pair};
   const int m_tiles = (M + BM - 1) / BM;
-  const int bns[4] = {256, 192, 144, 128};
-  cudaError_t err = cudaSuccess;
-  for (int bn : bns) {
-    if (epi == EPI_SWIGLU && (bn % 32)) continue;
-    for (int cm = 1; cm <= 4 && err == cudaSuccess; cm *= 2) {
-      if ((bn == 144 && cm == 4) || (cm > 1 && m_tiles < 2)) continue;
-      const Plan cand = plan_with(M, N, K, bn, cm);
-      float t = 1e30f;
-      for (int rep = 0; rep < 3 && err == cudaSuccess; ++rep) {
-        cudaEventRecord(e0, lc.stream);
-        err = launch_plan(cand, X, W, M, N, K, tepi, tout, tldo, nullptr, l2);
-        cudaEventRecord(e1, lc.stream);
-        if (err == cudaSuccess) err = cudaEventSynchronize(e1);
-        float ms = 0.f;
-        if (err == cudaSuccess && rep > 0 && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) t = std::min(t, ms);
+  std::vector<Tuned> cands;
+  if (variant != GEMM_PAIR)
+    for (int bn : {256, 192, 144, 128}) {
+      if (epi == EPI_SWIGLU && (bn % 32)) continue;
+      for (int cm = 1; cm <= 4; cm *= 2) {
+        if ((bn == 144 && cm == 4) || (cm > 1 && m_tiles < 2)) continue;
+        cands.push_back(Tuned{bn, cm, 0});
       }
-      if (t < best) { best = t; bbn = bn; bcm = cm; }
     }
+  if (variant != GEMM_SINGLE)
+    for (int bn : {256, 192, 128}) cands.push_back(Tuned{bn, 1, 1});
+  cudaError_t err = cudaSuccess;
+  for (const Tuned& c : cands) {
+    if (err != cudaSuccess) break;
+    const Plan cand = plan_of(M, N, K, c);
+    float t = 1e30f;
+    for (int rep = 0; rep < 3 && err == cudaSuccess; ++rep) {
+      cudaEventRecord(e0, lc.stream);
+      err = launch_plan(cand, X, W, M, N, K, tepi, tout, tldo, nullptr, l2);
+      cudaEventRecord(e1, lc.stream);
+      if (err == cudaSuccess) err = cudaEventSynchronize(e1);
+      float ms = 0.f;
+      if (err == cudaSuccess && rep > 0 && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) t = std::min(t, ms);
+    }
+    if (getenv("S1_GEMM_TUNE_LOG") && getenv("S1_GEMM_TUNE_LOG")[0] == '2')
+      fprintf(stderr, "gemm cand M=%d N=%d K=%d epi=%d %s bn=%d cm=%d %.2f us\n", M, N, K, epi,
+              c.pair ? "pair" : "single", c.bn, c.cm, 1e3f * t);
+    if (t < best) { best = t; bt = c; }
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
   if (err != cudaSuccess) return err;
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
-    g_tuned[key] = std::make_pair(bbn, bcm);
+    g_tuned[key] = bt;
   }
-  pl = plan_with(M, N, K, bbn, bcm);
+  if (getenv("S1_GEMM_TUNE_LOG"))
+    fprintf(stderr, "gemm tune M=%d N=%d K=%d epi=%d -> %s bn=%d cm=%d (%.2f us)\n", M, N, K, epi,
+            bt.pair ? "pair" : "single", bt.bn, bt.cm, 1e3f * best);
+  pl = plan_of(M, N, K, bt);
   return cudaSuccess;
 }
 }  // namespace tc
@@ -798,9 +1168,11 @@ cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, in
                            float* splitk_ws, size_t ws_floats, const LaunchCtx& lc) {
   if (M == 0) return cudaSuccess;
   if (!gemm_tc_supported(M, N, K, epi)) return cudaErrorInvalidValue;
-  tc::Plan pl = tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
+  const int variant = tc::variant_of(lc);
+  tc::Plan pl = variant == GEMM_PAIR ? tc::plan_pair_for(M, N, K, lc.num_sms)
+                                     : tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
   if (pl.splits == 1 && lc.tune && tc::tune_enabled() && !getenv("S1_GEMM_CM")) {
-    cudaError_t e = tc::tune(pl, X, W, M, N, K, epi, out, ldo, lc);
+    cudaError_t e = tc::tune(pl, X, W, M, N, K, epi, out, ldo, lc, variant);
     if (e != cudaSuccess) return e;
   }
   return launch_plan(pl, X, W, M, N, K, epi, out, ldo, splitk_ws, lc);

@@ -43,6 +43,9 @@ struct CtxDesc {
   int cap;      // capacity rows
 };
 
+// GEMM kernel families a launch may choose from.
+enum { GEMM_ANY = 0, GEMM_SINGLE = 1, GEMM_PAIR = 2 };
+
 struct LaunchCtx {
   cudaStream_t stream;
   int* d_err;        // device error word (bounded waits record here)
@@ -51,6 +54,7 @@ struct LaunchCtx {
   bool tune = false;          // GEMM: measure the tile / cluster choice on first use of a shape
   void* tune_out = nullptr;   // GEMM tuning: scratch output for residual-add shapes (fp32)
   size_t tune_floats = 0;
+  int variant = GEMM_ANY;     // GEMM: kernel families allowed (GEMM_ANY, GEMM_SINGLE, GEMM_PAIR)
 };
 
 // ---- kernels (launchers) ----

@@ -47,7 +47,8 @@ int s1_op_gemm(const void* X, const void* W, int32_t M, int32_t N, int32_t K, in
   if (M < 0 || N <= 0 || K <= 0 || K % 64 || N % 32 || epi < 0 || epi > 3)
     return op_fail(S1_ERR_INVALID_ARG, "gemm: bad sizes or epilogue");
   Tmp t;
-  if (impl == 0) {
+  if (impl < 0 || impl > 3) return op_fail(S1_ERR_INVALID_ARG, "gemm: impl must be 0..3");
+  if (impl != 1) {
     if (!gemm_tc_supported(M, N, K, epi)) return op_fail(S1_ERR_UNSUPPORTED, "gemm: shape not supported by the tensor-core kernel");
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -58,6 +59,7 @@ int s1_op_gemm(const void* X, const void* W, int32_t M, int32_t N, int32_t K, in
     if (!ws || !err) return op_fail(S1_ERR_OOM, "gemm: temporaries");
     OCK(cudaMemsetAsync(err, 0, 256, st));
     LaunchCtx lc{st, err, sms, nullptr};
+    lc.variant = impl == 2 ? GEMM_PAIR : (impl == 3 ? GEMM_SINGLE : GEMM_ANY);
     OCK(launch_gemm_tc((const bf16*)X, (const bf16*)W, M, N, K, epi, out, ldo, ws, wsf, lc));
     int h = 0;
     OCK(cudaMemcpyAsync(&h, err, 4, cudaMemcpyDeviceToHost, st));

@@ -47,11 +47,14 @@ def swiglu_pack(Wg, Wu):
 
 
 GEMM_SHAPES = [(1, 32, 64), (100, 160, 128), (128, 256, 256), (300, 544, 320), (1024, 2560, 2560),
-               (144, 2560, 9216), (1024, 6176, 2560), (144, 18432, 2560), (77, 2048, 1024)]
+               (144, 2560, 9216), (1024, 6176, 2560), (144, 18432, 2560), (77, 2048, 1024),
+               (1168, 2560, 9216), (1168, 3072, 2560), (257, 1056, 1024)]
 
 
-IMPLS = [pytest.param(0, id="tc", marks=pytest.mark.skipif(bool(os.environ.get("S1_TEST_NO_TC")),
-                                                         reason="tensor-core path disabled")),
+_NO_TC = pytest.mark.skipif(bool(os.environ.get("S1_TEST_NO_TC")), reason="tensor-core path disabled")
+IMPLS = [pytest.param(0, id="tc", marks=_NO_TC),
+         pytest.param(2, id="tc_pair", marks=_NO_TC),     # CTA-pair tiles (tcgen05 cta_group::2)
+         pytest.param(3, id="tc_single", marks=_NO_TC),   # single-CTA tiles
          pytest.param(1, id="simt")]
 
 
@@ -81,7 +84,8 @@ def test_gemm(B, impl, M, N, K, epi):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
-@pytest.mark.parametrize("M,F,K", [(5, 64, 64), (200, 768, 256), (1024, 9216, 2560), (144, 9216, 2560)])
+@pytest.mark.parametrize("M,F,K", [(5, 64, 64), (200, 768, 256), (1024, 9216, 2560), (144, 9216, 2560),
+                                   (1168, 9216, 2560)])
 def test_gemm_swiglu(B, impl, M, F, K):
     if impl == 1 and M * F * K > 2e9:
         pytest.skip("SIMT reference only on small shapes")
@@ -115,6 +119,23 @@ def test_gemm_row_invariance(B):
         outs.append(o.cpu().numpy())
     err = np.abs(outs[0] - outs[1][:64])
     assert err.max() <= 1e-5 * np.abs(outs[1][:64]).max()
+
+
+@_NO_TC
+@pytest.mark.parametrize("M,N,K", [(1168, 2560, 2048), (300, 18432, 256)])
+def test_gemm_pair_matches_single(B, M, N, K):
+    """CTA-pair and single-CTA tiles accumulate every output over K in the same order."""
+    g = np.random.default_rng(M + N + K)
+    dX = to_dev_bf16(bf16_round(g.standard_normal((M, K))))
+    dW = to_dev_bf16(bf16_round(g.standard_normal((N, K)) * 0.05))
+    outs = []
+    for impl in (2, 3):
+        o = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+        B.op_gemm(dX.data_ptr(), dW.data_ptr(), M, N, K, 0, o.data_ptr(), N, impl)
+        outs.append(o.cpu().numpy())
+    err = np.abs(outs[0] - outs[1])
+    print(f"[pair vs single {M}x{N}x{K}] max |diff| {err.max():.3e}, identical: {bool((err == 0).all())}")
+    assert err.max() <= 1e-6 * np.abs(outs[1]).max()
 
 
 def test_rmsnorm(B):
