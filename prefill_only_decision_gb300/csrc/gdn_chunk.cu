@@ -270,93 +270,185 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
 
 // ---------------------------------------------------------------------------------------
 // chunk_state: one CTA per (sequence, head, block of 16 value rows), 256 threads (8 warps).
-// Per chunk: U = Ut - W S^T (64 x 16, K = 128); S <- gamma_n S + U^T K' (16 x 128, K = 64),
-// K'_t = exp(g_n - g_t) k_t. Records S at each chunk's start (for chunk_out) and writes U
-// over Ut. The state block stays in shared memory in fp32.
+// Per chunk: U = Ut - W S^T (64 x 16, K = D); S <- gamma_n S + U^T K' (16 x D, K = 64),
+// K'_t = exp(g_n - g_t) k_t. Records each chunk's start state (TF32-rounded, for chunk_out)
+// and writes U over Ut. The state block stays in shared memory in fp32, next to a TF32-rounded
+// copy that feeds the tensor cores.
+//
+// The chunk tiles W, K (64 x D fp32) and Ut (64 x 16) arrive by TMA, issued by one thread one
+// chunk ahead, into 128-byte-swizzled boxes of 32 columns: ldmatrix then reads conflict-free
+// 8-row fragments (a TF32 fragment row is four 32-bit values = one 16-byte ldmatrix row).
+// Rows of a partial chunk past its end hold the following rows of the buffers (or zeros past
+// the last row); they only ever meet zero coefficients (Us rows past the end are set to 0).
 template <int D, int NS>
 struct StateSmem {
-  static constexpr int SW = D + 4;      // W tile stride  ([t][j], A-operand pattern)
-  static constexpr int SKK = D + 8;     // K tile stride  ([t][j], B-operand k-major pattern)
-  static constexpr int SS = D + 4;      // state stride   ([i][j])
-  static constexpr int SU = BV + 8;     // U tile stride  ([t][i])
-  float W[NS][C * SW];                  // NS = 2: next chunk loads while this one computes
-  float K[NS][C * SKK];
-  float Ut[NS][C * BV];
-  float g[NS][C];
+  static constexpr int NB = D / 32;     // 32-column boxes per tile row
+  static constexpr int SS = D + 4;      // fp32 state stride ([i][j])
+  static constexpr int SU = BV + 8;     // U stride ([t][i])
+  static constexpr int SUT = C + 4;     // Us^T stride ([i][t], ldmatrix rows 16-byte aligned)
+  float W[NS][C * D];                   // NB boxes [64][32], swizzled
+  float K[NS][C * D];
+  float Sr[BV * D];                     // TF32-rounded state, NB boxes [16][32], swizzled
+  float Ut[NS][C * BV];                 // [64][16] dense
   float S[BV * SS];
-  float U[C * SU];      // U (TF32-rounded), written back for chunk_out
-  float Us[C * SU];     // exp(g_n - g_t) U_t (TF32-rounded), A operand of the state update
+  float U[C * SU];                      // U (TF32-rounded), written back for chunk_out
+  float UsT[BV * SUT];                  // exp(g_n - g_t) U_t, transposed (TF32-rounded)
+  float g[NS][C];
+  uint64_t full[NS];
+  int flag;
 };
 
-// NS = 1 serves launches whose sequences have a single chunk (no prefetch needed, half the
-// shared memory, two CTAs per SM). 8 warps; every matrix-product chain is split over two
-// accumulators so the tensor-core latency of the sequential pass is halved.
+// float index of (row, col) in a 128-byte-swizzled box of 32 fp32 columns
+__device__ __forceinline__ int swz32(int row, int col) {
+  return row * 32 + ((((col >> 2) ^ (row & 7))) << 2) + (col & 3);
+}
+__device__ __forceinline__ void ldsm4(const float* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void cp4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (about 1 s of %globaltimer); false on expiry.
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
+  if (bar_try(bar, parity)) return true;
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t it = 1;; ++it) {
+    if (bar_try(bar, parity)) return true;
+    if ((it & 255) == 0) {
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > 1000000000ull) return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma2(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma3(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Maps: mapW over Wbuf [R, H, D] (box 32 x 1 x 64, swizzled), mapUt over Ubuf [R, H, D] (box
+// 16 x 1 x 64, dense), mapK over proj [R, ld] (box 32 x 64, swizzled).
+// NS = 1 serves launches whose sequences have a single chunk (half the shared memory, two CTAs
+// per SM).
 template <int D, int NS>
-__global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restrict__ proj, int ld,
+__global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant__ CUtensorMap mapW,
+                                                          const __grid_constant__ CUtensorMap mapK,
+                                                          const __grid_constant__ CUtensorMap mapUt,
                                                           const float* __restrict__ gbuf,
                                                           const SeqDesc* __restrict__ seqs,
                                                           const ChunkDesc* __restrict__ chunks,
                                                           const CtxDesc* __restrict__ ctxs, int layer_g, int H,
-                                                          const float* __restrict__ Wbuf, float* __restrict__ Ubuf,
-                                                          float* __restrict__ Schunk, int* __restrict__ d_err) {
-  extern __shared__ __align__(16) uint8_t smraw[];
+                                                          float* __restrict__ Ubuf, float* __restrict__ Schunk,
+                                                          int* __restrict__ d_err) {
+  extern __shared__ __align__(1024) uint8_t smraw[];
   using SM = StateSmem<D, NS>;
-  constexpr int SW = SM::SW, SKK = SM::SKK, SS = SM::SS, SU = SM::SU;
+  constexpr int SS = SM::SS, SU = SM::SU, SUT = SM::SUT, NB = SM::NB;
   constexpr int NTS = D / 64;            // 8-column n-tiles per warp in the state update
   constexpr int NTH = 256;
-  SM& s = *reinterpret_cast<SM*>(smraw);
+  constexpr uint32_t TILE_BYTES = 2 * C * D * 4 + C * BV * 4;
+  SM& s = *reinterpret_cast<SM*>((((uintptr_t)smraw) + 1023) & ~(uintptr_t)1023);
   const SeqDesc sd = seqs[blockIdx.x];
   const int h = blockIdx.y, v0 = blockIdx.z * BV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int HDk = H * D;
+  const int nch = (sd.len + C - 1) / C;
   const size_t head_off = (size_t)(layer_g * H + h) * D * D;
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) bar_init(&s.full[i], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](int cl, int st) {   // one thread: TMA of chunk cl's tiles into stage st
+    const ChunkDesc cd = chunks[sd.chunk0 + cl];
+    bar_expect_tx(&s.full[st], TILE_BYTES);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      tma3(&s.W[st][b * C * 32], &mapW, &s.full[st], 32 * b, h, cd.row0);
+      tma2(&s.K[st][b * C * 32], &mapK, &s.full[st], HDk + h * D + 32 * b, cd.row0);
+    }
+    tma3(&s.Ut[st][0], &mapUt, &s.full[st], v0, h, cd.row0);
+  };
+  auto load_g = [&](int cl, int st) {
+    const ChunkDesc cd = chunks[sd.chunk0 + cl];
+    if (tid < C) cp4(&s.g[st][tid], gbuf + (size_t)(cd.row0 + (tid < cd.len ? tid : 0)) * H + h, tid < cd.len);
+  };
+  if (nch > 0 && tid == 0) issue(0, 0);
+  if (nch > 0) load_g(0, 0);
+  cp_commit();
+  // initial state block: fp32 and TF32-rounded copies
   const float* S0 = sd.ctx_in >= 0 ? ctxs[sd.ctx_in].S + head_off : nullptr;
   for (int i = tid; i < BV * D; i += NTH) {
     const int r = i / D, c = i % D;
-    s.S[r * SS + c] = S0 ? S0[(size_t)(v0 + r) * D + c] : 0.f;
+    const float v = S0 ? S0[(size_t)(v0 + r) * D + c] : 0.f;
+    s.S[r * SS + c] = v;
+    s.Sr[(c >> 5) * (BV * 32) + swz32(r, c & 31)] = rnd(v);
   }
-  const int nch = (sd.len + C - 1) / C;
-  auto load = [&](int cl, int st) {
-    const ChunkDesc cd = chunks[sd.chunk0 + cl];
-    for (int i = tid; i < C * (D / 4); i += NTH) {
-      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-      const bool okr = r < cd.len;
-      const int row = cd.row0 + (okr ? r : 0);
-      cp16(&s.W[st][r * SW + c4], Wbuf + ((size_t)row * H + h) * D + c4, okr);
-      cp16(&s.K[st][r * SKK + c4], proj + (size_t)row * ld + HDk + h * D + c4, okr);
-    }
-    for (int i = tid; i < C * (BV / 4); i += NTH) {
-      const int r = i / (BV / 4), c4 = (i % (BV / 4)) * 4;
-      const bool okr = r < cd.len;
-      const int row = cd.row0 + (okr ? r : 0);
-      cp16(&s.Ut[st][r * BV + c4], Ubuf + ((size_t)row * H + h) * D + v0 + c4, okr);
-    }
-    if (tid < C) s.g[st][tid] = tid < cd.len ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
-  };
-  if (nch > 0) load(0, 0);
-  cp_commit();
-  const bool ok = true;
+  bool ok = true;
   for (int cl = 0; cl < nch; ++cl) {
     const int st = NS == 2 ? (cl & 1) : 0;
     const ChunkDesc cd = chunks[sd.chunk0 + cl];
     if (NS == 2) {
-      if (cl + 1 < nch) load(cl + 1, st ^ 1);
+      if (cl + 1 < nch) {
+        if (tid == 0) issue(cl + 1, st ^ 1);
+        load_g(cl + 1, st ^ 1);
+      }
       cp_commit();
       cp_wait<1>();
     } else {
-      if (cl > 0) load(cl, 0);   // single stage: the previous chunk's tiles are no longer read
+      if (cl > 0) {   // single stage: the previous chunk's tiles are no longer read
+        if (tid == 0) issue(cl, 0);
+        load_g(cl, 0);
+      }
       cp_commit();
       cp_wait<0>();
     }
+    // one thread waits (bounded) for the chunk's tiles; the others then find the phase complete
+    const uint32_t parity = NS == 2 ? ((cl >> 1) & 1) : (cl & 1);
+    if (tid == 0) s.flag = bar_wait(&s.full[st], parity) ? 1 : 0;
     __syncthreads();
-    // record the chunk-start state block
+    if (!s.flag) {
+      if (tid == 0) atomicExch(d_err, 0x201);
+      ok = false;
+      break;
+    }
+    while (!bar_try(&s.full[st], parity)) {
+    }
+    // record the chunk-start state block (already rounded) for chunk_out
     {
       float* dst = Schunk + ((size_t)(sd.chunk0 + cl) * H + h) * D * D + (size_t)v0 * D;
       for (int i = tid; i < BV * (D / 4); i += NTH) {
-        const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-        const float4 v = *reinterpret_cast<const float4*>(&s.S[r * SS + c4]);
-        *reinterpret_cast<float4*>(dst + (size_t)r * D + c4) = make_float4(rnd(v.x), rnd(v.y), rnd(v.z), rnd(v.w));
+        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
+        *reinterpret_cast<float4*>(dst + (size_t)r * D + c) =
+            *reinterpret_cast<const float4*>(&s.Sr[(c >> 5) * (BV * 32) + swz32(r, c & 31)]);
       }
     }
     // U = Ut - W S^T : warp -> rows 16*(warp&3) .., value columns 8*(warp>>2) .. +7
@@ -364,16 +456,22 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
       float a0c[4] = {0.f, 0.f, 0.f, 0.f}, a1c[4] = {0.f, 0.f, 0.f, 0.f};
       const float* Wt = s.W[st];
       const int r0 = (warp & 3) * 16, n0 = (warp >> 2) * 8;
+      const int mi = lane >> 3;
+      const int arow = r0 + (lane & 7) + 8 * (mi & 1), acol = 4 * (mi >> 1);   // A: ldmatrix lane row
+      const int brow = n0 + (lane & 7), bcol = 4 * mi;                          // B: ldmatrix lane row
 #pragma unroll 4
       for (int k = 0; k < D; k += 16) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int kk = k + half * 8;
-          const uint32_t x0 = raw(Wt[(r0 + gq) * SW + kk + tq]), x1 = raw(Wt[(r0 + gq + 8) * SW + kk + tq]);
-          const uint32_t x2 = raw(Wt[(r0 + gq) * SW + kk + tq + 4]), x3 = raw(Wt[(r0 + gq + 8) * SW + kk + tq + 4]);
-          const uint32_t b0 = tf32(s.S[(n0 + gq) * SS + kk + tq]), b1 = tf32(s.S[(n0 + gq) * SS + kk + tq + 4]);
-          mma_tf32(half ? a1c : a0c, x0, x1, x2, x3, b0, b1);
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3, b0, b1, b2, b3;
+        {
+          const int c = k + acol;
+          ldsm4(&Wt[(c >> 5) * (C * 32) + swz32(arow, c & 31)], x0, x1, x2, x3);
+          const int c2 = k + 8 + acol;
+          ldsm4(&Wt[(c2 >> 5) * (C * 32) + swz32(arow, c2 & 31)], y0, y1, y2, y3);
+          const int cb = k + bcol;
+          ldsm4(&s.Sr[(cb >> 5) * (BV * 32) + swz32(brow, cb & 31)], b0, b1, b2, b3);
         }
+        mma_tf32(a0c, x0, x1, x2, x3, b0, b1);
+        mma_tf32(a1c, y0, y1, y2, y3, b2, b3);
       }
       const int c = n0 + 2 * tq;
       const int ra = r0 + gq, rb = r0 + gq + 8;
@@ -385,10 +483,11 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
       s.U[ra * SU + c + 1] = rnd(u1);
       s.U[rb * SU + c] = rnd(u2);
       s.U[rb * SU + c + 1] = rnd(u3);
-      s.Us[ra * SU + c] = rnd(ea * u0);
-      s.Us[ra * SU + c + 1] = rnd(ea * u1);
-      s.Us[rb * SU + c] = rnd(eb * u2);
-      s.Us[rb * SU + c + 1] = rnd(eb * u3);
+      const bool oka = ra < cd.len, okb = rb < cd.len;
+      s.UsT[c * SUT + ra] = oka ? rnd(ea * u0) : 0.f;
+      s.UsT[(c + 1) * SUT + ra] = oka ? rnd(ea * u1) : 0.f;
+      s.UsT[c * SUT + rb] = okb ? rnd(eb * u2) : 0.f;
+      s.UsT[(c + 1) * SUT + rb] = okb ? rnd(eb * u3) : 0.f;
     }
     __syncthreads();
     // write U (this block's 16 value columns) over Ut
@@ -397,11 +496,10 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
       *reinterpret_cast<float4*>(Ubuf + ((size_t)(cd.row0 + r) * H + h) * D + v0 + c4) =
           make_float4(s.U[r * SU + c4], s.U[r * SU + c4 + 1], s.U[r * SU + c4 + 2], s.U[r * SU + c4 + 3]);
     }
-    // S <- gamma_n S + U^T K' : warp -> value rows 0..15, key columns 8*NTS*warp .. (NTS n-tiles)
+    // S <- gamma_n S + Us^T K : warp -> value rows 0..15, key columns 8*NTS*warp .. (NTS n-tiles)
     // (not needed after the last chunk of a sequence whose final state nobody keeps)
     if (cl + 1 < nch || sd.ctx_out >= 0) {
-      const float gn = s.g[st][cd.len - 1];
-      const float gam = __expf(gn);
+      const float gam = __expf(s.g[st][cd.len - 1]);
       float acc[NTS][4], acc2[NTS][4];
 #pragma unroll
       for (int nt = 0; nt < NTS; ++nt) {
@@ -413,35 +511,52 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const float* __restric
         acc2[nt][0] = acc2[nt][1] = acc2[nt][2] = acc2[nt][3] = 0.f;
       }
       const float* Kt = s.K[st];
+      const int mi = lane >> 3;
+      const int arow = (lane & 7) + 8 * (mi & 1), acol = 4 * (mi >> 1);
 #pragma unroll 2
       for (int k = 0; k < C; k += 16) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int kk = k + half * 8;
-          // A[i][t] = exp(g_n - g_t) U[t][i]
-          const uint32_t x0 = raw(s.Us[(kk + tq) * SU + gq]), x1 = raw(s.Us[(kk + tq) * SU + gq + 8]);
-          const uint32_t x2 = raw(s.Us[(kk + tq + 4) * SU + gq]), x3 = raw(s.Us[(kk + tq + 4) * SU + gq + 8]);
+          uint32_t x0, x1, x2, x3;
+          ldsm4(&s.UsT[arow * SUT + kk + acol], x0, x1, x2, x3);
 #pragma unroll
           for (int nt = 0; nt < NTS; ++nt) {
-            const int c = warp * (8 * NTS) + nt * 8 + gq;
-            mma_tf32(half ? acc2[nt] : acc[nt], x0, x1, x2, x3, raw(Kt[(kk + tq) * SKK + c]),
-                     raw(Kt[(kk + tq + 4) * SKK + c]));
+            const int j = warp * (8 * NTS) + nt * 8 + gq;
+            const float* kb = Kt + (j >> 5) * (C * 32);
+            mma_tf32(half ? acc2[nt] : acc[nt], x0, x1, x2, x3, raw(kb[swz32(kk + tq, j & 31)]),
+                     raw(kb[swz32(kk + tq + 4, j & 31)]));
           }
         }
       }
-      __syncthreads();   // every warp has read S and U
+      __syncthreads();   // every warp has read S, Sr and Us
 #pragma unroll
       for (int nt = 0; nt < NTS; ++nt) {
         const int c = warp * (8 * NTS) + nt * 8 + 2 * tq;
-        s.S[gq * SS + c] = acc[nt][0] + acc2[nt][0];
-        s.S[gq * SS + c + 1] = acc[nt][1] + acc2[nt][1];
-        s.S[(gq + 8) * SS + c] = acc[nt][2] + acc2[nt][2];
-        s.S[(gq + 8) * SS + c + 1] = acc[nt][3] + acc2[nt][3];
+        const float e0 = acc[nt][0] + acc2[nt][0], e1 = acc[nt][1] + acc2[nt][1];
+        const float e2 = acc[nt][2] + acc2[nt][2], e3 = acc[nt][3] + acc2[nt][3];
+        s.S[gq * SS + c] = e0;
+        s.S[gq * SS + c + 1] = e1;
+        s.S[(gq + 8) * SS + c] = e2;
+        s.S[(gq + 8) * SS + c + 1] = e3;
+        float* sb = s.Sr + (c >> 5) * (BV * 32);
+        *reinterpret_cast<float2*>(&sb[swz32(gq, c & 31)]) = make_float2(rnd(e0), rnd(e1));
+        *reinterpret_cast<float2*>(&sb[swz32(gq + 8, c & 31)]) = make_float2(rnd(e2), rnd(e3));
       }
     }
     __syncthreads();
   }
-  if (ok && sd.ctx_out >= 0) {
+  if (!ok) {
+    // a tile never arrived: wait (bounded) for this CTA's copies in flight, then leave
+    if (tid == 0)
+      for (int i = 0; i < NS; ++i) {
+        bar_wait(&s.full[i], 0);
+        bar_wait(&s.full[i], 1);
+      }
+    __syncthreads();
+    return;
+  }
+  if (sd.ctx_out >= 0) {
     float* So = ctxs[sd.ctx_out].S + head_off;
     for (int i = tid; i < BV * D; i += NTH) {
       const int r = i / D, c = i % D;
@@ -588,25 +703,28 @@ bool gdn_chunked_supported(int H, int Dk, int Dv, int ld) {
   return Dk == Dv && (Dk == 64 || Dk == 128) && H > 0 && (ld % 4) == 0;
 }
 
+template <int D, int NS>
+static constexpr size_t state_smem() { return sizeof(gc::StateSmem<D, NS>) + 1024; }
+
 template <int D>
-static cudaError_t launch_state(const float* proj, int ld, const float* g, const SeqDesc* d_seq, int n_seq,
-                                const ChunkDesc* d_chunks, const CtxDesc* d_ctx, int layer_g, int H,
-                                const float* Wbuf, float* Ubuf, float* Schunk, int max_chunks, int* d_err,
-                                cudaStream_t st) {
+static cudaError_t launch_state(const CUtensorMap& mW, const CUtensorMap& mK, const CUtensorMap& mU,
+                                const float* g, const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks,
+                                const CtxDesc* d_ctx, int layer_g, int H, float* Ubuf, float* Schunk,
+                                int max_chunks, int* d_err, cudaStream_t st) {
   if (n_seq <= 0) return cudaSuccess;
   const dim3 grid(n_seq, H, D / gc::BV);
   if (max_chunks <= 1) {
-    gc::chunk_state_kernel<D, 1><<<grid, 256, sizeof(gc::StateSmem<D, 1>), st>>>(
-        proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk, d_err);
+    gc::chunk_state_kernel<D, 1><<<grid, 256, state_smem<D, 1>(), st>>>(mW, mK, mU, g, d_seq, d_chunks, d_ctx,
+                                                                        layer_g, H, Ubuf, Schunk, d_err);
   } else {
-    gc::chunk_state_kernel<D, 2><<<grid, 256, sizeof(gc::StateSmem<D, 2>), st>>>(
-        proj, ld, g, d_seq, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk, d_err);
+    gc::chunk_state_kernel<D, 2><<<grid, 256, state_smem<D, 2>(), st>>>(mW, mK, mU, g, d_seq, d_chunks, d_ctx,
+                                                                        layer_g, H, Ubuf, Schunk, d_err);
   }
   return cudaGetLastError();
 }
 
 template <int D>
-static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const float* beta, bf16* out,
+static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, const float* beta, bf16* out,
                                     const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                     const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
                                     float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
@@ -618,32 +736,46 @@ static cudaError_t launch_chunked_d(float* proj, int ld, float* loga, const floa
     cudaError_t e = cudaFuncSetAttribute(gc::chunk_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gc::chunk_state_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sizeof(gc::StateSmem<D, 1>));
+                               (int)state_smem<D, 1>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gc::chunk_state_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sizeof(gc::StateSmem<D, 2>));
+                               (int)state_smem<D, 2>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gc::chunk_out_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   gc::chunk_prep_kernel<D><<<dim3(n_chunks, H), 256, sp, st>>>(proj, ld, loga, beta, d_chunks, H, D, Wbuf, Ubuf);
+  // TMA views of the chunk tiles: W and Ut rows of head h ([R, H, D] fp32), K columns of proj
+  CUtensorMap mW, mK, mU;
+  {
+    const uint64_t dims3[3] = {(uint64_t)D, (uint64_t)H, (uint64_t)R};
+    const uint64_t str3[2] = {(uint64_t)D * 4, (uint64_t)H * D * 4};
+    const uint32_t boxW[3] = {32, 1, (uint32_t)gc::C}, boxU[3] = {(uint32_t)gc::BV, 1, (uint32_t)gc::C};
+    const uint64_t dims2[2] = {(uint64_t)ld, (uint64_t)R};
+    const uint64_t str2[1] = {(uint64_t)ld * 4};
+    const uint32_t boxK[2] = {32, (uint32_t)gc::C};
+    if (!tensor_map(&mW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, Wbuf, dims3, str3, boxW, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tensor_map(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, Ubuf, dims3, str3, boxU, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !tensor_map(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, proj, dims2, str2, boxK, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   // sequences [0, n_first) run before the rest (the rest continue from their states)
   const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
-  cudaError_t e = launch_state<D>(proj, ld, loga, d_seq, split, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf, Schunk,
+  cudaError_t e = launch_state<D>(mW, mK, mU, loga, d_seq, split, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
                                   split < n_seq ? max_chunks_first : std::max(max_chunks_first, max_chunks_rest),
                                   d_err, st);
   if (e != cudaSuccess) return e;
   if (split < n_seq) {
-    e = launch_state<D>(proj, ld, loga, d_seq + split, n_seq - split, d_chunks, d_ctx, layer_g, H, Wbuf, Ubuf,
-                        Schunk, max_chunks_rest, d_err, st);
+    e = launch_state<D>(mW, mK, mU, loga, d_seq + split, n_seq - split, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
+                        max_chunks_rest, d_err, st);
     if (e != cudaSuccess) return e;
   }
   gc::chunk_out_kernel<D><<<dim3(n_chunks, H), 256, so, st>>>(proj, ld, loga, d_chunks, H, Ubuf, Schunk, out);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gdn_chunked(float* proj, int ld, float* loga, const float* beta, bf16* out,
+cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, const float* beta, bf16* out,
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
@@ -652,10 +784,10 @@ cudaError_t launch_gdn_chunked(float* proj, int ld, float* loga, const float* be
   if (!gdn_chunked_supported(H, Dk, Dv, ld)) return cudaErrorNotSupported;
   if (n_seq > 65535 || n_chunks > 2147483647 / 2) return cudaErrorInvalidValue;
   cudaError_t e = (Dk == 128)
-                      ? launch_chunked_d<128>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
+                      ? launch_chunked_d<128>(proj, ld, R, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                               layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
                                               max_chunks_rest, d_err, st)
-                      : launch_chunked_d<64>(proj, ld, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
+                      : launch_chunked_d<64>(proj, ld, R, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                              layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
                                              max_chunks_rest, d_err, st);
   if (launches) *launches += (n_first > 0 && n_first < n_seq) ? 4 : 3;

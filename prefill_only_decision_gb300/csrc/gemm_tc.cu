@@ -787,6 +787,36 @@ bool make_map(CUtensorMap* out, const void* ptr, int rows, int cols, int box_row
   return true;
 }
 
+}  // namespace tc
+
+bool tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, int rank, const void* ptr, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  static std::mutex mu;
+  static std::map<std::vector<uint64_t>, CUtensorMap> cache;
+  if (rank < 1 || rank > 5) return false;
+  std::vector<uint64_t> key{(uint64_t)dtype, (uint64_t)rank, (uint64_t)(uintptr_t)ptr, (uint64_t)swizzle};
+  for (int i = 0; i < rank; ++i) key.push_back(dims[i]);
+  for (int i = 0; i + 1 < rank; ++i) key.push_back(strides[i]);
+  for (int i = 0; i < rank; ++i) key.push_back(box[i]);
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) { *out = it->second; return true; }
+  tc::EncodeTiledFn enc = tc::get_encode();
+  if (!enc) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; e[i] = 1; }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  CUresult r = enc(out, dtype, (cuuint32_t)rank, const_cast<void*>(ptr), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = *out;
+  return true;
+}
+
+namespace tc {
+
 struct Plan {
   int bn, m_tiles, n_tiles, splits, kb_per_split, kb_total, units, grid;
   int cm;     // cluster size along M (B tiles multicast within the cluster)

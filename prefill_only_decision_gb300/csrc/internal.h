@@ -1,5 +1,6 @@
 // Internal declarations shared by the library's translation units (not part of the ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -57,6 +58,12 @@ struct LaunchCtx {
   int variant = GEMM_ANY;     // GEMM: kernel families allowed (GEMM_ANY, GEMM_SINGLE, GEMM_PAIR)
 };
 
+// Tiled TMA descriptor over a global tensor (dims and box innermost first, strides in bytes for
+// dims 1..rank-1), encoded through the driver entry point and cached by its arguments.
+// Returns false if the driver entry point is missing or rejects the arguments.
+bool tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, int rank, const void* ptr, const uint64_t* dims,
+                const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle);
+
 // ---- kernels (launchers) ----
 cudaError_t launch_embed(const bf16* E, const int* row_src, const bf16* embeds, float* x, int R, int d,
                          cudaStream_t st);
@@ -75,7 +82,7 @@ cudaError_t launch_gdn_scan(const float* proj, int ld, const float* alpha, const
                             bf16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
                             int layer_g, int H, int Dk, int Dv, cudaStream_t st);
 bool gdn_chunked_supported(int H, int Dk, int Dv, int ld);
-cudaError_t launch_gdn_chunked(float* proj, int ld, float* loga, const float* beta, bf16* out,
+cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, const float* beta, bf16* out,
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,

@@ -397,7 +397,7 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
             m->schunk_chunks = m->schunk ? cap : 0;
             if (!m->schunk) return fail(S1_ERR_OOM, "chunk-state buffer (%zu chunks) allocation failed", cap);
           }
-          CK(launch_gdn_chunked(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
+          CK(launch_gdn_chunked(sc.proj, L.n_in, R, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
                                 mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first,
                                 mt.max_chunks_first, mt.max_chunks_rest, m->d_err, st, &m->launches));
         } else {
