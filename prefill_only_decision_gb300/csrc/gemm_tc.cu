@@ -259,13 +259,39 @@ __host__ __device__ constexpr uint32_t idesc_bf16_pair(int bn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
 }
 
+
+// ---- epilogue bulk stores ----------------------------------------------------------------------
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// box of the output tensor at (x, y) <- shared memory (rows outside the tensor are not written)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+// box of the output tensor at (x, y) += shared memory, element by element in L2
+__device__ __forceinline__ void tma_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Epilogue staging: two 2 KB boxes (32 rows x 64 bytes) per epilogue warp.
+constexpr int STG_BYTES = 4 * 2 * 2048;
+// Shared memory left for pipeline stages: the opt-in maximum less staging, barriers and alignment.
+constexpr int STAGE_BUDGET = 232448 - STG_BYTES - 1024 - 256;
+
 template <int BN>
 struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
 
@@ -278,8 +304,8 @@ struct Cfg2 {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = (BN / 2) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (208 * 1024) / STAGE_BYTES > 8 ? 8 : (208 * 1024) / STAGE_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + STG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 };
 
 struct Params {
@@ -295,11 +321,41 @@ struct Params {
 };
 constexpr int EPI_PARTIAL = 100;
 
-// Epilogue of one accumulator row: this thread's output row m (stored only if row_ok) over the
-// BN columns from n0, read from TMEM at tbase (lane = this thread's row, column = tile column).
-// 64-column groups: up to four TMEM loads in flight per wait.
+// Epilogue of one epilogue warp's 32 accumulator rows of a tile: TMEM -> registers (up to four
+// 16-column loads in flight per wait). fp32 outputs then go through a 32 x 16 box in shared
+// memory (one 64-byte row per lane, swizzled like the output map) to one TMA bulk store per box,
+// or a TMA add-reduction into the fp32 residual stream for EPI_RESADD (each output element has
+// exactly one writer, so the sum is the plain fp32 x + acc); a lane's row of a store box is
+// 64 bytes, where a direct store from registers would write 16-byte pieces of 32 rows. bf16
+// outputs (32 contiguous bytes per row and chunk) are stored from registers. Two staging boxes per
+// warp alternate; a box is rewritten only after the store issued from it two boxes earlier has
+// read it. m0 = the warp's first row of the product, y0 = its row in the output map (m0, or
+// m0 + split x padded rows for split-K partials), n0 = the tile's first column, `nst` = this
+// warp's running count of issued boxes. Warps whose rows all lie past M store nothing: rows past
+// the end of a padded cluster's last tile would otherwise land in the next split's partials.
 template <int BN>
-__device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, int m, int n0, int sp, bool row_ok) {
+__device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap* mapO, uint32_t tbase, int m0, int y0,
+                                              int n0, uint8_t* stg, int lane, int& nst) {
+  if (m0 >= p.M) return;
+  auto acquire = [&]() -> uint8_t* {
+    if (nst >= 2) {
+      if (lane == 0) bulk_wait_read1();
+      __syncwarp();
+    }
+    return stg + (nst & 1) * 2048;
+  };
+  auto issue = [&](uint8_t* box, int x) {
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (p.epi == EPI_RESADD) tma_add_2d(mapO, box, x, y0);
+      else tma_store_2d(mapO, box, x, y0);
+      bulk_commit();
+    }
+    ++nst;
+  };
+  // 16-byte chunk c of this lane's row in a 64-byte swizzled row (the output map's 64-byte swizzle)
+  auto chunk64 = [&](uint8_t* box, int c) { return reinterpret_cast<uint4*>(box + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)); };
 #pragma unroll 1
   for (int c0 = 0; c0 < BN; c0 += 64) {
     const int nc = (BN - c0) < 64 ? (BN - c0) / 16 : 4;   // 16-column chunks in this group
@@ -312,12 +368,13 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, in
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int i = 0; i < 16; ++i) reg_fence(v[j][i]);
-    if (!row_ok) continue;
+    const int m = m0 + lane;   // this lane's output row (bf16 outputs: stored from registers)
     if (p.epi == EPI_SWIGLU) {
-      // chunk pairs (gate, up): tile columns [32b, 32b+16) gate, [32b+16, 32b+32) up
+      // chunk pairs (gate, up): tile columns [32b, 32b+16) gate, [32b+16, 32b+32) up; each row's
+      // 16 outputs are 32 contiguous bytes (one full sector)
 #pragma unroll
       for (int j = 0; j + 1 < 4; j += 2) {
-        if (j + 1 < nc && n0 + c0 + 16 * j < p.N) {
+        if (m < p.M && j + 1 < nc && n0 + c0 + 16 * j < p.N) {
           bf16* o = reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + (n0 + c0 + 16 * j) / 2;
           __align__(16) bf16 r[16];
 #pragma unroll
@@ -326,47 +383,29 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, in
           reinterpret_cast<uint4*>(o)[1] = reinterpret_cast<uint4*>(r)[1];
         }
       }
-    } else if (p.epi == EPI_RESADD) {
-      float* xrow = reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n0 + c0;
-      float4 xr[16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          xr[j * 4 + i] = (j < nc && n0 + c0 + 16 * j < p.N) ? reinterpret_cast<const float4*>(xrow + 16 * j)[i]
-                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else if (p.epi == EPI_BF16) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (j < nc && n0 + c0 + 16 * j < p.N) {
-          float4* o = reinterpret_cast<float4*>(xrow + 16 * j);
+        const int n = n0 + c0 + 16 * j;
+        if (m >= p.M || j >= nc || n >= p.N) continue;
+        __align__(16) bf16 r[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 x = xr[j * 4 + i];
-            o[i] = make_float4(x.x + v[j][4 * i], x.y + v[j][4 * i + 1], x.z + v[j][4 * i + 2], x.w + v[j][4 * i + 3]);
-          }
-        }
+        for (int i = 0; i < 16; ++i) r[i] = f2bf(v[j][i]);
+        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
+        o[0] = reinterpret_cast<uint4*>(r)[0];
+        o[1] = reinterpret_cast<uint4*>(r)[1];
       }
-    } else {
+    } else {   // fp32 outputs: staged boxes, TMA store or add-reduction
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int n = n0 + c0 + 16 * j;
         if (j >= nc || n >= p.N) continue;
-        if (p.epi == EPI_F32) {
-          float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + (size_t)m * p.ldo + n);
+        uint8_t* box = acquire();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
-        } else if (p.epi == EPI_BF16) {
-          __align__(16) bf16 r[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = f2bf(v[j][i]);
-          uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
-          o[0] = reinterpret_cast<uint4*>(r)[0];
-          o[1] = reinterpret_cast<uint4*>(r)[1];
-        } else {  // split-K partial
-          float4* o = reinterpret_cast<float4*>(p.ws + ((size_t)sp * p.m_tiles * BM + m) * p.N + n);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
-        }
+        for (int c = 0; c < 4; ++c)
+          *chunk64(box, c) = make_uint4(__float_as_uint(v[j][4 * c]), __float_as_uint(v[j][4 * c + 1]),
+                                        __float_as_uint(v[j][4 * c + 2]), __float_as_uint(v[j][4 * c + 3]));
+        issue(box, n);
       }
     }
   }
@@ -379,7 +418,8 @@ __device__ __forceinline__ void epilogue_row(const Params& p, uint32_t tbase, in
 // barriers).
 template <int BN, int CM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const __grid_constant__ CUtensorMap mapO, Params p) {
   using C = Cfg<BN>;
   constexpr int SLICE = BN / CM;                    // B rows loaded by each CTA of the cluster
   constexpr uint16_t MASK = (uint16_t)((1u << CM) - 1);
@@ -388,7 +428,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t* bars = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* stg_all = smem + C::STAGES * C::STAGE_BYTES;          // epilogue staging (1024-aligned)
+  uint64_t* bars = (uint64_t*)(stg_all + STG_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* tfull = bars + 2 * C::STAGES;
@@ -504,7 +545,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // epilogue warps 2..5: TMEM lane quadrant = warp % 4
     const int q = warp & 3;
-    const int row_in_tile = q * 32 + lane;
+    uint8_t* stg = stg_all + (warp - 2) * 4096;
+    int nst = 0;
     int it = 0;
     for (int u = cid; u < p.units; u += ncl, ++it) {
       const int mg = u % p.m_groups;
@@ -513,25 +555,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int nt = rest / p.splits;
       const int mt = mg * CM + crank;
       const int buf = it & 1;
-      if (p.epi == EPI_RESADD) {
-        // the residual rows this thread will add to are fetched into L2 while the tile's main
-        // loop runs (otherwise the epilogue waits on DRAM after the last MMA)
-        const int mm = mt * BM + row_in_tile, nn = nt * BN;
-        if (mm < p.M && nn < p.N) {
-          const int cols = min(BN, p.N - nn);
-          prefetch_l2_bytes(reinterpret_cast<const float*>(p.out) + (size_t)mm * p.ldo + nn, (uint32_t)cols * 4);
-        }
-      }
       if (!mbar_wait(&tfull[buf], (it >> 1) & 1, abort_flag, p.d_err, ERR_TIMEOUT_TFULL)) break;
       fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 256);
-      const int m = mt * BM + row_in_tile;
-      const int n0 = nt * BN;
-      const bool row_ok = m < p.M;
-      epilogue_row<BN>(p, tbase, m, n0, sp, row_ok);
+      const int m0 = mt * BM + q * 32;
+      epilogue_tile<BN>(p, &mapO, tbase, m0, (p.epi == EPI_PARTIAL ? sp * p.m_tiles * BM : 0) + m0, nt * BN, stg,
+                        lane, nst);
       fence_before();
       if (lane == 0) mbar_arrive(&tempty[buf]);
     }
+    if (lane == 0) bulk_wait_all();   // this warp's stores have completed
   }
   __syncthreads();
   if (CM > 1) cluster_sync_all();   // no CTA leaves while a peer may still target its memory
@@ -552,7 +585,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // and `tfull` barriers. Work units are (m pair tile, split, n tile), m fastest.
 template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB, Params p) {
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                     const __grid_constant__ CUtensorMap mapO, Params p) {
   using C = Cfg2<BN>;
   static_assert((BN / 2) % 8 == 0 && BN % 16 == 0 && BN <= 256, "pair tile width");
   constexpr int BUFCOLS = BN <= 128 ? 128 : 256;          // TMEM columns per accumulator buffer
@@ -562,7 +596,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t* bars = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* stg_all = smem + C::STAGES * C::STAGE_BYTES;          // epilogue staging (1024-aligned)
+  uint64_t* bars = (uint64_t*)(stg_all + STG_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
   uint64_t* tfull = bars + 2 * C::STAGES;
@@ -672,7 +707,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     const int q = warp & 3;
-    const int row_in_tile = q * 32 + lane;
+    uint8_t* stg = stg_all + (warp - 2) * 4096;
+    int nst = 0;
     const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
     int it = 0;
     for (int u = cid; u < p.units; u += ncl, ++it) {
@@ -681,17 +717,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int sp = rest % p.splits;
       const int nt = rest / p.splits;
       const int buf = it % NBUF, use = it / NBUF;
-      const int m = mg * (2 * BM) + (int)crank * BM + row_in_tile;
-      const int n0 = nt * BN;
-      if (p.epi == EPI_RESADD && m < p.M && n0 < p.N)
-        prefetch_l2_bytes(reinterpret_cast<const float*>(p.out) + (size_t)m * p.ldo + n0, (uint32_t)min(BN, p.N - n0) * 4);
       if (!mbar_wait(&tfull[buf], use & 1, abort_flag, p.d_err, ERR_TIMEOUT_TFULL)) break;
       fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BUFCOLS);
-      epilogue_row<BN>(p, tbase, m, n0, sp, m < p.M);
+      const int m0 = mg * (2 * BM) + (int)crank * BM + q * 32;
+      epilogue_tile<BN>(p, &mapO, tbase, m0, (p.epi == EPI_PARTIAL ? sp * p.m_tiles * BM : 0) + m0, nt * BN, stg,
+                        lane, nst);
       fence_before();
       if (lane == 0) mbar_arrive_remote(tempty0 + (uint32_t)(buf * 8));
     }
+    if (lane == 0) bulk_wait_all();   // this warp's stores have completed
   }
   __syncthreads();
   cluster_sync_all();   // neither CTA leaves while the other may still signal or read it
@@ -1005,7 +1040,8 @@ inline int max_pairs_of(int bn, int num_sms) {
 }
 
 template <int BN>
-cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, Params p, int num_sms, cudaStream_t st) {
+cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, Params p, int num_sms,
+                        cudaStream_t st) {
   const int mp = max_pairs<BN>(num_sms);
   cudaLaunchAttribute attr[2];
   static const bool pdl = !(getenv("S1_PDL") && getenv("S1_PDL")[0] == '0');
@@ -1014,11 +1050,12 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, Params p, 
   p.units = p.m_groups * p.splits * p.n_tiles;
   const int ncl = p.units < mp ? p.units : mp;
   cfg.gridDim = dim3(2 * ncl);
-  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN>, ma, mb, p);
+  return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN>, ma, mb, mo, p);
 }
 
 template <int BN, int CM>
-cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, Params p, int num_sms, cudaStream_t st) {
+cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, Params p, int num_sms,
+                      cudaStream_t st) {
   const int mc = max_clusters<BN, CM>(num_sms);
   cudaLaunchAttribute attr[2];
   static const bool pdl = !(getenv("S1_PDL") && getenv("S1_PDL")[0] == '0');
@@ -1027,15 +1064,15 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, Params p, in
   p.units = p.m_groups * p.splits * p.n_tiles;
   const int ncl = p.units < mc ? p.units : mc;
   cfg.gridDim = dim3(ncl * CM);
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, CM>, ma, mb, p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, CM>, ma, mb, mo, p);
 }
 
 template <int BN>
-cudaError_t launch_cm(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int cm, int num_sms,
-                      cudaStream_t st) {
-  if (cm == 4) return launch_bn<BN, (BN == 144 ? 2 : 4)>(ma, mb, p, num_sms, st);
-  if (cm == 2) return launch_bn<BN, 2>(ma, mb, p, num_sms, st);
-  return launch_bn<BN, 1>(ma, mb, p, num_sms, st);
+cudaError_t launch_cm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const Params& p, int cm,
+                      int num_sms, cudaStream_t st) {
+  if (cm == 4) return launch_bn<BN, (BN == 144 ? 2 : 4)>(ma, mb, mo, p, num_sms, st);
+  if (cm == 2) return launch_bn<BN, 2>(ma, mb, mo, p, num_sms, st);
+  return launch_bn<BN, 1>(ma, mb, mo, p, num_sms, st);
 }
 
 }  // namespace tc
@@ -1070,18 +1107,37 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
   p.m_groups = 0; p.units = 0;   // set by the launcher for its cluster size
   p.epi = pl.splits > 1 ? tc::EPI_PARTIAL : epi;
   p.out = out; p.ldo = ldo; p.ws = splitk_ws; p.d_err = lc.d_err;
+  // fp32 output map: 32-row x 16-column boxes (64-byte rows, 64-byte swizzle), matching the
+  // epilogue's staging layout
+  CUtensorMap mo;
+  {
+    const bool part = pl.splits > 1;
+    if (part || epi == EPI_F32 || epi == EPI_RESADD) {
+      const uint64_t rows = part ? (uint64_t)pl.splits * pl.m_tiles * tc::BM : (uint64_t)M;
+      const uint64_t pitch = part ? (uint64_t)N * 4 : (uint64_t)ldo * 4;
+      const void* base = part ? (const void*)splitk_ws : out;
+      if ((pitch % 16) != 0 || ((uintptr_t)base % 16) != 0) return cudaErrorInvalidValue;
+      const uint64_t dims[2] = {(uint64_t)N, rows};
+      const uint64_t strides[1] = {pitch};
+      const uint32_t box[2] = {16, 32};
+      if (!tensor_map(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    } else {
+      memset(&mo, 0, sizeof(mo));   // bf16 outputs are stored from registers
+    }
+  }
   cudaError_t e;
   if (pl.pair) {
     switch (pl.bn) {
-      case 256: e = tc::launch_pair<256>(ma, mb, p, lc.num_sms, lc.stream); break;
-      case 192: e = tc::launch_pair<192>(ma, mb, p, lc.num_sms, lc.stream); break;
-      default: e = tc::launch_pair<128>(ma, mb, p, lc.num_sms, lc.stream); break;
+      case 256: e = tc::launch_pair<256>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+      case 192: e = tc::launch_pair<192>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+      default: e = tc::launch_pair<128>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
     }
   } else switch (pl.bn) {
-    case 256: e = tc::launch_cm<256>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
-    case 192: e = tc::launch_cm<192>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
-    case 144: e = tc::launch_cm<144>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
-    default: e = tc::launch_cm<128>(ma, mb, p, cm, lc.num_sms, lc.stream); break;
+    case 256: e = tc::launch_cm<256>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
+    case 192: e = tc::launch_cm<192>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
+    case 144: e = tc::launch_cm<144>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
+    default: e = tc::launch_cm<128>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
   }
   if (lc.launches) *lc.launches += 1;
   if (e != cudaSuccess || pl.splits == 1) return e;
