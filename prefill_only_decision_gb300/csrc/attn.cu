@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
                                                     const CtxDesc* __restrict__ ctxs, int layer_f, int Hq,
                                                     int Hkv, float scale_log2) {
   allow_dependents();
+  wait_prerequisites();
   constexpr int CH = HD / 8;                 // 16-byte chunks per row
   constexpr int TILE = BKV * HD * 2;         // bytes per K or V tile
   extern __shared__ __align__(128) uint8_t sm[];
@@ -254,10 +255,10 @@ cudaError_t launch_attention(const bf16* q, const bf16* knew, const bf16* vnew, 
       if (e != cudaSuccess) return e;
       set = true;
     }
-    fa::flash_kernel<128><<<grid, 128, smem, st>>>(q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2);
+    CK_RET(launch_pdl(fa::flash_kernel<128>, grid, dim3(128), smem, st, q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2));
   } else if (hd == 64) {
     constexpr int smem = fa::BQ * 64 * 2 + 4 * fa::BKV * 64 * 2;
-    fa::flash_kernel<64><<<grid, 128, smem, st>>>(q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2);
+    CK_RET(launch_pdl(fa::flash_kernel<64>, grid, dim3(128), smem, st, q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2));
   } else {
     return cudaErrorNotSupported;
   }

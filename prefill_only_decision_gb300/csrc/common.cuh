@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <utility>
 #include "internal.h"
 
 namespace s1 {
@@ -42,5 +44,38 @@ __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontro
 // Waits until the preceding grid in the stream has completed and its writes are visible (a
 // no-op for kernels launched without the attribute).
 __device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Returns a CUDA error from the enclosing launcher.
+#define CK_RET(x)                               \
+  do {                                          \
+    cudaError_t e_ = (x);                       \
+    if (e_ != cudaSuccess) return e_;           \
+  } while (0)
+
+// Programmatic dependent launch is on unless S1_PDL=0 (a measurement override).
+inline bool pdl_enabled() {
+  static const bool on = !(getenv("S1_PDL") && getenv("S1_PDL")[0] == '0');
+  return on;
+}
+
+// Launch with the programmatic-serialisation attribute: the kernel may start while its
+// predecessor in the stream finishes. Every kernel launched this way calls wait_prerequisites()
+// before its first access to data an earlier kernel wrote, in every CTA and before any early
+// return, so the completion of any kernel still implies the completion of all earlier ones.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 }  // namespace s1

@@ -17,6 +17,8 @@ namespace s1 {
 // proj row: [q (H*Dk) | k (H*Dk) | v (H*Dv) | a (H) | b (H)].
 __global__ void gdn_prep_kernel(float* __restrict__ proj, int ld, float* __restrict__ loga,
                                 float* __restrict__ beta, int H, int Dk, int Dv, float eps) {
+  allow_dependents();
+  wait_prerequisites();
   const int r = blockIdx.x;
   float* pr = proj + (size_t)r * ld;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -46,7 +48,7 @@ __global__ void gdn_prep_kernel(float* __restrict__ proj, int ld, float* __restr
 cudaError_t launch_gdn_prep(float* proj, int ld, float* loga, float* beta, int R, int H, int Dk,
                             int Dv, float eps, cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
-  gdn_prep_kernel<<<R, 256, 0, st>>>(proj, ld, loga, beta, H, Dk, Dv, eps);
+  CK_RET(launch_pdl(gdn_prep_kernel, dim3(R), dim3(256), 0, st, proj, ld, loga, beta, H, Dk, Dv, eps));
   return cudaGetLastError();
 }
 
@@ -59,6 +61,7 @@ __global__ void __launch_bounds__(128) gdn_scan_token_kernel(
     const float* __restrict__ beta, bf16* __restrict__ out, const SeqDesc* __restrict__ seqs,
     const CtxDesc* __restrict__ ctxs, int layer_g, int H, int Dv) {
   allow_dependents();
+  wait_prerequisites();
   constexpr int E = DK / 32;
   const int sq = blockIdx.x, h = blockIdx.y;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -151,9 +154,9 @@ cudaError_t launch_gdn_scan(const float* proj, int ld, const float* loga, const 
   if (Dk != Dv || (Dv % 16) != 0) return cudaErrorNotSupported;
   dim3 grid(n_seq, H, Dv / 16);
   if (Dk == 128)
-    gdn_scan_token_kernel<128><<<grid, 128, 0, st>>>(proj, ld, loga, beta, out, d_seq, d_ctx, layer_g, H, Dv);
+    CK_RET(launch_pdl(gdn_scan_token_kernel<128>, grid, dim3(128), 0, st, proj, ld, loga, beta, out, d_seq, d_ctx, layer_g, H, Dv));
   else if (Dk == 64)
-    gdn_scan_token_kernel<64><<<grid, 128, 0, st>>>(proj, ld, loga, beta, out, d_seq, d_ctx, layer_g, H, Dv);
+    CK_RET(launch_pdl(gdn_scan_token_kernel<64>, grid, dim3(128), 0, st, proj, ld, loga, beta, out, d_seq, d_ctx, layer_g, H, Dv));
   else
     return cudaErrorNotSupported;
   return cudaGetLastError();

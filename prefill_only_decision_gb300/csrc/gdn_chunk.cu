@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
                                                             const float* __restrict__ beta,
                                                             const ChunkDesc* __restrict__ chunks, int H, int Dv,
                                                             float* __restrict__ Wbuf, float* __restrict__ Ubuf) {
+  allow_dependents();
+  wait_prerequisites();
   using SM = PrepSmem<D>;
   constexpr int SX = SM::SX, SA = SM::SA, ST = SM::ST, S17 = SM::SM17;
   constexpr int NX = 2 * D;                 // columns of X
@@ -368,6 +370,8 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
                                                           const CtxDesc* __restrict__ ctxs, int layer_g, int H,
                                                           float* __restrict__ Ubuf, float* __restrict__ Schunk,
                                                           int* __restrict__ d_err) {
+  allow_dependents();
+  wait_prerequisites();
   extern __shared__ __align__(1024) uint8_t smraw[];
   using SM = StateSmem<D, NS>;
   constexpr int SS = SM::SS, SU = SM::SU, SUT = SM::SUT, NB = SM::NB;
@@ -588,6 +592,7 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
                                                         const float* __restrict__ Ubuf,
                                                         const float* __restrict__ Schunk, bf16* __restrict__ out) {
   allow_dependents();
+  wait_prerequisites();
   extern __shared__ __align__(16) uint8_t smraw[];
   using SM = OutSmem<D>;
   constexpr int SQ = SM::SQ, SSC = SM::SSC, SUo = SM::SUo, SP = SM::SP;
@@ -714,11 +719,11 @@ static cudaError_t launch_state(const CUtensorMap& mW, const CUtensorMap& mK, co
   if (n_seq <= 0) return cudaSuccess;
   const dim3 grid(n_seq, H, D / gc::BV);
   if (max_chunks <= 1) {
-    gc::chunk_state_kernel<D, 1><<<grid, 256, state_smem<D, 1>(), st>>>(mW, mK, mU, g, d_seq, d_chunks, d_ctx,
-                                                                        layer_g, H, Ubuf, Schunk, d_err);
+    CK_RET(launch_pdl(gc::chunk_state_kernel<D, 1>, grid, dim3(256), state_smem<D, 1>(), st, mW, mK, mU, g, d_seq,
+                      d_chunks, d_ctx, layer_g, H, Ubuf, Schunk, d_err));
   } else {
-    gc::chunk_state_kernel<D, 2><<<grid, 256, state_smem<D, 2>(), st>>>(mW, mK, mU, g, d_seq, d_chunks, d_ctx,
-                                                                        layer_g, H, Ubuf, Schunk, d_err);
+    CK_RET(launch_pdl(gc::chunk_state_kernel<D, 2>, grid, dim3(256), state_smem<D, 2>(), st, mW, mK, mU, g, d_seq,
+                      d_chunks, d_ctx, layer_g, H, Ubuf, Schunk, d_err));
   }
   return cudaGetLastError();
 }
@@ -745,7 +750,8 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, con
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  gc::chunk_prep_kernel<D><<<dim3(n_chunks, H), 256, sp, st>>>(proj, ld, loga, beta, d_chunks, H, D, Wbuf, Ubuf);
+  CK_RET(launch_pdl(gc::chunk_prep_kernel<D>, dim3(n_chunks, H), dim3(256), sp, st, proj, ld, loga, beta, d_chunks, H, D,
+                    Wbuf, Ubuf));
   // TMA views of the chunk tiles: W and Ut rows of head h ([R, H, D] fp32), K columns of proj
   CUtensorMap mW, mK, mU;
   {
@@ -771,7 +777,8 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, con
                         max_chunks_rest, d_err, st);
     if (e != cudaSuccess) return e;
   }
-  gc::chunk_out_kernel<D><<<dim3(n_chunks, H), 256, so, st>>>(proj, ld, loga, d_chunks, H, Ubuf, Schunk, out);
+  CK_RET(launch_pdl(gc::chunk_out_kernel<D>, dim3(n_chunks, H), dim3(256), so, st, proj, ld, loga, d_chunks, H, Ubuf,
+                    Schunk, out));
   return cudaGetLastError();
 }
 

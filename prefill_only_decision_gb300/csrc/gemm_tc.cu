@@ -739,6 +739,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // Sum of the split-K partials in split order, then the epilogue.
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int Mpad, int M, int N, int epi,
                                      void* __restrict__ out, int ldo) {
+  allow_dependents();
+  wait_prerequisites();
   const int cols = (epi == EPI_SWIGLU) ? N / 2 : N;
   const size_t total = (size_t)M * (cols / 4);
   for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < total; t += (size_t)gridDim.x * blockDim.x) {
@@ -1145,8 +1147,8 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
   const size_t work = (size_t)M * cols / 4;
   int blocks = (int)((work + 255) / 256);
   if (blocks > 4 * lc.num_sms) blocks = 4 * lc.num_sms;
-  tc::splitk_reduce_kernel<<<blocks, 256, 0, lc.stream>>>(splitk_ws, pl.splits, pl.m_tiles * tc::BM, M, N, epi,
-                                                           out, ldo);
+  CK_RET(launch_pdl(tc::splitk_reduce_kernel, dim3(blocks), dim3(256), 0, lc.stream, splitk_ws, pl.splits,
+                    pl.m_tiles * tc::BM, M, N, epi, out, ldo));
   if (lc.launches) *lc.launches += 1;
   return cudaGetLastError();
 }

@@ -33,6 +33,7 @@ template <int NV>   // float4 per lane: d = 128 * NV
 __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                            bf16* __restrict__ out, int R, int d, float eps) {
   allow_dependents();
+  wait_prerequisites();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (r >= R) return;
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restri
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                bf16* __restrict__ out, int d, float eps) {
   allow_dependents();
+  wait_prerequisites();
   __shared__ float red[32];
   const int r = blockIdx.x;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)r * d);
@@ -88,11 +90,11 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int
   if (R <= 0) return cudaSuccess;
   const int blocks = (R + 7) / 8;
   switch (d) {
-    case 256: rmsnorm_warp_kernel<2><<<blocks, 256, 0, st>>>(x, w, out, R, d, eps); break;
-    case 1024: rmsnorm_warp_kernel<8><<<blocks, 256, 0, st>>>(x, w, out, R, d, eps); break;
-    case 2560: rmsnorm_warp_kernel<20><<<blocks, 256, 0, st>>>(x, w, out, R, d, eps); break;
-    case 5120: rmsnorm_warp_kernel<40><<<blocks, 256, 0, st>>>(x, w, out, R, d, eps); break;
-    default: rmsnorm_kernel<<<R, 256, 0, st>>>(x, w, out, d, eps); break;
+    case 256: CK_RET(launch_pdl(rmsnorm_warp_kernel<2>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;
+    case 1024: CK_RET(launch_pdl(rmsnorm_warp_kernel<8>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;
+    case 2560: CK_RET(launch_pdl(rmsnorm_warp_kernel<20>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;
+    case 5120: CK_RET(launch_pdl(rmsnorm_warp_kernel<40>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;
+    default: CK_RET(launch_pdl(rmsnorm_kernel, dim3(R), dim3(256), 0, st, x, w, out, d, eps)); break;
   }
   return cudaGetLastError();
 }
@@ -105,6 +107,8 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
                                   const CtxDesc* __restrict__ ctxs, int layer_f, bf16* __restrict__ q,
                                   bf16* __restrict__ knew, bf16* __restrict__ vnew, int Hq, int Hkv,
                                   int hd) {
+  allow_dependents();
+  wait_prerequisites();
   const int r = blockIdx.x;
   const SeqDesc sd = seqs[row_seq[r]];
   const int pos = sd.pos0 + (r - sd.row0);
@@ -151,8 +155,8 @@ cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab,
                               bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,
                               cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
-  rope_split_kernel<<<R, 256, 0, st>>>(proj, ld, rope_tab, row_seq, d_seq, d_ctx, layer_f, q, knew,
-                                       vnew, Hq, Hkv, hd);
+  CK_RET(launch_pdl(rope_split_kernel, dim3(R), dim3(256), 0, st, proj, ld, rope_tab, row_seq, d_seq, d_ctx, layer_f,
+                    q, knew, vnew, Hq, Hkv, hd));
   return cudaGetLastError();
 }
 
