@@ -79,14 +79,15 @@ struct PrepSmem {
   float M[3][4 * SM17];                    // series scratch: N^(2^k) and products
   float g[C];
   float b[C];
+  float la[C];                             // log alpha
 };
 
 template <int D>
-__global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restrict__ proj, int ld,
+__global__ void __launch_bounds__(256, 2) chunk_prep_kernel(float* __restrict__ proj, int ld,
                                                             float* __restrict__ loga,
-                                                            const float* __restrict__ beta,
                                                             const ChunkDesc* __restrict__ chunks, int H, int Dv,
-                                                            float* __restrict__ Wbuf, float* __restrict__ Ubuf) {
+                                                            float eps, float* __restrict__ Wbuf,
+                                                            float* __restrict__ Ubuf) {
   allow_dependents();
   wait_prerequisites();
   using SM = PrepSmem<D>;
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
   const int h = blockIdx.y, n = cd.len, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   const int HDk = H * D;
-  // ---- load K (normalised) and V into X, g = cumsum(log alpha), beta
+  // ---- load K and V into X; gates from the a, b columns of the projection
   for (int i = tid; i < C * (D / 4); i += 256) {
     const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
     const bool ok = r < n;
@@ -107,9 +108,23 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
     cp16(&s.X[r * SX + D + c4], pr + 2 * HDk + h * Dv + c4, ok);
   }
   cp_commit();
+  if (tid < C) {
+    // alpha_t = exp(-softplus(a_t)), beta_t = sigmoid(b_t)
+    float la = 0.f, bt = 0.f;
+    if (tid < n) {
+      const float* ab = proj + (size_t)(cd.row0 + tid) * ld + 2 * HDk + H * Dv;
+      const float a = ab[h], b = ab[H + h];
+      la = -(fmaxf(a, 0.f) + log1pf(expf(-fabsf(a))));
+      bt = 1.f / (1.f + expf(-b));
+    }
+    s.la[tid] = la;
+    s.b[tid] = bt;
+  }
+  cp_wait<0>();
+  __syncthreads();
+  // g = cumsum(log alpha) within the chunk (one warp, two rows per lane)
   if (tid < 32) {
-    const float a0 = (2 * tid < n) ? loga[(size_t)(cd.row0 + 2 * tid) * H + h] : 0.f;
-    const float a1 = (2 * tid + 1 < n) ? loga[(size_t)(cd.row0 + 2 * tid + 1) * H + h] : 0.f;
+    const float a0 = s.la[2 * tid], a1 = s.la[2 * tid + 1];
     float v = a0 + a1;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -119,11 +134,36 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
     const float excl = v - (a0 + a1);
     s.g[2 * tid] = excl + a0;
     s.g[2 * tid + 1] = excl + a0 + a1;
-  } else if (tid < 32 + C) {
-    const int r = tid - 32;
-    s.b[r] = (r < n) ? beta[(size_t)(cd.row0 + r) * H + h] : 0.f;
   }
-  cp_wait<0>();
+  // k <- k / sqrt(sum k^2 + eps), rounded to TF32 (every later product of k runs on TF32 tensor-core
+  // inputs), in shared memory and back in the projection for the later kernels; four threads per
+  // row. (q is normalised the same way where it is used, in chunk_out.)
+  {
+    constexpr int PER = D / 4;
+    const int r = tid >> 2, sub = tid & 3;
+    float* xs = &s.X[r * SX + sub * PER];
+    float v[PER];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; i += 4) {
+      const float4 t = *reinterpret_cast<const float4*>(xs + i);
+      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) ss += v[i] * v[i];
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float inv = 1.0f / sqrtf(ss + eps);
+    if (r < n) {
+      float* kg = proj + (size_t)(cd.row0 + r) * ld + HDk + h * D + sub * PER;
+#pragma unroll
+      for (int i = 0; i < PER; i += 4) {
+        const float4 t = make_float4(rnd(v[i] * inv), rnd(v[i + 1] * inv), rnd(v[i + 2] * inv), rnd(v[i + 3] * inv));
+        *reinterpret_cast<float4*>(xs + i) = t;
+        *reinterpret_cast<float4*>(kg + i) = t;
+      }
+    }
+  }
   __syncthreads();
   // ---- A = strict_lower(beta_t exp(g_t - g_s) k_t.k_s): warp -> m-tile (warp & 3), 4 n-tiles
   {
@@ -385,14 +425,19 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
   const int gq = lane >> 2, tq = lane & 3;
   const int HDk = H * D;
   const int nch = (sd.len + C - 1) / C;
+  // followers: single-chunk sequences continuing from this one's final state; each adds one
+  // step after the last chunk (U and the chunk-start record from the final state, no update)
+  const int nf = sd.fol1 > sd.fol0 ? sd.fol1 - sd.fol0 : 0;
+  const int nsteps = nch + nf;
+  auto chunk_of = [&](int cl) { return cl < nch ? sd.chunk0 + cl : seqs[sd.fol0 + (cl - nch)].chunk0; };
   const size_t head_off = (size_t)(layer_g * H + h) * D * D;
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) bar_init(&s.full[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  auto issue = [&](int cl, int st) {   // one thread: TMA of chunk cl's tiles into stage st
-    const ChunkDesc cd = chunks[sd.chunk0 + cl];
+  auto issue = [&](int cl, int st) {   // one thread: TMA of step cl's tiles into stage st
+    const ChunkDesc cd = chunks[chunk_of(cl)];
     bar_expect_tx(&s.full[st], TILE_BYTES);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -402,11 +447,11 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
     tma3(&s.Ut[st][0], &mapUt, &s.full[st], v0, h, cd.row0);
   };
   auto load_g = [&](int cl, int st) {
-    const ChunkDesc cd = chunks[sd.chunk0 + cl];
+    const ChunkDesc cd = chunks[chunk_of(cl)];
     if (tid < C) cp4(&s.g[st][tid], gbuf + (size_t)(cd.row0 + (tid < cd.len ? tid : 0)) * H + h, tid < cd.len);
   };
-  if (nch > 0 && tid == 0) issue(0, 0);
-  if (nch > 0) load_g(0, 0);
+  if (nsteps > 0 && tid == 0) issue(0, 0);
+  if (nsteps > 0) load_g(0, 0);
   cp_commit();
   // initial state block: fp32 and TF32-rounded copies
   const float* S0 = sd.ctx_in >= 0 ? ctxs[sd.ctx_in].S + head_off : nullptr;
@@ -417,11 +462,12 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
     s.Sr[(c >> 5) * (BV * 32) + swz32(r, c & 31)] = rnd(v);
   }
   bool ok = true;
-  for (int cl = 0; cl < nch; ++cl) {
+  for (int cl = 0; cl < nsteps; ++cl) {
     const int st = NS == 2 ? (cl & 1) : 0;
-    const ChunkDesc cd = chunks[sd.chunk0 + cl];
+    const int ci = chunk_of(cl);
+    const ChunkDesc cd = chunks[ci];
     if (NS == 2) {
-      if (cl + 1 < nch) {
+      if (cl + 1 < nsteps) {
         if (tid == 0) issue(cl + 1, st ^ 1);
         load_g(cl + 1, st ^ 1);
       }
@@ -448,7 +494,7 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
     }
     // record the chunk-start state block (already rounded) for chunk_out
     {
-      float* dst = Schunk + ((size_t)(sd.chunk0 + cl) * H + h) * D * D + (size_t)v0 * D;
+      float* dst = Schunk + ((size_t)ci * H + h) * D * D + (size_t)v0 * D;
       for (int i = tid; i < BV * (D / 4); i += NTH) {
         const int r = i / (D / 4), c = (i % (D / 4)) * 4;
         *reinterpret_cast<float4*>(dst + (size_t)r * D + c) =
@@ -501,8 +547,9 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
           make_float4(s.U[r * SU + c4], s.U[r * SU + c4 + 1], s.U[r * SU + c4 + 2], s.U[r * SU + c4 + 3]);
     }
     // S <- gamma_n S + Us^T K : warp -> value rows 0..15, key columns 8*NTS*warp .. (NTS n-tiles)
-    // (not needed after the last chunk of a sequence whose final state nobody keeps)
-    if (cl + 1 < nch || sd.ctx_out >= 0) {
+    // (not needed after the last chunk of a sequence whose final state nobody keeps, nor for
+    // followers)
+    if (cl < nch && (cl + 1 < nch || sd.ctx_out >= 0)) {
       const float gam = __expf(s.g[st][cd.len - 1]);
       float acc[NTS][4], acc2[NTS][4];
 #pragma unroll
@@ -588,7 +635,7 @@ struct OutSmem {
 template <int D>
 __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict__ proj, int ld,
                                                         const float* __restrict__ gbuf,
-                                                        const ChunkDesc* __restrict__ chunks, int H,
+                                                        const ChunkDesc* __restrict__ chunks, int H, float eps,
                                                         const float* __restrict__ Ubuf,
                                                         const float* __restrict__ Schunk, bf16* __restrict__ out) {
   allow_dependents();
@@ -619,6 +666,29 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
   if (tid < C) s.g[tid] = tid < n ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
   cp_commit();
   cp_wait<0>();
+  __syncthreads();
+  // q <- q / sqrt(sum q^2 + eps), rounded to TF32 (as k is in chunk_prep); four threads per row
+  {
+    constexpr int PER = D / 4;
+    const int r = tid >> 2, sub = tid & 3;
+    float* xs = &s.Q[r * SQ + sub * PER];
+    float v[PER];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; i += 4) {
+      const float4 t = *reinterpret_cast<const float4*>(xs + i);
+      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) ss += v[i] * v[i];
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float inv = 1.0f / sqrtf(ss + eps);
+#pragma unroll
+    for (int i = 0; i < PER; i += 4)
+      *reinterpret_cast<float4*>(xs + i) =
+          make_float4(rnd(v[i] * inv), rnd(v[i + 1] * inv), rnd(v[i + 2] * inv), rnd(v[i + 3] * inv));
+  }
   __syncthreads();
   const int mt = warp & 3;          // 16-row m-tile
   const int r0 = mt * 16;
@@ -729,11 +799,11 @@ static cudaError_t launch_state(const CUtensorMap& mW, const CUtensorMap& mK, co
 }
 
 template <int D>
-static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, const float* beta, bf16* out,
+static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, float eps, bf16* out,
                                     const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                     const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
                                     float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                                    int* d_err, cudaStream_t st) {
+                                    int fold_from, int* d_err, cudaStream_t st) {
   static bool attr = false;
   const size_t sp = sizeof(gc::PrepSmem<D>);
   const size_t so = sizeof(gc::OutSmem<D>);
@@ -750,7 +820,7 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, con
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  CK_RET(launch_pdl(gc::chunk_prep_kernel<D>, dim3(n_chunks, H), dim3(256), sp, st, proj, ld, loga, beta, d_chunks, H, D,
+  CK_RET(launch_pdl(gc::chunk_prep_kernel<D>, dim3(n_chunks, H), dim3(256), sp, st, proj, ld, loga, d_chunks, H, D, eps,
                     Wbuf, Ubuf));
   // TMA views of the chunk tiles: W and Ut rows of head h ([R, H, D] fp32), K columns of proj
   CUtensorMap mW, mK, mU;
@@ -766,38 +836,44 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, con
         !tensor_map(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, proj, dims2, str2, boxK, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  // sequences [0, n_first) run before the rest (the rest continue from their states)
+  // sequences [0, n_first) run before the rest (the rest continue from their states); a group
+  // from fold_from on (single-chunk sequences that keep no state) needs no state pass at all:
+  // chunk_out forms their U itself
   const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
-  cudaError_t e = launch_state<D>(mW, mK, mU, loga, d_seq, split, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
+  const int n1 = std::min(split, fold_from);
+  cudaError_t e = launch_state<D>(mW, mK, mU, loga, d_seq, n1, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
                                   split < n_seq ? max_chunks_first : std::max(max_chunks_first, max_chunks_rest),
                                   d_err, st);
   if (e != cudaSuccess) return e;
-  if (split < n_seq) {
+  if (split < n_seq && fold_from > split) {
     e = launch_state<D>(mW, mK, mU, loga, d_seq + split, n_seq - split, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
                         max_chunks_rest, d_err, st);
     if (e != cudaSuccess) return e;
   }
-  CK_RET(launch_pdl(gc::chunk_out_kernel<D>, dim3(n_chunks, H), dim3(256), so, st, proj, ld, loga, d_chunks, H, Ubuf,
-                    Schunk, out));
+  CK_RET(launch_pdl(gc::chunk_out_kernel<D>, dim3(n_chunks, H), dim3(256), so, st, proj, ld, loga, d_chunks, H, eps,
+                    Ubuf, Schunk, out));
   return cudaGetLastError();
 }
 
-cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, const float* beta, bf16* out,
+cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float eps, bf16* out,
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                               int* d_err, cudaStream_t st, long* launches) {
+                               int fold_from, int* d_err, cudaStream_t st, long* launches) {
   if (n_seq <= 0 || n_chunks <= 0) return cudaSuccess;
   if (!gdn_chunked_supported(H, Dk, Dv, ld)) return cudaErrorNotSupported;
   if (n_seq > 65535 || n_chunks > 2147483647 / 2) return cudaErrorInvalidValue;
   cudaError_t e = (Dk == 128)
-                      ? launch_chunked_d<128>(proj, ld, R, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
+                      ? launch_chunked_d<128>(proj, ld, R, loga, eps, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                               layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
-                                              max_chunks_rest, d_err, st)
-                      : launch_chunked_d<64>(proj, ld, R, loga, beta, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
+                                              max_chunks_rest, fold_from, d_err, st)
+                      : launch_chunked_d<64>(proj, ld, R, loga, eps, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                              layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
-                                             max_chunks_rest, d_err, st);
-  if (launches) *launches += (n_first > 0 && n_first < n_seq) ? 4 : 3;
+                                             max_chunks_rest, fold_from, d_err, st);
+  if (launches) {
+    const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
+    *launches += 2 + (std::min(split, fold_from) > 0 ? 1 : 0) + (split < n_seq && fold_from > split ? 1 : 0);
+  }
   return e;
 }
 

@@ -26,6 +26,9 @@ struct SeqDesc {
   int ctx_in;   // context continued (-1: start from zero state / no cached keys)
   int ctx_out;  // context whose snapshot this sequence writes (-1: none)
   int chunk0;   // index of its first 64-row chunk in the chunk table
+  int fol0, fol1;   // gated delta rule: single-chunk sequences [fol0, fol1) that continue from this
+                    // one's final state and keep none of their own (their U and chunk-start state
+                    // come from this sequence's state pass; empty if fol1 <= fol0)
 };
 
 // 64-row chunks of the sequences (chunk boundaries restart at every sequence start).
@@ -82,11 +85,11 @@ cudaError_t launch_gdn_scan(const float* proj, int ld, const float* alpha, const
                             bf16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
                             int layer_g, int H, int Dk, int Dv, cudaStream_t st);
 bool gdn_chunked_supported(int H, int Dk, int Dv, int ld);
-cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, const float* beta, bf16* out,
+cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float l2_eps, bf16* out,
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                               int* d_err, cudaStream_t st, long* launches);
+                               int fold_from, int* d_err, cudaStream_t st, long* launches);
 cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab, const int* row_seq,
                               const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, bf16* q,
                               bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,

@@ -101,8 +101,7 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
   OCK(cudaMemcpyAsync(dctx, ctxs.data(), ctxs.size() * sizeof(CtxDesc), cudaMemcpyHostToDevice, st));
   if (nch) OCK(cudaMemcpyAsync(dch, chunks.data(), nch * sizeof(ChunkDesc), cudaMemcpyHostToDevice, st));
   const int ld = 2 * H * dk + H * dv + 2 * H;
-  OCK(launch_gdn_prep(proj, ld, loga, beta, R, H, dk, dv, l2_eps, st));
-  if (gdn_chunked_supported(H, dk, dv, ld)) {
+  if (gdn_chunked_supported(H, dk, dv, ld)) {   // normalisation and gates inside the chunked kernels
     float* W = (float*)t.get((size_t)R * H * dk * 4 + 16);
     float* U = (float*)t.get((size_t)R * H * dv * 4 + 16);
     float* Sc = (float*)t.get((size_t)(nch + 1) * per * 4);
@@ -111,13 +110,14 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
     OCK(cudaMemsetAsync(err, 0, 256, st));
     int maxc = 0;
     for (int q = 0; q < n_seq; ++q) maxc = std::max(maxc, (len[q] + GDN_CHUNK - 1) / GDN_CHUNK);
-    OCK(launch_gdn_chunked(proj, ld, R, loga, beta, (bf16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
-                           0, maxc, maxc, err, st, nullptr));
+    OCK(launch_gdn_chunked(proj, ld, R, loga, l2_eps, (bf16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
+                           0, maxc, maxc, n_seq, err, st, nullptr));
     int herr = 0;
     OCK(cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
     OCK(cudaStreamSynchronize(st));
     if (herr) return op_fail(S1_ERR_DEVICE_TIMEOUT, "gdn: a bounded device wait gave up");
   } else {
+    OCK(launch_gdn_prep(proj, ld, loga, beta, R, H, dk, dv, l2_eps, st));
     OCK(launch_gdn_scan(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dctx, 0, H, dk, dv, st));
   }
   OCK(cudaStreamSynchronize(st));

@@ -271,6 +271,8 @@ struct Meta {
   int max_len = 0, max_opts = 0;
   int n_first = 0;   // fused sweep: the first n_first sequences (prefixes) scan before the rest
   int max_chunks_first = 0, max_chunks_rest = 0;   // longest sequence (in chunks) of each group
+  // sequences from fold_from on are handled by their prefixes' state pass (see build_chunks)
+  int fold_from = 0;
   // device views
   int* d_row_src = nullptr;
   int* d_row_seq = nullptr;
@@ -291,6 +293,36 @@ void build_chunks(Meta& mt) {
     const int nc = (sd.len + GDN_CHUNK - 1) / GDN_CHUNK;
     int& mx = ((int)s < mt.n_first) ? mt.max_chunks_first : mt.max_chunks_rest;
     mx = std::max(mx, nc);
+  }
+  // Fused sweep: when every later sequence is a single chunk that keeps no state and continues
+  // a prefix of this call (contiguously per prefix), the prefixes' state pass also produces the
+  // later sequences' U and chunk-start states, and they get no state pass of their own.
+  const int n = (int)mt.seqs.size();
+  mt.fold_from = n;
+  if (mt.n_first > 0 && mt.n_first < n) {
+    std::vector<int> owner(mt.ctxs.size(), -1);
+    for (int p = 0; p < mt.n_first; ++p)
+      if (mt.seqs[p].ctx_out >= 0 && mt.seqs[p].ctx_out < (int)owner.size()) owner[mt.seqs[p].ctx_out] = p;
+    bool ok = true;
+    for (int s = mt.n_first; s < n && ok; ++s) {
+      const SeqDesc& q = mt.seqs[s];
+      const int p = (q.ctx_in >= 0 && q.ctx_in < (int)owner.size()) ? owner[q.ctx_in] : -1;
+      if (q.len > GDN_CHUNK || q.ctx_out >= 0 || p < 0) { ok = false; break; }
+      SeqDesc& ps = mt.seqs[p];
+      if (ps.fol1 <= ps.fol0) { ps.fol0 = s; ps.fol1 = s + 1; }
+      else if (ps.fol1 == s) ps.fol1 = s + 1;
+      else ok = false;
+    }
+    if (ok) {
+      mt.fold_from = mt.n_first;
+      for (int p = 0; p < mt.n_first; ++p) {
+        const SeqDesc& ps = mt.seqs[p];
+        const int nf = ps.fol1 > ps.fol0 ? ps.fol1 - ps.fol0 : 0;
+        mt.max_chunks_first = std::max(mt.max_chunks_first, (ps.len + GDN_CHUNK - 1) / GDN_CHUNK + nf);
+      }
+    } else {
+      for (int p = 0; p < mt.n_first; ++p) mt.seqs[p].fol0 = mt.seqs[p].fol1 = 0;
+    }
   }
 }
 
@@ -384,23 +416,24 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
       const int H = s.la_heads;
       {
         ProfScope ps(m, S1_PROF_GDN, 0, 0);
-        CK(launch_gdn_prep(sc.proj, L.n_in, sc.loga, sc.beta, R, H, s.la_dk, s.la_dv, s.l2_eps, st));
-        m->launches += 1;
         const int nch = (int)mt.chunks.size();
         if (!m->gdn_token && gdn_chunked_supported(H, s.la_dk, s.la_dv, L.n_in)) {
+          // (the chunked path normalises q, k and forms the gates inside its first kernel)
           if ((size_t)nch > m->schunk_chunks) {
             CK(cudaStreamSynchronize(st));
             dfree(m->schunk);
-  dfree(m->lm_buf);
             const size_t cap = std::max<size_t>(nch, 2 * m->schunk_chunks);
             m->schunk = (float*)dalloc(cap * H * (size_t)s.la_dv * s.la_dk * 4);
             m->schunk_chunks = m->schunk ? cap : 0;
             if (!m->schunk) return fail(S1_ERR_OOM, "chunk-state buffer (%zu chunks) allocation failed", cap);
           }
-          CK(launch_gdn_chunked(sc.proj, L.n_in, R, sc.loga, sc.beta, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
+          CK(launch_gdn_chunked(sc.proj, L.n_in, R, sc.loga, s.l2_eps, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
                                 mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first,
-                                mt.max_chunks_first, mt.max_chunks_rest, m->d_err, st, &m->launches));
+                                mt.max_chunks_first, mt.max_chunks_rest, mt.fold_from, m->d_err, st,
+                                &m->launches));
         } else {
+          CK(launch_gdn_prep(sc.proj, L.n_in, sc.loga, sc.beta, R, H, s.la_dk, s.la_dv, s.l2_eps, st));
+          m->launches += 1;
           const int split = (mt.n_first > 0 && mt.n_first < nseq) ? mt.n_first : nseq;
           CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, split, mt.d_ctxs,
                              L.ord, H, s.la_dk, s.la_dv, st));

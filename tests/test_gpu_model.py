@@ -340,3 +340,20 @@ def test_tiny_lm_logprobs_vs_oracle(tiny, tiny_weights, tiny_requests):
         # renormalised over the options they give back the option probabilities
         np.testing.assert_allclose(np.exp(g["lm_logprobs"] - logsumexp(g["lm_logprobs"])), g["probs"], atol=1e-4)
         assert np.all(g["lm_logprobs"] < 0)
+
+
+def test_lm_logprobs_survive_chunk_state_growth(B, tiny_weights, tiny_requests):
+    """Full-vocabulary log-probabilities stay correct after a longer prefix has grown the
+    model's per-chunk state buffer between two calls (the buffers are reallocated separately)."""
+    m = B.Model(tiny_weights)
+    try:
+        r = tiny_requests[0]
+        first = m.decide(m.prefill(r.tokens), r.questions, want_lm=True)
+        long_tokens = np.concatenate([r.tokens] * 8)            # many more chunks than before
+        m.decide(m.prefill(long_tokens), r.questions, want_lm=True)
+        again = m.decide(m.prefill(r.tokens), r.questions, want_lm=True)
+        for a, b in zip(first, again):
+            assert np.array_equal(a["lm_logprobs"], b["lm_logprobs"])
+            assert np.array_equal(a["probs"], b["probs"])
+    finally:
+        m.close()
