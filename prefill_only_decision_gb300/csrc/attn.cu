@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
   uint8_t* sV = sK + 2 * TILE;               // 2 stages
 
   const SeqDesc sd = seqs[blockIdx.z];
-  const int q0 = blockIdx.x * BQ;
+  // the last (longest-key-range) query tiles first, so the heavy CTAs do not form the tail
+  const int q0 = (gridDim.x - 1 - blockIdx.x) * BQ;
   if (q0 >= sd.len) return;
   const int h = blockIdx.y;
   const int g = (h * Hkv) / Hq;

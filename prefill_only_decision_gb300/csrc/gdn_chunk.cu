@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(float* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------------------
-// chunk_state: one CTA per (sequence, head, block of 16 value rows), 256 threads (8 warps).
+// chunk_state: one CTA per (sequence, head, block of 16 value rows), 512 threads (16 warps).
 // Per chunk: U = Ut - W S^T (64 x 16, K = D); S <- gamma_n S + U^T K' (16 x D, K = 64),
 // K'_t = exp(g_n - g_t) k_t. Records each chunk's start state (TF32-rounded, for chunk_out)
 // and writes U over Ut. The state block stays in shared memory in fp32, next to a TF32-rounded
@@ -335,9 +335,9 @@ struct StateSmem {
   float S[BV * SS];
   float U[C * SU];                      // U (TF32-rounded), written back for chunk_out
   float UsT[BV * SUT];                  // exp(g_n - g_t) U_t, transposed (TF32-rounded)
+  float Up[C * BV];                     // second key half's partial W S^T
   float g[NS][C];
   uint64_t full[NS];
-  int flag;
 };
 
 // float index of (row, col) in a 128-byte-swizzled box of 32 fp32 columns
@@ -396,14 +396,27 @@ __device__ __forceinline__ void tma3(void* dst, const CUtensorMap* map, uint64_t
       : "memory");
 }
 
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tma_store2(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Maps: mapW over Wbuf [R, H, D] (box 32 x 1 x 64, swizzled), mapUt over Ubuf [R, H, D] (box
-// 16 x 1 x 64, dense), mapK over proj [R, ld] (box 32 x 64, swizzled).
+// 16 x 1 x 64, dense), mapK over proj [R, ld] (box 32 x 64, swizzled), mapSc over the chunk-start
+// records [n_chunks * H * D, D] (box 32 x 16, swizzled like Sr).
 // NS = 1 serves launches whose sequences have a single chunk (half the shared memory, two CTAs
 // per SM).
 template <int D, int NS>
-__global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant__ CUtensorMap mapW,
+__global__ void __launch_bounds__(512) chunk_state_kernel(const __grid_constant__ CUtensorMap mapW,
                                                           const __grid_constant__ CUtensorMap mapK,
                                                           const __grid_constant__ CUtensorMap mapUt,
+                                                          const __grid_constant__ CUtensorMap mapSc,
                                                           const float* __restrict__ gbuf,
                                                           const SeqDesc* __restrict__ seqs,
                                                           const ChunkDesc* __restrict__ chunks,
@@ -415,8 +428,8 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
   extern __shared__ __align__(1024) uint8_t smraw[];
   using SM = StateSmem<D, NS>;
   constexpr int SS = SM::SS, SU = SM::SU, SUT = SM::SUT, NB = SM::NB;
-  constexpr int NTS = D / 64;            // 8-column n-tiles per warp in the state update
-  constexpr int NTH = 256;
+  constexpr int NTH = 512;               // 16 warps
+  constexpr int NUPD = D / 8;            // warps of the state update (one 8-column n-tile each)
   constexpr uint32_t TILE_BYTES = 2 * C * D * 4 + C * BV * 4;
   SM& s = *reinterpret_cast<SM*>((((uintptr_t)smraw) + 1023) & ~(uintptr_t)1023);
   const SeqDesc sd = seqs[blockIdx.x];
@@ -436,8 +449,15 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  auto issue = [&](int cl, int st) {   // one thread: TMA of step cl's tiles into stage st
-    const ChunkDesc cd = chunks[chunk_of(cl)];
+  // step descriptors (chunk index + chunk) are fetched two steps ahead, so no step waits on a
+  // global load before issuing its TMA or using its row range
+  struct Step { int ci; ChunkDesc cd; };
+  auto fetch = [&](int cl) -> Step {
+    if (cl >= nsteps) return Step{0, ChunkDesc{0, 1, 0}};
+    const int ci = chunk_of(cl);
+    return Step{ci, chunks[ci]};
+  };
+  auto issue = [&](const ChunkDesc& cd, int st) {   // one thread: TMA of a step's tiles into stage st
     bar_expect_tx(&s.full[st], TILE_BYTES);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -446,12 +466,12 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
     }
     tma3(&s.Ut[st][0], &mapUt, &s.full[st], v0, h, cd.row0);
   };
-  auto load_g = [&](int cl, int st) {
-    const ChunkDesc cd = chunks[chunk_of(cl)];
+  auto load_g = [&](const ChunkDesc& cd, int st) {
     if (tid < C) cp4(&s.g[st][tid], gbuf + (size_t)(cd.row0 + (tid < cd.len ? tid : 0)) * H + h, tid < cd.len);
   };
-  if (nsteps > 0 && tid == 0) issue(0, 0);
-  if (nsteps > 0) load_g(0, 0);
+  Step s0 = fetch(0), s1 = fetch(1);
+  if (nsteps > 0 && tid == 0) issue(s0.cd, 0);
+  if (nsteps > 0) load_g(s0.cd, 0);
   cp_commit();
   // initial state block: fp32 and TF32-rounded copies
   const float* S0 = sd.ctx_in >= 0 ? ctxs[sd.ctx_in].S + head_off : nullptr;
@@ -461,56 +481,58 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
     s.S[r * SS + c] = v;
     s.Sr[(c >> 5) * (BV * 32) + swz32(r, c & 31)] = rnd(v);
   }
+  fence_async_smem();   // Sr is read by bulk stores
   bool ok = true;
   for (int cl = 0; cl < nsteps; ++cl) {
     const int st = NS == 2 ? (cl & 1) : 0;
-    const int ci = chunk_of(cl);
-    const ChunkDesc cd = chunks[ci];
+    const Step s2 = fetch(cl + 2);   // used two steps from now
+    const int ci = s0.ci;
+    const ChunkDesc cd = s0.cd;
     if (NS == 2) {
       if (cl + 1 < nsteps) {
-        if (tid == 0) issue(cl + 1, st ^ 1);
-        load_g(cl + 1, st ^ 1);
+        if (tid == 0) issue(s1.cd, st ^ 1);
+        load_g(s1.cd, st ^ 1);
       }
       cp_commit();
       cp_wait<1>();
     } else {
       if (cl > 0) {   // single stage: the previous chunk's tiles are no longer read
-        if (tid == 0) issue(cl, 0);
-        load_g(cl, 0);
+        if (tid == 0) issue(cd, 0);
+        load_g(cd, 0);
       }
       cp_commit();
       cp_wait<0>();
     }
-    // one thread waits (bounded) for the chunk's tiles; the others then find the phase complete
+    s0 = s1;
+    s1 = s2;
+    // every thread waits (bounded) for the chunk's tiles; one barrier agrees on the outcome, so
+    // all threads take the same path
     const uint32_t parity = NS == 2 ? ((cl >> 1) & 1) : (cl & 1);
-    if (tid == 0) s.flag = bar_wait(&s.full[st], parity) ? 1 : 0;
-    __syncthreads();
-    if (!s.flag) {
+    if (!__syncthreads_and(bar_wait(&s.full[st], parity) ? 1 : 0)) {
       if (tid == 0) atomicExch(d_err, 0x201);
       ok = false;
       break;
     }
-    while (!bar_try(&s.full[st], parity)) {
+    // record the chunk-start state block (already rounded, in the map's swizzled box layout) for
+    // chunk_out: one bulk store per 32-column box, read asynchronously from Sr
+    if (tid == 0) {
+      fence_async_smem();
+      const int y = (ci * H + h) * D + v0;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) tma_store2(&mapSc, &s.Sr[b * (BV * 32)], 32 * b, y);
+      bulk_commit();
     }
-    // record the chunk-start state block (already rounded) for chunk_out
-    {
-      float* dst = Schunk + ((size_t)ci * H + h) * D * D + (size_t)v0 * D;
-      for (int i = tid; i < BV * (D / 4); i += NTH) {
-        const int r = i / (D / 4), c = (i % (D / 4)) * 4;
-        *reinterpret_cast<float4*>(dst + (size_t)r * D + c) =
-            *reinterpret_cast<const float4*>(&s.Sr[(c >> 5) * (BV * 32) + swz32(r, c & 31)]);
-      }
-    }
-    // U = Ut - W S^T : warp -> rows 16*(warp&3) .., value columns 8*(warp>>2) .. +7
+    // U = Ut - W S^T : warp -> rows 16*(warp&3) .., value columns 8*((warp>>2)&1) .. +7, key
+    // half (warp>>3) of the contraction; the two halves meet in shared memory
     {
       float a0c[4] = {0.f, 0.f, 0.f, 0.f}, a1c[4] = {0.f, 0.f, 0.f, 0.f};
       const float* Wt = s.W[st];
-      const int r0 = (warp & 3) * 16, n0 = (warp >> 2) * 8;
+      const int r0 = (warp & 3) * 16, n0 = ((warp >> 2) & 1) * 8, kh = warp >> 3;
       const int mi = lane >> 3;
       const int arow = r0 + (lane & 7) + 8 * (mi & 1), acol = 4 * (mi >> 1);   // A: ldmatrix lane row
       const int brow = n0 + (lane & 7), bcol = 4 * mi;                          // B: ldmatrix lane row
-#pragma unroll 4
-      for (int k = 0; k < D; k += 16) {
+#pragma unroll
+      for (int k = kh * (D / 2); k < (kh + 1) * (D / 2); k += 16) {
         uint32_t x0, x1, x2, x3, y0, y1, y2, y3, b0, b1, b2, b3;
         {
           const int c = k + acol;
@@ -525,19 +547,30 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
       }
       const int c = n0 + 2 * tq;
       const int ra = r0 + gq, rb = r0 + gq + 8;
-      const float gn = s.g[st][cd.len - 1];
-      const float ea = __expf(gn - s.g[st][ra]), eb = __expf(gn - s.g[st][rb]);
-      const float u0 = s.Ut[st][ra * BV + c] - (a0c[0] + a1c[0]), u1 = s.Ut[st][ra * BV + c + 1] - (a0c[1] + a1c[1]);
-      const float u2 = s.Ut[st][rb * BV + c] - (a0c[2] + a1c[2]), u3 = s.Ut[st][rb * BV + c + 1] - (a0c[3] + a1c[3]);
-      s.U[ra * SU + c] = rnd(u0);
-      s.U[ra * SU + c + 1] = rnd(u1);
-      s.U[rb * SU + c] = rnd(u2);
-      s.U[rb * SU + c + 1] = rnd(u3);
-      const bool oka = ra < cd.len, okb = rb < cd.len;
-      s.UsT[c * SUT + ra] = oka ? rnd(ea * u0) : 0.f;
-      s.UsT[(c + 1) * SUT + ra] = oka ? rnd(ea * u1) : 0.f;
-      s.UsT[c * SUT + rb] = okb ? rnd(eb * u2) : 0.f;
-      s.UsT[(c + 1) * SUT + rb] = okb ? rnd(eb * u3) : 0.f;
+      if (kh == 1) {
+        s.Up[ra * BV + c] = a0c[0] + a1c[0];
+        s.Up[ra * BV + c + 1] = a0c[1] + a1c[1];
+        s.Up[rb * BV + c] = a0c[2] + a1c[2];
+        s.Up[rb * BV + c + 1] = a0c[3] + a1c[3];
+      }
+      __syncthreads();
+      if (kh == 0) {
+        const float gn = s.g[st][cd.len - 1];
+        const float ea = __expf(gn - s.g[st][ra]), eb = __expf(gn - s.g[st][rb]);
+        const float u0 = s.Ut[st][ra * BV + c] - ((a0c[0] + a1c[0]) + s.Up[ra * BV + c]);
+        const float u1 = s.Ut[st][ra * BV + c + 1] - ((a0c[1] + a1c[1]) + s.Up[ra * BV + c + 1]);
+        const float u2 = s.Ut[st][rb * BV + c] - ((a0c[2] + a1c[2]) + s.Up[rb * BV + c]);
+        const float u3 = s.Ut[st][rb * BV + c + 1] - ((a0c[3] + a1c[3]) + s.Up[rb * BV + c + 1]);
+        s.U[ra * SU + c] = rnd(u0);
+        s.U[ra * SU + c + 1] = rnd(u1);
+        s.U[rb * SU + c] = rnd(u2);
+        s.U[rb * SU + c + 1] = rnd(u3);
+        const bool oka = ra < cd.len, okb = rb < cd.len;
+        s.UsT[c * SUT + ra] = oka ? rnd(ea * u0) : 0.f;
+        s.UsT[(c + 1) * SUT + ra] = oka ? rnd(ea * u1) : 0.f;
+        s.UsT[c * SUT + rb] = okb ? rnd(eb * u2) : 0.f;
+        s.UsT[(c + 1) * SUT + rb] = okb ? rnd(eb * u3) : 0.f;
+      }
     }
     __syncthreads();
     // write U (this block's 16 value columns) over Ut
@@ -546,46 +579,41 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
       *reinterpret_cast<float4*>(Ubuf + ((size_t)(cd.row0 + r) * H + h) * D + v0 + c4) =
           make_float4(s.U[r * SU + c4], s.U[r * SU + c4 + 1], s.U[r * SU + c4 + 2], s.U[r * SU + c4 + 3]);
     }
-    // S <- gamma_n S + Us^T K : warp -> value rows 0..15, key columns 8*NTS*warp .. (NTS n-tiles)
+    // S <- gamma_n S + Us^T K : warp w < D/8 -> value rows 0..15, key columns 8w .. 8w+7
     // (not needed after the last chunk of a sequence whose final state nobody keeps, nor for
     // followers)
     if (cl < nch && (cl + 1 < nch || sd.ctx_out >= 0)) {
       const float gam = __expf(s.g[st][cd.len - 1]);
-      float acc[NTS][4], acc2[NTS][4];
+      const bool upd = warp < NUPD;
+      const int c = warp * 8 + 2 * tq;   // this lane's output columns c, c+1 (warp's n-tile)
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+      if (upd) {
+        acc[0] = gam * s.S[gq * SS + c];
+        acc[1] = gam * s.S[gq * SS + c + 1];
+        acc[2] = gam * s.S[(gq + 8) * SS + c];
+        acc[3] = gam * s.S[(gq + 8) * SS + c + 1];
+        const float* Kt = s.K[st];
+        const int mi = lane >> 3;
+        const int arow = (lane & 7) + 8 * (mi & 1), acol = 4 * (mi >> 1);
+        const int j = warp * 8 + gq;
+        const float* kb = Kt + (j >> 5) * (C * 32);
 #pragma unroll
-      for (int nt = 0; nt < NTS; ++nt) {
-        const int c = warp * (8 * NTS) + nt * 8 + 2 * tq;
-        acc[nt][0] = gam * s.S[gq * SS + c];
-        acc[nt][1] = gam * s.S[gq * SS + c + 1];
-        acc[nt][2] = gam * s.S[(gq + 8) * SS + c];
-        acc[nt][3] = gam * s.S[(gq + 8) * SS + c + 1];
-        acc2[nt][0] = acc2[nt][1] = acc2[nt][2] = acc2[nt][3] = 0.f;
-      }
-      const float* Kt = s.K[st];
-      const int mi = lane >> 3;
-      const int arow = (lane & 7) + 8 * (mi & 1), acol = 4 * (mi >> 1);
-#pragma unroll 2
-      for (int k = 0; k < C; k += 16) {
+        for (int k = 0; k < C; k += 16) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int kk = k + half * 8;
-          uint32_t x0, x1, x2, x3;
-          ldsm4(&s.UsT[arow * SUT + kk + acol], x0, x1, x2, x3);
-#pragma unroll
-          for (int nt = 0; nt < NTS; ++nt) {
-            const int j = warp * (8 * NTS) + nt * 8 + gq;
-            const float* kb = Kt + (j >> 5) * (C * 32);
-            mma_tf32(half ? acc2[nt] : acc[nt], x0, x1, x2, x3, raw(kb[swz32(kk + tq, j & 31)]),
+          for (int half = 0; half < 2; ++half) {
+            const int kk = k + half * 8;
+            uint32_t x0, x1, x2, x3;
+            ldsm4(&s.UsT[arow * SUT + kk + acol], x0, x1, x2, x3);
+            mma_tf32(half ? acc2 : acc, x0, x1, x2, x3, raw(kb[swz32(kk + tq, j & 31)]),
                      raw(kb[swz32(kk + tq + 4, j & 31)]));
           }
         }
       }
+      if (tid == 0) bulk_wait_read0();   // the chunk-start record has left Sr
       __syncthreads();   // every warp has read S, Sr and Us
-#pragma unroll
-      for (int nt = 0; nt < NTS; ++nt) {
-        const int c = warp * (8 * NTS) + nt * 8 + 2 * tq;
-        const float e0 = acc[nt][0] + acc2[nt][0], e1 = acc[nt][1] + acc2[nt][1];
-        const float e2 = acc[nt][2] + acc2[nt][2], e3 = acc[nt][3] + acc2[nt][3];
+      if (upd) {
+        const float e0 = acc[0] + acc2[0], e1 = acc[1] + acc2[1];
+        const float e2 = acc[2] + acc2[2], e3 = acc[3] + acc2[3];
         s.S[gq * SS + c] = e0;
         s.S[gq * SS + c + 1] = e1;
         s.S[(gq + 8) * SS + c] = e2;
@@ -594,9 +622,11 @@ __global__ void __launch_bounds__(256) chunk_state_kernel(const __grid_constant_
         *reinterpret_cast<float2*>(&sb[swz32(gq, c & 31)]) = make_float2(rnd(e0), rnd(e1));
         *reinterpret_cast<float2*>(&sb[swz32(gq + 8, c & 31)]) = make_float2(rnd(e2), rnd(e3));
       }
+      fence_async_smem();   // the next record reads Sr by bulk store
     }
     __syncthreads();
   }
+  if (tid == 0) bulk_wait_all0();   // this CTA's records have been written
   if (!ok) {
     // a tile never arrived: wait (bounded) for this CTA's copies in flight, then leave
     if (tid == 0)
@@ -783,16 +813,16 @@ static constexpr size_t state_smem() { return sizeof(gc::StateSmem<D, NS>) + 102
 
 template <int D>
 static cudaError_t launch_state(const CUtensorMap& mW, const CUtensorMap& mK, const CUtensorMap& mU,
-                                const float* g, const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks,
+                                const CUtensorMap& mS, const float* g, const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks,
                                 const CtxDesc* d_ctx, int layer_g, int H, float* Ubuf, float* Schunk,
                                 int max_chunks, int* d_err, cudaStream_t st) {
   if (n_seq <= 0) return cudaSuccess;
   const dim3 grid(n_seq, H, D / gc::BV);
   if (max_chunks <= 1) {
-    CK_RET(launch_pdl(gc::chunk_state_kernel<D, 1>, grid, dim3(256), state_smem<D, 1>(), st, mW, mK, mU, g, d_seq,
+    CK_RET(launch_pdl(gc::chunk_state_kernel<D, 1>, grid, dim3(512), state_smem<D, 1>(), st, mW, mK, mU, mS, g, d_seq,
                       d_chunks, d_ctx, layer_g, H, Ubuf, Schunk, d_err));
   } else {
-    CK_RET(launch_pdl(gc::chunk_state_kernel<D, 2>, grid, dim3(256), state_smem<D, 2>(), st, mW, mK, mU, g, d_seq,
+    CK_RET(launch_pdl(gc::chunk_state_kernel<D, 2>, grid, dim3(512), state_smem<D, 2>(), st, mW, mK, mU, mS, g, d_seq,
                       d_chunks, d_ctx, layer_g, H, Ubuf, Schunk, d_err));
   }
   return cudaGetLastError();
@@ -823,7 +853,7 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, flo
   CK_RET(launch_pdl(gc::chunk_prep_kernel<D>, dim3(n_chunks, H), dim3(256), sp, st, proj, ld, loga, d_chunks, H, D, eps,
                     Wbuf, Ubuf));
   // TMA views of the chunk tiles: W and Ut rows of head h ([R, H, D] fp32), K columns of proj
-  CUtensorMap mW, mK, mU;
+  CUtensorMap mW, mK, mU, mS;
   {
     const uint64_t dims3[3] = {(uint64_t)D, (uint64_t)H, (uint64_t)R};
     const uint64_t str3[2] = {(uint64_t)D * 4, (uint64_t)H * D * 4};
@@ -835,18 +865,23 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, flo
         !tensor_map(&mU, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, Ubuf, dims3, str3, boxU, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !tensor_map(&mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, proj, dims2, str2, boxK, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
+    const uint64_t dimsS[2] = {(uint64_t)D, (uint64_t)n_chunks * H * D};
+    const uint64_t strS[1] = {(uint64_t)D * 4};
+    const uint32_t boxS[2] = {32, (uint32_t)gc::BV};
+    if (!tensor_map(&mS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Schunk, dimsS, strS, boxS, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
   }
   // sequences [0, n_first) run before the rest (the rest continue from their states); a group
   // from fold_from on (single-chunk sequences that keep no state) needs no state pass at all:
   // chunk_out forms their U itself
   const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
   const int n1 = std::min(split, fold_from);
-  cudaError_t e = launch_state<D>(mW, mK, mU, loga, d_seq, n1, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
+  cudaError_t e = launch_state<D>(mW, mK, mU, mS, loga, d_seq, n1, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
                                   split < n_seq ? max_chunks_first : std::max(max_chunks_first, max_chunks_rest),
                                   d_err, st);
   if (e != cudaSuccess) return e;
   if (split < n_seq && fold_from > split) {
-    e = launch_state<D>(mW, mK, mU, loga, d_seq + split, n_seq - split, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
+    e = launch_state<D>(mW, mK, mU, mS, loga, d_seq + split, n_seq - split, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
                         max_chunks_rest, d_err, st);
     if (e != cudaSuccess) return e;
   }
