@@ -52,7 +52,8 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling during the timed region (clocks, throttle reasons)."""
+    """nvidia-smi sampling (every 50 ms) of clocks and throttle reasons; summary() keeps the samples
+    taken between mark_start() and mark_end() (the timed region)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -61,21 +62,31 @@ class ClockSampler:
         self.idx = gpu_index
         self.proc = None
         self.lines = []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.time() + 5.0      # sampling is running before the timed region starts
+            while not self.lines and time.time() < deadline and self.proc.poll() is None:
+                time.sleep(0.02)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *a):
         if self.proc:
@@ -88,7 +99,11 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.t0 is not None and self.t1 is not None:
+            inside = [x for x in lines if self.t0 <= x[0] <= self.t1 + 0.05]
+            lines = inside if inside else lines[-1:]
+        for _, ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -336,6 +351,8 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     nvtx = os.environ.get("S1_NVTX") == "1"     # lets ncu --nvtx-include "timed/" select the timed steps
     with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        clk.mark_start()
         if nvtx:
             torch.cuda.nvtx.range_push("timed")
         e0.record(stream)
@@ -345,6 +362,8 @@ def main():
         if nvtx:
             torch.cuda.nvtx.range_pop()
         barrier()
+        torch.cuda.synchronize()
+        clk.mark_end()
     ms_total = e0.elapsed_time(e1)
     launches = (model.counters()["launches"] - launches0) // max(1, args.steps)
     model.sync()
@@ -364,8 +383,12 @@ def main():
     achieved = g["flops"] / (g["ms"] / 1000.0) / 1e12 if g["ms"] > 0 else 0.0
     peak = peaks["bf16_tflops_sustained"]
     total_prof_ms = sum(v["ms"] for v in prof.values())
+    # DRAM bytes per GEMM launch from the committed per-shape ncu capture of the 4B step's five
+    # projection shapes (profiles/gemm_tc_4b_shapes.md), weighted by their launches per step
+    traffic = 62.0e6 if (cfg.name == "4b" and args.path == "fused") else None
     roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05, all projections)", "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": None,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": traffic,
+                "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                 "peak_source": f"{peaks['source']} bf16 sustained",
                 "share_of_step": g["ms"] / total_prof_ms if total_prof_ms else None,
                 "launches_per_step": g["count"] / max(1, args.steps),
