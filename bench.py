@@ -346,6 +346,32 @@ def main():
     model.sync()
     t_prefill, t_decide, t_fused = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]), ev[2].elapsed_time(ev[3])
 
+    # ---- decide phase alone (questions over the cached prefix): the weight-streaming regime ----
+    # every projection weight is read once per call while only the questions' rows are computed,
+    # so its roofline is HBM bandwidth over the model's weight bytes (bf16, LoRA merged)
+    weight_bytes = sum(a.size * 2 for layer in W.layers for a in layer if a is not None and a.ndim == 2)
+    dts = []
+    nvtx_dec = os.environ.get("S1_NVTX") == "1"   # lets ncu --nvtx-include "decide/" select these calls
+    for _ in range(5):
+        if nvtx_dec:
+            torch.cuda.nvtx.range_push("decide")
+        ev[1].record(stream)
+        model.decide_async(st, qarr, n_q, d_probs.data_ptr(), d_stats.data_ptr(), 0)
+        ev[2].record(stream)
+        if nvtx_dec:
+            torch.cuda.nvtx.range_pop()
+        model.sync()
+        dts.append(ev[1].elapsed_time(ev[2]))
+    t_dec = float(np.median(dts))
+    hbm_peak = load_peaks()["hbm_gbs"]
+    decide_rows = sum(len(q.suffix) for q in req.questions)
+    decide_roofline = {"bound": "hbm", "phase": f"s1_decide_async: {n_q} question(s), {decide_rows} rows over "
+                                                 f"the cached {P}-row prefix",
+                       "weight_bytes": int(weight_bytes), "ms": t_dec,
+                       "achieved": weight_bytes / (t_dec / 1000.0) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                       "frac": weight_bytes / (t_dec / 1000.0) / 1e9 / hbm_peak,
+                       "peak_source": load_peaks()["source"] + " HBM copy"}
+
     launches0 = model.counters()["launches"]
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -433,7 +459,8 @@ def main():
                        "one_step_ms": {"two_call_prefill": round(t_prefill, 4), "two_call_decide": round(t_decide, 4),
                                        "fused": round(t_fused, 4)},
                        "class_ms_per_step": phase_split},
-            "roofline": roofline, "clocks": clk.summary(), "gpu_launches": int(launches), "e2e": e2e}
+            "roofline": roofline, "decide_roofline": decide_roofline, "clocks": clk.summary(),
+            "gpu_launches": int(launches), "e2e": e2e}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = time_oracle(cfg, W, req, budget_s=float(os.environ.get("S1_CPU_BUDGET", "25")))
     if rank == 0:

@@ -98,6 +98,15 @@ int s1_profile_read(struct s1_model* m, double* ms, double* flops, double* bytes
 int s1_counters(struct s1_model* m, long long* launches, long long* h2d_bytes, long long* d2h_bytes);
 /* 0 = tensor-core GEMM (default), 1 = SIMT GEMM for every projection (debug only). */
 int s1_set_gemm_impl(struct s1_model* m, int impl);
+/* Layer trace (a debugging and verification aid, no counterpart in the pages): while set, every
+ * forward pass of the model copies its fp32 residual stream into d_trace, stream-ordered —
+ * plane 0 after the embedding rows, plane l + 1 after layer l — as [n_layers + 1][R][d_model]
+ * in the call's packed row order (prefill: the prefix rows; decide: the questions' suffix rows
+ * in question order; one sweep: every prefix, then every question's suffix). d_trace is a
+ * device buffer of capacity_floats floats owned by the caller, who keeps it alive while it is
+ * set; a call that needs more fails with S1_ERR_BUDGET before any launch. NULL clears it.
+ * Synchronises the model's stream. */
+int s1_set_layer_trace(struct s1_model* m, float* d_trace, long long capacity_floats);
 
 #ifdef __cplusplus
 }

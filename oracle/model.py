@@ -225,21 +225,28 @@ class Oracle:
         prefix (None = start from zero state). Returns the last layer's output
         [T, d] (before the final norm) and the per-layer continuation state.
         """
-        eps = self.s.rms_eps
         x = x.astype(self.dt, copy=True)
         out_caches = []
-        for l, full in enumerate(self.full):
-            c = caches[l] if caches is not None else None
-            xn = rmsnorm(x, self._w(l, 0), eps)
-            if full:
-                y, nc = self.attn_layer(l, xn, pos, c)
-            else:
-                y, nc = self.gdn_layer(l, xn, c)
-            h = x + y
-            hn = rmsnorm(h, self._w(l, 5 if full else 7), eps)
-            x = h + self.mlp(l, hn)
+        for l in range(len(self.full)):
+            x, nc = self.layer(l, x, pos, caches[l] if caches is not None else None)
             out_caches.append(nc)
         return x, out_caches
+
+    def layer(self, l, x, pos, cache: Optional[LayerCache] = None):
+        """One pre-norm block l on rows x [T, d] at positions pos (continuing `cache`, None =
+        from zero state): returns x' = h + MLP(RMSNorm(h)), h = x + Mixer(RMSNorm(x)), and the
+        layer's continuation state."""
+        eps = self.s.rms_eps
+        full = self.full[l]
+        x = x.astype(self.dt, copy=False)
+        xn = rmsnorm(x, self._w(l, 0), eps)
+        if full:
+            y, nc = self.attn_layer(l, xn, pos, cache)
+        else:
+            y, nc = self.gdn_layer(l, xn, cache)
+        h = x + y
+        hn = rmsnorm(h, self._w(l, 5 if full else 7), eps)
+        return h + self.mlp(l, hn), nc
 
     def readout(self, h_last, qtype, option_ids):
         """Decision readout from the last-layer hidden row h_last [d]."""

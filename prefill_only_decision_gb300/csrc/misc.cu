@@ -28,30 +28,36 @@ cudaError_t launch_embed(const bf16* E, const int* row_src, const bf16* embeds, 
 }
 
 // ---- RMSNorm: out = bf16(x / sqrt(mean(x^2) + eps) * w) --------------------------------
-// One warp per row, the row held in registers (one read of x), 8 rows per block.
+// One warp per row, the row held in registers (one read of x), 8 rows per block; the block
+// stages w in shared memory while its rows load, so no global round trip follows the reduction.
 template <int NV>   // float4 per lane: d = 128 * NV
 __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                            bf16* __restrict__ out, int R, int d, float eps) {
   allow_dependents();
+  __shared__ float4 ws[32 * NV];
+  const float4* wr = reinterpret_cast<const float4*>(w);
+  for (int i = threadIdx.x; i < 32 * NV; i += 256) ws[i] = wr[i];   // w does not depend on earlier kernels
   wait_prerequisites();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= R) return;
-  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)r * d);
   float4 v[NV];
   float ss = 0.f;
+  if (r < R) {
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)r * d);
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    v[i] = xr[lane + 32 * i];
-    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    for (int i = 0; i < NV; ++i) {
+      v[i] = xr[lane + 32 * i];
+      ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    }
   }
+  __syncthreads();   // ws complete (every thread reaches this, rows past R included)
+  if (r >= R) return;
   ss = warp_sum(ss);
   const float inv = 1.0f / sqrtf(ss / (float)d + eps);
-  const float4* wr = reinterpret_cast<const float4*>(w);
   uint2* o = reinterpret_cast<uint2*>(out + (size_t)r * d);
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
-    const float4 g = wr[lane + 32 * i];
+    const float4 g = ws[lane + 32 * i];
     __nv_bfloat162 a = __floats2bfloat162_rn(v[i].x * inv * g.x, v[i].y * inv * g.y);
     __nv_bfloat162 b = __floats2bfloat162_rn(v[i].z * inv * g.z, v[i].w * inv * g.w);
     uint2 u;

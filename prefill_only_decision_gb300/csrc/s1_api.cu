@@ -130,6 +130,8 @@ struct s1_model {
   size_t pinned_bytes = 0;
   cudaEvent_t meta_done = nullptr;
   int gemm_impl = 0;           // 0 = tensor cores (tcgen05), 1 = SIMT reference
+  float* trace = nullptr;      // layer trace: residual stream after the embedding and each layer
+  long long trace_floats = 0;
   bool force_simt = false;     // S1_GEMM=simt in the environment (debugging)
   // profiling
   bool prof = false;
@@ -399,11 +401,17 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
   const int d = s.d_model, F = s.ffn;
   Scratch& sc = m->sc;
   cudaStream_t st = m->stream;
+  const size_t plane = (size_t)R * d;
+  if (m->trace && (long long)((s.n_layers + 1) * plane) > m->trace_floats)
+    return fail(S1_ERR_BUDGET, "layer trace holds %lld floats, this call needs %zu", m->trace_floats,
+                (size_t)(s.n_layers + 1) * plane);
   {
     ProfScope ps(m, S1_PROF_OTHER, 0, (double)R * d * 6);
     CK(launch_embed(m->embed, mt.d_row_src, d_embeds, sc.x, R, d, st));
     m->launches += 1;
   }
+  if (m->trace) CK(cudaMemcpyAsync(m->trace, sc.x, plane * 4, cudaMemcpyDeviceToDevice, st));
+  int li = 0;
   for (const Layer& L : m->layers) {
     {
       ProfScope ps(m, S1_PROF_NORM, 0, (double)R * d * 6);
@@ -468,6 +476,8 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
     if (rc) return rc;
     rc = gemm(m, sc.h, L.w_down, R, d, F, EPI_RESADD, sc.x, d);
     if (rc) return rc;
+    ++li;
+    if (m->trace) CK(cudaMemcpyAsync(m->trace + (size_t)li * plane, sc.x, plane * 4, cudaMemcpyDeviceToDevice, st));
   }
   const int nq = (int)mt.q_row.size();
   if (nq > 0) {
@@ -1336,6 +1346,15 @@ int s1_counters(s1_model* m, long long* launches, long long* h2d_bytes, long lon
   if (launches) *launches = m->launches;
   if (h2d_bytes) *h2d_bytes = m->h2d_bytes;
   if (d2h_bytes) *d2h_bytes = m->d2h_bytes;
+  return S1_OK;
+}
+
+int s1_set_layer_trace(s1_model* m, float* d_trace, long long capacity_floats) {
+  if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  if (d_trace && capacity_floats <= 0) return fail(S1_ERR_INVALID_ARG, "layer trace needs a positive capacity");
+  CK(cudaStreamSynchronize(m->stream));
+  m->trace = d_trace;
+  m->trace_floats = d_trace ? capacity_floats : 0;
   return S1_OK;
 }
 

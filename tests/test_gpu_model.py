@@ -40,21 +40,28 @@ def tiny(B, tiny_weights):
     m.close()
 
 
-def compare(gpu, ref, qs, tag="", check_hidden=True, p_tol=P_TOL):
-    """Assert the tolerance contract for one list of results; returns the worst errors."""
+def compare(gpu, ref, qs, tag="", check_hidden=True, p_tol=P_TOL, h_tol=H_TOL, policy=None):
+    """Assert the tolerance contract for one list of results; returns the worst errors.
+    `policy` (the bf16-policy oracle's results, when `ref` is the fp32 reference): the bounds on p
+    and E grow by the two oracles' own distance on each question, since the GPU is held to the
+    contract against the policy oracle and |gpu - ref| <= |gpu - policy| + |policy - ref|."""
     worst = dict(p=0.0, e=0.0, h=0.0)
     for j, (g, r, q) in enumerate(zip(gpu, ref, qs)):
         p_err = float(np.abs(g["probs"] - r["probs"]).max())
         e_err = abs(g["expected_score"] - r["expected_score"])
-        assert p_err <= p_tol, (tag, j, p_err)
-        assert e_err <= E_TOL, (tag, j, e_err)
+        p_lim, e_lim = p_tol, E_TOL
+        if policy is not None:
+            p_lim += float(np.abs(policy[j]["probs"] - r["probs"]).max())
+            e_lim += abs(policy[j]["expected_score"] - r["expected_score"])
+        assert p_err <= p_lim, (tag, j, p_err, p_lim)
+        assert e_err <= e_lim, (tag, j, e_err, e_lim)
         srt = np.sort(r["probs"])[::-1]
         if len(srt) == 1 or srt[0] - srt[1] > MARGIN:
             assert g["argmax"] == r["argmax"], (tag, j, g["probs"], r["probs"])
         if g.get("hidden") is not None:
             h_err = float(np.linalg.norm(g["hidden"] - r["hidden"]) / np.linalg.norm(r["hidden"]))
             if check_hidden:
-                assert h_err <= H_TOL, (tag, j, h_err)
+                assert h_err <= h_tol, (tag, j, h_err)
             worst["h"] = max(worst["h"], h_err)
         assert abs(float(np.sum(g["probs"])) - 1) < 1e-5
         assert 0 <= g["expected_score"] <= len(q.option_ids) - 1 + 1e-6
@@ -65,6 +72,53 @@ def compare(gpu, ref, qs, tag="", check_hidden=True, p_tol=P_TOL):
         worst["e"] = max(worst["e"], e_err)
     print(f"[parity {tag}] max |dp| {worst['p']:.2e}  max |dE| {worst['e']:.2e}  max hidden rel L2 {worst['h']:.2e}")
     return worst
+
+
+LAYER_TOL = 1e-2
+
+
+def layerwise(B, W, req, tag, tol=LAYER_TOL):
+    """Teacher-forced per-layer parity on one fused sweep: the GPU's residual stream entering
+    each layer goes through the bf16-policy oracle's layer (the prefix rows, then each
+    question's rows continuing from the prefix's layer state), and the result is held against
+    the GPU's stream after that layer (rel L2 per row block). Independent of depth: an error in
+    any layer's kernels shows up in that layer, not amplified by the layers after it."""
+    s = W.shape
+    P = req.prefix_rows
+    n_rows = P + sum(len(q.suffix) for q in req.questions)
+    L, d = s.n_layers, s.d_model
+    buf = torch.zeros(((L + 1) * n_rows * d,), dtype=torch.float32, device="cuda")
+    m = B.Model(W)
+    try:
+        m.set_layer_trace(buf.data_ptr(), buf.numel())
+        m.prefill_decide(req)
+        m.set_layer_trace(0, 0)
+    finally:
+        m.close()
+    X = buf.view(L + 1, n_rows, d).cpu().numpy()
+    o = om.Oracle(W, np.float32, precision="bf16")
+    rel = lambda a, b: float(np.linalg.norm(a - b) / np.linalg.norm(b))
+    worst = 0.0
+    for l in range(L):
+        xp, cache = o.layer(l, X[l, :P], np.arange(P), None)
+        errs = [rel(xp, X[l + 1, :P])]
+        r = P
+        for q in req.questions:
+            n = len(q.suffix)
+            xq, _ = o.layer(l, X[l, r:r + n], P + np.arange(n), cache)
+            errs.append(rel(xq, X[l + 1, r:r + n]))
+            r += n
+        worst = max(worst, max(errs))
+        assert max(errs) <= tol, (tag, l, errs)
+    print(f"[layerwise {tag}] {L} layers, worst per-layer rel L2 {worst:.2e}")
+    return worst
+
+
+def test_small_layerwise(B):
+    """Per-layer parity of the small model (8 layers, LoRA, bf16) on one request's fused sweep."""
+    cfg = configs.SMALL
+    W = synth.make_weights(cfg)
+    layerwise(B, W, synth.make_requests(cfg, n_requests=1)[0], "small")
 
 
 def test_tiny_vs_oracle_unbranched(tiny, tiny_weights, tiny_requests):
@@ -230,8 +284,11 @@ def test_4b_vs_oracle(B):
         gpu = m.decide(st, req.questions)
     finally:
         m.close()
-    compare(gpu, om.Oracle(W, np.float32, precision="bf16").decide(req, branched=True), req.questions, "4b bf16")
-    compare(gpu, om.Oracle(W, np.float32).decide(req, branched=True), req.questions, "4b fp32", check_hidden=False)
+    pol = om.Oracle(W, np.float32, precision="bf16").decide(req, branched=True)
+    compare(gpu, pol, req.questions, "4b bf16")
+    compare(gpu, om.Oracle(W, np.float32).decide(req, branched=True), req.questions, "4b fp32", check_hidden=False,
+            policy=pol)
+    layerwise(B, W, req, "4b")
 
 
 @pytest.mark.slow
@@ -249,10 +306,13 @@ def test_4b_multimodal_batch_sampled(B):
     finally:
         m.close()
     qs = reqs[0].questions[:6]
+    refs = {}
     for prec in ("bf16", "fp32"):
         o = om.Oracle(W, np.float32, precision=prec)
         _, caches, P = o.prefill(reqs[0].tokens, reqs[0].embeds)
-        compare(gpu[0][:6], o.decide_branched(caches, P, qs), qs, f"4b-mm {prec}", check_hidden=prec == "bf16")
+        refs[prec] = o.decide_branched(caches, P, qs)
+        compare(gpu[0][:6], refs[prec], qs, f"4b-mm {prec}", check_hidden=prec == "bf16",
+                policy=refs["bf16"] if prec == "fp32" else None)
 
 
 @pytest.mark.slow
@@ -276,11 +336,17 @@ def test_27b_sampled_requests(B):
         assert abs(float(g[0]["probs"].sum()) - 1) < 1e-5
         assert 0 <= g[0]["expected_score"] <= 3
     i = int(np.argmin([len(r.tokens) for r in reqs]))
+    refs = {}
     for prec in ("bf16", "fp32"):
-        ref = om.Oracle(W, np.float32, precision=prec).decide(reqs[i], branched=True)
-        # against the fp32 reference at 64 layers the bf16 drift itself reaches ~2e-2: bounded at 5e-2
+        ref = refs[prec] = om.Oracle(W, np.float32, precision=prec).decide(reqs[i], branched=True)
+        # against the fp32 reference the bounds widen by the policy's own drift (compare's
+        # `policy`). The last hidden state of two correct bf16-policy implementations differs by
+        # rounding flips that grow with depth (1.6 % at 32 layers between the oracle in fp32 and
+        # in fp64): at 64 layers it is bounded at 5e-2, and every layer is held to LAYER_TOL by
+        # the teacher-forced check below.
         compare(res[i], ref, reqs[i].questions, f"27b req {i} P={len(reqs[i].tokens)} {prec}",
-                check_hidden=prec == "bf16", p_tol=P_TOL if prec == "bf16" else 5e-2)
+                check_hidden=prec == "bf16", h_tol=5e-2, policy=refs["bf16"] if prec == "fp32" else None)
+    layerwise(B, W, reqs[i], f"27b req {i}")
 
 
 # -- one sweep over prefix + questions ---------------------------------------------------------
