@@ -666,8 +666,12 @@ template <int D>
 __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict__ proj, int ld,
                                                         const float* __restrict__ gbuf,
                                                         const ChunkDesc* __restrict__ chunks, int H, float eps,
+                                                        const float* __restrict__ Wbuf,
                                                         const float* __restrict__ Ubuf,
-                                                        const float* __restrict__ Schunk, bf16* __restrict__ out) {
+                                                        const float* __restrict__ Schunk,
+                                                        const SeqDesc* __restrict__ seqs,
+                                                        const CtxDesc* __restrict__ ctxs, int layer_g, int out_fold,
+                                                        bf16* __restrict__ out) {
   allow_dependents();
   wait_prerequisites();
   extern __shared__ __align__(16) uint8_t smraw[];
@@ -688,10 +692,23 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
     cp16(&s.Q[r * SQ + c4], proj + (size_t)row * ld + h * D + c4, ok);
     cp16(&s.KU[r * SQ + c4], proj + (size_t)row * ld + HDk + h * D + c4, ok);   // K with the Q stride
   }
-  const float* Sc = Schunk + ((size_t)ci * H + h) * D * D;
-  for (int i = tid; i < D * (D / 4); i += 256) {
-    const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-    cp16(&s.S[r * SSC + c4], Sc + (size_t)r * D + c4, true);
+  // folded chunk (a single-chunk sequence without a state pass): its start state is the
+  // snapshot's (or zero), TF32-rounded as the state pass records it
+  const bool fold = cd.seq >= out_fold;
+  if (!fold) {
+    const float* Sc = Schunk + ((size_t)ci * H + h) * D * D;
+    for (int i = tid; i < D * (D / 4); i += 256) {
+      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+      cp16(&s.S[r * SSC + c4], Sc + (size_t)r * D + c4, true);
+    }
+  } else {
+    const int cin = seqs[cd.seq].ctx_in;
+    const float* S0 = cin >= 0 ? ctxs[cin].S + (size_t)(layer_g * H + h) * D * D : nullptr;
+    for (int i = tid; i < D * (D / 4); i += 256) {
+      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+      const float4 v = S0 ? *reinterpret_cast<const float4*>(S0 + (size_t)r * D + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(&s.S[r * SSC + c4]) = make_float4(rnd(v.x), rnd(v.y), rnd(v.z), rnd(v.w));
+    }
   }
   if (tid < C) s.g[tid] = tid < n ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
   cp_commit();
@@ -747,12 +764,65 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
     }
   }
   __syncthreads();
-  // U tile over K (k-major stride)
-  for (int i = tid; i < C * (D / 4); i += 256) {
-    const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-    const bool ok = r < n;
-    const int row = cd.row0 + (ok ? r : 0);
-    cp16(&s.KU[r * SUo + c4], Ubuf + ((size_t)row * H + h) * D + c4, ok);
+  if (fold) {
+    // U = Ut - W S^T here, with the state pass's TF32 operands (two accumulation chains per
+    // output), then rounded to TF32. W -> KU (A-operand stride); warp -> rows r0.., value
+    // columns (D/2)*(warp>>2) ..; Ut straight into registers.
+    for (int i = tid; i < C * (D / 4); i += 256) {
+      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+      const bool ok = r < n;
+      const int row = cd.row0 + (ok ? r : 0);
+      cp16(&s.KU[r * SUo + c4], Wbuf + ((size_t)row * H + h) * D + c4, ok);
+    }
+    cp_commit();
+    const int cb = (warp >> 2) * (D / 2);
+    float ut[NTO][4];
+#pragma unroll
+    for (int nt = 0; nt < NTO; ++nt) {
+      const int c = cb + nt * 8 + 2 * tq;
+      const int ra = r0 + gq, rb = r0 + gq + 8;
+      const float2 x = ra < n ? *reinterpret_cast<const float2*>(Ubuf + ((size_t)(cd.row0 + ra) * H + h) * D + c)
+                              : make_float2(0.f, 0.f);
+      const float2 y = rb < n ? *reinterpret_cast<const float2*>(Ubuf + ((size_t)(cd.row0 + rb) * H + h) * D + c)
+                              : make_float2(0.f, 0.f);
+      ut[nt][0] = x.x; ut[nt][1] = x.y; ut[nt][2] = y.x; ut[nt][3] = y.y;
+    }
+    cp_wait<0>();
+    __syncthreads();
+    float u0[NTO][4] = {}, u1[NTO][4] = {};
+#pragma unroll 2
+    for (int k = 0; k < D; k += 16) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int kk = k + 8 * half;
+        const uint32_t a0 = raw(s.KU[(r0 + gq) * SUo + kk + tq]), a1 = raw(s.KU[(r0 + gq + 8) * SUo + kk + tq]);
+        const uint32_t a2 = raw(s.KU[(r0 + gq) * SUo + kk + tq + 4]), a3 = raw(s.KU[(r0 + gq + 8) * SUo + kk + tq + 4]);
+#pragma unroll
+        for (int nt = 0; nt < NTO; ++nt) {
+          const int i = cb + nt * 8 + gq;
+          const uint32_t b0 = raw(s.S[i * SSC + kk + tq]), b1 = raw(s.S[i * SSC + kk + tq + 4]);
+          mma_tf32(half ? u1[nt] : u0[nt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+    }
+    __syncthreads();   // every warp has read W
+#pragma unroll
+    for (int nt = 0; nt < NTO; ++nt) {
+      const int c = cb + nt * 8 + 2 * tq;
+      const int ra = r0 + gq, rb = r0 + gq + 8;
+      s.KU[ra * SUo + c] = ra < n ? rnd(ut[nt][0] - (u0[nt][0] + u1[nt][0])) : 0.f;
+      s.KU[ra * SUo + c + 1] = ra < n ? rnd(ut[nt][1] - (u0[nt][1] + u1[nt][1])) : 0.f;
+      s.KU[rb * SUo + c] = rb < n ? rnd(ut[nt][2] - (u0[nt][2] + u1[nt][2])) : 0.f;
+      s.KU[rb * SUo + c + 1] = rb < n ? rnd(ut[nt][3] - (u0[nt][3] + u1[nt][3])) : 0.f;
+    }
+  } else {
+    // U tile over K (k-major stride)
+    for (int i = tid; i < C * (D / 4); i += 256) {
+      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+      const bool ok = r < n;
+      const int row = cd.row0 + (ok ? r : 0);
+      cp16(&s.KU[r * SUo + c4], Ubuf + ((size_t)row * H + h) * D + c4, ok);
+    }
   }
   cp_commit();
   // O1 = Q S_c^T  (warp -> rows r0.., value columns (D/2)*(warp>>2) .. : NTO n-tiles)
@@ -833,7 +903,7 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, flo
                                     const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                     const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
                                     float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                                    int fold_from, int* d_err, cudaStream_t st) {
+                                    int fold_from, int out_fold, int* d_err, cudaStream_t st) {
   static bool attr = false;
   const size_t sp = sizeof(gc::PrepSmem<D>);
   const size_t so = sizeof(gc::OutSmem<D>);
@@ -871,22 +941,23 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, flo
     if (!tensor_map(&mS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, Schunk, dimsS, strS, boxS, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  // sequences [0, n_first) run before the rest (the rest continue from their states); a group
-  // from fold_from on (single-chunk sequences that keep no state) needs no state pass at all:
-  // chunk_out forms their U itself
+  // sequences [0, n_first) run before the rest (the rest continue from their states). Sequences
+  // from fold_from on are followers handled by their prefixes' state pass; sequences from
+  // out_fold on are single chunks whose U chunk_out forms itself: neither gets a state pass.
   const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
-  const int n1 = std::min(split, fold_from);
+  const int n1 = std::min(split, std::min(fold_from, out_fold));
   cudaError_t e = launch_state<D>(mW, mK, mU, mS, loga, d_seq, n1, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
                                   split < n_seq ? max_chunks_first : std::max(max_chunks_first, max_chunks_rest),
                                   d_err, st);
   if (e != cudaSuccess) return e;
-  if (split < n_seq && fold_from > split) {
-    e = launch_state<D>(mW, mK, mU, mS, loga, d_seq + split, n_seq - split, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
+  const int n2 = std::min(n_seq, out_fold) - split;
+  if (split < n_seq && fold_from > split && n2 > 0) {
+    e = launch_state<D>(mW, mK, mU, mS, loga, d_seq + split, n2, d_chunks, d_ctx, layer_g, H, Ubuf, Schunk,
                         max_chunks_rest, d_err, st);
     if (e != cudaSuccess) return e;
   }
   CK_RET(launch_pdl(gc::chunk_out_kernel<D>, dim3(n_chunks, H), dim3(256), so, st, proj, ld, loga, d_chunks, H, eps,
-                    Ubuf, Schunk, out));
+                    Wbuf, Ubuf, Schunk, d_seq, d_ctx, layer_g, out_fold, out));
   return cudaGetLastError();
 }
 
@@ -894,20 +965,21 @@ cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float ep
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                               int fold_from, int* d_err, cudaStream_t st, long* launches) {
+                               int fold_from, int out_fold, int* d_err, cudaStream_t st, long* launches) {
   if (n_seq <= 0 || n_chunks <= 0) return cudaSuccess;
   if (!gdn_chunked_supported(H, Dk, Dv, ld)) return cudaErrorNotSupported;
   if (n_seq > 65535 || n_chunks > 2147483647 / 2) return cudaErrorInvalidValue;
   cudaError_t e = (Dk == 128)
                       ? launch_chunked_d<128>(proj, ld, R, loga, eps, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                               layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
-                                              max_chunks_rest, fold_from, d_err, st)
+                                              max_chunks_rest, fold_from, out_fold, d_err, st)
                       : launch_chunked_d<64>(proj, ld, R, loga, eps, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                              layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
-                                             max_chunks_rest, fold_from, d_err, st);
+                                             max_chunks_rest, fold_from, out_fold, d_err, st);
   if (launches) {
     const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
-    *launches += 2 + (std::min(split, fold_from) > 0 ? 1 : 0) + (split < n_seq && fold_from > split ? 1 : 0);
+    *launches += 2 + (std::min(split, std::min(fold_from, out_fold)) > 0 ? 1 : 0) +
+                 (split < n_seq && fold_from > split && std::min(n_seq, out_fold) > split ? 1 : 0);
   }
   return e;
 }

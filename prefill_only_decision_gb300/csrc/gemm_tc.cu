@@ -313,7 +313,7 @@ struct Params {
   int m_tiles, n_tiles, splits, kb_per_split, kb_total;
   int m_groups;     // groups of CM consecutive m tiles (one group per cluster unit)
   int units;        // cluster units: m_groups x splits x n_tiles
-  int epi;          // epilogue; EPI_SPLITK_PARTIAL = write fp32 partials to ws
+  int epi;          // epilogue; EPI_PARTIAL = write fp32 partials to ws
   void* out;
   int ldo;
   float* ws;        // split-K partials [splits, m_tiles*BM, N]
@@ -394,6 +394,17 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
         uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
         o[0] = reinterpret_cast<uint4*>(r)[0];
         o[1] = reinterpret_cast<uint4*>(r)[1];
+      }
+    } else if (p.epi == EPI_PARTIAL) {
+      // split-K partials: plain stores, summed by splitk_reduce_kernel
+      const size_t yr = (size_t)(y0 + lane);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int n = n0 + c0 + 16 * j;
+        if (j >= nc || n >= p.N) continue;
+        float4* o = reinterpret_cast<float4*>(p.ws + yr * p.N + n);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = make_float4(v[j][4 * i], v[j][4 * i + 1], v[j][4 * i + 2], v[j][4 * i + 3]);
       }
     } else {   // fp32 outputs: staged boxes, TMA store or add-reduction
 #pragma unroll
@@ -1117,7 +1128,7 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
     if (part || epi == EPI_F32 || epi == EPI_RESADD) {
       const uint64_t rows = part ? (uint64_t)pl.splits * pl.m_tiles * tc::BM : (uint64_t)M;
       const uint64_t pitch = part ? (uint64_t)N * 4 : (uint64_t)ldo * 4;
-      const void* base = part ? (const void*)splitk_ws : out;
+      const void* base = part ? (const void*)p.ws : out;
       if ((pitch % 16) != 0 || ((uintptr_t)base % 16) != 0) return cudaErrorInvalidValue;
       const uint64_t dims[2] = {(uint64_t)N, rows};
       const uint64_t strides[1] = {pitch};
@@ -1147,7 +1158,7 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
   const size_t work = (size_t)M * cols / 4;
   int blocks = (int)((work + 255) / 256);
   if (blocks > 4 * lc.num_sms) blocks = 4 * lc.num_sms;
-  CK_RET(launch_pdl(tc::splitk_reduce_kernel, dim3(blocks), dim3(256), 0, lc.stream, splitk_ws, pl.splits,
+  CK_RET(launch_pdl(tc::splitk_reduce_kernel, dim3(blocks), dim3(256), 0, lc.stream, p.ws, pl.splits,
                     pl.m_tiles * tc::BM, M, N, epi, out, ldo));
   if (lc.launches) *lc.launches += 1;
   return cudaGetLastError();

@@ -95,6 +95,11 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int
                            cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
   const int blocks = (R + 7) / 8;
+  // few rows (questions over a snapshot): a block per row spreads them over more SMs
+  if (R <= 512 && d % 4 == 0) {
+    CK_RET(launch_pdl(rmsnorm_kernel, dim3(R), dim3(256), 0, st, x, w, out, d, eps));
+    return cudaGetLastError();
+  }
   switch (d) {
     case 256: CK_RET(launch_pdl(rmsnorm_warp_kernel<2>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;
     case 1024: CK_RET(launch_pdl(rmsnorm_warp_kernel<8>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;

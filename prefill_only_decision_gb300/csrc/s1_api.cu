@@ -273,8 +273,10 @@ struct Meta {
   int max_len = 0, max_opts = 0;
   int n_first = 0;   // fused sweep: the first n_first sequences (prefixes) scan before the rest
   int max_chunks_first = 0, max_chunks_rest = 0;   // longest sequence (in chunks) of each group
-  // sequences from fold_from on are handled by their prefixes' state pass (see build_chunks)
+  // sequences from fold_from on are handled by their prefixes' state pass, sequences from
+  // out_fold on by the output kernel alone (see build_chunks)
   int fold_from = 0;
+  int out_fold = 0;
   // device views
   int* d_row_src = nullptr;
   int* d_row_seq = nullptr;
@@ -301,6 +303,15 @@ void build_chunks(Meta& mt) {
   // later sequences' U and chunk-start states, and they get no state pass of their own.
   const int n = (int)mt.seqs.size();
   mt.fold_from = n;
+  mt.out_fold = n;
+  if (mt.n_first <= 0 || mt.n_first >= n) {
+    // one group (e.g. questions over snapshots): if every sequence is a single chunk that keeps
+    // no state, the output kernel forms each chunk's U from its start state and no state pass runs
+    bool all = true;
+    for (int s = 0; s < n && all; ++s)
+      if (mt.seqs[s].len > GDN_CHUNK || mt.seqs[s].ctx_out >= 0) all = false;
+    if (all) mt.out_fold = 0;
+  }
   if (mt.n_first > 0 && mt.n_first < n) {
     std::vector<int> owner(mt.ctxs.size(), -1);
     for (int p = 0; p < mt.n_first; ++p)
@@ -437,7 +448,7 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
           }
           CK(launch_gdn_chunked(sc.proj, L.n_in, R, sc.loga, s.l2_eps, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
                                 mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first,
-                                mt.max_chunks_first, mt.max_chunks_rest, mt.fold_from, m->d_err, st,
+                                mt.max_chunks_first, mt.max_chunks_rest, mt.fold_from, mt.out_fold, m->d_err, st,
                                 &m->launches));
         } else {
           CK(launch_gdn_prep(sc.proj, L.n_in, sc.loga, sc.beta, R, H, s.la_dk, s.la_dv, s.l2_eps, st));
