@@ -267,6 +267,7 @@ def main():
                     help="fused: s1_prefill_decide (one sweep); two-call: s1_prefill_state + s1_decide")
     ap.add_argument("--shape", default="1024,18432,2560,3")
     ap.add_argument("--cm-sweep", action="store_true", help="gemm kernel mode: repeat with cluster sizes 1, 2, 4")
+    ap.add_argument("--no-graphs", action="store_true", help="no CUDA graphs for the stream-ordered one-sweep call")
     args = ap.parse_args()
     if args.kernel:
         return run_kernel(args)
@@ -288,9 +289,12 @@ def main():
     W = synth.make_weights(cfg)
     reqs = synth.make_requests(cfg)
     req = reqs[0]
-    stream = torch.cuda.current_stream()
+    # a stream of its own (CUDA graphs cannot capture the legacy default stream)
+    stream = torch.cuda.Stream()
     binding.use_torch_allocator()
     model = binding.Model(W, stream=stream.cuda_stream)
+    if not args.no_graphs:
+        model.set_graphs(True)   # repeated stream-ordered one-sweep calls replay a captured graph
     n_q = len(req.questions)
     P = req.prefix_rows
 
@@ -308,6 +312,7 @@ def main():
     n_opt = sum(len(q.option_ids) for q in req.questions)
     d_probs = torch.zeros(n_opt, dtype=torch.float32, device="cuda")
     d_stats = torch.zeros((n_q, 8), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()   # inputs made on the default stream are ready for the model's stream
 
     def step_two_call():
         model.prefill_async(st, d_tok.data_ptr(), len(req.tokens), d_emb.data_ptr() if d_emb is not None else 0,
@@ -453,6 +458,7 @@ def main():
                        "model": "4B-class hybrid decoder (24 gated delta-rule + 8 GQA layers, d 2560, "
                                 "FFN 9216, LoRA r32 merged)" if cfg.name.startswith("4b") else cfg.name,
                        "decisions_per_step": n_q, "parallelism": f"replicas x{ws}",
+                       "cuda_graphs": (not args.no_graphs) and args.path == "fused",
                        "l2": "inputs larger than L2 (weights read every step)",
                        "path": args.path + (" (s1_prefill_decide_async)" if args.path == "fused"
                                             else " (s1_prefill_async + s1_decide_async)"),

@@ -208,6 +208,17 @@ int s1_decide_async(s1_model* m, const s1_state* st, const s1_question* qs_dev, 
 int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, int32_t n_tokens,
                             const void* d_embeds, int32_t n_embeds, const s1_question* qs_dev,
                             int32_t n_q, float* d_probs, float* d_stats, float* d_last_hidden);
+
+/* CUDA graphs for s1_prefill_decide_async (off by default). While enabled, a call whose
+ * signature — state handle and capacity, every device pointer, size and question type it
+ * passes — repeats an earlier call's is captured once into a CUDA graph (its second occurrence)
+ * and later occurrences replay that graph with one launch: the ids, embeddings and outputs are
+ * read and written through the same device buffers at replay time, so their contents may change
+ * between calls while their addresses and sizes may not. Graphs are not used on the legacy
+ * default stream, while profiling or a layer trace is on. A graph is dropped when the model's
+ * scratch buffers grow, and all are dropped by s1_set_graphs(m, 0) and s1_model_destroy.
+ * Synchronises the model's stream. Errors: INVALID_HANDLE. */
+int s1_set_graphs(struct s1_model* m, int enable);
 int s1_sync(s1_model* m);   /* waits for the stream; reports device-side timeouts */
 
 /* ---- prefix split (host only) ------------------------------------------------------------

@@ -96,6 +96,7 @@ def lib():
         "s1_profile_read": (C.c_int, [vp, P(C.c_double), P(C.c_double), P(C.c_double), P(C.c_long)]),
         "s1_set_gemm_impl": (C.c_int, [vp, C.c_int]),
         "s1_set_layer_trace": (C.c_int, [vp, vp, C.c_longlong]),
+        "s1_set_graphs": (C.c_int, [vp, C.c_int]),
         "s1_counters": (C.c_int, [vp, P(C.c_longlong), P(C.c_longlong), P(C.c_longlong)]),
         "s1_split_prefix": (C.c_int, [P(P(i32)), P(i32), i32, i32, i32, P(i32)]),
     }
@@ -330,6 +331,10 @@ class Model:
 
     def set_gemm_impl(self, impl: int):
         check(lib().s1_set_gemm_impl(self.h, impl))
+
+    def set_graphs(self, enable: bool):
+        """CUDA graphs for prefill_decide_async calls whose signature repeats (s1_set_graphs)."""
+        check(lib().s1_set_graphs(self.h, 1 if enable else 0))
 
     def set_layer_trace(self, ptr: int, capacity_floats: int):
         """Record the fp32 residual stream after the embedding and after every layer of each

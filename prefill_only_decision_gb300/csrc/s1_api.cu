@@ -11,6 +11,9 @@
 #include <cstdlib>
 #include <cstring>
 #include <string>
+#include <map>
+#include <set>
+#include <string>
 #include <vector>
 
 #include "common.cuh"
@@ -143,7 +146,28 @@ struct s1_model {
   long prof_count[S1_PROF_NCLASS] = {0};
   long launches = 0;           // kernels launched by forward passes
   long long h2d_bytes = 0, d2h_bytes = 0;
+  // CUDA graphs of the stream-ordered one-sweep call (s1_set_graphs): keyed by the call's
+  // argument signature; a graph owns its metadata buffer and bakes in the scratch addresses
+  struct Graph {
+    cudaGraphExec_t exec = nullptr;
+    void* meta = nullptr;
+    long launches = 0;
+  };
+  bool graphs = false;
+  std::map<std::string, Graph> graph_cache;
+  std::set<std::string> graph_seen;
 };
+
+// Every captured graph is dropped when a buffer it uses moves (scratch or chunk-state growth)
+// or when graphs are switched off.
+void drop_graphs(s1_model* m) {
+  for (auto& kv : m->graph_cache) {
+    if (kv.second.exec) cudaGraphExecDestroy(kv.second.exec);
+    dfree(kv.second.meta);
+  }
+  m->graph_cache.clear();
+  m->graph_seen.clear();
+}
 
 struct s1_state {
   uint32_t magic;
@@ -208,6 +232,7 @@ int ensure_scratch(s1_model* m, int rows, int n_opts = 0) {
   want = std::min(std::max(want, m->sc.rows * 2), m->sh.max_rows);
   want = std::max(want, rows);
   CK(cudaStreamSynchronize(m->stream));
+  drop_graphs(m);
   free_scratch(m->sc);
   Scratch sc;
   const s1_shape& s = m->sh;
@@ -339,16 +364,30 @@ void build_chunks(Meta& mt) {
   }
 }
 
-int upload_meta(s1_model* m, Meta& mt) {
+// Packs the call's metadata and uploads it: through the pinned staging buffer into the scratch
+// (stream-ordered), or, for a graph being captured, synchronously into the graph's own buffer
+// `dest` of `dest_bytes` (allocated here when NULL; returned through `dest`).
+int upload_meta(s1_model* m, Meta& mt, void** dest = nullptr) {
   build_chunks(mt);
   const int R = (int)mt.row_src.size();
   const size_t need = meta_bytes_for(R, (int)mt.seqs.size(), (int)mt.ctxs.size(), (int)mt.q_row.size(),
                                      (int)mt.opt_ids.size());
   if (need > m->sc.meta_bytes) return fail(S1_ERR_BUDGET, "request metadata exceeds the scratch budget");
-  // the previous upload from the pinned buffer must have finished before it is rewritten
-  CK(cudaEventSynchronize(m->meta_done));
-  char* h = m->pinned;
-  char* d = (char*)m->sc.meta;
+  std::vector<char> stage;
+  char* h;
+  char* d;
+  if (dest) {
+    *dest = dalloc(need);
+    if (!*dest) return fail(S1_ERR_OOM, "graph metadata allocation failed");
+    stage.resize(need);
+    h = stage.data();
+    d = (char*)*dest;
+  } else {
+    // the previous upload from the pinned buffer must have finished before it is rewritten
+    CK(cudaEventSynchronize(m->meta_done));
+    h = m->pinned;
+    d = (char*)m->sc.meta;
+  }
   size_t off = 0;
   auto put = [&](const void* src, size_t bytes) -> char* {
     if (bytes) memcpy(h + off, src, bytes);
@@ -372,8 +411,12 @@ int upload_meta(s1_model* m, Meta& mt) {
   mt.d_q_type = base + nq;
   mt.d_opt_off = base + 2 * nq;
   mt.d_opt_ids = base + 3 * nq + (nq ? 1 : 0);
-  CK(cudaMemcpyAsync(d, h, off, cudaMemcpyHostToDevice, m->stream));
-  CK(cudaEventRecord(m->meta_done, m->stream));
+  if (dest) {
+    CK(cudaMemcpy(d, h, off, cudaMemcpyHostToDevice));
+  } else {
+    CK(cudaMemcpyAsync(d, h, off, cudaMemcpyHostToDevice, m->stream));
+    CK(cudaEventRecord(m->meta_done, m->stream));
+  }
   m->h2d_bytes += (long long)off;
   return S1_OK;
 }
@@ -440,6 +483,7 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
           // (the chunked path normalises q, k and forms the gates inside its first kernel)
           if ((size_t)nch > m->schunk_chunks) {
             CK(cudaStreamSynchronize(st));
+            drop_graphs(m);
             dfree(m->schunk);
             const size_t cap = std::max<size_t>(nch, 2 * m->schunk_chunks);
             m->schunk = (float*)dalloc(cap * H * (size_t)s.la_dv * s.la_dk * 4);
@@ -892,6 +936,7 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
 void s1_model_destroy(s1_model* m) {
   if (!valid_model(m)) return;
   cudaStreamSynchronize(m->stream);
+  drop_graphs(m);
   free_scratch(m->sc);
   dfree(m->arena);
   dfree(m->rope_tab);
@@ -1151,7 +1196,8 @@ int s1_decide_async(s1_model* m, const s1_state* st, const s1_question* qs_dev, 
 static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, const int32_t* n_tokens,
                       const void* const* embeds, const int32_t* n_embeds, s1_state* const* states,
                       const s1_question* const* qs, const int32_t* n_q, bool device_ptrs, float* d_probs,
-                      float* d_stats, float* d_hidden, int* NQ_out, int* NO_out, bool want_lm = false) {
+                      float* d_stats, float* d_hidden, int* NQ_out, int* NO_out, bool want_lm = false,
+                      s1_model::Graph* cap = nullptr) {
   int Rp = 0, Rs = 0, NQ = 0, NO = 0, NE = 0;
   for (int r = 0; r < n_req; ++r) {
     const int P = n_tokens[r] + n_embeds[r];
@@ -1212,8 +1258,11 @@ static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, cons
       mt.max_opts = std::max(mt.max_opts, q.n_options);
       row += q.n_suffix;
     }
-  rc = upload_meta(m, mt);
+  rc = upload_meta(m, mt, cap ? &cap->meta : nullptr);
   if (rc) return rc;
+  // capture: everything from here on (id copies, the forward) becomes the graph
+  const long launches0 = m->launches;
+  if (cap) CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
   if (device_ptrs) {
     int rr = 0, opt = 0;
     for (int r = 0; r < n_req; ++r) {
@@ -1243,6 +1292,22 @@ static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, cons
     }
   }
   rc = run_forward(m, mt, m->sc.xn, d_probs, d_stats, d_hidden, want_lm);
+  if (cap) {
+    cudaGraph_t g = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(m->stream, &g);
+    if (rc == S1_OK && ec != cudaSuccess) rc = fail(S1_ERR_CUDA, "graph capture: %s", cudaGetErrorString(ec));
+    if (rc == S1_OK) {
+      const cudaError_t ei = cudaGraphInstantiate(&cap->exec, g, 0);
+      if (ei != cudaSuccess) rc = fail(S1_ERR_CUDA, "graph instantiation: %s", cudaGetErrorString(ei));
+    }
+    if (g) cudaGraphDestroy(g);
+    cap->launches = m->launches - launches0;
+    m->launches = launches0;
+    if (rc == S1_OK) {
+      CK(cudaGraphLaunch(cap->exec, m->stream));
+      m->launches += cap->launches;
+    }
+  }
   if (rc) return rc;
   for (int r = 0; r < n_req; ++r) states[r]->P = n_tokens[r] + n_embeds[r];
   *NQ_out = NQ;
@@ -1318,8 +1383,55 @@ int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, 
   if (!d_probs || !d_stats) return fail(S1_ERR_INVALID_ARG, "NULL output");
   const void* e[1] = {d_embeds};
   int NQ = 0, NO = 0;
+  if (m->graphs && !m->prof && !m->trace && m->stream != nullptr && n_q > 0 && qs_dev) {
+    // the call's signature: every pointer, size and type it passes, and the state's capacity
+    std::string key;
+    auto add = [&key](const void* p, size_t n) { key.append((const char*)p, n); };
+    add(&st, sizeof(st)); add(&st->cap, sizeof(int));
+    add(&d_tokens, sizeof(d_tokens)); add(&n_tokens, sizeof(n_tokens));
+    add(&d_embeds, sizeof(d_embeds)); add(&n_embeds, sizeof(n_embeds));
+    add(&d_probs, sizeof(d_probs)); add(&d_stats, sizeof(d_stats)); add(&d_last_hidden, sizeof(d_last_hidden));
+    for (int j = 0; j < n_q; ++j) add(&qs_dev[j], sizeof(s1_question));
+    auto it = m->graph_cache.find(key);
+    if (it != m->graph_cache.end()) {
+      if (n_tokens < 0 || n_embeds < 0 || n_tokens + n_embeds > st->cap)
+        return fail(S1_ERR_BUDGET, "prefix exceeds the state's capacity");
+      CK(cudaGraphLaunch(it->second.exec, m->stream));
+      m->launches += it->second.launches;
+      st->P = n_tokens + n_embeds;
+      return S1_OK;
+    }
+    if (!m->graph_seen.insert(key).second) {   // second occurrence: capture it
+      s1_model::Graph g;
+      const int rc = fused_impl(m, 1, &d_tokens, &n_tokens, e, &n_embeds, &st, &qs_dev, &n_q, true, d_probs,
+                                d_stats, d_last_hidden, &NQ, &NO, false, &g);
+      if (rc == S1_OK) {
+        m->graph_cache[key] = g;
+      } else {
+        // an error inside the capture may have left it open: close it and drop the partial graph
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(m->stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone) {
+          cudaGraph_t partial = nullptr;
+          cudaStreamEndCapture(m->stream, &partial);
+          if (partial) cudaGraphDestroy(partial);
+        }
+        cudaGetLastError();
+        if (g.exec) cudaGraphExecDestroy(g.exec);
+        dfree(g.meta);
+      }
+      return rc;
+    }
+  }
   return fused_impl(m, 1, &d_tokens, &n_tokens, e, &n_embeds, &st, &qs_dev, &n_q, true, d_probs, d_stats,
                     d_last_hidden, &NQ, &NO);
+}
+
+int s1_set_graphs(s1_model* m, int enable) {
+  if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  CK(cudaStreamSynchronize(m->stream));
+  if (!enable) drop_graphs(m);
+  m->graphs = enable != 0;
+  return S1_OK;
 }
 
 // -- instrumentation ---------------------------------------------------------------------

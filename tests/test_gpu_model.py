@@ -423,3 +423,55 @@ def test_lm_logprobs_survive_chunk_state_growth(B, tiny_weights, tiny_requests):
             assert np.array_equal(a["probs"], b["probs"])
     finally:
         m.close()
+
+
+def test_graphs_replay_matches_eager(B, tiny_weights):
+    """With CUDA graphs on, repeated stream-ordered one-sweep calls (the second captured, the
+    rest replayed) give the eager call's results bit for bit, and a replay reads ids rewritten in
+    the same device buffers (results follow the new ids)."""
+    import ctypes as C
+    s = torch.cuda.Stream()
+    m = B.Model(tiny_weights, stream=s.cuda_stream)
+    try:
+        r0, r1 = synth.make_requests(configs.TINY, n_requests=2)
+        assert len(r0.tokens) == len(r1.tokens)
+        assert [(q.type, len(q.suffix), len(q.option_ids)) for q in r0.questions] == \
+               [(q.type, len(q.suffix), len(q.option_ids)) for q in r1.questions]
+        dt = torch.from_numpy(r0.tokens.copy()).cuda()
+        qd = [(torch.from_numpy(q.suffix.copy()).cuda(), torch.from_numpy(q.option_ids.copy()).cuda(), q.type)
+              for q in r0.questions]
+        arr = (B.Question * len(qd))()
+        for j, (su, op, t) in enumerate(qd):
+            arr[j] = B.Question(t, C.cast(C.c_void_p(su.data_ptr()), C.POINTER(C.c_int32)), su.numel(),
+                                C.cast(C.c_void_p(op.data_ptr()), C.POINTER(C.c_int32)), op.numel())
+        n_opt = sum(len(q.option_ids) for q in r0.questions)
+        probs = torch.zeros(n_opt, dtype=torch.float32, device="cuda")
+        stats = torch.zeros((len(qd), 8), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        st = m.state_create(len(r0.tokens))
+
+        def run():
+            m.prefill_decide_async(st, dt.data_ptr(), len(r0.tokens), arr, len(qd), probs.data_ptr(), stats.data_ptr())
+            m.sync()
+            return probs.cpu().numpy().copy(), stats.cpu().numpy().copy()
+
+        eager = run()                      # graphs off
+        m.set_graphs(True)
+        outs = [run() for _ in range(4)]   # eager, capture, replay, replay
+        for p, sstat in outs:
+            np.testing.assert_array_equal(p, eager[0])
+            np.testing.assert_array_equal(sstat, eager[1])
+        # new ids in the same buffers: the replay follows them and matches a graph-free call
+        dt.copy_(torch.from_numpy(r1.tokens))
+        for (su, op, _), q in zip(qd, r1.questions):
+            su.copy_(torch.from_numpy(q.suffix))
+            op.copy_(torch.from_numpy(q.option_ids))
+        torch.cuda.synchronize()
+        replay = run()
+        m.set_graphs(False)
+        fresh = run()
+        np.testing.assert_array_equal(replay[0], fresh[0])
+        np.testing.assert_array_equal(replay[1], fresh[1])
+        assert not np.array_equal(replay[0], eager[0])
+    finally:
+        m.close()
