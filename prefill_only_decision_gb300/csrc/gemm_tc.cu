@@ -871,10 +871,13 @@ struct Plan {
   int pair;   // 1: CTA-pair kernel (256-row tiles, cta_group::2); bn is the pair's tile width
 };
 
-// Cluster size along M: as many m tiles as share a B tile, up to 4 (2 when BN = 144).
+// Tile widths whose quarter is not a whole number of 8-row swizzle atoms: clusters of at most 2.
+constexpr bool max_cm2(int bn) { return bn == 144 || bn == 176 || bn == 208; }
+
+// Cluster size along M: as many m tiles as share a B tile, up to 4 (2 for the widths above).
 inline int cluster_m(int m_tiles, int bn) {
   int cm = m_tiles >= 4 ? 4 : (m_tiles >= 2 ? 2 : 1);
-  if (bn == 144 && cm > 2) cm = 2;
+  if (max_cm2(bn) && cm > 2) cm = 2;
   return cm;
 }
 
@@ -895,11 +898,15 @@ inline Plan plan_pair(int M, int N, int K, int bn) {
 inline int max_pairs_of(int bn, int num_sms);
 
 // Heuristic choice among the pair plans: fewest waves of pairs x tile width.
-inline Plan plan_pair_for(int M, int N, int K, int num_sms) {
-  const int cands[3] = {256, 192, 128};
+inline Plan plan_pair_for(int M, int N, int K, int epi, int num_sms) {
+  const int cands[5] = {256, 208, 192, 176, 128};
   Plan best{};
   double best_cost = 1e30;
+  const char* fb = getenv("S1_GEMM_BN");   // measurement / test override of the tile width
+  const int force_bn = fb ? atoi(fb) : -1;
   for (int bn : cands) {
+    if (epi == EPI_SWIGLU && (bn % 32)) continue;   // SwiGLU tiles hold whole 32-row gate/up groups
+    if (force_bn > 0 && bn != force_bn) continue;
     const Plan pl = plan_pair(M, N, K, bn);
     const int maxp = max_pairs_of(bn, num_sms);
     const int waves = (pl.units + maxp - 1) / maxp;
@@ -919,14 +926,17 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
   double best_cost = 1e30;
   const int kb_total = K / BK;
   const int m_tiles = (M + BM - 1) / BM;
-  const int cands[4] = {256, 192, 144, 128};
+  const int cands[6] = {256, 208, 192, 176, 144, 128};
   const char* fe = getenv("S1_GEMM_CM");   // measurement override of the cluster size
   const int force_cm = fe ? atoi(fe) : -1;
+  const char* fb = getenv("S1_GEMM_BN");   // measurement / test override of the tile width
+  const int force_bn = fb ? atoi(fb) : -1;
   for (int bn : cands) {
     if (epi == EPI_SWIGLU && (bn % 32)) continue;
+    if (force_bn > 0 && bn != force_bn) continue;
     const int n_tiles = (N + bn - 1) / bn;
     for (int cm = 1; cm <= 4; cm *= 2) {
-      if (bn == 144 && cm == 4) continue;
+      if (max_cm2(bn) && cm == 4) continue;
       if (cm > 1 && m_tiles < 2) continue;
       if (force_cm > 0 && cm != force_cm) continue;
       const int maxcl = max_clusters_of(bn, cm, num_sms);
@@ -998,6 +1008,10 @@ inline int max_clusters_of(int bn, int cm, int num_sms) {
     case 192 * 8 + 1: return max_clusters<192, 1>(num_sms);
     case 192 * 8 + 2: return max_clusters<192, 2>(num_sms);
     case 192 * 8 + 4: return max_clusters<192, 4>(num_sms);
+    case 208 * 8 + 1: return max_clusters<208, 1>(num_sms);
+    case 208 * 8 + 2: return max_clusters<208, 2>(num_sms);
+    case 176 * 8 + 1: return max_clusters<176, 1>(num_sms);
+    case 176 * 8 + 2: return max_clusters<176, 2>(num_sms);
     case 144 * 8 + 1: return max_clusters<144, 1>(num_sms);
     case 144 * 8 + 2: return max_clusters<144, 2>(num_sms);
     case 128 * 8 + 1: return max_clusters<128, 1>(num_sms);
@@ -1047,7 +1061,9 @@ int max_pairs(int num_sms) {
 inline int max_pairs_of(int bn, int num_sms) {
   switch (bn) {
     case 256: return max_pairs<256>(num_sms);
+    case 208: return max_pairs<208>(num_sms);
     case 192: return max_pairs<192>(num_sms);
+    case 176: return max_pairs<176>(num_sms);
     default: return max_pairs<128>(num_sms);
   }
 }
@@ -1083,7 +1099,7 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
 template <int BN>
 cudaError_t launch_cm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const Params& p, int cm,
                       int num_sms, cudaStream_t st) {
-  if (cm == 4) return launch_bn<BN, (BN == 144 ? 2 : 4)>(ma, mb, mo, p, num_sms, st);
+  if (cm == 4) return launch_bn<BN, (max_cm2(BN) ? 2 : 4)>(ma, mb, mo, p, num_sms, st);
   if (cm == 2) return launch_bn<BN, 2>(ma, mb, mo, p, num_sms, st);
   return launch_bn<BN, 1>(ma, mb, mo, p, num_sms, st);
 }
@@ -1143,12 +1159,16 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
   if (pl.pair) {
     switch (pl.bn) {
       case 256: e = tc::launch_pair<256>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+      case 208: e = tc::launch_pair<208>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
       case 192: e = tc::launch_pair<192>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+      case 176: e = tc::launch_pair<176>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
       default: e = tc::launch_pair<128>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
     }
   } else switch (pl.bn) {
     case 256: e = tc::launch_cm<256>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
+    case 208: e = tc::launch_cm<208>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
     case 192: e = tc::launch_cm<192>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
+    case 176: e = tc::launch_cm<176>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
     case 144: e = tc::launch_cm<144>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
     default: e = tc::launch_cm<128>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
   }
@@ -1191,8 +1211,8 @@ inline Plan plan_of(int M, int N, int K, const Tuned& t) {
 }
 
 // Times every candidate (single-CTA BN x CM, and CTA-pair BN) three times on the caller's stream
-// (tuning output `scratch`, RESADD shapes tuned with a plain fp32 store of the same size) and
-// keeps the fastest of the last two runs.
+// from a flushed L2 (tuning output `scratch`, RESADD shapes tuned with a plain fp32 store of the
+// same size) and keeps the fastest of the last two runs.
 cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
                  const LaunchCtx& lc, int variant) {
   int dev = 0;
@@ -1213,6 +1233,14 @@ cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, in
   if (!tout || (resadd && (size_t)M * N > lc.tune_floats)) return cudaSuccess;   // keep the heuristic plan
   LaunchCtx l2 = lc;
   l2.launches = nullptr;
+  // Each timed run starts with L2 flushed (a 192 MB write), as in a forward pass, where every
+  // weight tile comes from DRAM. The buffer lives for the tuning of this shape only.
+  const size_t flush_bytes = (size_t)192 << 20;
+  void* flush = nullptr;
+  if (cudaMalloc(&flush, flush_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    flush = nullptr;
+  }
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess) return cudaGetLastError();
   if (cudaEventCreate(&e1) != cudaSuccess) { cudaEventDestroy(e0); return cudaGetLastError(); }
@@ -1221,21 +1249,23 @@ cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, in
   const int m_tiles = (M + BM - 1) / BM;
   std::vector<Tuned> cands;
   if (variant != GEMM_PAIR)
-    for (int bn : {256, 192, 144, 128}) {
+    for (int bn : {256, 208, 192, 176, 144, 128}) {
       if (epi == EPI_SWIGLU && (bn % 32)) continue;
       for (int cm = 1; cm <= 4; cm *= 2) {
-        if ((bn == 144 && cm == 4) || (cm > 1 && m_tiles < 2)) continue;
+        if ((max_cm2(bn) && cm == 4) || (cm > 1 && m_tiles < 2)) continue;
         cands.push_back(Tuned{bn, cm, 0});
       }
     }
   if (variant != GEMM_SINGLE)
-    for (int bn : {256, 192, 128}) cands.push_back(Tuned{bn, 1, 1});
+    for (int bn : {256, 208, 192, 176, 128})
+      if (!(epi == EPI_SWIGLU && (bn % 32))) cands.push_back(Tuned{bn, 1, 1});
   cudaError_t err = cudaSuccess;
   for (const Tuned& c : cands) {
     if (err != cudaSuccess) break;
     const Plan cand = plan_of(M, N, K, c);
     float t = 1e30f;
     for (int rep = 0; rep < 3 && err == cudaSuccess; ++rep) {
+      if (flush) cudaMemsetAsync(flush, rep, flush_bytes, lc.stream);
       cudaEventRecord(e0, lc.stream);
       err = launch_plan(cand, X, W, M, N, K, tepi, tout, tldo, nullptr, l2);
       cudaEventRecord(e1, lc.stream);
@@ -1250,6 +1280,10 @@ cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, in
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
+  if (flush) {
+    cudaStreamSynchronize(lc.stream);
+    cudaFree(flush);
+  }
   if (err != cudaSuccess) return err;
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
@@ -1268,9 +1302,9 @@ cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, in
   if (M == 0) return cudaSuccess;
   if (!gemm_tc_supported(M, N, K, epi)) return cudaErrorInvalidValue;
   const int variant = tc::variant_of(lc);
-  tc::Plan pl = variant == GEMM_PAIR ? tc::plan_pair_for(M, N, K, lc.num_sms)
+  tc::Plan pl = variant == GEMM_PAIR ? tc::plan_pair_for(M, N, K, epi, lc.num_sms)
                                      : tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
-  if (pl.splits == 1 && lc.tune && tc::tune_enabled() && !getenv("S1_GEMM_CM")) {
+  if (pl.splits == 1 && lc.tune && tc::tune_enabled() && !getenv("S1_GEMM_CM") && !getenv("S1_GEMM_BN")) {
     cudaError_t e = tc::tune(pl, X, W, M, N, K, epi, out, ldo, lc, variant);
     if (e != cudaSuccess) return e;
   }

@@ -210,3 +210,31 @@ def test_attention(B, Hq, Hkv, hd, P, lens):
         V = np.concatenate([vc, vn[r0:r0 + n]]).astype(np.float64)
         ref = om.attention(q[r0:r0 + n].astype(np.float64), K, V, P + np.arange(n), np.arange(P + n))
         assert np.abs(got[r0:r0 + n] - ref).max() <= 2.0 ** -8 * np.abs(ref).max() + 2e-3
+
+
+@_NO_TC
+@pytest.mark.parametrize("bn", [256, 208, 192, 176, 144, 128])
+@pytest.mark.parametrize("impl", [2, 3])
+@pytest.mark.parametrize("M,N,K,epi", [(1168, 2560, 2048, 2), (300, 6176, 256, 0), (77, 3072, 512, 1)])
+def test_gemm_tile_widths(B, bn, impl, M, N, K, epi, monkeypatch):
+    """Every tile width of the single-CTA and CTA-pair kernels (S1_GEMM_BN pins the planner's choice)."""
+    if impl == 2 and bn == 144:
+        pytest.skip("no CTA-pair kernel of width 144")
+    monkeypatch.setenv("S1_GEMM_BN", str(bn))
+    g = np.random.default_rng(M + N + K + bn)
+    X = bf16_round(g.standard_normal((M, K)))
+    W = bf16_round(g.standard_normal((N, K)) * 0.05)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    dX, dW = to_dev_bf16(X), to_dev_bf16(W)
+    if epi == 1:
+        out = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    else:
+        base = g.standard_normal((M, N)).astype(np.float32) if epi == 2 else np.zeros((M, N), np.float32)
+        out = torch.from_numpy(base).cuda()
+        ref = ref + base
+    B.op_gemm(dX.data_ptr(), dW.data_ptr(), M, N, K, epi, out.data_ptr(), N, impl)
+    got = from_dev_bf16(out) if epi == 1 else out.cpu().numpy()
+    scale = np.sqrt(K) * 0.05
+    tol = 1e-5 * scale + (np.abs(ref) * 2.0 ** -8 if epi == 1 else 0)
+    err = np.abs(got - ref)
+    assert np.all(err <= tol + 1e-4 * scale), (bn, impl, err.max())
