@@ -11,13 +11,16 @@
 // Networks", 2024; it reaches the token recurrence's result up to rounding, which the pages
 // allow for chunk boundaries: System1-Omni RFC #114, section 5.)
 //
-// Three launches per layer:
-//   chunk_prep   (chunk, head)          : g, A, forward substitution for W and Ut   (parallel)
+// Launches per layer (the gated delta rule's gates and q/k L2 norms are formed inside them):
+//   chunk_prep   (chunk, head)          : gates, k norm, g, A, forward substitution for W, Ut
+//                                         (parallel)
 //   chunk_state  (sequence, head, 16 v) : U = Ut - W S^T, S <- gamma S + U^T K'     (sequential
 //                                         over chunks; records each chunk's start state)
-//   chunk_out    (chunk, head)          : O = gamma Q S_c^T + P U                   (parallel)
-// The two small matrix products of the state pass and all of chunk_out run on the tensor
-// cores (mma.sync m16n8k8 TF32 -> fp32); the state itself stays fp32.
+//   chunk_out    (chunk, head)          : q norm, O = gamma Q S_c^T + P U           (parallel)
+// Single-chunk sequences that keep no state need no state pass: in a one-sweep call the
+// prefix's pass also serves the questions that continue from it; otherwise chunk_out forms
+// their U from the start state itself. The small matrix products run on the tensor cores
+// (mma.sync m16n8k8 TF32 -> fp32); the state itself stays fp32.
 #include <algorithm>
 
 #include "common.cuh"
@@ -46,8 +49,8 @@ __device__ __forceinline__ uint32_t tf32(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return r;
 }
-// Operands already rounded to TF32 when they were produced (q, k by gdn_prep; W, Ut, U and the
-// recorded chunk states by the kernels below) are passed to the tensor cores as they are.
+// Operands already rounded to TF32 when they were produced (k by chunk_prep, q by chunk_out;
+// W, Ut, U and the recorded chunk states by the kernels below) go to the tensor cores as they are.
 __device__ __forceinline__ uint32_t raw(float x) { return __float_as_uint(x); }
 __device__ __forceinline__ float rnd(float x) { return __uint_as_float(tf32(x)); }
 // D += A(16x8, row) * B(8x8, col), tf32 inputs, fp32 accumulate

@@ -6,12 +6,15 @@
 //   warp 0       TMA producer: 128 x 64 A tile and BN x 64 B tile per stage (128-byte swizzle)
 //   warp 1       TMEM allocator and MMA issuer (one thread): 4 x tcgen05.mma (K = 16) per stage
 //   warps 2..5   epilogue: tcgen05.ld of the 128 x BN accumulator (one row per thread),
-//                fused epilogue (fp32 / bf16 / residual add / SwiGLU / split-K partial)
+//                fused epilogue (fp32 store or residual add-reduction by TMA from swizzled
+//                shared-memory boxes; bf16 / SwiGLU stores from registers; split-K partials)
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
 // overlaps the main loop of the next. Work units are (m tile, split, n tile) with the m tile
 // fastest, so CTAs running at the same time read the same weight tile (L2 reuse). When the
 // tile count cannot fill the SMs, K is split and a reduction kernel applies the epilogue in a
-// fixed order (deterministic).
+// fixed order (deterministic). A CTA-pair variant (tcgen05.mma.cta_group::2, 256-row tiles)
+// and clusters that multicast weight tiles are further candidates; the planner and a per-shape
+// autotuner choose among them. Launches use programmatic dependent launch.
 //
 // Every mbarrier wait is bounded (~1 s of %globaltimer); on expiry the kernel records an
 // error code in the caller's error word and every role leaves its loop, so no launch can
