@@ -13,6 +13,8 @@
 // flash kernel: CTA = 64 queries x one q head (4 warps x 16 rows); K/V tiles of 64 keys staged
 // in shared memory by cp.async (double-buffered, 16-byte chunks XOR-swizzled by row);
 // S = Q K^T and O += P V on the tensor cores (mma.sync m16n8k16 bf16 -> fp32).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace s1 {
@@ -52,6 +54,23 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// float at shared-memory address `saddr` of cluster CTA `rank`
+__device__ __forceinline__ float ld_cluster_f32(uint32_t saddr, uint32_t rank) {
+  uint32_t a;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(saddr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 // byte offset of 16-byte chunk c of row r in a tile whose rows are HD bf16 wide
 template <int HD>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
@@ -63,7 +82,7 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
                                                     const bf16* __restrict__ vnew, bf16* __restrict__ out,
                                                     const SeqDesc* __restrict__ seqs,
                                                     const CtxDesc* __restrict__ ctxs, int layer_f, int Hq,
-                                                    int Hkv, float scale_log2) {
+                                                    int Hkv, float scale_log2, int nparts) {
   allow_dependents();
   wait_prerequisites();
   constexpr int CH = HD / 8;                 // 16-byte chunks per row
@@ -74,9 +93,11 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
   uint8_t* sV = sK + 2 * TILE;               // 2 stages
 
   const SeqDesc sd = seqs[blockIdx.z];
-  // the last (longest-key-range) query tiles first, so the heavy CTAs do not form the tail
-  const int q0 = (gridDim.x - 1 - blockIdx.x) * BQ;
-  if (q0 >= sd.len) return;
+  // nparts CTAs (a cluster, consecutive in x) share a query tile, each taking one contiguous
+  // part of its key tiles; the last (longest-key-range) query tiles go first
+  const int part = (int)(blockIdx.x % nparts);
+  const int q0 = ((int)(gridDim.x / nparts) - 1 - (int)(blockIdx.x / nparts)) * BQ;
+  if (q0 >= sd.len) return;   // uniform over the cluster
   const int h = blockIdx.y;
   const int g = (h * Hkv) / Hq;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -95,7 +116,9 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
   const bf16* Vn = vnew + ((size_t)sd.row0 * Hkv + g) * HD;
   const size_t kstride = (size_t)Hkv * HD;
   const int n_keys = P + min(sd.len, q0 + BQ);     // keys any query of this tile can see
-  const int n_tiles = (n_keys + BKV - 1) / BKV;
+  const int n_all = (n_keys + BKV - 1) / BKV;
+  const int per = (n_all + nparts - 1) / nparts;
+  const int t_begin = min(n_all, part * per), t_end = min(n_all, t_begin + per);
 
   // ---- stage Q (rows beyond len are zero)
   for (int i = tid; i < BQ * CH; i += 128) {
@@ -118,7 +141,7 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
       cp_async16(smem_u32(sV + stage * TILE) + swz<HD>(r, c), vs + c * 8, ok);
     }
   };
-  load_kv(0, 0);
+  if (t_begin < t_end) load_kv(t_begin, 0);
   cp_commit();
 
   // Q fragments (A operand), rows 16*warp .. +15
@@ -140,9 +163,9 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
   const int qi0 = q0 + warp * 16 + (lane >> 2);    // this thread's rows: qi0 and qi0 + 8
   const int lim0 = P + qi0, lim1 = P + qi0 + 8;    // last visible key index
 
-  for (int t = 0; t < n_tiles; ++t) {
-    const int stage = t & 1;
-    if (t + 1 < n_tiles) load_kv(t + 1, stage ^ 1);
+  for (int t = t_begin; t < t_end; ++t) {
+    const int stage = (t - t_begin) & 1;
+    if (t + 1 < t_end) load_kv(t + 1, stage ^ 1);
     cp_commit();
     cp_wait<1>();
     __syncthreads();
@@ -222,6 +245,51 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
     }
     __syncthreads();
   }
+  if (nparts > 1) {
+    // publish this part's (o, m, l) in shared memory (the K/V buffers, no longer read), k-major
+    // by thread; rank 0 merges the parts in rank order
+    constexpr int NO = HD / 2;               // o values per thread
+    float* pub = reinterpret_cast<float*>(sK);
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pub[(i * 4 + e) * 128 + tid] = o[i][e];
+    pub[(NO + 0) * 128 + tid] = m0;
+    pub[(NO + 1) * 128 + tid] = m1;
+    pub[(NO + 2) * 128 + tid] = l0;
+    pub[(NO + 3) * 128 + tid] = l1;
+    cluster_sync();
+    if (cluster_ctarank() == 0) {
+      const uint32_t base = smem_u32(pub);
+      auto peer = [&](int k, int r) { return ld_cluster_f32(base + (uint32_t)((k * 128 + tid) * 4), (uint32_t)r); };
+      float M0 = -INFINITY, M1 = -INFINITY;
+      for (int r = 0; r < nparts; ++r) {
+        M0 = fmaxf(M0, peer(NO + 0, r));
+        M1 = fmaxf(M1, peer(NO + 1, r));
+      }
+      float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      for (int r = 0; r < nparts; ++r) {
+        const float pm0 = peer(NO + 0, r), pm1 = peer(NO + 1, r);
+        const float w0 = pm0 == -INFINITY ? 0.f : exp2f(pm0 - M0);
+        const float w1 = pm1 == -INFINITY ? 0.f : exp2f(pm1 - M1);
+        L0 += w0 * peer(NO + 2, r);
+        L1 += w1 * peer(NO + 3, r);
+#pragma unroll
+        for (int i = 0; i < HD / 8; ++i) {
+          o[i][0] += w0 * peer(i * 4 + 0, r);
+          o[i][1] += w0 * peer(i * 4 + 1, r);
+          o[i][2] += w1 * peer(i * 4 + 2, r);
+          o[i][3] += w1 * peer(i * 4 + 3, r);
+        }
+      }
+      l0 = L0;
+      l1 = L1;
+    }
+    cluster_sync();   // the peers' partials stay in place until rank 0 has read them
+    if (cluster_ctarank() != 0) return;
+  }
   // normalise and store rows qi0, qi0 + 8
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
   const int col = 2 * (lane & 3);
@@ -241,28 +309,65 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
 
 }  // namespace fa
 
+// Key-range parts per query tile (the cluster size): the longest key range decides.
+static int attention_parts(int max_keys) {
+  const int tiles = (max_keys + fa::BKV - 1) / fa::BKV;
+  return tiles <= 4 ? 1 : (tiles <= 24 ? 2 : 4);
+}
+
+template <int HD>
+static cudaError_t launch_flash(dim3 grid, int nparts, int smem, cudaStream_t st, const bf16* q, const bf16* knew,
+                                const bf16* vnew, bf16* out, const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f,
+                                int Hq, int Hkv, float scale_log2) {
+  static bool set = false;
+  if (!set) {
+    cudaError_t e = cudaFuncSetAttribute(fa::flash_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = nparts;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, fa::flash_kernel<HD>, q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2,
+                            nparts);
+}
+
 cudaError_t launch_attention(const bf16* q, const bf16* knew, const bf16* vnew, bf16* out,
                              const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx, int layer_f,
-                             int Hq, int Hkv, int hd, int max_len, cudaStream_t st) {
+                             int Hq, int Hkv, int hd, int max_len, int max_keys, long work_ctas, int num_sms,
+                             cudaStream_t st) {
   if (n_seq <= 0 || max_len <= 0) return cudaSuccess;
   if (n_seq > 65535) return cudaErrorInvalidValue;
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
-  dim3 grid((max_len + fa::BQ - 1) / fa::BQ, Hq, n_seq);
-  if (hd == 128) {
-    constexpr int smem = fa::BQ * 128 * 2 + 4 * fa::BKV * 128 * 2;
-    static bool set = false;
-    if (!set) {
-      cudaError_t e = cudaFuncSetAttribute(fa::flash_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      set = true;
-    }
-    CK_RET(launch_pdl(fa::flash_kernel<128>, grid, dim3(128), smem, st, q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2));
-  } else if (hd == 64) {
-    constexpr int smem = fa::BQ * 64 * 2 + 4 * fa::BKV * 64 * 2;
-    CK_RET(launch_pdl(fa::flash_kernel<64>, grid, dim3(128), smem, st, q, knew, vnew, out, d_seq, d_ctx, layer_f, Hq, Hkv, scale_log2));
-  } else {
+  // split key ranges only when the query tiles alone leave SMs idle (two CTAs fit per SM)
+  const int nparts = work_ctas >= 2L * num_sms ? 1 : attention_parts(std::max(max_keys, max_len));
+  dim3 grid(((max_len + fa::BQ - 1) / fa::BQ) * nparts, Hq, n_seq);
+  cudaError_t e;
+  if (hd == 128)
+    e = launch_flash<128>(grid, nparts, fa::BQ * 128 * 2 + 4 * fa::BKV * 128 * 2, st, q, knew, vnew, out, d_seq, d_ctx,
+                          layer_f, Hq, Hkv, scale_log2);
+  else if (hd == 64)
+    e = launch_flash<64>(grid, nparts, fa::BQ * 64 * 2 + 4 * fa::BKV * 64 * 2, st, q, knew, vnew, out, d_seq, d_ctx,
+                         layer_f, Hq, Hkv, scale_log2);
+  else
     return cudaErrorNotSupported;
-  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

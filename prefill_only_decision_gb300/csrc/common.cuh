@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <atomic>
 #include <utility>
 #include "internal.h"
 
@@ -52,10 +53,17 @@ __device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcont
     if (e_ != cudaSuccess) return e_;           \
   } while (0)
 
-// Programmatic dependent launch is on unless S1_PDL=0 (a measurement override).
+// Models being profiled (their per-launch CUDA events must not absorb an early-launched kernel's
+// wait for its predecessor, so programmatic dependent launch is off while any model profiles).
+inline std::atomic<int>& pdl_suppressed() {
+  static std::atomic<int> n{0};
+  return n;
+}
+// Programmatic dependent launch is on unless S1_PDL=0 (a measurement override) or a model
+// is being profiled.
 inline bool pdl_enabled() {
   static const bool on = !(getenv("S1_PDL") && getenv("S1_PDL")[0] == '0');
-  return on;
+  return on && pdl_suppressed().load(std::memory_order_relaxed) == 0;
 }
 
 // Launch with the programmatic-serialisation attribute: the kernel may start while its

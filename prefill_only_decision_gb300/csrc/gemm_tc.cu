@@ -1076,7 +1076,7 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
                         cudaStream_t st) {
   const int mp = max_pairs<BN>(num_sms);
   cudaLaunchAttribute attr[2];
-  static const bool pdl = !(getenv("S1_PDL") && getenv("S1_PDL")[0] == '0');
+  const bool pdl = pdl_enabled();
   cudaLaunchConfig_t cfg = launch_config_pair<BN>(attr, st, pdl);
   p.m_groups = p.m_tiles / 2;
   p.units = p.m_groups * p.splits * p.n_tiles;
@@ -1090,7 +1090,7 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
                       cudaStream_t st) {
   const int mc = max_clusters<BN, CM>(num_sms);
   cudaLaunchAttribute attr[2];
-  static const bool pdl = !(getenv("S1_PDL") && getenv("S1_PDL")[0] == '0');
+  const bool pdl = pdl_enabled();
   cudaLaunchConfig_t cfg = launch_config<BN, CM>(attr, st, pdl);
   p.m_groups = (p.m_tiles + CM - 1) / CM;
   p.units = p.m_groups * p.splits * p.n_tiles;

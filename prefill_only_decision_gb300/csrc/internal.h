@@ -96,7 +96,8 @@ cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab,
                               cudaStream_t st);
 cudaError_t launch_attention(const bf16* q, const bf16* knew, const bf16* vnew, bf16* out,
                              const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx, int layer_f,
-                             int Hq, int Hkv, int hd, int max_len, cudaStream_t st);
+                             int Hq, int Hkv, int hd, int max_len, int max_keys, long work_ctas, int num_sms,
+                             cudaStream_t st);
 cudaError_t launch_readout(const float* x, const float* final_norm, const bf16* E, int d, float eps,
                            const int* q_row, const int* q_type, const int* opt_off,
                            const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,

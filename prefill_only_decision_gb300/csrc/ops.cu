@@ -143,8 +143,13 @@ int s1_op_attention(const void* q, const void* k_new, const void* v_new, const v
   if (!dseq || !dctx) return op_fail(S1_ERR_OOM, "attention: temporaries");
   OCK(cudaMemcpyAsync(dseq, seqs.data(), seqs.size() * sizeof(SeqDesc), cudaMemcpyHostToDevice, st));
   OCK(cudaMemcpyAsync(dctx, &c, sizeof(CtxDesc), cudaMemcpyHostToDevice, st));
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long work_ctas = 0;
+  for (int i = 0; i < n_seq; ++i) work_ctas += (long)((len[i] + 63) / 64) * Hq;
   OCK(launch_attention((const bf16*)q, (const bf16*)k_new, (const bf16*)v_new, (bf16*)out, dseq, n_seq,
-                       dctx, 0, Hq, Hkv, hd, max_len, st));
+                       dctx, 0, Hq, Hkv, hd, max_len, P + max_len, work_ctas, sms, st));
   OCK(cudaStreamSynchronize(st));
   return S1_OK;
 }

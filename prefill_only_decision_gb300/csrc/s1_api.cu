@@ -455,6 +455,12 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
   const int d = s.d_model, F = s.ffn;
   Scratch& sc = m->sc;
   cudaStream_t st = m->stream;
+  int max_keys = 0;     // longest key range of any sequence (snapshot rows + own rows)
+  long att_tiles = 0;   // query tiles of the attention launches (per head)
+  for (const SeqDesc& q : mt.seqs) {
+    max_keys = std::max(max_keys, q.len + (q.ctx_in >= 0 ? mt.ctxs[q.ctx_in].P : 0));
+    att_tiles += (q.len + 63) / 64;
+  }
   const size_t plane = (size_t)R * d;
   if (m->trace && (long long)((s.n_layers + 1) * plane) > m->trace_floats)
     return fail(S1_ERR_BUDGET, "layer trace holds %lld floats, this call needs %zu", m->trace_floats,
@@ -516,7 +522,8 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
       {
         ProfScope ps(m, S1_PROF_ATTN, 0, 0);
         CK(launch_attention(sc.q, sc.knew, sc.vnew, sc.mix, mt.d_seqs, nseq, mt.d_ctxs, L.ord,
-                            s.fa_q_heads, s.fa_kv_heads, s.fa_head_dim, mt.max_len, st));
+                            s.fa_q_heads, s.fa_kv_heads, s.fa_head_dim, mt.max_len, max_keys,
+                            att_tiles * s.fa_q_heads, m->num_sms, st));
         m->launches += 1;
       }
     }
@@ -936,6 +943,7 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
 void s1_model_destroy(s1_model* m) {
   if (!valid_model(m)) return;
   cudaStreamSynchronize(m->stream);
+  if (m->prof) --pdl_suppressed();
   drop_graphs(m);
   free_scratch(m->sc);
   dfree(m->arena);
@@ -1437,6 +1445,9 @@ int s1_set_graphs(s1_model* m, int enable) {
 // -- instrumentation ---------------------------------------------------------------------
 int s1_profile(s1_model* m, int enable) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  CK(cudaStreamSynchronize(m->stream));
+  if (enable && !m->prof) ++pdl_suppressed();
+  if (!enable && m->prof) --pdl_suppressed();
   m->prof = enable != 0;
   m->prof_ev.clear();
   m->ev_next = 0;
