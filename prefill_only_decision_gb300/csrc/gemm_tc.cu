@@ -929,14 +929,16 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
   double best_cost = 1e30;
   const int kb_total = K / BK;
   const int m_tiles = (M + BM - 1) / BM;
-  const int cands[6] = {256, 208, 192, 176, 144, 128};
+  // (176 and 208 are autotuner candidates only: measured slower than 144 in the split-K,
+  // few-row weight-streaming plans this heuristic chooses; S1_GEMM_BN may still pin them)
+  const int cands[6] = {256, 192, 144, 128, 208, 176};
   const char* fe = getenv("S1_GEMM_CM");   // measurement override of the cluster size
   const int force_cm = fe ? atoi(fe) : -1;
   const char* fb = getenv("S1_GEMM_BN");   // measurement / test override of the tile width
   const int force_bn = fb ? atoi(fb) : -1;
   for (int bn : cands) {
     if (epi == EPI_SWIGLU && (bn % 32)) continue;
-    if (force_bn > 0 && bn != force_bn) continue;
+    if (force_bn > 0 ? bn != force_bn : (bn == 208 || bn == 176)) continue;
     const int n_tiles = (N + bn - 1) / bn;
     for (int cm = 1; cm <= 4; cm *= 2) {
       if (max_cm2(bn) && cm == 4) continue;
