@@ -294,7 +294,7 @@ def main():
     binding.use_torch_allocator()
     model = binding.Model(W, stream=stream.cuda_stream)
     if not args.no_graphs:
-        model.set_graphs(True)   # repeated stream-ordered one-sweep calls replay a captured graph
+        model.set_graphs(True)   # repeated stream-ordered calls replay a captured graph
     n_q = len(req.questions)
     P = req.prefix_rows
 
@@ -458,7 +458,7 @@ def main():
                        "model": "4B-class hybrid decoder (24 gated delta-rule + 8 GQA layers, d 2560, "
                                 "FFN 9216, LoRA r32 merged)" if cfg.name.startswith("4b") else cfg.name,
                        "decisions_per_step": n_q, "parallelism": f"replicas x{ws}",
-                       "cuda_graphs": (not args.no_graphs) and args.path == "fused",
+                       "cuda_graphs": not args.no_graphs,
                        "l2": "inputs larger than L2 (weights read every step)",
                        "path": args.path + (" (s1_prefill_decide_async)" if args.path == "fused"
                                             else " (s1_prefill_async + s1_decide_async)"),

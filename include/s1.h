@@ -209,10 +209,12 @@ int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, 
                             const void* d_embeds, int32_t n_embeds, const s1_question* qs_dev,
                             int32_t n_q, float* d_probs, float* d_stats, float* d_last_hidden);
 
-/* CUDA graphs for s1_prefill_decide_async (off by default). While enabled, a call whose
- * signature — state handle and capacity, every device pointer, size and question type it
- * passes — repeats an earlier call's is captured once into a CUDA graph (its second occurrence)
- * and later occurrences replay that graph with one launch: the ids, embeddings and outputs are
+/* CUDA graphs for the stream-ordered calls s1_prefill_async, s1_decide_async and
+ * s1_prefill_decide_async (off by default). While enabled, a call whose signature — the
+ * function, the state handle, its buffers and capacity (and, for s1_decide_async, its prefix
+ * length), every device pointer, size and question type it passes — repeats an earlier call's
+ * is captured once into a CUDA graph (its second occurrence) and later occurrences replay that
+ * graph with one launch: the ids, embeddings and outputs are
  * read and written through the same device buffers at replay time, so their contents may change
  * between calls while their addresses and sizes may not. Graphs are not used on the legacy
  * default stream, while profiling or a layer trace is on. A graph is dropped when the model's

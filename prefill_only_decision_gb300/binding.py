@@ -333,7 +333,8 @@ class Model:
         check(lib().s1_set_gemm_impl(self.h, impl))
 
     def set_graphs(self, enable: bool):
-        """CUDA graphs for prefill_decide_async calls whose signature repeats (s1_set_graphs)."""
+        """CUDA graphs for the stream-ordered calls (prefill_async, decide_async,
+        prefill_decide_async) whose signature repeats (s1_set_graphs)."""
         check(lib().s1_set_graphs(self.h, 1 if enable else 0))
 
     def set_layer_trace(self, ptr: int, capacity_floats: int):

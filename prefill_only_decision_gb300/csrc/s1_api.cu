@@ -987,10 +987,93 @@ void s1_state_destroy(s1_state* st) {
 
 int s1_state_rows(const s1_state* st) { return (st && st->magic == STATE_MAGIC) ? st->P : -1; }
 
+extern "C++" {
+// -- CUDA graphs of the stream-ordered calls ----------------------------------------------
+// Runs `body` (everything a call enqueues after its metadata upload) eagerly, or, with `cap`,
+// captures it into cap->exec and launches that graph once. Kernel launches counted while
+// capturing are booked to the graph, which adds them on every replay.
+template <class Body>
+static int run_captured(s1_model* m, s1_model::Graph* cap, Body&& body) {
+  if (!cap) return body();
+  const long launches0 = m->launches;
+  CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
+  int rc = body();
+  cudaGraph_t g = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(m->stream, &g);
+  if (rc == S1_OK && ec != cudaSuccess) rc = fail(S1_ERR_CUDA, "graph capture: %s", cudaGetErrorString(ec));
+  if (rc == S1_OK) {
+    const cudaError_t ei = cudaGraphInstantiate(&cap->exec, g, 0);
+    if (ei != cudaSuccess) rc = fail(S1_ERR_CUDA, "graph instantiation: %s", cudaGetErrorString(ei));
+  }
+  if (g) cudaGraphDestroy(g);
+  cap->launches = m->launches - launches0;
+  m->launches = launches0;
+  if (rc == S1_OK) {
+    CK(cudaGraphLaunch(cap->exec, m->stream));
+    m->launches += cap->launches;
+  }
+  return rc;
+}
+
+// Signature of a stream-ordered call: every pointer, size and descriptor it passes, plus the
+// state buffers it reads or writes. Two calls with equal signatures enqueue identical work.
+struct CallKey {
+  std::string s;
+  explicit CallKey(char kind) : s(1, kind) {}
+  template <class T> CallKey& add(const T& v) {
+    s.append((const char*)&v, sizeof(T));
+    return *this;
+  }
+  CallKey& state(const s1_state* st, bool with_rows) {
+    add(st).add(st->S).add(st->KV).add(st->cap);
+    if (with_rows) add(st->P);
+    return *this;
+  }
+  // field by field: the struct's padding bytes are not part of the signature
+  CallKey& question(const s1_question& q) {
+    return add(q.type).add(q.suffix).add(q.n_suffix).add(q.option_ids).add(q.n_options);
+  }
+};
+
+// With graphs on, a call whose signature was seen before replays (on its second occurrence,
+// captures) a graph; `run(cap)` performs the call, capturing into `cap` when it is non-null,
+// and `replayed()` applies the host-side effects of a replay. Anything else runs eagerly.
+template <class Run, class Replayed>
+static int graph_call(s1_model* m, const CallKey& key, Run&& run, Replayed&& replayed) {
+  if (!m->graphs || m->prof || m->trace || m->stream == nullptr) return run(nullptr);
+  auto it = m->graph_cache.find(key.s);
+  if (it != m->graph_cache.end()) {
+    CK(cudaGraphLaunch(it->second.exec, m->stream));
+    m->launches += it->second.launches;
+    replayed();
+    return S1_OK;
+  }
+  if (m->graph_seen.insert(key.s).second) return run(nullptr);
+  s1_model::Graph g;
+  const int rc = run(&g);
+  if (rc == S1_OK) {
+    m->graph_cache[key.s] = g;
+  } else {
+    // an error inside the capture may have left it open: close it and drop the partial graph
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(m->stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone) {
+      cudaGraph_t partial = nullptr;
+      cudaStreamEndCapture(m->stream, &partial);
+      if (partial) cudaGraphDestroy(partial);
+    }
+    cudaGetLastError();
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    dfree(g.meta);
+  }
+  return rc;
+}
+
+}  // extern "C++"
+
 // -- prefill -----------------------------------------------------------------------------
 static int prefill_impl(s1_model* m, int n_req, const int32_t* const* tokens, const int32_t* n_tokens,
                         const void* const* embeds, const int32_t* n_embeds, s1_state** states,
-                        bool device_ptrs) {
+                        bool device_ptrs, s1_model::Graph* cap = nullptr) {
   Meta mt;
   int R = 0, NE = 0;
   int rc = build_prefill_meta(m, n_req, n_tokens, n_embeds, states, mt, &R, &NE);
@@ -1009,31 +1092,34 @@ static int prefill_impl(s1_model* m, int n_req, const int32_t* const* tokens, co
     }
     row += n_tokens[r];
   }
-  rc = upload_meta(m, mt);
+  for (int r = 0; r < n_req; ++r)
+    if (n_embeds[r] > 0 && (!embeds || !embeds[r])) return fail(S1_ERR_INVALID_ARG, "request %d: NULL embeds", r);
+  rc = upload_meta(m, mt, cap ? &cap->meta : nullptr);
   if (rc) return rc;
-  if (device_ptrs) {
-    row = 0;
-    for (int r = 0; r < n_req; ++r) {
-      row += n_embeds[r];
-      if (n_tokens[r] > 0)
-        CK(cudaMemcpyAsync(mt.d_row_src + row, tokens[r], n_tokens[r] * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
-      row += n_tokens[r];
+  rc = run_captured(m, cap, [&]() -> int {
+    if (device_ptrs) {
+      int rr = 0;
+      for (int r = 0; r < n_req; ++r) {
+        rr += n_embeds[r];
+        if (n_tokens[r] > 0)
+          CK(cudaMemcpyAsync(mt.d_row_src + rr, tokens[r], n_tokens[r] * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+        rr += n_tokens[r];
+      }
     }
-  }
-  // given embedding rows are staged in the normed-activation buffer (free until layer 0)
-  const size_t rowb = (size_t)m->sh.d_model * 2;
-  if (NE > 0) {
-    size_t eoff = 0;
-    for (int r = 0; r < n_req; ++r) {
-      if (n_embeds[r] == 0) continue;
-      if (!embeds || !embeds[r]) return fail(S1_ERR_INVALID_ARG, "request %d: NULL embeds", r);
-      CK(cudaMemcpyAsync((char*)m->sc.xn + eoff, embeds[r], n_embeds[r] * rowb,
-                         device_ptrs ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, m->stream));
-      if (!device_ptrs) m->h2d_bytes += (long long)(n_embeds[r] * rowb);
-      eoff += n_embeds[r] * rowb;
+    // given embedding rows are staged in the normed-activation buffer (free until layer 0)
+    const size_t rowb = (size_t)m->sh.d_model * 2;
+    if (NE > 0) {
+      size_t eoff = 0;
+      for (int r = 0; r < n_req; ++r) {
+        if (n_embeds[r] == 0) continue;
+        CK(cudaMemcpyAsync((char*)m->sc.xn + eoff, embeds[r], n_embeds[r] * rowb,
+                           device_ptrs ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, m->stream));
+        if (!device_ptrs) m->h2d_bytes += (long long)(n_embeds[r] * rowb);
+        eoff += n_embeds[r] * rowb;
+      }
     }
-  }
-  rc = run_forward(m, mt, m->sc.xn, nullptr, nullptr, nullptr);
+    return run_forward(m, mt, m->sc.xn, nullptr, nullptr, nullptr);
+  });
   if (rc) return rc;
   for (int r = 0; r < n_req; ++r) states[r]->P = n_tokens[r] + n_embeds[r];
   return S1_OK;
@@ -1075,31 +1161,38 @@ int s1_prefill_async(s1_model* m, s1_state* st, const int32_t* d_tokens, int32_t
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
   if (!valid_state(m, st)) return fail(S1_ERR_INVALID_HANDLE, "invalid state");
   const void* e[1] = {d_embeds};
-  return prefill_impl(m, 1, &d_tokens, &n_tokens, e, &n_embeds, &st, true);
+  CallKey key('P');
+  key.state(st, false).add(d_tokens).add(n_tokens).add(d_embeds).add(n_embeds);
+  return graph_call(
+      m, key,
+      [&](s1_model::Graph* cap) { return prefill_impl(m, 1, &d_tokens, &n_tokens, e, &n_embeds, &st, true, cap); },
+      [&]() { st->P = n_tokens + n_embeds; });
 }
 
 // -- decide ------------------------------------------------------------------------------
 static int decide_impl(s1_model* m, int n_req, const s1_state* const* states, const s1_question* const* qs,
                        const int32_t* n_q, bool device_ptrs, float* d_probs, float* d_stats,
-                       float* d_hidden, Meta& mt, int* NQ, int* NO) {
+                       float* d_hidden, Meta& mt, int* NQ, int* NO, s1_model::Graph* cap = nullptr) {
   int R = 0;
   int rc = build_decide_meta(m, n_req, states, qs, n_q, !device_ptrs, mt, &R, NQ, NO);
   if (rc) return rc;
-  rc = upload_meta(m, mt);
+  rc = upload_meta(m, mt, cap ? &cap->meta : nullptr);
   if (rc) return rc;
-  if (device_ptrs) {
-    // gather ids from the caller's device arrays into the uploaded metadata
-    int row = 0, opt = 0;
-    for (int r = 0; r < n_req; ++r)
-      for (int j = 0; j < n_q[r]; ++j) {
-        const s1_question& q = qs[r][j];
-        CK(cudaMemcpyAsync(mt.d_row_src + row, q.suffix, q.n_suffix * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
-        CK(cudaMemcpyAsync(mt.d_opt_ids + opt, q.option_ids, q.n_options * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
-        row += q.n_suffix;
-        opt += q.n_options;
-      }
-  }
-  return run_forward(m, mt, nullptr, d_probs, d_stats, d_hidden);
+  return run_captured(m, cap, [&]() -> int {
+    if (device_ptrs) {
+      // gather ids from the caller's device arrays into the uploaded metadata
+      int row = 0, opt = 0;
+      for (int r = 0; r < n_req; ++r)
+        for (int j = 0; j < n_q[r]; ++j) {
+          const s1_question& q = qs[r][j];
+          CK(cudaMemcpyAsync(mt.d_row_src + row, q.suffix, q.n_suffix * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+          CK(cudaMemcpyAsync(mt.d_opt_ids + opt, q.option_ids, q.n_options * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+          row += q.n_suffix;
+          opt += q.n_options;
+        }
+    }
+    return run_forward(m, mt, nullptr, d_probs, d_stats, d_hidden);
+  });
 }
 
 // Copies the readout outputs (probs | stats | hidden in the scratch output block) back into
@@ -1190,9 +1283,19 @@ int s1_decide_async(s1_model* m, const s1_state* st, const s1_question* qs_dev, 
                     float* d_probs, float* d_stats, float* d_last_hidden) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
   if (!d_probs || !d_stats) return fail(S1_ERR_INVALID_ARG, "NULL output");
-  Meta mt;
-  int NQ = 0, NO = 0;
-  return decide_impl(m, 1, &st, &qs_dev, &n_q, true, d_probs, d_stats, d_last_hidden, mt, &NQ, &NO);
+  if (!valid_state(m, st)) return fail(S1_ERR_INVALID_HANDLE, "invalid state");
+  if (n_q < 1 || !qs_dev) return fail(S1_ERR_INVALID_ARG, "no questions");
+  CallKey key('D');
+  key.state(st, true).add(d_probs).add(d_stats).add(d_last_hidden).add(n_q);
+  for (int j = 0; j < n_q; ++j) key.question(qs_dev[j]);
+  return graph_call(
+      m, key,
+      [&](s1_model::Graph* cap) {
+        Meta mt;
+        int NQ = 0, NO = 0;
+        return decide_impl(m, 1, &st, &qs_dev, &n_q, true, d_probs, d_stats, d_last_hidden, mt, &NQ, &NO, cap);
+      },
+      []() {});
 }
 
 // -- fused sweep: prefixes and their questions in one pass over the layers ---------------
@@ -1268,54 +1371,37 @@ static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, cons
     }
   rc = upload_meta(m, mt, cap ? &cap->meta : nullptr);
   if (rc) return rc;
-  // capture: everything from here on (id copies, the forward) becomes the graph
-  const long launches0 = m->launches;
-  if (cap) CK(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
-  if (device_ptrs) {
-    int rr = 0, opt = 0;
-    for (int r = 0; r < n_req; ++r) {
-      rr += n_embeds[r];
-      if (n_tokens[r] > 0)
-        CK(cudaMemcpyAsync(mt.d_row_src + rr, tokens[r], n_tokens[r] * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
-      rr += n_tokens[r];
-    }
-    for (int r = 0; r < n_req; ++r)
-      for (int j = 0; j < n_q[r]; ++j) {
-        const s1_question& q = qs[r][j];
-        CK(cudaMemcpyAsync(mt.d_row_src + rr, q.suffix, q.n_suffix * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
-        CK(cudaMemcpyAsync(mt.d_opt_ids + opt, q.option_ids, q.n_options * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
-        rr += q.n_suffix;
-        opt += q.n_options;
+  rc = run_captured(m, cap, [&]() -> int {
+    if (device_ptrs) {
+      int rr = 0, opt = 0;
+      for (int r = 0; r < n_req; ++r) {
+        rr += n_embeds[r];
+        if (n_tokens[r] > 0)
+          CK(cudaMemcpyAsync(mt.d_row_src + rr, tokens[r], n_tokens[r] * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+        rr += n_tokens[r];
       }
-  }
-  if (NE > 0) {
-    const size_t rowb = (size_t)m->sh.d_model * 2;
-    size_t eoff = 0;
-    for (int r = 0; r < n_req; ++r) {
-      if (n_embeds[r] == 0) continue;
-      CK(cudaMemcpyAsync((char*)m->sc.xn + eoff, embeds[r], n_embeds[r] * rowb,
-                         device_ptrs ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, m->stream));
-      if (!device_ptrs) m->h2d_bytes += (long long)(n_embeds[r] * rowb);
-      eoff += n_embeds[r] * rowb;
+      for (int r = 0; r < n_req; ++r)
+        for (int j = 0; j < n_q[r]; ++j) {
+          const s1_question& q = qs[r][j];
+          CK(cudaMemcpyAsync(mt.d_row_src + rr, q.suffix, q.n_suffix * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+          CK(cudaMemcpyAsync(mt.d_opt_ids + opt, q.option_ids, q.n_options * sizeof(int), cudaMemcpyDeviceToDevice, m->stream));
+          rr += q.n_suffix;
+          opt += q.n_options;
+        }
     }
-  }
-  rc = run_forward(m, mt, m->sc.xn, d_probs, d_stats, d_hidden, want_lm);
-  if (cap) {
-    cudaGraph_t g = nullptr;
-    const cudaError_t ec = cudaStreamEndCapture(m->stream, &g);
-    if (rc == S1_OK && ec != cudaSuccess) rc = fail(S1_ERR_CUDA, "graph capture: %s", cudaGetErrorString(ec));
-    if (rc == S1_OK) {
-      const cudaError_t ei = cudaGraphInstantiate(&cap->exec, g, 0);
-      if (ei != cudaSuccess) rc = fail(S1_ERR_CUDA, "graph instantiation: %s", cudaGetErrorString(ei));
+    if (NE > 0) {
+      const size_t rowb = (size_t)m->sh.d_model * 2;
+      size_t eoff = 0;
+      for (int r = 0; r < n_req; ++r) {
+        if (n_embeds[r] == 0) continue;
+        CK(cudaMemcpyAsync((char*)m->sc.xn + eoff, embeds[r], n_embeds[r] * rowb,
+                           device_ptrs ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice, m->stream));
+        if (!device_ptrs) m->h2d_bytes += (long long)(n_embeds[r] * rowb);
+        eoff += n_embeds[r] * rowb;
+      }
     }
-    if (g) cudaGraphDestroy(g);
-    cap->launches = m->launches - launches0;
-    m->launches = launches0;
-    if (rc == S1_OK) {
-      CK(cudaGraphLaunch(cap->exec, m->stream));
-      m->launches += cap->launches;
-    }
-  }
+    return run_forward(m, mt, m->sc.xn, d_probs, d_stats, d_hidden, want_lm);
+  });
   if (rc) return rc;
   for (int r = 0; r < n_req; ++r) states[r]->P = n_tokens[r] + n_embeds[r];
   *NQ_out = NQ;
@@ -1390,48 +1476,19 @@ int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, 
   if (!valid_state(m, st)) return fail(S1_ERR_INVALID_HANDLE, "invalid state");
   if (!d_probs || !d_stats) return fail(S1_ERR_INVALID_ARG, "NULL output");
   const void* e[1] = {d_embeds};
-  int NQ = 0, NO = 0;
-  if (m->graphs && !m->prof && !m->trace && m->stream != nullptr && n_q > 0 && qs_dev) {
-    // the call's signature: every pointer, size and type it passes, and the state's capacity
-    std::string key;
-    auto add = [&key](const void* p, size_t n) { key.append((const char*)p, n); };
-    add(&st, sizeof(st)); add(&st->cap, sizeof(int));
-    add(&d_tokens, sizeof(d_tokens)); add(&n_tokens, sizeof(n_tokens));
-    add(&d_embeds, sizeof(d_embeds)); add(&n_embeds, sizeof(n_embeds));
-    add(&d_probs, sizeof(d_probs)); add(&d_stats, sizeof(d_stats)); add(&d_last_hidden, sizeof(d_last_hidden));
-    for (int j = 0; j < n_q; ++j) add(&qs_dev[j], sizeof(s1_question));
-    auto it = m->graph_cache.find(key);
-    if (it != m->graph_cache.end()) {
-      if (n_tokens < 0 || n_embeds < 0 || n_tokens + n_embeds > st->cap)
-        return fail(S1_ERR_BUDGET, "prefix exceeds the state's capacity");
-      CK(cudaGraphLaunch(it->second.exec, m->stream));
-      m->launches += it->second.launches;
-      st->P = n_tokens + n_embeds;
-      return S1_OK;
-    }
-    if (!m->graph_seen.insert(key).second) {   // second occurrence: capture it
-      s1_model::Graph g;
-      const int rc = fused_impl(m, 1, &d_tokens, &n_tokens, e, &n_embeds, &st, &qs_dev, &n_q, true, d_probs,
-                                d_stats, d_last_hidden, &NQ, &NO, false, &g);
-      if (rc == S1_OK) {
-        m->graph_cache[key] = g;
-      } else {
-        // an error inside the capture may have left it open: close it and drop the partial graph
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(m->stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone) {
-          cudaGraph_t partial = nullptr;
-          cudaStreamEndCapture(m->stream, &partial);
-          if (partial) cudaGraphDestroy(partial);
-        }
-        cudaGetLastError();
-        if (g.exec) cudaGraphExecDestroy(g.exec);
-        dfree(g.meta);
-      }
-      return rc;
-    }
-  }
-  return fused_impl(m, 1, &d_tokens, &n_tokens, e, &n_embeds, &st, &qs_dev, &n_q, true, d_probs, d_stats,
-                    d_last_hidden, &NQ, &NO);
+  if (n_q < 1 || !qs_dev) return fail(S1_ERR_INVALID_ARG, "no questions");
+  CallKey key('F');
+  key.state(st, false).add(d_tokens).add(n_tokens).add(d_embeds).add(n_embeds);
+  key.add(d_probs).add(d_stats).add(d_last_hidden).add(n_q);
+  for (int j = 0; j < n_q; ++j) key.question(qs_dev[j]);
+  return graph_call(
+      m, key,
+      [&](s1_model::Graph* cap) {
+        int NQ = 0, NO = 0;
+        return fused_impl(m, 1, &d_tokens, &n_tokens, e, &n_embeds, &st, &qs_dev, &n_q, true, d_probs, d_stats,
+                          d_last_hidden, &NQ, &NO, false, cap);
+      },
+      [&]() { st->P = n_tokens + n_embeds; });
 }
 
 int s1_set_graphs(s1_model* m, int enable) {

@@ -475,3 +475,61 @@ def test_graphs_replay_matches_eager(B, tiny_weights):
         assert not np.array_equal(replay[0], eager[0])
     finally:
         m.close()
+
+
+@pytest.mark.gpu
+def test_graphs_two_call_path(B, tiny_weights):
+    """With CUDA graphs on, the stream-ordered prefill and decide calls (each captured on its
+    second occurrence, then replayed) give the eager calls' results bit for bit; replays follow
+    ids rewritten in the same device buffers, and a decide after a shorter prefill (another
+    prefix length) does not replay the longer prefix's graph."""
+    import ctypes as C
+    s = torch.cuda.Stream()
+    m = B.Model(tiny_weights, stream=s.cuda_stream)
+    try:
+        r0, r1 = synth.make_requests(configs.TINY, n_requests=2)
+        P = len(r0.tokens)
+        assert len(r1.tokens) == P
+        dt = torch.from_numpy(r0.tokens.copy()).cuda()
+        qd = [(torch.from_numpy(q.suffix.copy()).cuda(), torch.from_numpy(q.option_ids.copy()).cuda(), q.type)
+              for q in r0.questions]
+        arr = (B.Question * len(qd))()
+        for j, (su, op, t) in enumerate(qd):
+            arr[j] = B.Question(t, C.cast(C.c_void_p(su.data_ptr()), C.POINTER(C.c_int32)), su.numel(),
+                                C.cast(C.c_void_p(op.data_ptr()), C.POINTER(C.c_int32)), op.numel())
+        n_opt = sum(len(q.option_ids) for q in r0.questions)
+        probs = torch.zeros(n_opt, dtype=torch.float32, device="cuda")
+        stats = torch.zeros((len(qd), 8), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        st = m.state_create(P)
+
+        def run(n=P):
+            m.prefill_async(st, dt.data_ptr(), n)
+            m.decide_async(st, arr, len(qd), probs.data_ptr(), stats.data_ptr())
+            m.sync()
+            return probs.cpu().numpy().copy(), stats.cpu().numpy().copy()
+
+        eager = run()
+        eager_short = run(P - 3)
+        m.set_graphs(True)
+        outs = [run() for _ in range(4)]     # eager, capture, replay, replay
+        for p, sstat in outs:
+            np.testing.assert_array_equal(p, eager[0])
+            np.testing.assert_array_equal(sstat, eager[1])
+        for _ in range(3):                   # another prefix length: its own graphs
+            p, sstat = run(P - 3)
+            np.testing.assert_array_equal(p, eager_short[0])
+            np.testing.assert_array_equal(sstat, eager_short[1])
+        dt.copy_(torch.from_numpy(r1.tokens))
+        for (su, op, _), q in zip(qd, r1.questions):
+            su.copy_(torch.from_numpy(q.suffix))
+            op.copy_(torch.from_numpy(q.option_ids))
+        torch.cuda.synchronize()
+        replay = run()
+        m.set_graphs(False)
+        fresh = run()
+        np.testing.assert_array_equal(replay[0], fresh[0])
+        np.testing.assert_array_equal(replay[1], fresh[1])
+        assert not np.array_equal(replay[0], eager[0])
+    finally:
+        m.close()
