@@ -795,6 +795,42 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
   }
 }
 
+// Split-K reduction of a residual-add GEMM with the RMSNorm that follows it: one block per
+// row sums the partials in split order, adds them to the residual row and writes it back, then
+// writes the row normalised. Per element and per thread the sums run in the same order as
+// splitk_reduce_kernel followed by the block-per-row RMSNorm, so the results are the same bits.
+__global__ void __launch_bounds__(256) splitk_resadd_norm_kernel(const float* __restrict__ ws, int splits, int Mpad,
+                                                                 int N, float* __restrict__ x, int ldx,
+                                                                 const float* __restrict__ w, bf16* __restrict__ xn,
+                                                                 float eps) {
+  allow_dependents();
+  wait_prerequisites();
+  __shared__ float red[32];
+  const int m = blockIdx.x;
+  float4* xr = reinterpret_cast<float4*>(x + (size_t)m * ldx);
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < N / 4; i += blockDim.x) {
+    float4 a = make_float4(0, 0, 0, 0);
+    for (int s = 0; s < splits; ++s) {
+      const float4 b = *reinterpret_cast<const float4*>(ws + ((size_t)s * Mpad + m) * N + 4 * i);
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    float4 v = xr[i];
+    v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
+    xr[i] = v;
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)N + eps);
+  const float4* wr = reinterpret_cast<const float4*>(w);
+  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(xn + (size_t)m * N);
+  for (int i = threadIdx.x; i < N / 4; i += blockDim.x) {
+    const float4 v = xr[i], g = wr[i];   // this thread's own row entries, written above
+    o2[2 * i] = __floats2bfloat162_rn(v.x * inv * g.x, v.y * inv * g.y);
+    o2[2 * i + 1] = __floats2bfloat162_rn(v.z * inv * g.z, v.w * inv * g.w);
+  }
+}
+
 // ---- host side -------------------------------------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1179,6 +1215,13 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
   }
   if (lc.launches) *lc.launches += 1;
   if (e != cudaSuccess || pl.splits == 1) return e;
+  if (epi == EPI_RESADD && lc.norm_w && lc.norm_out && M <= 512 && N % 4 == 0) {
+    CK_RET(launch_pdl(tc::splitk_resadd_norm_kernel, dim3(M), dim3(256), 0, lc.stream, p.ws, pl.splits,
+                      pl.m_tiles * tc::BM, N, (float*)out, ldo, lc.norm_w, lc.norm_out, lc.norm_eps));
+    if (lc.launches) *lc.launches += 1;
+    if (lc.norm_done) *lc.norm_done = true;
+    return cudaGetLastError();
+  }
   const int cols = epi == EPI_SWIGLU ? N / 2 : N;
   const size_t work = (size_t)M * cols / 4;
   int blocks = (int)((work + 255) / 256);

@@ -59,6 +59,13 @@ struct LaunchCtx {
   void* tune_out = nullptr;   // GEMM tuning: scratch output for residual-add shapes (fp32)
   size_t tune_floats = 0;
   int variant = GEMM_ANY;     // GEMM: kernel families allowed (GEMM_ANY, GEMM_SINGLE, GEMM_PAIR)
+  // GEMM, residual add with a K split over at most 512 rows: the RMSNorm of the updated rows,
+  // out = bf16(x / sqrt(mean(x^2) + norm_eps) * norm_w), fused into the split-K reduction
+  // (same arithmetic and order as launch_rmsnorm over that many rows, so the same bits).
+  const float* norm_w = nullptr;   // [N] fp32; NULL: no fused norm
+  bf16* norm_out = nullptr;        // [M, N] bf16
+  float norm_eps = 0.f;
+  bool* norm_done = nullptr;       // set to true when the norm was fused (the caller skips its own)
 };
 
 // Tiled TMA descriptor over a global tensor (dims and box innermost first, strides in bytes for

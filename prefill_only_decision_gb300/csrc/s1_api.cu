@@ -136,6 +136,7 @@ struct s1_model {
   float* trace = nullptr;      // layer trace: residual stream after the embedding and each layer
   long long trace_floats = 0;
   bool force_simt = false;     // S1_GEMM=simt in the environment (debugging)
+  bool fuse_norm = true;       // RMSNorm fused into split-K residual reductions (S1_NORM_FUSE=0: off)
   // profiling
   bool prof = false;
   std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> prof_ev;
@@ -428,10 +429,21 @@ bool valid_state(const s1_model* m, const s1_state* st) {
 
 // ---------------------------------------------------------------------------------------
 // GEMM dispatch
-int gemm(s1_model* m, const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo) {
+// For a residual-add GEMM, `norm_w` (may be NULL) is the weight of the RMSNorm that follows it;
+// when the GEMM's split-K reduction also forms that norm (into the normed-activation buffer),
+// *normed is set and the caller launches no norm of its own.
+int gemm(s1_model* m, const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
+         const float* norm_w = nullptr, bool* normed = nullptr) {
   ProfScope ps(m, S1_PROF_GEMM, 2.0 * M * N * K, (double)N * K * 2 + (double)M * K * 2);
+  if (normed) *normed = false;
   if (m->gemm_impl == 0 && !m->force_simt && gemm_tc_supported(M, N, K, epi)) {
     LaunchCtx lc{m->stream, m->d_err, m->num_sms, &m->launches};
+    if (norm_w && normed && m->fuse_norm) {
+      lc.norm_w = norm_w;
+      lc.norm_out = m->sc.xn;
+      lc.norm_eps = m->sh.rms_eps;
+      lc.norm_done = normed;
+    }
     // the projection buffer is free whenever a residual-add GEMM runs (its contents were
     // consumed by the layer's mixer), so it serves as the tuning output of those shapes
     lc.tune = !m->prof;
@@ -472,8 +484,9 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
   }
   if (m->trace) CK(cudaMemcpyAsync(m->trace, sc.x, plane * 4, cudaMemcpyDeviceToDevice, st));
   int li = 0;
+  bool normed = false;   // xn already holds this layer's input norm (formed by the previous reduction)
   for (const Layer& L : m->layers) {
-    {
+    if (!normed) {
       ProfScope ps(m, S1_PROF_NORM, 0, (double)R * d * 6);
       CK(launch_rmsnorm(sc.x, L.attn_norm, sc.xn, R, d, s.rms_eps, st));
       m->launches += 1;
@@ -527,16 +540,18 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
         m->launches += 1;
       }
     }
-    rc = gemm(m, sc.mix, L.w_o, R, d, L.k_o, EPI_RESADD, sc.x, d);
+    rc = gemm(m, sc.mix, L.w_o, R, d, L.k_o, EPI_RESADD, sc.x, d, L.mlp_norm, &normed);
     if (rc) return rc;
-    {
+    if (!normed) {
       ProfScope ps(m, S1_PROF_NORM, 0, (double)R * d * 6);
       CK(launch_rmsnorm(sc.x, L.mlp_norm, sc.xn, R, d, s.rms_eps, st));
       m->launches += 1;
     }
     rc = gemm(m, sc.xn, L.w_gu, R, 2 * F, d, EPI_SWIGLU, sc.h, F);
     if (rc) return rc;
-    rc = gemm(m, sc.h, L.w_down, R, d, F, EPI_RESADD, sc.x, d);
+    // (the last layer's output is normalised by the readout, on the question rows only)
+    const float* next_norm = li + 1 < (int)m->layers.size() ? m->layers[li + 1].attn_norm : nullptr;
+    rc = gemm(m, sc.h, L.w_down, R, d, F, EPI_RESADD, sc.x, d, next_norm, &normed);
     if (rc) return rc;
     ++li;
     if (m->trace) CK(cudaMemcpyAsync(m->trace + (size_t)li * plane, sc.x, plane * 4, cudaMemcpyDeviceToDevice, st));
@@ -786,6 +801,8 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   m->force_simt = gi && strcmp(gi, "simt") == 0;
   const char* gd = getenv("S1_GDN");
   m->gdn_token = gd && strcmp(gd, "token") == 0;
+  const char* nf = getenv("S1_NORM_FUSE");
+  m->fuse_norm = !(nf && strcmp(nf, "0") == 0);
   m->gemm_impl = m->force_simt ? 1 : 0;
   auto bail = [&](int rc) {
     s1_model_destroy(m);

@@ -273,6 +273,33 @@ def test_small_batch_vs_oracle(B):
         m.close()
 
 
+def test_norm_fused_into_splitk_reduction_bitexact(B, monkeypatch):
+    """Decide calls (few rows: residual-add GEMMs split over K) form the following RMSNorm
+    inside the split-K reduction; results are bit-identical to the separate norm launches and
+    the call launches fewer kernels."""
+    cfg = configs.SMALL
+    W = synth.make_weights(cfg)
+    req = synth.make_requests(cfg)[0]
+    out = {}
+    for fuse in ("1", "0"):
+        monkeypatch.setenv("S1_NORM_FUSE", fuse)
+        m = B.Model(W)
+        try:
+            st = m.prefill(req.tokens)
+            m.decide(st, req.questions)              # first use of each GEMM shape
+            n0 = m.counters()["launches"]
+            res = m.decide(st, req.questions)
+            out[fuse] = (res, m.counters()["launches"] - n0)
+        finally:
+            m.close()
+    (a, la), (b, lb) = out["1"], out["0"]
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x["probs"], y["probs"])
+        np.testing.assert_array_equal(x["hidden"], y["hidden"])
+    # every layer's two norms but the first layer's input norm ride on a reduction
+    assert lb - la == 2 * cfg.shape.n_layers - 1, (la, lb)
+
+
 @pytest.mark.slow
 def test_4b_vs_oracle(B):
     cfg = configs.QWEN4B
