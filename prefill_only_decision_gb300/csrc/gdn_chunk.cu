@@ -652,20 +652,25 @@ __global__ void __launch_bounds__(512) chunk_state_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------------------
 // chunk_out: one CTA per (chunk, head), 256 threads (8 warps).
 // O = diag(gamma) Q S_c^T + P U, P = lower_incl(Gamma * Q K^T); out bf16 [R, H*Dv].
-template <int D>
+// chunk_out: one CTA per (chunk, head, value slice), 256 threads. A CTA forms the output
+// columns [vs * D/VS, (vs + 1) * D/VS) of its head; the launcher splits the value columns over
+// VS CTAs when (chunks x heads) alone leaves SMs idle (a few questions over a snapshot). P, q's
+// norm and (for folded chunks) the whole of W are formed or loaded by every slice.
+template <int D, int VS>
 struct OutSmem {
+  static constexpr int DW = D / VS;  // value columns of the slice
   static constexpr int SQ = D + 4;   // Q, K tiles ([t][j], A / B(n-major) pattern)
-  static constexpr int SSC = D + 4;  // chunk-start state ([i][j])
-  static constexpr int SUo = D + 8;  // U tile ([s][i], B k-major pattern)
+  static constexpr int SSC = D + 4;  // chunk-start state rows of the slice ([i][j])
+  static constexpr int SUo = D + 8;  // W tile / U slice ([s][i], B k-major pattern)
   static constexpr int SP = C + 4;   // P ([t][s])
   float Q[C * SQ];
-  float KU[C * SUo];        // K, then U
-  float S[D * SSC];
+  float KU[C * SUo];        // K, then (folded) W, then U
+  float S[DW * SSC];
   float P[C * SP];
   float g[C];
 };
 
-template <int D>
+template <int D, int VS>
 __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict__ proj, int ld,
                                                         const float* __restrict__ gbuf,
                                                         const ChunkDesc* __restrict__ chunks, int H, float eps,
@@ -678,11 +683,11 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
   allow_dependents();
   wait_prerequisites();
   extern __shared__ __align__(16) uint8_t smraw[];
-  using SM = OutSmem<D>;
-  constexpr int SQ = SM::SQ, SSC = SM::SSC, SUo = SM::SUo, SP = SM::SP;
-  constexpr int NTO = D / 16;            // 8-column n-tiles per warp of the output
+  using SM = OutSmem<D, VS>;
+  constexpr int SQ = SM::SQ, SSC = SM::SSC, SUo = SM::SUo, SP = SM::SP, DW = SM::DW;
+  constexpr int NTO = DW / 16;           // 8-column n-tiles per warp of the output
   SM& s = *reinterpret_cast<SM*>(smraw);
-  const int ci = blockIdx.x, h = blockIdx.y;
+  const int ci = blockIdx.x, h = blockIdx.y, cs = blockIdx.z * DW;
   const ChunkDesc cd = chunks[ci];
   const int n = cd.len;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -695,28 +700,34 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
     cp16(&s.Q[r * SQ + c4], proj + (size_t)row * ld + h * D + c4, ok);
     cp16(&s.KU[r * SQ + c4], proj + (size_t)row * ld + HDk + h * D + c4, ok);   // K with the Q stride
   }
-  // folded chunk (a single-chunk sequence without a state pass): its start state is the
-  // snapshot's (or zero), TF32-rounded as the state pass records it
+  // the slice's rows of the chunk-start state. A folded chunk (a single-chunk sequence without
+  // a state pass) starts from the snapshot's state (or zero), TF32-rounded below as the state
+  // pass records it.
   const bool fold = cd.seq >= out_fold;
-  if (!fold) {
-    const float* Sc = Schunk + ((size_t)ci * H + h) * D * D;
-    for (int i = tid; i < D * (D / 4); i += 256) {
-      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-      cp16(&s.S[r * SSC + c4], Sc + (size_t)r * D + c4, true);
+  {
+    const float* S0;
+    if (!fold) {
+      S0 = Schunk + ((size_t)ci * H + h) * D * D;
+    } else {
+      const int cin = seqs[cd.seq].ctx_in;
+      S0 = cin >= 0 ? ctxs[cin].S + (size_t)(layer_g * H + h) * D * D : nullptr;
     }
-  } else {
-    const int cin = seqs[cd.seq].ctx_in;
-    const float* S0 = cin >= 0 ? ctxs[cin].S + (size_t)(layer_g * H + h) * D * D : nullptr;
-    for (int i = tid; i < D * (D / 4); i += 256) {
+    for (int i = tid; i < DW * (D / 4); i += 256) {
       const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
-      const float4 v = S0 ? *reinterpret_cast<const float4*>(S0 + (size_t)r * D + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
-      *reinterpret_cast<float4*>(&s.S[r * SSC + c4]) = make_float4(rnd(v.x), rnd(v.y), rnd(v.z), rnd(v.w));
+      cp16(&s.S[r * SSC + c4], S0 ? S0 + (size_t)(cs + r) * D + c4 : proj, S0 != nullptr);
     }
   }
   if (tid < C) s.g[tid] = tid < n ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
   cp_commit();
   cp_wait<0>();
   __syncthreads();
+  if (fold) {
+    for (int i = tid; i < DW * (D / 4); i += 256) {
+      float4* p = reinterpret_cast<float4*>(&s.S[(i / (D / 4)) * SSC + (i % (D / 4)) * 4]);
+      const float4 v = *p;
+      *p = make_float4(rnd(v.x), rnd(v.y), rnd(v.z), rnd(v.w));
+    }
+  }
   // q <- q / sqrt(sum q^2 + eps), rounded to TF32 (as k is in chunk_prep); four threads per row
   {
     constexpr int PER = D / 4;
@@ -767,10 +778,11 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
     }
   }
   __syncthreads();
+  // warp -> rows r0.., value columns cb .. cb + DW/2 of the slice (NTO n-tiles)
+  const int cb = (warp >> 2) * (DW / 2);
   if (fold) {
     // U = Ut - W S^T here, with the state pass's TF32 operands (two accumulation chains per
-    // output), then rounded to TF32. W -> KU (A-operand stride); warp -> rows r0.., value
-    // columns (D/2)*(warp>>2) ..; Ut straight into registers.
+    // output), then rounded to TF32. W (all D key columns) -> KU; Ut straight into registers.
     for (int i = tid; i < C * (D / 4); i += 256) {
       const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
       const bool ok = r < n;
@@ -778,11 +790,10 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
       cp16(&s.KU[r * SUo + c4], Wbuf + ((size_t)row * H + h) * D + c4, ok);
     }
     cp_commit();
-    const int cb = (warp >> 2) * (D / 2);
     float ut[NTO][4];
 #pragma unroll
     for (int nt = 0; nt < NTO; ++nt) {
-      const int c = cb + nt * 8 + 2 * tq;
+      const int c = cs + cb + nt * 8 + 2 * tq;
       const int ra = r0 + gq, rb = r0 + gq + 8;
       const float2 x = ra < n ? *reinterpret_cast<const float2*>(Ubuf + ((size_t)(cd.row0 + ra) * H + h) * D + c)
                               : make_float2(0.f, 0.f);
@@ -819,25 +830,24 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
       s.KU[rb * SUo + c + 1] = rb < n ? rnd(ut[nt][3] - (u0[nt][3] + u1[nt][3])) : 0.f;
     }
   } else {
-    // U tile over K (k-major stride)
-    for (int i = tid; i < C * (D / 4); i += 256) {
-      const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
+    // the slice of the U tile written by the state pass (k-major stride)
+    for (int i = tid; i < C * (DW / 4); i += 256) {
+      const int r = i / (DW / 4), c4 = (i % (DW / 4)) * 4;
       const bool ok = r < n;
       const int row = cd.row0 + (ok ? r : 0);
-      cp16(&s.KU[r * SUo + c4], Ubuf + ((size_t)row * H + h) * D + c4, ok);
+      cp16(&s.KU[r * SUo + c4], Ubuf + ((size_t)row * H + h) * D + cs + c4, ok);
     }
   }
   cp_commit();
-  // O1 = Q S_c^T  (warp -> rows r0.., value columns (D/2)*(warp>>2) .. : NTO n-tiles)
+  // O1 = Q S_c^T over the slice's value columns
   float o[NTO][4] = {};
-  const int cbase = (warp >> 2) * (D / 2);
 #pragma unroll 2
   for (int k = 0; k < D; k += 8) {
     const uint32_t a0 = raw(s.Q[(r0 + gq) * SQ + k + tq]), a1 = raw(s.Q[(r0 + gq + 8) * SQ + k + tq]);
     const uint32_t a2 = raw(s.Q[(r0 + gq) * SQ + k + tq + 4]), a3 = raw(s.Q[(r0 + gq + 8) * SQ + k + tq + 4]);
 #pragma unroll
     for (int nt = 0; nt < NTO; ++nt) {
-      const int i = cbase + nt * 8 + gq;
+      const int i = cb + nt * 8 + gq;
       const uint32_t b0 = raw(s.S[i * SSC + k + tq]), b1 = raw(s.S[i * SSC + k + tq + 4]);
       mma_tf32(o[nt], a0, a1, a2, a3, b0, b1);
     }
@@ -856,7 +866,7 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
     const uint32_t a2 = raw(s.P[(r0 + gq) * SP + k + tq + 4]), a3 = raw(s.P[(r0 + gq + 8) * SP + k + tq + 4]);
 #pragma unroll
     for (int nt = 0; nt < NTO; ++nt) {
-      const int i = cbase + nt * 8 + gq;
+      const int i = cb + nt * 8 + gq;
       const uint32_t b0 = raw(s.KU[(k + tq) * SUo + i]), b1 = raw(s.KU[(k + tq + 4) * SUo + i]);
       mma_tf32(o[nt], a0, a1, a2, a3, b0, b1);
     }
@@ -864,7 +874,7 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
   const int HDv = H * D;
 #pragma unroll
   for (int nt = 0; nt < NTO; ++nt) {
-    const int c = cbase + nt * 8 + 2 * tq;
+    const int c = cs + cb + nt * 8 + 2 * tq;
     const int ta = r0 + gq, tb = r0 + gq + 8;
     if (ta < n)
       *reinterpret_cast<__nv_bfloat162*>(out + (size_t)(cd.row0 + ta) * HDv + h * D + c) =
@@ -906,10 +916,9 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, flo
                                     const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                     const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
                                     float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                                    int fold_from, int out_fold, int* d_err, cudaStream_t st) {
+                                    int fold_from, int out_fold, int* d_err, int num_sms, cudaStream_t st) {
   static bool attr = false;
   const size_t sp = sizeof(gc::PrepSmem<D>);
-  const size_t so = sizeof(gc::OutSmem<D>);
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(gc::chunk_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (e == cudaSuccess)
@@ -919,7 +928,14 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, flo
       e = cudaFuncSetAttribute(gc::chunk_state_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)state_smem<D, 2>());
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gc::chunk_out_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)so);
+      e = cudaFuncSetAttribute(gc::chunk_out_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sizeof(gc::OutSmem<D, 1>));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gc::chunk_out_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sizeof(gc::OutSmem<D, 2>));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gc::chunk_out_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sizeof(gc::OutSmem<D, 4>));
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -959,8 +975,23 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, flo
                         max_chunks_rest, d_err, st);
     if (e != cudaSuccess) return e;
   }
-  CK_RET(launch_pdl(gc::chunk_out_kernel<D>, dim3(n_chunks, H), dim3(256), so, st, proj, ld, loga, d_chunks, H, eps,
-                    Wbuf, Ubuf, Schunk, d_seq, d_ctx, layer_g, out_fold, out));
+  // value columns split over 2 or 4 CTAs while (chunks x heads) CTAs leave SMs idle
+  int vs = 1;
+  while (vs < 4 && (long)n_chunks * H * vs < num_sms) vs *= 2;
+  switch (vs) {
+    case 1:
+      CK_RET(launch_pdl(gc::chunk_out_kernel<D, 1>, dim3(n_chunks, H, 1), dim3(256), sizeof(gc::OutSmem<D, 1>), st,
+                        proj, ld, loga, d_chunks, H, eps, Wbuf, Ubuf, Schunk, d_seq, d_ctx, layer_g, out_fold, out));
+      break;
+    case 2:
+      CK_RET(launch_pdl(gc::chunk_out_kernel<D, 2>, dim3(n_chunks, H, 2), dim3(256), sizeof(gc::OutSmem<D, 2>), st,
+                        proj, ld, loga, d_chunks, H, eps, Wbuf, Ubuf, Schunk, d_seq, d_ctx, layer_g, out_fold, out));
+      break;
+    default:
+      CK_RET(launch_pdl(gc::chunk_out_kernel<D, 4>, dim3(n_chunks, H, 4), dim3(256), sizeof(gc::OutSmem<D, 4>), st,
+                        proj, ld, loga, d_chunks, H, eps, Wbuf, Ubuf, Schunk, d_seq, d_ctx, layer_g, out_fold, out));
+      break;
+  }
   return cudaGetLastError();
 }
 
@@ -968,17 +999,18 @@ cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float ep
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                               int fold_from, int out_fold, int* d_err, cudaStream_t st, long* launches) {
+                               int fold_from, int out_fold, int* d_err, int num_sms, cudaStream_t st,
+                               long* launches) {
   if (n_seq <= 0 || n_chunks <= 0) return cudaSuccess;
   if (!gdn_chunked_supported(H, Dk, Dv, ld)) return cudaErrorNotSupported;
   if (n_seq > 65535 || n_chunks > 2147483647 / 2) return cudaErrorInvalidValue;
   cudaError_t e = (Dk == 128)
                       ? launch_chunked_d<128>(proj, ld, R, loga, eps, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                               layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
-                                              max_chunks_rest, fold_from, out_fold, d_err, st)
+                                              max_chunks_rest, fold_from, out_fold, d_err, num_sms, st)
                       : launch_chunked_d<64>(proj, ld, R, loga, eps, out, d_seq, n_seq, d_chunks, n_chunks, d_ctx,
                                              layer_g, H, Wbuf, Ubuf, Schunk, n_first, max_chunks_first,
-                                             max_chunks_rest, fold_from, out_fold, d_err, st);
+                                             max_chunks_rest, fold_from, out_fold, d_err, num_sms, st);
   if (launches) {
     const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
     *launches += 2 + (std::min(split, std::min(fold_from, out_fold)) > 0 ? 1 : 0) +

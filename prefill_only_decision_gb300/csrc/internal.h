@@ -96,7 +96,8 @@ cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float l2
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                               int fold_from, int out_fold, int* d_err, cudaStream_t st, long* launches);
+                               int fold_from, int out_fold, int* d_err, int num_sms, cudaStream_t st,
+                               long* launches);
 cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab, const int* row_seq,
                               const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, bf16* q,
                               bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,

@@ -113,6 +113,9 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int
 // ---- RoPE (rotate-half over the whole head) + split of the fused q|k|v projection -------
 // proj row r: [q (Hq*hd) | k (Hkv*hd) | v (Hkv*hd)] fp32. Writes q, k_new, v_new (bf16) at
 // packed row r and, for sequences that own a snapshot, K/V into its cache at row = position.
+// Grid (row, item block): one thread per item, items = the (Hq + Hkv) * hd/2 rotated pairs of
+// q and k, then the Hkv * hd values of v (one round trip to memory per thread, so that a few
+// rows still spread over the whole GPU).
 __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const float2* __restrict__ tab,
                                   const int* __restrict__ row_seq, const SeqDesc* __restrict__ seqs,
                                   const CtxDesc* __restrict__ ctxs, int layer_f, bf16* __restrict__ q,
@@ -121,11 +124,13 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
   allow_dependents();
   wait_prerequisites();
   const int r = blockIdx.x;
+  const int half = hd / 2;
+  const int nq = Hq * half, nk = Hkv * half;
+  const int t = blockIdx.y * blockDim.x + threadIdx.x;
+  if (t >= nq + nk + Hkv * hd) return;
+  const float* pr = proj + (size_t)r * ld;
   const SeqDesc sd = seqs[row_seq[r]];
   const int pos = sd.pos0 + (r - sd.row0);
-  const int half = hd / 2;
-  const float* pr = proj + (size_t)r * ld;
-  const float2* tr = tab + (size_t)pos * half;
   bf16* kc = nullptr;
   bf16* vc = nullptr;
   if (sd.ctx_out >= 0) {
@@ -134,14 +139,13 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
     kc = c.KV + (size_t)layer_f * 2 * plane + (size_t)pos * Hkv * hd;
     vc = kc + plane;
   }
-  const int nq = Hq * half, nk = Hkv * half;
-  for (int t = threadIdx.x; t < nq + nk; t += blockDim.x) {
+  if (t < nq + nk) {
     const bool isq = t < nq;
     const int tt = isq ? t : t - nq;
     const int h = tt / half, i = tt % half;
     const float* src = pr + (isq ? 0 : Hq * hd) + h * hd;
     const float x1 = src[i], x2 = src[i + half];
-    const float2 cs = tr[i];
+    const float2 cs = tab[(size_t)pos * half + i];
     const bf16 y1 = f2bf(x1 * cs.x - x2 * cs.y);
     const bf16 y2 = f2bf(x2 * cs.x + x1 * cs.y);
     if (isq) {
@@ -152,12 +156,11 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
       knew[(size_t)r * Hkv * hd + h * hd + i + half] = y2;
       if (kc) { kc[h * hd + i] = y1; kc[h * hd + i + half] = y2; }
     }
-  }
-  const float* vs = pr + (Hq + Hkv) * hd;
-  for (int t = threadIdx.x; t < Hkv * hd; t += blockDim.x) {
-    const bf16 v = f2bf(vs[t]);
-    vnew[(size_t)r * Hkv * hd + t] = v;
-    if (vc) vc[t] = v;
+  } else {
+    const int tv = t - (nq + nk);
+    const bf16 v = f2bf(pr[(Hq + Hkv) * hd + tv]);
+    vnew[(size_t)r * Hkv * hd + tv] = v;
+    if (vc) vc[tv] = v;
   }
 }
 
@@ -166,7 +169,10 @@ cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab,
                               bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,
                               cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
-  CK_RET(launch_pdl(rope_split_kernel, dim3(R), dim3(256), 0, st, proj, ld, rope_tab, row_seq, d_seq, d_ctx, layer_f,
+  const int items = (Hq + Hkv) * (hd / 2) + Hkv * hd;
+  const dim3 grid(R, (items + 255) / 256);
+  if (grid.y > 65535) return cudaErrorInvalidValue;
+  CK_RET(launch_pdl(rope_split_kernel, grid, dim3(256), 0, st, proj, ld, rope_tab, row_seq, d_seq, d_ctx, layer_f,
                     q, knew, vnew, Hq, Hkv, hd));
   return cudaGetLastError();
 }

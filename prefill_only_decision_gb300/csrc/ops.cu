@@ -110,8 +110,11 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
     OCK(cudaMemsetAsync(err, 0, 256, st));
     int maxc = 0;
     for (int q = 0; q < n_seq; ++q) maxc = std::max(maxc, (len[q] + GDN_CHUNK - 1) / GDN_CHUNK);
+    int dev = 0, sms = 0;
+    OCK(cudaGetDevice(&dev));
+    OCK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     OCK(launch_gdn_chunked(proj, ld, R, loga, l2_eps, (bf16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
-                           0, maxc, maxc, n_seq, n_seq, err, st, nullptr));
+                           0, maxc, maxc, n_seq, n_seq, err, sms, st, nullptr));
     int herr = 0;
     OCK(cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
     OCK(cudaStreamSynchronize(st));

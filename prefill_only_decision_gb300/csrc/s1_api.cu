@@ -511,8 +511,8 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
           }
           CK(launch_gdn_chunked(sc.proj, L.n_in, R, sc.loga, s.l2_eps, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
                                 mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first,
-                                mt.max_chunks_first, mt.max_chunks_rest, mt.fold_from, mt.out_fold, m->d_err, st,
-                                &m->launches));
+                                mt.max_chunks_first, mt.max_chunks_rest, mt.fold_from, mt.out_fold, m->d_err,
+                                m->num_sms, st, &m->launches));
         } else {
           CK(launch_gdn_prep(sc.proj, L.n_in, sc.loga, sc.beta, R, H, s.la_dk, s.la_dv, s.l2_eps, st));
           m->launches += 1;

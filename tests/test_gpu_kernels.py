@@ -156,8 +156,11 @@ def _gdn_inputs(R, H, D, seed):
     return proj
 
 
+# (chunks x heads) picks how many CTAs share a head's value columns in the output kernel: 4 below
+# about half the SM count, 2 below the SM count (16 heads x 5 chunks), else 1 (16 x 10)
 @pytest.mark.parametrize("H,D,lens,with_s0", [(2, 64, [1, 63, 64, 65], False), (4, 128, [130], True),
-                                              (16, 128, [48, 48, 48], True), (3, 128, [200, 7], False)])
+                                              (16, 128, [48, 48, 48], True), (3, 128, [200, 7], False),
+                                              (16, 128, [320], True), (16, 64, [640], False)])
 def test_gdn_scan(B, H, D, lens, with_s0):
     R = int(sum(lens))
     proj = _gdn_inputs(R, H, D, R + H)
