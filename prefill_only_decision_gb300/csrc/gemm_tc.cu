@@ -795,11 +795,11 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
   }
 }
 
-// Split-K reduction of a residual-add GEMM with the RMSNorm that follows it: one block per
-// row sums the partials in split order, adds them to the residual row and writes it back, then
-// writes the row normalised. Per element and per thread the sums run in the same order as
+// Split-K reduction of a residual-add GEMM with the RMSNorm that follows it: one block of
+// norm_row_threads(N) threads per row sums the partials in split order, adds them to the
+// residual row and writes it back, then writes the row normalised. Per element and per thread the sums run in the same order as
 // splitk_reduce_kernel followed by the block-per-row RMSNorm, so the results are the same bits.
-__global__ void __launch_bounds__(256) splitk_resadd_norm_kernel(const float* __restrict__ ws, int splits, int Mpad,
+__global__ void __launch_bounds__(1024) splitk_resadd_norm_kernel(const float* __restrict__ ws, int splits, int Mpad,
                                                                  int N, float* __restrict__ x, int ldx,
                                                                  const float* __restrict__ w, bf16* __restrict__ xn,
                                                                  float eps) {
@@ -1216,7 +1216,7 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
   if (lc.launches) *lc.launches += 1;
   if (e != cudaSuccess || pl.splits == 1) return e;
   if (epi == EPI_RESADD && lc.norm_w && lc.norm_out && M <= 512 && N % 4 == 0) {
-    CK_RET(launch_pdl(tc::splitk_resadd_norm_kernel, dim3(M), dim3(256), 0, lc.stream, p.ws, pl.splits,
+    CK_RET(launch_pdl(tc::splitk_resadd_norm_kernel, dim3(M), dim3(norm_row_threads(N)), 0, lc.stream, p.ws, pl.splits,
                       pl.m_tiles * tc::BM, N, (float*)out, ldo, lc.norm_w, lc.norm_out, lc.norm_eps));
     if (lc.launches) *lc.launches += 1;
     if (lc.norm_done) *lc.norm_done = true;

@@ -68,6 +68,14 @@ struct LaunchCtx {
   bool* norm_done = nullptr;       // set to true when the norm was fused (the caller skips its own)
 };
 
+// Threads of a block that normalises one row of width d (one float4 per thread and pass): the
+// block-per-row RMSNorm and the split-K reduction that fuses it use the same count, so that
+// their sums run in the same order.
+inline int norm_row_threads(int d) {
+  const int t = ((d / 4 + 31) / 32) * 32;
+  return t < 32 ? 32 : (t > 1024 ? 1024 : t);
+}
+
 // Tiled TMA descriptor over a global tensor (dims and box innermost first, strides in bytes for
 // dims 1..rank-1), encoded through the driver entry point and cached by its arguments.
 // Returns false if the driver entry point is missing or rejects the arguments.

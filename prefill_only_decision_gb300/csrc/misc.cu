@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restri
   }
 }
 
-// General width (d % 4 == 0): one block per row, two passes.
+// General width (d % 4 == 0): one block of norm_row_threads(d) threads per row, two passes.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                bf16* __restrict__ out, int d, float eps) {
   allow_dependents();
@@ -97,7 +97,7 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int
   const int blocks = (R + 7) / 8;
   // few rows (questions over a snapshot): a block per row spreads them over more SMs
   if (R <= 512 && d % 4 == 0) {
-    CK_RET(launch_pdl(rmsnorm_kernel, dim3(R), dim3(256), 0, st, x, w, out, d, eps));
+    CK_RET(launch_pdl(rmsnorm_kernel, dim3(R), dim3(norm_row_threads(d)), 0, st, x, w, out, d, eps));
     return cudaGetLastError();
   }
   switch (d) {
@@ -105,7 +105,7 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int
     case 1024: CK_RET(launch_pdl(rmsnorm_warp_kernel<8>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;
     case 2560: CK_RET(launch_pdl(rmsnorm_warp_kernel<20>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;
     case 5120: CK_RET(launch_pdl(rmsnorm_warp_kernel<40>, dim3(blocks), dim3(256), 0, st, x, w, out, R, d, eps)); break;
-    default: CK_RET(launch_pdl(rmsnorm_kernel, dim3(R), dim3(256), 0, st, x, w, out, d, eps)); break;
+    default: CK_RET(launch_pdl(rmsnorm_kernel, dim3(R), dim3(norm_row_threads(d)), 0, st, x, w, out, d, eps)); break;
   }
   return cudaGetLastError();
 }
