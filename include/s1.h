@@ -218,7 +218,8 @@ int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, 
  * read and written through the same device buffers at replay time, so their contents may change
  * between calls while their addresses and sizes may not. Graphs are not used on the legacy
  * default stream, while profiling or a layer trace is on. A graph is dropped when the model's
- * scratch buffers grow, and all are dropped by s1_set_graphs(m, 0) and s1_model_destroy.
+ * scratch buffers grow, and all are dropped by s1_set_graphs(m, 0) and s1_model_destroy. At
+ * most 64 graphs are kept per model; further signatures run without one.
  * Synchronises the model's stream. Errors: INVALID_HANDLE. */
 int s1_set_graphs(struct s1_model* m, int enable);
 int s1_sync(s1_model* m);   /* waits for the stream; reports device-side timeouts */

@@ -147,13 +147,16 @@ struct s1_model {
   long prof_count[S1_PROF_NCLASS] = {0};
   long launches = 0;           // kernels launched by forward passes
   long long h2d_bytes = 0, d2h_bytes = 0;
-  // CUDA graphs of the stream-ordered one-sweep call (s1_set_graphs): keyed by the call's
-  // argument signature; a graph owns its metadata buffer and bakes in the scratch addresses
+  // CUDA graphs of the stream-ordered calls (s1_set_graphs): keyed by the call's argument
+  // signature; a graph owns its metadata buffer and bakes in the scratch addresses. Both sets
+  // are bounded (kMaxGraphs captured graphs; the seen-once set is cleared at kMaxSeen entries),
+  // so callers whose signatures never repeat cost no memory growth.
   struct Graph {
     cudaGraphExec_t exec = nullptr;
     void* meta = nullptr;
     long launches = 0;
   };
+  static constexpr size_t kMaxGraphs = 64, kMaxSeen = 4096;
   bool graphs = false;
   std::map<std::string, Graph> graph_cache;
   std::set<std::string> graph_seen;
@@ -1065,6 +1068,8 @@ static int graph_call(s1_model* m, const CallKey& key, Run&& run, Replayed&& rep
     replayed();
     return S1_OK;
   }
+  if (m->graph_cache.size() >= s1_model::kMaxGraphs) return run(nullptr);
+  if (m->graph_seen.size() >= s1_model::kMaxSeen) m->graph_seen.clear();
   if (m->graph_seen.insert(key.s).second) return run(nullptr);
   s1_model::Graph g;
   const int rc = run(&g);
