@@ -262,9 +262,16 @@ def test_small_batch_vs_oracle(B):
         gpu = m.decide_batch(states, [r.questions for r in reqs])
         o = om.Oracle(W, np.float32)
         o16 = om.Oracle(W, np.float32, precision="bf16")
+        refs = {}
         for i in (0, 5, 15):
-            compare(gpu[i], o.decide(reqs[i], branched=True), reqs[i].questions, f"small req {i} fp32")
-            compare(gpu[i], o16.decide(reqs[i], branched=True), reqs[i].questions, f"small req {i} bf16")
+            refs[i] = (o.decide(reqs[i], branched=True), o16.decide(reqs[i], branched=True))
+            compare(gpu[i], refs[i][0], reqs[i].questions, f"small req {i} fp32")
+            compare(gpu[i], refs[i][1], reqs[i].questions, f"small req {i} bf16")
+        # three requests (12 single-chunk questions x 8 heads: each head's value columns are
+        # split over 2 CTAs in the output kernel)
+        three = m.decide_batch(states[:3], [r.questions for r in reqs[:3]])
+        compare(three[0], refs[0][0], reqs[0].questions, "small 3-request batch fp32")
+        compare(three[0], refs[0][1], reqs[0].questions, "small 3-request batch bf16")
         # batched and one-at-a-time calls agree
         one = m.decide(m.prefill(reqs[5].tokens), reqs[5].questions)
         for a, b in zip(one, gpu[5]):
