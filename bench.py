@@ -414,12 +414,15 @@ def main():
     achieved = g["flops"] / (g["ms"] / 1000.0) / 1e12 if g["ms"] > 0 else 0.0
     peak = peaks["bf16_tflops_sustained"]
     total_prof_ms = sum(v["ms"] for v in prof.values())
-    # DRAM bytes per GEMM launch from the committed per-shape ncu capture of the 4B step's five
-    # projection shapes (profiles/gemm_tc_4b_shapes.md), weighted by their launches per step
-    traffic = 62.0e6 if (cfg.name == "4b" and args.path == "fused") else None
+    # DRAM bytes per GEMM launch: the committed per-shape ncu capture of the 4B step's five
+    # projection shapes (profiles/gemm_tc_4b_shapes.md: 62.0 MB per launch, equal to the
+    # algorithmic bytes) predates the current tile set (widths 176/208, CTA pairs), so no
+    # counter figure is claimed for the kernels that run now
+    traffic = None
     roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05, all projections)", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": traffic,
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
+                "traffic_note": "last capture (earlier tile set): 62.0e6 bytes per launch = algorithmic bytes",
                 "peak_source": f"{peaks['source']} bf16 sustained",
                 "share_of_step": g["ms"] / total_prof_ms if total_prof_ms else None,
                 "launches_per_step": g["count"] / max(1, args.steps),
