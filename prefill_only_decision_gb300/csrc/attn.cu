@@ -21,7 +21,7 @@ namespace s1 {
 
 namespace fa {
 
-constexpr int BQ = 64, BKV = 64, NWARP = 4;
+constexpr int BQ = 64, BKV = 64;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(512) chunk_state_kernel(const __grid_constant_
                                                           int* __restrict__ d_err) {
   allow_dependents();
   wait_prerequisites();
-  extern __shared__ __align__(1024) uint8_t smraw[];
+  extern __shared__ __align__(16) uint8_t smraw[];   // (rounded up to 1024 bytes below)
   using SM = StateSmem<D, NS>;
   constexpr int SS = SM::SS, SU = SM::SU, SUT = SM::SUT, NB = SM::NB;
   constexpr int NTH = 512;               // 16 warps
