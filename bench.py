@@ -29,6 +29,22 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The reference arm (the oracle on the host cores) runs on rank 0 alone: its BLAS gets every
+# core the process may use, also under torchrun (which sets OMP_NUM_THREADS=1 for its ranks).
+# Set before numpy is imported, which reads these once.
+def _impl_arg(argv):
+    for i, a in enumerate(argv):
+        if a == "--impl" and i + 1 < len(argv):
+            return argv[i + 1]
+        if a.startswith("--impl="):
+            return a.split("=", 1)[1]
+    return None
+
+
+if _impl_arg(sys.argv) == "reference":
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = str(len(os.sched_getaffinity(0)))
+
 import numpy as np  # noqa: E402
 
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
