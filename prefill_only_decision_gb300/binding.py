@@ -99,6 +99,7 @@ def lib():
         "s1_set_graphs": (C.c_int, [vp, C.c_int]),
         "s1_counters": (C.c_int, [vp, P(C.c_longlong), P(C.c_longlong), P(C.c_longlong)]),
         "s1_split_prefix": (C.c_int, [P(P(i32)), P(i32), i32, i32, i32, P(i32)]),
+        "s1_gemm_plan": (C.c_int, [i32, i32, i32, i32, i32, i32, P(i32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -424,6 +425,13 @@ def op_attention(q: int, k_new: int, v_new: int, kv_cache: int, P: int, row0, le
     check(lib().s1_op_attention(C.c_void_p(q), C.c_void_p(k_new), C.c_void_p(v_new),
                                 C.c_void_p(kv_cache) if kv_cache else None, P, len(r0), _iptr(r0), _iptr(ln),
                                 Hq, Hkv, hd, C.c_void_p(out), C.c_void_p(stream) if stream else None))
+
+
+def gemm_plan(M: int, N: int, K: int, epi: int, num_sms: int, pair: bool = False) -> dict:
+    """The planner's heuristic GEMM plan (s1_gemm_plan; host logic, no GPU needed)."""
+    out = (C.c_int32 * 7)()
+    check(lib().s1_gemm_plan(M, N, K, epi, num_sms, 1 if pair else 0, out))
+    return dict(zip(("bn", "cm", "pair", "splits", "kbp", "m_tiles", "n_tiles"), list(out)))
 
 
 def op_rmsnorm(x: int, w: int, R: int, d: int, eps: float, out: int, stream: int = 0):

@@ -1448,3 +1448,20 @@ extern "C" int s1_op_gemm_noalloc(const void* X, const void* W, int32_t M, int32
   if (h) return set_error(S1_ERR_DEVICE_TIMEOUT, "gemm_noalloc: a bounded device wait gave up");
   return S1_OK;
 }
+
+extern "C" int s1_gemm_plan(int32_t M, int32_t N, int32_t K, int32_t epi, int32_t num_sms, int32_t pair,
+                            int32_t* out) {
+  using namespace s1;
+  if (!out || M < 1 || N < 32 || N % 32 || K < 64 || K % 64 || epi < 0 || epi > 3 || num_sms < 1)
+    return set_error(S1_ERR_INVALID_ARG, "gemm_plan: bad sizes, epilogue, SM count or NULL output");
+  const tc::Plan pl = pair ? tc::plan_pair_for(M, N, K, epi, num_sms)
+                           : tc::plan_for(M, N, K, epi, num_sms, gemm_tc_workspace_floats(M, N, K, epi, num_sms));
+  out[0] = pl.bn;
+  out[1] = pl.cm;
+  out[2] = pl.pair;
+  out[3] = pl.splits;
+  out[4] = pl.kb_per_split;
+  out[5] = pl.m_tiles;
+  out[6] = pl.n_tiles;
+  return S1_OK;
+}
