@@ -22,7 +22,11 @@ What is computed (sources by page and section):
 Readings where the pages are silent (each is listed in the design notes):
   pre-norm residual blocks; RMSNorm eps 1e-6 with weights as given; L2 norm
   x / sqrt(sum x^2 + 1e-6); a_t and b_t are per-head scalar projections
-  w_a x, w_b x; no 1/sqrt(dk) on q in the delta rule; rotate-half RoPE over the
+  w_a x, w_b x; no 1/sqrt(dk) on q in the delta rule; the optional short
+  convolution (shape.conv_width > 0; the RFC's "convolution history" of the
+  snapshot, section 5, width not given) is depthwise and causal over the
+  q|k|v projections, followed by SiLU, before the L2 norms, with the last
+  width-1 input rows as the continuation history; rotate-half RoPE over the
   whole head dimension with inv_freq_i = theta^(-2i/hd); plain 1-D positions,
   the suffix continuing at P; readout row = last suffix token; noul option
   ids are [yes, no]; argmax ties go to the lowest index.
@@ -91,6 +95,24 @@ def rope(x, pos, theta):
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
+def causal_conv(x, w, hist):
+    """Depthwise causal convolution over rows, continuing from `hist`.
+
+    x: [T, C] input rows; w: [C, W] per-channel taps, tap j weighting the row W-1-j steps
+    back (tap W-1 is the current row); hist: [W-1, C] the inputs before x (zeros at the
+    start of a sequence). Returns y [T, C] with y_t = sum_j w[:, j] * x_{t-(W-1)+j}, and the
+    history after x (its last W-1 input rows, reaching into hist when T < W-1).
+    """
+    W = w.shape[1]
+    xx = np.concatenate([hist, x], axis=0)
+    T = x.shape[0]
+    y = np.zeros_like(x)
+    for j in range(W):
+        y += w[:, j][None, :] * xx[j:j + T]
+    new_hist = xx[xx.shape[0] - (W - 1):] if W > 1 else xx[:0]
+    return y, new_hist.copy()
+
+
 def attention(q, k, v, q_pos, k_pos):
     """Causal GQA attention by brute force.
 
@@ -118,6 +140,7 @@ def attention(q, k, v, q_pos, k_pos):
 class LayerCache:
     """Complete continuation state of one layer after a prefix."""
     S: Optional[np.ndarray] = None        # gated delta rule: [H, Dv, Dk]
+    conv: Optional[np.ndarray] = None     # short convolution history: last w-1 input rows [w-1, C]
     K: Optional[np.ndarray] = None        # attention: post-RoPE keys [P, Hkv, hd]
     V: Optional[np.ndarray] = None
     pos: Optional[np.ndarray] = None      # key positions [P]
@@ -181,9 +204,23 @@ class Oracle:
         s = self.s
         T = xn.shape[0]
         H, Dk, Dv = s.la_heads, s.la_dk, s.la_dv
-        q = self.linear(xn, l, "q").reshape(T, H, Dk)
-        k = self.linear(xn, l, "k").reshape(T, H, Dk)
-        v = self.linear(xn, l, "v").reshape(T, H, Dv)
+        q = self.linear(xn, l, "q")
+        k = self.linear(xn, l, "k")
+        v = self.linear(xn, l, "v")
+        conv_hist = None
+        if s.conv_width > 0:
+            # short causal convolution over the q|k|v projections, then SiLU (before the
+            # L2 norms); its history continues the prefix like the recurrent state does
+            qkv = np.concatenate([q, k, v], axis=1)
+            Wc = self._w(l, 11)
+            hist = cache.conv if cache is not None and cache.conv is not None else \
+                np.zeros((s.conv_width - 1, qkv.shape[1]), dtype=self.dt)
+            y, conv_hist = causal_conv(qkv, Wc, hist)
+            y = silu(y)
+            q, k, v = y[:, :H * Dk], y[:, H * Dk:2 * H * Dk], y[:, 2 * H * Dk:]
+        q = q.reshape(T, H, Dk)
+        k = k.reshape(T, H, Dk)
+        v = v.reshape(T, H, Dv)
         xa = round_bf16(xn).astype(self.dt) if self.bf16 else xn
         a = xa @ self._w(l, 4).T
         b = xa @ self._w(l, 5).T
@@ -193,7 +230,7 @@ class Oracle:
         S0 = cache.S if cache is not None else np.zeros((H, Dv, Dk), dtype=self.dt)
         o, S = gdn.recurrent(q, k, v, alpha, beta, S0)
         y = self.linear(o.reshape(T, H * Dv), l, "o")
-        return y, LayerCache(S=S)
+        return y, LayerCache(S=S, conv=conv_hist)
 
     def attn_layer(self, l, xn, pos, cache: Optional[LayerCache]):
         s = self.s

@@ -139,6 +139,8 @@ class Model:
     def __init__(self, weights, max_rows: int = 0, stream: Optional[int] = None):
         L = lib()
         sh = weights.shape
+        if getattr(sh, "conv_width", 0):
+            raise S1Error(S1_ERR_UNSUPPORTED, "the gated delta-rule short convolution is not in the CUDA path")
         self.shape = sh
         full = np.asarray(sh.layer_is_full, dtype=np.uint8)
         self._full = full

@@ -33,6 +33,9 @@ class ModelShape:
     lora_rank: int = 0
     lora_alpha: float = 0.0
     bf16_weights: bool = True
+    # short causal convolution over each gated delta-rule layer's q|k|v projections (0: none).
+    # Oracle only for now: the CUDA path refuses models that set it.
+    conv_width: int = 0
 
     @property
     def layer_is_full(self) -> List[int]:
@@ -49,6 +52,7 @@ class ModelShape:
             else:
                 H, dk, dv = self.la_heads, self.la_dk, self.la_dv
                 tot += (2 * H * dk + H * dv + 2 * H) * d + d * H * dv
+                tot += (2 * H * dk + H * dv) * self.conv_width
             tot += 3 * F * d
         if with_embed:
             tot += self.vocab * d + d

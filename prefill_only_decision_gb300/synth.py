@@ -16,6 +16,10 @@ Recipe
     option ids are distinct within a question.
   * given prefix embedding rows (image-patch stand-ins): normal(0, 1), bf16,
     from SeedSequence([s, 2000000 + request]).
+  * models with a short convolution (conv_width > 0): its depthwise weights
+    [channels, width], normal(0, 0.3) (about the spread of a default
+    1-D convolution initialisation at width 4), are the last tensor of each
+    gated delta-rule layer.
 """
 from __future__ import annotations
 
@@ -58,6 +62,8 @@ def layer_tensor_shapes(shape: ModelShape, full: bool):
         out += [("w_q", (H * dk, d)), ("w_k", (H * dk, d)), ("w_v", (H * dv, d)),
                 ("w_a", (H, d)), ("w_b", (H, d)), ("w_o", (d, H * dv))]
     out += [("mlp_norm", (d,)), ("w_gate", (F, d)), ("w_up", (F, d)), ("w_down", (d, F))]
+    if not full and shape.conv_width > 0:
+        out += [("conv", (2 * shape.la_heads * shape.la_dk + shape.la_heads * shape.la_dv, shape.conv_width))]
     return out
 
 
@@ -106,6 +112,8 @@ def make_weights(cfg: Config, threads: Optional[int] = None) -> Weights:
             idx = 2 + l * 64 + t
             if name.endswith("norm"):
                 jobs.append((("layer", l, t), (lambda shp=shp: _ones(shp, bf16))))
+            elif name == "conv":
+                jobs.append((("layer", l, t), (lambda shp=shp, idx=idx: _normal(seed, idx, shp, 0.3, bf16))))
             else:
                 jobs.append((("layer", l, t), (lambda shp=shp, idx=idx: _normal(seed, idx, shp, 0.02, bf16))))
         if shape.lora_rank > 0:

@@ -96,3 +96,15 @@ def test_ops_argument_validation(L):
     assert L.s1_op_gemm(None, None, 4, 30, 64, 0, None, 30, 1, None) == binding.S1_ERR_INVALID_ARG   # N % 32
     assert L.s1_op_gemm(None, None, 4, 32, 60, 0, None, 32, 1, None) == binding.S1_ERR_INVALID_ARG   # K % 64
     assert L.s1_op_rmsnorm(None, None, 4, 30, 1e-6, None, None) == binding.S1_ERR_INVALID_ARG
+
+
+def test_short_convolution_models_are_refused_by_the_cuda_path(L):
+    """The gated delta-rule short convolution exists in the oracle only: the binding refuses such
+    a model before any device work instead of running it without the convolution."""
+    from prefill_only_decision_gb300 import binding
+    shape = configs.ModelShape(vocab=300, d_model=64, n_layers=4, ffn=64, la_heads=1, la_dk=64, la_dv=64,
+                               fa_q_heads=1, fa_kv_heads=1, fa_head_dim=64, bf16_weights=False, conv_width=4)
+    W = synth.make_weights(configs.Config("conv", 0, shape, configs.TINY.work))
+    with pytest.raises(binding.S1Error) as e:
+        binding.Model(W)
+    assert e.value.code == binding.S1_ERR_UNSUPPORTED
