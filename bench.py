@@ -195,8 +195,7 @@ def run_kernel(args):
     g = torch.Generator(device="cuda").manual_seed(0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.kernel == "gemm":
-        # several shapes may be given as "M,N,K,epi;M,N,K,epi"; --cm-sweep repeats each with
-        # cluster sizes 1, 2, 4 (S1_GEMM_CM) for a measurement pass under ncu
+        # several shapes may be given as "M,N,K,epi;M,N,K,epi" (one measurement pass under ncu)
         shapes = [[int(x) for x in sh.split(",")] for sh in args.shape.split(";")]
         res = []
         for sh in shapes:
@@ -206,24 +205,20 @@ def run_kernel(args):
             W = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.bfloat16)
             out = torch.zeros((M, N // 2 if epi == 3 else N), device="cuda",
                               dtype=torch.bfloat16 if epi in (1, 3) else torch.float32)
-            for cm in ((1, 2, 4) if args.cm_sweep else (None,)):
-                if cm is not None:
-                    os.environ["S1_GEMM_CM"] = str(cm)
-                call = lambda: B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), out.shape[1], 0)
-                for _ in range(max(1, args.warmup)):
-                    call()
+            call = lambda: B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), out.shape[1], 0)
+            for _ in range(max(1, args.warmup)):
+                call()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(max(1, args.steps)):
+                ev0.record()
+                call()
+                ev1.record()
                 torch.cuda.synchronize()
-                ts = []
-                for _ in range(max(1, args.steps)):
-                    ev0.record()
-                    call()
-                    ev1.record()
-                    torch.cuda.synchronize()
-                    ts.append(ev0.elapsed_time(ev1))
-                ms = float(np.median(ts))
-                res.append({"shape": sh, "cm": cm, "us_median": round(1e3 * ms, 2),
-                            "tflops": round(2.0 * M * N * K / (ms / 1e3) / 1e12, 1)})
-            os.environ.pop("S1_GEMM_CM", None)
+                ts.append(ev0.elapsed_time(ev1))
+            ms = float(np.median(ts))
+            res.append({"shape": sh, "us_median": round(1e3 * ms, 2),
+                        "tflops": round(2.0 * M * N * K / (ms / 1e3) / 1e12, 1)})
         torch.cuda.synchronize()
         print(json.dumps({"kernel": "gemm", "runs": res,
                           "note": "CUDA events around each op call (one launch; inputs L2-resident after the first call)"}))
@@ -282,7 +277,6 @@ def main():
     ap.add_argument("--path", default="fused", choices=["fused", "two-call"],
                     help="fused: s1_prefill_decide (one sweep); two-call: s1_prefill_state + s1_decide")
     ap.add_argument("--shape", default="1024,18432,2560,3")
-    ap.add_argument("--cm-sweep", action="store_true", help="gemm kernel mode: repeat with cluster sizes 1, 2, 4")
     ap.add_argument("--no-graphs", action="store_true", help="no CUDA graphs for the stream-ordered one-sweep call")
     args = ap.parse_args()
     if args.kernel:

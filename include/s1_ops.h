@@ -63,11 +63,11 @@ int s1_op_gemm_noalloc(const void* X, const void* W, int32_t M, int32_t N, int32
 
 /* The tensor-core GEMM plan the planner's heuristic picks for an M x N x K product with
  * epilogue `epi` on a GPU of num_sms SMs: pair = 0 for the single-CTA kernel family, 1 for the
- * CTA-pair family (as impl 3 / 2 of s1_op_gemm). out (host, 7 int32): tile width BN, cluster
- * size along M, CTA pair (0/1), K splits, 64-deep k-blocks per split, 128-row M tiles, N tiles.
- * Host logic only, callable without a GPU: the clusters of a tile width that fit at once come
- * from the device's occupancy query when a device is present, else num_sms / cluster size (the
- * first answer is kept for the process). The autotuner's measured choice, which can replace a
+ * CTA-pair family (as impl 3 / 2 of s1_op_gemm). out (host, 7 int32): tile width BN, CTAs per
+ * weight tile (always 1: no load is shared across a cluster), CTA pair (0/1), K splits, 64-deep
+ * k-blocks per split, 128-row M tiles, N tiles. Host logic only, callable without a GPU: the CTAs
+ * (or pairs) of a tile width that fit at once come from the device's occupancy query when a
+ * device is present, else one per SM (or per two SMs) (the first answer is kept for the process). The autotuner's measured choice, which can replace a
  * split-free plan on first use of a shape in a model, is not applied. Errors: INVALID_ARG
  * (M < 1, N % 32, K % 64, epi outside 0..3, num_sms < 1, NULL out). */
 int s1_gemm_plan(int32_t M, int32_t N, int32_t K, int32_t epi, int32_t num_sms, int32_t pair, int32_t* out);

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(PKG, "libs1.so")
 S1_OK, S1_ERR_INVALID_ARG, S1_ERR_INVALID_HANDLE, S1_ERR_OOM, S1_ERR_BUDGET, S1_ERR_CUDA, \
     S1_ERR_DEVICE_TIMEOUT, S1_ERR_UNSUPPORTED = range(8)
 S1_F32, S1_BF16 = 0, 1
+S1_NOALLOC_WS_FLOATS = 4 * 1024 * 1024   # fixed split-K scratch of s1_op_gemm_noalloc (include/s1_ops.h)
 S1_STAT_COUNT = 8
 PROF_NCLASS = 8
 PROF_NAMES = ["gemm", "gdn", "attn", "norm", "other"]

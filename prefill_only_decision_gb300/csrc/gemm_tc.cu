@@ -12,9 +12,10 @@
 // overlaps the main loop of the next. Work units are (m tile, split, n tile) with the m tile
 // fastest, so CTAs running at the same time read the same weight tile (L2 reuse). When the
 // tile count cannot fill the SMs, K is split and a reduction kernel applies the epilogue in a
-// fixed order (deterministic). A CTA-pair variant (tcgen05.mma.cta_group::2, 256-row tiles)
-// and clusters that multicast weight tiles are further candidates; the planner and a per-shape
-// autotuner choose among them. Launches use programmatic dependent launch.
+// fixed order (deterministic). A CTA-pair variant (tcgen05.mma.cta_group::2, 256-row tiles,
+// each CTA loading its own half of the weight tile) is the other candidate; the planner and a
+// per-shape autotuner choose among them. No load is multicast across a cluster. Launches use
+// programmatic dependent launch.
 //
 // Every mbarrier wait is bounded (~1 s of %globaltimer); on expiry the kernel records an
 // error code in the caller's error word and every role leaves its loop, so no launch can
@@ -96,16 +97,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Multicast variant: the box lands at the same shared-memory offset in every CTA of `mask`
-// and completes bytes on each destination CTA's mbarrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
-      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
 // Hint: bring a box of the tensor into L2 ahead of its TMA load (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
@@ -152,15 +143,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
-}
-// Arrive (when this thread's earlier MMAs complete) on the mbarrier at `bar`'s offset in every
-// CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(mask)
-      : "memory");
 }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -314,8 +296,8 @@ struct Cfg2 {
 struct Params {
   int M, N, K;
   int m_tiles, n_tiles, splits, kb_per_split, kb_total;
-  int m_groups;     // groups of CM consecutive m tiles (one group per cluster unit)
-  int units;        // cluster units: m_groups x splits x n_tiles
+  int m_groups;     // m work groups: m tiles (single-CTA kernel) or 256-row pair tiles
+  int units;        // work units: m_groups x splits x n_tiles
   int epi;          // epilogue; EPI_PARTIAL = write fp32 partials to ws
   void* out;
   int ldo;
@@ -425,19 +407,14 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
   }
 }
 
-// CM CTAs of a cluster (consecutive m tiles of the same n tile and K split) share each B
-// tile: CTA r loads rows [r*BN/CM, (r+1)*BN/CM) of it and multicasts them to the cluster, so
-// each weight byte leaves L2 once per cluster instead of once per CTA. A stage is refilled only
-// after every CTA of the cluster has released it (each MMA commit arrives on all CTAs' empty
-// barriers).
-template <int BN, int CM>
+// One CTA per SM, each loading its own A and B tiles; CTAs that run at the same time work on
+// consecutive m tiles of the same n tile, so a weight tile is read from DRAM once and served to
+// the others from L2.
+template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapO, Params p) {
   using C = Cfg<BN>;
-  constexpr int SLICE = BN / CM;                    // B rows loaded by each CTA of the cluster
-  constexpr uint16_t MASK = (uint16_t)((1u << CM) - 1);
-  static_assert(SLICE % 8 == 0, "B slices must be whole 8-row swizzle atoms");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -452,10 +429,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int crank = CM > 1 ? (int)cluster_rank() : 0;
-  const int cid = blockIdx.x / CM, ncl = gridDim.x / CM;
+  const int cid = blockIdx.x, ncl = gridDim.x;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], CM); }
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&tfull[b], 1); mbar_init(&tempty[b], 4); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -468,7 +444,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   __syncthreads();
-  if (CM > 1) cluster_sync_all();   // peers' barriers are initialised before anyone multicasts
   fence_after();
   const uint32_t tmem_base = *tmem_slot;
   allow_dependents();
@@ -479,7 +454,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int mg = u % p.m_groups, rest = u / p.m_groups, sp = rest % p.splits, nt = rest / p.splits;
     if (mg == 0) {
       const int kb0 = sp * p.kb_per_split, kb1 = min(p.kb_total, kb0 + p.kb_per_split);
-      for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, nt * BN + (CM > 1 ? crank * SLICE : 0));
+      for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, nt * BN);
     }
   }
   wait_prerequisites();
@@ -494,12 +469,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int rest = u / p.m_groups;
         const int sp = rest % p.splits;
         const int nt = rest / p.splits;
-        const int mt = mg * CM + crank;
+        const int mt = mg;
         const int kb0 = sp * p.kb_per_split;
         const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
-        // the weight slice this CTA loads is fetched from DRAM into L2 PF blocks ahead
-        // (only the first m group of each n tile prefetches; the others run alongside it)
-        const int brow = nt * BN + (CM > 1 ? crank * SLICE : 0);
+        // the weight tile is fetched from DRAM into L2 PF blocks ahead (only the first m tile
+        // of each n tile prefetches; the others run alongside it)
+        const int brow = nt * BN;
         const bool pf = mg == 0;
         if (pf)
           for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, brow);
@@ -508,16 +483,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
           mbar_expect_tx(&full[stage], C::STAGE_BYTES);
           tma_load_2d(sA + stage * C::A_BYTES, &mapA, &full[stage], kb * BK, mt * BM);
-          if (CM == 1)
-            tma_load_2d(sB + stage * C::B_BYTES, &mapB, &full[stage], kb * BK, nt * BN);
-          else
-            tma_load_2d_mc(sB + stage * C::B_BYTES + crank * SLICE * (BK * 2), &mapB, &full[stage], kb * BK,
-                           nt * BN + crank * SLICE, MASK);
+          tma_load_2d(sB + stage * C::B_BYTES, &mapB, &full[stage], kb * BK, brow);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }
-      // drain: every CTA's release of the stages this CTA filled has arrived here, so no peer
-      // signals this CTA's barriers after it exits
+      // drain: every stage this CTA filled has been released by its MMAs before the CTA exits
       for (int i = 0; i < C::STAGES && ok; ++i) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) break;
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -549,8 +519,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mma_bf16(tmem_d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                      (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          if (CM == 1) mma_commit(&empty[stage]);
-          else mma_commit_mc(&empty[stage], MASK);
+          mma_commit(&empty[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
         if (ok) mma_commit(&tfull[buf]);
@@ -567,7 +536,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int rest = u / p.m_groups;
       const int sp = rest % p.splits;
       const int nt = rest / p.splits;
-      const int mt = mg * CM + crank;
+      const int mt = mg;
       const int buf = it & 1;
       if (!mbar_wait(&tfull[buf], (it >> 1) & 1, abort_flag, p.d_err, ERR_TIMEOUT_TFULL)) break;
       fence_after();
@@ -581,7 +550,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) bulk_wait_all();   // this warp's stores have completed
   }
   __syncthreads();
-  if (CM > 1) cluster_sync_all();   // no CTA leaves while a peer may still target its memory
   if (warp == 1) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512));
@@ -906,32 +874,21 @@ namespace tc {
 
 struct Plan {
   int bn, m_tiles, n_tiles, splits, kb_per_split, kb_total, units, grid;
-  int cm;     // cluster size along M (B tiles multicast within the cluster)
   int pair;   // 1: CTA-pair kernel (256-row tiles, cta_group::2); bn is the pair's tile width
 };
 
-// Tile widths whose quarter is not a whole number of 8-row swizzle atoms: clusters of at most 2.
-constexpr bool max_cm2(int bn) { return bn == 144 || bn == 176 || bn == 208; }
+inline int max_ctas_of(int bn, int num_sms);
 
-// Cluster size along M: as many m tiles as share a B tile, up to 4 (2 for the widths above).
-inline int cluster_m(int m_tiles, int bn) {
-  int cm = m_tiles >= 4 ? 4 : (m_tiles >= 2 ? 2 : 1);
-  if (max_cm2(bn) && cm > 2) cm = 2;
-  return cm;
-}
-
-inline int max_clusters_of(int bn, int cm, int num_sms);
-
-// The plan of a fixed tile width and cluster size without a K split.
-inline Plan plan_with(int M, int N, int K, int bn, int cm) {
+// The single-CTA plan of a fixed tile width without a K split.
+inline Plan plan_with(int M, int N, int K, int bn) {
   const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + bn - 1) / bn, kb = K / BK;
-  return Plan{bn, m_tiles, n_tiles, 1, kb, kb, m_tiles * n_tiles, 0, cm, 0};
+  return Plan{bn, m_tiles, n_tiles, 1, kb, kb, m_tiles * n_tiles, 0, 0};
 }
 
 // The CTA-pair plan of tile width bn (no K split): m_tiles counts 128-row halves, units pairs.
 inline Plan plan_pair(int M, int N, int K, int bn) {
   const int m_pairs = (M + 2 * BM - 1) / (2 * BM), n_tiles = (N + bn - 1) / bn, kb = K / BK;
-  return Plan{bn, 2 * m_pairs, n_tiles, 1, kb, kb, m_pairs * n_tiles, 0, 1, 1};
+  return Plan{bn, 2 * m_pairs, n_tiles, 1, kb, kb, m_pairs * n_tiles, 0, 1};
 }
 
 inline int max_pairs_of(int bn, int num_sms);
@@ -955,11 +912,8 @@ inline Plan plan_pair_for(int M, int N, int K, int epi, int num_sms) {
   return best;
 }
 
-// Choose the N tile, the K split and the cluster size together: minimise
-// (waves of cluster units) x (k blocks per unit) x (per-k-block cost of the tile), where a
-// cluster unit is CM m tiles (padding tiles when CM does not divide the m-tile count cost
-// like real ones) and sharing the weight tile in a cluster lowers the per-block cost
-// (fewer bytes requested from L2 per stage).
+// Choose the N tile and the K split together: minimise (waves of work units) x (k blocks per
+// unit) x (per-k-block cost of the tile).
 Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
   Plan best{};
   double best_cost = 1e30;
@@ -968,97 +922,72 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
   // (176 and 208 are autotuner candidates only: measured slower than 144 in the split-K,
   // few-row weight-streaming plans this heuristic chooses; S1_GEMM_BN may still pin them)
   const int cands[6] = {256, 192, 144, 128, 208, 176};
-  const char* fe = getenv("S1_GEMM_CM");   // measurement override of the cluster size
-  const int force_cm = fe ? atoi(fe) : -1;
   const char* fb = getenv("S1_GEMM_BN");   // measurement / test override of the tile width
   const int force_bn = fb ? atoi(fb) : -1;
   for (int bn : cands) {
     if (epi == EPI_SWIGLU && (bn % 32)) continue;
     if (force_bn > 0 ? bn != force_bn : (bn == 208 || bn == 176)) continue;
     const int n_tiles = (N + bn - 1) / bn;
-    for (int cm = 1; cm <= 4; cm *= 2) {
-      if (max_cm2(bn) && cm == 4) continue;
-      if (cm > 1 && m_tiles < 2) continue;
-      if (force_cm > 0 && cm != force_cm) continue;
-      const int maxcl = max_clusters_of(bn, cm, num_sms);
-      const int groups = (m_tiles + cm - 1) / cm;
-      const double share = cm == 1 ? 1.0 : (cm == 2 ? 0.88 : 0.82);
-      for (int splits = 1; splits <= 16; ++splits) {
-        if (splits > 1 && (kb_total / splits) < 4) break;
-        const int kbp = (kb_total + splits - 1) / splits;
-        const int sp = (kb_total + kbp - 1) / kbp;
-        if (sp != splits) continue;
-        if (sp > 1 && (size_t)sp * m_tiles * BM * (size_t)N > ws_cap) break;
-        const int cunits = groups * n_tiles * sp;
-        const int waves = (cunits + maxcl - 1) / maxcl;
-        double cost = (double)waves * kbp * (bn + 48.0) * share;
-        if (sp > 1) cost *= 1.0 + 0.04 * sp;
-        if (cost < best_cost * 0.999) {
-          best_cost = cost;
-          best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, m_tiles * n_tiles * sp, 0, cm, 0};
-        }
-        if (cunits >= maxcl) break;
+    const int maxc = max_ctas_of(bn, num_sms);
+    for (int splits = 1; splits <= 16; ++splits) {
+      if (splits > 1 && (kb_total / splits) < 4) break;
+      const int kbp = (kb_total + splits - 1) / splits;
+      const int sp = (kb_total + kbp - 1) / kbp;
+      if (sp != splits) continue;
+      if (sp > 1 && (size_t)sp * m_tiles * BM * (size_t)N > ws_cap) break;
+      const int units = m_tiles * n_tiles * sp;
+      const int waves = (units + maxc - 1) / maxc;
+      double cost = (double)waves * kbp * (bn + 48.0);
+      if (sp > 1) cost *= 1.0 + 0.04 * sp;
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, 0, 0};
       }
+      if (units >= maxc) break;
     }
   }
   return best;
 }
 
-template <int BN, int CM>
+template <int BN>
 cudaLaunchConfig_t launch_config(cudaLaunchAttribute* attr, cudaStream_t st, bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
   cfg.stream = st;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CM;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cfg;
 }
 
-// Clusters of this configuration that fit on the GPU at once (queried once, then cached).
-template <int BN, int CM>
-int max_clusters(int num_sms) {
+// CTAs of this tile width that fit on the GPU at once (queried once, then cached).
+template <int BN>
+int max_ctas(int num_sms) {
   static int cached = -1;
   if (cached < 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<BN, CM>(attr, 0);
-    cfg.gridDim = dim3(CM * ((num_sms + CM - 1) / CM));
-    int n = 0;
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<BN, CM>, &cfg);
-    if (e != cudaSuccess || n <= 0) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
+    int per_sm = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<BN>, NUM_THREADS, Cfg<BN>::SMEM);
+    if (e != cudaSuccess || per_sm <= 0) {
       cudaGetLastError();
-      n = num_sms / CM;
+      per_sm = 1;
     }
-    cached = n;
+    cached = per_sm * num_sms;
   }
   return cached;
 }
 
-inline int max_clusters_of(int bn, int cm, int num_sms) {
-  switch (bn * 8 + cm) {
-    case 256 * 8 + 1: return max_clusters<256, 1>(num_sms);
-    case 256 * 8 + 2: return max_clusters<256, 2>(num_sms);
-    case 256 * 8 + 4: return max_clusters<256, 4>(num_sms);
-    case 192 * 8 + 1: return max_clusters<192, 1>(num_sms);
-    case 192 * 8 + 2: return max_clusters<192, 2>(num_sms);
-    case 192 * 8 + 4: return max_clusters<192, 4>(num_sms);
-    case 208 * 8 + 1: return max_clusters<208, 1>(num_sms);
-    case 208 * 8 + 2: return max_clusters<208, 2>(num_sms);
-    case 176 * 8 + 1: return max_clusters<176, 1>(num_sms);
-    case 176 * 8 + 2: return max_clusters<176, 2>(num_sms);
-    case 144 * 8 + 1: return max_clusters<144, 1>(num_sms);
-    case 144 * 8 + 2: return max_clusters<144, 2>(num_sms);
-    case 128 * 8 + 1: return max_clusters<128, 1>(num_sms);
-    case 128 * 8 + 2: return max_clusters<128, 2>(num_sms);
-    case 128 * 8 + 4: return max_clusters<128, 4>(num_sms);
-    default: return num_sms / cm;
+inline int max_ctas_of(int bn, int num_sms) {
+  switch (bn) {
+    case 256: return max_ctas<256>(num_sms);
+    case 208: return max_ctas<208>(num_sms);
+    case 192: return max_ctas<192>(num_sms);
+    case 176: return max_ctas<176>(num_sms);
+    case 144: return max_ctas<144>(num_sms);
+    default: return max_ctas<128>(num_sms);
   }
 }
 
@@ -1123,26 +1052,17 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN>, ma, mb, mo, p);
 }
 
-template <int BN, int CM>
+template <int BN>
 cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, Params p, int num_sms,
                       cudaStream_t st) {
-  const int mc = max_clusters<BN, CM>(num_sms);
-  cudaLaunchAttribute attr[2];
+  const int mc = max_ctas<BN>(num_sms);
+  cudaLaunchAttribute attr[1];
   const bool pdl = pdl_enabled();
-  cudaLaunchConfig_t cfg = launch_config<BN, CM>(attr, st, pdl);
-  p.m_groups = (p.m_tiles + CM - 1) / CM;
+  cudaLaunchConfig_t cfg = launch_config<BN>(attr, st, pdl);
+  p.m_groups = p.m_tiles;
   p.units = p.m_groups * p.splits * p.n_tiles;
-  const int ncl = p.units < mc ? p.units : mc;
-  cfg.gridDim = dim3(ncl * CM);
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, CM>, ma, mb, mo, p);
-}
-
-template <int BN>
-cudaError_t launch_cm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, const Params& p, int cm,
-                      int num_sms, cudaStream_t st) {
-  if (cm == 4) return launch_bn<BN, (max_cm2(BN) ? 2 : 4)>(ma, mb, mo, p, num_sms, st);
-  if (cm == 2) return launch_bn<BN, 2>(ma, mb, mo, p, num_sms, st);
-  return launch_bn<BN, 1>(ma, mb, mo, p, num_sms, st);
+  cfg.gridDim = dim3(p.units < mc ? p.units : mc);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, ma, mb, mo, p);
 }
 
 }  // namespace tc
@@ -1166,15 +1086,14 @@ size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms) {
 
 static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, int epi,
                                void* out, int ldo, float* splitk_ws, const LaunchCtx& lc) {
-  const int cm = pl.cm;
   CUtensorMap ma, mb;
-  const int brows = pl.pair ? pl.bn / 2 : pl.bn / cm;
+  const int brows = pl.pair ? pl.bn / 2 : pl.bn;
   if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, brows)) return cudaErrorInvalidValue;
   tc::Params p;
   p.M = M; p.N = N; p.K = K;
   p.m_tiles = pl.m_tiles; p.n_tiles = pl.n_tiles; p.splits = pl.splits;
   p.kb_per_split = pl.kb_per_split; p.kb_total = pl.kb_total;
-  p.m_groups = 0; p.units = 0;   // set by the launcher for its cluster size
+  p.m_groups = 0; p.units = 0;   // set by the launcher for its kernel family
   p.epi = pl.splits > 1 ? tc::EPI_PARTIAL : epi;
   p.out = out; p.ldo = ldo; p.ws = splitk_ws; p.d_err = lc.d_err;
   // fp32 output map: 32-row x 16-column boxes (64-byte rows, 64-byte swizzle), matching the
@@ -1206,12 +1125,12 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
       default: e = tc::launch_pair<128>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
     }
   } else switch (pl.bn) {
-    case 256: e = tc::launch_cm<256>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
-    case 208: e = tc::launch_cm<208>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
-    case 192: e = tc::launch_cm<192>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
-    case 176: e = tc::launch_cm<176>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
-    case 144: e = tc::launch_cm<144>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
-    default: e = tc::launch_cm<128>(ma, mb, mo, p, cm, lc.num_sms, lc.stream); break;
+    case 256: e = tc::launch_bn<256>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+    case 208: e = tc::launch_bn<208>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+    case 192: e = tc::launch_bn<192>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+    case 176: e = tc::launch_bn<176>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+    case 144: e = tc::launch_bn<144>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
+    default: e = tc::launch_bn<128>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
   }
   if (lc.launches) *lc.launches += 1;
   if (e != cudaSuccess || pl.splits == 1) return e;
@@ -1233,9 +1152,9 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
 }
 
 namespace tc {
-// Measured choice of (BN, CM, pair) per GEMM shape for plans without a K split. Every such plan
+// Measured choice of (BN, pair) per GEMM shape for plans without a K split. Every such plan
 // accumulates each output over K in the same order, so the choice never changes results.
-struct Tuned { int bn, cm, pair; };
+struct Tuned { int bn, pair; };
 std::mutex g_tune_mu;
 std::map<std::tuple<int, int, int, int, int, int>, Tuned> g_tuned;
 
@@ -1255,10 +1174,10 @@ int variant_of(const LaunchCtx& lc) {
 }
 
 inline Plan plan_of(int M, int N, int K, const Tuned& t) {
-  return t.pair ? plan_pair(M, N, K, t.bn) : plan_with(M, N, K, t.bn, t.cm);
+  return t.pair ? plan_pair(M, N, K, t.bn) : plan_with(M, N, K, t.bn);
 }
 
-// Times every candidate (single-CTA BN x CM, and CTA-pair BN) three times on the caller's stream
+// Times every candidate (single-CTA BN, and CTA-pair BN) three times on the caller's stream
 // from a flushed L2 (tuning output `scratch`, RESADD shapes tuned with a plain fp32 store of the
 // same size) and keeps the fastest of the last two runs.
 cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
@@ -1281,32 +1200,23 @@ cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, in
   if (!tout || (resadd && (size_t)M * N > lc.tune_floats)) return cudaSuccess;   // keep the heuristic plan
   LaunchCtx l2 = lc;
   l2.launches = nullptr;
-  // Each timed run starts with L2 flushed (a 192 MB write), as in a forward pass, where every
-  // weight tile comes from DRAM. The buffer lives for the tuning of this shape only.
-  const size_t flush_bytes = (size_t)192 << 20;
-  void* flush = nullptr;
-  if (cudaMalloc(&flush, flush_bytes) != cudaSuccess) {
-    cudaGetLastError();
-    flush = nullptr;
-  }
+  // Each timed run starts with L2 flushed (the caller's buffer, larger than L2, rewritten), as in
+  // a forward pass, where every weight tile comes from DRAM. Without a buffer the runs are timed
+  // from a warm L2.
+  void* flush = lc.tune_flush;
+  const size_t flush_bytes = lc.tune_flush_bytes;
   cudaEvent_t e0, e1;
   if (cudaEventCreate(&e0) != cudaSuccess) return cudaGetLastError();
   if (cudaEventCreate(&e1) != cudaSuccess) { cudaEventDestroy(e0); return cudaGetLastError(); }
   float best = 1e30f;
-  Tuned bt{pl.bn, pl.cm, pl.pair};
-  const int m_tiles = (M + BM - 1) / BM;
+  Tuned bt{pl.bn, pl.pair};
   std::vector<Tuned> cands;
   if (variant != GEMM_PAIR)
-    for (int bn : {256, 208, 192, 176, 144, 128}) {
-      if (epi == EPI_SWIGLU && (bn % 32)) continue;
-      for (int cm = 1; cm <= 4; cm *= 2) {
-        if ((max_cm2(bn) && cm == 4) || (cm > 1 && m_tiles < 2)) continue;
-        cands.push_back(Tuned{bn, cm, 0});
-      }
-    }
+    for (int bn : {256, 208, 192, 176, 144, 128})
+      if (!(epi == EPI_SWIGLU && (bn % 32))) cands.push_back(Tuned{bn, 0});
   if (variant != GEMM_SINGLE)
     for (int bn : {256, 208, 192, 176, 128})
-      if (!(epi == EPI_SWIGLU && (bn % 32))) cands.push_back(Tuned{bn, 1, 1});
+      if (!(epi == EPI_SWIGLU && (bn % 32))) cands.push_back(Tuned{bn, 1});
   cudaError_t err = cudaSuccess;
   for (const Tuned& c : cands) {
     if (err != cudaSuccess) break;
@@ -1322,24 +1232,20 @@ cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, in
       if (err == cudaSuccess && rep > 0 && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess) t = std::min(t, ms);
     }
     if (getenv("S1_GEMM_TUNE_LOG") && getenv("S1_GEMM_TUNE_LOG")[0] == '2')
-      fprintf(stderr, "gemm cand M=%d N=%d K=%d epi=%d %s bn=%d cm=%d %.2f us\n", M, N, K, epi,
-              c.pair ? "pair" : "single", c.bn, c.cm, 1e3f * t);
+      fprintf(stderr, "gemm cand M=%d N=%d K=%d epi=%d %s bn=%d %.2f us\n", M, N, K, epi,
+              c.pair ? "pair" : "single", c.bn, 1e3f * t);
     if (t < best) { best = t; bt = c; }
   }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
-  if (flush) {
-    cudaStreamSynchronize(lc.stream);
-    cudaFree(flush);
-  }
   if (err != cudaSuccess) return err;
   {
     std::lock_guard<std::mutex> lk(g_tune_mu);
     g_tuned[key] = bt;
   }
   if (getenv("S1_GEMM_TUNE_LOG"))
-    fprintf(stderr, "gemm tune M=%d N=%d K=%d epi=%d -> %s bn=%d cm=%d (%.2f us)\n", M, N, K, epi,
-            bt.pair ? "pair" : "single", bt.bn, bt.cm, 1e3f * best);
+    fprintf(stderr, "gemm tune M=%d N=%d K=%d epi=%d -> %s bn=%d (%.2f us)\n", M, N, K, epi,
+            bt.pair ? "pair" : "single", bt.bn, 1e3f * best);
   pl = plan_of(M, N, K, bt);
   return cudaSuccess;
 }
@@ -1352,7 +1258,7 @@ cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, in
   const int variant = tc::variant_of(lc);
   tc::Plan pl = variant == GEMM_PAIR ? tc::plan_pair_for(M, N, K, epi, lc.num_sms)
                                      : tc::plan_for(M, N, K, epi, lc.num_sms, splitk_ws ? ws_floats : 0);
-  if (pl.splits == 1 && lc.tune && tc::tune_enabled() && !getenv("S1_GEMM_CM") && !getenv("S1_GEMM_BN")) {
+  if (pl.splits == 1 && lc.tune && tc::tune_enabled() && !getenv("S1_GEMM_BN")) {
     cudaError_t e = tc::tune(pl, X, W, M, N, K, epi, out, ldo, lc, variant);
     if (e != cudaSuccess) return e;
   }
@@ -1457,7 +1363,7 @@ extern "C" int s1_gemm_plan(int32_t M, int32_t N, int32_t K, int32_t epi, int32_
   const tc::Plan pl = pair ? tc::plan_pair_for(M, N, K, epi, num_sms)
                            : tc::plan_for(M, N, K, epi, num_sms, gemm_tc_workspace_floats(M, N, K, epi, num_sms));
   out[0] = pl.bn;
-  out[1] = pl.cm;
+  out[1] = 1;   // CTAs per weight tile (no clusters along M)
   out[2] = pl.pair;
   out[3] = pl.splits;
   out[4] = pl.kb_per_split;

@@ -55,9 +55,11 @@ struct LaunchCtx {
   int* d_err;        // device error word (bounded waits record here)
   int num_sms;
   long* launches;    // incremented per kernel launched (may be NULL)
-  bool tune = false;          // GEMM: measure the tile / cluster choice on first use of a shape
+  bool tune = false;          // GEMM: measure the tile choice on first use of a shape
   void* tune_out = nullptr;   // GEMM tuning: scratch output for residual-add shapes (fp32)
   size_t tune_floats = 0;
+  void* tune_flush = nullptr; // GEMM tuning: buffer larger than L2, rewritten before each timed run
+  size_t tune_flush_bytes = 0;
   int variant = GEMM_ANY;     // GEMM: kernel families allowed (GEMM_ANY, GEMM_SINGLE, GEMM_PAIR)
   // GEMM, residual add with a K split over at most 512 rows: the RMSNorm of the updated rows,
   // out = bf16(x / sqrt(mean(x^2) + norm_eps) * norm_w), fused into the split-K reduction

@@ -128,6 +128,8 @@ struct s1_model {
   size_t lm_floats = 0;
   float* schunk = nullptr;     // chunk-start states of the chunked scan [chunks, H, dv, dk]
   size_t schunk_chunks = 0;
+  void* tune_flush = nullptr;  // GEMM autotuner: L2-flush buffer (allocated with the model)
+  size_t tune_flush_bytes = 0;
   bool gdn_token = false;      // S1_GDN=token: token-by-token scan (debugging)
   char* pinned = nullptr;      // host staging for metadata uploads
   size_t pinned_bytes = 0;
@@ -452,6 +454,8 @@ int gemm(s1_model* m, const bf16* X, const bf16* W, int M, int N, int K, int epi
     lc.tune = !m->prof;
     lc.tune_out = m->sc.proj;
     lc.tune_floats = (size_t)m->sc.rows * m->n_proj;
+    lc.tune_flush = m->tune_flush;
+    lc.tune_flush_bytes = m->tune_flush_bytes;
     CK(launch_gemm_tc(X, W, M, N, K, epi, out, ldo, m->sc.ws, m->sc.ws_floats, lc));
   } else {
     CK(launch_gemm_simt(X, W, M, N, K, epi, out, ldo, m->stream));
@@ -953,6 +957,16 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   }
   m->d_err = (int*)dalloc(256);
   if (!m->d_err) return bail(fail(S1_ERR_OOM, "error word allocation failed"));
+  // The GEMM autotuner times each candidate tile from a flushed L2 (a write larger than L2
+  // before each run); the buffer comes from the model's allocator like all its device memory.
+  {
+    const char* tn = getenv("S1_GEMM_TUNE");
+    if (!(tn && tn[0] == '0')) {
+      m->tune_flush_bytes = (size_t)192 << 20;
+      m->tune_flush = dalloc(m->tune_flush_bytes);
+      if (!m->tune_flush) return bail(fail(S1_ERR_OOM, "autotuner L2-flush buffer allocation failed"));
+    }
+  }
   if (cudaMemsetAsync(m->d_err, 0, 256, m->stream) != cudaSuccess ||
       cudaStreamSynchronize(m->stream) != cudaSuccess)
     return bail(fail(S1_ERR_CUDA, "model initialisation failed: %s", cudaGetErrorString(cudaGetLastError())));
@@ -971,6 +985,7 @@ void s1_model_destroy(s1_model* m) {
   dfree(m->d_err);
   dfree(m->schunk);
   dfree(m->lm_buf);
+  dfree(m->tune_flush);
   if (m->pinned) cudaFreeHost(m->pinned);
   if (m->meta_done) cudaEventDestroy(m->meta_done);
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);

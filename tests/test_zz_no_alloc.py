@@ -57,22 +57,47 @@ def test_noalloc_gemm_matches_allocating_entry_point(L, M, N, K, epi):
     torch.cuda.synchronize()
     refn = ref.float().cpu().numpy()
     scale = np.sqrt(K) * 0.05
-    for _ in range(2):   # two calls in a row: the fixed scratch keeps the previous call's contents
-        out = fresh()
+    tol = 1e-4 * scale + (np.abs(refn) * 2.0 ** -8 if epi in (1, 3) else 0)
+
+    def call(out):
         rc = L.s1_op_gemm_noalloc(C.c_void_p(X.data_ptr()), C.c_void_p(W.data_ptr()), M, N, K, epi,
                                   C.c_void_p(out.data_ptr()), ncol, None)
         assert rc == 0, L.s1_last_error()
+
+    call(fresh())                 # first call on this device: looks up the arrays' addresses
+    outs = [fresh(), fresh()]     # every output buffer exists before device memory is read
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for out in outs:              # two calls in a row: the fixed scratch keeps the previous call's contents
+        call(out)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0, "the call changed the device's free memory"
+    for out in outs:
         got = out.float().cpu().numpy()
-        tol = 1e-4 * scale + (np.abs(refn) * 2.0 ** -8 if epi in (1, 3) else 0)
         assert np.all(np.abs(got - refn) <= tol), np.abs(got - refn).max()
+
+
+def _oversized_shape(sms):
+    """A shape whose planned split-K partials exceed the fixed array on a GPU of `sms` SMs (the
+    planner is host logic, so the search needs no device work), or None."""
+    from prefill_only_decision_gb300 import binding
+    cap = binding.S1_NOALLOC_WS_FLOATS
+    for N in (256, 512, 1024, 2048):
+        for mt in range(1, 4 * sms):
+            M = 128 * mt
+            p = binding.gemm_plan(M, N, 8192, 0, sms, False)
+            if p["splits"] > 1 and p["splits"] * p["m_tiles"] * 128 * N > cap:
+                return M, N, 8192
+    return None
 
 
 def test_noalloc_gemm_rejects_oversized_scratch(L):
     """A plan whose split-K partials exceed the fixed array is refused before any device work."""
     from prefill_only_decision_gb300 import binding
-    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
-        pytest.skip("the oversized example is derived for 152 SMs")
-    M, N, K = 2176, 1024, 8192
+    shp = _oversized_shape(torch.cuda.get_device_properties(0).multi_processor_count)
+    if shp is None:
+        pytest.skip("no split-K plan on this GPU needs more scratch than the fixed array holds")
+    M, N, K = shp
     X = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
     W = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
     out = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
