@@ -201,10 +201,10 @@ def run_kernel(args):
         for sh in shapes:
             M, N, K = sh[:3]
             epi = sh[3] if len(sh) > 3 else 0
-            X = torch.randn((M, K), device="cuda", generator=g).to(torch.bfloat16)
-            W = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.bfloat16)
+            X = torch.randn((M, K), device="cuda", generator=g).to(torch.float16)
+            W = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.float16)
             out = torch.zeros((M, N // 2 if epi == 3 else N), device="cuda",
-                              dtype=torch.bfloat16 if epi in (1, 3) else torch.float32)
+                              dtype=torch.float16 if epi in (1, 3) else torch.float32)
             call = lambda: B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), out.shape[1], 0)
             for _ in range(max(1, args.warmup)):
                 call()
@@ -228,7 +228,7 @@ def run_kernel(args):
         nseq = dims[3] if len(dims) > 3 else 1
         ld = 3 * H * D + 2 * H
         proj = torch.randn((R, ld), device="cuda", generator=g)
-        out = torch.zeros((R, H * D), device="cuda", dtype=torch.bfloat16)
+        out = torch.zeros((R, H * D), device="cuda", dtype=torch.float16)
         lens = [R // nseq] * nseq
         lens[-1] += R - sum(lens)
         row0 = list(np.cumsum([0] + lens[:-1]))
@@ -237,11 +237,11 @@ def run_kernel(args):
     else:
         P, L, nseq, Hq, Hkv, hd = dims[:6]
         R = L * nseq
-        q = torch.randn((R, Hq, hd), device="cuda", generator=g).to(torch.bfloat16)
-        kn = torch.randn((R, Hkv, hd), device="cuda", generator=g).to(torch.bfloat16)
-        vn = torch.randn((R, Hkv, hd), device="cuda", generator=g).to(torch.bfloat16)
-        kv = torch.randn((2, max(P, 1), Hkv, hd), device="cuda", generator=g).to(torch.bfloat16)
-        out = torch.zeros((R, Hq * hd), device="cuda", dtype=torch.bfloat16)
+        q = torch.randn((R, Hq, hd), device="cuda", generator=g).to(torch.float16)
+        kn = torch.randn((R, Hkv, hd), device="cuda", generator=g).to(torch.float16)
+        vn = torch.randn((R, Hkv, hd), device="cuda", generator=g).to(torch.float16)
+        kv = torch.randn((2, max(P, 1), Hkv, hd), device="cuda", generator=g).to(torch.float16)
+        out = torch.zeros((R, Hq * hd), device="cuda", dtype=torch.float16)
         row0 = [i * L for i in range(nseq)]
         fn = lambda: B.op_attention(q.data_ptr(), kn.data_ptr(), vn.data_ptr(), kv.data_ptr() if P else 0, P, row0,
                                     [L] * nseq, Hq, Hkv, hd, out.data_ptr())

@@ -128,7 +128,10 @@ enum { S1_STAT_ARGMAX = 0, S1_STAT_EXPECTED, S1_STAT_YES, S1_STAT_ANSWER_CONF,
 
 /* ---- model ----------------------------------------------------------------------
  * Validates the shape, uploads the weights, merges each LoRA pair as
- * W + (alpha/rank) * B A in fp32 and rounds once to bf16 (round to nearest even).
+ * W + (alpha/rank) * B A in fp32 and rounds once to f16 (round to nearest even): every
+ * tensor-core operand of the forward pass is f16 (the tensor cores' bf16 rate, three more
+ * mantissa bits; a bf16 weight converts to f16 exactly when |w| >= 2^-14, and to within 2^-25
+ * below it). The tied embedding is kept as an f16 copy too.
  * Blocking. Errors: INVALID_ARG (shape), UNSUPPORTED, OOM, CUDA. */
 int s1_model_create(const s1_shape* shape, const s1_weights* weights, s1_model** out);
 void s1_model_destroy(s1_model* m);      /* waits for the model's stream first */
@@ -144,7 +147,7 @@ int s1_set_allocator(void* (*alloc)(size_t bytes, void* ctx), void (*free_fn)(vo
  * Prefill the state prefix: n_embeds given embedding rows (bf16 [n_embeds, d], host),
  * followed by n_tokens token rows; positions 0 .. n_embeds+n_tokens-1. Returns an
  * immutable snapshot (per-layer gated delta-rule state, fp32 [H, dv, dk], and
- * post-RoPE K/V, bf16 [P, Hkv, hd]). Host pointers; blocking.
+ * post-RoPE K/V, f16 [P, Hkv, hd]). Host pointers; blocking.
  * Errors: INVALID_ARG (ids, empty prefix), BUDGET (rows > max_rows), OOM, CUDA. */
 int s1_prefill_state(s1_model* m, const int32_t* tokens, int32_t n_tokens,
                      const void* embeds, int32_t n_embeds, s1_state** out);

@@ -24,18 +24,18 @@ enum { S1_PROF_GEMM = 0, S1_PROF_GDN = 1, S1_PROF_ATTN = 2, S1_PROF_NORM = 3, S1
        S1_PROF_NCLASS = 8 };
 
 /* GEMM epilogues of s1_op_gemm */
-enum { S1_EPI_F32 = 0, S1_EPI_BF16 = 1, S1_EPI_RESADD = 2, S1_EPI_SWIGLU = 3 };
+enum { S1_EPI_F32 = 0, S1_EPI_F16 = 1, S1_EPI_RESADD = 2, S1_EPI_SWIGLU = 3 };
 
-/* Y = epi(X[M,K] . W[N,K]^T): bf16 operands (row-major, K contiguous), fp32 accumulate.
+/* Y = epi(X[M,K] . W[N,K]^T): f16 operands (row-major, K contiguous), fp32 accumulate.
  * The projections of every decoder layer (gated delta-rule in-projection
  * [q|k|v|a|b], attention in-projection [q|k|v], out-projections, SwiGLU MLP) are of
  * this form (layer definition of the hybrid decoder; LoRA merged into W at load,
  * System1-Omni issue #10 plan item 3).
  *   S1_EPI_F32:    out fp32 [M, ldo] = acc
- *   S1_EPI_BF16:   out bf16 [M, ldo] = acc (round to nearest even)
+ *   S1_EPI_F16:    out f16 [M, ldo] = acc (round to nearest even)
  *   S1_EPI_RESADD: out fp32 [M, ldo] += acc        (residual stream)
  *   S1_EPI_SWIGLU: W rows interleaved in blocks of 16 gate rows then 16 up rows;
- *                  out bf16 [M, ldo], N/2 columns: silu(gate) * up
+ *                  out f16 [M, ldo], N/2 columns: silu(gate) * up
  * impl: 0 = tcgen05 tensor-core kernel (the product path: single-CTA or CTA-pair tiles, the
  *       planner's choice), 1 = SIMT reference, 2 = tensor-core kernel restricted to CTA-pair
  *       tiles (256 x N per pair, tcgen05.mma.cta_group::2), 3 = restricted to single-CTA tiles.
@@ -78,21 +78,21 @@ int s1_gemm_plan(int32_t M, int32_t N, int32_t K, int32_t epi, int32_t num_sms, 
  * proj: fp32 [R, 2*H*dk + H*dv + 2*H] rows [q | k | v | a | b] (q, k normalised IN PLACE).
  * Sequence s covers rows row0[s] .. row0[s]+len[s]-1 (host arrays). S0: device fp32
  * [n_seq, H, dv, dk] initial states or NULL (zero). S_out: device [n_seq, H, dv, dk] final
- * states or NULL. out: bf16 [R, H*dv]. */
+ * states or NULL. out: f16 [R, H*dv]. */
 int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l2_eps,
               int32_t n_seq, const int32_t* row0, const int32_t* len, const float* S0,
               float* S_out, void* out, void* stream);
 
 /* Causal GQA attention with continuation (System1-Omni RFC #114 section 4, "Branching").
- * q bf16 [R, Hq, hd] and k_new, v_new bf16 [R, Hkv, hd] (already rotated). Sequence s
- * (rows row0[s] .. +len[s]) attends to the P cached keys kv_cache = bf16 [2, P, Hkv, hd]
+ * q f16 [R, Hq, hd] and k_new, v_new f16 [R, Hkv, hd] (already rotated). Sequence s
+ * (rows row0[s] .. +len[s]) attends to the P cached keys kv_cache = f16 [2, P, Hkv, hd]
  * (K plane then V plane; NULL when P == 0) and causally to its own rows.
- * softmax(q.k / sqrt(hd)) v; q head h reads kv head floor(h*Hkv/Hq). out bf16 [R, Hq*hd]. */
+ * softmax(q.k / sqrt(hd)) v; q head h reads kv head floor(h*Hkv/Hq). out f16 [R, Hq*hd]. */
 int s1_op_attention(const void* q, const void* k_new, const void* v_new, const void* kv_cache,
                     int32_t P, int32_t n_seq, const int32_t* row0, const int32_t* len, int32_t Hq,
                     int32_t Hkv, int32_t hd, void* out, void* stream);
 
-/* out bf16 [R, d] = x / sqrt(mean(x^2) + eps) * w;  x fp32 [R, d], w fp32 [d]. */
+/* out f16 [R, d] = x / sqrt(mean(x^2) + eps) * w;  x fp32 [R, d], w fp32 [d]. */
 int s1_op_rmsnorm(const float* x, const float* w, int32_t R, int32_t d, float eps, void* out,
                   void* stream);
 

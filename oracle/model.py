@@ -61,6 +61,12 @@ def round_bf16(x):
     return u.astype(np.uint32).view(np.float32)
 
 
+def round_f16(x):
+    """Round to the nearest IEEE half-precision value (ties to even; values below 2^-14 to the
+    subnormal grid of 2^-24) and return it as float32."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float32)
+
+
 def upcast(w, dt):
     """Weights as stored (float32, or bf16 bit patterns in uint16) -> dt."""
     if w is None:
@@ -148,20 +154,22 @@ class LayerCache:
 
 class Oracle:
     """precision="fp32": every step in dt, LoRA unmerged (the author's-reference semantics).
-    precision="bf16": the pages' BF16 backbone policy (System1-Omni issue #10, the fast path's
-    "bfloat16 ... float32 head"; RFC #114 section 2 "Start with BF16 CUDA inference" and section 3
-    on merging the adapter): the LoRA delta is merged into each weight at load in fp32 and the
-    merged weight rounded once to bf16, and every matrix-product input (normed rows, mixer
-    output, SwiGLU output) is rounded to bf16; accumulation, the recurrent state, attention
-    softmax, residual stream and the readout stay fp32."""
+    precision="bf16" / "f16": a backbone precision policy (System1-Omni issue #10, the fast
+    path's half-precision backbone with "a float32 head"; RFC #114 section 3 on merging the
+    adapter): the LoRA delta is merged into each weight at load in fp32 and the merged weight
+    rounded once to the 16-bit type, and every matrix-product input (normed rows, mixer output,
+    SwiGLU output, attention q/k/v) is rounded to it; accumulation, the recurrent state,
+    attention softmax, residual stream and the readout stay fp32. These modes measure what a
+    16-bit backbone costs against the fp32 definition; "f16" is the CUDA path's policy."""
 
     def __init__(self, weights, dtype=np.float32, precision="fp32"):
         self.W = weights
         self.s = weights.shape
         self.dt = np.dtype(dtype)
-        if precision not in ("fp32", "bf16"):
+        if precision not in ("fp32", "bf16", "f16"):
             raise ValueError(precision)
-        self.bf16 = precision == "bf16"
+        self.policy = precision != "fp32"         # a 16-bit policy mode is active
+        self.rnd = round_f16 if precision == "f16" else round_bf16
         self.full = list(self.s.layer_is_full)
         r = self.s.lora_rank
         self.lora_scale = (self.s.lora_alpha / r) if r > 0 else 0.0
@@ -179,13 +187,13 @@ class Oracle:
         else:
             idx, j = target_or_idx, None
         has_lora = j is not None and self.s.lora_rank > 0 and self.W.lora_a[l][j] is not None
-        if self.bf16:
+        if self.policy:
             Wm = self._w(l, idx)
             if has_lora:
                 A = upcast(self.W.lora_a[l][j], self.dt)
                 B = upcast(self.W.lora_b[l][j], self.dt)
                 Wm = Wm + self.dt.type(self.lora_scale) * (B @ A)
-            return round_bf16(x).astype(self.dt) @ round_bf16(Wm).astype(self.dt).T
+            return self.rnd(x).astype(self.dt) @ self.rnd(Wm).astype(self.dt).T
         y = x @ self._w(l, idx).T
         if has_lora:
             A = upcast(self.W.lora_a[l][j], self.dt)
@@ -221,7 +229,7 @@ class Oracle:
         q = q.reshape(T, H, Dk)
         k = k.reshape(T, H, Dk)
         v = v.reshape(T, H, Dv)
-        xa = round_bf16(xn).astype(self.dt) if self.bf16 else xn
+        xa = self.rnd(xn).astype(self.dt) if self.policy else xn
         a = xa @ self._w(l, 4).T
         b = xa @ self._w(l, 5).T
         q = gdn.l2norm(q, s.l2_eps)
@@ -239,8 +247,8 @@ class Oracle:
         q = rope(self.linear(xn, l, "q").reshape(T, Hq, hd), pos, s.rope_theta)
         k = rope(self.linear(xn, l, "k").reshape(T, Hkv, hd), pos, s.rope_theta)
         v = self.linear(xn, l, "v").reshape(T, Hkv, hd)
-        if self.bf16:   # attention operands and the cached K/V are stored in bf16 by the policy
-            q, k, v = (round_bf16(t).astype(self.dt) for t in (q, k, v))
+        if self.policy:   # attention operands and the cached K/V are stored in the 16-bit type by the policy
+            q, k, v = (self.rnd(t).astype(self.dt) for t in (q, k, v))
         if cache is not None:
             K = np.concatenate([cache.K, k]); V = np.concatenate([cache.V, v])
             kp = np.concatenate([cache.pos, pos])
@@ -251,7 +259,7 @@ class Oracle:
         return y, LayerCache(K=K, V=V, pos=kp)
 
     def mlp(self, l, xn):
-        # (in bf16 mode, `linear` rounds the SwiGLU output like every other product input)
+        # (in a policy mode, `linear` rounds the SwiGLU output like every other product input)
         return self.linear(silu(self.linear(xn, l, "gate")) * self.linear(xn, l, "up"), l, "down")
 
     # -- forward ------------------------------------------------------------

@@ -12,7 +12,7 @@
 //
 // flash kernel: CTA = 64 queries x one q head (4 warps x 16 rows); K/V tiles of 64 keys staged
 // in shared memory by cp.async (double-buffered, 16-byte chunks XOR-swizzled by row);
-// S = Q K^T and O += P V on the tensor cores (mma.sync m16n8k16 bf16 -> fp32).
+// S = Q K^T and O += P V on the tensor cores (mma.sync m16n8k16 f16 -> fp32).
 #include <algorithm>
 
 #include "common.cuh"
@@ -44,13 +44,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -71,15 +71,15 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t saddr, uint32_t rank) {
   return v;
 }
 
-// byte offset of 16-byte chunk c of row r in a tile whose rows are HD bf16 wide
+// byte offset of 16-byte chunk c of row r in a tile whose rows are HD f16 wide
 template <int HD>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * (HD * 2) + ((c ^ (r & 7)) << 4));
 }
 
 template <int HD>
-__global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, const bf16* __restrict__ knew,
-                                                    const bf16* __restrict__ vnew, bf16* __restrict__ out,
+__global__ void __launch_bounds__(128) flash_kernel(const f16* __restrict__ q, const f16* __restrict__ knew,
+                                                    const f16* __restrict__ vnew, f16* __restrict__ out,
                                                     const SeqDesc* __restrict__ seqs,
                                                     const CtxDesc* __restrict__ ctxs, int layer_f, int Hq,
                                                     int Hkv, float scale_log2, int nparts) {
@@ -103,8 +103,8 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   int P = 0;
-  const bf16* Kc = nullptr;
-  const bf16* Vc = nullptr;
+  const f16* Kc = nullptr;
+  const f16* Vc = nullptr;
   if (sd.ctx_in >= 0) {
     const CtxDesc c = ctxs[sd.ctx_in];
     P = c.P;
@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
     Kc = c.KV + (size_t)layer_f * 2 * plane + (size_t)g * HD;
     Vc = Kc + plane;
   }
-  const bf16* Kn = knew + ((size_t)sd.row0 * Hkv + g) * HD;
-  const bf16* Vn = vnew + ((size_t)sd.row0 * Hkv + g) * HD;
+  const f16* Kn = knew + ((size_t)sd.row0 * Hkv + g) * HD;
+  const f16* Vn = vnew + ((size_t)sd.row0 * Hkv + g) * HD;
   const size_t kstride = (size_t)Hkv * HD;
   const int n_keys = P + min(sd.len, q0 + BQ);     // keys any query of this tile can see
   const int n_all = (n_keys + BKV - 1) / BKV;
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
   for (int i = tid; i < BQ * CH; i += 128) {
     const int r = i / CH, c = i % CH;
     const bool ok = q0 + r < sd.len;
-    const bf16* src = q + ((size_t)(sd.row0 + (ok ? q0 + r : 0)) * Hq + h) * HD + c * 8;
+    const f16* src = q + ((size_t)(sd.row0 + (ok ? q0 + r : 0)) * Hq + h) * HD + c * 8;
     cp_async16(smem_u32(sQ) + swz<HD>(r, c), src, ok);
   }
   auto load_kv = [&](int t, int stage) {
@@ -133,8 +133,8 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
       const int r = i / CH, c = i % CH;
       const int j = j0 + r;
       const bool ok = j < n_keys;
-      const bf16* ks;
-      const bf16* vs;
+      const f16* ks;
+      const f16* vs;
       if (j < P) { ks = Kc + (size_t)j * kstride; vs = Vc + (size_t)j * kstride; }
       else { const int jj = ok ? j - P : 0; ks = Kn + (size_t)jj * kstride; vs = Vn + (size_t)jj * kstride; }
       cp_async16(smem_u32(sK + stage * TILE) + swz<HD>(r, c), ks + c * 8, ok);
@@ -217,8 +217,8 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
       const float p2 = exp2f(s[n][2] - base1), p3 = exp2f(s[n][3] - base1);
       rs0 += p0 + p1;
       rs1 += p2 + p3;
-      pa[n >> 1][(n & 1) * 2 + 0] = pack_bf16(p0, p1);
-      pa[n >> 1][(n & 1) * 2 + 1] = pack_bf16(p2, p3);
+      pa[n >> 1][(n & 1) * 2 + 0] = pack_f16(p0, p1);
+      pa[n >> 1][(n & 1) * 2 + 1] = pack_f16(p2, p3);
     }
     rs0 += __shfl_xor_sync(0xffffffffu, rs0, 1);
     rs0 += __shfl_xor_sync(0xffffffffu, rs0, 2);
@@ -294,16 +294,16 @@ __global__ void __launch_bounds__(128) flash_kernel(const bf16* __restrict__ q, 
   const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
   const int col = 2 * (lane & 3);
   if (qi0 < sd.len) {
-    bf16* op = out + ((size_t)(sd.row0 + qi0) * Hq + h) * HD + col;
+    f16* op = out + ((size_t)(sd.row0 + qi0) * Hq + h) * HD + col;
 #pragma unroll
     for (int i = 0; i < HD / 8; ++i)
-      *reinterpret_cast<uint32_t*>(op + i * 8) = pack_bf16(o[i][0] * inv0, o[i][1] * inv0);
+      *reinterpret_cast<uint32_t*>(op + i * 8) = pack_f16(o[i][0] * inv0, o[i][1] * inv0);
   }
   if (qi0 + 8 < sd.len) {
-    bf16* op = out + ((size_t)(sd.row0 + qi0 + 8) * Hq + h) * HD + col;
+    f16* op = out + ((size_t)(sd.row0 + qi0 + 8) * Hq + h) * HD + col;
 #pragma unroll
     for (int i = 0; i < HD / 8; ++i)
-      *reinterpret_cast<uint32_t*>(op + i * 8) = pack_bf16(o[i][2] * inv1, o[i][3] * inv1);
+      *reinterpret_cast<uint32_t*>(op + i * 8) = pack_f16(o[i][2] * inv1, o[i][3] * inv1);
   }
 }
 
@@ -316,8 +316,8 @@ static int attention_parts(int max_keys) {
 }
 
 template <int HD>
-static cudaError_t launch_flash(dim3 grid, int nparts, int smem, cudaStream_t st, const bf16* q, const bf16* knew,
-                                const bf16* vnew, bf16* out, const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f,
+static cudaError_t launch_flash(dim3 grid, int nparts, int smem, cudaStream_t st, const f16* q, const f16* knew,
+                                const f16* vnew, f16* out, const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f,
                                 int Hq, int Hkv, float scale_log2) {
   static bool set = false;
   if (!set) {
@@ -348,7 +348,7 @@ static cudaError_t launch_flash(dim3 grid, int nparts, int smem, cudaStream_t st
                             nparts);
 }
 
-cudaError_t launch_attention(const bf16* q, const bf16* knew, const bf16* vnew, bf16* out,
+cudaError_t launch_attention(const f16* q, const f16* knew, const f16* vnew, f16* out,
                              const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx, int layer_f,
                              int Hq, int Hkv, int hd, int max_len, int max_keys, long work_ctas, int num_sms,
                              cudaStream_t st) {

@@ -58,7 +58,7 @@ cudaError_t launch_gdn_prep(float* proj, int ld, float* loga, float* beta, int R
 template <int DK>
 __global__ void __launch_bounds__(128) gdn_scan_token_kernel(
     const float* __restrict__ proj, int ld, const float* __restrict__ loga,
-    const float* __restrict__ beta, bf16* __restrict__ out, const SeqDesc* __restrict__ seqs,
+    const float* __restrict__ beta, f16* __restrict__ out, const SeqDesc* __restrict__ seqs,
     const CtxDesc* __restrict__ ctxs, int layer_g, int H, int Dv) {
   allow_dependents();
   wait_prerequisites();
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(128) gdn_scan_token_kernel(
       float val = ov[0];
 #pragma unroll
       for (int r = 1; r < 4; ++r) if (lane == r) val = ov[r];
-      out[(size_t)row * H * Dv + h * Dv + rbase + lane] = f2bf(val);
+      out[(size_t)row * H * Dv + h * Dv + rbase + lane] = f2h(val);
     }
   }
   if (sd.ctx_out >= 0) {
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(128) gdn_scan_token_kernel(
 }
 
 cudaError_t launch_gdn_scan(const float* proj, int ld, const float* loga, const float* beta,
-                            bf16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
+                            f16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
                             int layer_g, int H, int Dk, int Dv, cudaStream_t st) {
   if (n_seq <= 0) return cudaSuccess;
   if (Dk != Dv || (Dv % 16) != 0) return cudaErrorNotSupported;

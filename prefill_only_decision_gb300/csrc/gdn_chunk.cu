@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(512) chunk_state_kernel(const __grid_constant_
 
 // ---------------------------------------------------------------------------------------
 // chunk_out: one CTA per (chunk, head), 256 threads (8 warps).
-// O = diag(gamma) Q S_c^T + P U, P = lower_incl(Gamma * Q K^T); out bf16 [R, H*Dv].
+// O = diag(gamma) Q S_c^T + P U, P = lower_incl(Gamma * Q K^T); out f16 [R, H*Dv].
 // chunk_out: one CTA per (chunk, head, value slice), 256 threads. A CTA forms the output
 // columns [vs * D/VS, (vs + 1) * D/VS) of its head; the launcher splits the value columns over
 // VS CTAs when (chunks x heads) alone leaves SMs idle (a few questions over a snapshot). P, q's
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
                                                         const float* __restrict__ Schunk,
                                                         const SeqDesc* __restrict__ seqs,
                                                         const CtxDesc* __restrict__ ctxs, int layer_g, int out_fold,
-                                                        bf16* __restrict__ out) {
+                                                        f16* __restrict__ out) {
   allow_dependents();
   wait_prerequisites();
   extern __shared__ __align__(16) uint8_t smraw[];
@@ -877,11 +877,11 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
     const int c = cs + cb + nt * 8 + 2 * tq;
     const int ta = r0 + gq, tb = r0 + gq + 8;
     if (ta < n)
-      *reinterpret_cast<__nv_bfloat162*>(out + (size_t)(cd.row0 + ta) * HDv + h * D + c) =
-          __floats2bfloat162_rn(o[nt][0], o[nt][1]);
+      *reinterpret_cast<__half2*>(out + (size_t)(cd.row0 + ta) * HDv + h * D + c) =
+          __floats2half2_rn(o[nt][0], o[nt][1]);
     if (tb < n)
-      *reinterpret_cast<__nv_bfloat162*>(out + (size_t)(cd.row0 + tb) * HDv + h * D + c) =
-          __floats2bfloat162_rn(o[nt][2], o[nt][3]);
+      *reinterpret_cast<__half2*>(out + (size_t)(cd.row0 + tb) * HDv + h * D + c) =
+          __floats2half2_rn(o[nt][2], o[nt][3]);
   }
 }
 
@@ -912,7 +912,7 @@ static cudaError_t launch_state(const CUtensorMap& mW, const CUtensorMap& mK, co
 }
 
 template <int D>
-static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, float eps, bf16* out,
+static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, float eps, f16* out,
                                     const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                     const CtxDesc* d_ctx, int layer_g, int H, float* Wbuf, float* Ubuf,
                                     float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
@@ -995,7 +995,7 @@ static cudaError_t launch_chunked_d(float* proj, int ld, int R, float* loga, flo
   return cudaGetLastError();
 }
 
-cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float eps, bf16* out,
+cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float eps, f16* out,
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,

@@ -1,4 +1,4 @@
-// Plain SIMT GEMM (CUDA cores): Y = epilogue(X[M,K] . W[N,K]^T), bf16 in, fp32 accumulate.
+// Plain SIMT GEMM (CUDA cores): Y = epilogue(X[M,K] . W[N,K]^T), f16 in, fp32 accumulate.
 // Used as the in-library reference for the tensor-core GEMM's kernel tests.
 // Requires K % 32 == 0; any M, N.
 #include "common.cuh"
@@ -12,12 +12,12 @@ __device__ __forceinline__ void epilogue_store(int epi, void* out, int ldo, int 
   (void)tile_row; (void)n_in_tile;
   if (m >= M || n >= N) return;
   if (epi == EPI_F32) reinterpret_cast<float*>(out)[(size_t)m * ldo + n] = v;
-  else if (epi == EPI_BF16) reinterpret_cast<bf16*>(out)[(size_t)m * ldo + n] = f2bf(v);
+  else if (epi == EPI_HALF) reinterpret_cast<f16*>(out)[(size_t)m * ldo + n] = f2h(v);
   else if (epi == EPI_RESADD) reinterpret_cast<float*>(out)[(size_t)m * ldo + n] += v;
 }
 
-__global__ void __launch_bounds__(256) gemm_simt_kernel(const bf16* __restrict__ X,
-                                                        const bf16* __restrict__ W, int M, int N,
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const f16* __restrict__ X,
+                                                        const f16* __restrict__ W, int M, int N,
                                                         int K, int epi, void* __restrict__ out,
                                                         int ldo) {
   __shared__ float As[SK][SB + 4];
@@ -35,10 +35,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const bf16* __restrict__
       if (m < M) va = *reinterpret_cast<const uint4*>(X + (size_t)m * K + k0 + lk);
       const int n = n0 + lr;
       if (n < N) vb = *reinterpret_cast<const uint4*>(W + (size_t)n * K + k0 + lk);
-      const bf16* pa = reinterpret_cast<const bf16*>(&va);
-      const bf16* pb = reinterpret_cast<const bf16*>(&vb);
+      const f16* pa = reinterpret_cast<const f16*>(&va);
+      const f16* pb = reinterpret_cast<const f16*>(&vb);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) { As[lk + e][lr] = bf2f(pa[e]); Bs[lk + e][lr] = bf2f(pb[e]); }
+      for (int e = 0; e < 8; ++e) { As[lk + e][lr] = h2f(pa[e]); Bs[lk + e][lr] = h2f(pb[e]); }
     }
     __syncthreads();
 #pragma unroll 8
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const bf16* __restrict__
       const int m = m0 + r, nout = n0 / 2 + c;
       if (m < M && n0 + 32 * b + 16 + i < N) {
         const float g = Cs[r][32 * b + i], u = Cs[r][32 * b + 16 + i];
-        reinterpret_cast<bf16*>(out)[(size_t)m * ldo + nout] = f2bf(silu_f(g) * u);
+        reinterpret_cast<f16*>(out)[(size_t)m * ldo + nout] = f2h(silu_f(g) * u);
       }
     }
   } else {
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const bf16* __restrict__
   }
 }
 
-cudaError_t launch_gemm_simt(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out,
+cudaError_t launch_gemm_simt(const f16* X, const f16* W, int M, int N, int K, int epi, void* out,
                              int ldo, cudaStream_t st) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if (K % SK) return cudaErrorInvalidValue;

@@ -1,13 +1,13 @@
 // Tensor-core GEMM for sm_103a: TMA -> shared memory -> tcgen05.mma -> TMEM -> epilogue.
 //
-//   Y = epi(X[M,K] . W[N,K]^T), bf16 operands (both K-major), fp32 accumulation in TMEM.
+//   Y = epi(X[M,K] . W[N,K]^T), f16 operands (both K-major), fp32 accumulation in TMEM.
 //
 // Persistent, warp-specialised CTA of 6 warps, one CTA per SM:
 //   warp 0       TMA producer: 128 x 64 A tile and BN x 64 B tile per stage (128-byte swizzle)
 //   warp 1       TMEM allocator and MMA issuer (one thread): 4 x tcgen05.mma (K = 16) per stage
 //   warps 2..5   epilogue: tcgen05.ld of the 128 x BN accumulator (one row per thread),
 //                fused epilogue (fp32 store or residual add-reduction by TMA from swizzled
-//                shared-memory boxes; bf16 / SwiGLU stores from registers; split-K partials)
+//                shared-memory boxes; f16 / SwiGLU stores from registers; split-K partials)
 // The accumulator is double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
 // overlaps the main loop of the next. Work units are (m tile, split, n tile) with the m tile
 // fastest, so CTAs running at the same time read the same weight tile (L2 reuse). When the
@@ -127,12 +127,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A/B, fp32 D, both K-major, M = 128, N = bn.
-__host__ __device__ constexpr uint32_t idesc_bf16(int bn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor, kind::f16: f16 A/B (format code 0 in bits 7-9 and 10-12), fp32 D
+// (bits 4-5 = 1), both K-major, N / 8 in bits 17-22, M / 16 in bits 24-28; M = 128, N = bn.
+__host__ __device__ constexpr uint32_t idesc_f16(int bn) {
+  return (1u << 4) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -194,7 +195,7 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
 // D[256 x N] (+)= A[256 x 16] . B[N x 16]^T over the CTA pair: A rows 0..127 and B rows
 // 0..N/2-1 from the issuing CTA's shared memory, the rest from the peer's at the same offsets;
 // D rows 0..127 land in the issuing CTA's TMEM, rows 128..255 in the peer's.
-__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void mma_f16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                               uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -240,8 +241,8 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 }
 
 // Instruction descriptor for the pair: M = 256.
-__host__ __device__ constexpr uint32_t idesc_bf16_pair(int bn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f16_pair(int bn) {
+  return (1u << 4) | ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
 }
 
 
@@ -311,7 +312,7 @@ constexpr int EPI_PARTIAL = 100;
 // memory (one 64-byte row per lane, swizzled like the output map) to one TMA bulk store per box,
 // or a TMA add-reduction into the fp32 residual stream for EPI_RESADD (each output element has
 // exactly one writer, so the sum is the plain fp32 x + acc); a lane's row of a store box is
-// 64 bytes, where a direct store from registers would write 16-byte pieces of 32 rows. bf16
+// 64 bytes, where a direct store from registers would write 16-byte pieces of 32 rows. f16
 // outputs (32 contiguous bytes per row and chunk) are stored from registers. Two staging boxes per
 // warp alternate; a box is rewritten only after the store issued from it two boxes earlier has
 // read it. m0 = the warp's first row of the product, y0 = its row in the output map (m0, or
@@ -353,30 +354,30 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
     for (int j = 0; j < 4; ++j)
 #pragma unroll
       for (int i = 0; i < 16; ++i) reg_fence(v[j][i]);
-    const int m = m0 + lane;   // this lane's output row (bf16 outputs: stored from registers)
+    const int m = m0 + lane;   // this lane's output row (f16 outputs: stored from registers)
     if (p.epi == EPI_SWIGLU) {
       // chunk pairs (gate, up): tile columns [32b, 32b+16) gate, [32b+16, 32b+32) up; each row's
       // 16 outputs are 32 contiguous bytes (one full sector)
 #pragma unroll
       for (int j = 0; j + 1 < 4; j += 2) {
         if (m < p.M && j + 1 < nc && n0 + c0 + 16 * j < p.N) {
-          bf16* o = reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + (n0 + c0 + 16 * j) / 2;
-          __align__(16) bf16 r[16];
+          f16* o = reinterpret_cast<f16*>(p.out) + (size_t)m * p.ldo + (n0 + c0 + 16 * j) / 2;
+          __align__(16) f16 r[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) r[i] = f2bf(silu_f(v[j][i]) * v[j + 1][i]);
+          for (int i = 0; i < 16; ++i) r[i] = f2h(silu_f(v[j][i]) * v[j + 1][i]);
           reinterpret_cast<uint4*>(o)[0] = reinterpret_cast<uint4*>(r)[0];
           reinterpret_cast<uint4*>(o)[1] = reinterpret_cast<uint4*>(r)[1];
         }
       }
-    } else if (p.epi == EPI_BF16) {
+    } else if (p.epi == EPI_HALF) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int n = n0 + c0 + 16 * j;
         if (m >= p.M || j >= nc || n >= p.N) continue;
-        __align__(16) bf16 r[16];
+        __align__(16) f16 r[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = f2bf(v[j][i]);
-        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out) + (size_t)m * p.ldo + n);
+        for (int i = 0; i < 16; ++i) r[i] = f2h(v[j][i]);
+        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<f16*>(p.out) + (size_t)m * p.ldo + n);
         o[0] = reinterpret_cast<uint4*>(r)[0];
         o[1] = reinterpret_cast<uint4*>(r)[1];
       }
@@ -495,7 +496,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BN);
+      constexpr uint32_t idesc = idesc_f16(BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -516,7 +517,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            mma_bf16(tmem_d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+            mma_f16(tmem_d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                      (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
@@ -655,7 +656,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && crank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_pair(BN);
+      constexpr uint32_t idesc = idesc_f16_pair(BN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -679,7 +680,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            mma_bf16_pair(tmem_d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+            mma_f16_pair(tmem_d, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                           (kb > kb0 || kk > 0) ? 1u : 0u);
           mma_commit_pair(&empty[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -739,9 +740,9 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
         g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
         u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
       }
-      bf16* o = reinterpret_cast<bf16*>(out) + (size_t)m * ldo + c;
-      o[0] = f2bf(silu_f(g.x) * u.x); o[1] = f2bf(silu_f(g.y) * u.y);
-      o[2] = f2bf(silu_f(g.z) * u.z); o[3] = f2bf(silu_f(g.w) * u.w);
+      f16* o = reinterpret_cast<f16*>(out) + (size_t)m * ldo + c;
+      o[0] = f2h(silu_f(g.x) * u.x); o[1] = f2h(silu_f(g.y) * u.y);
+      o[2] = f2h(silu_f(g.z) * u.z); o[3] = f2h(silu_f(g.w) * u.w);
     } else {
       float4 a = make_float4(0, 0, 0, 0);
       for (int s = 0; s < splits; ++s) {
@@ -756,8 +757,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
         x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
         *o = x;
       } else {
-        bf16* o = reinterpret_cast<bf16*>(out) + (size_t)m * ldo + c;
-        o[0] = f2bf(a.x); o[1] = f2bf(a.y); o[2] = f2bf(a.z); o[3] = f2bf(a.w);
+        f16* o = reinterpret_cast<f16*>(out) + (size_t)m * ldo + c;
+        o[0] = f2h(a.x); o[1] = f2h(a.y); o[2] = f2h(a.z); o[3] = f2h(a.w);
       }
     }
   }
@@ -769,7 +770,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
 // splitk_reduce_kernel followed by the block-per-row RMSNorm, so the results are the same bits.
 __global__ void __launch_bounds__(1024) splitk_resadd_norm_kernel(const float* __restrict__ ws, int splits, int Mpad,
                                                                  int N, float* __restrict__ x, int ldx,
-                                                                 const float* __restrict__ w, bf16* __restrict__ xn,
+                                                                 const float* __restrict__ w, f16* __restrict__ xn,
                                                                  float eps) {
   allow_dependents();
   wait_prerequisites();
@@ -791,11 +792,11 @@ __global__ void __launch_bounds__(1024) splitk_resadd_norm_kernel(const float* _
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)N + eps);
   const float4* wr = reinterpret_cast<const float4*>(w);
-  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(xn + (size_t)m * N);
+  __half2* o2 = reinterpret_cast<__half2*>(xn + (size_t)m * N);
   for (int i = threadIdx.x; i < N / 4; i += blockDim.x) {
     const float4 v = xr[i], g = wr[i];   // this thread's own row entries, written above
-    o2[2 * i] = __floats2bfloat162_rn(v.x * inv * g.x, v.y * inv * g.y);
-    o2[2 * i + 1] = __floats2bfloat162_rn(v.z * inv * g.z, v.w * inv * g.w);
+    o2[2 * i] = __floats2half2_rn(v.x * inv * g.x, v.y * inv * g.y);
+    o2[2 * i + 1] = __floats2half2_rn(v.z * inv * g.z, v.w * inv * g.w);
   }
 }
 
@@ -818,7 +819,7 @@ EncodeTiledFn get_encode() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major [rows, cols] matrix, box = [box_rows, 64 cols], 128-byte swizzle.
+// 2-D f16 map over a row-major [rows, cols] matrix, box = [box_rows, 64 cols], 128-byte swizzle.
 // Cached by (pointer, rows, cols, box_rows).
 bool make_map(CUtensorMap* out, const void* ptr, int rows, int cols, int box_rows) {
   static std::mutex mu;
@@ -833,7 +834,7 @@ bool make_map(CUtensorMap* out, const void* ptr, int rows, int cols, int box_row
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
@@ -1084,7 +1085,7 @@ size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms) {
   return (size_t)2 * (num_sms > 0 ? num_sms : 160) * tc::BM * 256;
 }
 
-static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, int epi,
+static cudaError_t launch_plan(const tc::Plan& pl, const f16* X, const f16* W, int M, int N, int K, int epi,
                                void* out, int ldo, float* splitk_ws, const LaunchCtx& lc) {
   CUtensorMap ma, mb;
   const int brows = pl.pair ? pl.bn / 2 : pl.bn;
@@ -1112,7 +1113,7 @@ static cudaError_t launch_plan(const tc::Plan& pl, const bf16* X, const bf16* W,
       if (!tensor_map(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     } else {
-      memset(&mo, 0, sizeof(mo));   // bf16 outputs are stored from registers
+      memset(&mo, 0, sizeof(mo));   // f16 outputs are stored from registers
     }
   }
   cudaError_t e;
@@ -1180,7 +1181,7 @@ inline Plan plan_of(int M, int N, int K, const Tuned& t) {
 // Times every candidate (single-CTA BN, and CTA-pair BN) three times on the caller's stream
 // from a flushed L2 (tuning output `scratch`, RESADD shapes tuned with a plain fp32 store of the
 // same size) and keeps the fastest of the last two runs.
-cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
+cudaError_t tune(Plan& pl, const f16* X, const f16* W, int M, int N, int K, int epi, void* out, int ldo,
                  const LaunchCtx& lc, int variant) {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1251,7 +1252,7 @@ cudaError_t tune(Plan& pl, const bf16* X, const bf16* W, int M, int N, int K, in
 }
 }  // namespace tc
 
-cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
+cudaError_t launch_gemm_tc(const f16* X, const f16* W, int M, int N, int K, int epi, void* out, int ldo,
                            float* splitk_ws, size_t ws_floats, const LaunchCtx& lc) {
   if (M == 0) return cudaSuccess;
   if (!gemm_tc_supported(M, N, K, epi)) return cudaErrorInvalidValue;
@@ -1345,7 +1346,7 @@ extern "C" int s1_op_gemm_noalloc(const void* X, const void* W, int32_t M, int32
     return set_error(S1_ERR_CUDA, "gemm_noalloc: clearing the error word failed");
   LaunchCtx lc{st, d->err, d->sms, nullptr};
   // the plan writes only `need` floats of the array; plan_cap only selects the same plan
-  cudaError_t e = launch_gemm_tc((const bf16*)X, (const bf16*)W, M, N, K, epi, out, ldo, d->ws, plan_cap, lc);
+  cudaError_t e = launch_gemm_tc((const f16*)X, (const f16*)W, M, N, K, epi, out, ldo, d->ws, plan_cap, lc);
   if (e != cudaSuccess) return set_error(S1_ERR_CUDA, cudaGetErrorString(e));
   int h = 0;
   if (cudaMemcpyAsync(&h, d->err, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||

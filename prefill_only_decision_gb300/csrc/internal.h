@@ -3,19 +3,26 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace s1 {
 
+// bf16: the model's stored tensors as the caller gives them (embedding table, given embedding
+// rows, bf16 weight arrays). f16: every tensor-core operand of the forward pass (merged weights,
+// normed rows, mixer and MLP outputs, attention q/k/v and the K/V snapshot): the same tensor-core
+// rate as bf16 with three more mantissa bits (bf16 weights convert to f16 exactly down to 2^-14,
+// and below it to within 2^-25).
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // GEMM epilogues: Y = X[M,K] . W[N,K]^T accumulated in fp32, then
 enum Epilogue {
   EPI_F32 = 0,      // out fp32 [M, ldo]: out = acc
-  EPI_BF16 = 1,     // out bf16 [M, ldo]: out = bf16(acc)
+  EPI_HALF = 1,     // out f16 [M, ldo]: out = f16(acc)
   EPI_RESADD = 2,   // out fp32 [M, ldo]: out += acc   (residual stream)
   EPI_SWIGLU = 3,   // W rows interleaved in blocks of 16 gate / 16 up rows;
-                    // out bf16 [M, ldo] with N/2 columns: silu(gate) * up
+                    // out f16 [M, ldo] with N/2 columns: silu(gate) * up
 };
 
 // Packed description of the sequences of one forward call.
@@ -42,7 +49,7 @@ constexpr int GDN_CHUNK = 64;
 // A prefix snapshot as seen by kernels: all layers' tensors of one state.
 struct CtxDesc {
   float* S;     // [n_gdn_layers, H, Dv, Dk] fp32
-  bf16* KV;     // [n_fa_layers, 2, cap, Hkv, hd] bf16
+  f16* KV;      // [n_fa_layers, 2, cap, Hkv, hd] f16
   int P;        // cached rows
   int cap;      // capacity rows
 };
@@ -62,10 +69,10 @@ struct LaunchCtx {
   size_t tune_flush_bytes = 0;
   int variant = GEMM_ANY;     // GEMM: kernel families allowed (GEMM_ANY, GEMM_SINGLE, GEMM_PAIR)
   // GEMM, residual add with a K split over at most 512 rows: the RMSNorm of the updated rows,
-  // out = bf16(x / sqrt(mean(x^2) + norm_eps) * norm_w), fused into the split-K reduction
+  // out = f16(x / sqrt(mean(x^2) + norm_eps) * norm_w), fused into the split-K reduction
   // (same arithmetic and order as launch_rmsnorm over that many rows, so the same bits).
   const float* norm_w = nullptr;   // [N] fp32; NULL: no fused norm
-  bf16* norm_out = nullptr;        // [M, N] bf16
+  f16* norm_out = nullptr;         // [M, N] f16
   float norm_eps = 0.f;
   bool* norm_done = nullptr;       // set to true when the norm was fused (the caller skips its own)
 };
@@ -85,47 +92,47 @@ bool tensor_map(CUtensorMap* out, CUtensorMapDataType dtype, int rank, const voi
                 const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle);
 
 // ---- kernels (launchers) ----
-cudaError_t launch_embed(const bf16* E, const int* row_src, const bf16* embeds, float* x, int R, int d,
+cudaError_t launch_embed(const f16* E, const int* row_src, const bf16* embeds, float* x, int R, int d,
                          cudaStream_t st);
-cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int d, float eps,
+cudaError_t launch_rmsnorm(const float* x, const float* w, f16* out, int R, int d, float eps,
                            cudaStream_t st);
-cudaError_t launch_gemm_simt(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out,
+cudaError_t launch_gemm_simt(const f16* X, const f16* W, int M, int N, int K, int epi, void* out,
                              int ldo, cudaStream_t st);
 bool gemm_tc_supported(int M, int N, int K, int epi);
-cudaError_t launch_gemm_tc(const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out,
+cudaError_t launch_gemm_tc(const f16* X, const f16* W, int M, int N, int K, int epi, void* out,
                            int ldo, float* splitk_ws, size_t ws_floats, const LaunchCtx& lc);
 size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms);
 size_t gemm_tc_plan_ws_floats(int M, int N, int K, int epi, int num_sms, size_t ws_cap);
 cudaError_t launch_gdn_prep(float* proj, int ld, float* alpha, float* beta, int R, int H, int Dk,
                             int Dv, float eps, cudaStream_t st);
 cudaError_t launch_gdn_scan(const float* proj, int ld, const float* alpha, const float* beta,
-                            bf16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
+                            f16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
                             int layer_g, int H, int Dk, int Dv, cudaStream_t st);
 bool gdn_chunked_supported(int H, int Dk, int Dv, int ld);
-cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float l2_eps, bf16* out,
+cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float l2_eps, f16* out,
                                const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
                                const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
                                float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
                                int fold_from, int out_fold, int* d_err, int num_sms, cudaStream_t st,
                                long* launches);
 cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab, const int* row_seq,
-                              const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, bf16* q,
-                              bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,
+                              const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, f16* q,
+                              f16* knew, f16* vnew, int R, int Hq, int Hkv, int hd,
                               cudaStream_t st);
-cudaError_t launch_attention(const bf16* q, const bf16* knew, const bf16* vnew, bf16* out,
+cudaError_t launch_attention(const f16* q, const f16* knew, const f16* vnew, f16* out,
                              const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx, int layer_f,
                              int Hq, int Hkv, int hd, int max_len, int max_keys, long work_ctas, int num_sms,
                              cudaStream_t st);
-cudaError_t launch_readout(const float* x, const float* final_norm, const bf16* E, int d, float eps,
+cudaError_t launch_readout(const float* x, const float* final_norm, const f16* E, int d, float eps,
                            const int* q_row, const int* q_type, const int* opt_off,
                            const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,
                            int max_opts, float* hn_out, float* z_out, cudaStream_t st);
 size_t vocab_lm_scratch_floats(int n_q, int n_opts, int d, int num_sms);
-cudaError_t launch_vocab_lm(const bf16* E, int V, int d, const float* hn, const float* z, const int* opt_off, int n_q,
+cudaError_t launch_vocab_lm(const f16* E, int V, int d, const float* hn, const float* z, const int* opt_off, int n_q,
                             float* lm, float* scratch, int num_sms, cudaStream_t st, long* launches);
 cudaError_t launch_merge_lora(const void* W, int w_is_bf16, const void* A, const void* B,
                               int ab_is_bf16, int rank, float scale, int out_f, int in_f,
-                              bf16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,
+                              f16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,
                               int swiglu_F, float* tmpA, float* tmpB, cudaStream_t st);
 cudaError_t launch_to_f32(const void* src, int is_bf16, float* dst, size_t n, cudaStream_t st);
 cudaError_t launch_rope_table(float2* tab, int max_pos, int hd, double theta, cudaStream_t st);

@@ -6,33 +6,37 @@ namespace s1 {
 
 // ---- embedding rows: x[r] = E[id] (fp32), or a given embedding row ---------------------
 // row_src[r] >= 0: token id; row_src[r] < 0: row (-1 - row_src[r]) of `embeds`.
-__global__ void embed_kernel(const bf16* __restrict__ E, const int* __restrict__ row_src,
+// E is the model's f16 copy of the tied embedding; given rows are the caller's bf16.
+__global__ void embed_kernel(const f16* __restrict__ E, const int* __restrict__ row_src,
                              const bf16* __restrict__ embeds, float* __restrict__ x, int d) {
   allow_dependents();
   const int r = blockIdx.x;
   const int s = row_src[r];
-  const bf16* src = (s >= 0) ? E + (size_t)s * d : embeds + (size_t)(-1 - s) * d;
   float* dst = x + (size_t)r * d;
-  for (int i = threadIdx.x * 2; i < d; i += blockDim.x * 2) {
-    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(src + i);
-    float2 f = __bfloat1622float2(v);
-    *reinterpret_cast<float2*>(dst + i) = f;
+  if (s >= 0) {
+    const f16* src = E + (size_t)s * d;
+    for (int i = threadIdx.x * 2; i < d; i += blockDim.x * 2)
+      *reinterpret_cast<float2*>(dst + i) = __half22float2(*reinterpret_cast<const __half2*>(src + i));
+  } else {
+    const bf16* src = embeds + (size_t)(-1 - s) * d;
+    for (int i = threadIdx.x * 2; i < d; i += blockDim.x * 2)
+      *reinterpret_cast<float2*>(dst + i) = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + i));
   }
 }
 
-cudaError_t launch_embed(const bf16* E, const int* row_src, const bf16* embeds, float* x, int R, int d,
+cudaError_t launch_embed(const f16* E, const int* row_src, const bf16* embeds, float* x, int R, int d,
                          cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
   embed_kernel<<<R, 256, 0, st>>>(E, row_src, embeds, x, d);
   return cudaGetLastError();
 }
 
-// ---- RMSNorm: out = bf16(x / sqrt(mean(x^2) + eps) * w) --------------------------------
+// ---- RMSNorm: out = f16(x / sqrt(mean(x^2) + eps) * w) ---------------------------------
 // One warp per row, the row held in registers (one read of x), 8 rows per block; the block
 // stages w in shared memory while its rows load, so no global round trip follows the reduction.
 template <int NV>   // float4 per lane: d = 128 * NV
 __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restrict__ x, const float* __restrict__ w,
-                                                           bf16* __restrict__ out, int R, int d, float eps) {
+                                                           f16* __restrict__ out, int R, int d, float eps) {
   allow_dependents();
   __shared__ float4 ws[32 * NV];
   const float4* wr = reinterpret_cast<const float4*>(w);
@@ -58,8 +62,8 @@ __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restri
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const float4 g = ws[lane + 32 * i];
-    __nv_bfloat162 a = __floats2bfloat162_rn(v[i].x * inv * g.x, v[i].y * inv * g.y);
-    __nv_bfloat162 b = __floats2bfloat162_rn(v[i].z * inv * g.z, v[i].w * inv * g.w);
+    __half2 a = __floats2half2_rn(v[i].x * inv * g.x, v[i].y * inv * g.y);
+    __half2 b = __floats2half2_rn(v[i].z * inv * g.z, v[i].w * inv * g.w);
     uint2 u;
     u.x = *reinterpret_cast<uint32_t*>(&a);
     u.y = *reinterpret_cast<uint32_t*>(&b);
@@ -69,7 +73,7 @@ __global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restri
 
 // General width (d % 4 == 0): one block of norm_row_threads(d) threads per row, two passes.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ w,
-                               bf16* __restrict__ out, int d, float eps) {
+                               f16* __restrict__ out, int d, float eps) {
   allow_dependents();
   wait_prerequisites();
   __shared__ float red[32];
@@ -83,15 +87,15 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, const float* __restr
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)d + eps);
   const float4* wr = reinterpret_cast<const float4*>(w);
-  __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(out + (size_t)r * d);
+  __half2* o2 = reinterpret_cast<__half2*>(out + (size_t)r * d);
   for (int i = threadIdx.x; i < d / 4; i += blockDim.x) {
     float4 v = xr[i], g = wr[i];
-    o2[2 * i] = __floats2bfloat162_rn(v.x * inv * g.x, v.y * inv * g.y);
-    o2[2 * i + 1] = __floats2bfloat162_rn(v.z * inv * g.z, v.w * inv * g.w);
+    o2[2 * i] = __floats2half2_rn(v.x * inv * g.x, v.y * inv * g.y);
+    o2[2 * i + 1] = __floats2half2_rn(v.z * inv * g.z, v.w * inv * g.w);
   }
 }
 
-cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int d, float eps,
+cudaError_t launch_rmsnorm(const float* x, const float* w, f16* out, int R, int d, float eps,
                            cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
   const int blocks = (R + 7) / 8;
@@ -111,15 +115,15 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, bf16* out, int R, int
 }
 
 // ---- RoPE (rotate-half over the whole head) + split of the fused q|k|v projection -------
-// proj row r: [q (Hq*hd) | k (Hkv*hd) | v (Hkv*hd)] fp32. Writes q, k_new, v_new (bf16) at
+// proj row r: [q (Hq*hd) | k (Hkv*hd) | v (Hkv*hd)] fp32. Writes q, k_new, v_new (f16) at
 // packed row r and, for sequences that own a snapshot, K/V into its cache at row = position.
 // Grid (row, item block): one thread per item, items = the (Hq + Hkv) * hd/2 rotated pairs of
 // q and k, then the Hkv * hd values of v (one round trip to memory per thread, so that a few
 // rows still spread over the whole GPU).
 __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const float2* __restrict__ tab,
                                   const int* __restrict__ row_seq, const SeqDesc* __restrict__ seqs,
-                                  const CtxDesc* __restrict__ ctxs, int layer_f, bf16* __restrict__ q,
-                                  bf16* __restrict__ knew, bf16* __restrict__ vnew, int Hq, int Hkv,
+                                  const CtxDesc* __restrict__ ctxs, int layer_f, f16* __restrict__ q,
+                                  f16* __restrict__ knew, f16* __restrict__ vnew, int Hq, int Hkv,
                                   int hd) {
   allow_dependents();
   wait_prerequisites();
@@ -131,8 +135,8 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
   const float* pr = proj + (size_t)r * ld;
   const SeqDesc sd = seqs[row_seq[r]];
   const int pos = sd.pos0 + (r - sd.row0);
-  bf16* kc = nullptr;
-  bf16* vc = nullptr;
+  f16* kc = nullptr;
+  f16* vc = nullptr;
   if (sd.ctx_out >= 0) {
     const CtxDesc c = ctxs[sd.ctx_out];
     const size_t plane = (size_t)c.cap * Hkv * hd;
@@ -146,8 +150,8 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
     const float* src = pr + (isq ? 0 : Hq * hd) + h * hd;
     const float x1 = src[i], x2 = src[i + half];
     const float2 cs = tab[(size_t)pos * half + i];
-    const bf16 y1 = f2bf(x1 * cs.x - x2 * cs.y);
-    const bf16 y2 = f2bf(x2 * cs.x + x1 * cs.y);
+    const f16 y1 = f2h(x1 * cs.x - x2 * cs.y);
+    const f16 y2 = f2h(x2 * cs.x + x1 * cs.y);
     if (isq) {
       q[(size_t)r * Hq * hd + h * hd + i] = y1;
       q[(size_t)r * Hq * hd + h * hd + i + half] = y2;
@@ -158,15 +162,15 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
     }
   } else {
     const int tv = t - (nq + nk);
-    const bf16 v = f2bf(pr[(Hq + Hkv) * hd + tv]);
+    const f16 v = f2h(pr[(Hq + Hkv) * hd + tv]);
     vnew[(size_t)r * Hkv * hd + tv] = v;
     if (vc) vc[tv] = v;
   }
 }
 
 cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab, const int* row_seq,
-                              const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, bf16* q,
-                              bf16* knew, bf16* vnew, int R, int Hq, int Hkv, int hd,
+                              const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, f16* q,
+                              f16* knew, f16* vnew, int R, int Hq, int Hkv, int hd,
                               cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
   const int items = (Hq + Hkv) * (hd / 2) + Hkv * hd;
@@ -199,7 +203,7 @@ cudaError_t launch_rope_table(float2* tab, int max_pos, int hd, double theta, cu
 // One block per question: final RMSNorm of its last row, tied-embedding logits over its
 // option ids (fp32), softmax, argmax, expected level, yes probability and confidences.
 __global__ void readout_kernel(const float* __restrict__ x, const float* __restrict__ fnorm,
-                               const bf16* __restrict__ E, int d, float eps,
+                               const f16* __restrict__ E, int d, float eps,
                                const int* __restrict__ q_row, const int* __restrict__ q_type,
                                const int* __restrict__ opt_off, const int* __restrict__ opt_ids,
                                float* __restrict__ probs, float* __restrict__ stats,
@@ -228,9 +232,9 @@ __global__ void readout_kernel(const float* __restrict__ x, const float* __restr
   __syncthreads();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int m = w; m < n; m += nw) {
-    const bf16* e = E + (size_t)opt_ids[o0 + m] * d;
+    const f16* e = E + (size_t)opt_ids[o0 + m] * d;
     float acc = 0.f;
-    for (int i = lane; i < d; i += 32) acc += hn[i] * bf2f(e[i]);
+    for (int i = lane; i < d; i += 32) acc += hn[i] * h2f(e[i]);
     acc = warp_sum(acc);
     if (lane == 0) {
       z[m] = acc;
@@ -268,7 +272,7 @@ __global__ void readout_kernel(const float* __restrict__ x, const float* __restr
   }
 }
 
-cudaError_t launch_readout(const float* x, const float* final_norm, const bf16* E, int d, float eps,
+cudaError_t launch_readout(const float* x, const float* final_norm, const f16* E, int d, float eps,
                            const int* q_row, const int* q_type, const int* opt_off,
                            const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,
                            int max_opts, float* hn_out, float* z_out, cudaStream_t st) {
@@ -279,7 +283,7 @@ cudaError_t launch_readout(const float* x, const float* final_norm, const bf16* 
   return cudaGetLastError();
 }
 
-// ---- load-time: W' = W + scale * B A (fp32 accumulate, one bf16 rounding) ----------------
+// ---- load-time: W' = W + scale * B A (fp32 accumulate, one f16 rounding) -----------------
 // dst row mapping: plain (dst_row0 + o), or SwiGLU interleave: the gate (half 0) / up
 // (half 1) row o lands at 32*(o/16) + 16*half + o%16 of the packed [2F, in] matrix.
 __device__ __forceinline__ float ld_any(const void* p, int is_bf16, size_t i) {
@@ -289,7 +293,7 @@ __device__ __forceinline__ float ld_any(const void* p, int is_bf16, size_t i) {
 
 __global__ void merge_lora_kernel(const void* __restrict__ W, int w_bf16, const void* __restrict__ A,
                                   const void* __restrict__ B, int ab_bf16, int rank, float scale,
-                                  int out_f, int in_f, bf16* __restrict__ dst, int dst_row0,
+                                  int out_f, int in_f, f16* __restrict__ dst, int dst_row0,
                                   int interleave, int half) {
   const int o = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -302,12 +306,12 @@ __global__ void merge_lora_kernel(const void* __restrict__ W, int w_bf16, const 
     acc = fmaf(scale, t, acc);
   }
   const int drow = interleave ? (32 * (o / 16) + 16 * half + (o % 16)) : (dst_row0 + o);
-  dst[(size_t)drow * in_f + i] = __float2bfloat16_rn(acc);
+  dst[(size_t)drow * in_f + i] = __float2half_rn(acc);
 }
 
 cudaError_t launch_merge_lora(const void* W, int w_is_bf16, const void* A, const void* B,
                               int ab_is_bf16, int rank, float scale, int out_f, int in_f,
-                              bf16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,
+                              f16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,
                               int swiglu_F, float* tmpA, float* tmpB, cudaStream_t st) {
   (void)swiglu_F; (void)tmpA; (void)tmpB;
   if (interleave_swiglu && out_f > 65535) return cudaErrorNotSupported;

@@ -60,14 +60,14 @@ int s1_op_gemm(const void* X, const void* W, int32_t M, int32_t N, int32_t K, in
     OCK(cudaMemsetAsync(err, 0, 256, st));
     LaunchCtx lc{st, err, sms, nullptr};
     lc.variant = impl == 2 ? GEMM_PAIR : (impl == 3 ? GEMM_SINGLE : GEMM_ANY);
-    OCK(launch_gemm_tc((const bf16*)X, (const bf16*)W, M, N, K, epi, out, ldo, ws, wsf, lc));
+    OCK(launch_gemm_tc((const f16*)X, (const f16*)W, M, N, K, epi, out, ldo, ws, wsf, lc));
     int h = 0;
     OCK(cudaMemcpyAsync(&h, err, 4, cudaMemcpyDeviceToHost, st));
     OCK(cudaStreamSynchronize(st));
     if (h) return op_fail(S1_ERR_DEVICE_TIMEOUT, "gemm: a bounded device wait gave up");
     return S1_OK;
   }
-  OCK(launch_gemm_simt((const bf16*)X, (const bf16*)W, M, N, K, epi, out, ldo, st));
+  OCK(launch_gemm_simt((const f16*)X, (const f16*)W, M, N, K, epi, out, ldo, st));
   OCK(cudaStreamSynchronize(st));
   return S1_OK;
 }
@@ -113,7 +113,7 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
     int dev = 0, sms = 0;
     OCK(cudaGetDevice(&dev));
     OCK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    OCK(launch_gdn_chunked(proj, ld, R, loga, l2_eps, (bf16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
+    OCK(launch_gdn_chunked(proj, ld, R, loga, l2_eps, (f16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
                            0, maxc, maxc, n_seq, n_seq, err, sms, st, nullptr));
     int herr = 0;
     OCK(cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
@@ -121,7 +121,7 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
     if (herr) return op_fail(S1_ERR_DEVICE_TIMEOUT, "gdn: a bounded device wait gave up");
   } else {
     OCK(launch_gdn_prep(proj, ld, loga, beta, R, H, dk, dv, l2_eps, st));
-    OCK(launch_gdn_scan(proj, ld, loga, beta, (bf16*)out, dseq, n_seq, dctx, 0, H, dk, dv, st));
+    OCK(launch_gdn_scan(proj, ld, loga, beta, (f16*)out, dseq, n_seq, dctx, 0, H, dk, dv, st));
   }
   OCK(cudaStreamSynchronize(st));
   return S1_OK;
@@ -139,7 +139,7 @@ int s1_op_attention(const void* q, const void* k_new, const void* v_new, const v
     seqs[s] = SeqDesc{row0[s], len[s], P, P > 0 ? 0 : -1, -1, 0};
     max_len = len[s] > max_len ? len[s] : max_len;
   }
-  CtxDesc c{nullptr, (bf16*)kv_cache, P, P};
+  CtxDesc c{nullptr, (f16*)kv_cache, P, P};
   Tmp t;
   SeqDesc* dseq = (SeqDesc*)t.get(seqs.size() * sizeof(SeqDesc));
   CtxDesc* dctx = (CtxDesc*)t.get(sizeof(CtxDesc));
@@ -151,7 +151,7 @@ int s1_op_attention(const void* q, const void* k_new, const void* v_new, const v
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   long work_ctas = 0;
   for (int i = 0; i < n_seq; ++i) work_ctas += (long)((len[i] + 63) / 64) * Hq;
-  OCK(launch_attention((const bf16*)q, (const bf16*)k_new, (const bf16*)v_new, (bf16*)out, dseq, n_seq,
+  OCK(launch_attention((const f16*)q, (const f16*)k_new, (const f16*)v_new, (f16*)out, dseq, n_seq,
                        dctx, 0, Hq, Hkv, hd, max_len, P + max_len, work_ctas, sms, st));
   OCK(cudaStreamSynchronize(st));
   return S1_OK;
@@ -160,7 +160,7 @@ int s1_op_attention(const void* q, const void* k_new, const void* v_new, const v
 int s1_op_rmsnorm(const float* x, const float* w, int32_t R, int32_t d, float eps, void* out, void* stream) {
   cudaStream_t st = (cudaStream_t)stream;
   if (R < 0 || d <= 0 || d % 4) return op_fail(S1_ERR_INVALID_ARG, "rmsnorm: bad sizes");
-  OCK(launch_rmsnorm(x, w, (bf16*)out, R, d, eps, st));
+  OCK(launch_rmsnorm(x, w, (f16*)out, R, d, eps, st));
   OCK(cudaStreamSynchronize(st));
   return S1_OK;
 }

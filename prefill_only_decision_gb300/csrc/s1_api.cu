@@ -3,7 +3,7 @@
 // The executor owns the device weights (LoRA merged at load, packed for the fused
 // projections), the per-call scratch, and the launch sequence of one forward pass over
 // packed rows on one stream. A state (prefix snapshot) owns the per-layer gated
-// delta-rule states (fp32) and full-attention K/V (bf16, post-RoPE).
+// delta-rule states (fp32) and full-attention K/V (f16, post-RoPE).
 #include <algorithm>
 #include <climits>
 #include <cstdarg>
@@ -77,25 +77,25 @@ struct Layer {
   int ord;             // index among layers of its kind
   float* attn_norm;
   float* mlp_norm;
-  bf16* w_in;          // packed in-projection
+  f16 * w_in;          // packed in-projection
   int n_in;
-  bf16* w_o;
+  f16 * w_o;
   int k_o;             // in-features of w_o
-  bf16* w_gu;          // [2F, d], gate/up interleaved by 16 rows
-  bf16* w_down;        // [d, F]
+  f16 * w_gu;          // [2F, d], gate/up interleaved by 16 rows
+  f16 * w_down;        // [d, F]
 };
 
 struct Scratch {
   int rows = 0;
   int opt_cap = 0;           // option ids the metadata / output blocks hold
   float* x = nullptr;
-  bf16* xn = nullptr;
+  f16 * xn = nullptr;
   float* proj = nullptr;
-  bf16* mix = nullptr;
-  bf16* h = nullptr;
-  bf16* q = nullptr;
-  bf16* knew = nullptr;
-  bf16* vnew = nullptr;
+  f16 * mix = nullptr;
+  f16 * h = nullptr;
+  f16 * q = nullptr;
+  f16 * knew = nullptr;
+  f16 * vnew = nullptr;
   float* loga = nullptr;
   float* beta = nullptr;
   float* gw = nullptr;       // chunked scan: W rows [R, H, dk]
@@ -117,7 +117,7 @@ struct s1_model {
   int device = 0, num_sms = 0;
   cudaStream_t stream = nullptr;
   void* arena = nullptr;
-  bf16* embed = nullptr;
+  f16* embed = nullptr;          // tied embedding, f16 copy
   float* final_norm = nullptr;
   std::vector<Layer> layers;
   float2* rope_tab = nullptr;
@@ -180,7 +180,7 @@ struct s1_state {
   s1_model* model;
   int P, cap;
   float* S;
-  bf16* KV;
+  f16 * KV;
   void* mem;
 };
 
@@ -250,13 +250,13 @@ int ensure_scratch(s1_model* m, int rows, int n_opts = 0) {
   const size_t R = (size_t)want;
   const int H = s.la_heads > 0 ? s.la_heads : 1;
   sc.x = (float*)take(R * s.d_model * 4);
-  sc.xn = (bf16*)take(R * s.d_model * 2);
+  sc.xn = (f16*)take(R * s.d_model * 2);
   sc.proj = (float*)take(R * m->n_proj * 4);
-  sc.mix = (bf16*)take(R * m->n_mix * 2);
-  sc.h = (bf16*)take(R * s.ffn * 2);
-  sc.q = (bf16*)take(R * (size_t)s.fa_q_heads * s.fa_head_dim * 2 + 256);
-  sc.knew = (bf16*)take(R * (size_t)s.fa_kv_heads * s.fa_head_dim * 2 + 256);
-  sc.vnew = (bf16*)take(R * (size_t)s.fa_kv_heads * s.fa_head_dim * 2 + 256);
+  sc.mix = (f16*)take(R * m->n_mix * 2);
+  sc.h = (f16*)take(R * s.ffn * 2);
+  sc.q = (f16*)take(R * (size_t)s.fa_q_heads * s.fa_head_dim * 2 + 256);
+  sc.knew = (f16*)take(R * (size_t)s.fa_kv_heads * s.fa_head_dim * 2 + 256);
+  sc.vnew = (f16*)take(R * (size_t)s.fa_kv_heads * s.fa_head_dim * 2 + 256);
   sc.loga = (float*)take(R * H * 4);
   sc.beta = (float*)take(R * H * 4);
   sc.gw = (float*)take(R * H * (size_t)std::max(s.la_dk, 1) * 4);
@@ -437,7 +437,7 @@ bool valid_state(const s1_model* m, const s1_state* st) {
 // For a residual-add GEMM, `norm_w` (may be NULL) is the weight of the RMSNorm that follows it;
 // when the GEMM's split-K reduction also forms that norm (into the normed-activation buffer),
 // *normed is set and the caller launches no norm of its own.
-int gemm(s1_model* m, const bf16* X, const bf16* W, int M, int N, int K, int epi, void* out, int ldo,
+int gemm(s1_model* m, const f16* X, const f16* W, int M, int N, int K, int epi, void* out, int ldo,
          const float* norm_w = nullptr, bool* normed = nullptr) {
   ProfScope ps(m, S1_PROF_GEMM, 2.0 * M * N * K, (double)N * K * 2 + (double)M * K * 2);
   if (normed) *normed = false;
@@ -621,7 +621,7 @@ int new_state(s1_model* m, int cap, s1_state** out) {
   st->cap = cap;
   st->mem = mem;
   st->S = (float*)mem;
-  st->KV = (bf16*)((char*)mem + sb);
+  st->KV = (f16*)((char*)mem + sb);
   *out = st;
   return S1_OK;
 }
@@ -846,7 +846,7 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   m->arena = dalloc(total);
   if (!m->arena) return bail(fail(S1_ERR_OOM, "weight arena (%zu bytes) allocation failed", total));
   char* A = (char*)m->arena;
-  m->embed = (bf16*)(A + offs[i_embed]);
+  m->embed = (f16*)(A + offs[i_embed]);
   m->final_norm = (float*)(A + offs[i_fnorm]);
   int ordG = 0, ordF = 0;
   for (int l = 0; l < s.n_layers; ++l) {
@@ -855,12 +855,12 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
     L.ord = L.full ? ordF++ : ordG++;
     L.attn_norm = (float*)(A + offs[li[l * 6 + 0]]);
     L.mlp_norm = (float*)(A + offs[li[l * 6 + 1]]);
-    L.w_in = (bf16*)(A + offs[li[l * 6 + 2]]);
+    L.w_in = (f16*)(A + offs[li[l * 6 + 2]]);
     L.n_in = L.full ? m->n_in_fa : m->n_in_gdn;
-    L.w_o = (bf16*)(A + offs[li[l * 6 + 3]]);
+    L.w_o = (f16*)(A + offs[li[l * 6 + 3]]);
     L.k_o = L.full ? Hq * hd : H * Dv;
-    L.w_gu = (bf16*)(A + offs[li[l * 6 + 4]]);
-    L.w_down = (bf16*)(A + offs[li[l * 6 + 5]]);
+    L.w_gu = (f16*)(A + offs[li[l * 6 + 4]]);
+    L.w_down = (f16*)(A + offs[li[l * 6 + 5]]);
     m->layers.push_back(L);
   }
 
@@ -882,8 +882,8 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
     CK(cudaMemcpy(dev, host, numel * esz, cudaMemcpyHostToDevice));
     return S1_OK;
   };
-  // base matrix [out_f, in_f] (+ optional LoRA pair) -> bf16 at dst
-  auto merge = [&](const void* Wh, int out_f, int in_f, int l, int target, bf16* dst, int row0,
+  // base matrix [out_f, in_f] (+ optional LoRA pair) -> f16 at dst
+  auto merge = [&](const void* Wh, int out_f, int in_f, int l, int target, f16* dst, int row0,
                    int inter, int half) -> int {
     int rc2 = up(Wh, (size_t)out_f * in_f, stage);
     if (rc2) return rc2;
@@ -1155,7 +1155,7 @@ static int prefill_impl(s1_model* m, int n_req, const int32_t* const* tokens, co
         eoff += n_embeds[r] * rowb;
       }
     }
-    return run_forward(m, mt, m->sc.xn, nullptr, nullptr, nullptr);
+    return run_forward(m, mt, reinterpret_cast<const bf16*>(m->sc.xn), nullptr, nullptr, nullptr);
   });
   if (rc) return rc;
   for (int r = 0; r < n_req; ++r) states[r]->P = n_tokens[r] + n_embeds[r];
@@ -1437,7 +1437,7 @@ static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, cons
         eoff += n_embeds[r] * rowb;
       }
     }
-    return run_forward(m, mt, m->sc.xn, d_probs, d_stats, d_hidden, want_lm);
+    return run_forward(m, mt, reinterpret_cast<const bf16*>(m->sc.xn), d_probs, d_stats, d_hidden, want_lm);
   });
   if (rc) return rc;
   for (int r = 0; r < n_req; ++r) states[r]->P = n_tokens[r] + n_embeds[r];

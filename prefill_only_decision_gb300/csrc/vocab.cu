@@ -10,7 +10,7 @@
 namespace s1 {
 
 template <int QG>
-__global__ void __launch_bounds__(256) vocab_lse_kernel(const bf16* __restrict__ E, int V, int d,
+__global__ void __launch_bounds__(256) vocab_lse_kernel(const f16* __restrict__ E, int V, int d,
                                                         const float* __restrict__ hn, int n_q, int rows_per_block,
                                                         float2* __restrict__ part) {
   extern __shared__ float hs[];   // [QG][d] normalised readout rows of the current group
@@ -36,10 +36,10 @@ __global__ void __launch_bounds__(256) vocab_lse_kernel(const bf16* __restrict__
       for (int q = 0; q < QG; ++q) acc[q] = 0.f;
       for (int c = lane; c < d / 8; c += 32) {
         const uint4 e = er[c];
-        const bf16* eb = reinterpret_cast<const bf16*>(&e);
+        const f16* eb = reinterpret_cast<const f16*>(&e);
         float ef[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ef[i] = bf2f(eb[i]);
+        for (int i = 0; i < 8; ++i) ef[i] = h2f(eb[i]);
 #pragma unroll
         for (int q = 0; q < QG; ++q) {
           const float4 h0 = *reinterpret_cast<const float4*>(&hs[q * d + 8 * c]);
@@ -112,7 +112,7 @@ size_t vocab_lm_scratch_floats(int n_q, int n_opts, int d, int num_sms) {
   return (size_t)n_opts + (size_t)n_q * d + blocks * n_q * 2 + 64;
 }
 
-cudaError_t launch_vocab_lm(const bf16* E, int V, int d, const float* hn, const float* z, const int* opt_off, int n_q,
+cudaError_t launch_vocab_lm(const f16* E, int V, int d, const float* hn, const float* z, const int* opt_off, int n_q,
                             float* lm, float* scratch, int num_sms, cudaStream_t st, long* launches) {
   if (n_q <= 0) return cudaSuccess;
   const int blocks = 4 * (num_sms > 0 ? num_sms : 152);

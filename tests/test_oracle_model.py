@@ -262,3 +262,30 @@ def test_bf16_policy_merges_lora_then_rounds():
     x = om.round_bf16(np.random.default_rng(23).standard_normal((3, 32)))
     Wm = W.layers[0][1].astype(np.float64) + 2.0 * W.lora_b[0][0].astype(np.float64) @ W.lora_a[0][0].astype(np.float64)
     np.testing.assert_allclose(o16.linear(x, 0, "q"), x @ om.round_bf16(Wm).astype(np.float64).T, rtol=1e-12)
+
+
+# -- the f16 backbone policy mode (the CUDA path's rounding points) ---------------------------
+def test_round_f16_vs_torch():
+    g = np.random.default_rng(24)
+    x = np.concatenate([g.standard_normal(10000) * 10.0 ** g.integers(-9, 4, 10000),
+                        np.array([1.0, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, -2.5, 0.0, 65504.0, 2.0 ** -24,
+                                  3 * 2.0 ** -26, 6.1e-5])]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(om.round_f16(x), ref)
+    # ties go to the even neighbour: 1 + 2^-11 lies halfway between 1 and 1 + 2^-10
+    assert om.round_f16(np.float32(1.0 + 2.0 ** -11)) == 1.0
+    assert om.round_f16(np.float32(1.0 + 3 * 2.0 ** -11)) == np.float32(1.0 + 2.0 ** -9)
+
+
+def test_f16_policy_merges_lora_then_rounds_and_rounds_inputs():
+    W = _small_lora_weights()
+    o = om.Oracle(W, np.float64, precision="f16")
+    g = np.random.default_rng(25)
+    x = g.standard_normal((3, 32))
+    Wm = W.layers[0][1].astype(np.float64) + 2.0 * W.lora_b[0][0].astype(np.float64) @ W.lora_a[0][0].astype(np.float64)
+    np.testing.assert_allclose(o.linear(x, 0, "q"),
+                               om.round_f16(x).astype(np.float64) @ om.round_f16(Wm).astype(np.float64).T, rtol=1e-12)
+    # the f16 rounding of the merged weight is about eight times finer than bf16's
+    e16 = np.abs(om.round_f16(Wm) - Wm).max()
+    eb = np.abs(om.round_bf16(Wm) - Wm).max()
+    assert 0 < e16 < eb / 4

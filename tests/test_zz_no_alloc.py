@@ -11,7 +11,6 @@ import ctypes as C
 import numpy as np
 import pytest
 
-from prefill_only_decision_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -30,8 +29,8 @@ def L():
     return lib
 
 
-def _bf16(a):
-    return torch.from_numpy(synth.f32_to_bf16_bits(np.asarray(a, np.float32)).view(np.int16)).cuda().view(torch.bfloat16)
+def _f16(a):
+    return torch.from_numpy(np.asarray(a, np.float32).astype(np.float16)).cuda()
 
 
 # (M, N, K, epilogue): includes split-K plans (small M) and the SwiGLU / residual epilogues
@@ -43,10 +42,10 @@ SHAPES = [(144, 2560, 9216, 2), (144, 2560, 2560, 0), (1024, 2560, 2560, 0), (10
 def test_noalloc_gemm_matches_allocating_entry_point(L, M, N, K, epi):
     from prefill_only_decision_gb300 import binding
     g = np.random.default_rng(M + N + K + epi)
-    X = _bf16(g.standard_normal((M, K)))
-    W = _bf16(0.05 * g.standard_normal((N, K)))
+    X = _f16(g.standard_normal((M, K)))
+    W = _f16(0.05 * g.standard_normal((N, K)))
     ncol = N // 2 if epi == 3 else N
-    dt = torch.bfloat16 if epi in (1, 3) else torch.float32
+    dt = torch.float16 if epi in (1, 3) else torch.float32
     base = torch.from_numpy(g.standard_normal((M, ncol)).astype(np.float32)).cuda() if epi == 2 else None
 
     def fresh():
@@ -57,7 +56,7 @@ def test_noalloc_gemm_matches_allocating_entry_point(L, M, N, K, epi):
     torch.cuda.synchronize()
     refn = ref.float().cpu().numpy()
     scale = np.sqrt(K) * 0.05
-    tol = 1e-4 * scale + (np.abs(refn) * 2.0 ** -8 if epi in (1, 3) else 0)
+    tol = 1e-4 * scale + (np.abs(refn) * 2.0 ** -10 if epi in (1, 3) else 0)
 
     def call(out):
         rc = L.s1_op_gemm_noalloc(C.c_void_p(X.data_ptr()), C.c_void_p(W.data_ptr()), M, N, K, epi,
@@ -98,8 +97,8 @@ def test_noalloc_gemm_rejects_oversized_scratch(L):
     if shp is None:
         pytest.skip("no split-K plan on this GPU needs more scratch than the fixed array holds")
     M, N, K = shp
-    X = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
-    W = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    X = torch.zeros((M, K), dtype=torch.float16, device="cuda")
+    W = torch.zeros((N, K), dtype=torch.float16, device="cuda")
     out = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
     rc = L.s1_op_gemm_noalloc(C.c_void_p(X.data_ptr()), C.c_void_p(W.data_ptr()), M, N, K, 0,
                               C.c_void_p(out.data_ptr()), N, None)
