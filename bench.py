@@ -3,7 +3,8 @@
 One step = one request of the workload: prefill a 1024-token state prefix, then decide 3
 questions (choice over 3 labels, score over 4 levels, noul) with 48-token suffixes branched
 from the prefix snapshot -> 3 decisions per step. Weights are seeded random-init of the
-4B-class shape (bf16, rank-32 LoRA merged at load); inputs are seeded synthetic token ids.
+4B-class shape (bf16 weights, rank-32 LoRA merged at load into f16 tensor-core operands); inputs
+are seeded synthetic token ids.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config 4b] [--impl ours|reference]
 
@@ -11,7 +12,8 @@ value  = decisions/s measured on the device (CUDA events on the library's stream
          request's ids already in device memory (stream-ordered API);
 e2e    = decisions/s through the blocking public API (host ids in, host results out,
          host<->device copies inside the timed region), with its p50 latency;
-roofline = the tensor-core GEMM (the dominant kernel) against the measured bf16 peak;
+roofline = the tensor-core GEMM (the dominant kernel) against the measured dense 16-bit peak
+         (cuBLAS bf16 burst; f16 runs at the same nominal tensor-core rate), plus the whole step;
 cpu_baseline = the oracle (numpy, fp32) on a bounded sample of the same workload.
 `--impl reference` times the oracle alone (the reference arm of this comparison).
 Under torchrun (N > 1) every rank runs an independent replica ("replicas only").
@@ -48,6 +50,11 @@ if _impl_arg(sys.argv) == "reference":
 import numpy as np  # noqa: E402
 
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per tensor-core GEMM launch, averaged
+# over one step's GEMM launches in an ncu capture of this bench's timed step, per workload; a
+# workload whose kernels changed since their capture has no entry (the field reads null).
+GEMM_DRAM_BYTES_PER_LAUNCH = {}
 
 
 def load_peaks():
@@ -144,7 +151,8 @@ def dist_setup():
 
 def time_oracle(cfg, W, req, budget_s: float = 25.0):
     """The oracle (as it stands) on a bounded sample: whole questions of the request, each
-    the plain unbranched forward over prefix + suffix, until ~budget_s of CPU time."""
+    the plain unbranched forward over prefix + suffix, until ~budget_s of CPU time. Returns the
+    rate, and the sample's wall time in `seconds`."""
     from oracle import model as om
     o = om.Oracle(W, np.float32)
     t0 = time.perf_counter()
@@ -157,7 +165,7 @@ def time_oracle(cfg, W, req, budget_s: float = 25.0):
     dt = time.perf_counter() - t0
     cores = len(os.sched_getaffinity(0))
     rows = req.prefix_rows + int(np.mean([len(q.suffix) for q in req.questions]))
-    return {"value": n / dt, "unit": "decisions/s", "cores": cores, "kind": "oracle",
+    return {"value": n / dt, "unit": "decisions/s", "cores": cores, "kind": "oracle", "seconds": dt,
             "sample": f"{n} question(s) of request 0, each a full unbranched forward over ~{rows} rows "
                       f"(numpy fp32, {cores} host threads), {dt:.1f} s"}
 
@@ -169,14 +177,16 @@ def run_reference(args, cfg):
     from prefill_only_decision_gb300 import synth
     W = synth.make_weights(cfg)
     req = synth.make_requests(cfg)[0]
-    vals = []
+    runs = []
     for _ in range(args.warmup + args.steps):
-        vals.append(time_oracle(cfg, W, req, budget_s=float(os.environ.get("S1_REF_BUDGET", "10")))["value"])
-    v = float(np.mean(vals[args.warmup:])) if args.steps else float(vals[-1])
-    cb = time_oracle(cfg, W, req, budget_s=1.0)
+        runs.append(time_oracle(cfg, W, req, budget_s=float(os.environ.get("S1_REF_BUDGET", "10"))))
+    timed = runs[args.warmup:] if args.steps else runs[-1:]
+    v = float(np.mean([r["value"] for r in timed]))
+    step_ms = 1000.0 * float(np.mean([r["seconds"] for r in timed]))   # wall time of one timed step
+    cb = dict(timed[-1])
     cb["value"] = v
     line = {"impl": "reference", "metric": "decisions/s", "value": v, "unit": "decisions/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * len(req.questions) / v,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": cfg.name + " (oracle sample)", "prefix_rows": req.prefix_rows,
                        "questions": len(req.questions), "suffix_len": len(req.questions[0].suffix)},
@@ -422,21 +432,24 @@ def main():
     peaks = load_peaks()
     g = prof["gemm"]
     achieved = g["flops"] / (g["ms"] / 1000.0) / 1e12 if g["ms"] > 0 else 0.0
-    peak = peaks["bf16_tflops_sustained"]
+    # the timed region lasts a fraction of a second at full clocks: the burst peak applies; the
+    # GEMMs take f16 operands, whose nominal dense rate equals bf16's (ratio 1)
+    peak = peaks["bf16_tflops"]
     total_prof_ms = sum(v["ms"] for v in prof.values())
-    # DRAM bytes per GEMM launch: the committed per-shape ncu capture of the 4B step's five
-    # projection shapes (profiles/gemm_tc_4b_shapes.md: 62.0 MB per launch, equal to the
-    # algorithmic bytes) predates the current tile set (widths 176/208, CTA pairs), so no
-    # counter figure is claimed for the kernels that run now
-    traffic = None
-    roofline = {"bound": "tensor", "kernel": "gemm_kernel (tcgen05, all projections)", "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None, "traffic": traffic,
-                "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-                "traffic_note": "last capture (earlier tile set): 62.0e6 bytes per launch = algorithmic bytes",
-                "peak_source": f"{peaks['source']} bf16 sustained",
+    step_flops = g["flops"] / max(1, args.steps)
+    traffic = GEMM_DRAM_BYTES_PER_LAUNCH.get(cfg.name)
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel / gemm_pair_kernel (tcgen05, all projections)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None,
+                "traffic": traffic,
+                "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum, "
+                                "mean over the step's GEMM launches)",
+                "algorithmic_bytes_per_launch": g["bytes"] / max(1, g["count"]),
+                "peak_source": f"{peaks['source']} bf16 burst x 1 (f16 operands)",
                 "share_of_step": g["ms"] / total_prof_ms if total_prof_ms else None,
                 "launches_per_step": g["count"] / max(1, args.steps),
-                "flops_per_step": g["flops"] / max(1, args.steps)}
+                "flops_per_step": step_flops,
+                "step_achieved": step_flops / (ms_step / 1000.0) / 1e12,
+                "step_frac": step_flops / (ms_step / 1000.0) / 1e12 / peak if peak else None}
     phase_split = {k: round(v["ms"] / max(1, args.steps), 4) for k, v in prof.items()}
 
     # ---- end to end through the blocking public API (host buffers) ---------------------------
@@ -464,7 +477,7 @@ def main():
 
     line = {"metric": "decisions/s", "value": value, "unit": "decisions/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights and token ids)",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded random-init weights and token ids)",
             "p50_ms": e2e["p50_ms"],
             "config": {"workload": f"{cfg.name}: 1 request, {P}-row state prefix + {n_q} x "
                                    f"{len(req.questions[0].suffix)}-token questions",

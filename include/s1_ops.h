@@ -75,7 +75,8 @@ int s1_gemm_plan(int32_t M, int32_t N, int32_t K, int32_t epi, int32_t num_sms, 
 /* Gated delta rule over packed sequences, per head (Yang, Kautz & Hatamizadeh 2024):
  *   q, k <- L2-normalised (x / sqrt(sum x^2 + l2_eps)), alpha = exp(-softplus(a)),
  *   beta = sigmoid(b), S_t = alpha S_{t-1}(I - beta k k^T) + beta v k^T, o_t = S_t q_t.
- * proj: fp32 [R, 2*H*dk + H*dv + 2*H] rows [q | k | v | a | b] (q, k normalised IN PLACE).
+ * proj: fp32 [R, 2*H*dk + H*dv + 2*H] rows [q | k | v | a | b] (read; the token-by-token path,
+ * taken for head sizes other than 64 and 128, normalises q and k in place).
  * Sequence s covers rows row0[s] .. row0[s]+len[s]-1 (host arrays). S0: device fp32
  * [n_seq, H, dv, dk] initial states or NULL (zero). S_out: device [n_seq, H, dv, dk] final
  * states or NULL. out: f16 [R, H*dv]. */

@@ -109,12 +109,25 @@ cudaError_t launch_gdn_scan(const float* proj, int ld, const float* alpha, const
                             f16* out, const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx,
                             int layer_g, int H, int Dk, int Dv, cudaStream_t st);
 bool gdn_chunked_supported(int H, int Dk, int Dv, int ld);
-cudaError_t launch_gdn_chunked(float* proj, int ld, int R, float* loga, float l2_eps, f16* out,
-                               const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks, int n_chunks,
-                               const CtxDesc* d_ctx, int layer_g, int H, int Dk, int Dv, float* Wbuf, float* Ubuf,
-                               float* Schunk, int n_first, int max_chunks_first, int max_chunks_rest,
-                               int fold_from, int out_fold, int* d_err, int num_sms, cudaStream_t st,
-                               long* launches);
+// Scratch of the chunked gated delta rule (D = dk = dv): per packed row and head, the normalised
+// k, W and Ut (f16 [R, H, D] each); per chunk and head, B = Ut^T K' (fp32 [D, D]), N^T = (W^T K')^T
+// (f16 [D, D]) and the chunk's start state (f16 [D, D]).
+struct GdnBufs {
+  f16* Kn;
+  f16* W;
+  f16* Ut;
+  float* Bc;
+  f16* NT;
+  f16* Srec;
+  size_t n_chunks_cap;
+};
+size_t gdn_row_bytes(int H, int D);     // bytes per packed row
+size_t gdn_chunk_bytes(int H, int D);   // bytes per chunk
+GdnBufs gdn_bufs(void* rows, size_t R, void* per_chunk, size_t n_chunks, int H, int D);
+cudaError_t launch_gdn_chunked(const float* proj, int ld, float* gbuf, float l2_eps, f16* out, const SeqDesc* d_seq,
+                               int n_seq, const ChunkDesc* d_chunks, int n_chunks, const CtxDesc* d_ctx, int layer_g,
+                               int H, int Dk, int Dv, const GdnBufs& bufs, int n_first, int fold_from, int out_fold,
+                               int* d_err, int num_sms, cudaStream_t st, long* launches);
 cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab, const int* row_seq,
                               const SeqDesc* d_seq, const CtxDesc* d_ctx, int layer_f, f16* q,
                               f16* knew, f16* vnew, int R, int Hq, int Hkv, int hd,

@@ -102,19 +102,17 @@ int s1_op_gdn(float* proj, int32_t R, int32_t H, int32_t dk, int32_t dv, float l
   if (nch) OCK(cudaMemcpyAsync(dch, chunks.data(), nch * sizeof(ChunkDesc), cudaMemcpyHostToDevice, st));
   const int ld = 2 * H * dk + H * dv + 2 * H;
   if (gdn_chunked_supported(H, dk, dv, ld)) {   // normalisation and gates inside the chunked kernels
-    float* W = (float*)t.get((size_t)R * H * dk * 4 + 16);
-    float* U = (float*)t.get((size_t)R * H * dv * 4 + 16);
-    float* Sc = (float*)t.get((size_t)(nch + 1) * per * 4);
+    void* rows = t.get((size_t)R * gdn_row_bytes(H, dk) + 16);
+    void* per_chunk = t.get((size_t)nch * gdn_chunk_bytes(H, dk) + 16);
     int* err = (int*)t.get(256);
-    if (!W || !U || !Sc || !err) return op_fail(S1_ERR_OOM, "gdn: temporaries");
+    if (!rows || !per_chunk || !err) return op_fail(S1_ERR_OOM, "gdn: temporaries");
     OCK(cudaMemsetAsync(err, 0, 256, st));
-    int maxc = 0;
-    for (int q = 0; q < n_seq; ++q) maxc = std::max(maxc, (len[q] + GDN_CHUNK - 1) / GDN_CHUNK);
     int dev = 0, sms = 0;
     OCK(cudaGetDevice(&dev));
     OCK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    OCK(launch_gdn_chunked(proj, ld, R, loga, l2_eps, (f16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, W, U, Sc,
-                           0, maxc, maxc, n_seq, n_seq, err, sms, st, nullptr));
+    const GdnBufs gb = gdn_bufs(rows, (size_t)R, per_chunk, (size_t)nch, H, dk);
+    OCK(launch_gdn_chunked(proj, ld, loga, l2_eps, (f16*)out, dseq, n_seq, dch, nch, dctx, 0, H, dk, dv, gb, 0, n_seq,
+                           n_seq, err, sms, st, nullptr));
     int herr = 0;
     OCK(cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
     OCK(cudaStreamSynchronize(st));

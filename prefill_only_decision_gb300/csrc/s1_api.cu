@@ -98,8 +98,7 @@ struct Scratch {
   f16 * vnew = nullptr;
   float* loga = nullptr;
   float* beta = nullptr;
-  float* gw = nullptr;       // chunked scan: W rows [R, H, dk]
-  float* gu = nullptr;       // chunked scan: Ut / U rows [R, H, dv]
+  void* gdn = nullptr;       // chunked scan, per row: normalised k, W, Ut (f16 [R, H, dk] each)
   int* meta = nullptr;       // row_src | row_seq | seqs | ctxs | readout metadata
   size_t meta_bytes = 0;
   float* ws = nullptr;       // split-K workspace
@@ -126,7 +125,7 @@ struct s1_model {
   Scratch sc;
   float* lm_buf = nullptr;     // full-vocabulary option log-probabilities: lm | z | h_hat | partials
   size_t lm_floats = 0;
-  float* schunk = nullptr;     // chunk-start states of the chunked scan [chunks, H, dv, dk]
+  void* schunk = nullptr;      // chunked scan, per chunk: B, N^T and the start state ([chunks, H, dk, dk])
   size_t schunk_chunks = 0;
   void* tune_flush = nullptr;  // GEMM autotuner: L2-flush buffer (allocated with the model)
   size_t tune_flush_bytes = 0;
@@ -259,8 +258,7 @@ int ensure_scratch(s1_model* m, int rows, int n_opts = 0) {
   sc.vnew = (f16*)take(R * (size_t)s.fa_kv_heads * s.fa_head_dim * 2 + 256);
   sc.loga = (float*)take(R * H * 4);
   sc.beta = (float*)take(R * H * 4);
-  sc.gw = (float*)take(R * H * (size_t)std::max(s.la_dk, 1) * 4);
-  sc.gu = (float*)take(R * H * (size_t)std::max(s.la_dv, 1) * 4);
+  sc.gdn = take(R * gdn_row_bytes(H, std::max(s.la_dk, 1)));
   const int max_seq = want, max_ctx = want, max_q = want;
   const int max_opt = std::max(64 * want, std::max(n_opts, m->sc.opt_cap));
   sc.opt_cap = max_opt;
@@ -271,7 +269,7 @@ int ensure_scratch(s1_model* m, int rows, int n_opts = 0) {
   sc.out_floats = (size_t)max_opt + (size_t)max_q * S1_STAT_COUNT + (size_t)max_q * s.d_model;
   sc.out = (float*)take(sc.out_floats * 4);
   for (void* p : {(void*)sc.x, (void*)sc.xn, (void*)sc.proj, (void*)sc.mix, (void*)sc.h, (void*)sc.q,
-                  (void*)sc.knew, (void*)sc.vnew, (void*)sc.loga, (void*)sc.beta, (void*)sc.gw, (void*)sc.gu,
+                  (void*)sc.knew, (void*)sc.vnew, (void*)sc.loga, (void*)sc.beta, sc.gdn,
                   (void*)sc.meta,
                   (void*)sc.ws, (void*)sc.out}) {
     if (!p) {
@@ -303,7 +301,6 @@ struct Meta {
   std::vector<int> q_row, q_type, opt_off, opt_ids;
   int max_len = 0, max_opts = 0;
   int n_first = 0;   // fused sweep: the first n_first sequences (prefixes) scan before the rest
-  int max_chunks_first = 0, max_chunks_rest = 0;   // longest sequence (in chunks) of each group
   // sequences from fold_from on are handled by their prefixes' state pass, sequences from
   // out_fold on by the output kernel alone (see build_chunks)
   int fold_from = 0;
@@ -325,19 +322,17 @@ void build_chunks(Meta& mt) {
     sd.chunk0 = (int)mt.chunks.size();
     for (int c = 0; c < sd.len; c += GDN_CHUNK)
       mt.chunks.push_back(ChunkDesc{sd.row0 + c, std::min(GDN_CHUNK, sd.len - c), (int)s});
-    const int nc = (sd.len + GDN_CHUNK - 1) / GDN_CHUNK;
-    int& mx = ((int)s < mt.n_first) ? mt.max_chunks_first : mt.max_chunks_rest;
-    mx = std::max(mx, nc);
   }
   // Fused sweep: when every later sequence is a single chunk that keeps no state and continues
-  // a prefix of this call (contiguously per prefix), the prefixes' state pass also produces the
-  // later sequences' U and chunk-start states, and they get no state pass of their own.
+  // a prefix of this call (contiguously per prefix), the prefixes' state pass also records the
+  // later sequences' start states, and they get no state pass of their own.
   const int n = (int)mt.seqs.size();
   mt.fold_from = n;
   mt.out_fold = n;
   if (mt.n_first <= 0 || mt.n_first >= n) {
     // one group (e.g. questions over snapshots): if every sequence is a single chunk that keeps
-    // no state, the output kernel forms each chunk's U from its start state and no state pass runs
+    // no state, the output kernel reads each chunk's start state from its snapshot and no state
+    // pass runs
     bool all = true;
     for (int s = 0; s < n && all; ++s)
       if (mt.seqs[s].len > GDN_CHUNK || mt.seqs[s].ctx_out >= 0) all = false;
@@ -359,11 +354,6 @@ void build_chunks(Meta& mt) {
     }
     if (ok) {
       mt.fold_from = mt.n_first;
-      for (int p = 0; p < mt.n_first; ++p) {
-        const SeqDesc& ps = mt.seqs[p];
-        const int nf = ps.fol1 > ps.fol0 ? ps.fol1 - ps.fol0 : 0;
-        mt.max_chunks_first = std::max(mt.max_chunks_first, (ps.len + GDN_CHUNK - 1) / GDN_CHUNK + nf);
-      }
     } else {
       for (int p = 0; p < mt.n_first; ++p) mt.seqs[p].fol0 = mt.seqs[p].fol1 = 0;
     }
@@ -512,14 +502,14 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
             drop_graphs(m);
             dfree(m->schunk);
             const size_t cap = std::max<size_t>(nch, 2 * m->schunk_chunks);
-            m->schunk = (float*)dalloc(cap * H * (size_t)s.la_dv * s.la_dk * 4);
+            m->schunk = dalloc(cap * gdn_chunk_bytes(H, s.la_dk));
             m->schunk_chunks = m->schunk ? cap : 0;
             if (!m->schunk) return fail(S1_ERR_OOM, "chunk-state buffer (%zu chunks) allocation failed", cap);
           }
-          CK(launch_gdn_chunked(sc.proj, L.n_in, R, sc.loga, s.l2_eps, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
-                                mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, sc.gw, sc.gu, m->schunk, mt.n_first,
-                                mt.max_chunks_first, mt.max_chunks_rest, mt.fold_from, mt.out_fold, m->d_err,
-                                m->num_sms, st, &m->launches));
+          const GdnBufs gb = gdn_bufs(sc.gdn, (size_t)sc.rows, m->schunk, m->schunk_chunks, H, s.la_dk);
+          CK(launch_gdn_chunked(sc.proj, L.n_in, sc.loga, s.l2_eps, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
+                                mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, gb, mt.n_first, mt.fold_from, mt.out_fold,
+                                m->d_err, m->num_sms, st, &m->launches));
         } else {
           CK(launch_gdn_prep(sc.proj, L.n_in, sc.loga, sc.beta, R, H, s.la_dk, s.la_dv, s.l2_eps, st));
           m->launches += 1;

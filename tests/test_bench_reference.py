@@ -5,6 +5,7 @@ import os
 import socket
 import subprocess
 import sys
+import time
 
 import pytest
 
@@ -32,11 +33,15 @@ def _check(line, n_gpus):
 
 
 def test_reference_arm_single_process():
+    t0 = time.time()
     r = subprocess.run([sys.executable, *ARGS], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    wall = time.time() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check(lines[0], 1)
+    # ms_per_step is the measured wall time of a timed step: the steps fit inside the run
+    assert 0 < lines[0]["steps"] * lines[0]["ms_per_step"] <= 1000.0 * wall
 
 
 def test_reference_arm_under_torchrun_prints_once():
