@@ -13,15 +13,16 @@
 //
 // With U substituted, a chunk's state step is affine in its start state:
 //   S_next = gamma_n S0 - S0 N + B,    N = W^T K' [Dk, Dk],   B = Ut^T K' [Dv, Dk]
-// N and B depend on the chunk's own rows only, so they are formed in parallel with the rest of
-// the chunk's algebra, and the pass that has to run chunk after chunk is one [16, Dk] x [Dk, Dk]
-// product per 16 state rows and chunk (the state itself stays fp32, in registers).
+// N depends on the chunk's own rows only, so chunk_prep forms it in parallel with the rest of
+// the chunk's algebra; B is formed by the state pass off its critical path. What has to run
+// chunk after chunk is one [16, Dk] x [Dk, Dk] product per 16 state rows and chunk (the state
+// itself stays fp32, in registers).
 //
 // Launches per layer (the gates and the q/k L2 norms are formed inside them):
 //   chunk_prep  (chunk, head)             gates, k norm, g, A, forward substitution for W and
-//                                         Ut, then N and B                         (parallel)
-//   chunk_state (sequence, head, 16 rows) S <- gamma_n S - S N + B per chunk; records every
-//                                         chunk's start state                    (sequential)
+//                                         Ut, then K' and N^T                      (parallel)
+//   chunk_state (sequence, head, 16 rows) S <- gamma_n S + Ut^T K' - S N per chunk; records
+//                                         every chunk's start state             (sequential)
 //   chunk_out   (chunk, head, v slice)    q norm, P, U = Ut - W S_c^T, O = gamma Q S_c^T + P U
 //                                                                                 (parallel)
 // Single-chunk sequences that keep no state need no state step: in a one-sweep call the
@@ -37,7 +38,7 @@ namespace gc {
 
 constexpr int C = 64;      // chunk rows
 constexpr int BV = 16;     // state rows per state-pass CTA
-constexpr int NS = 4;      // N tiles in flight per state-pass CTA
+constexpr int NS = 3;      // chunk tiles in flight per state-pass CTA
 // D = dk = dv (64 or 128) is a template parameter of every kernel.
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -102,7 +103,8 @@ __device__ __forceinline__ float4 ld4(const float* src, bool ok) {
 // ---------------------------------------------------------------------------------------
 // chunk_prep: one CTA per (chunk, head), 256 threads (8 warps), two CTAs per SM.
 // Writes g (within-chunk cumsum of log alpha), the normalised k, W and Ut (f16 [R, H, D]) and,
-// when a state pass takes a step over this chunk, N^T and B ([chunks, H, D, D]).
+// when a state pass takes a step over this chunk, K' (f16 [R, H, D]), N^T (f16 [chunks, H, D, D])
+// and gamma_n.
 // The unit-lower-triangular system (I + A) X = [diag(beta gamma) K | diag(beta) V] is solved in
 // 16-row blocks: each 16 x 16 diagonal block's inverse comes from the nilpotent series
 // (I + N)^-1 = (I - N)(I + N^2)(I + N^4)(I + N^8) (N strictly lower, N^16 = 0) in fp32, then
@@ -364,22 +366,33 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
   }
   if (tid < n) gout[(size_t)(cd.row0 + tid) * H + h] = s.g[tid];
   if (!need_nb) return;
-  // ---- K'_t = exp(g_n - g_t) k_t (into the series scratch, no longer read)
+  // ---- K'_t = exp(g_n - g_t) k_t (into the series scratch, no longer read, and to global), gamma_n
   {
     const float gl = s.g[n - 1];
-    for (int i = tid; i < C * (D / 2); i += 256) {
-      const int rr = i / (D / 2), c = (i % (D / 2)) * 2;
+    for (int i = tid; i < C * (D / 8); i += 256) {
+      const int rr = i / (D / 8), c = (i % (D / 8)) * 8;
       const float e = rr < n ? __expf(gl - s.g[rr]) : 0.f;
-      const float2 k = __half22float2(*reinterpret_cast<const __half2*>(&s.Kh[rr * SK + c]));
-      *reinterpret_cast<uint32_t*>(&s.u.Kp[rr * SK + c]) = h2u(k.x * e, k.y * e);
+      const uint4 kq = *reinterpret_cast<const uint4*>(&s.Kh[rr * SK + c]);
+      const __half2* kh = reinterpret_cast<const __half2*>(&kq);
+      uint32_t w[4];
+#pragma unroll
+      for (int e2 = 0; e2 < 4; ++e2) {
+        const float2 k = __half22float2(kh[e2]);
+        w[e2] = h2u(k.x * e, k.y * e);
+      }
+      const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(&s.u.Kp[rr * SK + c]) = v;
+      if (rr < n) *reinterpret_cast<uint4*>(bufs.Kp + ((size_t)(cd.row0 + rr) * H + h) * D + c) = v;
     }
+    if (tid == 0) bufs.gam[(size_t)ci * H + h] = __expf(gl);
   }
   __syncthreads();
-  // ---- N^T = K'^T W and B = Ut^T K' ([D, D] each); warp -> m-tile, NPW n-tiles
+  // ---- N^T = K'^T W ([D, D]); warp -> m-tile, NPW n-tiles; staged in shared memory (over the
+  // normalised k and X, no longer read) and written out in 16-byte pieces
   {
-    constexpr int MT = D / 16, NG = 8 / MT, NPW = (D / 8) / NG;
+    constexpr int MT = D / 16, NG = 8 / MT, NPW = (D / 8) / NG, SN = D + 8;
+    static_assert(D * SN * 2 <= (int)(sizeof(s.Kh) + sizeof(s.X)), "N^T staging exceeds the free space");
     const int m0 = (warp % MT) * 16, n0 = (warp / MT) * NPW * 8;
-    const size_t base = ((size_t)ci * H + h) * D * D;
     float acc[NPW][4];
 #pragma unroll
     for (int j = 0; j < NPW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
@@ -395,30 +408,19 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
         mma16(acc[j + 1], a, b[2], b[3]);
       }
     }
+    __syncthreads();   // every warp has read X and K'
+    __half* stg = s.Kh;
 #pragma unroll
     for (int j = 0; j < NPW; ++j) {
       const int c = n0 + j * 8 + 2 * tq;
-      *reinterpret_cast<uint32_t*>(bufs.NT + base + (size_t)(m0 + gq) * D + c) = h2u(acc[j][0], acc[j][1]);
-      *reinterpret_cast<uint32_t*>(bufs.NT + base + (size_t)(m0 + gq + 8) * D + c) = h2u(acc[j][2], acc[j][3]);
-      acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      *reinterpret_cast<uint32_t*>(&stg[(m0 + gq) * SN + c]) = h2u(acc[j][0], acc[j][1]);
+      *reinterpret_cast<uint32_t*>(&stg[(m0 + gq + 8) * SN + c]) = h2u(acc[j][2], acc[j][3]);
     }
-#pragma unroll
-    for (int k = 0; k < C; k += 16) {
-      uint32_t a[4];
-      lda_t(s.X + D, SX, m0, k, lane, a);
-#pragma unroll
-      for (int j = 0; j < NPW; j += 2) {
-        uint32_t b[4];
-        ldb_kn2(s.u.Kp, SK, n0 + j * 8, k, lane, b);
-        mma16(acc[j], a, b[0], b[1]);
-        mma16(acc[j + 1], a, b[2], b[3]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NPW; ++j) {
-      const int c = n0 + j * 8 + 2 * tq;
-      *reinterpret_cast<float2*>(bufs.Bc + base + (size_t)(m0 + gq) * D + c) = make_float2(acc[j][0], acc[j][1]);
-      *reinterpret_cast<float2*>(bufs.Bc + base + (size_t)(m0 + gq + 8) * D + c) = make_float2(acc[j][2], acc[j][3]);
+    __syncthreads();
+    f16* dst = bufs.NT + ((size_t)ci * H + h) * D * D;
+    for (int i = tid; i < D * (D / 8); i += 256) {
+      const int rr = i / (D / 8), c = (i % (D / 8)) * 8;
+      *reinterpret_cast<uint4*>(dst + (size_t)rr * D + c) = *reinterpret_cast<const uint4*>(&stg[rr * SN + c]);
     }
   }
 }
@@ -426,15 +428,22 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
 // ---------------------------------------------------------------------------------------
 // chunk_state: one CTA per (sequence, head, block of 16 state rows), D / 8 warps; warp w keeps
 // columns [8w, 8w + 8) of the block's fp32 state in registers (one m16n8 accumulator). Per
-// chunk: S <- gamma_n S + B - Sr N, Sr the f16 copy of S in shared memory (all warps' columns,
-// the product's A operand). The N^T tiles arrive by TMA into 128-byte-swizzled boxes of 64
-// columns, issued up to NS chunks ahead by one thread; every wait is bounded. Each chunk's
-// start state is recorded (f16) for chunk_out.
+// chunk: S <- gamma_n S + Ut_b^T K' - Sr N, Sr the f16 copy of S in shared memory (all warps'
+// columns, the A operand of the product that depends on the previous chunk), Ut_b the block's
+// 16 columns of Ut. Each chunk's N^T, K' and Ut_b tiles arrive by TMA (one thread issues them
+// up to NS chunks ahead; every wait is bounded); its start state is recorded (f16) for
+// chunk_out.
 template <int D>
 struct StateSmem {
   static constexpr int SR = D + 8;
-  __half NT[NS][D * D];                  // D / 64 boxes of [D rows][64 columns], swizzled
+  static constexpr int NT_BYTES = D * D * 2;       // D / 64 boxes of [D rows][64 columns], swizzled
+  static constexpr int KP_BYTES = C * D * 2;       // D / 64 boxes of [64 rows][64 columns], swizzled
+  static constexpr int UT_BYTES = C * BV * 2;      // [64 rows][16 columns], dense
+  static constexpr int STAGE = NT_BYTES + KP_BYTES + UT_BYTES;
+  static constexpr int GAM = 1024;                 // gamma_n of up to this many chunks at a time
+  uint8_t stage[NS][STAGE];
   __half Sr[2][BV * SR];
+  float gam[GAM];
   uint64_t full[NS];
 };
 
@@ -480,11 +489,22 @@ __device__ __forceinline__ void tma2(void* dst, const CUtensorMap* map, uint64_t
       : "memory");
 }
 
-// mapNT: N^T tiles [n_chunks * H * D rows, D columns] f16, box 64 x D, 128-byte swizzle.
+__device__ __forceinline__ void tma3(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// mapNT: N^T [n_chunks * H * D rows, D columns] f16, box 64 x D, 128-byte swizzle.
+// mapKp: K' [R, H, D] f16 as (D, H, R), box 64 x 1 x 64, 128-byte swizzle.
+// mapUt: Ut [R, H, D] f16 as (D, H, R), box 16 x 1 x 64, no swizzle.
 template <int D>
 __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constant__ CUtensorMap mapNT,
-                                                            const float* __restrict__ Bc,
-                                                            const float* __restrict__ gbuf,
+                                                            const __grid_constant__ CUtensorMap mapKp,
+                                                            const __grid_constant__ CUtensorMap mapUt,
+                                                            const float* __restrict__ gam,
                                                             const SeqDesc* __restrict__ seqs,
                                                             const ChunkDesc* __restrict__ chunks,
                                                             const CtxDesc* __restrict__ ctxs, int layer_g, int H,
@@ -493,7 +513,6 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
   wait_prerequisites();
   using SM = StateSmem<D>;
   constexpr int SR = SM::SR;
-  constexpr uint32_t TILE_BYTES = D * D * 2;
   extern __shared__ __align__(16) uint8_t smraw[];   // (rounded up to 1024 bytes below)
   SM& s = *reinterpret_cast<SM*>((((uintptr_t)smraw) + 1023) & ~(uintptr_t)1023);
   const SeqDesc sd = seqs[blockIdx.x];
@@ -510,17 +529,25 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  int issued = 0;                              // steps whose tile was requested (thread 0)
+  int issued = 0;                              // steps whose tiles were requested (thread 0)
   auto issue = [&](int cl) {
     const int st = cl % NS;
-    bar_expect_tx(&s.full[st], TILE_BYTES);
-    const int y = ((sd.chunk0 + cl) * H + h) * D;
+    uint8_t* sb = s.stage[st];
+    bar_expect_tx(&s.full[st], SM::STAGE);
+    const int ci = sd.chunk0 + cl;
+    const int row0 = sd.row0 + cl * C;         // the chunk's first packed row
 #pragma unroll
-    for (int b = 0; b < D / 64; ++b) tma2(&s.NT[st][b * D * 64], &mapNT, &s.full[st], 64 * b, y);
+    for (int b = 0; b < D / 64; ++b) {
+      tma2(sb + b * D * 128, &mapNT, &s.full[st], 64 * b, (ci * H + h) * D);
+      tma3(sb + SM::NT_BYTES + b * C * 128, &mapKp, &s.full[st], 64 * b, h, row0);
+    }
+    tma3(sb + SM::NT_BYTES + SM::KP_BYTES, &mapUt, &s.full[st], v0, h, row0);
     ++issued;
   };
   if (tid == 0)
     for (int cl = 0; cl < nupd && cl < NS; ++cl) issue(cl);
+  // gamma_n of the first steps
+  for (int i = tid; i < nupd && i < SM::GAM; i += blockDim.x) s.gam[i] = gam[(size_t)(sd.chunk0 + i) * H + h];
   // the state block's fragment: rows v0 + gq and v0 + gq + 8, columns col and col + 1
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   if (sd.ctx_in >= 0) {
@@ -529,16 +556,6 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
     const float2 y = *reinterpret_cast<const float2*>(S0 + (size_t)(v0 + gq + 8) * D + col);
     acc[0] = x.x; acc[1] = x.y; acc[2] = y.x; acc[3] = y.y;
   }
-  // B's fragment and gamma_n of a step (loaded one step ahead)
-  auto fetch = [&](int cl, float* bv, float& gam) {
-    const int ci = sd.chunk0 + cl;
-    const ChunkDesc cd = chunks[ci];
-    gam = __expf(gbuf[(size_t)(cd.row0 + cd.len - 1) * H + h]);
-    const float* bp = Bc + ((size_t)ci * H + h) * DD;
-    const float2 x = *reinterpret_cast<const float2*>(bp + (size_t)(v0 + gq) * D + col);
-    const float2 y = *reinterpret_cast<const float2*>(bp + (size_t)(v0 + gq + 8) * D + col);
-    bv[0] = x.x; bv[1] = x.y; bv[2] = y.x; bv[3] = y.y;
-  };
   // f16 copy of the fragment into Sr[buf], and into the start record of chunk ci (ci >= 0)
   auto put = [&](int buf, int ci) {
     const uint32_t lo = h2u(acc[0], acc[1]), hi = h2u(acc[2], acc[3]);
@@ -550,20 +567,46 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
       *reinterpret_cast<uint32_t*>(rp + (size_t)(v0 + gq + 8) * D + col) = hi;
     }
   };
-  float bcur[4] = {0.f, 0.f, 0.f, 0.f}, gcur = 1.f;
-  if (nupd > 0) fetch(0, bcur, gcur);
   put(0, sd.chunk0);
-  // the first tile; one barrier agrees on its arrival and on Sr being complete
+  // the first tiles; one barrier agrees on their arrival and on Sr and gamma being in place
   bool ok = __syncthreads_and(nupd > 0 ? (bar_wait(&s.full[0], 0) ? 1 : 0) : 1) != 0;
-  int waited = (ok && nupd > 0) ? 1 : 0;     // steps whose tile has arrived
+  int waited = (ok && nupd > 0) ? 1 : 0;     // steps whose tiles have arrived
   int cur = 0;
   for (int cl = 0; cl < nupd && ok; ++cl) {
     const int st = cl % NS;
-    float bnext[4] = {0.f, 0.f, 0.f, 0.f}, gnext = 1.f;
-    if (cl + 1 < nupd) fetch(cl + 1, bnext, gnext);
+    const uint8_t* sb = s.stage[st];
+    const __half* ntile = reinterpret_cast<const __half*>(sb);
+    const uint32_t kp_base = smem_u32(sb + SM::NT_BYTES);
+    const __half* ut = reinterpret_cast<const __half*>(sb + SM::NT_BYTES + SM::KP_BYTES);
+    const int n = min(C, sd.len - cl * C);     // rows of this chunk (later tile rows belong to others)
+    // B block = Ut_b^T K' over this warp's 8 columns (independent of the state): rows t >= n of
+    // the Ut tile are zeroed in the A fragments
+    float q0v[4] = {0.f, 0.f, 0.f, 0.f}, q1v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < C; k += 32) {
+      uint32_t a0[4], a1[4], b[4];
+      lda_t(ut, BV, 0, k, lane, a0);
+      lda_t(ut, BV, 0, k + 16, lane, a1);
+      if (n < C) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t0 = k + ((e >> 1) << 3) + 2 * tq, t1 = t0 + 16;
+          const uint32_t m0 = (t0 < n ? 0x0000FFFFu : 0u) | (t0 + 1 < n ? 0xFFFF0000u : 0u);
+          const uint32_t m1 = (t1 < n ? 0x0000FFFFu : 0u) | (t1 + 1 < n ? 0xFFFF0000u : 0u);
+          a0[e] &= m0;
+          a1[e] &= m1;
+        }
+      }
+      // K' rows k .. k+31 (token), columns of this warp's n-tile; swizzled boxes of 64 columns
+      {
+        const int t = k + lane, c = warp * 8;
+        ldsm4t(kp_base + (uint32_t)((c >> 6) * (C * 128) + t * 128 + ((((c & 63) >> 3) ^ (t & 7)) << 4)), b);
+      }
+      mma16(q0v, a0, b[0], b[1]);
+      mma16(q1v, a1, b[2], b[3]);
+    }
     // Sr (16 x D) x N (D x D) over this warp's 8 columns, in two accumulation chains
     float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-    const __half* ntile = s.NT[st];
 #pragma unroll
     for (int k = 0; k < D; k += 32) {
       uint32_t a0[4], a1[4], b[4];
@@ -573,20 +616,23 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
       mma16(p0, a0, b[0], b[1]);
       mma16(p1, a1, b[2], b[3]);
     }
+    const float g = s.gam[cl % SM::GAM];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = fmaf(gcur, acc[i], bcur[i] - (p0[i] + p1[i]));
+    for (int i = 0; i < 4; ++i) acc[i] = fmaf(g, acc[i], (q0v[i] + q1v[i]) - (p0[i] + p1[i]));
     put(cur ^ 1, cl + 1 < nch ? sd.chunk0 + cl + 1 : -1);
-    // the next step's tile; one barrier agrees on it, on Sr being complete and on this step's
-    // tile having been read by every warp
+    // the next step's tiles; one barrier agrees on them, on Sr being complete and on this step's
+    // tiles having been read by every warp
     const bool w = cl + 1 < nupd ? bar_wait(&s.full[(cl + 1) % NS], ((cl + 1) / NS) & 1) : true;
     ok = __syncthreads_and(w ? 1 : 0) != 0;
     if (!ok) break;
     if (cl + 1 < nupd) ++waited;
     if (tid == 0 && cl + NS < nupd) issue(cl + NS);   // refill the stage this step consumed
     cur ^= 1;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) bcur[i] = bnext[i];
-    gcur = gnext;
+    if ((cl + 1) % SM::GAM == 0 && cl + 1 < nupd) {   // the next block of gamma_n
+      for (int i = tid; i < SM::GAM && cl + 1 + i < nupd; i += blockDim.x)
+        s.gam[i] = gam[(size_t)(sd.chunk0 + cl + 1 + i) * H + h];
+      __syncthreads();
+    }
   }
   if (!ok) {
     // a tile never arrived: wait (bounded) for this CTA's copies in flight, then leave
@@ -801,8 +847,8 @@ bool gdn_chunked_supported(int H, int Dk, int Dv, int ld) {
   return Dk == Dv && (Dk == 64 || Dk == 128) && H > 0 && (ld % 4) == 0;
 }
 
-size_t gdn_row_bytes(int H, int D) { return (size_t)3 * H * D * sizeof(f16); }
-size_t gdn_chunk_bytes(int H, int D) { return (size_t)H * D * D * (2 * sizeof(f16) + sizeof(float)); }
+size_t gdn_row_bytes(int H, int D) { return (size_t)4 * H * D * sizeof(f16); }
+size_t gdn_chunk_bytes(int H, int D) { return (size_t)H * D * D * 2 * sizeof(f16) + (size_t)H * sizeof(float); }
 
 GdnBufs gdn_bufs(void* rows, size_t R, void* per_chunk, size_t n_chunks, int H, int D) {
   GdnBufs b;
@@ -810,10 +856,12 @@ GdnBufs gdn_bufs(void* rows, size_t R, void* per_chunk, size_t n_chunks, int H, 
   b.Kn = (f16*)rows;
   b.W = b.Kn + rn;
   b.Ut = b.W + rn;
+  b.Kp = b.Ut + rn;
   const size_t cn = n_chunks * H * (size_t)D * D;
-  b.Bc = (float*)per_chunk;
-  b.NT = (f16*)(b.Bc + cn);
+  b.NT = (f16*)per_chunk;
   b.Srec = b.NT + cn;
+  b.gam = (float*)(b.Srec + cn);
+  b.rows = R;
   b.n_chunks_cap = n_chunks;
   return b;
 }
@@ -822,13 +870,13 @@ template <int D>
 static constexpr size_t state_smem() { return sizeof(gc::StateSmem<D>) + 1024; }
 
 template <int D>
-static cudaError_t launch_state(const CUtensorMap& mNT, const float* g, const SeqDesc* d_seq, int n_seq,
-                                const ChunkDesc* d_chunks, const CtxDesc* d_ctx, int layer_g, int H,
-                                const GdnBufs& bufs, int* d_err, cudaStream_t st) {
+static cudaError_t launch_state(const CUtensorMap* maps, const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks,
+                                const CtxDesc* d_ctx, int layer_g, int H, const GdnBufs& bufs, int* d_err,
+                                cudaStream_t st) {
   if (n_seq <= 0) return cudaSuccess;
   const dim3 grid(n_seq, H, D / gc::BV);
-  CK_RET(launch_pdl(gc::chunk_state_kernel<D>, grid, dim3(D * 4), state_smem<D>(), st, mNT, bufs.Bc, g, d_seq,
-                    d_chunks, d_ctx, layer_g, H, bufs.Srec, d_err));
+  CK_RET(launch_pdl(gc::chunk_state_kernel<D>, grid, dim3(D * 4), state_smem<D>(), st, maps[0], maps[1], maps[2],
+                    (const float*)bufs.gam, d_seq, d_chunks, d_ctx, layer_g, H, bufs.Srec, d_err));
   return cudaGetLastError();
 }
 
@@ -868,13 +916,20 @@ static cudaError_t launch_chunked_d(const float* proj, int ld, float* gbuf, floa
   }
   CK_RET(launch_pdl(gc::chunk_prep_kernel<D>, dim3(n_chunks, H), dim3(256), sp, st, proj, ld, gbuf, d_chunks, d_seq, H,
                     eps, bufs));
-  // TMA view of the N^T tiles: [n_chunks * H * D rows, D columns] f16, boxes of 64 columns x D rows
-  CUtensorMap mNT;
+  // TMA views of the state pass's tiles: N^T [n_chunks * H * D rows, D columns] (boxes of 64
+  // columns x D rows), K' and Ut [R, H, D] (64 rows of one head: 64-column swizzled boxes of K',
+  // the CTA's 16 columns of Ut)
+  CUtensorMap maps[3];
   {
     const uint64_t dims[2] = {(uint64_t)D, (uint64_t)n_chunks * H * D};
     const uint64_t str[1] = {(uint64_t)D * 2};
     const uint32_t box[2] = {64, (uint32_t)D};
-    if (!tensor_map(&mNT, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, bufs.NT, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const uint64_t dr[3] = {(uint64_t)D, (uint64_t)H, (uint64_t)bufs.rows};
+    const uint64_t sr[2] = {(uint64_t)D * 2, (uint64_t)H * D * 2};
+    const uint32_t bk[3] = {64, 1, (uint32_t)gc::C}, bu[3] = {(uint32_t)gc::BV, 1, (uint32_t)gc::C};
+    if (!tensor_map(&maps[0], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, bufs.NT, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tensor_map(&maps[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, bufs.Kp, dr, sr, bk, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !tensor_map(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, bufs.Ut, dr, sr, bu, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
   // sequences [0, n_first) run before the rest (the rest continue from their states). Sequences
@@ -883,11 +938,11 @@ static cudaError_t launch_chunked_d(const float* proj, int ld, float* gbuf, floa
   // snapshot: neither gets a state pass.
   const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
   const int n1 = std::min(split, std::min(fold_from, out_fold));
-  cudaError_t e = launch_state<D>(mNT, gbuf, d_seq, n1, d_chunks, d_ctx, layer_g, H, bufs, d_err, st);
+  cudaError_t e = launch_state<D>(maps, d_seq, n1, d_chunks, d_ctx, layer_g, H, bufs, d_err, st);
   if (e != cudaSuccess) return e;
   const int n2 = std::min(n_seq, out_fold) - split;
   if (split < n_seq && fold_from > split && n2 > 0) {
-    e = launch_state<D>(mNT, gbuf, d_seq + split, n2, d_chunks, d_ctx, layer_g, H, bufs, d_err, st);
+    e = launch_state<D>(maps, d_seq + split, n2, d_chunks, d_ctx, layer_g, H, bufs, d_err, st);
     if (e != cudaSuccess) return e;
   }
   // value columns split over up to VMAX CTAs while (chunks x heads) CTAs leave SMs idle

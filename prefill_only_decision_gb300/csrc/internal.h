@@ -110,15 +110,17 @@ cudaError_t launch_gdn_scan(const float* proj, int ld, const float* alpha, const
                             int layer_g, int H, int Dk, int Dv, cudaStream_t st);
 bool gdn_chunked_supported(int H, int Dk, int Dv, int ld);
 // Scratch of the chunked gated delta rule (D = dk = dv): per packed row and head, the normalised
-// k, W and Ut (f16 [R, H, D] each); per chunk and head, B = Ut^T K' (fp32 [D, D]), N^T = (W^T K')^T
-// (f16 [D, D]) and the chunk's start state (f16 [D, D]).
+// k, W, Ut and the decayed keys K' (f16 [R, H, D] each); per chunk and head, N^T = (W^T K')^T
+// (f16 [D, D]), the chunk's start state (f16 [D, D]) and its total decay gamma_n (fp32).
 struct GdnBufs {
   f16* Kn;
   f16* W;
   f16* Ut;
-  float* Bc;
+  f16* Kp;
   f16* NT;
   f16* Srec;
+  float* gam;
+  size_t rows;                          // R of the per-row arrays
   size_t n_chunks_cap;
 };
 size_t gdn_row_bytes(int H, int D);     // bytes per packed row
@@ -136,6 +138,16 @@ cudaError_t launch_attention(const f16* q, const f16* knew, const f16* vnew, f16
                              const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx, int layer_f,
                              int Hq, int Hkv, int hd, int max_len, int max_keys, long work_ctas, int num_sms,
                              cudaStream_t st);
+// Attention on tcgen05 (head dims 64 and 128). d_ctx_maps: device array of tensor maps, one per
+// context of the call (attention_ctx_map over its snapshot's K/V; 64-byte aligned entries of
+// attention_ctx_map_bytes() bytes). R: rows of q / knew / vnew.
+bool attention_tc_supported(int hd);
+size_t attention_ctx_map_bytes();
+bool attention_ctx_map(void* map_out, const f16* kv, int n_fa_layers, int P, int cap, int Hkv, int hd);
+cudaError_t launch_attention_tc(const f16* q, const f16* knew, const f16* vnew, f16* out, int R,
+                                const SeqDesc* d_seq, int n_seq, const CtxDesc* d_ctx, const void* d_ctx_maps,
+                                int layer_f, int Hq, int Hkv, int hd, int max_len, int max_keys, long work_ctas,
+                                int num_sms, int* d_err, cudaStream_t st);
 cudaError_t launch_readout(const float* x, const float* final_norm, const f16* E, int d, float eps,
                            const int* q_row, const int* q_type, const int* opt_off,
                            const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,

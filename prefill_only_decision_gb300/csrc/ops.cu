@@ -147,6 +147,30 @@ int s1_op_attention(const void* q, const void* k_new, const void* v_new, const v
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int R = 0;
+  for (int i = 0; i < n_seq; ++i) R = std::max(R, row0[i] + len[i]);
+  const char* ga = getenv("S1_ATTN");   // "sync": the mma.sync kernel (debugging)
+  if (!(ga && strcmp(ga, "sync") == 0) && attention_tc_supported(hd)) {
+    // the tensor-core kernel: the cache as one context of one layer ([2, P, Hkv, hd])
+    long work_ctas = 0;
+    for (int i = 0; i < n_seq; ++i) work_ctas += (long)((len[i] + 127) / 128) * Hq;
+    std::vector<uint8_t> map(attention_ctx_map_bytes(), 0);
+    if (P > 0 && !attention_ctx_map(map.data(), (const f16*)kv_cache, 1, P, P, Hkv, hd))
+      return op_fail(S1_ERR_CUDA, "attention: tensor map encoding failed");
+    void* dmap = t.get(map.size() + 128);
+    int* err = (int*)t.get(256);
+    if (!dmap || !err) return op_fail(S1_ERR_OOM, "attention: temporaries");
+    dmap = (void*)(((uintptr_t)dmap + 127) & ~(uintptr_t)127);
+    OCK(cudaMemcpyAsync(dmap, map.data(), map.size(), cudaMemcpyHostToDevice, st));
+    OCK(cudaMemsetAsync(err, 0, 256, st));
+    OCK(launch_attention_tc((const f16*)q, (const f16*)k_new, (const f16*)v_new, (f16*)out, R, dseq, n_seq, dctx,
+                            dmap, 0, Hq, Hkv, hd, max_len, P + max_len, work_ctas, sms, err, st));
+    int herr = 0;
+    OCK(cudaMemcpyAsync(&herr, err, 4, cudaMemcpyDeviceToHost, st));
+    OCK(cudaStreamSynchronize(st));
+    if (herr) return op_fail(S1_ERR_DEVICE_TIMEOUT, "attention: a bounded device wait gave up");
+    return S1_OK;
+  }
   long work_ctas = 0;
   for (int i = 0; i < n_seq; ++i) work_ctas += (long)((len[i] + 63) / 64) * Hq;
   OCK(launch_attention((const f16*)q, (const f16*)k_new, (const f16*)v_new, (f16*)out, dseq, n_seq,

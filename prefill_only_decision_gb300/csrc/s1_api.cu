@@ -130,6 +130,7 @@ struct s1_model {
   void* tune_flush = nullptr;  // GEMM autotuner: L2-flush buffer (allocated with the model)
   size_t tune_flush_bytes = 0;
   bool gdn_token = false;      // S1_GDN=token: token-by-token scan (debugging)
+  bool attn_sync = false;      // S1_ATTN=sync: mma.sync attention kernel (debugging)
   char* pinned = nullptr;      // host staging for metadata uploads
   size_t pinned_bytes = 0;
   cudaEvent_t meta_done = nullptr;
@@ -221,7 +222,7 @@ namespace {
 size_t meta_bytes_for(int rows, int max_seq, int max_ctx, int max_q, int max_opt) {
   return align_up((size_t)rows * 2 * sizeof(int), 256) + align_up((size_t)max_seq * sizeof(SeqDesc), 256) +
          align_up((size_t)(rows + max_seq) * sizeof(ChunkDesc), 256) +
-         align_up((size_t)max_ctx * sizeof(CtxDesc), 256) +
+         align_up((size_t)max_ctx * sizeof(CtxDesc), 256) + align_up((size_t)max_ctx * attention_ctx_map_bytes(), 256) +
          align_up((size_t)(3 * max_q + 1 + max_opt) * sizeof(int), 256);
 }
 
@@ -310,6 +311,7 @@ struct Meta {
   int* d_row_seq = nullptr;
   SeqDesc* d_seqs = nullptr;
   CtxDesc* d_ctxs = nullptr;
+  void* d_ctx_maps = nullptr;   // attention's tensor map of each context's K/V (tcgen05 path)
   ChunkDesc* d_chunks = nullptr;
   int *d_q_row = nullptr, *d_q_type = nullptr, *d_opt_off = nullptr, *d_opt_ids = nullptr;
 };
@@ -395,6 +397,18 @@ int upload_meta(s1_model* m, Meta& mt, void** dest = nullptr) {
   mt.d_row_seq = (int*)put(mt.row_seq.data(), R * sizeof(int));
   mt.d_seqs = (SeqDesc*)put(mt.seqs.data(), mt.seqs.size() * sizeof(SeqDesc));
   mt.d_ctxs = (CtxDesc*)put(mt.ctxs.data(), mt.ctxs.size() * sizeof(CtxDesc));
+  {
+    // tensor maps over each context's K/V planes for the tcgen05 attention (its P cached rows)
+    const s1_shape& s = m->sh;
+    const size_t mb = attention_ctx_map_bytes();
+    std::vector<uint8_t> maps(mt.ctxs.size() * mb, 0);
+    if (m->nF > 0 && attention_tc_supported(s.fa_head_dim))
+      for (size_t c = 0; c < mt.ctxs.size(); ++c)
+        if (!attention_ctx_map(maps.data() + c * mb, mt.ctxs[c].KV, m->nF, mt.ctxs[c].P, mt.ctxs[c].cap,
+                               s.fa_kv_heads, s.fa_head_dim))
+          return fail(S1_ERR_CUDA, "attention tensor map encoding failed");
+    mt.d_ctx_maps = put(maps.data(), maps.size());
+  }
   mt.d_chunks = (ChunkDesc*)put(mt.chunks.data(), mt.chunks.size() * sizeof(ChunkDesc));
   std::vector<int> rq;
   rq.insert(rq.end(), mt.q_row.begin(), mt.q_row.end());
@@ -465,10 +479,12 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
   Scratch& sc = m->sc;
   cudaStream_t st = m->stream;
   int max_keys = 0;     // longest key range of any sequence (snapshot rows + own rows)
-  long att_tiles = 0;   // query tiles of the attention launches (per head)
+  long att_tiles = 0;   // 64-row query tiles of the attention launches (per head)
+  long att_tiles128 = 0;   // the same in 128-row tiles (the tensor-core kernel's)
   for (const SeqDesc& q : mt.seqs) {
     max_keys = std::max(max_keys, q.len + (q.ctx_in >= 0 ? mt.ctxs[q.ctx_in].P : 0));
     att_tiles += (q.len + 63) / 64;
+    att_tiles128 += (q.len + 127) / 128;
   }
   const size_t plane = (size_t)R * d;
   if (m->trace && (long long)((s.n_layers + 1) * plane) > m->trace_floats)
@@ -531,9 +547,14 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
       }
       {
         ProfScope ps(m, S1_PROF_ATTN, 0, 0);
-        CK(launch_attention(sc.q, sc.knew, sc.vnew, sc.mix, mt.d_seqs, nseq, mt.d_ctxs, L.ord,
-                            s.fa_q_heads, s.fa_kv_heads, s.fa_head_dim, mt.max_len, max_keys,
-                            att_tiles * s.fa_q_heads, m->num_sms, st));
+        if (m->attn_sync || !attention_tc_supported(s.fa_head_dim))
+          CK(launch_attention(sc.q, sc.knew, sc.vnew, sc.mix, mt.d_seqs, nseq, mt.d_ctxs, L.ord,
+                              s.fa_q_heads, s.fa_kv_heads, s.fa_head_dim, mt.max_len, max_keys,
+                              att_tiles * s.fa_q_heads, m->num_sms, st));
+        else
+          CK(launch_attention_tc(sc.q, sc.knew, sc.vnew, sc.mix, R, mt.d_seqs, nseq, mt.d_ctxs, mt.d_ctx_maps,
+                                 L.ord, s.fa_q_heads, s.fa_kv_heads, s.fa_head_dim, mt.max_len, max_keys,
+                                 att_tiles128 * s.fa_q_heads, m->num_sms, m->d_err, st));
         m->launches += 1;
       }
     }
@@ -798,6 +819,8 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   m->force_simt = gi && strcmp(gi, "simt") == 0;
   const char* gd = getenv("S1_GDN");
   m->gdn_token = gd && strcmp(gd, "token") == 0;
+  const char* ga = getenv("S1_ATTN");
+  m->attn_sync = ga && strcmp(ga, "sync") == 0;
   const char* nf = getenv("S1_NORM_FUSE");
   m->fuse_norm = !(nf && strcmp(nf, "0") == 0);
   m->gemm_impl = m->force_simt ? 1 : 0;

@@ -194,9 +194,20 @@ def test_gdn_scan(B, H, D, lens, with_s0):
         np.testing.assert_allclose(gotS[s], S, atol=3e-3 * max(1.0, np.abs(S).max()))
 
 
-@pytest.mark.parametrize("Hq,Hkv,hd,P,lens", [(4, 2, 64, 0, [96]), (16, 4, 128, 0, [300, 17]),
-                                                (16, 4, 128, 1024, [48, 48, 48]), (8, 2, 128, 77, [1, 5, 33])])
-def test_attention(B, Hq, Hkv, hd, P, lens):
+# shapes: a causal prefix, ragged sequences, questions over a 1024-row snapshot, a snapshot whose
+# rows end mid-tile, and few query tiles over long key ranges (key tiles split over a cluster)
+ATTN_SHAPES = [(4, 2, 64, 0, [96]), (16, 4, 128, 0, [300, 17]), (16, 4, 128, 1024, [48, 48, 48]),
+               (8, 2, 128, 77, [1, 5, 33]), (8, 2, 128, 1536, [64]), (40, 8, 128, 600, [64, 130]),
+               (4, 2, 64, 300, [200])]
+
+
+@pytest.mark.parametrize("kernel", ["tcgen05", "sync"])
+@pytest.mark.parametrize("Hq,Hkv,hd,P,lens", ATTN_SHAPES)
+def test_attention(B, Hq, Hkv, hd, P, lens, kernel, monkeypatch):
+    """Both attention kernels (tcgen05 / TMEM / TMA, and the mma.sync one kept for debugging)
+    against softmax(QK^T)V by brute force."""
+    if kernel == "sync":
+        monkeypatch.setenv("S1_ATTN", "sync")
     g = np.random.default_rng(P + Hq)
     R = int(sum(lens))
     q = f16_round(g.standard_normal((R, Hq, hd)))
