@@ -205,17 +205,19 @@ def run_kernel(args):
     g = torch.Generator(device="cuda").manual_seed(0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.kernel == "gemm":
-        # several shapes may be given as "M,N,K,epi;M,N,K,epi" (one measurement pass under ncu)
+        # several shapes may be given as "M,N,K,epi[,impl];..." (one measurement pass under ncu);
+        # impl as s1_op_gemm's: 0 planner's choice, 2 CTA-pair tiles, 3 single-CTA tiles
         shapes = [[int(x) for x in sh.split(",")] for sh in args.shape.split(";")]
         res = []
         for sh in shapes:
             M, N, K = sh[:3]
             epi = sh[3] if len(sh) > 3 else 0
+            impl = sh[4] if len(sh) > 4 else 0
             X = torch.randn((M, K), device="cuda", generator=g).to(torch.float16)
             W = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.float16)
             out = torch.zeros((M, N // 2 if epi == 3 else N), device="cuda",
                               dtype=torch.float16 if epi in (1, 3) else torch.float32)
-            call = lambda: B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), out.shape[1], 0)
+            call = lambda: B.op_gemm(X.data_ptr(), W.data_ptr(), M, N, K, epi, out.data_ptr(), out.shape[1], impl)
             for _ in range(max(1, args.warmup)):
                 call()
             torch.cuda.synchronize()
@@ -275,6 +277,130 @@ def run_kernel(args):
     return 0
 
 
+def run_batch(args, cfg, torch, ws, rank, local):
+    """A batch workload (the small model's 16 requests, the 4B multimodal batch of 8): one step =
+    one s1_prefill_decide_batch_async over every request of the batch (each prefix and its
+    questions in one layer sweep), ids and embedding rows resident in device memory; e2e = the
+    blocking s1_prefill_decide_batch with host buffers."""
+    import ctypes as C
+    from prefill_only_decision_gb300 import binding, replicas, synth
+    W = synth.make_weights(cfg)
+    reqs = synth.make_requests(cfg)
+    stream = torch.cuda.Stream()
+    binding.use_torch_allocator()
+    model = binding.Model(W, stream=stream.cuda_stream)
+    if not args.no_graphs:
+        model.set_graphs(True)
+    states = [model.state_create(r.prefix_rows) for r in reqs]
+    toks = [torch.from_numpy(r.tokens).cuda() for r in reqs]
+    embs = [torch.from_numpy(r.embeds.view(np.int16)).cuda() if r.embeds is not None else None for r in reqs]
+    keep, qarrs = [], []
+    for r in reqs:
+        dq = [(torch.from_numpy(q.suffix).cuda(), torch.from_numpy(q.option_ids).cuda(), q.type) for q in r.questions]
+        keep += dq
+        arr = (binding.Question * len(dq))()
+        for j, (su, op, t) in enumerate(dq):
+            arr[j] = binding.Question(t, C.cast(C.c_void_p(su.data_ptr()), C.POINTER(C.c_int32)), su.numel(),
+                                      C.cast(C.c_void_p(op.data_ptr()), C.POINTER(C.c_int32)), op.numel())
+        qarrs.append(arr)
+    n_q = [len(r.questions) for r in reqs]
+    n_opt = sum(len(q.option_ids) for r in reqs for q in r.questions)
+    d_probs = torch.zeros(n_opt, dtype=torch.float32, device="cuda")
+    d_stats = torch.zeros((sum(n_q), 8), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    dec = sum(n_q)
+
+    def step():
+        model.prefill_decide_batch_async(states, [t.data_ptr() for t in toks], [len(r.tokens) for r in reqs], qarrs,
+                                         n_q, d_probs.data_ptr(), d_stats.data_ptr(), 0,
+                                         [e.data_ptr() if e is not None else 0 for e in embs],
+                                         [0 if r.embeds is None else r.embeds.shape[0] for r in reqs])
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    model.sync()
+    launches0 = model.counters()["launches"]
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        clk.mark_start()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        barrier()
+        clk.mark_end()
+    ms_total = replicas.max_over_ranks(e0.elapsed_time(e1), device="cuda")
+    launches = (model.counters()["launches"] - launches0) // max(1, args.steps)
+    ms_step = ms_total / max(1, args.steps)
+    value = ws * dec * args.steps / (ms_total / 1000.0)
+    model.profile(True)
+    for _ in range(args.steps):
+        step()
+    prof = model.profile_read()
+    model.profile(False)
+    peaks = load_peaks()
+    g = prof["gemm"]
+    peak = peaks["bf16_tflops"]
+    achieved = g["flops"] / (g["ms"] / 1000.0) / 1e12 if g["ms"] > 0 else 0.0
+    total_prof_ms = sum(v["ms"] for v in prof.values())
+    step_flops = g["flops"] / max(1, args.steps)
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel / gemm_pair_kernel (tcgen05, all projections)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None,
+                "traffic": GEMM_DRAM_BYTES_PER_LAUNCH.get(cfg.name),
+                "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum, "
+                                "mean over the step's GEMM launches)",
+                "algorithmic_bytes_per_launch": g["bytes"] / max(1, g["count"]),
+                "peak_source": f"{peaks['source']} bf16 burst x 1 (f16 operands)",
+                "share_of_step": g["ms"] / total_prof_ms if total_prof_ms else None,
+                "launches_per_step": g["count"] / max(1, args.steps), "flops_per_step": step_flops,
+                "step_achieved": step_flops / (ms_step / 1000.0) / 1e12,
+                "step_frac": step_flops / (ms_step / 1000.0) / 1e12 / peak if peak else None}
+    model.sync()
+    c0 = model.counters()
+    lat = []
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        a = time.perf_counter()
+        model.prefill_decide_batch(reqs, want_hidden=False)
+        lat.append((time.perf_counter() - a) * 1000.0)
+    barrier()
+    e2e_s = time.perf_counter() - t0
+    c1 = model.counters()
+    e2e = {"value": ws * dec * args.steps / e2e_s, "unit": "decisions/s",
+           "h2d_bytes_per_step": (c1["h2d_bytes"] - c0["h2d_bytes"]) // max(1, args.steps),
+           "d2h_bytes_per_step": (c1["d2h_bytes"] - c0["d2h_bytes"]) // max(1, args.steps),
+           "p50_ms": float(np.median(lat)), "p95_ms": float(np.percentile(lat, 95))}
+    r0 = reqs[0]
+    line = {"metric": "decisions/s", "value": value, "unit": "decisions/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded random-init weights and token ids)",
+            "p50_ms": e2e["p50_ms"],
+            "config": {"workload": f"{cfg.name}: batch of {len(reqs)} requests, each a {r0.prefix_rows}-row state "
+                                   f"prefix + {len(r0.questions)} x {len(r0.questions[0].suffix)}-token questions",
+                       "model": cfg.name, "decisions_per_step": dec, "parallelism": f"replicas x{ws}",
+                       "cuda_graphs": not args.no_graphs, "path": "fused batch (s1_prefill_decide_batch_async)",
+                       "class_ms_per_step": {k: round(v["ms"] / max(1, args.steps), 4) for k, v in prof.items()}},
+            "roofline": roofline, "clocks": clk.summary(), "gpu_launches": int(launches), "e2e": e2e}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle(cfg, W, r0, budget_s=float(os.environ.get("S1_CPU_BUDGET", "25")))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for s_ in states:
+        s_.close()
+    model.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -304,6 +430,12 @@ def main():
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if cfg.work.n_requests > 1 and cfg.name != "27b":
+        rc = run_batch(args, cfg, torch, ws, rank, local)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return rc
     from prefill_only_decision_gb300 import binding, synth
 
     W = synth.make_weights(cfg)

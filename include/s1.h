@@ -60,7 +60,12 @@ typedef struct s1_state s1_state;
 /* Model shape. Layer l is full attention iff layer_is_full[l] != 0, otherwise a
  * gated delta-rule layer. Requirements: d_model % 64 == 0, ffn % 64 == 0,
  * la_dk == la_dv and la_dk in {64, 128}, fa_head_dim in {64, 128},
- * fa_q_heads % fa_kv_heads == 0. */
+ * fa_q_heads % fa_kv_heads == 0, 0 <= conv_width <= 8.
+ * conv_width > 0 adds the gated delta rule's short convolution (the snapshot's "convolution
+ * history", System1-Omni RFC #114 section 5): each of the q|k|v projection channels of a gated
+ * delta-rule layer is convolved causally over rows with its own conv_width taps, then passed
+ * through SiLU, before the L2 norms; a sequence continues the last conv_width - 1 input rows of
+ * the snapshot it continues (zeros at a sequence start), and a snapshot keeps its own. */
 typedef struct {
   int32_t vocab, d_model, n_layers, ffn;
   int32_t la_heads, la_dk, la_dv;               /* gated delta-rule layers             */
@@ -71,6 +76,7 @@ typedef struct {
   float lora_alpha;                             /* delta scale = lora_alpha/lora_rank  */
   int32_t weight_dtype;                         /* S1_F32 or S1_BF16 host arrays       */
   int32_t max_rows;                             /* rows per forward call; 0 -> 32768   */
+  int32_t conv_width;                           /* 0 = no short convolution            */
 } s1_shape;
 
 /* Host weight arrays, copied at create time (caller keeps ownership).
@@ -78,6 +84,9 @@ typedef struct {
  *   gated delta-rule layer: attn_norm[d], w_q[H*dk,d], w_k[H*dk,d], w_v[H*dv,d],
  *                           w_a[H,d], w_b[H,d], w_o[d,H*dv], mlp_norm[d],
  *                           w_gate[F,d], w_up[F,d], w_down[d,F]            (11 tensors)
+ *                           and, when conv_width > 0, conv[2*H*dk + H*dv, conv_width] (12):
+ *                           channel c's taps, tap j weighting the input row conv_width-1-j
+ *                           rows back (tap conv_width-1 is the current row)
  *   full-attention layer:   attn_norm[d], w_q[Hq*hd,d], w_k[Hkv*hd,d], w_v[Hkv*hd,d],
  *                           w_o[d,Hq*hd], mlp_norm[d], w_gate, w_up, w_down  (9 tensors)
  * lora_a / lora_b: [n_layers*7] pointers, targets in the order q,k,v,o,gate,up,down;
@@ -212,8 +221,18 @@ int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, 
                             const void* d_embeds, int32_t n_embeds, const s1_question* qs_dev,
                             int32_t n_q, float* d_probs, float* d_stats, float* d_last_hidden);
 
-/* CUDA graphs for the stream-ordered calls s1_prefill_async, s1_decide_async and
- * s1_prefill_decide_async (off by default). While enabled, a call whose signature — the
+/* one sweep over a batch (as s1_prefill_decide_batch) into n_req states from s1_state_create:
+ * request r's prefix is d_embeds[r] (bf16 [n_embeds[r], d], device; the arrays may be NULL) then
+ * d_tokens[r] (device ids), its questions qs_dev[r][0 .. n_q[r]) with device id arrays; outputs as
+ * s1_decide_async, concatenated over the requests in order. */
+int s1_prefill_decide_batch_async(s1_model* m, int32_t n_req, s1_state* const* states,
+                                  const int32_t* const* d_tokens, const int32_t* n_tokens,
+                                  const void* const* d_embeds, const int32_t* n_embeds,
+                                  const s1_question* const* qs_dev, const int32_t* n_q, float* d_probs,
+                                  float* d_stats, float* d_last_hidden);
+
+/* CUDA graphs for the stream-ordered calls s1_prefill_async, s1_decide_async,
+ * s1_prefill_decide_async and s1_prefill_decide_batch_async (off by default). While enabled, a call whose signature — the
  * function, the state handle, its buffers and capacity (and, for s1_decide_async, its prefix
  * length), every device pointer, size and question type it passes — repeats an earlier call's
  * is captured once into a CUDA graph (its second occurrence) and later occurrences replay that

@@ -36,7 +36,7 @@ class Shape(C.Structure):
                 ("layer_is_full", C.POINTER(C.c_uint8)),
                 ("rope_theta", C.c_float), ("rms_eps", C.c_float), ("l2_eps", C.c_float),
                 ("lora_rank", C.c_int32), ("lora_alpha", C.c_float), ("weight_dtype", C.c_int32),
-                ("max_rows", C.c_int32)]
+                ("max_rows", C.c_int32), ("conv_width", C.c_int32)]
 
 
 class Weights(C.Structure):
@@ -87,6 +87,8 @@ def lib():
         "s1_prefill_decide_batch": (C.c_int, [vp, i32, P(P(i32)), P(i32), P(vp), P(i32), P(P(Question)), P(i32),
                                               P(P(Result)), P(P(f32)), P(vp)]),
         "s1_prefill_decide_async": (C.c_int, [vp, vp, vp, i32, vp, i32, P(Question), i32, vp, vp, vp]),
+        "s1_prefill_decide_batch_async": (C.c_int, [vp, i32, P(vp), P(vp), P(i32), P(vp), P(i32), P(vp), P(i32),
+                                                    vp, vp, vp]),
         "s1_last_error": (C.c_char_p, []),
         "s1_version": (C.c_char_p, []),
         "s1_op_gemm": (C.c_int, [vp, vp, i32, i32, i32, i32, vp, i32, i32, vp]),
@@ -140,15 +142,14 @@ class Model:
     def __init__(self, weights, max_rows: int = 0, stream: Optional[int] = None):
         L = lib()
         sh = weights.shape
-        if getattr(sh, "conv_width", 0):
-            raise S1Error(S1_ERR_UNSUPPORTED, "the gated delta-rule short convolution is not in the CUDA path")
         self.shape = sh
         full = np.asarray(sh.layer_is_full, dtype=np.uint8)
         self._full = full
         c_shape = Shape(sh.vocab, sh.d_model, sh.n_layers, sh.ffn, sh.la_heads, sh.la_dk, sh.la_dv,
                         sh.fa_q_heads, sh.fa_kv_heads, sh.fa_head_dim,
                         full.ctypes.data_as(C.POINTER(C.c_uint8)), sh.rope_theta, sh.rms_eps, sh.l2_eps,
-                        sh.lora_rank, sh.lora_alpha, S1_BF16 if sh.bf16_weights else S1_F32, max_rows)
+                        sh.lora_rank, sh.lora_alpha, S1_BF16 if sh.bf16_weights else S1_F32, max_rows,
+                        int(getattr(sh, "conv_width", 0)))
         keep = []
 
         def ptr(a):
@@ -297,6 +298,21 @@ class Model:
                                             C.c_void_p(d_embeds) if d_embeds else None, n_embeds, qarr, n_q,
                                             C.c_void_p(d_probs), C.c_void_p(d_stats),
                                             C.c_void_p(d_hidden) if d_hidden else None))
+
+    def prefill_decide_batch_async(self, states, d_tokens, n_tokens, qarrs, n_q, d_probs: int, d_stats: int,
+                                   d_hidden: int = 0, d_embeds=None, n_embeds=None):
+        """s1_prefill_decide_batch_async: per request a state, a device id pointer and count, a
+        Question array with device ids (and optional device embedding rows)."""
+        n = len(states)
+        S = (C.c_void_p * n)(*[s.h for s in states])
+        T = (C.c_void_p * n)(*[C.c_void_p(p) for p in d_tokens])
+        NT = (C.c_int32 * n)(*n_tokens)
+        Q = (C.c_void_p * n)(*[C.cast(q, C.c_void_p) for q in qarrs])
+        NQ = (C.c_int32 * n)(*n_q)
+        E = (C.c_void_p * n)(*[C.c_void_p(p) if p else None for p in d_embeds]) if d_embeds else None
+        NE = (C.c_int32 * n)(*n_embeds) if n_embeds else None
+        check(lib().s1_prefill_decide_batch_async(self.h, n, S, T, NT, E, NE, Q, NQ, C.c_void_p(d_probs),
+                                                  C.c_void_p(d_stats), C.c_void_p(d_hidden) if d_hidden else None))
 
     # -- stream-ordered API (device pointers) -----------------------------------------------
     def state_create(self, capacity_rows: int) -> "State":

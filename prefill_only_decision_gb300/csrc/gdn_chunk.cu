@@ -38,7 +38,7 @@ namespace gc {
 
 constexpr int C = 64;      // chunk rows
 constexpr int BV = 16;     // state rows per state-pass CTA
-constexpr int NS = 3;      // chunk tiles in flight per state-pass CTA
+constexpr int NS = 4;      // chunk tiles in flight per state-pass CTA
 // D = dk = dv (64 or 128) is a template parameter of every kernel.
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -747,6 +747,17 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
   cp_wait<0>();
   __syncthreads();
   const int m0 = (warp & 3) * 16;
+  // warp -> rows m0.., value columns cb .. cb + DW/2 of the slice (NTO n-tiles)
+  const int cb = (warp >> 2) * (DW / 2);
+  const int ta = m0 + gq, tb = m0 + gq + 8;
+  // this thread's Ut values (rows ta, tb; its 2 columns of each n-tile), loaded ahead of use
+  uint32_t utv[NTO][2];
+#pragma unroll
+  for (int nt = 0; nt < NTO; ++nt) {
+    const int c = cs + cb + nt * 8 + 2 * tq;
+    utv[nt][0] = ta < n ? *reinterpret_cast<const uint32_t*>(bufs.Ut + ((size_t)(cd.row0 + ta) * H + h) * D + c) : 0u;
+    utv[nt][1] = tb < n ? *reinterpret_cast<const uint32_t*>(bufs.Ut + ((size_t)(cd.row0 + tb) * H + h) * D + c) : 0u;
+  }
   // P = lower_incl(exp(g_t - g_s) q_t.k_s): warp -> rows m0.., key columns 32*(warp>>2) .. +31
   {
     float acc[4][4] = {};
@@ -776,8 +787,6 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
       *reinterpret_cast<uint32_t*>(&s.P[tb * SP + c]) = h2u(vb0, vb1);
     }
   }
-  // warp -> rows m0.., value columns cb .. cb + DW/2 of the slice (NTO n-tiles)
-  const int cb = (warp >> 2) * (DW / 2);
   // W S^T (before Ut) and O = Q S^T over the slice's value columns
   float u[NTO][4] = {}, o[NTO][4] = {};
 #pragma unroll
@@ -797,7 +806,6 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
       mma16(o[nt], q1, b[2], b[3]);
     }
   }
-  const int ta = m0 + gq, tb = m0 + gq + 8;
   {
     const float ga = __expf(s.g[ta]), gb = __expf(s.g[tb]);
 #pragma unroll
@@ -808,11 +816,8 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
 #pragma unroll
   for (int nt = 0; nt < NTO; ++nt) {
     const int c = cb + nt * 8 + 2 * tq;
-    float2 x = make_float2(0.f, 0.f), y = make_float2(0.f, 0.f);
-    if (ta < n)
-      x = __half22float2(*reinterpret_cast<const __half2*>(bufs.Ut + ((size_t)(cd.row0 + ta) * H + h) * D + cs + c));
-    if (tb < n)
-      y = __half22float2(*reinterpret_cast<const __half2*>(bufs.Ut + ((size_t)(cd.row0 + tb) * H + h) * D + cs + c));
+    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&utv[nt][0]));
+    const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&utv[nt][1]));
     *reinterpret_cast<uint32_t*>(&Us[ta * SU + c]) = h2u(ta < n ? x.x - u[nt][0] : 0.f, ta < n ? x.y - u[nt][1] : 0.f);
     *reinterpret_cast<uint32_t*>(&Us[tb * SU + c]) = h2u(tb < n ? y.x - u[nt][2] : 0.f, tb < n ? y.y - u[nt][3] : 0.f);
   }

@@ -52,6 +52,7 @@ struct CtxDesc {
   f16* KV;      // [n_fa_layers, 2, cap, Hkv, hd] f16
   int P;        // cached rows
   int cap;      // capacity rows
+  float* conv = nullptr;   // short-convolution history [n_gdn_layers, width - 1, channels] fp32
 };
 
 // GEMM kernel families a launch may choose from.
@@ -160,6 +161,15 @@ cudaError_t launch_merge_lora(const void* W, int w_is_bf16, const void* A, const
                               f16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,
                               int swiglu_F, float* tmpA, float* tmpB, cudaStream_t st);
 cudaError_t launch_to_f32(const void* src, int is_bf16, float* dst, size_t n, cudaStream_t st);
+// Short causal convolution of the gated delta-rule layers: out[:, c] = SiLU(sum_j w[c][j] *
+// x[row - (W-1) + j, c]) over the first `channels` columns of each row (q | k | v), the rows
+// before a sequence's start taken from its snapshot's history (ctx_in, else zeros); the a | b
+// columns [channels, ld) are copied. Sequences that write a snapshot (ctx_out) store their last
+// W - 1 input rows as its history. w: fp32 [channels, W]. One launch covers sequences
+// [seq0, seq0 + n_seq); rows of other sequences are left alone.
+cudaError_t launch_short_conv(const float* x, float* out, int ld, int channels, const float* w, int W,
+                              const SeqDesc* d_seq, int seq0, int n_seq, int max_len, const CtxDesc* d_ctx,
+                              int layer_g, cudaStream_t st);
 cudaError_t launch_rope_table(float2* tab, int max_pos, int hd, double theta, cudaStream_t st);
 
 }  // namespace s1

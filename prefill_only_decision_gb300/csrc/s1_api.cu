@@ -83,6 +83,7 @@ struct Layer {
   int k_o;             // in-features of w_o
   f16 * w_gu;          // [2F, d], gate/up interleaved by 16 rows
   f16 * w_down;        // [d, F]
+  float* conv_w;       // gated delta rule's short convolution taps [2*H*dk + H*dv, width] (or NULL)
 };
 
 struct Scratch {
@@ -98,7 +99,8 @@ struct Scratch {
   f16 * vnew = nullptr;
   float* loga = nullptr;
   float* beta = nullptr;
-  void* gdn = nullptr;       // chunked scan, per row: normalised k, W, Ut (f16 [R, H, dk] each)
+  void* gdn = nullptr;       // chunked scan, per row: normalised k, W, Ut, K' (f16 [R, H, dk] each)
+  float* projc = nullptr;    // gated delta rule's in-projection after the short convolution (or NULL)
   int* meta = nullptr;       // row_src | row_seq | seqs | ctxs | readout metadata
   size_t meta_bytes = 0;
   float* ws = nullptr;       // split-K workspace
@@ -181,6 +183,7 @@ struct s1_state {
   int P, cap;
   float* S;
   f16 * KV;
+  float* conv;         // short-convolution history [n_gdn_layers, width - 1, channels] (or NULL)
   void* mem;
 };
 
@@ -260,6 +263,13 @@ int ensure_scratch(s1_model* m, int rows, int n_opts = 0) {
   sc.loga = (float*)take(R * H * 4);
   sc.beta = (float*)take(R * H * 4);
   sc.gdn = take(R * gdn_row_bytes(H, std::max(s.la_dk, 1)));
+  if (s.conv_width > 0 && m->n_in_gdn > 0) {
+    sc.projc = (float*)take(R * m->n_in_gdn * 4);
+    if (!sc.projc) {
+      free_scratch(sc);
+      return fail(S1_ERR_OOM, "scratch allocation for %d rows failed", want);
+    }
+  }
   const int max_seq = want, max_ctx = want, max_q = want;
   const int max_opt = std::max(64 * want, std::max(n_opts, m->sc.opt_cap));
   sc.opt_cap = max_opt;
@@ -508,6 +518,21 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
     if (rc) return rc;
     if (!L.full) {
       const int H = s.la_heads;
+      float* gin = sc.proj;   // the gated delta rule's input rows [q | k | v | a | b]
+      if (L.conv_w) {
+        // short causal convolution + SiLU of q | k | v (prefixes first when the call also
+        // continues them: their snapshots' history is what the later sequences read)
+        ProfScope ps(m, S1_PROF_GDN, 0, 0);
+        const int split = (mt.n_first > 0 && mt.n_first < nseq) ? mt.n_first : nseq;
+        const int ch = 2 * H * s.la_dk + H * s.la_dv;
+        CK(launch_short_conv(sc.proj, sc.projc, L.n_in, ch, L.conv_w, s.conv_width, mt.d_seqs, 0, split, mt.max_len,
+                             mt.d_ctxs, L.ord, st));
+        if (split < nseq)
+          CK(launch_short_conv(sc.proj, sc.projc, L.n_in, ch, L.conv_w, s.conv_width, mt.d_seqs, split, nseq - split,
+                               mt.max_len, mt.d_ctxs, L.ord, st));
+        m->launches += split < nseq ? 2 : 1;
+        gin = sc.projc;
+      }
       {
         ProfScope ps(m, S1_PROF_GDN, 0, 0);
         const int nch = (int)mt.chunks.size();
@@ -523,17 +548,17 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
             if (!m->schunk) return fail(S1_ERR_OOM, "chunk-state buffer (%zu chunks) allocation failed", cap);
           }
           const GdnBufs gb = gdn_bufs(sc.gdn, (size_t)sc.rows, m->schunk, m->schunk_chunks, H, s.la_dk);
-          CK(launch_gdn_chunked(sc.proj, L.n_in, sc.loga, s.l2_eps, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
+          CK(launch_gdn_chunked(gin, L.n_in, sc.loga, s.l2_eps, sc.mix, mt.d_seqs, nseq, mt.d_chunks, nch,
                                 mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, gb, mt.n_first, mt.fold_from, mt.out_fold,
                                 m->d_err, m->num_sms, st, &m->launches));
         } else {
-          CK(launch_gdn_prep(sc.proj, L.n_in, sc.loga, sc.beta, R, H, s.la_dk, s.la_dv, s.l2_eps, st));
+          CK(launch_gdn_prep(gin, L.n_in, sc.loga, sc.beta, R, H, s.la_dk, s.la_dv, s.l2_eps, st));
           m->launches += 1;
           const int split = (mt.n_first > 0 && mt.n_first < nseq) ? mt.n_first : nseq;
-          CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, split, mt.d_ctxs,
+          CK(launch_gdn_scan(gin, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs, split, mt.d_ctxs,
                              L.ord, H, s.la_dk, s.la_dv, st));
           if (split < nseq)
-            CK(launch_gdn_scan(sc.proj, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs + split, nseq - split,
+            CK(launch_gdn_scan(gin, L.n_in, sc.loga, sc.beta, sc.mix, mt.d_seqs + split, nseq - split,
                                mt.d_ctxs, L.ord, H, s.la_dk, s.la_dv, st));
           m->launches += split < nseq ? 2 : 1;
         }
@@ -619,12 +644,19 @@ size_t state_S_floats(const s1_model* m) {
 size_t state_KV_elems(const s1_model* m, int cap) {
   return (size_t)m->nF * 2 * cap * m->sh.fa_kv_heads * m->sh.fa_head_dim;
 }
+// short-convolution history: the last width - 1 input rows of q | k | v per gated delta-rule layer
+size_t state_conv_floats(const s1_model* m) {
+  const s1_shape& s = m->sh;
+  if (s.conv_width <= 1) return 0;
+  return (size_t)m->nG * (s.conv_width - 1) * (2 * s.la_heads * s.la_dk + s.la_heads * s.la_dv);
+}
 
 int new_state(s1_model* m, int cap, s1_state** out) {
   const size_t sb = align_up(state_S_floats(m) * 4, 1024);
   const size_t kb = align_up(state_KV_elems(m, cap) * 2, 1024);
-  void* mem = dalloc(sb + kb);
-  if (!mem) return fail(S1_ERR_OOM, "state allocation (%zu bytes) failed", sb + kb);
+  const size_t cb = align_up(state_conv_floats(m) * 4, 1024);
+  void* mem = dalloc(sb + kb + cb);
+  if (!mem) return fail(S1_ERR_OOM, "state allocation (%zu bytes) failed", sb + kb + cb);
   s1_state* st = new s1_state;
   st->magic = STATE_MAGIC;
   st->model = m;
@@ -633,6 +665,7 @@ int new_state(s1_model* m, int cap, s1_state** out) {
   st->mem = mem;
   st->S = (float*)mem;
   st->KV = (f16*)((char*)mem + sb);
+  st->conv = cb ? (float*)((char*)mem + sb + kb) : nullptr;
   *out = st;
   return S1_OK;
 }
@@ -687,7 +720,7 @@ int build_decide_meta(s1_model* m, int n_req, const s1_state* const* states, con
   int row = 0;
   for (int r = 0; r < n_req; ++r) {
     const s1_state* st = states[r];
-    mt.ctxs.push_back(CtxDesc{st->S, st->KV, st->P, st->cap});
+    mt.ctxs.push_back(CtxDesc{st->S, st->KV, st->P, st->cap, st->conv});
     for (int j = 0; j < n_q[r]; ++j) {
       const s1_question& q = qs[r][j];
       const int sidx = (int)mt.seqs.size();
@@ -728,7 +761,7 @@ int build_prefill_meta(s1_model* m, int n_req, const int32_t* n_tokens, const in
   int row = 0, erow = 0;
   for (int r = 0; r < n_req; ++r) {
     const int P = n_tokens[r] + n_embeds[r];
-    mt.ctxs.push_back(CtxDesc{states[r]->S, states[r]->KV, 0, states[r]->cap});
+    mt.ctxs.push_back(CtxDesc{states[r]->S, states[r]->KV, 0, states[r]->cap, states[r]->conv});
     mt.seqs.push_back(SeqDesc{row, P, 0, -1, r, 0});
     mt.max_len = std::max(mt.max_len, P);
     for (int i = 0; i < P; ++i) mt.row_seq.push_back(r);
@@ -798,6 +831,7 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   if (nF && (s.fa_q_heads <= 0 || s.fa_kv_heads <= 0 || s.fa_q_heads % s.fa_kv_heads ||
              (s.fa_head_dim != 64 && s.fa_head_dim != 128)))
     return fail(S1_ERR_UNSUPPORTED, "attention layers need Hq %% Hkv == 0 and head_dim in {64, 128}");
+  if (s.conv_width < 0 || s.conv_width > 8) return fail(S1_ERR_INVALID_ARG, "shape: conv_width outside [0, 8]");
   if (!w->embed || !w->final_norm || !w->layer) return fail(S1_ERR_INVALID_ARG, "weights: NULL tensor array");
 
   s1_model* m = new s1_model();
@@ -844,17 +878,19 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   };
   const size_t i_embed = reserve((size_t)s.vocab * d * 2);
   const size_t i_fnorm = reserve((size_t)d * 4);
-  std::vector<size_t> li(s.n_layers * 6);
+  std::vector<size_t> li(s.n_layers * 7);
+  const int conv_ch = 2 * H * Dk + H * Dv;   // channels of the short convolution (q | k | v)
   for (int l = 0; l < s.n_layers; ++l) {
     const bool full = m->is_full[l];
     const int n_in = full ? m->n_in_fa : m->n_in_gdn;
     const int k_o = full ? Hq * hd : H * Dv;
-    li[l * 6 + 0] = reserve((size_t)d * 4);
-    li[l * 6 + 1] = reserve((size_t)d * 4);
-    li[l * 6 + 2] = reserve((size_t)n_in * d * 2);
-    li[l * 6 + 3] = reserve((size_t)d * k_o * 2);
-    li[l * 6 + 4] = reserve((size_t)2 * F * d * 2);
-    li[l * 6 + 5] = reserve((size_t)d * F * 2);
+    li[l * 7 + 0] = reserve((size_t)d * 4);
+    li[l * 7 + 1] = reserve((size_t)d * 4);
+    li[l * 7 + 2] = reserve((size_t)n_in * d * 2);
+    li[l * 7 + 3] = reserve((size_t)d * k_o * 2);
+    li[l * 7 + 4] = reserve((size_t)2 * F * d * 2);
+    li[l * 7 + 5] = reserve((size_t)d * F * 2);
+    li[l * 7 + 6] = reserve(!full && s.conv_width > 0 ? (size_t)conv_ch * s.conv_width * 4 : 0);
   }
   m->arena = dalloc(total);
   if (!m->arena) return bail(fail(S1_ERR_OOM, "weight arena (%zu bytes) allocation failed", total));
@@ -866,14 +902,15 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
     Layer L;
     L.full = m->is_full[l];
     L.ord = L.full ? ordF++ : ordG++;
-    L.attn_norm = (float*)(A + offs[li[l * 6 + 0]]);
-    L.mlp_norm = (float*)(A + offs[li[l * 6 + 1]]);
-    L.w_in = (f16*)(A + offs[li[l * 6 + 2]]);
+    L.attn_norm = (float*)(A + offs[li[l * 7 + 0]]);
+    L.mlp_norm = (float*)(A + offs[li[l * 7 + 1]]);
+    L.w_in = (f16*)(A + offs[li[l * 7 + 2]]);
     L.n_in = L.full ? m->n_in_fa : m->n_in_gdn;
-    L.w_o = (f16*)(A + offs[li[l * 6 + 3]]);
+    L.w_o = (f16*)(A + offs[li[l * 7 + 3]]);
     L.k_o = L.full ? Hq * hd : H * Dv;
-    L.w_gu = (f16*)(A + offs[li[l * 6 + 4]]);
-    L.w_down = (f16*)(A + offs[li[l * 6 + 5]]);
+    L.w_gu = (f16*)(A + offs[li[l * 7 + 4]]);
+    L.w_down = (f16*)(A + offs[li[l * 7 + 5]]);
+    L.conv_w = (!L.full && s.conv_width > 0) ? (float*)(A + offs[li[l * 7 + 6]]) : nullptr;
     m->layers.push_back(L);
   }
 
@@ -918,13 +955,14 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
     CK(cudaStreamSynchronize(m->stream));
     return S1_OK;
   };
-  auto norm = [&](const void* host, float* dst) -> int {
-    int rc2 = up(host, d, stage);
+  auto to_f32 = [&](const void* host, size_t n, float* dst) -> int {
+    int rc2 = up(host, n, stage);
     if (rc2) return rc2;
-    CK(launch_to_f32(stage, wb, dst, d, m->stream));
+    CK(launch_to_f32(stage, wb, dst, n, m->stream));
     CK(cudaStreamSynchronize(m->stream));
     return S1_OK;
   };
+  auto norm = [&](const void* host, float* dst) -> int { return to_f32(host, d, dst); };
   rc = merge(w->embed, s.vocab, d, 0, -1, m->embed, 0, 0, 0);
   if (!rc) rc = norm(w->final_norm, m->final_norm);
   size_t t = 0;
@@ -932,7 +970,7 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
     Layer& L = m->layers[l];
     const void* const* T = w->layer + t;
     if (!L.full) {
-      t += 11;
+      t += s.conv_width > 0 ? 12 : 11;
       rc = norm(T[0], L.attn_norm);
       if (!rc) rc = merge(T[1], H * Dk, d, l, 0, L.w_in, 0, 0, 0);
       if (!rc) rc = merge(T[2], H * Dk, d, l, 1, L.w_in, H * Dk, 0, 0);
@@ -944,6 +982,7 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
       if (!rc) rc = merge(T[8], F, d, l, 4, L.w_gu, 0, 1, 0);
       if (!rc) rc = merge(T[9], F, d, l, 5, L.w_gu, 0, 1, 1);
       if (!rc) rc = merge(T[10], d, F, l, 6, L.w_down, 0, 0, 0);
+      if (!rc && L.conv_w) rc = to_f32(T[11], (size_t)conv_ch * s.conv_width, L.conv_w);
     } else {
       t += 9;
       rc = norm(T[0], L.attn_norm);
@@ -1392,7 +1431,7 @@ static int fused_impl(s1_model* m, int n_req, const int32_t* const* tokens, cons
   int row = 0, erow = 0;
   for (int r = 0; r < n_req; ++r) {
     const int P = n_tokens[r] + n_embeds[r];
-    mt.ctxs.push_back(CtxDesc{states[r]->S, states[r]->KV, P, states[r]->cap});
+    mt.ctxs.push_back(CtxDesc{states[r]->S, states[r]->KV, P, states[r]->cap, states[r]->conv});
     mt.seqs.push_back(SeqDesc{row, P, 0, -1, r, 0});
     mt.max_len = std::max(mt.max_len, P);
     for (int i = 0; i < P; ++i) mt.row_seq.push_back(r);
@@ -1539,6 +1578,39 @@ int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, 
                           d_last_hidden, &NQ, &NO, false, cap);
       },
       [&]() { st->P = n_tokens + n_embeds; });
+}
+
+int s1_prefill_decide_batch_async(s1_model* m, int32_t n_req, s1_state* const* states,
+                                  const int32_t* const* d_tokens, const int32_t* n_tokens,
+                                  const void* const* d_embeds, const int32_t* n_embeds,
+                                  const s1_question* const* qs_dev, const int32_t* n_q, float* d_probs,
+                                  float* d_stats, float* d_last_hidden) {
+  if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  if (n_req < 1 || !states || !d_tokens || !n_tokens || !qs_dev || !n_q)
+    return fail(S1_ERR_INVALID_ARG, "bad batch arguments");
+  if (!d_probs || !d_stats) return fail(S1_ERR_INVALID_ARG, "NULL output");
+  std::vector<int32_t> ne(n_req, 0);
+  std::vector<const void*> de(n_req, nullptr);
+  if (n_embeds) ne.assign(n_embeds, n_embeds + n_req);
+  if (d_embeds) de.assign(d_embeds, d_embeds + n_req);
+  CallKey key('B');
+  key.add(n_req).add(d_probs).add(d_stats).add(d_last_hidden);
+  for (int r = 0; r < n_req; ++r) {
+    if (!valid_state(m, states[r])) return fail(S1_ERR_INVALID_HANDLE, "request %d: invalid state", r);
+    if (n_q[r] < 1 || !qs_dev[r]) return fail(S1_ERR_INVALID_ARG, "request %d: no questions", r);
+    key.state(states[r], false).add(d_tokens[r]).add(n_tokens[r]).add(de[r]).add(ne[r]).add(n_q[r]);
+    for (int j = 0; j < n_q[r]; ++j) key.question(qs_dev[r][j]);
+  }
+  return graph_call(
+      m, key,
+      [&](s1_model::Graph* cap) {
+        int NQ = 0, NO = 0;
+        return fused_impl(m, n_req, d_tokens, n_tokens, de.data(), ne.data(), states, qs_dev, n_q, true, d_probs,
+                          d_stats, d_last_hidden, &NQ, &NO, false, cap);
+      },
+      [&]() {
+        for (int r = 0; r < n_req; ++r) states[r]->P = n_tokens[r] + ne[r];
+      });
 }
 
 int s1_set_graphs(s1_model* m, int enable) {

@@ -98,13 +98,13 @@ def test_ops_argument_validation(L):
     assert L.s1_op_rmsnorm(None, None, 4, 30, 1e-6, None, None) == binding.S1_ERR_INVALID_ARG
 
 
-def test_short_convolution_models_are_refused_by_the_cuda_path(L):
-    """The gated delta-rule short convolution exists in the oracle only: the binding refuses such
-    a model before any device work instead of running it without the convolution."""
+def test_short_convolution_width_is_validated(L):
+    """The gated delta-rule short convolution takes widths 0 (none) to 8; a wider one is refused
+    with INVALID_ARG before any device work."""
     from prefill_only_decision_gb300 import binding
     shape = configs.ModelShape(vocab=300, d_model=64, n_layers=4, ffn=64, la_heads=1, la_dk=64, la_dv=64,
-                               fa_q_heads=1, fa_kv_heads=1, fa_head_dim=64, bf16_weights=False, conv_width=4)
+                               fa_q_heads=1, fa_kv_heads=1, fa_head_dim=64, bf16_weights=False, conv_width=9)
     W = synth.make_weights(configs.Config("conv", 0, shape, configs.TINY.work))
     with pytest.raises(binding.S1Error) as e:
         binding.Model(W)
-    assert e.value.code == binding.S1_ERR_UNSUPPORTED
+    assert e.value.code == binding.S1_ERR_INVALID_ARG

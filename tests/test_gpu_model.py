@@ -407,3 +407,103 @@ def test_graphs_two_call_path(B, tiny_weights):
         assert not np.array_equal(replay[0], eager[0])
     finally:
         m.close()
+
+
+# -- the gated delta rule's short convolution (its history continues the snapshot) -------------
+def _conv_config(base, width=4):
+    import dataclasses
+    shape = dataclasses.replace(base.shape, conv_width=width)
+    return configs.Config(base.name + "-conv", base.seed + 100, shape, base.work)
+
+
+def test_tiny_conv_vs_oracle(B):
+    """Tiny model with a width-4 short convolution: the two-call path against the plain
+    unbranched oracle, then the one-sweep call with suffixes shorter than the history (1 and 2
+    rows), a 130-row suffix and prefixes of 1, 2 and 200 rows against the branched oracle."""
+    cfg = _conv_config(configs.TINY)
+    W = synth.make_weights(cfg)
+    req = synth.make_requests(cfg)[0]
+    o = om.Oracle(W, np.float32)
+    m = B.Model(W)
+    try:
+        st = m.prefill(req.tokens)
+        compare(m.decide(st, req.questions), o.decide(req, branched=False), req.questions, "tiny conv")
+        g = np.random.default_rng(9)
+        qs = [synth.random_question(g, 4096, configs.CHOICE, 1, 3), synth.random_question(g, 4096, configs.NOUL, 2, 2),
+              synth.random_question(g, 4096, configs.SCORE, 130, 5)]
+        for P in (1, 2, 200):
+            toks = g.integers(16, 4096, size=P).astype(np.int32)
+            _, caches, PP = o.prefill(toks)
+            ref = o.decide_branched(caches, PP, qs)
+            fused, st2 = m.prefill_decide(synth.Request(toks, None, qs), keep_state=True)
+            compare(fused, ref, qs, f"tiny conv fused P={P}")
+            # the kept snapshot carries the convolution history into later questions
+            compare(m.decide(st2, qs), ref, qs, f"tiny conv decide over snapshot P={P}")
+    finally:
+        m.close()
+
+
+def test_small_conv_batch_vs_oracle(B):
+    """Small model (8 layers, LoRA) with a width-4 short convolution: batched prefill and decide,
+    and the batched one-sweep call, against the oracle on three requests."""
+    cfg = _conv_config(configs.SMALL)
+    W = synth.make_weights(cfg)
+    reqs = synth.make_requests(cfg, n_requests=4)
+    m = B.Model(W)
+    try:
+        states = m.prefill_batch(reqs)
+        gpu = m.decide_batch(states, [r.questions for r in reqs])
+        fused, _ = m.prefill_decide_batch(reqs)
+    finally:
+        m.close()
+    o = om.Oracle(W, np.float32)
+    for i in (0, 3):
+        ref = o.decide(reqs[i], branched=True)
+        compare(gpu[i], ref, reqs[i].questions, f"small conv {i}")
+        compare(fused[i], ref, reqs[i].questions, f"small conv fused {i}")
+
+
+def test_batch_async_one_sweep_matches_blocking_call(B):
+    """s1_prefill_decide_batch_async (device ids, stream-ordered, into states from
+    s1_state_create) gives the blocking s1_prefill_decide_batch's results bit for bit, also when
+    replayed as a CUDA graph."""
+    import ctypes as C
+    cfg = configs.SMALL
+    W = synth.make_weights(cfg)
+    reqs = synth.make_requests(cfg, n_requests=3)
+    s = torch.cuda.Stream()
+    m = B.Model(W, stream=s.cuda_stream)
+    try:
+        ref, _ = m.prefill_decide_batch(reqs)
+        states = [m.state_create(len(r.tokens)) for r in reqs]
+        keep, qarrs = [], []
+        for r in reqs:
+            dq = [(torch.from_numpy(q.suffix.copy()).cuda(), torch.from_numpy(q.option_ids.copy()).cuda(), q.type)
+                  for q in r.questions]
+            keep += dq
+            arr = (B.Question * len(dq))()
+            for j, (su, op, t) in enumerate(dq):
+                arr[j] = B.Question(t, C.cast(C.c_void_p(su.data_ptr()), C.POINTER(C.c_int32)), su.numel(),
+                                    C.cast(C.c_void_p(op.data_ptr()), C.POINTER(C.c_int32)), op.numel())
+            qarrs.append(arr)
+        toks = [torch.from_numpy(r.tokens.copy()).cuda() for r in reqs]
+        n_opt = sum(len(q.option_ids) for r in reqs for q in r.questions)
+        n_q = [len(r.questions) for r in reqs]
+        probs = torch.zeros(n_opt, dtype=torch.float32, device="cuda")
+        stats = torch.zeros((sum(n_q), 8), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        m.set_graphs(True)
+        for rep in range(3):   # eager, capture, replay
+            m.prefill_decide_batch_async(states, [t.data_ptr() for t in toks], [len(r.tokens) for r in reqs], qarrs,
+                                         n_q, probs.data_ptr(), stats.data_ptr())
+            m.sync()
+            p = probs.cpu().numpy()
+            off = 0
+            for r, res in zip(reqs, ref):
+                for q, x in zip(r.questions, res):
+                    np.testing.assert_array_equal(p[off:off + len(q.option_ids)], x["probs"])
+                    off += len(q.option_ids)
+        m.set_graphs(False)
+        assert all(st.rows == len(r.tokens) for st, r in zip(states, reqs))
+    finally:
+        m.close()
