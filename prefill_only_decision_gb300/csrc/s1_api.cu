@@ -845,8 +845,11 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   const int d = s.d_model, F = s.ffn;
   const int H = s.la_heads, Dk = s.la_dk, Dv = s.la_dv;
   const int Hq = s.fa_q_heads, Hkv = s.fa_kv_heads, hd = s.fa_head_dim;
-  m->n_in_gdn = nG ? 2 * H * Dk + H * Dv + 2 * H : 0;
-  m->n_in_fa = nF ? (Hq + 2 * Hkv) * hd : 0;
+  // packed in-projection widths, rounded up to whole 32-column groups (the tensor-core GEMM's
+  // N granule) with zero weight rows; the padding columns of the projection are never read
+  const int in_gdn = 2 * H * Dk + H * Dv + 2 * H, in_fa = (Hq + 2 * Hkv) * hd;
+  m->n_in_gdn = nG ? (in_gdn + 31) / 32 * 32 : 0;
+  m->n_in_fa = nF ? (in_fa + 31) / 32 * 32 : 0;
   m->n_proj = std::max(m->n_in_gdn, m->n_in_fa);
   m->n_mix = std::max(nG ? H * Dv : 0, nF ? Hq * hd : 0);
   const char* gi = getenv("S1_GEMM");
@@ -998,6 +1001,12 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   }
   dfree(stage);
   if (rc) return bail(rc);
+  for (const Layer& L : m->layers) {
+    const int used = L.full ? in_fa : in_gdn;
+    if (L.n_in > used &&
+        cudaMemsetAsync(L.w_in + (size_t)used * d, 0, (size_t)(L.n_in - used) * d * 2, m->stream) != cudaSuccess)
+      return bail(fail(S1_ERR_CUDA, "in-projection padding rows: memset failed"));
+  }
 
   // ---- rotary table, error word
   m->max_pos = 2 * m->sh.max_rows;

@@ -289,3 +289,45 @@ def test_f16_policy_merges_lora_then_rounds_and_rounds_inputs():
     e16 = np.abs(om.round_f16(Wm) - Wm).max()
     eb = np.abs(om.round_bf16(Wm) - Wm).max()
     assert 0 < e16 < eb / 4
+
+
+# -- given embedding rows ahead of the tokens ----------------------------------------------
+def _bf16_table_weights(tiny_weights):
+    """The tiny model with its embedding table rounded to bf16, so that a row of it is exactly
+    representable as a given embedding row (bf16 bits)."""
+    import dataclasses
+    bits = synth.f32_to_bf16_bits(np.asarray(tiny_weights.embed, np.float32))
+    return dataclasses.replace(tiny_weights, embed=bits), bits
+
+
+def test_given_rows_precede_tokens_and_share_positions(tiny_weights, tiny_requests):
+    """Given embedding rows that are exactly the table rows of ids t1, followed by tokens t2, must
+    act as the prompt t1 + t2: the given rows come first, the tokens' positions continue from
+    them (RoPE and causality see one sequence of len(t1) + len(t2) rows), and the rows are used
+    as-is (equality with the table rows leaves no room for a scale). Swapping the order or
+    restarting the tokens' positions at 0 changes the result, which is checked too, so the
+    equality is sensitive to both."""
+    W, bits = _bf16_table_weights(tiny_weights)
+    o = om.Oracle(W, np.float64)
+    r = tiny_requests[0]
+    t1, t2 = r.tokens[:40], r.tokens[40:]
+    given = bits[t1.astype(np.int64)]
+    as_ids = synth.Request(tokens=r.tokens, embeds=None, questions=r.questions)
+    as_rows = synth.Request(tokens=t2, embeds=given, questions=r.questions)
+    assert as_rows.prefix_rows == len(r.tokens)
+    for branched in (True, False):
+        for a, b in zip(o.decide(as_ids, branched), o.decide(as_rows, branched)):
+            np.testing.assert_array_equal(a["probs"], b["probs"])
+            np.testing.assert_array_equal(a["hidden"], b["hidden"])
+    # the row order is observable: the same rows with the given block placed after the tokens
+    x_first = o.embed_rows(t2, given)
+    x_ids = o.embed_rows(r.tokens, None)
+    np.testing.assert_array_equal(x_first, x_ids)
+    h_ids, _ = o.forward(x_ids, np.arange(len(x_ids)))
+    x_last = np.concatenate([x_ids[40:], x_ids[:40]])
+    h_last, _ = o.forward(x_last, np.arange(len(x_last)))
+    assert np.abs(h_last[-1] - h_ids[-1]).max() > 1e-3
+    # so is the numbering: tokens restarting at position 0 after the given rows
+    pos_restart = np.concatenate([np.arange(40), np.arange(len(t2))])
+    h_restart, _ = o.forward(x_ids, pos_restart)
+    assert np.abs(h_restart[-1] - h_ids[-1]).max() > 1e-3
