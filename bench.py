@@ -214,14 +214,20 @@ def run_kernel(args):
     g = torch.Generator(device="cuda").manual_seed(0)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.kernel == "gemm":
-        # several shapes may be given as "M,N,K,epi[,impl];..." (one measurement pass under ncu);
-        # impl as s1_op_gemm's: 0 planner's choice, 2 CTA-pair tiles, 3 single-CTA tiles
+        # several shapes may be given as "M,N,K,epi[,impl[,bn,splits]];..." (one measurement pass
+        # under ncu); impl as s1_op_gemm's: 0 planner's choice, 2 CTA-pair tiles, 3 single-CTA
+        # tiles; bn / splits > 0 pin the single-CTA planner's tile width / K split for that entry
         shapes = [[int(x) for x in sh.split(",")] for sh in args.shape.split(";")]
         res = []
         for sh in shapes:
             M, N, K = sh[:3]
             epi = sh[3] if len(sh) > 3 else 0
             impl = sh[4] if len(sh) > 4 else 0
+            for var, val in (("S1_GEMM_BN", sh[5] if len(sh) > 5 else 0), ("S1_GEMM_SPLITS", sh[6] if len(sh) > 6 else 0)):
+                if val > 0:
+                    os.environ[var] = str(val)
+                else:
+                    os.environ.pop(var, None)
             X = torch.randn((M, K), device="cuda", generator=g).to(torch.float16)
             W = (0.02 * torch.randn((N, K), device="cuda", generator=g)).to(torch.float16)
             out = torch.zeros((M, N // 2 if epi == 3 else N), device="cuda",

@@ -182,11 +182,21 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float ld_peer(uint32_t saddr, uint32_t rank) {
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
   uint32_t a;
-  float v;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(saddr), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return a;
+}
+// Loads from a peer's shared memory (published before a cluster barrier, so no ordering is
+// needed among the loads themselves: they issue back to back).
+__device__ __forceinline__ float ld_peer(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 ld_peer4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
   return v;
 }
 
@@ -201,6 +211,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     int layer_f, int Hq, int Hkv, float scale_log2, int nparts, int* __restrict__ d_err) {
   using L = Lay<HD>;
   constexpr int NB = HD / 64;                // 64-column boxes per row of Q, K, V
+  constexpr int PSTR = HD + 4;               // floats per published row (o, m, l; 16-byte rows)
+  static_assert(BQ * PSTR * 4 <= 2 * ST * L::TILE, "published partials fit the K/V stage buffers");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
@@ -352,14 +364,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_after();
       float sv[BKV];
       {
-        uint32_t u[32];
+        uint32_t u[BKV];   // the row's four 32-column loads in flight together
 #pragma unroll
-        for (int c = 0; c < BKV; c += 32) {
-          tld32(tmem + lane_off + b * 128 + c, u);
-          ld_wait();
+        for (int c = 0; c < BKV; c += 32) tld32(tmem + lane_off + b * 128 + c, u + c);
+        ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) sv[c + e] = __uint_as_float(u[e]);
-        }
+        for (int c = 0; c < BKV; ++c) sv[c] = __uint_as_float(u[c]);
       }
       fence_before();
       __syncwarp();
@@ -369,10 +379,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int kbase = cache ? j * BKV : (j - ncache) * BKV;
       const int klim = cache ? P - 1 : qi;   // last visible key of this tile's source
       float mx = -INFINITY;
+      if (kbase + BKV - 1 <= klim) {         // every key of the tile is visible to this row
 #pragma unroll
-      for (int c = 0; c < BKV; ++c) {
-        sv[c] = (kbase + c <= klim) ? sv[c] * scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[c]);
+        for (int c = 0; c < BKV; ++c) {
+          sv[c] *= scale_log2;
+          mx = fmaxf(mx, sv[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < BKV; ++c) {
+          sv[c] = (kbase + c <= klim) ? sv[c] * scale_log2 : -INFINITY;
+          mx = fmaxf(mx, sv[c]);
+        }
       }
       // lazy rescale: move the reference maximum only when it grows by more than 8 (2^8)
       float alpha = 1.f;
@@ -438,12 +456,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) { m = -INFINITY; l = 0.f; }
     }
     if (nparts > 1) {
-      // publish (o, m, l) in the K/V stage buffers (no longer read once every tile was consumed)
-      float* pub = reinterpret_cast<float*>(sm + L::K);
+      // publish (o, m, l) in the K/V stage buffers (no longer read once every tile was consumed),
+      // one row of PSTR floats per query row
+      float* pub = reinterpret_cast<float*>(sm + L::K) + r * PSTR;
 #pragma unroll
-      for (int c = 0; c < HD; ++c) pub[c * BQ + r] = o[c];
-      pub[HD * BQ + r] = m;
-      pub[(HD + 1) * BQ + r] = l;
+      for (int c = 0; c < HD; c += 4) *reinterpret_cast<float4*>(pub + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+      pub[HD] = m;
+      pub[HD + 1] = l;
     }
     if (nparts == 1) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -464,33 +483,64 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   if (nparts > 1) {
     cluster_sync();
-    if (cluster_rank() == 0 && warp >= 2) {
+    // every CTA of the cluster merges HD / nparts of the output columns of all 128 rows, from
+    // the parts in rank order
+    if (warp >= 2) {
       const int r = (warp & 3) * 32 + lane, qi = q0 + r;
-      const uint32_t base = smem_u32(sm + L::K);
+      const uint32_t rank = cluster_rank();
+      const uint32_t row = smem_u32(sm + L::K) + (uint32_t)(r * PSTR * 4);
+      float pm[4], pl[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        if (p < nparts) {
+          const uint32_t a = peer_addr(row, (uint32_t)p);
+          pm[p] = ld_peer(a + HD * 4);
+          pl[p] = ld_peer(a + (HD + 1) * 4);
+        }
       float M = -INFINITY;
-      for (int p = 0; p < nparts; ++p) M = fmaxf(M, ld_peer(base + (uint32_t)((HD * BQ + r) * 4), (uint32_t)p));
-      float Lsum = 0.f;
-      float o[HD];
 #pragma unroll
-      for (int c = 0; c < HD; ++c) o[c] = 0.f;
-      for (int p = 0; p < nparts; ++p) {
-        const float pm = ld_peer(base + (uint32_t)((HD * BQ + r) * 4), (uint32_t)p);
-        const float w = pm == -INFINITY ? 0.f : exp2f(pm - M);
-        Lsum += w * ld_peer(base + (uint32_t)(((HD + 1) * BQ + r) * 4), (uint32_t)p);
+      for (int p = 0; p < 4; ++p)
+        if (p < nparts) M = fmaxf(M, pm[p]);
+      float Lsum = 0.f, w[4];
 #pragma unroll
-        for (int c = 0; c < HD; ++c) o[c] += w * ld_peer(base + (uint32_t)((c * BQ + r) * 4), (uint32_t)p);
-      }
+      for (int p = 0; p < 4; ++p)
+        if (p < nparts) {
+          w[p] = pm[p] == -INFINITY ? 0.f : exp2f(pm[p] - M);
+          Lsum += w[p] * pl[p];
+        }
       const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-      if (qi < sd.len && !*abort_flag) {
-        f16* op = out + ((size_t)(sd.row0 + qi) * Hq + h) * HD;
+      const int cw = HD / nparts, c0 = (int)rank * cw;   // this CTA's columns (a multiple of 16)
+      for (int cb = 0; cb < cw; cb += 16) {
+        float acc[16];
 #pragma unroll
-        for (int c = 0; c < HD; c += 8)
-          *reinterpret_cast<uint4*>(op + c) =
-              make_uint4(h2u(o[c] * inv, o[c + 1] * inv), h2u(o[c + 2] * inv, o[c + 3] * inv),
-                         h2u(o[c + 4] * inv, o[c + 5] * inv), h2u(o[c + 6] * inv, o[c + 7] * inv));
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          if (p >= nparts) break;
+          const uint32_t a = peer_addr(row, (uint32_t)p) + (uint32_t)((c0 + cb) * 4);
+          float4 v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = ld_peer4(a + 16 * q);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            acc[4 * q] += w[p] * v[q].x;
+            acc[4 * q + 1] += w[p] * v[q].y;
+            acc[4 * q + 2] += w[p] * v[q].z;
+            acc[4 * q + 3] += w[p] * v[q].w;
+          }
+        }
+        if (qi < sd.len && !*abort_flag) {
+          f16* op = out + ((size_t)(sd.row0 + qi) * Hq + h) * HD + c0 + cb;
+          reinterpret_cast<uint4*>(op)[0] =
+              make_uint4(h2u(acc[0] * inv, acc[1] * inv), h2u(acc[2] * inv, acc[3] * inv),
+                         h2u(acc[4] * inv, acc[5] * inv), h2u(acc[6] * inv, acc[7] * inv));
+          reinterpret_cast<uint4*>(op)[1] =
+              make_uint4(h2u(acc[8] * inv, acc[9] * inv), h2u(acc[10] * inv, acc[11] * inv),
+                         h2u(acc[12] * inv, acc[13] * inv), h2u(acc[14] * inv, acc[15] * inv));
+        }
       }
     }
-    cluster_sync();   // the peers' partials stay in place until rank 0 has read them
+    cluster_sync();   // every CTA's partials stay in place until all of the cluster has read them
   }
   if (warp == 1) {
     fence_after();

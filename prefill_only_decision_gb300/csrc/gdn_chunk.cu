@@ -426,8 +426,8 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
 }
 
 // ---------------------------------------------------------------------------------------
-// chunk_state: one CTA per (sequence, head, block of 16 state rows), D / 8 warps; warp w keeps
-// columns [8w, 8w + 8) of the block's fp32 state in registers (one m16n8 accumulator). Per
+// chunk_state: one CTA per (sequence, head, block of 16 state rows), D / 16 warps; warp w keeps
+// columns [16w, 16w + 16) of the block's fp32 state in registers (two m16n8 accumulators). Per
 // chunk: S <- gamma_n S + Ut_b^T K' - Sr N, Sr the f16 copy of S in shared memory (all warps'
 // columns, the A operand of the product that depends on the previous chunk), Ut_b the block's
 // 16 columns of Ut. Each chunk's N^T, K' and Ut_b tiles arrive by TMA (one thread issues them
@@ -500,8 +500,12 @@ __device__ __forceinline__ void tma3(void* dst, const CUtensorMap* map, uint64_t
 // mapNT: N^T [n_chunks * H * D rows, D columns] f16, box 64 x D, 128-byte swizzle.
 // mapKp: K' [R, H, D] f16 as (D, H, R), box 64 x 1 x 64, 128-byte swizzle.
 // mapUt: Ut [R, H, D] f16 as (D, H, R), box 16 x 1 x 64, no swizzle.
+// Threads of the state pass: one warp per 16 state columns.
 template <int D>
-__global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constant__ CUtensorMap mapNT,
+constexpr int state_threads() { return D * 2; }
+
+template <int D>
+__global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_constant__ CUtensorMap mapNT,
                                                             const __grid_constant__ CUtensorMap mapKp,
                                                             const __grid_constant__ CUtensorMap mapUt,
                                                             const float* __restrict__ gam,
@@ -513,6 +517,7 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
   wait_prerequisites();
   using SM = StateSmem<D>;
   constexpr int SR = SM::SR;
+  constexpr int KS = D / 32;                   // 32-deep k steps of Sr x N
   extern __shared__ __align__(16) uint8_t smraw[];   // (rounded up to 1024 bytes below)
   SM& s = *reinterpret_cast<SM*>((((uintptr_t)smraw) + 1023) & ~(uintptr_t)1023);
   const SeqDesc sd = seqs[blockIdx.x];
@@ -521,7 +526,7 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
   const int nch = (sd.len + C - 1) / C;
   // steps that update the state: all but the last chunk's, unless the final state is kept
   const int nupd = (sd.ctx_out >= 0 || sd.fol1 > sd.fol0) ? nch : nch - 1;
-  const int col = warp * 8 + 2 * tq;           // this thread's state columns col, col + 1
+  const int cw = warp * 16;                    // this warp's state columns cw .. cw + 15
   const size_t DD = (size_t)D * D;
   const size_t head_off = (size_t)(layer_g * H + h) * DD;
   if (tid == 0) {
@@ -548,43 +553,51 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
     for (int cl = 0; cl < nupd && cl < NS; ++cl) issue(cl);
   // gamma_n of the first steps
   for (int i = tid; i < nupd && i < SM::GAM; i += blockDim.x) s.gam[i] = gam[(size_t)(sd.chunk0 + i) * H + h];
-  // the state block's fragment: rows v0 + gq and v0 + gq + 8, columns col and col + 1
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // the state block's fragments: rows v0 + gq and v0 + gq + 8, columns cw + 8 nt + 2 tq and + 1
+  float acc[2][4] = {};
   if (sd.ctx_in >= 0) {
     const float* S0 = ctxs[sd.ctx_in].S + head_off;
-    const float2 x = *reinterpret_cast<const float2*>(S0 + (size_t)(v0 + gq) * D + col);
-    const float2 y = *reinterpret_cast<const float2*>(S0 + (size_t)(v0 + gq + 8) * D + col);
-    acc[0] = x.x; acc[1] = x.y; acc[2] = y.x; acc[3] = y.y;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = cw + 8 * nt + 2 * tq;
+      const float2 x = *reinterpret_cast<const float2*>(S0 + (size_t)(v0 + gq) * D + col);
+      const float2 y = *reinterpret_cast<const float2*>(S0 + (size_t)(v0 + gq + 8) * D + col);
+      acc[nt][0] = x.x; acc[nt][1] = x.y; acc[nt][2] = y.x; acc[nt][3] = y.y;
+    }
   }
-  // f16 copy of the fragment into Sr[buf], and into the start record of chunk ci (ci >= 0)
+  // f16 copy of the fragments into Sr[buf], and into the start record of chunk ci (ci >= 0)
   auto put = [&](int buf, int ci) {
-    const uint32_t lo = h2u(acc[0], acc[1]), hi = h2u(acc[2], acc[3]);
-    *reinterpret_cast<uint32_t*>(&s.Sr[buf][gq * SR + col]) = lo;
-    *reinterpret_cast<uint32_t*>(&s.Sr[buf][(gq + 8) * SR + col]) = hi;
-    if (ci >= 0) {
-      f16* rp = Srec + ((size_t)ci * H + h) * DD;
-      *reinterpret_cast<uint32_t*>(rp + (size_t)(v0 + gq) * D + col) = lo;
-      *reinterpret_cast<uint32_t*>(rp + (size_t)(v0 + gq + 8) * D + col) = hi;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int col = cw + 8 * nt + 2 * tq;
+      const uint32_t lo = h2u(acc[nt][0], acc[nt][1]), hi = h2u(acc[nt][2], acc[nt][3]);
+      *reinterpret_cast<uint32_t*>(&s.Sr[buf][gq * SR + col]) = lo;
+      *reinterpret_cast<uint32_t*>(&s.Sr[buf][(gq + 8) * SR + col]) = hi;
+      if (ci >= 0) {
+        f16* rp = Srec + ((size_t)ci * H + h) * DD;
+        *reinterpret_cast<uint32_t*>(rp + (size_t)(v0 + gq) * D + col) = lo;
+        *reinterpret_cast<uint32_t*>(rp + (size_t)(v0 + gq + 8) * D + col) = hi;
+      }
     }
   };
   put(0, sd.chunk0);
-  // the first tiles; one barrier agrees on their arrival and on Sr and gamma being in place
-  bool ok = __syncthreads_and(nupd > 0 ? (bar_wait(&s.full[0], 0) ? 1 : 0) : 1) != 0;
-  int waited = (ok && nupd > 0) ? 1 : 0;     // steps whose tiles have arrived
-  int cur = 0;
-  for (int cl = 0; cl < nupd && ok; ++cl) {
-    const int st = cl % NS;
-    const uint8_t* sb = s.stage[st];
+  // Everything a step needs from its tiles is taken before the barrier that ends the previous
+  // step: the B block = Ut_b^T K' over this warp's 16 columns (independent of the state; rows
+  // t >= n of both tiles are zeroed in the fragments), kept in qv, and this warp's N fragments,
+  // kept in nb. After the barrier a step is only Sr x N, the update and the f16 copy.
+  float qv[2][4];
+  uint32_t nb[KS][2][4];
+  auto take_tiles = [&](int cl) {
+    const uint8_t* sb = s.stage[cl % NS];
     const __half* ntile = reinterpret_cast<const __half*>(sb);
     const uint32_t kp_base = smem_u32(sb + SM::NT_BYTES);
     const __half* ut = reinterpret_cast<const __half*>(sb + SM::NT_BYTES + SM::KP_BYTES);
-    const int n = min(C, sd.len - cl * C);     // rows of this chunk (later tile rows belong to others)
-    // B block = Ut_b^T K' over this warp's 8 columns (independent of the state): rows t >= n of
-    // the Ut tile are zeroed in the A fragments
-    float q0v[4] = {0.f, 0.f, 0.f, 0.f}, q1v[4] = {0.f, 0.f, 0.f, 0.f};
+    const int n = min(C, sd.len - cl * C);     // rows of this chunk (later tile rows belong to others
+                                               // or, past the call's rows, hold whatever the scratch held)
+    float q[2][2][4] = {};
 #pragma unroll
     for (int k = 0; k < C; k += 32) {
-      uint32_t a0[4], a1[4], b[4];
+      uint32_t a0[4], a1[4];
       lda_t(ut, BV, 0, k, lane, a0);
       lda_t(ut, BV, 0, k + 16, lane, a1);
       if (n < C) {
@@ -597,32 +610,67 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
           a1[e] &= m1;
         }
       }
-      // K' rows k .. k+31 (token), columns of this warp's n-tile; swizzled boxes of 64 columns
-      {
-        const int t = k + lane, c = warp * 8;
-        ldsm4t(kp_base + (uint32_t)((c >> 6) * (C * 128) + t * 128 + ((((c & 63) >> 3) ^ (t & 7)) << 4)), b);
-      }
-      mma16(q0v, a0, b[0], b[1]);
-      mma16(q1v, a1, b[2], b[3]);
-    }
-    // Sr (16 x D) x N (D x D) over this warp's 8 columns, in two accumulation chains
-    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < D; k += 32) {
-      uint32_t a0[4], a1[4], b[4];
-      lda(s.Sr[cur], SR, 0, k, lane, a0);
-      lda(s.Sr[cur], SR, 0, k + 16, lane, a1);
-      ldsm4(smem_u32(ntile + nt_off<D>(warp * 8 + (lane & 7), k + 8 * (lane >> 3))), b);
-      mma16(p0, a0, b[0], b[1]);
-      mma16(p1, a1, b[2], b[3]);
+      for (int nt = 0; nt < 2; ++nt) {
+        // K' rows k .. k+31 (token), 8 columns of this warp; swizzled boxes of 64 columns;
+        // b[j] holds tokens k + 8j + 2tq and + 1
+        uint32_t b[4];
+        const int t = k + lane, c = cw + 8 * nt;
+        ldsm4t(kp_base + (uint32_t)((c >> 6) * (C * 128) + t * 128 + ((((c & 63) >> 3) ^ (t & 7)) << 4)), b);
+        if (n < C) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int t0 = k + 8 * j + 2 * tq;
+            b[j] &= (t0 < n ? 0x0000FFFFu : 0u) | (t0 + 1 < n ? 0xFFFF0000u : 0u);
+          }
+        }
+        mma16(q[nt][0], a0, b[0], b[1]);
+        mma16(q[nt][1], a1, b[2], b[3]);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[nt][i] = q[nt][0][i] + q[nt][1][i];
+#pragma unroll
+    for (int i = 0; i < KS; ++i)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+        ldsm4(smem_u32(ntile + nt_off<D>(cw + 8 * nt + (lane & 7), 32 * i + 8 * (lane >> 3))), nb[i][nt]);
+  };
+  // the first tiles; one barrier agrees on their arrival and on Sr and gamma being in place
+  bool ok = __syncthreads_and(nupd > 0 ? (bar_wait(&s.full[0], 0) ? 1 : 0) : 1) != 0;
+  int waited = (ok && nupd > 0) ? 1 : 0;     // steps whose tiles have arrived
+  if (ok && nupd > 0) take_tiles(0);
+  int cur = 0;
+  for (int cl = 0; cl < nupd && ok; ++cl) {
+    // Sr (16 x D) x N (D x D) over this warp's 16 columns: the A fragments are shared by both
+    // column tiles; two accumulation chains per tile
+    float p[2][2][4] = {};
+#pragma unroll
+    for (int i = 0; i < KS; ++i) {
+      uint32_t a0[4], a1[4];
+      lda(s.Sr[cur], SR, 0, 32 * i, lane, a0);
+      lda(s.Sr[cur], SR, 0, 32 * i + 16, lane, a1);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        mma16(p[nt][i & 1], a0, nb[i][nt][0], nb[i][nt][1]);
+        mma16(p[nt][i & 1], a1, nb[i][nt][2], nb[i][nt][3]);
+      }
     }
     const float g = s.gam[cl % SM::GAM];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] = fmaf(g, acc[i], (q0v[i] + q1v[i]) - (p0[i] + p1[i]));
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] = fmaf(g, acc[nt][i], qv[nt][i] - (p[nt][0][i] + p[nt][1][i]));
     put(cur ^ 1, cl + 1 < nch ? sd.chunk0 + cl + 1 : -1);
-    // the next step's tiles; one barrier agrees on them, on Sr being complete and on this step's
-    // tiles having been read by every warp
-    const bool w = cl + 1 < nupd ? bar_wait(&s.full[(cl + 1) % NS], ((cl + 1) / NS) & 1) : true;
+    // the next step's tiles, then one barrier that agrees on them, on Sr being complete and on
+    // this step's tiles having been read by every warp
+    bool w = true;
+    if (cl + 1 < nupd) {
+      w = bar_wait(&s.full[(cl + 1) % NS], ((cl + 1) / NS) & 1);
+      if (w) take_tiles(cl + 1);
+    }
     ok = __syncthreads_and(w ? 1 : 0) != 0;
     if (!ok) break;
     if (cl + 1 < nupd) ++waited;
@@ -648,8 +696,12 @@ __global__ void __launch_bounds__(D * 4) chunk_state_kernel(const __grid_constan
     for (int f = sd.fol0; f < sd.fol1; ++f) put(cur, seqs[f].chunk0);
     if (sd.ctx_out >= 0) {
       float* So = ctxs[sd.ctx_out].S + head_off;
-      *reinterpret_cast<float2*>(So + (size_t)(v0 + gq) * D + col) = make_float2(acc[0], acc[1]);
-      *reinterpret_cast<float2*>(So + (size_t)(v0 + gq + 8) * D + col) = make_float2(acc[2], acc[3]);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int col = cw + 8 * nt + 2 * tq;
+        *reinterpret_cast<float2*>(So + (size_t)(v0 + gq) * D + col) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2*>(So + (size_t)(v0 + gq + 8) * D + col) = make_float2(acc[nt][2], acc[nt][3]);
+      }
     }
   }
 }
@@ -880,7 +932,7 @@ static cudaError_t launch_state(const CUtensorMap* maps, const SeqDesc* d_seq, i
                                 cudaStream_t st) {
   if (n_seq <= 0) return cudaSuccess;
   const dim3 grid(n_seq, H, D / gc::BV);
-  CK_RET(launch_pdl(gc::chunk_state_kernel<D>, grid, dim3(D * 4), state_smem<D>(), st, maps[0], maps[1], maps[2],
+  CK_RET(launch_pdl(gc::chunk_state_kernel<D>, grid, dim3(gc::state_threads<D>()), state_smem<D>(), st, maps[0], maps[1], maps[2],
                     (const float*)bufs.gam, d_seq, d_chunks, d_ctx, layer_g, H, bufs.Srec, d_err));
   return cudaGetLastError();
 }

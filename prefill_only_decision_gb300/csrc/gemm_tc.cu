@@ -342,6 +342,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
   };
   // 16-byte chunk c of this lane's row in a 64-byte swizzled row (the output map's 64-byte swizzle)
   auto chunk64 = [&](uint8_t* box, int c) { return reinterpret_cast<uint4*>(box + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)); };
+  float lmx = -INFINITY, lsum = 0.f;   // EPI_LSE: running max and sum of exp over the row's columns
 #pragma unroll 1
   for (int c0 = 0; c0 < BN; c0 += 64) {
     const int nc = (BN - c0) < 64 ? (BN - c0) / 16 : 4;   // 16-column chunks in this group
@@ -381,6 +382,21 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
         o[0] = reinterpret_cast<uint4*>(r)[0];
         o[1] = reinterpret_cast<uint4*>(r)[1];
       }
+    } else if (p.epi == EPI_LSE) {
+      // N is a multiple of 32, so a chunk that starts before N is whole
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j >= nc || n0 + c0 + 16 * j >= p.N) continue;
+        float cm = v[j][0];
+#pragma unroll
+        for (int i = 1; i < 16; ++i) cm = fmaxf(cm, v[j][i]);
+        const float nm = fmaxf(lmx, cm);
+        float add = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) add += __expf(v[j][i] - nm);
+        lsum = lsum * __expf(lmx - nm) + add;
+        lmx = nm;
+      }
     } else if (p.epi == EPI_PARTIAL) {
       // split-K partials: plain stores, summed by splitk_reduce_kernel
       const size_t yr = (size_t)(y0 + lane);
@@ -406,6 +422,8 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
       }
     }
   }
+  if (p.epi == EPI_LSE && m0 + lane < p.M)
+    reinterpret_cast<float2*>(p.out)[(size_t)(n0 / BN) * p.ldo + m0 + lane] = make_float2(lmx, lsum);
 }
 
 // One CTA per SM, each loading its own A and B tiles; CTAs that run at the same time work on
@@ -913,18 +931,55 @@ inline Plan plan_pair_for(int M, int N, int K, int epi, int num_sms) {
   return best;
 }
 
+// Few rows (at most two m tiles: questions over a snapshot) stream the weights: the estimated
+// time in microseconds of a plan is a fixed launch and ramp cost, then the longer of the weight
+// bytes at HBM speed and one CTA's share of k blocks (about 0.32 us per 64-deep block of 128
+// weight rows), plus the split-K reduction when K is split. Fitted to cold-cache launch times of
+// the 4B and 27B decide shapes over tile widths 128..256 and splits 1..8; ties (within 3 %) go
+// to the narrower tile and the smaller split.
+static double few_rows_cost_us(int N, int K, int bn, int kbp, int sp, int units, int maxc) {
+  const double hbm_us = (double)N * K * 2 / 6.7e6;
+  const int rounds = (units + maxc - 1) / maxc;
+  const double stream_us = (double)rounds * kbp * 0.32 * bn / 128.0;
+  return 5.0 + (hbm_us > stream_us ? hbm_us : stream_us) + (sp > 1 ? 6.0 + sp : 0.0);
+}
+
 // Choose the N tile and the K split together: minimise (waves of work units) x (k blocks per
-// unit) x (per-k-block cost of the tile).
+// unit) x (per-k-block cost of the tile); few-row shapes by few_rows_cost_us.
 Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
   Plan best{};
   double best_cost = 1e30;
   const int kb_total = K / BK;
   const int m_tiles = (M + BM - 1) / BM;
+  const char* fb0 = getenv("S1_GEMM_BN");
+  const char* fs0 = getenv("S1_GEMM_SPLITS");
+  if (m_tiles <= 2 && !fb0 && !fs0) {
+    for (int bn : {128, 144, 176, 192, 208, 256}) {
+      if (epi == EPI_SWIGLU && (bn % 32)) continue;
+      const int n_tiles = (N + bn - 1) / bn;
+      const int maxc = max_ctas_of(bn, num_sms);
+      for (int sp = 1; sp <= 4; ++sp) {
+        if (sp > 1 && kb_total / sp < 4) break;
+        const int kbp = (kb_total + sp - 1) / sp;
+        if ((kb_total + kbp - 1) / kbp != sp) continue;
+        if (sp > 1 && (size_t)sp * m_tiles * BM * (size_t)N > ws_cap) break;
+        const int units = m_tiles * n_tiles * sp;
+        const double cost = few_rows_cost_us(N, K, bn, kbp, sp, units, maxc);
+        if (cost < best_cost * 0.97) {
+          best_cost = cost;
+          best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, 0, 0};
+        }
+      }
+    }
+    if (best.bn != 0) return best;
+  }
   // (176 and 208 are autotuner candidates only: measured slower than 144 in the split-K,
   // few-row weight-streaming plans this heuristic chooses; S1_GEMM_BN may still pin them)
   const int cands[6] = {256, 192, 144, 128, 208, 176};
   const char* fb = getenv("S1_GEMM_BN");   // measurement / test override of the tile width
   const int force_bn = fb ? atoi(fb) : -1;
+  const char* fs = getenv("S1_GEMM_SPLITS");   // measurement override of the K split
+  const int force_sp = fs ? atoi(fs) : -1;
   for (int bn : cands) {
     if (epi == EPI_SWIGLU && (bn % 32)) continue;
     if (force_bn > 0 ? bn != force_bn : (bn == 208 || bn == 176)) continue;
@@ -940,13 +995,14 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
       const int waves = (units + maxc - 1) / maxc;
       double cost = (double)waves * kbp * (bn + 48.0);
       if (sp > 1) cost *= 1.0 + 0.04 * sp;
-      if (cost < best_cost * 0.999) {
+      if ((force_sp <= 0 || sp == force_sp) && cost < best_cost * 0.999) {
         best_cost = cost;
         best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, 0, 0};
       }
-      if (units >= maxc) break;
+      if (force_sp <= 0 && units >= maxc) break;
     }
   }
+  if (best.bn == 0) best = plan_with(M, N, K, 128);   // (an override no candidate satisfies)
   return best;
 }
 
@@ -1264,6 +1320,14 @@ cudaError_t launch_gemm_tc(const f16* X, const f16* W, int M, int N, int K, int 
     if (e != cudaSuccess) return e;
   }
   return launch_plan(pl, X, W, M, N, K, epi, out, ldo, splitk_ws, lc);
+}
+
+cudaError_t launch_gemm_lse(const f16* X, const f16* W, int M, int N, int K, float2* part, int ldp,
+                            const LaunchCtx& lc) {
+  if (M <= 0) return cudaSuccess;
+  if (!gemm_tc_supported(M, N, K, EPI_F32) || M > ldp || !part) return cudaErrorInvalidValue;
+  const tc::Plan pl = tc::plan_with(M, N, K, GEMM_LSE_BN);
+  return launch_plan(pl, X, W, M, N, K, EPI_LSE, part, ldp, nullptr, lc);
 }
 
 }  // namespace s1

@@ -23,6 +23,8 @@ enum Epilogue {
   EPI_RESADD = 2,   // out fp32 [M, ldo]: out += acc   (residual stream)
   EPI_SWIGLU = 3,   // W rows interleaved in blocks of 16 gate / 16 up rows;
                     // out f16 [M, ldo] with N/2 columns: silu(gate) * up
+  EPI_LSE = 4,      // out float2 [ceil(N / BN), ldo]: per row m and N tile t, (max, sum of
+                    // exp(acc - max)) over the tile's columns (launch_gemm_lse only)
 };
 
 // Packed description of the sequences of one forward call.
@@ -102,6 +104,11 @@ cudaError_t launch_gemm_simt(const f16* X, const f16* W, int M, int N, int K, in
 bool gemm_tc_supported(int M, int N, int K, int epi);
 cudaError_t launch_gemm_tc(const f16* X, const f16* W, int M, int N, int K, int epi, void* out,
                            int ldo, float* splitk_ws, size_t ws_floats, const LaunchCtx& lc);
+// Row-wise log-sum-exp partials of X . W^T on the tensor cores (no K split, 256-wide N tiles):
+// part[t * ldp + m] = (max, sum exp(acc - max)) over the columns of N tile t, for m < M <= ldp.
+constexpr int GEMM_LSE_BN = 256;
+cudaError_t launch_gemm_lse(const f16* X, const f16* W, int M, int N, int K, float2* part, int ldp,
+                            const LaunchCtx& lc);
 size_t gemm_tc_workspace_floats(int M, int N, int K, int epi, int num_sms);
 size_t gemm_tc_plan_ws_floats(int M, int N, int K, int epi, int num_sms, size_t ws_cap);
 cudaError_t launch_gdn_prep(float* proj, int ld, float* alpha, float* beta, int R, int H, int Dk,
@@ -153,9 +160,9 @@ cudaError_t launch_readout(const float* x, const float* final_norm, const f16* E
                            const int* q_row, const int* q_type, const int* opt_off,
                            const int* opt_ids, int n_q, float* probs, float* stats, float* hidden,
                            int max_opts, float* hn_out, float* z_out, cudaStream_t st);
-size_t vocab_lm_scratch_floats(int n_q, int n_opts, int d, int num_sms);
+size_t vocab_lm_scratch_floats(int n_q, int n_opts, int d, int V, int num_sms);
 cudaError_t launch_vocab_lm(const f16* E, int V, int d, const float* hn, const float* z, const int* opt_off, int n_q,
-                            float* lm, float* scratch, int num_sms, cudaStream_t st, long* launches);
+                            float* lm, float* scratch, const LaunchCtx& lc, bool tensor_cores);
 cudaError_t launch_merge_lora(const void* W, int w_is_bf16, const void* A, const void* B,
                               int ab_is_bf16, int rank, float scale, int out_f, int in_f,
                               f16* dst, int dst_row0, int interleave_swiglu, int swiglu_half,

@@ -26,9 +26,17 @@ using namespace s1;
 // errors and allocation
 namespace {
 thread_local std::string g_err;
-void* (*g_alloc)(size_t, void*) = nullptr;
-void (*g_free)(void*, void*) = nullptr;
-void* g_alloc_ctx = nullptr;
+// Device allocator: the hooks installed by s1_set_allocator (NULL: cudaMalloc / cudaFree). A model
+// keeps the hooks that were installed when it was created, and every allocation and free made on
+// its behalf goes through them (t_alloc points at them for the duration of each call on it), so
+// installing other hooks later never frees its blocks through the wrong allocator.
+struct Alloc {
+  void* (*alloc)(size_t, void*) = nullptr;
+  void (*free)(void*, void*) = nullptr;
+  void* ctx = nullptr;
+};
+Alloc g_al;
+thread_local const Alloc* t_alloc = nullptr;
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -42,7 +50,8 @@ int fail(int code, const char* fmt, ...) {
 
 void* dalloc(size_t bytes) {
   if (bytes == 0) bytes = 256;
-  if (g_alloc) return g_alloc(bytes, g_alloc_ctx);
+  const Alloc& a = t_alloc ? *t_alloc : g_al;
+  if (a.alloc) return a.alloc(bytes, a.ctx);
   void* p = nullptr;
   if (cudaMalloc(&p, bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -52,7 +61,8 @@ void* dalloc(size_t bytes) {
 }
 void dfree(void* p) {
   if (!p) return;
-  if (g_free) g_free(p, g_alloc_ctx);
+  const Alloc& a = t_alloc ? *t_alloc : g_al;
+  if (a.free) a.free(p, a.ctx);
   else cudaFree(p);
 }
 
@@ -112,6 +122,7 @@ struct Scratch {
 
 struct s1_model {
   uint32_t magic;
+  Alloc al;   // the allocator hooks of this model's device memory (those installed at creation)
   s1_shape sh;
   std::vector<uint8_t> is_full;
   int nG = 0, nF = 0, n_in_gdn = 0, n_in_fa = 0, n_proj = 0, n_mix = 0;
@@ -140,6 +151,7 @@ struct s1_model {
   float* trace = nullptr;      // layer trace: residual stream after the embedding and each layer
   long long trace_floats = 0;
   bool force_simt = false;     // S1_GEMM=simt in the environment (debugging)
+  bool vocab_simt = false;     // S1_VOCAB=simt: full-vocabulary pass on CUDA cores
   bool fuse_norm = true;       // RMSNorm fused into split-K residual reductions (S1_NORM_FUSE=0: off)
   // profiling
   bool prof = false;
@@ -185,6 +197,7 @@ struct s1_state {
   f16 * KV;
   float* conv;         // short-convolution history [n_gdn_layers, width - 1, channels] (or NULL)
   void* mem;
+  Alloc al;            // the hooks `mem` came from (its model's)
 };
 
 // ---------------------------------------------------------------------------------------
@@ -441,6 +454,15 @@ int upload_meta(s1_model* m, Meta& mt, void** dest = nullptr) {
   return S1_OK;
 }
 
+// Routes the allocations and frees of one call on a model through the model's own hooks.
+struct AllocScope {
+  const Alloc* prev;
+  explicit AllocScope(const s1_model* m) : prev(t_alloc) { t_alloc = m ? &m->al : prev; }
+  ~AllocScope() { t_alloc = prev; }
+  AllocScope(const AllocScope&) = delete;
+  AllocScope& operator=(const AllocScope&) = delete;
+};
+
 bool valid_model(const s1_model* m) { return m && m->magic == MODEL_MAGIC; }
 bool valid_state(const s1_model* m, const s1_state* st) {
   return st && st->magic == STATE_MAGIC && st->model == m;
@@ -605,7 +627,7 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
     float *hn = nullptr, *z = nullptr;
     const int no = (int)mt.opt_ids.size();
     if (want_lm) {
-      const size_t need = (size_t)no + vocab_lm_scratch_floats(nq, no, d, m->num_sms);
+      const size_t need = (size_t)no + vocab_lm_scratch_floats(nq, no, d, s.vocab, m->num_sms);
       if (need > m->lm_floats) {
         CK(cudaStreamSynchronize(st));
         dfree(m->lm_buf);
@@ -619,9 +641,11 @@ int run_forward(s1_model* m, Meta& mt, const bf16* d_embeds, float* probs, float
     CK(launch_readout(sc.x, m->final_norm, m->embed, d, s.rms_eps, mt.d_q_row, mt.d_q_type,
                       mt.d_opt_off, mt.d_opt_ids, nq, probs, stats, hidden, mt.max_opts, hn, z, st));
     m->launches += 1;
-    if (want_lm)
-      CK(launch_vocab_lm(m->embed, s.vocab, d, hn, z, mt.d_opt_off, nq, m->lm_buf, hn + (size_t)nq * d,
-                         m->num_sms, st, &m->launches));
+    if (want_lm) {
+      LaunchCtx lc{st, m->d_err, m->num_sms, &m->launches};
+      CK(launch_vocab_lm(m->embed, s.vocab, d, hn, z, mt.d_opt_off, nq, m->lm_buf, hn + (size_t)nq * d, lc,
+                         !m->vocab_simt));
+    }
   }
   return S1_OK;
 }
@@ -658,6 +682,7 @@ int new_state(s1_model* m, int cap, s1_state** out) {
   void* mem = dalloc(sb + kb + cb);
   if (!mem) return fail(S1_ERR_OOM, "state allocation (%zu bytes) failed", sb + kb + cb);
   s1_state* st = new s1_state;
+  st->al = m->al;
   st->magic = STATE_MAGIC;
   st->model = m;
   st->P = 0;
@@ -808,9 +833,9 @@ const char* s1_version(void) { return "s1 0.1 (sm_103a)"; }
 
 int s1_set_allocator(void* (*alloc)(size_t, void*), void (*free_fn)(void*, void*), void* ctx) {
   if ((alloc == nullptr) != (free_fn == nullptr)) return fail(S1_ERR_INVALID_ARG, "alloc and free must both be set or both NULL");
-  g_alloc = alloc;
-  g_free = free_fn;
-  g_alloc_ctx = ctx;
+  g_al.alloc = alloc;
+  g_al.free = free_fn;
+  g_al.ctx = ctx;
   return S1_OK;
 }
 
@@ -835,6 +860,8 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   if (!w->embed || !w->final_norm || !w->layer) return fail(S1_ERR_INVALID_ARG, "weights: NULL tensor array");
 
   s1_model* m = new s1_model();
+  m->al = g_al;
+  AllocScope alloc_scope(m);
   m->magic = MODEL_MAGIC;
   m->sh = s;
   m->is_full.assign(s.layer_is_full, s.layer_is_full + s.n_layers);
@@ -856,6 +883,8 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
   m->force_simt = gi && strcmp(gi, "simt") == 0;
   const char* gd = getenv("S1_GDN");
   m->gdn_token = gd && strcmp(gd, "token") == 0;
+  const char* gv = getenv("S1_VOCAB");
+  m->vocab_simt = gv && strcmp(gv, "simt") == 0;
   const char* ga = getenv("S1_ATTN");
   m->attn_sync = ga && strcmp(ga, "sync") == 0;
   const char* nf = getenv("S1_NORM_FUSE");
@@ -1037,6 +1066,7 @@ int s1_model_create(const s1_shape* shape, const s1_weights* w, s1_model** out) 
 
 void s1_model_destroy(s1_model* m) {
   if (!valid_model(m)) return;
+  AllocScope alloc_scope(m);
   cudaStreamSynchronize(m->stream);
   if (m->prof) --pdl_suppressed();
   drop_graphs(m);
@@ -1069,6 +1099,7 @@ int s1_sync(s1_model* m) {
 
 int s1_state_create(s1_model* m, int32_t capacity_rows, s1_state** out) {
   if (!valid_model(m) || !out) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (capacity_rows < 1 || capacity_rows > m->sh.max_rows) return fail(S1_ERR_BUDGET, "capacity %d outside [1, max_rows]", capacity_rows);
   return new_state(m, capacity_rows, out);
 }
@@ -1076,7 +1107,12 @@ int s1_state_create(s1_model* m, int32_t capacity_rows, s1_state** out) {
 void s1_state_destroy(s1_state* st) {
   if (!st || st->magic != STATE_MAGIC) return;
   if (st->model && valid_model(st->model)) cudaStreamSynchronize(st->model->stream);
-  dfree(st->mem);
+  {
+    const Alloc* prev = t_alloc;
+    t_alloc = &st->al;
+    dfree(st->mem);
+    t_alloc = prev;
+  }
   st->magic = DEAD;
   delete st;
 }
@@ -1226,6 +1262,7 @@ static int prefill_impl(s1_model* m, int n_req, const int32_t* const* tokens, co
 int s1_prefill_state_batch(s1_model* m, int32_t n_req, const int32_t* const* tokens, const int32_t* n_tokens,
                            const void* const* embeds, const int32_t* n_embeds, s1_state** out) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (n_req < 1 || !n_tokens || !out) return fail(S1_ERR_INVALID_ARG, "bad batch arguments");
   std::vector<int32_t> ne(n_req, 0);
   if (n_embeds) ne.assign(n_embeds, n_embeds + n_req);
@@ -1257,6 +1294,7 @@ int s1_prefill_state(s1_model* m, const int32_t* tokens, int32_t n_tokens, const
 int s1_prefill_async(s1_model* m, s1_state* st, const int32_t* d_tokens, int32_t n_tokens,
                      const void* d_embeds, int32_t n_embeds) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (!valid_state(m, st)) return fail(S1_ERR_INVALID_HANDLE, "invalid state");
   const void* e[1] = {d_embeds};
   CallKey key('P');
@@ -1353,6 +1391,7 @@ static void output_slots(s1_model* m, int NQ, int NO, float** probs, float** sta
 int s1_decide_batch(s1_model* m, int32_t n_req, const s1_state* const* states, const s1_question* const* qs,
                     const int32_t* n_q, s1_result* const* out, float* const* last_hidden) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (n_req < 1 || !states || !qs || !n_q || !out) return fail(S1_ERR_INVALID_ARG, "bad batch arguments");
   for (int r = 0; r < n_req; ++r)
     if (n_q[r] > 0 && !out[r]) return fail(S1_ERR_INVALID_ARG, "request %d: NULL results", r);
@@ -1380,6 +1419,7 @@ int s1_decide(s1_model* m, const s1_state* st, const s1_question* qs, int32_t n_
 int s1_decide_async(s1_model* m, const s1_state* st, const s1_question* qs_dev, int32_t n_q,
                     float* d_probs, float* d_stats, float* d_last_hidden) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (!d_probs || !d_stats) return fail(S1_ERR_INVALID_ARG, "NULL output");
   if (!valid_state(m, st)) return fail(S1_ERR_INVALID_HANDLE, "invalid state");
   if (n_q < 1 || !qs_dev) return fail(S1_ERR_INVALID_ARG, "no questions");
@@ -1512,6 +1552,7 @@ int s1_prefill_decide_batch(s1_model* m, int32_t n_req, const int32_t* const* to
                             const int32_t* n_q, s1_result* const* out, float* const* last_hidden,
                             s1_state** states_out) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (n_req < 1 || !n_tokens || !qs || !n_q || !out) return fail(S1_ERR_INVALID_ARG, "bad batch arguments");
   for (int r = 0; r < n_req; ++r)
     if (n_q[r] > 0 && !out[r]) return fail(S1_ERR_INVALID_ARG, "request %d: NULL results", r);
@@ -1571,6 +1612,7 @@ int s1_prefill_decide_async(s1_model* m, s1_state* st, const int32_t* d_tokens, 
                             const void* d_embeds, int32_t n_embeds, const s1_question* qs_dev, int32_t n_q,
                             float* d_probs, float* d_stats, float* d_last_hidden) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (!valid_state(m, st)) return fail(S1_ERR_INVALID_HANDLE, "invalid state");
   if (!d_probs || !d_stats) return fail(S1_ERR_INVALID_ARG, "NULL output");
   const void* e[1] = {d_embeds};
@@ -1595,6 +1637,7 @@ int s1_prefill_decide_batch_async(s1_model* m, int32_t n_req, s1_state* const* s
                                   const s1_question* const* qs_dev, const int32_t* n_q, float* d_probs,
                                   float* d_stats, float* d_last_hidden) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (n_req < 1 || !states || !d_tokens || !n_tokens || !qs_dev || !n_q)
     return fail(S1_ERR_INVALID_ARG, "bad batch arguments");
   if (!d_probs || !d_stats) return fail(S1_ERR_INVALID_ARG, "NULL output");
@@ -1624,6 +1667,7 @@ int s1_prefill_decide_batch_async(s1_model* m, int32_t n_req, s1_state* const* s
 
 int s1_set_graphs(s1_model* m, int enable) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   CK(cudaStreamSynchronize(m->stream));
   if (!enable) drop_graphs(m);
   m->graphs = enable != 0;
@@ -1633,6 +1677,7 @@ int s1_set_graphs(s1_model* m, int enable) {
 // -- instrumentation ---------------------------------------------------------------------
 int s1_profile(s1_model* m, int enable) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   CK(cudaStreamSynchronize(m->stream));
   if (enable && !m->prof) ++pdl_suppressed();
   if (!enable && m->prof) --pdl_suppressed();
@@ -1673,6 +1718,7 @@ int s1_counters(s1_model* m, long long* launches, long long* h2d_bytes, long lon
 
 int s1_set_layer_trace(s1_model* m, float* d_trace, long long capacity_floats) {
   if (!valid_model(m)) return fail(S1_ERR_INVALID_HANDLE, "invalid model");
+  AllocScope alloc_scope(m);
   if (d_trace && capacity_floats <= 0) return fail(S1_ERR_INVALID_ARG, "layer trace needs a positive capacity");
   CK(cudaStreamSynchronize(m->stream));
   m->trace = d_trace;

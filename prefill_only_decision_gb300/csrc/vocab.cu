@@ -2,9 +2,14 @@
 // log p(o) = z_o - log sum_v exp(z_v), z = E h_hat with E the tied embedding [V, d]
 // (System1-Omni RFC #114, section 4 "Readout" row and the paragraph after the table: token
 // log-probabilities normalised over the full vocabulary, computed in bounded vocabulary chunks).
-// One pass streams E from HBM once per group of up to QG questions: every CTA owns a block of
-// vocabulary rows, keeps a running (max, sum of exp) per question, and writes one partial pair
-// per question; a second kernel combines the partials in a fixed order.
+// Tensor-core pass (the default): z = E h_hat for all questions at once is a [n_q, V] x d
+// contraction, run on the tcgen05 GEMM with h_hat rounded to f16; its epilogue reduces each row's
+// 256 logits of an N tile to a (max, sum of exp) pair, so no logit is ever stored, and E streams
+// from HBM once per 128 questions. CUDA-core pass (vocabularies that are not a multiple of 32, or
+// S1_VOCAB=simt): every CTA owns a block of vocabulary rows and keeps a running (max, sum of exp)
+// per question in fp32 over groups of up to QG questions. Either way a second kernel combines the
+// partials in a fixed order, and lm[o] = z_o - lse with z_o the readout's fp32 option logit.
+#include <algorithm>
 #include "common.cuh"
 
 namespace s1 {
@@ -107,17 +112,39 @@ __global__ void vocab_finish_kernel(const float2* __restrict__ part, int n_block
   for (int o = opt_off[q] + threadIdx.x; o < opt_off[q + 1]; o += blockDim.x) lm[o] = z[o] - s_lse;
 }
 
-size_t vocab_lm_scratch_floats(int n_q, int n_opts, int d, int num_sms) {
-  const size_t blocks = (size_t)4 * (num_sms > 0 ? num_sms : 152);
-  return (size_t)n_opts + (size_t)n_q * d + blocks * n_q * 2 + 64;
+__global__ void to_half_kernel(const float* __restrict__ x, f16* __restrict__ y, size_t n) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = f2h(x[i]);
+}
+
+static int cuda_core_blocks(int num_sms) { return 4 * (num_sms > 0 ? num_sms : 152); }
+
+size_t vocab_lm_scratch_floats(int n_q, int n_opts, int d, int V, int num_sms) {
+  const size_t tiles = (size_t)(V + GEMM_LSE_BN - 1) / GEMM_LSE_BN;
+  const size_t parts = std::max(tiles, (size_t)cuda_core_blocks(num_sms));
+  // h_hat fp32 | h_hat f16 (128-byte aligned) | partial pairs
+  return (size_t)n_opts + (size_t)n_q * d + ((size_t)n_q * d + 1) / 2 + 64 + parts * n_q * 2 + 64;
 }
 
 cudaError_t launch_vocab_lm(const f16* E, int V, int d, const float* hn, const float* z, const int* opt_off, int n_q,
-                            float* lm, float* scratch, int num_sms, cudaStream_t st, long* launches) {
+                            float* lm, float* scratch, const LaunchCtx& lc, bool tensor_cores) {
   if (n_q <= 0) return cudaSuccess;
-  const int blocks = 4 * (num_sms > 0 ? num_sms : 152);
+  cudaStream_t st = lc.stream;
+  if (tensor_cores && gemm_tc_supported(n_q, V, d, EPI_F32)) {
+    f16* h16 = reinterpret_cast<f16*>(((uintptr_t)scratch + 127) & ~(uintptr_t)127);
+    const size_t nh = (size_t)n_q * d;
+    float2* part = reinterpret_cast<float2*>(((uintptr_t)(h16 + nh) + 127) & ~(uintptr_t)127);
+    to_half_kernel<<<(unsigned)((nh + 255) / 256), 256, 0, st>>>(hn, h16, nh);
+    CK_RET(cudaGetLastError());
+    CK_RET(launch_gemm_lse(h16, E, n_q, V, d, part, n_q, lc));
+    const int tiles = (V + GEMM_LSE_BN - 1) / GEMM_LSE_BN;
+    vocab_finish_kernel<<<n_q, 256, 0, st>>>(part, tiles, n_q, opt_off, z, lm, nullptr);
+    if (lc.launches) *lc.launches += 2;   // (the GEMM counts its own launch)
+    return cudaGetLastError();
+  }
+  const int blocks = cuda_core_blocks(lc.num_sms);
   const int rows_per_block = (V + blocks - 1) / blocks;
-  float2* part = reinterpret_cast<float2*>(scratch);
+  float2* part = reinterpret_cast<float2*>(((uintptr_t)scratch + 127) & ~(uintptr_t)127);
   const int qg = (d * 4 * 8 <= 96 * 1024) ? 8 : 4;
   const size_t smem = (size_t)qg * d * sizeof(float);
   static bool attr = false;
@@ -131,7 +158,7 @@ cudaError_t launch_vocab_lm(const f16* E, int V, int d, const float* hn, const f
   if (qg == 8) vocab_lse_kernel<8><<<blocks, 256, smem, st>>>(E, V, d, hn, n_q, rows_per_block, part);
   else vocab_lse_kernel<4><<<blocks, 256, smem, st>>>(E, V, d, hn, n_q, rows_per_block, part);
   vocab_finish_kernel<<<n_q, 256, 0, st>>>(part, blocks, n_q, opt_off, z, lm, nullptr);
-  if (launches) *launches += 2;
+  if (lc.launches) *lc.launches += 2;
   return cudaGetLastError();
 }
 

@@ -41,7 +41,8 @@ def test_single_cta_plans_are_well_formed(plan, epi):
                 rc, p = plan(M, N, K, epi)
                 assert rc == 0, (M, N, K, epi)
                 bn, cm, kb = p["bn"], p["cm"], K // BK
-                assert p["pair"] == 0 and bn in SINGLE - {176, 208}, p   # 176/208: autotuner or pinned only
+                # 176/208: autotuner or pinned only, except in the few-row (<= 2 m tiles) model
+                assert p["pair"] == 0 and bn in (SINGLE if M <= 2 * BM else SINGLE - {176, 208}), p
                 assert p["m_tiles"] == -(-M // BM) and p["n_tiles"] == -(-N // bn), (M, N, K, p)
                 assert cm == 1, p
                 if epi == EPI_SWIGLU:
@@ -69,11 +70,13 @@ def test_pair_plans_are_well_formed(plan, epi):
 
 
 def test_decide_shapes_split_k(plan):
-    """64 rows (one question of the 27B-class model): the weight-streaming projections split K
-    so that about one CTA per SM streams its share of the weights."""
-    # out/down-projections (residual add), GDN in-projection, attention q/k/v
-    for (N, K, epi, bn, splits) in [(5120, 17408, EPI_RESADD, 144, 4), (5120, 4096, EPI_RESADD, 144, 4),
-                                    (12352, 5120, EPI_F32, 256, 3), (7168, 5120, EPI_F32, 192, 4)]:
+    """64 rows (one question of the 27B-class model): the weight-streaming projections get the
+    plans that measured fastest (cold caches, reduction included) in a sweep of tile widths
+    128..256 and splits 1..8 — K split where few n tiles would leave SMs idle, none where about
+    two thirds of the SMs already stream a tile each — and fill at most one wave."""
+    # down / out-projections (residual add), GDN in-projection, attention q/k/v
+    for (N, K, epi, bn, splits) in [(5120, 17408, EPI_RESADD, 144, 4), (5120, 4096, EPI_RESADD, 128, 3),
+                                    (12352, 5120, EPI_F32, 128, 1), (7168, 5120, EPI_F32, 144, 3)]:
         rc, p = plan(64, N, K, epi)
         assert rc == 0 and (p["bn"], p["splits"]) == (bn, splits), (N, K, p)
         assert p["n_tiles"] * p["splits"] <= SMS < p["n_tiles"] * (p["splits"] + 1), p   # one wave, filled

@@ -72,26 +72,57 @@ def test_every_allocation_failure_returns_oom_and_leaks_nothing(B):
             fa.reset(fail_at=n)
             m = st = None
             failed = False
+            where = "create"
             try:
                 m = B.Model(W)
+                where = "prefill"
                 st = m.prefill(req.tokens)
+                where = "decide"
                 m.decide(st, req.questions)
             except B.S1Error as e:
                 assert e.code == B.S1_ERR_OOM, (n, str(e))
                 failed = True
+                where += f" ({e})"
             assert failed, n   # the n-th request is made in every life
             if m is not None:
                 # the model is still usable: the same prefill and decide give the same results
                 fa.reset()
-                if st is not None:
-                    st.close()
-                st = m.prefill(req.tokens)
-                got = _results(m.decide(st, req.questions))
-                for (p, h), (rp, rh) in zip(got, ref):
-                    np.testing.assert_allclose(p, rp, rtol=0, atol=1e-6)
-                    np.testing.assert_allclose(h, rh, rtol=1e-6, atol=1e-6)
-                st.close()
-                m.close()
+                try:
+                    if st is not None:
+                        st.close()
+                    st = m.prefill(req.tokens)
+                    got = _results(m.decide(st, req.questions))
+                    for (p, h), (rp, rh) in zip(got, ref):
+                        msg = f"allocation {n} of {total}: {where}"
+                        np.testing.assert_allclose(p, rp, rtol=0, atol=1e-6, err_msg=msg)
+                        np.testing.assert_allclose(h, rh, rtol=1e-6, atol=1e-6, err_msg=msg)
+                finally:
+                    if st is not None:
+                        st.close()
+                    m.close()
             assert not fa.live, (n, fa.live)
     finally:
         B.use_default_allocator()
+
+
+def test_model_frees_through_the_allocator_it_was_created_with(B):
+    """Hooks installed after a model's creation do not apply to it: a model and its snapshot
+    created under one allocator give every block back to that allocator when they are closed
+    after the default allocator has been restored (no block freed through cudaFree)."""
+    W = synth.make_weights(configs.TINY)
+    req = synth.make_requests(configs.TINY)[0]
+    fa = FailingAllocator(B)
+    m = st = None
+    try:
+        m = B.Model(W)
+        st = m.prefill(req.tokens)
+        m.decide(st, req.questions)
+        assert fa.live
+    finally:
+        B.use_default_allocator()
+    try:
+        m.decide(st, req.questions + req.questions)   # may grow scratch: through the model's hooks
+    finally:
+        st.close()
+        m.close()
+    assert not fa.live, fa.live
