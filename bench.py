@@ -52,9 +52,10 @@ import numpy as np  # noqa: E402
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per tensor-core GEMM launch, averaged
-# over one step's GEMM launches in an ncu capture of this bench's timed step, per workload; a
-# workload whose kernels changed since their capture has no entry (the field reads null).
-GEMM_DRAM_BYTES_PER_LAUNCH = {"4b": 61900308}
+# over one step's GEMM launches in an ncu capture of this bench's timed step (caches not flushed
+# between launches), per workload; a workload whose kernels changed since their capture has no
+# entry (the field reads null).
+GEMM_DRAM_BYTES_PER_LAUNCH = {"4b": 75079876}
 
 
 def tensor_peak(peaks, ms_timed):
@@ -372,7 +373,7 @@ def run_batch(args, cfg, torch, ws, rank, local):
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None,
                 "traffic": GEMM_DRAM_BYTES_PER_LAUNCH.get(cfg.name),
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum, "
-                                "mean over the step's GEMM launches)",
+                                "mean over the timed step's GEMM launches, warm caches)",
                 "algorithmic_bytes_per_launch": g["bytes"] / max(1, g["count"]),
                 "peak_source": peak_source,
                 "share_of_step": g["ms"] / total_prof_ms if total_prof_ms else None,
@@ -524,7 +525,7 @@ def main():
     weight_bytes = sum(a.size * 2 for layer in W.layers for a in layer if a is not None and a.ndim == 2)
     dts = []
     nvtx_dec = os.environ.get("S1_NVTX") == "1"   # lets ncu --nvtx-include "decide/" select these calls
-    for _ in range(5):
+    for _ in range(15):
         if nvtx_dec:
             torch.cuda.nvtx.range_push("decide")
         ev[1].record(stream)
@@ -587,7 +588,7 @@ def main():
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak if peak else None,
                 "traffic": traffic,
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum, "
-                                "mean over the step's GEMM launches)",
+                                "mean over the timed step's GEMM launches, warm caches)",
                 "algorithmic_bytes_per_launch": g["bytes"] / max(1, g["count"]),
                 "peak_source": peak_source,
                 "share_of_step": g["ms"] / total_prof_ms if total_prof_ms else None,

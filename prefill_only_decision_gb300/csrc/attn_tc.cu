@@ -624,7 +624,13 @@ cudaError_t launch_attention_tc(const f16* q, const f16* knew, const f16* vnew, 
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
   // split key ranges over a cluster only when the query tiles alone leave SMs idle
-  const int nparts = work_ctas >= num_sms ? 1 : parts_for(std::max(max_keys, max_len));
+  // key ranges split over up to parts_for() CTAs while the split still fits one wave (one CTA
+  // per SM: a second wave would double the time of the whole launch)
+  int nparts = 1;
+  if (work_ctas < num_sms) {
+    const int want = parts_for(std::max(max_keys, max_len));
+    while (nparts < want && work_ctas * (nparts * 2) <= num_sms) nparts *= 2;
+  }
   const dim3 grid(((max_len + fat::BQ - 1) / fat::BQ) * nparts, Hq, n_seq);
   const CUtensorMap* cm = reinterpret_cast<const CUtensorMap*>(d_ctx_maps);
   cudaError_t e = hd == 128 ? launch_tc<128>(grid, nparts, st, mq, mk, mv, cm, out, d_seq, d_ctx, layer_f, Hq, Hkv,

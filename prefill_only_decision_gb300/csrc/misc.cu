@@ -117,9 +117,10 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, f16* out, int R, int 
 // ---- RoPE (rotate-half over the whole head) + split of the fused q|k|v projection -------
 // proj row r: [q (Hq*hd) | k (Hkv*hd) | v (Hkv*hd)] fp32. Writes q, k_new, v_new (f16) at
 // packed row r and, for sequences that own a snapshot, K/V into its cache at row = position.
-// Grid (row, item block): one thread per item, items = the (Hq + Hkv) * hd/2 rotated pairs of
-// q and k, then the Hkv * hd values of v (one round trip to memory per thread, so that a few
-// rows still spread over the whole GPU).
+// Grid (row, item block): one thread per item, items = the (Hq + Hkv) * hd/4 pairs of adjacent
+// rotated pairs of q and k (elements i, i+1 with partners i + hd/2, i+1 + hd/2), then the
+// Hkv * hd/2 pairs of v values (one round trip to memory per thread and 4-byte stores, so that a
+// few rows still spread over the whole GPU).
 __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const float2* __restrict__ tab,
                                   const int* __restrict__ row_seq, const SeqDesc* __restrict__ seqs,
                                   const CtxDesc* __restrict__ ctxs, int layer_f, f16* __restrict__ q,
@@ -128,10 +129,10 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
   allow_dependents();
   wait_prerequisites();
   const int r = blockIdx.x;
-  const int half = hd / 2;
-  const int nq = Hq * half, nk = Hkv * half;
+  const int half = hd / 2, quarter = hd / 4;
+  const int nq = Hq * quarter, nk = Hkv * quarter;
   const int t = blockIdx.y * blockDim.x + threadIdx.x;
-  if (t >= nq + nk + Hkv * hd) return;
+  if (t >= nq + nk + Hkv * half) return;
   const float* pr = proj + (size_t)r * ld;
   const SeqDesc sd = seqs[row_seq[r]];
   const int pos = sd.pos0 + (r - sd.row0);
@@ -146,25 +147,26 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
   if (t < nq + nk) {
     const bool isq = t < nq;
     const int tt = isq ? t : t - nq;
-    const int h = tt / half, i = tt % half;
+    const int h = tt / quarter, i = 2 * (tt % quarter);
     const float* src = pr + (isq ? 0 : Hq * hd) + h * hd;
-    const float x1 = src[i], x2 = src[i + half];
-    const float2 cs = tab[(size_t)pos * half + i];
-    const f16 y1 = f2h(x1 * cs.x - x2 * cs.y);
-    const f16 y2 = f2h(x2 * cs.x + x1 * cs.y);
-    if (isq) {
-      q[(size_t)r * Hq * hd + h * hd + i] = y1;
-      q[(size_t)r * Hq * hd + h * hd + i + half] = y2;
-    } else {
-      knew[(size_t)r * Hkv * hd + h * hd + i] = y1;
-      knew[(size_t)r * Hkv * hd + h * hd + i + half] = y2;
-      if (kc) { kc[h * hd + i] = y1; kc[h * hd + i + half] = y2; }
+    const float2 x1 = *reinterpret_cast<const float2*>(src + i);
+    const float2 x2 = *reinterpret_cast<const float2*>(src + i + half);
+    const float4 cs = *reinterpret_cast<const float4*>(tab + (size_t)pos * half + i);   // (cos, sin) of i, i + 1
+    const __half2 y1 = __floats2half2_rn(x1.x * cs.x - x2.x * cs.y, x1.y * cs.z - x2.y * cs.w);
+    const __half2 y2 = __floats2half2_rn(x2.x * cs.x + x1.x * cs.y, x2.y * cs.z + x1.y * cs.w);
+    f16* dst = isq ? q + (size_t)r * Hq * hd : knew + (size_t)r * Hkv * hd;
+    *reinterpret_cast<__half2*>(dst + h * hd + i) = y1;
+    *reinterpret_cast<__half2*>(dst + h * hd + i + half) = y2;
+    if (!isq && kc) {
+      *reinterpret_cast<__half2*>(kc + h * hd + i) = y1;
+      *reinterpret_cast<__half2*>(kc + h * hd + i + half) = y2;
     }
   } else {
-    const int tv = t - (nq + nk);
-    const f16 v = f2h(pr[(Hq + Hkv) * hd + tv]);
-    vnew[(size_t)r * Hkv * hd + tv] = v;
-    if (vc) vc[tv] = v;
+    const int tv = 2 * (t - (nq + nk));
+    const float2 x = *reinterpret_cast<const float2*>(pr + (Hq + Hkv) * hd + tv);
+    const __half2 v = __floats2half2_rn(x.x, x.y);
+    *reinterpret_cast<__half2*>(vnew + (size_t)r * Hkv * hd + tv) = v;
+    if (vc) *reinterpret_cast<__half2*>(vc + tv) = v;
   }
 }
 
@@ -173,10 +175,11 @@ cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab,
                               f16* knew, f16* vnew, int R, int Hq, int Hkv, int hd,
                               cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
-  const int items = (Hq + Hkv) * (hd / 2) + Hkv * hd;
-  const dim3 grid(R, (items + 255) / 256);
+  if (hd % 4 || ld % 2) return cudaErrorInvalidValue;
+  const int items = (Hq + Hkv) * (hd / 4) + Hkv * (hd / 2);
+  const dim3 grid(R, (items + 127) / 128);
   if (grid.y > 65535) return cudaErrorInvalidValue;
-  CK_RET(launch_pdl(rope_split_kernel, grid, dim3(256), 0, st, proj, ld, rope_tab, row_seq, d_seq, d_ctx, layer_f,
+  CK_RET(launch_pdl(rope_split_kernel, grid, dim3(128), 0, st, proj, ld, rope_tab, row_seq, d_seq, d_ctx, layer_f,
                     q, knew, vnew, Hq, Hkv, hd));
   return cudaGetLastError();
 }
@@ -213,9 +216,17 @@ __global__ void readout_kernel(const float* __restrict__ x, const float* __restr
   float* hn = sm;            // [d]
   float* z = sm + d;         // [n]
   __shared__ float red[32];
+  allow_dependents();
   const int j = blockIdx.x;
   const int row = q_row[j];
   const int o0 = opt_off[j], n = opt_off[j + 1] - o0;
+  // the option rows of the tied embedding do not depend on earlier kernels: ask L2 for them
+  // while the last layer finishes
+  for (int i = threadIdx.x; i < n * (d / 64); i += blockDim.x) {
+    const f16* e = E + (size_t)opt_ids[o0 + i / (d / 64)] * d + (i % (d / 64)) * 64;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(e));
+  }
+  wait_prerequisites();
   const float* h = x + (size_t)row * d;
   float ss = 0.f;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
@@ -234,7 +245,19 @@ __global__ void readout_kernel(const float* __restrict__ x, const float* __restr
   for (int m = w; m < n; m += nw) {
     const f16* e = E + (size_t)opt_ids[o0 + m] * d;
     float acc = 0.f;
-    for (int i = lane; i < d; i += 32) acc += hn[i] * h2f(e[i]);
+    if (d % 256 == 0) {   // eight halves per lane and load
+      for (int i = 8 * lane; i < d; i += 256) {
+        const uint4 u = *reinterpret_cast<const uint4*>(e + i);
+        const __half2* e2 = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(e2[k]);
+          acc += hn[i + 2 * k] * f.x + hn[i + 2 * k + 1] * f.y;
+        }
+      }
+    } else {
+      for (int i = lane; i < d; i += 32) acc += hn[i] * h2f(e[i]);
+    }
     acc = warp_sum(acc);
     if (lane == 0) {
       z[m] = acc;
@@ -278,8 +301,11 @@ cudaError_t launch_readout(const float* x, const float* final_norm, const f16* E
                            int max_opts, float* hn_out, float* z_out, cudaStream_t st) {
   if (n_q <= 0) return cudaSuccess;
   const size_t smem = (size_t)(d + max_opts) * sizeof(float);
-  readout_kernel<<<n_q, 256, smem, st>>>(x, final_norm, E, d, eps, q_row, q_type, opt_off, opt_ids,
-                                         probs, stats, hidden, hn_out, z_out);
+  if (smem > 48 * 1024) {
+    CK_RET(cudaFuncSetAttribute(readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  }
+  CK_RET(launch_pdl(readout_kernel, dim3(n_q), dim3(256), smem, st, x, final_norm, E, d, eps, q_row, q_type, opt_off,
+                    opt_ids, probs, stats, hidden, hn_out, z_out));
   return cudaGetLastError();
 }
 
