@@ -271,13 +271,9 @@ constexpr int STG_BYTES = 4 * 2 * 2048;
 // Shared memory left for pipeline stages: the opt-in maximum less staging, barriers and alignment.
 constexpr int STAGE_BUDGET = 232448 - STG_BYTES - 1024 - 256;
 
-// AR: A rows loaded per stage. 128 (BM) in general; 64 for products of at most 64 rows, whose
-// stage then holds only the 64 rows the product has (the MMA still runs 128 rows: the other 64
-// read the next bytes of shared memory, and their accumulator rows are never stored), so that
-// more weight tiles are in flight in the same shared memory.
-template <int BN, int AR = BM>
+template <int BN>
 struct Cfg {
-  static constexpr int A_BYTES = AR * BK * 2;
+  static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = STAGE_BUDGET / STAGE_BYTES > 8 ? 8 : STAGE_BUDGET / STAGE_BYTES;
@@ -433,11 +429,11 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, const CUtensorMap
 // One CTA per SM, each loading its own A and B tiles; CTAs that run at the same time work on
 // consecutive m tiles of the same n tile, so a weight tile is read from DRAM once and served to
 // the others from L2.
-template <int BN, int AR = BM>
+template <int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapO, Params p) {
-  using C = Cfg<BN, AR>;
+  using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
@@ -897,17 +893,15 @@ namespace tc {
 
 struct Plan {
   int bn, m_tiles, n_tiles, splits, kb_per_split, kb_total, units, grid;
-  int pair;        // 1: CTA-pair kernel (256-row tiles, cta_group::2); bn is the pair's tile width
-  int arows = BM;  // single-CTA kernel: A rows loaded per stage (64 for at most 64 rows)
+  int pair;   // 1: CTA-pair kernel (256-row tiles, cta_group::2); bn is the pair's tile width
 };
-inline int arows_for(int M) { return M <= 64 ? 64 : BM; }
 
 inline int max_ctas_of(int bn, int num_sms);
 
 // The single-CTA plan of a fixed tile width without a K split.
 inline Plan plan_with(int M, int N, int K, int bn) {
   const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + bn - 1) / bn, kb = K / BK;
-  return Plan{bn, m_tiles, n_tiles, 1, kb, kb, m_tiles * n_tiles, 0, 0, arows_for(M)};
+  return Plan{bn, m_tiles, n_tiles, 1, kb, kb, m_tiles * n_tiles, 0, 0};
 }
 
 // The CTA-pair plan of tile width bn (no K split): m_tiles counts 128-row halves, units pairs.
@@ -973,7 +967,7 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
         const double cost = few_rows_cost_us(N, K, bn, kbp, sp, units, maxc);
         if (cost < best_cost * 0.97) {
           best_cost = cost;
-          best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, 0, 0, arows_for(M)};
+          best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, 0, 0};
         }
       }
     }
@@ -1003,7 +997,7 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
       if (sp > 1) cost *= 1.0 + 0.04 * sp;
       if ((force_sp <= 0 || sp == force_sp) && cost < best_cost * 0.999) {
         best_cost = cost;
-        best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, 0, 0, arows_for(M)};
+        best = Plan{bn, m_tiles, n_tiles, sp, kbp, kb_total, units, 0, 0};
       }
       if (force_sp <= 0 && units >= maxc) break;
     }
@@ -1012,11 +1006,11 @@ Plan plan_for(int M, int N, int K, int epi, int num_sms, size_t ws_cap) {
   return best;
 }
 
-template <int BN, int AR = BM>
+template <int BN>
 cudaLaunchConfig_t launch_config(cudaLaunchAttribute* attr, cudaStream_t st, bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = Cfg<BN, AR>::SMEM;
+  cfg.dynamicSmemBytes = Cfg<BN>::SMEM;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1026,15 +1020,14 @@ cudaLaunchConfig_t launch_config(cudaLaunchAttribute* attr, cudaStream_t st, boo
 }
 
 // CTAs of this tile width that fit on the GPU at once (queried once, then cached).
-template <int BN, int AR = BM>
+template <int BN>
 int max_ctas(int num_sms) {
   static int cached = -1;
   if (cached < 0) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_kernel<BN, AR>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN, AR>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<BN>::SMEM);
     int per_sm = 0;
     if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<BN, AR>, NUM_THREADS, Cfg<BN, AR>::SMEM);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_kernel<BN>, NUM_THREADS, Cfg<BN>::SMEM);
     if (e != cudaSuccess || per_sm <= 0) {
       cudaGetLastError();
       per_sm = 1;
@@ -1116,17 +1109,17 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
   return cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN>, ma, mb, mo, p);
 }
 
-template <int BN, int AR = BM>
+template <int BN>
 cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo, Params p, int num_sms,
                       cudaStream_t st) {
-  const int mc = max_ctas<BN, AR>(num_sms);
+  const int mc = max_ctas<BN>(num_sms);
   cudaLaunchAttribute attr[1];
   const bool pdl = pdl_enabled();
-  cudaLaunchConfig_t cfg = launch_config<BN, AR>(attr, st, pdl);
+  cudaLaunchConfig_t cfg = launch_config<BN>(attr, st, pdl);
   p.m_groups = p.m_tiles;
   p.units = p.m_groups * p.splits * p.n_tiles;
   cfg.gridDim = dim3(p.units < mc ? p.units : mc);
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN, AR>, ma, mb, mo, p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, ma, mb, mo, p);
 }
 
 }  // namespace tc
@@ -1152,8 +1145,7 @@ static cudaError_t launch_plan(const tc::Plan& pl, const f16* X, const f16* W, i
                                void* out, int ldo, float* splitk_ws, const LaunchCtx& lc) {
   CUtensorMap ma, mb;
   const int brows = pl.pair ? pl.bn / 2 : pl.bn;
-  const int arows = pl.pair ? tc::BM : pl.arows;
-  if (!tc::make_map(&ma, X, M, K, arows) || !tc::make_map(&mb, W, N, K, brows)) return cudaErrorInvalidValue;
+  if (!tc::make_map(&ma, X, M, K, tc::BM) || !tc::make_map(&mb, W, N, K, brows)) return cudaErrorInvalidValue;
   tc::Params p;
   p.M = M; p.N = N; p.K = K;
   p.m_tiles = pl.m_tiles; p.n_tiles = pl.n_tiles; p.splits = pl.splits;
@@ -1189,13 +1181,6 @@ static cudaError_t launch_plan(const tc::Plan& pl, const f16* X, const f16* W, i
       case 176: e = tc::launch_pair<176>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
       default: e = tc::launch_pair<128>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
     }
-  } else if (arows == 64) switch (pl.bn) {
-    case 256: e = tc::launch_bn<256, 64>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
-    case 208: e = tc::launch_bn<208, 64>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
-    case 192: e = tc::launch_bn<192, 64>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
-    case 176: e = tc::launch_bn<176, 64>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
-    case 144: e = tc::launch_bn<144, 64>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
-    default: e = tc::launch_bn<128, 64>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
   } else switch (pl.bn) {
     case 256: e = tc::launch_bn<256>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
     case 208: e = tc::launch_bn<208>(ma, mb, mo, p, lc.num_sms, lc.stream); break;
