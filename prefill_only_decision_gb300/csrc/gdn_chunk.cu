@@ -131,7 +131,10 @@ struct PrepSmem {
   float la[C];                             // log alpha
 };
 
-template <int D>
+// SPLIT: the chunks need no state step (questions that continue a snapshot) and the right-hand
+// side is split over two CTAs per (chunk, head): blockIdx.z = 0 solves for W (and writes the
+// normalised k and g), 1 for Ut; both form A and its diagonal-block inverses.
+template <int D, bool SPLIT = false>
 __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restrict__ proj, int ld,
                                                             float* __restrict__ gout,
                                                             const ChunkDesc* __restrict__ chunks,
@@ -140,6 +143,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
   allow_dependents();
   wait_prerequisites();
   using SM = PrepSmem<D>;
+  const int half = SPLIT ? (int)blockIdx.z : 0;
   constexpr int SK = SM::SK, SX = SM::SX, SA = SM::SA, SAH = SM::SAH, ST = SM::ST, S17 = SM::S17;
   constexpr int PER = D / 4;               // columns per thread in the row-wise phases
   extern __shared__ __align__(16) uint8_t smraw[];
@@ -217,9 +221,14 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
         uu[j] = h2u(vv[i + 2 * j] * bt, vv[i + 2 * j + 1] * bt);
       }
       *reinterpret_cast<uint4*>(&s.Kh[r * SK + c0 + i]) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
-      *reinterpret_cast<uint4*>(&s.X[r * SX + c0 + i]) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
-      *reinterpret_cast<uint4*>(&s.X[r * SX + D + c0 + i]) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
-      if (r < n) *reinterpret_cast<uint4*>(kg + i) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
+      if constexpr (SPLIT) {   // this CTA's half of the right-hand side, in X's first D columns
+        *reinterpret_cast<uint4*>(&s.X[r * SX + c0 + i]) =
+            half ? make_uint4(uu[0], uu[1], uu[2], uu[3]) : make_uint4(ww[0], ww[1], ww[2], ww[3]);
+      } else {
+        *reinterpret_cast<uint4*>(&s.X[r * SX + c0 + i]) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+        *reinterpret_cast<uint4*>(&s.X[r * SX + D + c0 + i]) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
+      }
+      if (r < n && half == 0) *reinterpret_cast<uint4*>(kg + i) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
     }
   }
   __syncthreads();
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
   }
   __syncthreads();
   // ---- block forward substitution over the 4 row blocks; each warp owns NT n-tiles of X
-  constexpr int NT = 2 * D / 64;           // n-tiles per warp (D = 128: 4, D = 64: 2)
+  constexpr int NT = (SPLIT ? 1 : 2) * D / 64;   // n-tiles per warp (D = 128: 4, D = 64: 2; halved when split)
   const int cw = warp * NT * 8;            // this warp's first column of X
   for (int bb = 0; bb < 4; ++bb) {
     const int r0 = bb * 16;
@@ -358,14 +367,25 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
   }
   __syncthreads();
   // W and Ut rows (16-byte pieces) and g
-  for (int i = tid; i < n * (2 * D / 8); i += 256) {
-    const int rr = i / (2 * D / 8), c8 = (i % (2 * D / 8)) * 8;
-    const uint4 v = *reinterpret_cast<const uint4*>(&s.X[rr * SX + c8]);
-    const size_t o = ((size_t)(cd.row0 + rr) * H + h) * D;
-    *reinterpret_cast<uint4*>(c8 < D ? bufs.W + o + c8 : bufs.Ut + o + c8 - D) = v;
+  if constexpr (SPLIT) {
+    for (int i = tid; i < n * (D / 8); i += 256) {
+      const int rr = i / (D / 8), c8 = (i % (D / 8)) * 8;
+      const uint4 v = *reinterpret_cast<const uint4*>(&s.X[rr * SX + c8]);
+      const size_t o = ((size_t)(cd.row0 + rr) * H + h) * D;
+      *reinterpret_cast<uint4*>((half ? bufs.Ut : bufs.W) + o + c8) = v;
+    }
+    if (tid < n && half == 0) gout[(size_t)(cd.row0 + tid) * H + h] = s.g[tid];
+  } else {
+    for (int i = tid; i < n * (2 * D / 8); i += 256) {
+      const int rr = i / (2 * D / 8), c8 = (i % (2 * D / 8)) * 8;
+      const uint4 v = *reinterpret_cast<const uint4*>(&s.X[rr * SX + c8]);
+      const size_t o = ((size_t)(cd.row0 + rr) * H + h) * D;
+      *reinterpret_cast<uint4*>(c8 < D ? bufs.W + o + c8 : bufs.Ut + o + c8 - D) = v;
+    }
+    if (tid < n) gout[(size_t)(cd.row0 + tid) * H + h] = s.g[tid];
   }
-  if (tid < n) gout[(size_t)(cd.row0 + tid) * H + h] = s.g[tid];
-  if (!need_nb) return;
+  // (split chunks take no state step: no K', N^T or gamma_n)
+  if (SPLIT || !need_nb) return;
   // ---- K'_t = exp(g_n - g_t) k_t (into the series scratch, no longer read, and to global), gamma_n
   {
     const float gl = s.g[n - 1];
@@ -956,6 +976,9 @@ static cudaError_t launch_chunked_d(const float* proj, int ld, float* gbuf, floa
   const size_t sp = sizeof(gc::PrepSmem<D>);
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(gc::chunk_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
+    if constexpr (D == 128)
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gc::chunk_prep_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gc::chunk_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)state_smem<D>());
@@ -971,8 +994,19 @@ static cudaError_t launch_chunked_d(const float* proj, int ld, float* gbuf, floa
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  CK_RET(launch_pdl(gc::chunk_prep_kernel<D>, dim3(n_chunks, H), dim3(256), sp, st, proj, ld, gbuf, d_chunks, d_seq, H,
-                    eps, bufs));
+  // every sequence a single chunk that continues a snapshot (the questions of a decide call) and
+  // too few (chunk, head) pairs to fill the GPU: the right-hand side of the solve is split over
+  // two CTAs per pair
+  bool split_prep = false;
+  if constexpr (D == 128) split_prep = out_fold == 0 && (long)n_chunks * H * 2 <= 2L * num_sms;
+  if (split_prep) {
+    if constexpr (D == 128)
+      CK_RET(launch_pdl(gc::chunk_prep_kernel<D, true>, dim3(n_chunks, H, 2), dim3(256), sp, st, proj, ld, gbuf,
+                        d_chunks, d_seq, H, eps, bufs));
+  } else {
+    CK_RET(launch_pdl(gc::chunk_prep_kernel<D>, dim3(n_chunks, H), dim3(256), sp, st, proj, ld, gbuf, d_chunks, d_seq,
+                      H, eps, bufs));
+  }
   // TMA views of the state pass's tiles: N^T [n_chunks * H * D rows, D columns] (boxes of 64
   // columns x D rows), K' and Ut [R, H, D] (64 rows of one head: 64-column swizzled boxes of K',
   // the CTA's 16 columns of Ut)
