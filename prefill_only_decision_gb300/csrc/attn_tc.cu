@@ -232,7 +232,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   allow_dependents();
   wait_prerequisites();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const SeqDesc sd = seqs[blockIdx.z];
+  // sequences in reverse call order: the calls list the prefixes first and the sequences that
+  // continue them (whose query tiles see the most keys) after, so those start in the first wave
+  const SeqDesc sd = seqs[gridDim.z - 1 - blockIdx.z];
   const int part = (int)(blockIdx.x % nparts);
   const int q0 = ((int)(gridDim.x / nparts) - 1 - (int)(blockIdx.x / nparts)) * BQ;   // longest tiles first
   const int h = blockIdx.y, g = (h * Hkv) / Hq;

@@ -466,15 +466,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   fence_after();
   const uint32_t tmem_base = *tmem_slot;
   allow_dependents();
-  // The weights do not depend on earlier kernels: the first weight tiles go to L2 while the
-  // kernel producing this GEMM's activations may still be running.
+  // The weights do not depend on earlier kernels: while the kernel producing this GEMM's
+  // activations may still be running, the first unit's weight tiles are requested into the
+  // pipeline's stages (their A tiles follow after the wait) and the next ones into L2.
+  int early = 0;   // stages of the first unit whose weight tile is already requested
   if (warp == 0 && lane == 0 && cid < p.units) {
     const int u = cid;
     const int mg = u % p.m_groups, rest = u / p.m_groups, sp = rest % p.splits, nt = rest / p.splits;
-    if (mg == 0) {
-      const int kb0 = sp * p.kb_per_split, kb1 = min(p.kb_total, kb0 + p.kb_per_split);
-      for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, nt * BN);
+    const int kb0 = sp * p.kb_per_split, kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+    early = min(C::STAGES, kb1 - kb0);
+    for (int i = 0; i < early; ++i) {
+      mbar_expect_tx(&full[i], C::STAGE_BYTES);
+      tma_load_2d(sB + i * C::B_BYTES, &mapB, &full[i], (kb0 + i) * BK, nt * BN);
     }
+    if (mg == 0)
+      for (int kb = kb0 + early; kb < min(kb1, kb0 + early + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, nt * BN);
   }
   wait_prerequisites();
 
@@ -499,10 +505,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kb = kb0; kb < min(kb1, kb0 + PF); ++kb) tma_prefetch_l2(&mapB, kb * BK, brow);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (pf && kb + PF < kb1) tma_prefetch_l2(&mapB, (kb + PF) * BK, brow);
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
-          mbar_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sA + stage * C::A_BYTES, &mapA, &full[stage], kb * BK, mt * BM);
-          tma_load_2d(sB + stage * C::B_BYTES, &mapB, &full[stage], kb * BK, brow);
+          if (u == cid && kb - kb0 < early) {
+            // (a fresh stage whose weight tile and byte count were set before the wait)
+            tma_load_2d(sA + stage * C::A_BYTES, &mapA, &full[stage], kb * BK, mt * BM);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.d_err, ERR_TIMEOUT_EMPTY)) { ok = false; break; }
+            mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load_2d(sA + stage * C::A_BYTES, &mapA, &full[stage], kb * BK, mt * BM);
+            tma_load_2d(sB + stage * C::B_BYTES, &mapB, &full[stage], kb * BK, brow);
+          }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }
