@@ -554,23 +554,24 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  int issued = 0;                              // steps whose tiles were requested (thread 0)
-  auto issue = [&](int cl) {
+  int issued = 0;                              // steps whose tiles were requested (warp 0)
+  // warp 0 requests a step's tiles: lane 0 sets the byte count, then one copy per lane (the
+  // D / 64 boxes of N^T and of K', and the Ut block)
+  auto issue = [&](int cl, int ln) {
     const int st = cl % NS;
     uint8_t* sb = s.stage[st];
-    bar_expect_tx(&s.full[st], SM::STAGE);
+    if (ln == 0) bar_expect_tx(&s.full[st], SM::STAGE);
+    __syncwarp();
     const int ci = sd.chunk0 + cl;
     const int row0 = sd.row0 + cl * C;         // the chunk's first packed row
-#pragma unroll
-    for (int b = 0; b < D / 64; ++b) {
-      tma2(sb + b * D * 128, &mapNT, &s.full[st], 64 * b, (ci * H + h) * D);
-      tma3(sb + SM::NT_BYTES + b * C * 128, &mapKp, &s.full[st], 64 * b, h, row0);
-    }
-    tma3(sb + SM::NT_BYTES + SM::KP_BYTES, &mapUt, &s.full[st], v0, h, row0);
+    constexpr int NB = D / 64;
+    if (ln < NB) tma2(sb + ln * D * 128, &mapNT, &s.full[st], 64 * ln, (ci * H + h) * D);
+    else if (ln < 2 * NB) tma3(sb + SM::NT_BYTES + (ln - NB) * C * 128, &mapKp, &s.full[st], 64 * (ln - NB), h, row0);
+    else if (ln == 2 * NB) tma3(sb + SM::NT_BYTES + SM::KP_BYTES, &mapUt, &s.full[st], v0, h, row0);
     ++issued;
   };
-  if (tid == 0)
-    for (int cl = 0; cl < nupd && cl < NS; ++cl) issue(cl);
+  if (warp == 0)
+    for (int cl = 0; cl < nupd && cl < NS; ++cl) issue(cl, lane);
   // gamma_n of the first steps
   for (int i = tid; i < nupd && i < SM::GAM; i += blockDim.x) s.gam[i] = gam[(size_t)(sd.chunk0 + i) * H + h];
   // the state block's fragments: rows v0 + gq and v0 + gq + 8, columns cw + 8 nt + 2 tq and + 1
@@ -601,13 +602,14 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
     }
   };
   put(0, sd.chunk0);
-  // Everything a step needs from its tiles is taken before the barrier that ends the previous
-  // step: the B block = Ut_b^T K' over this warp's 16 columns (independent of the state; rows
-  // t >= n of both tiles are zeroed in the fragments), kept in qv, and this warp's N fragments,
-  // kept in nb. After the barrier a step is only Sr x N, the update and the f16 copy.
-  float qv[2][4];
-  uint32_t nb[KS][2][4];
-  auto take_tiles = [&](int cl) {
+  // Everything a step needs from its tiles is taken during the step before it, while that step's
+  // Sr x N products are in flight: the B block = Ut_b^T K' over this warp's 16 columns
+  // (independent of the state; rows t >= n of both tiles are zeroed in the fragments), kept in
+  // qv, and this warp's N fragments, kept in nb (qv2 / nb2 for the next step). After the barrier
+  // a step is only Sr x N, the update and the f16 copy.
+  float qv[2][4], qv2[2][4];
+  uint32_t nb[KS][2][4], nb2[KS][2][4];
+  auto take_tiles = [&](int cl, float (&qo)[2][4], uint32_t (&no)[KS][2][4]) {
     const uint8_t* sb = s.stage[cl % NS];
     const __half* ntile = reinterpret_cast<const __half*>(sb);
     const uint32_t kp_base = smem_u32(sb + SM::NT_BYTES);
@@ -651,17 +653,17 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qv[nt][i] = q[nt][0][i] + q[nt][1][i];
+      for (int i = 0; i < 4; ++i) qo[nt][i] = q[nt][0][i] + q[nt][1][i];
 #pragma unroll
     for (int i = 0; i < KS; ++i)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
-        ldsm4(smem_u32(ntile + nt_off<D>(cw + 8 * nt + (lane & 7), 32 * i + 8 * (lane >> 3))), nb[i][nt]);
+        ldsm4(smem_u32(ntile + nt_off<D>(cw + 8 * nt + (lane & 7), 32 * i + 8 * (lane >> 3))), no[i][nt]);
   };
   // the first tiles; one barrier agrees on their arrival and on Sr and gamma being in place
   bool ok = __syncthreads_and(nupd > 0 ? (bar_wait(&s.full[0], 0) ? 1 : 0) : 1) != 0;
   int waited = (ok && nupd > 0) ? 1 : 0;     // steps whose tiles have arrived
-  if (ok && nupd > 0) take_tiles(0);
+  if (ok && nupd > 0) take_tiles(0, qv, nb);
   int cur = 0;
   for (int cl = 0; cl < nupd && ok; ++cl) {
     // Sr (16 x D) x N (D x D) over this warp's 16 columns: the A fragments are shared by both
@@ -678,23 +680,34 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
         mma16(p[nt][i & 1], a1, nb[i][nt][2], nb[i][nt][3]);
       }
     }
+    // the next step's tiles, taken while those products complete
+    bool w = true;
+    if (cl + 1 < nupd) {
+      w = bar_wait(&s.full[(cl + 1) % NS], ((cl + 1) / NS) & 1);
+      if (w) take_tiles(cl + 1, qv2, nb2);
+    }
     const float g = s.gam[cl % SM::GAM];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[nt][i] = fmaf(g, acc[nt][i], qv[nt][i] - (p[nt][0][i] + p[nt][1][i]));
     put(cur ^ 1, cl + 1 < nch ? sd.chunk0 + cl + 1 : -1);
-    // the next step's tiles, then one barrier that agrees on them, on Sr being complete and on
-    // this step's tiles having been read by every warp
-    bool w = true;
-    if (cl + 1 < nupd) {
-      w = bar_wait(&s.full[(cl + 1) % NS], ((cl + 1) / NS) & 1);
-      if (w) take_tiles(cl + 1);
-    }
+    // one barrier that agrees on the next step's tiles, on Sr being complete and on the tiles
+    // of this step and the next having been read by every warp
     ok = __syncthreads_and(w ? 1 : 0) != 0;
     if (!ok) break;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[nt][i] = qv2[nt][i];
+#pragma unroll
+    for (int i = 0; i < KS; ++i)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) nb[i][nt][j] = nb2[i][nt][j];
     if (cl + 1 < nupd) ++waited;
-    if (tid == 0 && cl + NS < nupd) issue(cl + NS);   // refill the stage this step consumed
+    if (warp == 0 && cl + NS < nupd) issue(cl + NS, lane);   // refill the stage this step consumed
     cur ^= 1;
     if ((cl + 1) % SM::GAM == 0 && cl + 1 < nupd) {   // the next block of gamma_n
       for (int i = tid; i < SM::GAM && cl + 1 + i < nupd; i += blockDim.x)
