@@ -106,9 +106,8 @@ __device__ __forceinline__ float4 ld4(const float* src, bool ok) {
 // when a state pass takes a step over this chunk, K' (f16 [R, H, D]), N^T (f16 [chunks, H, D, D])
 // and gamma_n.
 // The unit-lower-triangular system (I + A) X = [diag(beta gamma) K | diag(beta) V] is solved in
-// 16-row blocks: each 16 x 16 diagonal block's inverse comes from the nilpotent series
-// (I + N)^-1 = (I - N)(I + N^2)(I + N^4)(I + N^8) (N strictly lower, N^16 = 0) in fp32, then
-// X_b = T_bb (RHS_b - sum_{c<b} A_bc X_c) on the tensor cores.
+// 16-row blocks: each 16 x 16 diagonal block's inverse T_bb comes from forward substitution in
+// fp32 (one thread per column), then X_b = T_bb (RHS_b - sum_{c<b} A_bc X_c) on the tensor cores.
 template <int D>
 struct PrepSmem {
   static constexpr int SK = D + 8;         // f16 stride of D-wide tiles
@@ -116,14 +115,12 @@ struct PrepSmem {
   static constexpr int SA = C + 4;         // fp32 A
   static constexpr int SAH = C + 8;        // f16 A
   static constexpr int ST = 24;            // f16 diagonal-block inverses
-  static constexpr int S17 = 16 * 17;      // 16 x 16 fp32 scratch, row stride 17
   __half Kh[C * SK];                       // normalised k
   __half X[C * SX];
   __half Ah[C * SAH];
   __half T[4][16 * ST];
   float A[C * SA];
-  union {
-    float M[3][4 * S17];                   // series scratch (diagonal-block inverses)
+  struct {
     __half Kp[C * SK];                     // K'_t = exp(g_n - g_t) k_t (after the solve)
   } u;
   float g[C];
@@ -144,7 +141,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
   wait_prerequisites();
   using SM = PrepSmem<D>;
   const int half = SPLIT ? (int)blockIdx.z : 0;
-  constexpr int SK = SM::SK, SX = SM::SX, SA = SM::SA, SAH = SM::SAH, ST = SM::ST, S17 = SM::S17;
+  constexpr int SK = SM::SK, SX = SM::SX, SA = SM::SA, SAH = SM::SAH, ST = SM::ST;
   constexpr int PER = D / 4;               // columns per thread in the row-wise phases
   extern __shared__ __align__(16) uint8_t smraw[];
   SM& s = *reinterpret_cast<SM*>(smraw);
@@ -260,53 +257,26 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
       }
   }
   __syncthreads();
-  // ---- diagonal-block inverses by the nilpotent series; thread -> block bb, row i, cols j0..j0+3
-  {
-    const int bb = tid >> 6, e = tid & 63, i = e >> 2, j0 = (e & 3) * 4;
-    float* N = s.u.M[0] + bb * S17;
+  // ---- diagonal-block inverses T_bb = (I + N_bb)^-1, N_bb the strictly lower 16 x 16 diagonal
+  // block of A: forward substitution in fp32, one thread per (block, column j):
+  // x_i = [i == j] - sum_{k < i} N_ik x_k (rows i < j come out zero)
+  if (tid < 64) {
+    const int bb = tid >> 4, j = tid & 15;
+    const float* Nb = s.A + bb * 16 * SA + bb * 16;
+    float x[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) N[i * 17 + j0 + j] = s.A[(bb * 16 + i) * SA + bb * 16 + j0 + j];
-    __syncthreads();
-    auto mm = [&](const float* Y, const float* Z, float* o) {   // o[4] = (Y Z)[i][j0..j0+3]
-      o[0] = o[1] = o[2] = o[3] = 0.f;
+    for (int i = 0; i < 16; ++i) {
+      float a0 = i == j ? 1.f : 0.f, a1 = 0.f;   // two partial sums: shorter dependent chains
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float y = Y[i * 17 + k];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = fmaf(y, Z[k * 17 + j0 + j], o[j]);
+      for (int k = 0; k + 1 < i; k += 2) {
+        a0 = fmaf(-Nb[i * SA + k], x[k], a0);
+        a1 = fmaf(-Nb[i * SA + k + 1], x[k + 1], a1);
       }
-    };
-    float* Pa = s.u.M[1] + bb * S17;
-    float* Pb = s.u.M[2] + bb * S17;
-    float o[4], tt[4];
-    mm(N, N, o);                                   // P1 = N^2
-#pragma unroll
-    for (int j = 0; j < 4; ++j) Pa[i * 17 + j0 + j] = o[j];
-    __syncthreads();
-    mm(N, Pa, o);                                  // N P1
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {                  // T1 = (I - N)(I + P1) = I - N + P1 - N P1
-      const int c = j0 + j;
-      tt[j] = (i == c ? 1.f : 0.f) - N[i * 17 + c] + Pa[i * 17 + c] - o[j];
+      if (i & 1) a0 = fmaf(-Nb[i * SA + i - 1], x[i - 1], a0);
+      x[i] = a0 + a1;
     }
-    mm(Pa, Pa, o);                                 // P2 = P1^2
-    __syncthreads();
 #pragma unroll
-    for (int j = 0; j < 4; ++j) { N[i * 17 + j0 + j] = tt[j]; Pb[i * 17 + j0 + j] = o[j]; }   // N <- T1
-    __syncthreads();
-    mm(N, Pb, o);                                  // T1 P2
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tt[j] = N[i * 17 + j0 + j] + o[j];   // T2 = T1 (I + P2)
-    mm(Pb, Pb, o);                                 // P3 = P2^2
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) { N[i * 17 + j0 + j] = tt[j]; Pa[i * 17 + j0 + j] = o[j]; }  // N <- T2
-    __syncthreads();
-    mm(N, Pa, o);                                  // T2 P3
-#pragma unroll
-    for (int j = 0; j < 4; j += 2)                 // T3 = T2 (I + P3)
-      *reinterpret_cast<uint32_t*>(&s.T[bb][i * ST + j0 + j]) =
-          h2u(N[i * 17 + j0 + j] + o[j], N[i * 17 + j0 + j + 1] + o[j + 1]);
+    for (int i = 0; i < 16; ++i) s.T[bb][i * ST + j] = __float2half_rn(x[i]);
   }
   __syncthreads();
   // ---- block forward substitution over the 4 row blocks; each warp owns NT n-tiles of X
@@ -386,7 +356,7 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
   }
   // (split chunks take no state step: no K', N^T or gamma_n)
   if (SPLIT || !need_nb) return;
-  // ---- K'_t = exp(g_n - g_t) k_t (into the series scratch, no longer read, and to global), gamma_n
+  // ---- K'_t = exp(g_n - g_t) k_t (into shared memory and to global), gamma_n
   {
     const float gl = s.g[n - 1];
     for (int i = tid; i < C * (D / 8); i += 256) {
@@ -740,9 +710,10 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------------------
-// chunk_out: one CTA per (chunk, head, value slice), 256 threads. A CTA forms the output columns
-// [vs * D/VS, (vs + 1) * D/VS) of its head; the launcher splits the value columns over VS CTAs
-// when (chunks x heads) alone leaves SMs idle (a few questions over a snapshot).
+// chunk_out: one CTA per (chunk, head, value slice), 256 threads, two CTAs per SM. A CTA forms
+// the output columns [vs * D/VS, (vs + 1) * D/VS) of its head; the launcher splits the value
+// columns over VS CTAs when (chunks x heads) alone leaves SMs idle (a few questions over a
+// snapshot).
 //   P = lower_incl(Gamma * Q K^T),  U = Ut - W S_c^T,  O = diag(gamma) Q S_c^T + P U
 // with S_c the chunk's start state: the state pass's record, or (a single-chunk sequence without
 // a state pass) the snapshot's state it continues, or zero.
@@ -761,7 +732,7 @@ struct OutSmem {
 };
 
 template <int D, int VS>
-__global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict__ proj, int ld,
+__global__ void __launch_bounds__(256, 2) chunk_out_kernel(const float* __restrict__ proj, int ld,
                                                         const float* __restrict__ gbuf,
                                                         const ChunkDesc* __restrict__ chunks, int H, float eps,
                                                         GdnBufs bufs, const SeqDesc* __restrict__ seqs,
@@ -781,6 +752,8 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const size_t DD = (size_t)D * D;
+  const bool fold = cd.seq >= out_fold;
+  const int cin = fold ? seqs[cd.seq].ctx_in : -1;
   for (int i = tid; i < C * (D / 8); i += 256) {
     const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
     const bool ok = r < n;
@@ -788,7 +761,6 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
     cp16(&s.K[r * SK + c8], bufs.Kn + o, ok);
     cp16(&s.W[r * SK + c8], bufs.W + o, ok);
   }
-  const bool fold = cd.seq >= out_fold;
   if (!fold) {
     const f16* rec = bufs.Srec + ((size_t)ci * H + h) * DD + (size_t)cs * D;
     for (int i = tid; i < DW * (D / 8); i += 256) {
@@ -798,7 +770,6 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(const float* __restrict_
   }
   cp_commit();
   if (fold) {
-    const int cin = seqs[cd.seq].ctx_in;
     const float* S0 = cin >= 0 ? ctxs[cin].S + (size_t)(layer_g * H + h) * DD + (size_t)cs * D : nullptr;
     for (int i = tid; i < DW * (D / 4); i += 256) {
       const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;

@@ -205,7 +205,10 @@ cudaError_t launch_rope_table(float2* tab, int max_pos, int hd, double theta, cu
 // ---- decision readout -----------------------------------------------------------------
 // One block per question: final RMSNorm of its last row, tied-embedding logits over its
 // option ids (fp32), softmax, argmax, expected level, yes probability and confidences.
-__global__ void readout_kernel(const float* __restrict__ x, const float* __restrict__ fnorm,
+// (x, the residual stream, is the previous kernels' output and is read only after the wait: it
+// carries no __restrict__, so its loads are not treated as invariant and cannot move above the
+// wait)
+__global__ void readout_kernel(const float* x, const float* __restrict__ fnorm,
                                const f16* __restrict__ E, int d, float eps,
                                const int* __restrict__ q_row, const int* __restrict__ q_type,
                                const int* __restrict__ opt_off, const int* __restrict__ opt_ids,
