@@ -229,8 +229,10 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
     }
   }
   __syncthreads();
-  // ---- A = strict_lower(beta_t exp(g_t - g_s) k_t.k_s): warp -> m-tile (warp & 3), 4 n-tiles
-  {
+  // ---- A = strict_lower(beta_t exp(g_t - g_s) k_t.k_s): warp -> m-tile (warp & 3), 4 n-tiles.
+  // Only the strictly lower part is ever read (the diagonal blocks' inverses and the blocks left
+  // of them), so the two warps whose tiles lie wholly above the diagonal skip theirs.
+  if ((warp >> 2) * 32 <= (warp & 3) * 16 + 15) {
     const int m0 = (warp & 3) * 16, nb = (warp >> 2) * 32;
     float acc[4][4] = {};
 #pragma unroll
@@ -246,15 +248,22 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
         mma16(acc[nt], a1, b[2], b[3]);
       }
     }
+    const int ta = m0 + gq, tb = ta + 8;       // this thread's rows; columns c, c + 1 per n-tile
+    const float ga = s.g[ta], gb = s.g[tb], ba = s.b[ta], bb = s.b[tb];
+    const bool oka = ta < n, okb = tb < n;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = m0 + gq + (e >> 1) * 8, sc = nb + nt * 8 + 2 * tq + (e & 1);
-        const float v = (sc < t && t < n) ? s.b[t] * __expf(s.g[t] - s.g[sc]) * acc[nt][e] : 0.f;
-        s.A[t * SA + sc] = v;
-        s.Ah[t * SAH + sc] = __float2half_rn(v);
-      }
+    for (int nt = 0; nt < 4; ++nt) {
+      const int c = nb + nt * 8 + 2 * tq;
+      const float g0 = s.g[c], g1 = s.g[c + 1];
+      const float va0 = (oka && c < ta) ? ba * __expf(ga - g0) * acc[nt][0] : 0.f;
+      const float va1 = (oka && c + 1 < ta) ? ba * __expf(ga - g1) * acc[nt][1] : 0.f;
+      const float vb0 = (okb && c < tb) ? bb * __expf(gb - g0) * acc[nt][2] : 0.f;
+      const float vb1 = (okb && c + 1 < tb) ? bb * __expf(gb - g1) * acc[nt][3] : 0.f;
+      *reinterpret_cast<float2*>(&s.A[ta * SA + c]) = make_float2(va0, va1);
+      *reinterpret_cast<float2*>(&s.A[tb * SA + c]) = make_float2(vb0, vb1);
+      *reinterpret_cast<uint32_t*>(&s.Ah[ta * SAH + c]) = h2u(va0, va1);
+      *reinterpret_cast<uint32_t*>(&s.Ah[tb * SAH + c]) = h2u(vb0, vb1);
+    }
   }
   __syncthreads();
   // ---- diagonal-block inverses T_bb = (I + N_bb)^-1, N_bb the strictly lower 16 x 16 diagonal
@@ -710,10 +719,10 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------------------
-// chunk_out: one CTA per (chunk, head, value slice), 256 threads, two CTAs per SM. A CTA forms
-// the output columns [vs * D/VS, (vs + 1) * D/VS) of its head; the launcher splits the value
-// columns over VS CTAs when (chunks x heads) alone leaves SMs idle (a few questions over a
-// snapshot).
+// chunk_out: one CTA per (chunk, head, value slice), 256 threads, at least two CTAs per SM (at
+// most 128 registers a thread). A CTA forms the output columns [vs * D/VS, (vs + 1) * D/VS) of
+// its head; the launcher splits the value columns over VS CTAs when (chunks x heads) alone leaves
+// SMs idle (a few questions over a snapshot).
 //   P = lower_incl(Gamma * Q K^T),  U = Ut - W S_c^T,  O = diag(gamma) Q S_c^T + P U
 // with S_c the chunk's start state: the state pass's record, or (a single-chunk sequence without
 // a state pass) the snapshot's state it continues, or zero.
@@ -752,8 +761,6 @@ __global__ void __launch_bounds__(256, 2) chunk_out_kernel(const float* __restri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const size_t DD = (size_t)D * D;
-  const bool fold = cd.seq >= out_fold;
-  const int cin = fold ? seqs[cd.seq].ctx_in : -1;
   for (int i = tid; i < C * (D / 8); i += 256) {
     const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
     const bool ok = r < n;
@@ -761,6 +768,7 @@ __global__ void __launch_bounds__(256, 2) chunk_out_kernel(const float* __restri
     cp16(&s.K[r * SK + c8], bufs.Kn + o, ok);
     cp16(&s.W[r * SK + c8], bufs.W + o, ok);
   }
+  const bool fold = cd.seq >= out_fold;
   if (!fold) {
     const f16* rec = bufs.Srec + ((size_t)ci * H + h) * DD + (size_t)cs * D;
     for (int i = tid; i < DW * (D / 8); i += 256) {
@@ -770,6 +778,7 @@ __global__ void __launch_bounds__(256, 2) chunk_out_kernel(const float* __restri
   }
   cp_commit();
   if (fold) {
+    const int cin = seqs[cd.seq].ctx_in;
     const float* S0 = cin >= 0 ? ctxs[cin].S + (size_t)(layer_g * H + h) * DD + (size_t)cs * D : nullptr;
     for (int i = tid; i < DW * (D / 4); i += 256) {
       const int r = i / (D / 4), c4 = (i % (D / 4)) * 4;
