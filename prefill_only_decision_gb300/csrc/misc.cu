@@ -34,8 +34,10 @@ cudaError_t launch_embed(const f16* E, const int* row_src, const bf16* embeds, f
 // ---- RMSNorm: out = f16(x / sqrt(mean(x^2) + eps) * w) ---------------------------------
 // One warp per row, the row held in registers (one read of x), 8 rows per block; the block
 // stages w in shared memory while its rows load, so no global round trip follows the reduction.
+// (x, the previous kernel's output, carries no __restrict__: with code ahead of the wait, its
+// loads must not be treated as invariant and moved above it.)
 template <int NV>   // float4 per lane: d = 128 * NV
-__global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restrict__ x, const float* __restrict__ w,
+__global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* x, const float* __restrict__ w,
                                                            f16* __restrict__ out, int R, int d, float eps) {
   allow_dependents();
   __shared__ float4 ws[32 * NV];
