@@ -235,9 +235,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // sequences in reverse call order: the calls list the prefixes first and the sequences that
   // continue them (whose query tiles see the most keys) after, so those start in the first wave
   const SeqDesc sd = seqs[gridDim.z - 1 - blockIdx.z];
+  // x = head x key part (a cluster's parts adjacent), y = query tile: blocks go out in x order
+  // first, so every head's longest query tile is handed out before any head's shorter ones
   const int part = (int)(blockIdx.x % nparts);
-  const int q0 = ((int)(gridDim.x / nparts) - 1 - (int)(blockIdx.x / nparts)) * BQ;   // longest tiles first
-  const int h = blockIdx.y, g = (h * Hkv) / Hq;
+  const int q0 = ((int)gridDim.y - 1 - (int)blockIdx.y) * BQ;   // longest tiles first
+  const int h = (int)(blockIdx.x / nparts), g = (h * Hkv) / Hq;
   // (the early exit is uniform over a cluster: its CTAs share q0)
   if (q0 >= sd.len) return;
   int P = 0;
@@ -611,7 +613,8 @@ cudaError_t launch_attention_tc(const f16* q, const f16* knew, const f16* vnew, 
                                 int layer_f, int Hq, int Hkv, int hd, int max_len, int max_keys, long work_ctas,
                                 int num_sms, int* d_err, cudaStream_t st) {
   if (n_seq <= 0 || max_len <= 0 || R <= 0) return cudaSuccess;
-  if (n_seq > 65535 || !attention_tc_supported(hd)) return cudaErrorInvalidValue;
+  if (n_seq > 65535 || (max_len + fat::BQ - 1) / fat::BQ > 65535 || !attention_tc_supported(hd))
+    return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv;
   {
     const uint64_t dq[3] = {(uint64_t)hd, (uint64_t)Hq, (uint64_t)R};
@@ -633,7 +636,7 @@ cudaError_t launch_attention_tc(const f16* q, const f16* knew, const f16* vnew, 
     const int want = parts_for(std::max(max_keys, max_len));
     while (nparts < want && work_ctas * (nparts * 2) <= num_sms) nparts *= 2;
   }
-  const dim3 grid(((max_len + fat::BQ - 1) / fat::BQ) * nparts, Hq, n_seq);
+  const dim3 grid(Hq * nparts, (max_len + fat::BQ - 1) / fat::BQ, n_seq);
   const CUtensorMap* cm = reinterpret_cast<const CUtensorMap*>(d_ctx_maps);
   cudaError_t e = hd == 128 ? launch_tc<128>(grid, nparts, st, mq, mk, mv, cm, out, d_seq, d_ctx, layer_f, Hq, Hkv,
                                              scale_log2, d_err)
