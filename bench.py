@@ -345,13 +345,18 @@ def run_batch(args, cfg, torch, ws, rank, local):
     launches0 = model.counters()["launches"]
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nvtx = os.environ.get("S1_NVTX") == "1"     # lets ncu --nvtx-include "timed/" select the timed steps
     with ClockSampler(local) as clk:
         torch.cuda.synchronize()
         clk.mark_start()
+        if nvtx:
+            torch.cuda.nvtx.range_push("timed")
         e0.record(stream)
         for _ in range(args.steps):
             step()
         e1.record(stream)
+        if nvtx:
+            torch.cuda.nvtx.range_pop()
         barrier()
         clk.mark_end()
     ms_total = replicas.max_over_ranks(e0.elapsed_time(e1), device="cuda")

@@ -432,18 +432,18 @@ __global__ void __launch_bounds__(256, 2) chunk_prep_kernel(const float* __restr
 // 16 columns of Ut. Each chunk's N^T, K' and Ut_b tiles arrive by TMA (one thread issues them
 // up to NS chunks ahead; every wait is bounded); its start state is recorded (f16) for
 // chunk_out.
-template <int D>
+template <int D, int NST>
 struct StateSmem {
   static constexpr int SR = D + 8;
   static constexpr int NT_BYTES = D * D * 2;       // D / 64 boxes of [D rows][64 columns], swizzled
   static constexpr int KP_BYTES = C * D * 2;       // D / 64 boxes of [64 rows][64 columns], swizzled
   static constexpr int UT_BYTES = C * BV * 2;      // [64 rows][16 columns], dense
   static constexpr int STAGE = NT_BYTES + KP_BYTES + UT_BYTES;
-  static constexpr int GAM = 1024;                 // gamma_n of up to this many chunks at a time
-  uint8_t stage[NS][STAGE];
+  static constexpr int GAM = 256;                  // gamma_n of up to this many chunks at a time
+  uint8_t stage[NST][STAGE];
   __half Sr[2][BV * SR];
   float gam[GAM];
-  uint64_t full[NS];
+  uint64_t full[NST];
 };
 
 // element offset of (row, col) in a swizzled N^T tile
@@ -503,8 +503,10 @@ __device__ __forceinline__ void tma3(void* dst, const CUtensorMap* map, uint64_t
 template <int D>
 constexpr int state_threads() { return D * 2; }
 
-template <int D>
-__global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_constant__ CUtensorMap mapNT,
+// NST chunk tiles in flight: 4 while the CTAs fit one wave (one CTA per SM), 2 when they need
+// several (two CTAs per SM, at most 128 registers a thread).
+template <int D, int NST>
+__global__ void __launch_bounds__(D * 2, NST == 2 ? 2 : 1) chunk_state_kernel(const __grid_constant__ CUtensorMap mapNT,
                                                             const __grid_constant__ CUtensorMap mapKp,
                                                             const __grid_constant__ CUtensorMap mapUt,
                                                             const float* __restrict__ gam,
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
                                                             f16* __restrict__ Srec, int* __restrict__ d_err) {
   allow_dependents();
   wait_prerequisites();
-  using SM = StateSmem<D>;
+  using SM = StateSmem<D, NST>;
   constexpr int SR = SM::SR;
   constexpr int KS = D / 32;                   // 32-deep k steps of Sr x N
   extern __shared__ __align__(16) uint8_t smraw[];   // (rounded up to 1024 bytes below)
@@ -529,7 +531,7 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
   const size_t DD = (size_t)D * D;
   const size_t head_off = (size_t)(layer_g * H + h) * DD;
   if (tid == 0) {
-    for (int i = 0; i < NS; ++i) bar_init(&s.full[i], 1);
+    for (int i = 0; i < NST; ++i) bar_init(&s.full[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -537,7 +539,7 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
   // warp 0 requests a step's tiles: lane 0 sets the byte count, then one copy per lane (the
   // D / 64 boxes of N^T and of K', and the Ut block)
   auto issue = [&](int cl, int ln) {
-    const int st = cl % NS;
+    const int st = cl % NST;
     uint8_t* sb = s.stage[st];
     if (ln == 0) bar_expect_tx(&s.full[st], SM::STAGE);
     __syncwarp();
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
     ++issued;
   };
   if (warp == 0)
-    for (int cl = 0; cl < nupd && cl < NS; ++cl) issue(cl, lane);
+    for (int cl = 0; cl < nupd && cl < NST; ++cl) issue(cl, lane);
   // gamma_n of the first steps
   for (int i = tid; i < nupd && i < SM::GAM; i += blockDim.x) s.gam[i] = gam[(size_t)(sd.chunk0 + i) * H + h];
   // the state block's fragments: rows v0 + gq and v0 + gq + 8, columns cw + 8 nt + 2 tq and + 1
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
   float qv[2][4], qv2[2][4];
   uint32_t nb[KS][2][4], nb2[KS][2][4];
   auto take_tiles = [&](int cl, float (&qo)[2][4], uint32_t (&no)[KS][2][4]) {
-    const uint8_t* sb = s.stage[cl % NS];
+    const uint8_t* sb = s.stage[cl % NST];
     const __half* ntile = reinterpret_cast<const __half*>(sb);
     const uint32_t kp_base = smem_u32(sb + SM::NT_BYTES);
     const __half* ut = reinterpret_cast<const __half*>(sb + SM::NT_BYTES + SM::KP_BYTES);
@@ -662,7 +664,7 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
     // the next step's tiles, taken while those products complete
     bool w = true;
     if (cl + 1 < nupd) {
-      w = bar_wait(&s.full[(cl + 1) % NS], ((cl + 1) / NS) & 1);
+      w = bar_wait(&s.full[(cl + 1) % NST], ((cl + 1) / NST) & 1);
       if (w) take_tiles(cl + 1, qv2, nb2);
     }
     const float g = s.gam[cl % SM::GAM];
@@ -686,7 +688,7 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
 #pragma unroll
         for (int j = 0; j < 4; ++j) nb[i][nt][j] = nb2[i][nt][j];
     if (cl + 1 < nupd) ++waited;
-    if (warp == 0 && cl + NS < nupd) issue(cl + NS, lane);   // refill the stage this step consumed
+    if (warp == 0 && cl + NST < nupd) issue(cl + NST, lane);   // refill the stage this step consumed
     cur ^= 1;
     if ((cl + 1) % SM::GAM == 0 && cl + 1 < nupd) {   // the next block of gamma_n
       for (int i = tid; i < SM::GAM && cl + 1 + i < nupd; i += blockDim.x)
@@ -698,7 +700,7 @@ __global__ void __launch_bounds__(D * 2, 1) chunk_state_kernel(const __grid_cons
     // a tile never arrived: wait (bounded) for this CTA's copies in flight, then leave
     if (tid == 0) {
       atomicExch(d_err, 0x201);
-      for (int j = waited; j < issued; ++j) bar_wait(&s.full[j % NS], (j / NS) & 1);
+      for (int j = waited; j < issued; ++j) bar_wait(&s.full[j % NST], (j / NST) & 1);
     }
     __syncthreads();
     return;
@@ -936,17 +938,24 @@ GdnBufs gdn_bufs(void* rows, size_t R, void* per_chunk, size_t n_chunks, int H, 
   return b;
 }
 
-template <int D>
-static constexpr size_t state_smem() { return sizeof(gc::StateSmem<D>) + 1024; }
+template <int D, int NST>
+static constexpr size_t state_smem() { return sizeof(gc::StateSmem<D, NST>) + 1024; }
 
 template <int D>
 static cudaError_t launch_state(const CUtensorMap* maps, const SeqDesc* d_seq, int n_seq, const ChunkDesc* d_chunks,
                                 const CtxDesc* d_ctx, int layer_g, int H, const GdnBufs& bufs, int* d_err,
-                                cudaStream_t st) {
+                                int num_sms, cudaStream_t st) {
   if (n_seq <= 0) return cudaSuccess;
   const dim3 grid(n_seq, H, D / gc::BV);
-  CK_RET(launch_pdl(gc::chunk_state_kernel<D>, grid, dim3(gc::state_threads<D>()), state_smem<D>(), st, maps[0], maps[1], maps[2],
-                    (const float*)bufs.gam, d_seq, d_chunks, d_ctx, layer_g, H, bufs.Srec, d_err));
+  if ((long)n_seq * H * (D / gc::BV) > num_sms) {   // several waves: two CTAs per SM
+    CK_RET(launch_pdl(gc::chunk_state_kernel<D, 2>, grid, dim3(gc::state_threads<D>()), state_smem<D, 2>(), st,
+                      maps[0], maps[1], maps[2], (const float*)bufs.gam, d_seq, d_chunks, d_ctx, layer_g, H,
+                      bufs.Srec, d_err));
+  } else {
+    CK_RET(launch_pdl(gc::chunk_state_kernel<D, gc::NS>, grid, dim3(gc::state_threads<D>()), state_smem<D, gc::NS>(),
+                      st, maps[0], maps[1], maps[2], (const float*)bufs.gam, d_seq, d_chunks, d_ctx, layer_g, H,
+                      bufs.Srec, d_err));
+  }
   return cudaGetLastError();
 }
 
@@ -973,8 +982,11 @@ static cudaError_t launch_chunked_d(const float* proj, int ld, float* gbuf, floa
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(gc::chunk_prep_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gc::chunk_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)state_smem<D>());
+      e = cudaFuncSetAttribute(gc::chunk_state_kernel<D, gc::NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)state_smem<D, gc::NS>());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gc::chunk_state_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)state_smem<D, 2>());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gc::chunk_out_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)sizeof(gc::OutSmem<D, 1>));
@@ -1022,11 +1034,11 @@ static cudaError_t launch_chunked_d(const float* proj, int ld, float* gbuf, floa
   // snapshot: neither gets a state pass.
   const int split = (n_first > 0 && n_first < n_seq) ? n_first : n_seq;
   const int n1 = std::min(split, std::min(fold_from, out_fold));
-  cudaError_t e = launch_state<D>(maps, d_seq, n1, d_chunks, d_ctx, layer_g, H, bufs, d_err, st);
+  cudaError_t e = launch_state<D>(maps, d_seq, n1, d_chunks, d_ctx, layer_g, H, bufs, d_err, num_sms, st);
   if (e != cudaSuccess) return e;
   const int n2 = std::min(n_seq, out_fold) - split;
   if (split < n_seq && fold_from > split && n2 > 0) {
-    e = launch_state<D>(maps, d_seq + split, n2, d_chunks, d_ctx, layer_g, H, bufs, d_err, st);
+    e = launch_state<D>(maps, d_seq + split, n2, d_chunks, d_ctx, layer_g, H, bufs, d_err, num_sms, st);
     if (e != cudaSuccess) return e;
   }
   // value columns split over up to VMAX CTAs while (chunks x heads) CTAs leave SMs idle
