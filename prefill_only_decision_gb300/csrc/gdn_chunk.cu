@@ -763,6 +763,19 @@ __global__ void __launch_bounds__(256, 2) chunk_out_kernel(const float* __restri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const size_t DD = (size_t)D * D;
+  // this thread's quarter of row rq of q, requested first (its loads are in flight while the
+  // tile copies below are issued)
+  const int rq = tid >> 2, cq = (tid & 3) * PER;
+  const bool okq = rq < n;
+  float qv[PER];
+  {
+    const float* pr = proj + (size_t)(cd.row0 + (okq ? rq : 0)) * ld + h * D + cq;
+#pragma unroll
+    for (int i = 0; i < PER; i += 4) {
+      const float4 t = ld4(pr + i, okq);
+      qv[i] = t.x; qv[i + 1] = t.y; qv[i + 2] = t.z; qv[i + 3] = t.w;
+    }
+  }
   for (int i = tid; i < C * (D / 8); i += 256) {
     const int r = i / (D / 8), c8 = (i % (D / 8)) * 8;
     const bool ok = r < n;
@@ -791,25 +804,17 @@ __global__ void __launch_bounds__(256, 2) chunk_out_kernel(const float* __restri
   if (tid < C) s.g[tid] = tid < n ? gbuf[(size_t)(cd.row0 + tid) * H + h] : 0.f;
   // q <- q / sqrt(sum q^2 + eps) (four threads per row)
   {
-    const int r = tid >> 2, c0 = (tid & 3) * PER;
-    const bool ok = r < n;
-    const float* pr = proj + (size_t)(cd.row0 + (ok ? r : 0)) * ld + h * D + c0;
-    float v[PER];
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < PER; i += 4) {
-      const float4 t = ld4(pr + i, ok);
-      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
-      ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
-    }
+    for (int i = 0; i < PER; ++i) ss += qv[i] * qv[i];
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
     const float inv = 1.0f / sqrtf(ss + eps);
 #pragma unroll
     for (int i = 0; i < PER; i += 8)
-      *reinterpret_cast<uint4*>(&s.Q[r * SK + c0 + i]) =
-          make_uint4(h2u(v[i] * inv, v[i + 1] * inv), h2u(v[i + 2] * inv, v[i + 3] * inv),
-                     h2u(v[i + 4] * inv, v[i + 5] * inv), h2u(v[i + 6] * inv, v[i + 7] * inv));
+      *reinterpret_cast<uint4*>(&s.Q[rq * SK + cq + i]) =
+          make_uint4(h2u(qv[i] * inv, qv[i + 1] * inv), h2u(qv[i + 2] * inv, qv[i + 3] * inv),
+                     h2u(qv[i + 4] * inv, qv[i + 5] * inv), h2u(qv[i + 6] * inv, qv[i + 7] * inv));
   }
   cp_wait<0>();
   __syncthreads();

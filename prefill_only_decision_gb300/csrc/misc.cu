@@ -119,10 +119,10 @@ cudaError_t launch_rmsnorm(const float* x, const float* w, f16* out, int R, int 
 // ---- RoPE (rotate-half over the whole head) + split of the fused q|k|v projection -------
 // proj row r: [q (Hq*hd) | k (Hkv*hd) | v (Hkv*hd)] fp32. Writes q, k_new, v_new (f16) at
 // packed row r and, for sequences that own a snapshot, K/V into its cache at row = position.
-// Grid (row, item block): one thread per item, items = the (Hq + Hkv) * hd/4 pairs of adjacent
-// rotated pairs of q and k (elements i, i+1 with partners i + hd/2, i+1 + hd/2), then the
-// Hkv * hd/2 pairs of v values (one round trip to memory per thread and 4-byte stores, so that a
-// few rows still spread over the whole GPU).
+// Grid (row, item block): one thread per item, items = the (Hq + Hkv) * hd/8 runs of four
+// adjacent rotated elements of q and k (i .. i+3 with partners i + hd/2 .. i + hd/2 + 3), then the
+// Hkv * hd/4 runs of four v values (16-byte loads, 8-byte stores, one round trip to memory per
+// thread, so that a few rows still spread over the whole GPU).
 __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const float2* __restrict__ tab,
                                   const int* __restrict__ row_seq, const SeqDesc* __restrict__ seqs,
                                   const CtxDesc* __restrict__ ctxs, int layer_f, f16* __restrict__ q,
@@ -131,10 +131,10 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
   allow_dependents();
   wait_prerequisites();
   const int r = blockIdx.x;
-  const int half = hd / 2, quarter = hd / 4;
-  const int nq = Hq * quarter, nk = Hkv * quarter;
+  const int half = hd / 2, eighth = hd / 8;
+  const int nq = Hq * eighth, nk = Hkv * eighth;
   const int t = blockIdx.y * blockDim.x + threadIdx.x;
-  if (t >= nq + nk + Hkv * half) return;
+  if (t >= nq + nk + Hkv * eighth * 2) return;
   const float* pr = proj + (size_t)r * ld;
   const SeqDesc sd = seqs[row_seq[r]];
   const int pos = sd.pos0 + (r - sd.row0);
@@ -147,28 +147,38 @@ __global__ void rope_split_kernel(const float* __restrict__ proj, int ld, const 
     vc = kc + plane;
   }
   if (t < nq + nk) {
+    // four adjacent elements i .. i+3 of the first half of a q or k head and their partners
+    // i + hd/2 .. i + hd/2 + 3
     const bool isq = t < nq;
     const int tt = isq ? t : t - nq;
-    const int h = tt / quarter, i = 2 * (tt % quarter);
+    const int h = tt / eighth, i = 4 * (tt % eighth);
     const float* src = pr + (isq ? 0 : Hq * hd) + h * hd;
-    const float2 x1 = *reinterpret_cast<const float2*>(src + i);
-    const float2 x2 = *reinterpret_cast<const float2*>(src + i + half);
-    const float4 cs = *reinterpret_cast<const float4*>(tab + (size_t)pos * half + i);   // (cos, sin) of i, i + 1
-    const __half2 y1 = __floats2half2_rn(x1.x * cs.x - x2.x * cs.y, x1.y * cs.z - x2.y * cs.w);
-    const __half2 y2 = __floats2half2_rn(x2.x * cs.x + x1.x * cs.y, x2.y * cs.z + x1.y * cs.w);
+    const float4 x1 = *reinterpret_cast<const float4*>(src + i);
+    const float4 x2 = *reinterpret_cast<const float4*>(src + i + half);
+    const float4 c01 = *reinterpret_cast<const float4*>(tab + (size_t)pos * half + i);       // (cos, sin) of i, i+1
+    const float4 c23 = *reinterpret_cast<const float4*>(tab + (size_t)pos * half + i + 2);   // of i+2, i+3
+    const __half2 a0 = __floats2half2_rn(x1.x * c01.x - x2.x * c01.y, x1.y * c01.z - x2.y * c01.w);
+    const __half2 a1 = __floats2half2_rn(x1.z * c23.x - x2.z * c23.y, x1.w * c23.z - x2.w * c23.w);
+    const __half2 b0 = __floats2half2_rn(x2.x * c01.x + x1.x * c01.y, x2.y * c01.z + x1.y * c01.w);
+    const __half2 b1 = __floats2half2_rn(x2.z * c23.x + x1.z * c23.y, x2.w * c23.z + x1.w * c23.w);
+    uint2 y1, y2;
+    y1.x = *reinterpret_cast<const uint32_t*>(&a0); y1.y = *reinterpret_cast<const uint32_t*>(&a1);
+    y2.x = *reinterpret_cast<const uint32_t*>(&b0); y2.y = *reinterpret_cast<const uint32_t*>(&b1);
     f16* dst = isq ? q + (size_t)r * Hq * hd : knew + (size_t)r * Hkv * hd;
-    *reinterpret_cast<__half2*>(dst + h * hd + i) = y1;
-    *reinterpret_cast<__half2*>(dst + h * hd + i + half) = y2;
+    *reinterpret_cast<uint2*>(dst + h * hd + i) = y1;
+    *reinterpret_cast<uint2*>(dst + h * hd + i + half) = y2;
     if (!isq && kc) {
-      *reinterpret_cast<__half2*>(kc + h * hd + i) = y1;
-      *reinterpret_cast<__half2*>(kc + h * hd + i + half) = y2;
+      *reinterpret_cast<uint2*>(kc + h * hd + i) = y1;
+      *reinterpret_cast<uint2*>(kc + h * hd + i + half) = y2;
     }
   } else {
-    const int tv = 2 * (t - (nq + nk));
-    const float2 x = *reinterpret_cast<const float2*>(pr + (Hq + Hkv) * hd + tv);
-    const __half2 v = __floats2half2_rn(x.x, x.y);
-    *reinterpret_cast<__half2*>(vnew + (size_t)r * Hkv * hd + tv) = v;
-    if (vc) *reinterpret_cast<__half2*>(vc + tv) = v;
+    const int tv = 4 * (t - (nq + nk));
+    const float4 x = *reinterpret_cast<const float4*>(pr + (Hq + Hkv) * hd + tv);
+    const __half2 v0 = __floats2half2_rn(x.x, x.y), v1 = __floats2half2_rn(x.z, x.w);
+    uint2 v;
+    v.x = *reinterpret_cast<const uint32_t*>(&v0); v.y = *reinterpret_cast<const uint32_t*>(&v1);
+    *reinterpret_cast<uint2*>(vnew + (size_t)r * Hkv * hd + tv) = v;
+    if (vc) *reinterpret_cast<uint2*>(vc + tv) = v;
   }
 }
 
@@ -177,8 +187,8 @@ cudaError_t launch_rope_split(const float* proj, int ld, const float2* rope_tab,
                               f16* knew, f16* vnew, int R, int Hq, int Hkv, int hd,
                               cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
-  if (hd % 4 || ld % 2) return cudaErrorInvalidValue;
-  const int items = (Hq + Hkv) * (hd / 4) + Hkv * (hd / 2);
+  if (hd % 8 || ld % 4) return cudaErrorInvalidValue;
+  const int items = (Hq + Hkv) * (hd / 8) + Hkv * (hd / 4);
   const dim3 grid(R, (items + 127) / 128);
   if (grid.y > 65535) return cudaErrorInvalidValue;
   CK_RET(launch_pdl(rope_split_kernel, grid, dim3(128), 0, st, proj, ld, rope_tab, row_seq, d_seq, d_ctx, layer_f,
