@@ -55,7 +55,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # over one step's GEMM launches in an ncu capture of this bench's timed step (caches not flushed
 # between launches), per workload; a workload whose kernels changed since their capture has no
 # entry (the field reads null).
-GEMM_DRAM_BYTES_PER_LAUNCH = {"4b": 76046312}
+GEMM_DRAM_BYTES_PER_LAUNCH = {"4b": 77264930}
 
 
 def tensor_peak(peaks, ms_timed):
