@@ -196,9 +196,11 @@ def test_gdn_scan(B, H, D, lens, with_s0):
 
 # shapes: a causal prefix, ragged sequences, questions over a 1024-row snapshot, a snapshot whose
 # rows end mid-tile, and few query tiles over long key ranges (key tiles split over a cluster)
+# (the suffix-over-prefix shapes with few query tiles split their key ranges over clusters of
+# 2 or 4 CTAs: 40 x 8 x 128 over 1536 cached rows is the 27B decide's attention layer)
 ATTN_SHAPES = [(4, 2, 64, 0, [96]), (16, 4, 128, 0, [300, 17]), (16, 4, 128, 1024, [48, 48, 48]),
                (8, 2, 128, 77, [1, 5, 33]), (8, 2, 128, 1536, [64]), (40, 8, 128, 600, [64, 130]),
-               (4, 2, 64, 300, [200])]
+               (4, 2, 64, 300, [200]), (40, 8, 128, 1536, [64]), (48, 8, 64, 1100, [64])]
 
 
 @pytest.mark.parametrize("kernel", ["tcgen05", "sync"])
