@@ -748,6 +748,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// Sum over the splits of one float4 of the partials, in split order; the loads of up to four
+// splits are issued before their sums, so a row waits for one round trip to memory, not one per
+// split.
+__device__ __forceinline__ float4 sum_splits(const float* ws, int splits, size_t split_stride, size_t off) {
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < splits; s0 += 4) {
+    float4 p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (s0 + j < splits) p[j] = *reinterpret_cast<const float4*>(ws + (size_t)(s0 + j) * split_stride + off);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (s0 + j < splits) { a.x += p[j].x; a.y += p[j].y; a.z += p[j].z; a.w += p[j].w; }
+  }
+  return a;
+}
+
 // Sum of the split-K partials in split order, then the epilogue.
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, int Mpad, int M, int N, int epi,
                                      void* __restrict__ out, int ldo) {
@@ -773,11 +790,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int splits, i
       o[0] = f2h(silu_f(g.x) * u.x); o[1] = f2h(silu_f(g.y) * u.y);
       o[2] = f2h(silu_f(g.z) * u.z); o[3] = f2h(silu_f(g.w) * u.w);
     } else {
-      float4 a = make_float4(0, 0, 0, 0);
-      for (int s = 0; s < splits; ++s) {
-        const float4 b = *reinterpret_cast<const float4*>(ws + ((size_t)s * Mpad + m) * N + c);
-        a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-      }
+      const float4 a = sum_splits(ws, splits, (size_t)Mpad * N, (size_t)m * N + c);
       if (epi == EPI_F32) {
         *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (size_t)m * ldo + c) = a;
       } else if (epi == EPI_RESADD) {
@@ -808,12 +821,8 @@ __global__ void __launch_bounds__(1024) splitk_resadd_norm_kernel(const float* _
   float4* xr = reinterpret_cast<float4*>(x + (size_t)m * ldx);
   float ss = 0.f;
   for (int i = threadIdx.x; i < N / 4; i += blockDim.x) {
-    float4 a = make_float4(0, 0, 0, 0);
-    for (int s = 0; s < splits; ++s) {
-      const float4 b = *reinterpret_cast<const float4*>(ws + ((size_t)s * Mpad + m) * N + 4 * i);
-      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-    }
     float4 v = xr[i];
+    const float4 a = sum_splits(ws, splits, (size_t)Mpad * N, (size_t)m * N + 4 * i);
     v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
     xr[i] = v;
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
