@@ -158,10 +158,13 @@ def _gdn_inputs(R, H, D, seed):
 
 
 # (chunks x heads) picks how many CTAs share a head's value columns in the output kernel: 4 below
-# about half the SM count, 2 below the SM count (16 heads x 5 chunks), else 1 (16 x 10)
+# about half the SM count, 2 below the SM count (16 heads x 5 chunks), else 1 (16 x 10); the
+# state pass keeps two chunk tiles in flight (two CTAs per SM) once its CTAs (sequences x heads x
+# D / 16) exceed the SM count (the last two shapes: 384 and 192 CTAs of several chunk steps)
 @pytest.mark.parametrize("H,D,lens,with_s0", [(2, 64, [1, 63, 64, 65], False), (4, 128, [130], True),
                                               (16, 128, [48, 48, 48], True), (3, 128, [200, 7], False),
-                                              (16, 128, [320], True), (16, 64, [640], False)])
+                                              (16, 128, [320], True), (16, 64, [640], False),
+                                              (16, 128, [200, 300, 130], True), (16, 64, [300, 300, 300], False)])
 def test_gdn_scan(B, H, D, lens, with_s0):
     R = int(sum(lens))
     proj = _gdn_inputs(R, H, D, R + H)
