@@ -8,17 +8,19 @@
 //
 // One CTA per (128-query tile, q head, sequence), or per part of its key tiles when the key range
 // is split over a thread-block cluster of 2 or 4 CTAs (parts merged by rank 0 over distributed
-// shared memory, in rank order). Warp-specialised, 6 warps:
+// shared memory, in rank order). Warp-specialised, 10 warps:
 //   warp 0     TMA producer: the Q tile once, then K and V tiles of 128 keys (two stages), from
 //              the snapshot's K/V planes (cached keys) or the call's new K/V rows (own keys);
 //              the two sources never share a tile, so each tile is one box per 64 columns.
 //   warp 1     TMEM allocator and MMA issuer (one thread): S = Q K^T (M 128, N 128, K hd) into
 //              one of two TMEM buffers, then O += P V (M 128, N hd, K 128) into the TMEM
 //              accumulator; V is read N-major (its rows are keys), P from shared memory.
-//   warps 2-5  softmax (one query row per thread = one TMEM lane): mask, running max with a
-//              lazy rescale (O and l are rescaled only when a row's maximum grows by more than
-//              2^8, so P <= 256 fits f16 and most tiles skip the O round trip), P as f16 into
-//              shared memory in the MMA's 128-byte-swizzled K-major layout; the epilogue.
+//   warps 2-9  softmax, two threads per query row (one TMEM lane; warps 2-5 the first 64 keys of
+//              a tile and the first half of O, warps 6-9 the rest, the row maximum and sum
+//              exchanged through shared memory): mask, running max with a lazy rescale (O and l
+//              are rescaled only when a row's maximum grows by more than 2^8, so P <= 256 fits
+//              f16 and most tiles skip the O round trip), P as f16 into shared memory in the
+//              MMA's 128-byte-swizzled K-major layout; the epilogue.
 // Key masks: a cached key j is valid iff j < P (the whole snapshot is visible); an own key r is
 // valid iff r <= i (causal). Rows of a tile past the sequence are computed and never stored.
 // Every mbarrier wait is bounded (~1 s of %globaltimer): on expiry the kernel records an error
@@ -31,7 +33,7 @@ namespace s1 {
 namespace fat {
 
 constexpr int BQ = 128, BKV = 128;
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;
 constexpr int ST = 2;                       // K/V stages
 constexpr int TMEM_COLS = 512;              // S (2 x 128 columns) + O (hd columns)
 constexpr uint64_t WAIT_NS = 1000000000ull;
@@ -44,7 +46,8 @@ struct Lay {
   static constexpr int K = Q + BQ * HD * 2;
   static constexpr int V = K + ST * TILE;
   static constexpr int P = V + ST * TILE;              // 2 boxes of [128 rows][64 keys]
-  static constexpr int BAR = P + BQ * BKV * 2;
+  static constexpr int XCH = P + BQ * BKV * 2;         // row maxima / sums of the two halves [3][2][BQ]
+  static constexpr int BAR = XCH + 3 * 2 * BQ * 4;
   // barriers and alignment slack; at least 120 KB, so that two CTAs never share an SM: each
   // allocates all 512 TMEM columns, and CTAs of one cluster wait for one another
   static constexpr int BYTES = (BAR + 256 + 1024) > 120 * 1024 ? (BAR + 256 + 1024) : 120 * 1024;
@@ -217,17 +220,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;              // [ST]
-  uint64_t* kv_empty = bars + 1 + ST;        // [ST]
-  uint64_t* s_full = bars + 1 + 2 * ST;      // [2]
-  uint64_t* s_empty = bars + 3 + 2 * ST;     // [2]
-  uint64_t* p_full = bars + 5 + 2 * ST;
-  uint64_t* o_done = bars + 6 + 2 * ST;
-  uint64_t* mma_idle = bars + 7 + 2 * ST;
-  uint32_t* tmem_slot = (uint32_t*)(bars + 8 + 2 * ST);
+  // K and V of a stage have barriers of their own: K_i's slot is free once S_i = Q K_i^T has
+  // completed, V_i's once P_i V_i has, so K_{i+ST} is requested a tile earlier than V_{i+ST}
+  uint64_t* k_full = bars + 1;               // [ST]
+  uint64_t* v_full = bars + 1 + ST;          // [ST]
+  uint64_t* k_empty = bars + 1 + 2 * ST;     // [ST]
+  uint64_t* v_empty = bars + 1 + 3 * ST;     // [ST]
+  uint64_t* s_full = bars + 1 + 4 * ST;      // [2]
+  uint64_t* s_empty = bars + 3 + 4 * ST;     // [2]
+  uint64_t* p_full = bars + 5 + 4 * ST;
+  uint64_t* o_done = bars + 6 + 4 * ST;
+  uint64_t* mma_idle = bars + 7 + 4 * ST;
+  uint64_t* xbar = bars + 8 + 4 * ST;        // [4 quadrants][2 tile parities + 1]: the two softmax
+                                             // warps of a row quadrant meet here (2 arrivals)
+  uint32_t* tmem_slot = (uint32_t*)(bars + 20 + 4 * ST);
+  static_assert((20 + 4 * ST) * 8 + 6 * 4 <= 256, "barriers and counters fit their 256 bytes");
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-  int* kv_waited = (int*)(tmem_slot + 2);    // K/V tiles the MMA issuer saw arrive
-  int* kv_issued = (int*)(tmem_slot + 3);    // K/V tiles the producer requested
+  int* k_waited = (int*)(tmem_slot + 2);     // K tiles the MMA issuer saw arrive
+  int* k_issued = (int*)(tmem_slot + 3);     // K tiles the producer requested
+  int* v_waited = (int*)(tmem_slot + 4);     // V tiles the MMA issuer saw arrive
+  int* v_issued = (int*)(tmem_slot + 5);     // V tiles the producer requested
 
   allow_dependents();
   wait_prerequisites();
@@ -258,14 +270,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < ST; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&s_full[b], 1); mbar_init(&s_empty[b], 4); }
-    mbar_init(p_full, 4);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&k_full[s], 1); mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1); mbar_init(&v_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) { mbar_init(&s_full[b], 1); mbar_init(&s_empty[b], 8); }
+    mbar_init(p_full, 8);
+    for (int x = 0; x < 12; ++x) mbar_init(&xbar[x], 2);
     mbar_init(o_done, 1);
     mbar_init(mma_idle, 1);
     *abort_flag = 0;
-    *kv_waited = 0;
-    *kv_issued = 0;
+    *k_waited = 0;
+    *k_issued = 0;
+    *v_waited = 0;
+    *v_issued = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -286,21 +304,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int b = 0; b < NB; ++b) tma3(sm + L::Q + b * BQ * 128, &mapQ, q_full, 64 * b, h, sd.row0 + q0);
       for (int i = 0; i < n; ++i) {
         const int s = i % ST, j = jb + i;
-        if (!mbar_wait(&kv_empty[s], ((i / ST) & 1) ^ 1, abort_flag, d_err)) break;
-        mbar_expect_tx(&kv_full[s], 2 * L::TILE);
-        *kv_issued = i + 1;
+        const int rnew = sd.row0 + (j - ncache) * BKV;   // (own keys) the tile's first packed row
+        if (!mbar_wait(&k_empty[s], ((i / ST) & 1) ^ 1, abort_flag, d_err)) break;
+        mbar_expect_tx(&k_full[s], L::TILE);
+        *k_issued = i + 1;
         uint8_t* kd = sm + L::K + s * L::TILE;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          if (j < ncache) tma4(kd + b * BKV * 128, cmap, &k_full[s], 64 * b, g, j * BKV, 2 * layer_f);
+          else tma3(kd + b * BKV * 128, &mapKn, &k_full[s], 64 * b, g, rnew);
+        }
+        if (!mbar_wait(&v_empty[s], ((i / ST) & 1) ^ 1, abort_flag, d_err)) break;
+        mbar_expect_tx(&v_full[s], L::TILE);
+        *v_issued = i + 1;
         uint8_t* vd = sm + L::V + s * L::TILE;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          if (j < ncache) {
-            tma4(kd + b * BKV * 128, cmap, &kv_full[s], 64 * b, g, j * BKV, 2 * layer_f);
-            tma4(vd + b * BKV * 128, cmap, &kv_full[s], 64 * b, g, j * BKV, 2 * layer_f + 1);
-          } else {
-            const int r = sd.row0 + (j - ncache) * BKV;
-            tma3(kd + b * BKV * 128, &mapKn, &kv_full[s], 64 * b, g, r);
-            tma3(vd + b * BKV * 128, &mapVn, &kv_full[s], 64 * b, g, r);
-          }
+          if (j < ncache) tma4(vd + b * BKV * 128, cmap, &v_full[s], 64 * b, g, j * BKV, 2 * layer_f + 1);
+          else tma3(vd + b * BKV * 128, &mapVn, &v_full[s], 64 * b, g, rnew);
         }
       }
     }
@@ -312,8 +333,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool ok = mbar_wait(q_full, 0, abort_flag, d_err);
       auto issue_s = [&](int i) -> bool {   // S_i = Q K_i^T into S buffer i & 1
         const int s = i % ST, b = i & 1;
-        if (!mbar_wait(&kv_full[s], (i / ST) & 1, abort_flag, d_err)) return false;
-        *kv_waited = i + 1;
+        if (!mbar_wait(&k_full[s], (i / ST) & 1, abort_flag, d_err)) return false;
+        *k_waited = i + 1;
         if (!mbar_wait(&s_empty[b], ((i >> 1) & 1) ^ 1, abort_flag, d_err)) return false;
         fence_after();
         const uint32_t qa = smem_u32(sm + L::Q), ka = smem_u32(sm + L::K + s * L::TILE);
@@ -323,11 +344,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma(tmem + b * 128, desc_sw128(qa + off, 16), desc_sw128(ka + off, 16), ID_S, kk > 0 ? 1u : 0u);
         }
         commit(&s_full[b]);
+        commit(&k_empty[s]);
         return true;
       };
       auto issue_pv = [&](int i) -> bool {   // O += P_i V_i
         const int s = i % ST;
         if (!mbar_wait(p_full, i & 1, abort_flag, d_err)) return false;
+        if (!mbar_wait(&v_full[s], (i / ST) & 1, abort_flag, d_err)) return false;
+        *v_waited = i + 1;
         fence_after();
         const uint32_t pa = smem_u32(sm + L::P), va = smem_u32(sm + L::V + s * L::TILE);
 #pragma unroll
@@ -337,7 +361,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mma(tO, desc_sw128(pa + poff, 16), desc_sw128(va + voff, BKV * 128), ID_O, (i > 0 || kk > 0) ? 1u : 0u);
         }
         commit(o_done);
-        commit(&kv_empty[s]);
+        commit(&v_empty[s]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -349,54 +373,70 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_drain(mma_idle, 0);
     }
   } else {
-    // ---- softmax warps: thread -> query row r (TMEM lane r). Waits are agreed on by the whole
-    // warp, so the warp-collective TMEM accesses below never diverge.
+    // ---- softmax warps: two threads per query row r (TMEM lane r), warps 2-5 the row's first
+    // half of the scores, warps 6-9 its second half. Waits are agreed on by the whole warp, so
+    // the warp-collective TMEM accesses below never diverge.
     auto wwait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, d_err) ? 1 : 0) != 0;
     };
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;        // 0: key columns 0..63 of a tile, 1: 64..127
     const int r = quad * 32 + lane;
     const int qi = q0 + r;                   // query index within the sequence
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t tO = tmem + lane_off + 256;
-    uint8_t* prow = sm + L::P + r * 128;     // this row in P's first 64-key box
-    float m = -INFINITY, l = 0.f;
+    const uint32_t tO = tmem + lane_off + 256 + (uint32_t)(half * (HD / 2));   // this half's O columns
+    uint8_t* prow = sm + L::P + half * (BQ * 128) + r * 128;   // this row in P's box `half`
+    float* xch = reinterpret_cast<float*>(sm + L::XCH);         // [3][2 halves][BQ]
+    // the two warps of a row quadrant meet on an mbarrier of two arrivals (a bounded wait)
+    auto pair_meet = [&](int slot, uint32_t parity) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xbar[quad * 3 + slot]);
+      return wwait(&xbar[quad * 3 + slot], parity);
+    };
+    constexpr int HB = BKV / 2;              // scores per thread and tile
+    float m = -INFINITY, l = 0.f;            // l: this half's share of the row sum
     bool ok = n > 0;
     for (int i = 0; i < n && ok; ++i) {
       const int j = jb + i, b = i & 1;
       if (!wwait(&s_full[b], (i >> 1) & 1)) { ok = false; break; }
       fence_after();
-      float sv[BKV];
+      float sv[HB];
       {
-        uint32_t u[BKV];   // the row's four 32-column loads in flight together
+        uint32_t u[HB];   // the half row's two 32-column loads in flight together
 #pragma unroll
-        for (int c = 0; c < BKV; c += 32) tld32(tmem + lane_off + b * 128 + c, u + c);
+        for (int c = 0; c < HB; c += 32) tld32(tmem + lane_off + b * 128 + half * HB + c, u + c);
         ld_wait();
 #pragma unroll
-        for (int c = 0; c < BKV; ++c) sv[c] = __uint_as_float(u[c]);
+        for (int c = 0; c < HB; ++c) sv[c] = __uint_as_float(u[c]);
       }
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[b]);
       // mask and scale (log2 domain)
       const bool cache = j < ncache;
-      const int kbase = cache ? j * BKV : (j - ncache) * BKV;
+      const int kbase = (cache ? j * BKV : (j - ncache) * BKV) + half * HB;
       const int klim = cache ? P - 1 : qi;   // last visible key of this tile's source
       float mx = -INFINITY;
-      if (kbase + BKV - 1 <= klim) {         // every key of the tile is visible to this row
+      if (kbase + HB - 1 <= klim) {          // every key of this half tile is visible to this row
 #pragma unroll
-        for (int c = 0; c < BKV; ++c) {
+        for (int c = 0; c < HB; ++c) {
           sv[c] *= scale_log2;
           mx = fmaxf(mx, sv[c]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < BKV; ++c) {
+        for (int c = 0; c < HB; ++c) {
           sv[c] = (kbase + c <= klim) ? sv[c] * scale_log2 : -INFINITY;
           mx = fmaxf(mx, sv[c]);
         }
       }
-      // lazy rescale: move the reference maximum only when it grows by more than 8 (2^8)
+      // the row's maximum over both halves (a buffer per tile parity: the next tile writes the
+      // other one, and the tile after that comes only after both threads passed the next barrier)
+      xch[(b * 2 + half) * BQ + r] = mx;
+      if (!pair_meet(b, (i >> 1) & 1)) { ok = false; break; }
+      mx = fmaxf(mx, xch[(b * 2 + (half ^ 1)) * BQ + r]);
+      // lazy rescale: move the reference maximum only when it grows by more than 8 (2^8); both
+      // halves of a row see the same maxima, so they take the same decisions
       float alpha = 1.f;
       if (mx > m + 8.f) {
         alpha = (m == -INFINITY) ? 1.f : exp2f(m - mx);
@@ -410,7 +450,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (__any_sync(0xffffffffu, alpha != 1.f) && i > 0) {
         uint32_t u[32];
 #pragma unroll
-        for (int c = 0; c < HD; c += 32) {
+        for (int c = 0; c < HD / 2; c += 32) {
           tld32(tO + c, u);
           ld_wait();
 #pragma unroll
@@ -421,16 +461,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       l *= alpha;
 #pragma unroll
-      for (int c8 = 0; c8 < BKV / 8; ++c8) {
+      for (int c8 = 0; c8 < HB / 8; ++c8) {
         float p[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           p[e] = exp2f(sv[c8 * 8 + e] - base);
           rs += p[e];
         }
-        // 16-byte chunk c8 of the row: box c8 / 8, chunk (c8 % 8) ^ (r % 8)
+        // 16-byte chunk c8 of the row in box `half`: chunk c8 ^ (r % 8)
         uint4 v = make_uint4(h2u(p[0], p[1]), h2u(p[2], p[3]), h2u(p[4], p[5]), h2u(p[6], p[7]));
-        *reinterpret_cast<uint4*>(prow + (c8 >> 3) * (BQ * 128) + ((((c8 & 7) ^ (r & 7))) << 4)) = v;
+        *reinterpret_cast<uint4*>(prow + (((c8 ^ (r & 7))) << 4)) = v;
       }
       l += rs;
       fence_async_smem();
@@ -438,15 +478,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    // ---- epilogue: O row / l (merged over the cluster's parts first)
-    float o[HD];
+    // ---- epilogue: O row / l (merged over the cluster's parts first); each thread its half of
+    // the O columns, the row sum over both halves
+    constexpr int HO = HD / 2;
+    float o[HO];
     if (ok && n > 0) {
       ok = wwait(o_done, (n - 1) & 1);
       fence_after();
       if (ok) {
         uint32_t u[32];
 #pragma unroll
-        for (int c = 0; c < HD; c += 32) {
+        for (int c = 0; c < HO; c += 32) {
           tld32(tO + c, u);
           ld_wait();
 #pragma unroll
@@ -456,24 +498,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     if (!ok || n == 0) {
 #pragma unroll
-      for (int c = 0; c < HD; ++c) o[c] = 0.f;
+      for (int c = 0; c < HO; ++c) o[c] = 0.f;
       if (!ok) { m = -INFINITY; l = 0.f; }
     }
+    // the row sum over both halves (every exit of the loop above falls through to here)
+    xch[(2 * 2 + half) * BQ + r] = l;
+    if (pair_meet(2, 0)) l += xch[(2 * 2 + (half ^ 1)) * BQ + r];
+    else ok = false;
     if (nparts > 1) {
       // publish (o, m, l) in the K/V stage buffers (no longer read once every tile was consumed),
       // one row of PSTR floats per query row
       float* pub = reinterpret_cast<float*>(sm + L::K) + r * PSTR;
 #pragma unroll
-      for (int c = 0; c < HD; c += 4) *reinterpret_cast<float4*>(pub + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-      pub[HD] = m;
-      pub[HD + 1] = l;
+      for (int c = 0; c < HO; c += 4)
+        *reinterpret_cast<float4*>(pub + half * HO + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+      if (half == 0) {
+        pub[HD] = m;
+        pub[HD + 1] = l;
+      }
     }
     if (nparts == 1) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       if (qi < sd.len && ok) {
-        f16* op = out + ((size_t)(sd.row0 + qi) * Hq + h) * HD;
+        f16* op = out + ((size_t)(sd.row0 + qi) * Hq + h) * HD + half * HO;
 #pragma unroll
-        for (int c = 0; c < HD; c += 8)
+        for (int c = 0; c < HO; c += 8)
           *reinterpret_cast<uint4*>(op + c) =
               make_uint4(h2u(o[c] * inv, o[c + 1] * inv), h2u(o[c + 2] * inv, o[c + 3] * inv),
                          h2u(o[c + 4] * inv, o[c + 5] * inv), h2u(o[c + 6] * inv, o[c + 7] * inv));
@@ -483,13 +532,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   // the producer's copies that the MMA issuer never waited for (an aborted call) land before exit
   if (threadIdx.x == 0 && *abort_flag) {
-    for (int i = *kv_waited; i < *kv_issued; ++i) mbar_drain(&kv_full[i % ST], (i / ST) & 1);
+    for (int i = *k_waited; i < *k_issued; ++i) mbar_drain(&k_full[i % ST], (i / ST) & 1);
+    for (int i = *v_waited; i < *v_issued; ++i) mbar_drain(&v_full[i % ST], (i / ST) & 1);
   }
   if (nparts > 1) {
     cluster_sync();
     // every CTA of the cluster merges HD / nparts of the output columns of all 128 rows, from
-    // the parts in rank order
+    // the parts in rank order; the two threads of a row take alternate 16-column groups
     if (warp >= 2) {
+      const int half = (warp - 2) >> 2;
       const int r = (warp & 3) * 32 + lane, qi = q0 + r;
       const uint32_t rank = cluster_rank();
       const uint32_t row = smem_u32(sm + L::K) + (uint32_t)(r * PSTR * 4);
@@ -514,7 +565,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
       const int cw = HD / nparts, c0 = (int)rank * cw;   // this CTA's columns (a multiple of 16)
-      for (int cb = 0; cb < cw; cb += 16) {
+      for (int cb = 16 * half; cb < cw; cb += 32) {
         float acc[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) acc[e] = 0.f;
